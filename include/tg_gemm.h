@@ -1,0 +1,140 @@
+/*
+ * tg_gemm.h -- C ABI of libtg_gemm.so, a tiled matrix multiply for GB300
+ * (sm_103a).
+ *
+ * The operation is the tiled GEMM that the TileLang pages use as their
+ * running example: C[M,N] = A[M,K] x B[K,N], row-major, fp16 (or fp32)
+ * inputs, fp32 accumulation, fp16 or fp32 output.  Sources:
+ *   - "企业官网建设流程全解析" (cf-1.com, a TileLang article), §3.3: the
+ *     matmul kernel clears an fp32 fragment, pipelines the K loop over
+ *     copy-A / copy-B / gemm, and copies the fragment out to an fp16 C.
+ *   - "TileLang实战：用Python DSL自动生成高性能GPU计算内核" (gsyq.cn), §3.1:
+ *     the fp32 128x128x128 triple loop C[i,j] += A[i,k] * B[k,j]; §3.3: the
+ *     tensor-core variant with fp16 inputs and an fp32 result.
+ *   - gsyq.cn/news/429607 (DeepSeek / Ascend TileLang toolchain article),
+ *     §3.3: unaligned sizes such as M=127, N=255 must work.
+ *
+ * No symbol here takes or returns a framework type: plain pointers, sizes
+ * and a CUDA stream handle.
+ */
+#ifndef TG_GEMM_H
+#define TG_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (cudaStream_t / CUstream).  0 is the legacy default
+ * stream. */
+typedef void* tg_stream_t;
+
+typedef enum {
+    TG_F16 = 1, /* IEEE-754 binary16 */
+    TG_F32 = 2  /* IEEE-754 binary32 */
+} tg_dtype;
+
+typedef enum {
+    TG_OK = 0,
+    TG_ERR_INVALID_ARG = 1, /* bad size, pointer, leading dimension or aliasing */
+    TG_ERR_UNSUPPORTED = 2, /* dtype pair or size the library does not handle */
+    TG_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+    TG_ERR_TIMEOUT = 4      /* a kernel gave up on a bounded wait (device flag) */
+} tg_status;
+
+/*
+ * tg_gemm -- C = A x B.
+ *
+ * Arguments
+ *   M, N, K   problem sizes, each in [0, 2^31 - 1].
+ *   A         device pointer, M rows of K elements, row i at A + i*lda.
+ *   lda       row stride of A in elements, lda >= K.
+ *   B         device pointer, K rows of N elements, row k at B + k*ldb.
+ *   ldb       row stride of B in elements, ldb >= N.
+ *   C         device pointer, M rows of N elements, row i at C + i*ldc.
+ *   ldc       row stride of C in elements, ldc >= N.
+ *   in_dtype  element type of A and B.
+ *   out_dtype element type of C.
+ *   stream    CUDA stream the work is enqueued on.
+ *
+ * Semantics: C is overwritten with the product (no alpha/beta, no
+ * accumulation into C), as in the pages' kernel, which clears its
+ * accumulator and copies it out.  Accumulation is in fp32 in every path; the
+ * fp32 -> fp16 output conversion rounds to nearest even.  Elements of C
+ * between column N and the row stride ldc are never written.
+ *
+ * Supported dtype pairs: (F16 -> F16) and (F16 -> F32) run on the tensor
+ * cores; (F32 -> F32) runs on the SIMT fp32 path.  Any other pair returns
+ * TG_ERR_UNSUPPORTED.  Pointer alignment and leading dimensions never cause
+ * an error: operands that the TMA engine cannot address (base not 16-byte
+ * aligned, or a row stride that is not a multiple of 16 bytes) go to a
+ * predicated-load boundary kernel instead.
+ *
+ * Degenerate sizes: M == 0 or N == 0 is a no-op returning TG_OK (pointers
+ * may then be NULL).  K == 0 writes zeros to C (the empty sum); A and B may
+ * then be NULL.
+ *
+ * Errors (checked on the host before anything is enqueued; nothing is
+ * written when an error is returned):
+ *   TG_ERR_INVALID_ARG  a negative size; a NULL pointer that would be read
+ *                       or written; lda < K, ldb < N or ldc < N; or the byte
+ *                       span of C overlapping the span of A or of B.
+ *   TG_ERR_UNSUPPORTED  an unsupported dtype pair, or a size above 2^31 - 1.
+ *   TG_ERR_CUDA         a CUDA call made while launching failed.
+ *
+ * Ownership and memory: the caller owns A, B and C.  The library allocates
+ * no device memory per call; it keeps only per-device launch attributes and
+ * a 4-byte device error word for bounded-wait failures.
+ *
+ * Asynchrony: the call only enqueues work on `stream` and returns; it never
+ * synchronizes.  A kernel that times out on a bounded wait records that in
+ * the device error word; tg_gemm_check reports it.
+ *
+ * Thread safety: calls from several host threads are safe.
+ */
+tg_status tg_gemm(int64_t M, int64_t N, int64_t K,
+                  const void* A, int64_t lda,
+                  const void* B, int64_t ldb,
+                  void* C, int64_t ldc,
+                  tg_dtype in_dtype, tg_dtype out_dtype,
+                  tg_stream_t stream);
+
+/*
+ * tg_gemm_check -- synchronize `stream`, then read and clear the current
+ * device's error word.  Returns TG_OK, TG_ERR_CUDA if the stream reported a
+ * CUDA error, or TG_ERR_TIMEOUT if a kernel abandoned a bounded wait (its
+ * output is then undefined).
+ */
+tg_status tg_gemm_check(tg_stream_t stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* tg_status_string(tg_status status);
+
+/*
+ * Path selection, for tests and benchmarks.  tg_gemm_path reports, without
+ * launching anything, which kernel tg_gemm would run for these arguments on
+ * the current device:
+ *   0 none (no-op or error), 1 zero-fill (K == 0), 2 SIMT fp32,
+ *   3 TMA + tcgen05 main kernel, 4 boundary kernel (predicated loads),
+ *   5 skinny kernel (small M, split-K across a thread-block cluster).
+ * tg_gemm_force_path forces one of 2..5 for subsequent calls in this process
+ * (0 restores automatic selection); a forced path that cannot serve a call
+ * (e.g. the main kernel for misaligned operands, SIMT for fp16) makes that
+ * call return TG_ERR_UNSUPPORTED.
+ */
+int tg_gemm_path(int64_t M, int64_t N, int64_t K,
+                 const void* A, int64_t lda,
+                 const void* B, int64_t ldb,
+                 void* C, int64_t ldc,
+                 tg_dtype in_dtype, tg_dtype out_dtype);
+void tg_gemm_force_path(int path);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int tg_gemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TG_GEMM_H */

@@ -1,0 +1,196 @@
+"""CPU oracle for the tiled GEMM C = A x B (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library in
+``tiled_gemm_tg_gb300`` never imports it, and it never imports that library.
+
+The arithmetic lives in ``tg_oracle.c`` (plain C, fp64, exact binary16
+decode); this module only compiles it with gcc and marshals NumPy arrays.
+Every function states the passage it follows in the C source's header.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "tg_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libtg_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F16 = 1
+F32 = 2
+
+
+def build(force: bool = False) -> str:
+    """Compile tg_oracle.c into libtg_oracle.so (gcc, OpenMP when available)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-fno-fast-math",
+            "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    try:
+        subprocess.run(base[:5] + ["-fopenmp"] + base[5:], check=True,
+                       capture_output=True, text=True)
+    except subprocess.CalledProcessError:
+        # No OpenMP runtime: the oracle still works, single-threaded.
+        subprocess.run(base, check=True, capture_output=True, text=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _bind(path: str):
+    lib = ctypes.CDLL(path)
+    i64, vp = ctypes.c_int64, ctypes.c_void_p
+    lib.tgo_f16_to_f64.restype = ctypes.c_double
+    lib.tgo_f16_to_f64.argtypes = [ctypes.c_uint16]
+    lib.tgo_f64_to_f16.restype = ctypes.c_uint16
+    lib.tgo_f64_to_f16.argtypes = [ctypes.c_double]
+    lib.tgo_f16_to_f64_n.argtypes = [vp, vp, i64]
+    lib.tgo_f64_to_f16_n.argtypes = [vp, vp, i64]
+    lib.tgo_num_threads.restype = ctypes.c_int
+    lib.tgo_gemm.restype = ctypes.c_int
+    lib.tgo_gemm.argtypes = [i64, i64, i64, vp, i64, vp, i64, ctypes.c_int,
+                             vp, vp, ctypes.c_int]
+    lib.tgo_gemm_at.restype = ctypes.c_int
+    lib.tgo_gemm_at.argtypes = [i64, i64, i64, vp, i64, vp, i64, ctypes.c_int,
+                                i64, vp, vp, vp, vp, ctypes.c_int]
+    return lib
+
+
+def _operand(x: np.ndarray):
+    """Return (array, dtype code, row stride in elements) for a 2-D operand.
+
+    fp16 operands may be given as float16 or as uint16 bit patterns.  Rows
+    must be unit-stride; the row stride (leading dimension) may exceed the
+    row length, as with a sub-matrix view.
+    """
+    if x.ndim != 2:
+        raise ValueError("operands must be 2-D")
+    if x.dtype == np.float16:
+        x = x.view(np.uint16)
+    if x.dtype == np.uint16:
+        code = F16
+    elif x.dtype == np.float32:
+        code = F32
+    else:
+        raise TypeError(f"unsupported operand dtype {x.dtype}")
+    if x.size == 0:
+        return x, code, max(x.shape[1], 1)
+    if x.shape[1] > 1 and x.strides[1] != x.itemsize:
+        raise ValueError("rows must be contiguous")
+    ld = x.strides[0] // x.itemsize if x.shape[0] > 1 else max(x.shape[1], 1)
+    return x, code, int(ld)
+
+
+def _pair(a, b):
+    a, ca, lda = _operand(a)
+    b, cb, ldb = _operand(b)
+    if ca != cb:
+        raise TypeError("A and B must have the same dtype")
+    if a.shape[1] != b.shape[0]:
+        raise ValueError("inner dimensions differ")
+    return a, b, ca, lda, ldb
+
+
+class Oracle:
+    """The oracle bound to one compiled copy of tg_oracle.c."""
+
+    def __init__(self, lib_path: str):
+        self.lib = _bind(lib_path)
+
+    def num_threads(self) -> int:
+        """Threads the oracle's OpenMP loops use by default."""
+        return int(self.lib.tgo_num_threads())
+
+    def f16_bits_to_f64(self, bits: np.ndarray) -> np.ndarray:
+        """Exact binary16 -> binary64 decode of uint16 bit patterns."""
+        src = np.ascontiguousarray(bits, dtype=np.uint16)
+        out = np.empty(src.shape, dtype=np.float64)
+        self.lib.tgo_f16_to_f64_n(src.ctypes.data, out.ctypes.data, src.size)
+        return out
+
+    def f64_to_f16_bits(self, x: np.ndarray) -> np.ndarray:
+        """binary64 -> binary16 bit patterns, round to nearest, ties to even."""
+        src = np.ascontiguousarray(x, dtype=np.float64)
+        out = np.empty(src.shape, dtype=np.uint16)
+        self.lib.tgo_f64_to_f16_n(src.ctypes.data, out.ctypes.data, src.size)
+        return out
+
+    def gemm(self, a: np.ndarray, b: np.ndarray, nthreads: int = 0):
+        """C = A x B and S = sum_k |A_ik B_kj|, both fp64 M x N arrays."""
+        a, b, code, lda, ldb = _pair(a, b)
+        M, K = a.shape
+        N = b.shape[1]
+        C = np.empty((M, N), dtype=np.float64)
+        S = np.empty((M, N), dtype=np.float64)
+        rc = self.lib.tgo_gemm(M, N, K, a.ctypes.data, lda, b.ctypes.data, ldb,
+                               code, C.ctypes.data, S.ctypes.data, int(nthreads))
+        if rc != 0:
+            raise RuntimeError("oracle rejected its arguments")
+        return C, S
+
+    def gemm_at(self, a: np.ndarray, b: np.ndarray, rows, cols, nthreads: int = 0):
+        """C and S at the listed output positions only (same definition)."""
+        a, b, code, lda, ldb = _pair(a, b)
+        M, K = a.shape
+        N = b.shape[1]
+        r = np.ascontiguousarray(rows, dtype=np.int64)
+        c = np.ascontiguousarray(cols, dtype=np.int64)
+        if r.shape != c.shape:
+            raise ValueError("rows and cols differ in length")
+        C = np.empty(r.shape, dtype=np.float64)
+        S = np.empty(r.shape, dtype=np.float64)
+        rc = self.lib.tgo_gemm_at(M, N, K, a.ctypes.data, lda, b.ctypes.data, ldb,
+                                  code, r.size, r.ctypes.data, c.ctypes.data,
+                                  C.ctypes.data, S.ctypes.data, int(nthreads))
+        if rc != 0:
+            raise RuntimeError("oracle rejected its arguments")
+        return C, S
+
+
+def _default() -> Oracle:
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = Oracle(build())
+        return _lib
+
+
+def num_threads() -> int:
+    return _default().num_threads()
+
+
+def f16_bits_to_f64(bits):
+    return _default().f16_bits_to_f64(bits)
+
+
+def f64_to_f16_bits(x):
+    return _default().f64_to_f16_bits(x)
+
+
+def gemm(a, b, nthreads: int = 0):
+    return _default().gemm(a, b, nthreads)
+
+
+def gemm_at(a, b, rows, cols, nthreads: int = 0):
+    return _default().gemm_at(a, b, rows, cols, nthreads)
+
+
+def tolerance(C_ref: np.ndarray, S: np.ndarray, out_f16: bool) -> np.ndarray:
+    """Per-element acceptance bound for a kernel result against the oracle.
+
+    2e-3 * S + 1e-5 for fp32 accumulation, plus 1e-2 * |C_ref| when the
+    output is fp16 (the relative threshold of §3.3 第四步 of the
+    gsyq.cn/news/429607 article).
+    """
+    tol = 2e-3 * S + 1e-5
+    if out_f16:
+        tol = tol + 1e-2 * np.abs(C_ref)
+    return tol

@@ -1,0 +1,206 @@
+/*
+ * tg_oracle.c -- plain, slow, obviously correct CPU oracle for C = A x B.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this code.  The product path (the
+ * CUDA library under tiled_gemm_tg_gb300/) never calls it and shares no code,
+ * header, table or helper with it.
+ *
+ * What it computes, and where the pages define it:
+ *   - The product is the plain definition  C[i,j] = sum_k A[i,k] * B[k,j]
+ *     over row-major operands, written out as the triple loop of
+ *     "TileLang实战：用Python DSL自动生成高性能GPU计算内核" (gsyq.cn), §3.1,
+ *     which the same page's §3.2 checks against a NumPy dot product.
+ *   - Inputs are fp16 (or fp32 for the small example) and the pages accumulate
+ *     in fp32 ("企业官网建设流程全解析" (cf-1.com), §3.3: accum_dtype float32).
+ *     The oracle is stricter than that: every fp16 input is decoded exactly to
+ *     binary64 from the IEEE-754 binary16 bit layout, every product of two
+ *     fp16 values is exact in binary64, and the sum runs in binary64 in
+ *     ascending k.  Its own error is therefore far below any kernel's.
+ *   - Alongside C it returns S[i,j] = sum_k |A[i,k] * B[k,j]|, the scale that
+ *     the acceptance bound  |C_gpu - C| <= 2e-3 * S + 1e-5 (+ 1e-2 |C| for an
+ *     fp16 output; the 1e-2 relative threshold is the one in §3.3 "第四步" of
+ *     the gsyq.cn/news/429607 article) is written against.
+ *   - An fp64 -> fp16 round-to-nearest-even encoder, written from the
+ *     binary16 definition, converts oracle results for bitwise comparison
+ *     with an fp16 kernel output.  It converts directly from binary64, so no
+ *     intermediate fp32 rounding (double rounding) can occur.
+ *
+ * Pins (tests/test_oracle.py): the decoder over all 65536 bit patterns
+ * against NumPy's binary16 conversion; the encoder against NumPy on random
+ * values and against hand-built ties; the product against a hand-computed
+ * 4x4 integer example (tests/golden), the 8x8 all-ones example of the
+ * TileLang实战 page §6.2, closed forms (identity, all-ones, diagonal), the
+ * transpose invariant (AB)^T = B^T A^T bitwise, and NumPy fp64 matmul on
+ * exactly representable inputs.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define TGO_F16 1
+#define TGO_F32 2
+
+/* ---- binary16 decode (IEEE-754: 1 sign, 5 exponent bits biased by 15,
+ *      10 fraction bits) ------------------------------------------------- */
+double tgo_f16_to_f64(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0) {
+        /* zero and subnormals: 2^-14 * (f / 1024) = f * 2^-24 */
+        v = ldexp((double)f, -24);
+    } else if (e == 31) {
+        v = f ? NAN : INFINITY;
+    } else {
+        /* normals: 2^(e-15) * (1 + f/1024) = (1024 + f) * 2^(e-25) */
+        v = ldexp((double)(1024 + f), e - 25);
+    }
+    return sign ? -v : v;
+}
+
+/* ---- binary64 -> binary16, round to nearest, ties to even -------------- */
+uint16_t tgo_f64_to_f16(double x)
+{
+    uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    if (isnan(x)) return (uint16_t)(sign | 0x7e00u);
+    double a = fabs(x);
+    if (isinf(a)) return (uint16_t)(sign | 0x7c00u);
+    /* 65504 is the largest finite half; the midpoint to the next binade
+     * value 65536 is 65520, and a tie there goes to the even significand
+     * (65536), which overflows.  So everything >= 65520 becomes infinity. */
+    if (a >= 65520.0) return (uint16_t)(sign | 0x7c00u);
+    if (a < ldexp(1.0, -14)) {
+        /* subnormal range: values are integer multiples of 2^-24.
+         * Scaling by 2^24 is exact; nearbyint() rounds ties to even under the
+         * default rounding mode.  A result of 1024 is the smallest normal,
+         * whose bit pattern 0x0400 is exactly 1024. */
+        double q = nearbyint(ldexp(a, 24));
+        return (uint16_t)(sign | (uint16_t)q);
+    }
+    int e2;
+    (void)frexp(a, &e2);            /* a in [2^(e2-1), 2^e2) */
+    int E = e2 - 1;                 /* a in [2^E, 2^(E+1)), E in [-14, 15] */
+    double q = nearbyint(ldexp(a, 10 - E)); /* significand scaled to [1024, 2048] */
+    uint32_t mant = (uint32_t)q;
+    if (mant == 2048u) {            /* rounding carried into the next binade */
+        mant = 1024u;
+        E += 1;
+    }
+    if (E > 15) return (uint16_t)(sign | 0x7c00u);
+    return (uint16_t)(sign | (uint16_t)(((uint32_t)(E + 15) << 10) | (mant - 1024u)));
+}
+
+/* Bulk helpers so the Python side need not loop element by element. */
+void tgo_f16_to_f64_n(const uint16_t* src, double* dst, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) dst[i] = tgo_f16_to_f64(src[i]);
+}
+
+void tgo_f64_to_f16_n(const double* src, uint16_t* dst, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) dst[i] = tgo_f64_to_f16(src[i]);
+}
+
+static double load_elem(const void* p, int64_t idx, int dtype)
+{
+    if (dtype == TGO_F16) return tgo_f16_to_f64(((const uint16_t*)p)[idx]);
+    return (double)(((const float*)p)[idx]);
+}
+
+int tgo_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * Full product.  A is M x K with row stride lda, B is K x N with row stride
+ * ldb (both row-major, element type in_dtype); C and S are dense M x N fp64.
+ * Rows of C are independent, so they are spread over threads; within a row
+ * the sum runs in ascending k exactly as the definition reads.
+ * Returns 0, or -1 on a bad argument or failed allocation.
+ */
+int tgo_gemm(int64_t M, int64_t N, int64_t K,
+             const void* A, int64_t lda, const void* B, int64_t ldb,
+             int in_dtype, double* C, double* S, int nthreads)
+{
+    if (M < 0 || N < 0 || K < 0) return -1;
+    if (in_dtype != TGO_F16 && in_dtype != TGO_F32) return -1;
+    if (M == 0 || N == 0) return 0;
+    if (K > 0 && (lda < K || ldb < N || !A || !B)) return -1;
+
+    /* Decode B once; A is decoded one element at a time inside the loop. */
+    double* Bd = NULL;
+    if (K > 0) {
+        Bd = (double*)malloc(sizeof(double) * (size_t)K * (size_t)N);
+        if (!Bd) return -1;
+        for (int64_t k = 0; k < K; ++k)
+            for (int64_t j = 0; j < N; ++j)
+                Bd[k * N + j] = load_elem(B, k * ldb + j, in_dtype);
+    }
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (int64_t i = 0; i < M; ++i) {
+        double* c = C + i * N;
+        double* s = S + i * N;
+        for (int64_t j = 0; j < N; ++j) { c[j] = 0.0; s[j] = 0.0; }
+        for (int64_t k = 0; k < K; ++k) {
+            double a = load_elem(A, i * lda + k, in_dtype);
+            const double* b = Bd + k * N;
+            for (int64_t j = 0; j < N; ++j) {
+                double p = a * b[j];
+                c[j] += p;
+                s[j] += fabs(p);
+            }
+        }
+    }
+    (void)nthreads;
+    free(Bd);
+    return 0;
+}
+
+/*
+ * Selected elements only: for each t < n, C[t] and S[t] for output element
+ * (rows[t], cols[t]), by the same definition (ascending k, fp64).  This is
+ * what lets the tests check a full-size product element by element without
+ * computing all of it.
+ */
+int tgo_gemm_at(int64_t M, int64_t N, int64_t K,
+                const void* A, int64_t lda, const void* B, int64_t ldb,
+                int in_dtype, int64_t n, const int64_t* rows,
+                const int64_t* cols, double* C, double* S, int nthreads)
+{
+    if (M < 0 || N < 0 || K < 0 || n < 0) return -1;
+    if (in_dtype != TGO_F16 && in_dtype != TGO_F32) return -1;
+    for (int64_t t = 0; t < n; ++t)
+        if (rows[t] < 0 || rows[t] >= M || cols[t] < 0 || cols[t] >= N) return -1;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 16) num_threads(nthreads)
+#endif
+    for (int64_t t = 0; t < n; ++t) {
+        int64_t i = rows[t], j = cols[t];
+        double c = 0.0, s = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double p = load_elem(A, i * lda + k, in_dtype) * load_elem(B, k * ldb + j, in_dtype);
+            c += p;
+            s += fabs(p);
+        }
+        C[t] = c;
+        S[t] = s;
+    }
+    (void)nthreads;
+    return 0;
+}

@@ -1,0 +1,269 @@
+"""Pins for the CPU oracle, checked against facts that do not come from it.
+
+Each pin would fail for a plausible mistake in the oracle: a wrong exponent
+bias or subnormal scale in the binary16 decoder, round-half-away instead of
+ties-to-even or an fp32 detour in the encoder, a dropped term, a wrong sign,
+a transposed operand or an ignored leading dimension in the product, or a
+missing absolute value in S.  test_planted_mistakes_are_caught builds such
+mutants of the oracle's C source and checks that the pins reject each one.
+"""
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import Oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_blocks(path):
+    blocks, cur = {}, None
+    with open(path) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            if re.fullmatch(r"[A-Za-z]+", line):
+                cur = line
+                blocks[cur] = []
+            else:
+                blocks[cur].append([float(v) for v in line.split()])
+    return {k: np.array(v) for k, v in blocks.items()}
+
+
+def _read_ties():
+    rows = []
+    with open(os.path.join(GOLDEN, "f16_ties.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            tok = line.split()
+            x = float.fromhex(tok[0]) if "0x" in tok[0] else float(tok[0])
+            rows.append((x, int(tok[1], 16)))
+    return rows
+
+
+# ---------------------------------------------------------------- pins, as
+# functions of an Oracle so the mutation test can run them on mutants.
+
+def pin_decode_exhaustive(o: Oracle):
+    bits = np.arange(65536, dtype=np.uint16)
+    got = o.f16_bits_to_f64(bits)
+    ref = bits.view(np.float16).astype(np.float64)  # NumPy's own binary16 conversion
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    # sign of zero
+    assert np.signbit(got[0x8000]) and not np.signbit(got[0x0000])
+
+
+def pin_decode_by_hand(o: Oracle):
+    cases = {0x3c00: 1.0, 0x0001: 2.0 ** -24, 0x0400: 2.0 ** -14, 0x03ff: 1023 * 2.0 ** -24,
+             0x7bff: 65504.0, 0xc000: -2.0, 0x3555: 0x555 * 2.0 ** -12,
+             0x7c00: np.inf, 0xfc00: -np.inf}
+    got = o.f16_bits_to_f64(np.array(list(cases), dtype=np.uint16))
+    assert np.array_equal(got, np.array(list(cases.values())))
+
+
+def pin_encode_ties(o: Oracle):
+    ties = _read_ties()
+    got = o.f64_to_f16_bits(np.array([x for x, _ in ties]))
+    want = np.array([h for _, h in ties], dtype=np.uint16)
+    bad = [(ties[i][0].hex(), hex(got[i]), hex(want[i])) for i in np.flatnonzero(got != want)]
+    assert not bad, bad
+
+
+def pin_encode_vs_numpy(o: Oracle):
+    rng = np.random.default_rng(7)
+    parts = [rng.standard_normal(20000) * s for s in (1e-7, 1e-5, 1e-3, 1.0, 1e2, 1e4, 6e4)]
+    parts.append(rng.uniform(-70000, 70000, 20000))
+    x = np.concatenate(parts)
+    got = o.f64_to_f16_bits(x)
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def pin_roundtrip(o: Oracle):
+    bits = np.arange(65536, dtype=np.uint16)
+    vals = o.f16_bits_to_f64(bits)
+    keep = ~np.isnan(vals)
+    assert np.array_equal(o.f64_to_f16_bits(vals[keep]), bits[keep])
+
+
+def pin_gemm_4x4(o: Oracle):
+    g = _read_blocks(os.path.join(GOLDEN, "gemm_4x4_int.txt"))
+    for dt in (np.float16, np.float32):
+        C, S = o.gemm(g["A"].astype(dt), g["B"].astype(dt))
+        assert np.array_equal(C, g["C"])
+        assert np.array_equal(S, g["S"])
+
+
+def pin_gemm_8x8_ones(o: Oracle):
+    spec = {}
+    with open(os.path.join(GOLDEN, "gemm_8x8_ones.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].split()
+            if line:
+                spec[line[0]] = int(line[1])
+    a = np.ones((spec["M"], spec["K"]), np.float16)
+    b = np.ones((spec["K"], spec["N"]), np.float16)
+    C, S = o.gemm(a, b)
+    assert np.all(C == spec["value"]) and np.all(S == spec["value"])
+
+
+def pin_closed_forms(o: Oracle):
+    rng = np.random.default_rng(1)
+    # identity B: C = A exactly (each row sums one exact product and zeros)
+    a = rng.standard_normal((37, 29)).astype(np.float16)
+    C, _ = o.gemm(a, np.eye(29, dtype=np.float16))
+    assert np.array_equal(C, a.astype(np.float64))
+    # all-ones: C = K
+    C, S = o.gemm(np.ones((5, 300), np.float16), np.ones((300, 7), np.float16))
+    assert np.all(C == 300) and np.all(S == 300)
+    # diagonal A scales the rows of B
+    d = rng.standard_normal(23).astype(np.float16)
+    b = rng.standard_normal((23, 19)).astype(np.float16)
+    C, _ = o.gemm(np.diag(d), b)
+    assert np.array_equal(C, d.astype(np.float64)[:, None] * b.astype(np.float64))
+    # a single nonzero A entry picks one row of B at one output row
+    a = np.zeros((6, 11), np.float16)
+    a[4, 9] = -3
+    b = rng.standard_normal((11, 13)).astype(np.float16)
+    C, _ = o.gemm(a, b)
+    want = np.zeros((6, 13))
+    want[4] = -3 * b[9].astype(np.float64)
+    assert np.array_equal(C, want)
+
+
+def pin_transpose(o: Oracle):
+    rng = np.random.default_rng(2)
+    a = rng.standard_normal((21, 34)).astype(np.float16)
+    b = rng.standard_normal((34, 13)).astype(np.float16)
+    C, S = o.gemm(a, b)
+    Ct, St = o.gemm(np.ascontiguousarray(b.T), np.ascontiguousarray(a.T))
+    assert np.array_equal(C, Ct.T) and np.array_equal(S, St.T)
+
+
+def pin_vs_numpy_exact(o: Oracle):
+    rng = np.random.default_rng(3)
+    a = rng.integers(-3, 4, (45, 70)).astype(np.float16)
+    b = rng.integers(-3, 4, (70, 33)).astype(np.float16)
+    C, S = o.gemm(a, b)
+    A, B = a.astype(np.float64), b.astype(np.float64)
+    assert np.array_equal(C, A @ B)
+    assert np.array_equal(S, np.abs(A) @ np.abs(B))
+
+
+def pin_vs_numpy_random(o: Oracle):
+    rng = np.random.default_rng(4)
+    for dt in (np.float16, np.float32):
+        a = rng.standard_normal((50, 130)).astype(dt)
+        b = rng.standard_normal((130, 41)).astype(dt)
+        C, S = o.gemm(a, b)
+        ref = a.astype(np.float64) @ b.astype(np.float64)
+        assert np.all(np.abs(C - ref) <= 1e-13 * S)
+        assert np.allclose(S, np.abs(a.astype(np.float64)) @ np.abs(b.astype(np.float64)),
+                           rtol=1e-13, atol=0)
+
+
+def pin_leading_dims(o: Oracle):
+    rng = np.random.default_rng(5)
+    big_a = rng.standard_normal((40, 64)).astype(np.float16)
+    big_b = rng.standard_normal((60, 72)).astype(np.float16)
+    a, b = big_a[:31, 3:50], big_b[7:54, 5:66]  # row strides exceed row lengths
+    C, S = o.gemm(a, b)
+    ref = a.astype(np.float64) @ b.astype(np.float64)
+    assert np.all(np.abs(C - ref) <= 1e-13 * S)
+    C2, S2 = o.gemm(np.ascontiguousarray(a), np.ascontiguousarray(b))
+    assert np.array_equal(C, C2) and np.array_equal(S, S2)
+
+
+def pin_sampled(o: Oracle):
+    rng = np.random.default_rng(6)
+    a = rng.standard_normal((33, 57)).astype(np.float16)
+    b = rng.standard_normal((57, 29)).astype(np.float16)
+    C, S = o.gemm(a, b)
+    r = rng.integers(0, 33, 200)
+    c = rng.integers(0, 29, 200)
+    Cs, Ss = o.gemm_at(a, b, r, c)
+    assert np.array_equal(Cs, C[r, c]) and np.array_equal(Ss, S[r, c])
+    ref = np.einsum("tk,kt->t", a[r].astype(np.float64), b[:, c].astype(np.float64))
+    assert np.all(np.abs(Cs - ref) <= 1e-13 * Ss)
+
+
+def pin_degenerate(o: Oracle):
+    C, S = o.gemm(np.zeros((3, 0), np.float16), np.zeros((0, 5), np.float16))
+    assert C.shape == (3, 5) and np.all(C == 0) and np.all(S == 0)
+    C, S = o.gemm(np.zeros((0, 4), np.float16), np.zeros((4, 5), np.float16))
+    assert C.shape == (0, 5)
+
+
+PINS = [pin_decode_exhaustive, pin_decode_by_hand, pin_encode_ties, pin_encode_vs_numpy,
+        pin_roundtrip, pin_gemm_4x4, pin_gemm_8x8_ones, pin_closed_forms, pin_transpose,
+        pin_vs_numpy_exact, pin_vs_numpy_random, pin_leading_dims, pin_sampled,
+        pin_degenerate]
+
+
+@pytest.fixture(scope="module")
+def o():
+    return oracle._default()
+
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
+def test_pin(o, pin):
+    pin(o)
+
+
+def test_tolerance_formula():
+    C = np.array([1.0, -2.0, 0.0])
+    S = np.array([3.0, 4.0, 5.0])
+    assert np.allclose(oracle.tolerance(C, S, False), 2e-3 * S + 1e-5)
+    assert np.allclose(oracle.tolerance(C, S, True), 2e-3 * S + 1e-5 + 1e-2 * np.abs(C))
+
+
+def test_threads_reported(o):
+    assert o.num_threads() >= 1
+
+
+# ------------------------------------------------------------ planted mistakes
+
+MUTANTS = {
+    "decode_bias": ("(double)(1024 + f), e - 25)", "(double)(1024 + f), e - 24)"),
+    "decode_subnormal": ("v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
+    "encode_half_away": ("double q = nearbyint(ldexp(a, 10 - E));",
+                         "double q = round(ldexp(a, 10 - E));"),
+    "encode_fp32_detour": ("double a = fabs(x);", "double a = (double)(float)fabs(x);"),
+    "product_sign": ("c[j] += p;", "c[j] -= p;"),
+    "dropped_term": ("for (int64_t k = 0; k < K; ++k) {\n            double a =",
+                     "for (int64_t k = 1; k < K; ++k) {\n            double a ="),
+    "ignored_lda": ("double a = load_elem(A, i * lda + k, in_dtype);",
+                    "double a = load_elem(A, i * K + k, in_dtype);"),
+    "missing_abs": ("s[j] += fabs(p);", "s[j] += p;"),
+    "transposed_b": ("Bd[k * N + j] = load_elem(B, k * ldb + j, in_dtype);",
+                     "Bd[k * N + j] = load_elem(B, (j % K) * ldb + (k % N), in_dtype);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistakes_are_caught(name, tmp_path):
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "tg_oracle.c")).read()
+    old, new = MUTANTS[name]
+    assert src.count(old) == 1, f"mutation anchor for {name} not found"
+    path = tmp_path / "mutant.c"
+    path.write_text(src.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O1", "-std=c11", "-shared", "-fPIC", "-ffp-contract=off",
+                    str(path), "-o", str(lib), "-lm"], check=True)
+    mutant = Oracle(str(lib))
+    caught = []
+    for pin in PINS:
+        try:
+            pin(mutant)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught the planted mistake {name}"

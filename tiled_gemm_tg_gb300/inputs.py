@@ -1,0 +1,96 @@
+"""Seeded synthetic operands for the GEMM workloads.
+
+This module is shared by the tests, the benchmark and the smoke check; it
+holds no GEMM arithmetic, only the random draws.  Every operand is drawn in
+fp32 on the CPU from ``torch.Generator().manual_seed(seed)`` and then cast to
+the input dtype (fp32 -> fp16 rounds to nearest even).  The A seed of a
+workload is ``seed_base + 1`` and the B seed ``seed_base + 2``.
+
+The shapes and distributions are the five workloads the GEMM is judged on:
+the fp32 128^3 triple-loop example, the fp16 edge set, the A[1024,512] x
+B[512,2048] tiling example, the 8192^3 compute-bound square and the two
+skinny/wide shapes.  The pages benchmark on no public dataset, so these
+synthetic draws are the whole input set.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    M: int
+    N: int
+    K: int
+    dist: str          # "normal", "normal_rsqrtk", "uniform", "normal_0.02", "int2"
+    in_dtype: str      # "f16" or "f32"
+    out_dtype: str     # "f16" or "f32"
+    seed_base: int
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+    def algorithmic_bytes(self) -> int:
+        """A and B read once, C written once."""
+        ein = 2 if self.in_dtype == "f16" else 4
+        eout = 2 if self.out_dtype == "f16" else 4
+        return (self.M * self.K + self.K * self.N) * ein + self.M * self.N * eout
+
+
+WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("f32_128x128x128", 128, 128, 128, "normal", "f32", "f32", 1000),
+        Workload("edge_4x4x4", 4, 4, 4, "normal", "f16", "f16", 2000),
+        Workload("edge_128x256x512", 128, 256, 512, "normal", "f16", "f16", 2010),
+        Workload("edge_127x255x512", 127, 255, 512, "normal", "f16", "f16", 2020),
+        Workload("edge_1x255x17", 1, 255, 17, "normal", "f16", "f16", 2030),
+        Workload("tile_1024x2048x512", 1024, 2048, 512, "normal_rsqrtk", "f16", "f16", 3000),
+        Workload("square_8192", 8192, 8192, 8192, "uniform", "f16", "f16", 4000),
+        Workload("skinny_16x4096x4096", 16, 4096, 4096, "normal_0.02", "f16", "f16", 5000),
+        Workload("wide_4096x16384x4096", 4096, 16384, 4096, "normal_0.02", "f16", "f16", 5100),
+    ]
+}
+
+EDGE_SET = ["edge_4x4x4", "edge_128x256x512", "edge_127x255x512", "edge_1x255x17"]
+
+
+def draw(shape, dist: str, seed: int, dtype: str, k: int | None = None) -> torch.Tensor:
+    """One seeded operand on the CPU, row-major and contiguous."""
+    g = torch.Generator().manual_seed(int(seed))
+    if dist == "normal":
+        x = torch.randn(shape, generator=g, dtype=torch.float32)
+    elif dist == "normal_rsqrtk":
+        if not k:
+            raise ValueError("normal_rsqrtk needs the contraction length k")
+        x = torch.randn(shape, generator=g, dtype=torch.float32) * (1.0 / math.sqrt(k))
+    elif dist == "uniform":
+        x = torch.rand(shape, generator=g, dtype=torch.float32) * 2.0 - 1.0
+    elif dist == "normal_0.02":
+        x = torch.randn(shape, generator=g, dtype=torch.float32) * 0.02
+    elif dist == "int2":
+        # integers in {-2,...,2}: every product and every partial sum up to
+        # 2^24 / 4 terms is exact in fp32, so results are unique.
+        x = torch.randint(-2, 3, shape, generator=g).to(torch.float32)
+    elif dist == "ones":
+        x = torch.ones(shape, dtype=torch.float32)
+    else:
+        raise ValueError(f"unknown distribution {dist}")
+    if dtype == "f16":
+        return x.to(torch.float16)
+    if dtype == "f32":
+        return x
+    raise ValueError(f"unknown dtype {dtype}")
+
+
+def operands(w: Workload, dist: str | None = None):
+    """(A, B) on the CPU for a workload, from its own seeds."""
+    d = dist or w.dist
+    a = draw((w.M, w.K), d, w.seed_base + 1, w.in_dtype, k=w.K)
+    b = draw((w.K, w.N), d, w.seed_base + 2, w.in_dtype, k=w.K)
+    return a, b
