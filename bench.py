@@ -1,0 +1,416 @@
+#!/usr/bin/env python
+"""Benchmark of the tiled GEMM C = A x B on GB300.
+
+A step is one pass of the whole path: one tg_gemm call (one kernel launch)
+on one batch of synthetic fp16 operands already resident in HBM.  The
+default workload is the 8192^3 fp16 GEMM (U(-1,1) inputs, fp32 accumulation,
+fp16 output), the shape the tensor-core roofline is judged on.  Two operand
+sets rotate between steps so every step streams 384 MB of fresh A/B/C, more
+than the 129 MB L2.
+
+Prints ONE JSON line (rank 0):
+  value      whole-job TFLOP/s (2*M*N*K per step) over the timed steps;
+  e2e        the same metric through the C ABI from pinned HOST buffers,
+             with the host->device copies of A and B and the device->host
+             copy of C inside the timed region;
+  roofline   achieved TFLOP/s of the GEMM kernel (CUDA events around each
+             launch on the launching stream) against the measured peak;
+  cpu_baseline  the CPU oracle timed on a bounded row sample of the same
+             product, on the host's cores (N=1 only).
+`--impl reference` times the oracle itself as the reference arm.
+
+Multi-GPU (torchrun): every rank runs an independent replica of the same
+workload on its own GPU; there is no data exchange.  value = all ranks'
+FLOPs / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s and % of GB300 dense FP16 tensor peak (1 GPU), vs CPU oracle"
+NOMINAL_FP16_DENSE_TFLOPS = 2500.0  # external vendor figure, context only
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic (read + write bytes per launch) of the main kernel from one
+# ncu capture, keyed by workload, with the hash of the kernel sources it was
+# taken on.  A stale hash means the kernel changed since: traffic is null.
+NCU_TRAFFIC = {}
+
+KERNEL_SOURCES = ["tiled_gemm_tg_gb300/csrc/gemm_tc.cu", "tiled_gemm_tg_gb300/csrc/ptx.cuh"]
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 100 ms while running."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.samples = []
+        self.proc = None
+        self.gpu_id = gpu_id
+        self.thread = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        window = "timed"
+        if len(inside) < 3:
+            inside = [p for (_, p) in self.samples]
+            window = "whole run (timed region shorter than the sampling period)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = sorted(v for v in (num(p[1]) for p in inside) if v is not None)
+        smax = max((v for v in (num(p[2]) for p in inside) if v is not None), default=None)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4)
+                          if p[5 + i].lower().startswith("active")})
+        power = [v for v in (num(p[3]) for p in inside) if v is not None]
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": smax,
+                "reasons": reasons, "samples": len(inside), "window": window,
+                "power_w_max": max(power) if power else None}
+
+
+# ----------------------------------------------------------- CPU oracle leg
+
+def oracle_rows_sample(w, a_cpu, b_cpu, target_s: float):
+    """Time the oracle on whole rows of C until about target_s of work.
+    Returns (TFLOP/s, rows, seconds, threads)."""
+    import oracle
+
+    nt = oracle.num_threads()
+    a_np = a_cpu.numpy()
+    b_np = b_cpu.numpy()
+    rows = max(1, min(nt, w.M))
+    t = time.perf_counter()
+    oracle.gemm(a_np[:rows], b_np)
+    dt = time.perf_counter() - t
+    if dt < target_s:
+        scale = max(1, int(target_s / max(dt, 1e-3)))
+        rows = min(w.M, rows * scale)
+        t = time.perf_counter()
+        oracle.gemm(a_np[:rows], b_np)
+        dt = time.perf_counter() - t
+    return 2.0 * rows * w.N * w.K / dt / 1e12, rows, dt, nt
+
+
+# ------------------------------------------------------------------- main
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args, w):
+    """The reference arm: the CPU oracle, timed on the host's cores."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from tiled_gemm_tg_gb300 import inputs
+
+    a, b = inputs.operands(w)
+    nt = oracle.num_threads()
+    a_np, b_np = a.numpy(), b.numpy()
+    # size one step so that warmup + steps stay within ~2-3 minutes
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    rows = max(1, min(nt, w.M))
+    t = time.perf_counter()
+    oracle.gemm(a_np[:rows], b_np)
+    dt = time.perf_counter() - t
+    if dt < budget:
+        rows = min(w.M, rows * max(1, int(budget / max(dt, 1e-3))))
+    for _ in range(args.warmup):
+        oracle.gemm(a_np[:rows], b_np)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.gemm(a_np[:rows], b_np)
+    el = time.perf_counter() - t0
+    value = 2.0 * rows * w.N * w.K * args.steps / el / 1e12
+    sample = f"{rows} of {w.M} rows of C per step (full N={w.N}, K={w.K})"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "in_dtype": w.in_dtype,
+                   "out_dtype": w.out_dtype, "dist": w.dist},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nt, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="square_8192")
+    ap.add_argument("--e2e-steps", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    from tiled_gemm_tg_gb300 import inputs
+    w = inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import torch
+
+    import tiled_gemm_tg_gb300 as tg
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    tg.lib()  # fail loudly if the library is missing
+
+    # operands: drawn on the host from the workload's seeds, copied to HBM
+    a_cpu, b_cpu = inputs.operands(w)
+    out_dt = torch.float16 if w.out_dtype == "f16" else torch.float32
+    in_code = tg.F16 if w.in_dtype == "f16" else tg.F32
+    out_code = tg.F16 if w.out_dtype == "f16" else tg.F32
+    n_sets = 2
+    sets = []
+    for i in range(n_sets):
+        a = a_cpu.to(dev)
+        b = b_cpu.to(dev)
+        if i:  # distinct buffers with the same values (rotated for L2)
+            a = a.clone()
+            b = b.clone()
+        c = torch.empty((w.M, w.N), dtype=out_dt, device=dev)
+        sets.append((a, b, c))
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    M, N, K = w.M, w.N, w.K
+
+    def step(i):
+        a, b, c = sets[i % n_sets]
+        st = tg.tg_gemm(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N, in_code,
+                        out_code, sh)
+        if st != tg.TG_OK:
+            raise tg.TgError(st)
+
+    path = tg.tg_gemm_path(M, N, K, sets[0][0].data_ptr(), K, sets[0][1].data_ptr(), N,
+                           sets[0][2].data_ptr(), N, in_code, out_code)
+
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = None
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.3)
+
+    for i in range(args.warmup):
+        step(i)
+    tg.check(stream)
+
+    # --- timed region: K steps, an event pair around every launch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    host_t0 = time.time()
+    t_start.record(stream)
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        step(i)
+        evs[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    host_t1 = time.time()
+    if ws > 1:
+        torch.distributed.barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    kern_ms = sum(s.elapsed_time(e) for s, e in evs) / args.steps
+    if tg.tg_gemm_check(sh) != tg.TG_OK:
+        raise RuntimeError("a kernel abandoned a bounded wait during the timed region")
+
+    if ws > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    flops = 2.0 * M * N * K
+    value = ws * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
+
+    # --- end to end through the C ABI from pinned host buffers
+    e2e_steps = args.e2e_steps or max(3, min(args.steps, 20))
+    a_h = a_cpu.pin_memory()
+    b_h = b_cpu.pin_memory()
+    c_h = torch.empty((M, N), dtype=out_dt).pin_memory()
+    a_d, b_d, c_d = sets[0]
+
+    def e2e_step():
+        a_d.copy_(a_h, non_blocking=True)
+        b_d.copy_(b_h, non_blocking=True)
+        st = tg.tg_gemm(M, N, K, a_d.data_ptr(), K, b_d.data_ptr(), N, c_d.data_ptr(), N,
+                        in_code, out_code, sh)
+        if st != tg.TG_OK:
+            raise tg.TgError(st)
+        c_h.copy_(c_d, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        torch.distributed.barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if ws > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = ws * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    ein = a_cpu.element_size()
+    h2d = (M * K + K * N) * ein
+    d2h = M * N * c_h.element_size()
+
+    sampler.stop()
+    clocks = sampler.summary(host_t0, host_t1)
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = flops / (kern_ms * 1e-3) / 1e12
+    traffic = None
+    rec = NCU_TRAFFIC.get(w.name)
+    if rec and rec.get("kernel_hash") == kernel_hash():
+        traffic = rec["bytes"]
+    roofline = {
+        "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+        "frac": achieved / peak, "traffic": traffic,
+        "kernel": {3: "gemm_tc_main_kernel", 4: "gemm_tc_boundary_kernel",
+                   2: "gemm_simt_f32_kernel"}.get(path, str(path)),
+        "kernel_ms": kern_ms,
+        "peak_source": f"{peak_src} bf16 burst (torch.matmul 8192^3) x 1.0 fp16/bf16 nominal ratio",
+        "frac_of_nominal_2500": achieved / NOMINAL_FP16_DENSE_TFLOPS,
+        "algorithmic_bytes": w.algorithmic_bytes(),
+        "achieved_gbs": w.algorithmic_bytes() / (kern_ms * 1e-3) / 1e9,
+    }
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        v, rows, secs, nt = oracle_rows_sample(w, a_cpu, b_cpu, args.cpu_seconds)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": nt, "kind": "oracle",
+               "sample": f"{rows} of {M} rows of C (full N={N}, K={K}), {secs:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "M": M, "N": N, "K": K, "in_dtype": w.in_dtype,
+                       "accum": "f32", "out_dtype": w.out_dtype, "dist": w.dist,
+                       "path": tg.PATHS.get(path, str(path)),
+                       "l2": "inputs larger than L2 (2 rotating A/B/C sets, 768 MB)",
+                       "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+            "clocks": clocks,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "gpu_launches": args.steps,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,160 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+The library must build, load, and export every function declared in
+include/tg_gemm.h.  Argument validation and path selection run entirely on
+the host before any CUDA call, so they are exercised here with fake device
+addresses (nothing is ever dereferenced or launched).
+"""
+import os
+import re
+
+import pytest
+
+import tiled_gemm_tg_gb300 as tg
+from tiled_gemm_tg_gb300 import build as tgbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tg_gemm.h")
+
+# fake, 256-byte aligned device addresses far apart from one another
+PA, PB, PC = 0x7F0000000000, 0x7F1000000000, 0x7F2000000000
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    tgbuild.build()
+    tg.lib()
+    yield
+    tg.tg_gemm_force_path(0)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(tg_[a-z_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for must in ["tg_gemm", "tg_gemm_check", "tg_status_string", "tg_gemm_path",
+                 "tg_gemm_force_path", "tg_gemm_version"]:
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported():
+    L = tg.lib()
+    for name in declared_functions():
+        assert hasattr(L, name), f"{name} declared in tg_gemm.h but not exported"
+
+
+def test_status_strings():
+    assert tg.tg_status_string(0) == "TG_OK"
+    assert tg.tg_status_string(1) == "TG_ERR_INVALID_ARG"
+    assert tg.tg_status_string(2) == "TG_ERR_UNSUPPORTED"
+    assert tg.tg_status_string(3) == "TG_ERR_CUDA"
+    assert tg.tg_status_string(4) == "TG_ERR_TIMEOUT"
+    assert tg.tg_status_string(99) == "TG_ERR_UNKNOWN"
+
+
+def test_version():
+    assert tg.tg_gemm_version() >= 100
+
+
+def call(M, N, K, A=PA, lda=None, B=PB, ldb=None, C=PC, ldc=None, i=tg.F16, o=tg.F16):
+    lda = K if lda is None else lda
+    ldb = N if ldb is None else ldb
+    ldc = N if ldc is None else ldc
+    return tg.tg_gemm(M, N, K, A, lda, B, ldb, C, ldc, i, o, 0)
+
+
+def path(M, N, K, A=PA, lda=None, B=PB, ldb=None, C=PC, ldc=None, i=tg.F16, o=tg.F16):
+    lda = K if lda is None else lda
+    ldb = N if ldb is None else ldb
+    ldc = N if ldc is None else ldc
+    return tg.tg_gemm_path(M, N, K, A, lda, B, ldb, C, ldc, i, o)
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(M=-1, N=4, K=4), tg.TG_ERR_INVALID_ARG),
+    (dict(M=4, N=-1, K=4), tg.TG_ERR_INVALID_ARG),
+    (dict(M=4, N=4, K=-1), tg.TG_ERR_INVALID_ARG),
+    (dict(M=4, N=4, K=4, C=0), tg.TG_ERR_INVALID_ARG),
+    (dict(M=4, N=4, K=4, A=0), tg.TG_ERR_INVALID_ARG),
+    (dict(M=4, N=4, K=4, B=0), tg.TG_ERR_INVALID_ARG),
+    (dict(M=4, N=4, K=8, lda=7), tg.TG_ERR_INVALID_ARG),
+    (dict(M=4, N=8, K=4, ldb=7), tg.TG_ERR_INVALID_ARG),
+    (dict(M=4, N=8, K=4, ldc=7), tg.TG_ERR_INVALID_ARG),
+    (dict(M=4, N=4, K=4, i=tg.F32, o=tg.F16), tg.TG_ERR_UNSUPPORTED),
+    (dict(M=4, N=4, K=4, i=3, o=3), tg.TG_ERR_UNSUPPORTED),
+    (dict(M=4, N=4, K=4, i=0, o=tg.F16), tg.TG_ERR_UNSUPPORTED),
+    (dict(M=2 ** 31, N=4, K=4), tg.TG_ERR_UNSUPPORTED),
+    (dict(M=4, N=4, K=2 ** 31), tg.TG_ERR_UNSUPPORTED),
+    # C overlapping A or B
+    (dict(M=64, N=64, K=64, C=PA + 64), tg.TG_ERR_INVALID_ARG),
+    (dict(M=64, N=64, K=64, C=PB - 100), tg.TG_ERR_INVALID_ARG),
+    # a span that would wrap past the end of the address space
+    (dict(M=2 ** 30, N=8, K=8, ldc=2 ** 40), tg.TG_ERR_INVALID_ARG),
+])
+def test_invalid_arguments_rejected_on_host(args, status):
+    assert call(**args) == status
+    assert path(**args) == 0
+
+
+def test_degenerate_sizes_are_noops():
+    # M == 0 or N == 0 returns before any CUDA call, even with NULL pointers
+    assert call(0, 5, 7, A=0, B=0, C=0) == tg.TG_OK
+    assert call(5, 0, 7, A=0, B=0, C=0) == tg.TG_OK
+    assert path(0, 5, 7) == 0
+    # K == 0 is the empty sum: C is zero-filled; A and B may be NULL
+    assert path(3, 5, 0, A=0, B=0) == 1
+
+
+def test_adjacent_operands_are_not_overlap():
+    # C starts exactly where A's span ends: legal
+    M, N, K = 4, 8, 8
+    end_a = PA + ((M - 1) * K + K) * 2
+    assert path(M, N, K, C=end_a) == 3
+
+
+def test_path_selection():
+    assert path(128, 128, 128, i=tg.F32, o=tg.F32) == 2
+    assert path(1024, 2048, 512) == 3
+    assert path(1024, 2048, 512, o=tg.F32) == 3
+    assert path(8192, 8192, 8192) == 3
+    # row stride not a multiple of 16 bytes -> boundary kernel
+    assert path(127, 255, 512) == 4
+    assert path(4, 4, 4) == 4
+    assert path(1, 255, 17) == 4
+    # base pointer not 16-byte aligned -> boundary kernel
+    assert path(128, 256, 512, A=PA + 2) == 4
+    assert path(128, 256, 512, B=PB + 8) == 4
+    # C alignment does not matter for the path (stores are predicated)
+    assert path(128, 256, 512, C=PC + 2) == 3
+
+
+def test_forced_paths():
+    try:
+        tg.tg_gemm_force_path(4)
+        assert path(1024, 2048, 512) == 4            # boundary can serve an aligned case
+        assert path(128, 128, 128, i=tg.F32, o=tg.F32) == 0  # but not fp32 inputs
+        tg.tg_gemm_force_path(3)
+        assert path(127, 255, 512) == 0              # main cannot serve misaligned operands
+        assert call(127, 255, 512) == tg.TG_ERR_UNSUPPORTED
+        tg.tg_gemm_force_path(2)
+        assert path(64, 64, 64) == 0                 # SIMT is fp32 only
+        assert path(3, 5, 0) == 1                    # K == 0 is never forced
+    finally:
+        tg.tg_gemm_force_path(0)
+    assert path(1024, 2048, 512) == 3
+
+
+def test_product_path_never_imports_oracle():
+    """The CUDA package must not import, load or call the CPU oracle."""
+    pkg = os.path.dirname(tg.__file__)
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                for needle in ("import oracle", "from oracle", "tg_oracle", "tgo_"):
+                    assert needle not in text, f"{f} mentions {needle}"

@@ -1,0 +1,296 @@
+"""GPU parity: every GEMM path, through the C ABI, against the CPU oracle.
+
+Acceptance per element (fp32 accumulation):
+    |C_gpu - C_ref| <= 2e-3 * S + 1e-5        (+ 1e-2 * |C_ref| for fp16 output)
+with S = sum_k |A_ik B_kj| from the oracle; the 1e-2 relative term is the
+fp16 threshold of §3.3 第四步 of the gsyq.cn/news/429607 article.  Where the
+inputs are small integers every partial sum is exact in fp32, the result is
+unique, and the GPU must match the oracle's round-to-nearest-even result
+bit for bit.
+
+The workloads are the five judged configurations (fp32 128^3, the fp16 edge
+set, the 1024x2048x512 tiling example, 8192^3, and the skinny/wide pair),
+followed by the verification flow of that article's §3.3: small cross-
+checks, unaligned sizes, seeded random stress with a 100% pass rate.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tiled_gemm_tg_gb300 as tg
+from tiled_gemm_tg_gb300 import inputs
+
+from gpu_util import check_full, compare, f16_bits_of, run
+
+pytestmark = pytest.mark.gpu
+
+MAIN, BOUNDARY, SIMT = 3, 4, 2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    tg.tg_gemm_force_path(0)
+    yield
+    tg.tg_gemm_force_path(0)
+
+
+def workload(name):
+    w = inputs.WORKLOADS[name]
+    a, b = inputs.operands(w)
+    out = torch.float16 if w.out_dtype == "f16" else torch.float32
+    return w, a, b, out
+
+
+# ---------------------------------------------------------- the five configs
+
+def test_config1_fp32_128_simt():
+    w, a, b, out = workload("f32_128x128x128")
+    got, C_ref, path = check_full(a, b, out)
+    assert path == SIMT
+    # the page's own fp32 criterion: max abs error below 1e-4 (TileLang实战 §3.2)
+    assert np.max(np.abs(got - C_ref)) < 1e-4
+
+
+@pytest.mark.parametrize("name", inputs.EDGE_SET)
+def test_config2_edge_set(name):
+    w, a, b, out = workload(name)
+    _, _, path = check_full(a, b, out)
+    # 4x4, 127x255 and 1x255x17 have row strides that are not multiples of
+    # 16 bytes; 128x256x512 is TMA-addressable
+    assert path == (MAIN if name == "edge_128x256x512" else BOUNDARY)
+
+
+def test_config3_tiling_example():
+    w, a, b, out = workload("tile_1024x2048x512")
+    _, _, path = check_full(a, b, out)
+    assert path == MAIN
+
+
+def _sampled_check(a, b, got, out_f16, seed, extra_rows=(), extra_cols=()):
+    M, K = a.shape
+    N = b.shape[1]
+    rng = np.random.default_rng(seed)
+    rows = [rng.integers(0, M, 4096)]
+    cols = [rng.integers(0, N, 4096)]
+    for r in extra_rows:
+        rows.append(np.full(N, r))
+        cols.append(np.arange(N))
+    for c in extra_cols:
+        rows.append(np.arange(M))
+        cols.append(np.full(M, c))
+    rows = np.concatenate(rows)
+    cols = np.concatenate(cols)
+    C_ref, S = oracle.gemm_at(a.numpy(), b.numpy(), rows, cols)
+    compare(got[rows, cols], C_ref, S, out_f16, f"sampled {M}x{N}x{K}")
+
+
+def _matvec_property(a, b, got, out_f16):
+    """At every row: |C x - A (B x)| <= sum_j tol_ij |x_j|, with the per-element
+    tolerance bounded through S <= |A| |B| (fp64 NumPy mat-vecs)."""
+    A = a.numpy().astype(np.float64)
+    B = b.numpy().astype(np.float64)
+    x = np.random.default_rng(5).standard_normal(B.shape[1])
+    lhs = got @ x
+    rhs = A @ (B @ x)
+    rel = 2e-3 + (1e-2 if out_f16 else 0.0)
+    bound = rel * (np.abs(A) @ (np.abs(B) @ np.abs(x))) + 1e-5 * np.abs(x).sum()
+    assert np.all(np.abs(lhs - rhs) <= bound)
+
+
+def test_config4_square_8192():
+    w, a, b, out = workload("square_8192")
+    got, intact, path = run(a, b, out)
+    assert path == MAIN and intact
+    assert np.isfinite(got).all(), "an output element was never written"
+    _sampled_check(a, b, got, True, 41, extra_rows=(0, 4095, 8191), extra_cols=(0, 4097, 8191))
+    _matvec_property(a, b, got, True)
+
+
+def test_config5_skinny_full():
+    w, a, b, out = workload("skinny_16x4096x4096")
+    check_full(a, b, out)
+
+
+def test_config5_wide_sampled():
+    w, a, b, out = workload("wide_4096x16384x4096")
+    got, intact, path = run(a, b, out)
+    assert path == MAIN and intact
+    assert np.isfinite(got).all()
+    _sampled_check(a, b, got, True, 51, extra_rows=(0, 4095), extra_cols=(0, 16383))
+    _matvec_property(a, b, got, True)
+
+
+# ---------------------------------------------- exact (integer-valued) results
+
+@pytest.mark.parametrize("M,N,K,ld_pad,off,out,path", [
+    (300, 520, 1000, (0, 0, 0), (0, 0, 0), torch.float16, MAIN),
+    (300, 520, 1000, (8, 24, 3), (8, 16, 1), torch.float32, MAIN),
+    (129, 257, 130, (0, 0, 0), (0, 0, 0), torch.float16, MAIN),
+    (127, 255, 512, (0, 0, 0), (0, 0, 0), torch.float16, BOUNDARY),
+    (200, 100, 333, (1, 3, 5), (1, 3, 7), torch.float32, BOUNDARY),
+    (100, 90, 300, (2, 1, 0), (0, 0, 0), torch.float16, BOUNDARY),
+])
+def test_integer_inputs_bitwise(M, N, K, ld_pad, off, out, path):
+    a = inputs.draw((M, K), "int2", 7001 + M, "f16")
+    b = inputs.draw((K, N), "int2", 7002 + N, "f16")
+    got, intact, p = run(a, b, out, lda=K + ld_pad[0], ldb=N + ld_pad[1], ldc=N + ld_pad[2],
+                         offs=off)
+    assert p == path and intact
+    C_ref, _ = oracle.gemm(a.numpy(), b.numpy())
+    if out == torch.float16:
+        want = f16_bits_of(C_ref)
+        have = torch.from_numpy(got).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(have, want)
+    else:
+        assert np.array_equal(got, C_ref)
+
+
+def test_fp32_integer_inputs_exact():
+    a = inputs.draw((77, 130), "int2", 7101, "f32")
+    b = inputs.draw((130, 45), "int2", 7102, "f32")
+    got, intact, p = run(a, b, torch.float32)
+    assert p == SIMT and intact
+    C_ref, _ = oracle.gemm(a.numpy(), b.numpy())
+    assert np.array_equal(got, C_ref)
+
+
+# ------------------------------------------------------- closed forms on GPU
+
+@pytest.mark.parametrize("force", [0, BOUNDARY])
+def test_identity_gives_a(force):
+    a = inputs.draw((256, 192), "normal", 7201, "f16")
+    eye = torch.eye(192, dtype=torch.float16)
+    tg.tg_gemm_force_path(force)
+    try:
+        got, intact, p = run(a, eye, torch.float16)
+    finally:
+        tg.tg_gemm_force_path(0)
+    assert intact and p == (force or MAIN)
+    assert np.array_equal(got, a.double().numpy())
+
+
+@pytest.mark.parametrize("K", [8, 64, 2048, 8192])
+def test_all_ones_gives_k(K):
+    a = torch.ones((130, K), dtype=torch.float16)
+    b = torch.ones((K, 136), dtype=torch.float16)
+    got, intact, _ = run(a, b, torch.float16)
+    assert intact and np.all(got == K)
+
+
+def test_transpose_invariant():
+    """(A B)^T = B^T A^T, the transposed product run through tg_gemm itself."""
+    a = inputs.draw((192, 320), "int2", 7301, "f16")
+    b = inputs.draw((320, 136), "int2", 7302, "f16")
+    c1, _, _ = run(a, b, torch.float32)
+    c2, _, _ = run(b.t().contiguous(), a.t().contiguous(), torch.float32)
+    assert np.array_equal(c1, c2.T)
+
+
+def test_8x8_ones_page_example():
+    a = torch.ones((8, 8), dtype=torch.float16)
+    got, intact, p = run(a, a, torch.float16)
+    assert intact and p == MAIN and np.all(got == 8)
+
+
+# ----------------------------------------------------------- degenerate sizes
+
+def test_k_zero_writes_zeros():
+    got, intact, _ = run(torch.zeros((5, 0), dtype=torch.float16),
+                         torch.zeros((0, 7), dtype=torch.float16), torch.float16, ldc=9)
+    assert intact and np.all(got == 0)
+
+
+def test_m_or_n_zero_is_noop():
+    dev = torch.device("cuda")
+    c = torch.full((4,), 3.0, dtype=torch.float16, device=dev)
+    s = torch.cuda.current_stream().cuda_stream
+    assert tg.tg_gemm(0, 4, 4, 0, 4, 0, 4, c.data_ptr(), 4, tg.F16, tg.F16, s) == tg.TG_OK
+    assert tg.tg_gemm(4, 0, 4, 0, 4, 0, 4, c.data_ptr(), 4, tg.F16, tg.F16, s) == tg.TG_OK
+    assert tg.tg_gemm_check(s) == tg.TG_OK
+    assert torch.all(c == 3.0)
+
+
+def test_invalid_args_leave_c_untouched():
+    dev = torch.device("cuda")
+    a = torch.ones((8, 8), dtype=torch.float16, device=dev)
+    c = torch.full((8, 8), 5.0, dtype=torch.float16, device=dev)
+    s = torch.cuda.current_stream().cuda_stream
+    st = tg.tg_gemm(8, 8, 8, a.data_ptr(), 7, a.data_ptr(), 8, c.data_ptr(), 8, tg.F16, tg.F16, s)
+    assert st == tg.TG_ERR_INVALID_ARG
+    st = tg.tg_gemm(8, 8, 8, a.data_ptr(), 8, a.data_ptr(), 8, a.data_ptr(), 8, tg.F16, tg.F16, s)
+    assert st == tg.TG_ERR_INVALID_ARG  # C aliases A
+    assert tg.tg_gemm_check(s) == tg.TG_OK
+    assert torch.all(c == 5.0)
+
+
+# ----------------------------------------------- leading dims, offsets, tails
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (1, 8, 8), (8, 1, 8), (128, 128, 64),
+                                   (129, 129, 65), (255, 257, 513), (64, 512, 1024),
+                                   (513, 136, 8), (17, 4096, 256)])
+@pytest.mark.parametrize("out", [torch.float16, torch.float32])
+def test_shapes_main_and_tails(M, N, K, out):
+    a = inputs.draw((M, K), "normal", 7400 + M, "f16")
+    b = inputs.draw((K, N), "normal", 7500 + N, "f16")
+    pad = lambda x: (x + 7) // 8 * 8  # noqa: E731  keep TMA-legal strides
+    check_full(a, b, out, lda=pad(K), ldb=pad(N), ldc=N + 3)
+
+
+@pytest.mark.parametrize("force", [MAIN, BOUNDARY])
+def test_same_problem_both_tensor_core_paths(force):
+    a = inputs.draw((333, 456), "normal", 7601, "f16")
+    b = inputs.draw((456, 520), "normal", 7602, "f16")
+    tg.tg_gemm_force_path(force)
+    try:
+        _, _, p = check_full(a, b, torch.float16)
+    finally:
+        tg.tg_gemm_force_path(0)
+    assert p == force
+
+
+def test_stream_argument_is_honoured():
+    s = torch.cuda.Stream()
+    a = inputs.draw((640, 384), "normal", 7701, "f16")
+    b = inputs.draw((384, 768), "normal", 7702, "f16")
+    with torch.cuda.stream(s):
+        check_full(a, b, torch.float16, stream=s)
+
+
+# ------------------------------------------------------- seeded random stress
+
+def test_random_stress_pass_rate():
+    """Hundreds of seeded random problems over every path, with random row
+    strides and base offsets; every one must pass (100% pass rate)."""
+    rng = np.random.default_rng(2024)
+    failures = []
+    for t in range(240):
+        M = int(rng.integers(1, 301))
+        N = int(rng.integers(1, 301))
+        K = int(rng.integers(1, 601))
+        fp32 = t % 8 == 7
+        dt = "f32" if fp32 else "f16"
+        out = torch.float32 if (fp32 or t % 3 == 0) else torch.float16
+        aligned = rng.random() < 0.5
+        if aligned and not fp32:
+            lda = (K + 7) // 8 * 8 + 8 * int(rng.integers(0, 3))
+            ldb = (N + 7) // 8 * 8 + 8 * int(rng.integers(0, 3))
+            offs = (8 * int(rng.integers(0, 4)), 8 * int(rng.integers(0, 4)),
+                    int(rng.integers(0, 9)))
+        else:
+            lda = K + int(rng.integers(0, 5))
+            ldb = N + int(rng.integers(0, 5))
+            offs = tuple(int(v) for v in rng.integers(0, 9, 3))
+        ldc = N + int(rng.integers(0, 5))
+        a = inputs.draw((M, K), "normal", 80000 + 2 * t, dt)
+        b = inputs.draw((K, N), "normal", 80001 + 2 * t, dt)
+        try:
+            check_full(a, b, out, lda=lda, ldb=ldb, ldc=ldc, offs=offs)
+        except AssertionError as e:
+            failures.append((t, M, N, K, lda, ldb, ldc, offs, str(e)[:200]))
+    assert not failures, f"{len(failures)}/240 failed: {failures[:5]}"

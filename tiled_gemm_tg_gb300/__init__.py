@@ -1,0 +1,155 @@
+"""tiled_gemm_tg_gb300 -- thin Python binding over libtg_gemm.so.
+
+The library computes C[M,N] = A[M,K] x B[K,N] (row-major; fp16 or fp32
+inputs, fp32 accumulation, fp16 or fp32 output) with hand-written CUDA
+kernels for sm_103a.  This module only marshals arguments: the entry points
+carry the names of the C ABI in include/tg_gemm.h, and ``gemm`` is a
+convenience that takes torch tensors, allocates the output with torch and
+calls ``tg_gemm``.  There is no fallback: if the compiled library is missing
+every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "F16", "F32", "TG_OK", "TG_ERR_INVALID_ARG", "TG_ERR_UNSUPPORTED", "TG_ERR_CUDA",
+    "TG_ERR_TIMEOUT", "PATHS", "TgError", "lib", "library_path", "tg_gemm", "tg_gemm_check",
+    "tg_status_string", "tg_gemm_path", "tg_gemm_force_path", "tg_gemm_version", "gemm",
+    "check",
+]
+
+F16 = 1
+F32 = 2
+TG_OK = 0
+TG_ERR_INVALID_ARG = 1
+TG_ERR_UNSUPPORTED = 2
+TG_ERR_CUDA = 3
+TG_ERR_TIMEOUT = 4
+PATHS = {0: "none", 1: "zero", 2: "simt_f32", 3: "tc_main", 4: "tc_boundary", 5: "tc_skinny"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libtg_gemm.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class TgError(RuntimeError):
+    def __init__(self, status: int, what: str = "tg_gemm"):
+        self.status = status
+        super().__init__(f"{what} failed: {tg_status_string(status)} ({status})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libtg_gemm.so; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(_LIB_PATH)
+        i64, vp, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+        L.tg_gemm.restype = i32
+        L.tg_gemm.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, i32, vp]
+        L.tg_gemm_check.restype = i32
+        L.tg_gemm_check.argtypes = [vp]
+        L.tg_status_string.restype = ctypes.c_char_p
+        L.tg_status_string.argtypes = [i32]
+        L.tg_gemm_path.restype = i32
+        L.tg_gemm_path.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, i32]
+        L.tg_gemm_force_path.restype = None
+        L.tg_gemm_force_path.argtypes = [i32]
+        L.tg_gemm_version.restype = i32
+        L.tg_gemm_version.argtypes = []
+        _lib = L
+        return L
+
+
+# ------------------------------------------------------------ raw C entry points
+
+def tg_gemm(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, stream=0) -> int:
+    """Enqueue C = A x B on `stream`; pointers are integers (device addresses)."""
+    return int(lib().tg_gemm(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, stream))
+
+
+def tg_gemm_check(stream=0) -> int:
+    """Synchronize `stream` and read/clear the device error word."""
+    return int(lib().tg_gemm_check(stream))
+
+
+def tg_status_string(status: int) -> str:
+    return lib().tg_status_string(int(status)).decode()
+
+
+def tg_gemm_path(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype) -> int:
+    return int(lib().tg_gemm_path(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype))
+
+
+def tg_gemm_force_path(path: int) -> None:
+    lib().tg_gemm_force_path(int(path))
+
+
+def tg_gemm_version() -> int:
+    return int(lib().tg_gemm_version())
+
+
+# ------------------------------------------------------------- torch marshalling
+
+def _code(dtype) -> int:
+    import torch
+    if dtype == torch.float16:
+        return F16
+    if dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {dtype}")
+
+
+def _ld(t) -> int:
+    if t.dim() != 2:
+        raise ValueError("operands must be 2-D")
+    if t.size(1) > 1 and t.stride(1) != 1:
+        raise ValueError("rows must be contiguous (row-major)")
+    return int(t.stride(0)) if t.size(0) > 1 else max(int(t.size(1)), 1)
+
+
+def _stream_handle(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def gemm(a, b, out=None, out_dtype=None, stream=None):
+    """C = A x B for 2-D CUDA tensors (row-major rows; row strides may exceed
+    the row length).  Allocates C with torch unless `out` is given."""
+    import torch
+    if not (a.is_cuda and b.is_cuda):
+        raise ValueError("operands must be CUDA tensors")
+    M, K = a.shape
+    K2, N = b.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    if out is None:
+        od = out_dtype if out_dtype is not None else a.dtype
+        out = torch.empty((M, N), dtype=od, device=a.device)
+    st = tg_gemm(M, N, K, a.data_ptr(), _ld(a), b.data_ptr(), _ld(b), out.data_ptr(), _ld(out),
+                 _code(a.dtype), _code(out.dtype), _stream_handle(stream))
+    if st != TG_OK:
+        raise TgError(st)
+    return out
+
+
+def check(stream=None) -> None:
+    """Raise TgError if a kernel on `stream` abandoned a bounded wait."""
+    st = tg_gemm_check(_stream_handle(stream))
+    if st != TG_OK:
+        raise TgError(st, "tg_gemm_check")

@@ -1,0 +1,378 @@
+// gemm_tc.cu -- the main fp16 GEMM kernel for sm_103a: C = A x B with fp32
+// accumulation in tensor memory.
+//
+// What the pages describe ("企业官网建设流程全解析" (cf-1.com), §2.3 and §3.3):
+// a 2-D grid of 128x128 output tiles, A and B tiles staged in shared memory,
+// an fp32 accumulator cleared once per tile, the K loop software-pipelined
+// over num_stages buffers (copy A, copy B, gemm), a swizzled shared-memory
+// layout against bank conflicts (§4.1), and warp specialisation with a
+// TMA producer feeding compute warps through mbarriers (§2.3).
+//
+// How it is built here for GB300:
+//   * persistent grid of one CTA per SM walking a grouped tile order, so a
+//     wave of tiles shares A rows and B columns in L2 (the "block_wise"
+//     mapping of "TileLang：GPU异构计算的声明式分块编程范式" (kwkr.cn), §3.3);
+//   * tiles of 128 x BN (BN = 256, 128 or 64), k-blocks of 64 fp16, so one
+//     A row of a k-block is exactly one 128-byte swizzle atom;
+//   * warp 0: TMA producer.  A is loaded K-major ([128 rows][64 k]), B is
+//     loaded MN-major in BN/64 boxes of [64 k rows][64 n], all with the
+//     128-byte swizzle, into a ring of STAGES full/empty mbarrier pairs;
+//   * warp 1: allocates tensor memory and issues tcgen05.mma (M=128,
+//     N=BN, K=16, four per k-block) from one thread, accumulating in a
+//     double-buffered TMEM accumulator (2 x BN fp32 columns);
+//   * warps 2..5: epilogue.  Each thread owns one output row: tcgen05.ld
+//     of 32 columns at a time, fp32 -> fp16 round-to-nearest-even (or fp32
+//     as is), 16-byte vector stores, predicated at the M/N edges.  The
+//     epilogue of tile i overlaps the main loop of tile i+1.
+// Out-of-range rows, columns and k are zero-filled by TMA, so any M, N, K
+// works as long as the operands are TMA-addressable (16-byte aligned bases,
+// row strides a multiple of 16 bytes); the host routes everything else to
+// the boundary kernel.
+//
+// Every mbarrier wait is bounded.  A role that gives up records a bit in the
+// device error word and raises a shared abort flag; the other roles then
+// give up too, the producer waits (bounded) for its own TMA copies in
+// flight, the MMA thread waits for its own MMAs, and tensor memory is freed
+// before the CTA exits.
+#include <cstdint>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+#include "tg_internal.h"
+
+namespace tg {
+namespace {
+
+using namespace tg::dev;
+
+constexpr int BM = 128;
+constexpr int BK = 64;                 // fp16: 128 bytes per row = one swizzle atom
+constexpr uint32_t A_STAGE = BM * BK * 2;
+constexpr uint32_t B_BOX = 64 * BK * 2; // one [64 k][64 n] box, 8 KB
+constexpr int kThreads = 192;
+
+template <int BN>
+struct MainCfg {
+    static constexpr uint32_t B_STAGE = BN * BK * 2;
+    static constexpr uint32_t STAGE = A_STAGE + B_STAGE;
+    static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+    static constexpr uint32_t TMEM_COLS = 2 * BN;
+    static constexpr uint32_t SMEM = STAGES * STAGE + 1024;  // + alignment slack
+    static_assert(SMEM <= 227 * 1024, "shared-memory budget exceeded");
+    static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
+                  "TMEM allocation must be a power of two in [32, 512]");
+};
+
+// Grouped tile order: tiles are visited in groups of `group_m` tile-rows,
+// column by column inside a group.
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int group_m,
+                                            int& tm, int& tn)
+{
+    const int span = group_m * tiles_n;
+    const int g = t / span;
+    const int first = g * group_m;
+    const int gs = min(tiles_m - first, group_m);
+    const int r = t - g * span;
+    tm = first + r % gs;
+    tn = r / gs;
+}
+
+template <bool OUT_F32>
+__device__ __forceinline__ void store_chunk(void* C, long long ldc, int m, int n, int N,
+                                            const uint32_t (&r)[32], bool vec)
+{
+    if constexpr (OUT_F32) {
+        float* row = static_cast<float*>(C) + static_cast<long long>(m) * ldc + n;
+        if (vec && n + 32 <= N) {
+            float4* d = reinterpret_cast<float4*>(row);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                d[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                   __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (n + j < N) row[j] = __uint_as_float(r[j]);
+        }
+    } else {
+        __half* row = static_cast<__half*>(C) + static_cast<long long>(m) * ldc + n;
+        if (vec && n + 32 <= N) {
+            uint32_t p[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                __half2 h = __floats2half2_rn(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                p[i] = *reinterpret_cast<uint32_t*>(&h);
+            }
+            uint4* d = reinterpret_cast<uint4*>(row);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (n + j < N) row[j] = __float2half_rn(__uint_as_float(r[j]));
+        }
+    }
+}
+
+template <int BN, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    void* __restrict__ C, long long ldc, int M, int N, int K, int tiles_m,
+                    int tiles_n, int group_m, int c_vec, unsigned int* err)
+{
+    using Cfg = MainCfg<BN>;
+    constexpr int STAGES = Cfg::STAGES;
+
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[STAGES];
+    __shared__ __align__(8) uint64_t empty_bar[STAGES];
+    __shared__ __align__(8) uint64_t tfull_bar[2];
+    __shared__ __align__(8) uint64_t tempty_bar[2];
+    __shared__ __align__(8) uint64_t drain_bar;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&tfull_bar[a]), 1);
+            mbar_init(smem_u32(&tempty_bar[a]), 128);
+        }
+        mbar_init(smem_u32(&drain_bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&tmem_slot), Cfg::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = tmem_slot;
+
+    const int num_kb = (K + BK - 1) / BK;
+    const int total = tiles_m * tiles_n;
+    // The epilogue waits for a whole tile's main loop; allow ~64 us per k-block
+    // on top of the base limit so long-K problems never time out spuriously.
+    const uint32_t epi_limit = kSlowPolls + 64u * static_cast<uint32_t>(min(num_kb, 1 << 20));
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t issued = 0;
+            for (int t = blockIdx.x; t < total; t += gridDim.x) {
+                int tm, tn;
+                tile_coords(t, tiles_m, tiles_n, group_m, tm, tn);
+                bool ok = true;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1u, &abort_flag)) {
+                        abort_flag = 1;
+                        atomicOr(err, ERR_MAIN_PRODUCER);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&full_bar[s]);
+                    const uint32_t sa = base + s * Cfg::STAGE;
+                    mbar_arrive_expect_tx(fb, Cfg::STAGE);
+                    tma_load_2d(sa, &tmA, fb, kb * BK, tm * BM);
+#pragma unroll
+                    for (int j = 0; j < BN / 64; ++j)
+                        tma_load_2d(sa + A_STAGE + j * B_BOX, &tmB, fb, tn * BN + j * 64, kb * BK);
+                    ++issued;
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+            }
+            // Wait for this thread's own copies still in flight: the most
+            // recent arming of each of the last min(issued, STAGES) stages.
+            int ds = s;
+            uint32_t dph = ph;
+            const uint32_t n_drain = issued < (uint32_t)STAGES ? issued : (uint32_t)STAGES;
+            for (uint32_t i = 0; i < n_drain; ++i) {
+                if (--ds < 0) {
+                    ds = STAGES - 1;
+                    dph ^= 1u;
+                }
+                if (!mbar_wait(smem_u32(&full_bar[ds]), dph, nullptr)) atomicOr(err, ERR_DRAIN);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ----------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16_f32(BM, BN, false, true);
+            int s = 0;
+            uint32_t ph = 0;
+            int acc = 0;
+            uint32_t aph = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                if (!mbar_wait(smem_u32(&tempty_bar[acc]), aph ^ 1u, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(smem_u32(&full_bar[s]), ph, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = base + s * Cfg::STAGE;
+                    // A: K-major, 8-row groups 1024 B apart.  B: MN-major,
+                    // 64-column boxes BK*128 B apart, 8-row k groups 1024 B apart.
+                    const uint64_t ad = sdesc_sw128(sa, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(sa + A_STAGE, BK * 128, 1024);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        umma_f16(d, ad + 2ull * k, bd + 128ull * k, idesc, (kb | k) != 0 ? 1u : 0u);
+                    umma_commit(smem_u32(&empty_bar[s]));
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(smem_u32(&tfull_bar[acc]));
+                acc ^= 1;
+                if (acc == 0) aph ^= 1u;
+            }
+            if (!ok) {
+                abort_flag = 1;
+                atomicOr(err, ERR_MAIN_MMA);
+            }
+            // Every MMA this thread issued must finish before TMEM is freed.
+            umma_commit(smem_u32(&drain_bar));
+            if (!mbar_wait(smem_u32(&drain_bar), 0, nullptr)) atomicOr(err, ERR_DRAIN);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------- epilogue
+        const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            int tm, tn;
+            tile_coords(t, tiles_m, tiles_n, group_m, tm, tn);
+            const bool got = mbar_wait(smem_u32(&tfull_bar[acc]), aph, &abort_flag, epi_limit);
+            if (!__all_sync(0xffffffffu, got)) {
+                if (lane == 0) {
+                    abort_flag = 1;
+                    atomicOr(err, ERR_MAIN_EPILOGUE);
+                }
+                break;
+            }
+            tc_fence_after();
+            const int m = tm * BM + q * 32 + lane;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(taddr + c, r);
+                tmem_ld_wait();
+                const int n = tn * BN + c;
+                if (m < M && n < N) store_chunk<OUT_F32>(C, ldc, m, n, N, r, c_vec != 0);
+            }
+            tc_fence_before();
+            mbar_arrive(smem_u32(&tempty_bar[acc]));
+            acc ^= 1;
+            if (acc == 0) aph ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+std::mutex g_attr_mu;
+bool g_attr_set[64][6];
+
+template <int BN, bool OUT_F32>
+cudaError_t launch_cfg(const GemmArgs& a)
+{
+    using Cfg = MainCfg<BN>;
+    auto kernel = gemm_tc_main_kernel<BN, OUT_F32>;
+    {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        const int slot = (BN == 256 ? 0 : BN == 128 ? 1 : 2) * 2 + (OUT_F32 ? 1 : 0);
+        std::lock_guard<std::mutex> lock(g_attr_mu);
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        if (!g_attr_set[dev][slot]) {
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(Cfg::SMEM));
+            if (e != cudaSuccess) return e;
+            g_attr_set[dev][slot] = true;
+        }
+    }
+    CUtensorMap ta, tb;
+    if (!encode_tmap_f16(&ta, a.A, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M),
+                         static_cast<uint64_t>(a.lda), BK, BM))
+        return cudaErrorInvalidValue;
+    if (!encode_tmap_f16(&tb, a.B, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
+                         static_cast<uint64_t>(a.ldb), 64, BK))
+        return cudaErrorInvalidValue;
+    const int tiles_m = (a.M + BM - 1) / BM;
+    const int tiles_n = (a.N + BN - 1) / BN;
+    const int total = tiles_m * tiles_n;
+    const int grid = total < a.num_sms ? total : a.num_sms;
+    const int group_m = 16;
+    const size_t es = OUT_F32 ? 4 : 2;
+    const int c_vec = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) &&
+                      ((static_cast<size_t>(a.ldc) * es) % 16 == 0);
+    kernel<<<grid, kThreads, Cfg::SMEM, a.stream>>>(ta, tb, a.C, a.ldc, a.M, a.N, a.K, tiles_m,
+                                                     tiles_n, group_m, c_vec, a.err);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int main_tile_n(int M, int N, int num_sms)
+{
+    const long long tm = (M + BM - 1) / BM;
+    if (tm * ((N + 255) / 256) >= num_sms) return 256;
+    if (tm * ((N + 127) / 128) >= num_sms / 2) return 128;
+    return 64;
+}
+
+cudaError_t launch_main(const GemmArgs& a, int bn)
+{
+    if (a.out_f32) {
+        if (bn == 256) return launch_cfg<256, true>(a);
+        if (bn == 128) return launch_cfg<128, true>(a);
+        return launch_cfg<64, true>(a);
+    }
+    if (bn == 256) return launch_cfg<256, false>(a);
+    if (bn == 128) return launch_cfg<128, false>(a);
+    return launch_cfg<64, false>(a);
+}
+
+}  // namespace tg

@@ -1,0 +1,221 @@
+// gemm_tc_boundary.cu -- fp16 GEMM on the tensor cores for operands the TMA
+// engine cannot address: a base pointer that is not 16-byte aligned or a row
+// stride that is not a multiple of 16 bytes (e.g. B of the M=127, N=255 case
+// has a 510-byte row stride; a 4x4 fp16 matrix has an 8-byte one).
+//
+// The pages require such unaligned shapes to work without reading out of
+// bounds or writing garbage (gsyq.cn/news/429607, §3.3 第三步 and §5.2); the
+// tile masking is what they call for.  Here every global load is predicated
+// and zero-filled, written by the threads themselves into the same 128-byte
+// swizzled shared-memory layout the TMA path produces, and fed to the same
+// tcgen05.mma (M=128, N=BN, K=16) with an fp32 accumulator in tensor memory.
+// Two shared-memory stages let the loads of k-block i+1 overlap the MMAs of
+// k-block i.  One CTA per 128 x BN output tile; 4 warps; stores predicated.
+#include <cstdint>
+#include <mutex>
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+#include "tg_internal.h"
+
+namespace tg {
+namespace {
+
+using namespace tg::dev;
+
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int BK = 64;
+constexpr uint32_t A_STAGE = BM * BK * 2;   // 16 KB
+constexpr uint32_t B_STAGE = BN * BK * 2;   // 16 KB: two [64 k][64 n] atoms-columns
+constexpr uint32_t STAGE = A_STAGE + B_STAGE;
+constexpr uint32_t SMEM = 2 * STAGE + 1024;
+constexpr uint32_t TMEM_COLS = BN;
+constexpr int kThreads = 128;
+
+// 8 consecutive fp16 elements starting at p, with columns at or past `limit`
+// (relative index) read as zero.  Uses one 16-byte load when it can.
+__device__ __forceinline__ uint4 load8(const __half* p, int valid)
+{
+    if (valid >= 8 && (reinterpret_cast<uintptr_t>(p) & 15u) == 0)
+        return __ldg(reinterpret_cast<const uint4*>(p));
+    const unsigned short* q = reinterpret_cast<const unsigned short*>(p);
+    uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t v = (i < valid) ? static_cast<uint32_t>(__ldg(q + i)) : 0u;
+        w[i >> 1] |= v << ((i & 1) * 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <bool OUT_F32>
+__global__ void __launch_bounds__(kThreads)
+gemm_tc_boundary_kernel(const __half* __restrict__ A, long long lda, const __half* __restrict__ B,
+                        long long ldb, void* __restrict__ C, long long ldc, int M, int N, int K,
+                        unsigned int* err)
+{
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t mma_bar[2];
+    __shared__ __align__(8) uint64_t drain_bar;
+    __shared__ uint32_t tmem_slot;
+
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    uint8_t* const gbase = smem_raw + (base - smem_u32(smem_raw));
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int m0 = blockIdx.y * BM;
+    const int n0 = blockIdx.x * BN;
+
+    if (tid == 0) {
+        mbar_init(smem_u32(&mma_bar[0]), 1);
+        mbar_init(smem_u32(&mma_bar[1]), 1);
+        mbar_init(smem_u32(&drain_bar), 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(&tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = tmem_slot;
+
+    constexpr uint32_t idesc = idesc_f16_f32(BM, BN, false, true);
+    const int num_kb = (K + BK - 1) / BK;
+    bool aborted = false;
+
+    for (int kb = 0; kb < num_kb; ++kb) {
+        const int s = kb & 1;
+        if (kb >= 2) {
+            // The MMAs issued two k-blocks ago read stage s; wait until done.
+            const bool got = mbar_wait(smem_u32(&mma_bar[s]), ((kb - 2) >> 1) & 1, nullptr);
+            if (__syncthreads_or(got ? 0 : 1)) {
+                aborted = true;
+                break;
+            }
+        }
+        uint8_t* sA = gbase + s * STAGE;
+        uint8_t* sB = sA + A_STAGE;
+        const int k0 = kb * BK;
+        // A tile: 128 rows x 8 chunks of 8 k; chunk (r, c) goes to row r of the
+        // K-major atom column, 16-byte slot c ^ (r % 8).
+#pragma unroll 2
+        for (int i = tid; i < BM * (BK / 8); i += kThreads) {
+            const int r = i >> 3, c = i & 7;
+            const int m = m0 + r, k = k0 + c * 8;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (m < M && k < K) v = load8(A + static_cast<long long>(m) * lda + k, K - k);
+            *reinterpret_cast<uint4*>(sA + r * 128 + ((c ^ (r & 7)) << 4)) = v;
+        }
+        // B tile: 64 k-rows x (BN/8) chunks of 8 n; 64-column box j = c / 8 sits
+        // at j * 8 KB, row kr at kr * 128 B, 16-byte slot (c % 8) ^ (kr % 8).
+#pragma unroll 2
+        for (int i = tid; i < BK * (BN / 8); i += kThreads) {
+            const int kr = i / (BN / 8), c = i % (BN / 8);
+            const int k = k0 + kr, n = n0 + c * 8;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (k < K && n < N) v = load8(B + static_cast<long long>(k) * ldb + n, N - n);
+            *reinterpret_cast<uint4*>(sB + (c >> 3) * (64 * 128) + kr * 128 +
+                                      (((c & 7) ^ (kr & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t sa = base + s * STAGE;
+            const uint64_t ad = sdesc_sw128(sa, 16, 1024);
+            const uint64_t bd = sdesc_sw128(sa + A_STAGE, BK * 128, 1024);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)
+                umma_f16(tmem_base, ad + 2ull * k, bd + 128ull * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            umma_commit(smem_u32(&mma_bar[s]));
+        }
+    }
+
+    if (!aborted) {
+        const int last = num_kb - 1;
+        const bool got = mbar_wait(smem_u32(&mma_bar[last & 1]), (last >> 1) & 1, nullptr);
+        if (__syncthreads_or(got ? 0 : 1)) aborted = true;
+    }
+    if (!aborted) {
+        tc_fence_after();
+        const int m = m0 + warp * 32 + lane;
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16);
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + c, r);
+            tmem_ld_wait();
+            const int n = n0 + c;
+            if (m < M && n < N) {
+                if constexpr (OUT_F32) {
+                    float* row = static_cast<float*>(C) + static_cast<long long>(m) * ldc + n;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (n + j < N) row[j] = __uint_as_float(r[j]);
+                } else {
+                    __half* row = static_cast<__half*>(C) + static_cast<long long>(m) * ldc + n;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (n + j < N) row[j] = __float2half_rn(__uint_as_float(r[j]));
+                }
+            }
+        }
+    } else if (tid == 0) {
+        atomicOr(err, ERR_BOUNDARY);
+    }
+
+    if (tid == 0) {
+        // Every MMA this CTA issued must finish before TMEM is freed.
+        umma_commit(smem_u32(&drain_bar));
+        if (!mbar_wait(smem_u32(&drain_bar), 0, nullptr)) atomicOr(err, ERR_DRAIN);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+std::mutex g_attr_mu;
+bool g_attr_set[64][2];
+
+template <bool OUT_F32>
+cudaError_t launch_cfg(const GemmArgs& a)
+{
+    auto kernel = gemm_tc_boundary_kernel<OUT_F32>;
+    {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        std::lock_guard<std::mutex> lock(g_attr_mu);
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        if (!g_attr_set[dev][OUT_F32 ? 1 : 0]) {
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(SMEM));
+            if (e != cudaSuccess) return e;
+            g_attr_set[dev][OUT_F32 ? 1 : 0] = true;
+        }
+    }
+    const dim3 grid((a.N + BN - 1) / BN, (a.M + BM - 1) / BM);
+    if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
+    kernel<<<grid, kThreads, SMEM, a.stream>>>(
+        static_cast<const __half*>(a.A), a.lda, static_cast<const __half*>(a.B), a.ldb, a.C, a.ldc,
+        a.M, a.N, a.K, a.err);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_boundary(const GemmArgs& a)
+{
+    return a.out_f32 ? launch_cfg<true>(a) : launch_cfg<false>(a);
+}
+
+}  // namespace tg

@@ -1,0 +1,58 @@
+// tg_internal.h -- host-side interface between the C-ABI dispatcher and the
+// kernel launchers.  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace tg {
+
+enum Path : int {
+    PATH_NONE = 0,
+    PATH_ZERO = 1,      // K == 0: C is the empty sum
+    PATH_SIMT = 2,      // fp32 register-blocked SIMT kernel
+    PATH_MAIN = 3,      // TMA + tcgen05 warp-specialised persistent kernel
+    PATH_BOUNDARY = 4,  // tcgen05 kernel with predicated (non-TMA) loads
+    PATH_SKINNY = 5,    // small M: swapped operands, split-K over a cluster
+};
+
+// Bits of the device error word (OR-ed by kernels that abandon a wait).
+enum ErrBits : unsigned int {
+    ERR_MAIN_PRODUCER = 1u << 0,
+    ERR_MAIN_MMA = 1u << 1,
+    ERR_MAIN_EPILOGUE = 1u << 2,
+    ERR_BOUNDARY = 1u << 3,
+    ERR_SKINNY = 1u << 4,
+    ERR_DRAIN = 1u << 5,
+};
+
+struct GemmArgs {
+    int M, N, K;
+    const void* A;
+    long long lda;
+    const void* B;
+    long long ldb;
+    void* C;
+    long long ldc;
+    bool out_f32;
+    unsigned int* err;  // device error word
+    int num_sms;
+    cudaStream_t stream;
+};
+
+// Encodes a 2-D row-major fp16 tensor map (inner extent `cols`, `rows` rows,
+// row stride `ld` elements) with a box of box_cols x box_rows and 128-byte
+// swizzle.  Returns false if the driver rejects it.
+bool encode_tmap_f16(CUtensorMap* map, const void* ptr, uint64_t cols, uint64_t rows,
+                     uint64_t ld, uint32_t box_cols, uint32_t box_rows);
+
+cudaError_t launch_simt_f32(const GemmArgs& a);
+cudaError_t launch_main(const GemmArgs& a, int bn);
+cudaError_t launch_boundary(const GemmArgs& a);
+cudaError_t launch_skinny(const GemmArgs& a);
+
+// Tile width the main kernel uses for this problem (64, 128 or 256).
+int main_tile_n(int M, int N, int num_sms);
+
+}  // namespace tg
