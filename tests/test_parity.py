@@ -131,7 +131,7 @@ def test_config5_wide_sampled():
 @pytest.mark.parametrize("M,N,K,ld_pad,off,out,path", [
     (300, 520, 1000, (0, 0, 0), (0, 0, 0), torch.float16, MAIN),
     (300, 520, 1000, (8, 24, 3), (8, 16, 1), torch.float32, MAIN),
-    (129, 257, 130, (0, 0, 0), (0, 0, 0), torch.float16, MAIN),
+    (129, 257, 130, (6, 7, 0), (0, 0, 0), torch.float16, MAIN),
     (127, 255, 512, (0, 0, 0), (0, 0, 0), torch.float16, BOUNDARY),
     (200, 100, 333, (1, 3, 5), (1, 3, 7), torch.float32, BOUNDARY),
     (100, 90, 300, (2, 1, 0), (0, 0, 0), torch.float16, BOUNDARY),
