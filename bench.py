@@ -45,7 +45,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic (read + write bytes per launch) of the main kernel from one
 # ncu capture, keyed by workload, with the hash of the kernel sources it was
 # taken on.  A stale hash means the kernel changed since: traffic is null.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/gemm_tc_main_square_8192.md: 949.3 MB read + 123.9 MB written
+    "square_8192": {"bytes": 1073185024, "kernel_hash": "a4053c0733734b32"},
+}
 
 KERNEL_SOURCES = ["tiled_gemm_tg_gb300/csrc/gemm_tc.cu", "tiled_gemm_tg_gb300/csrc/ptx.cuh"]
 
@@ -142,23 +145,21 @@ class ClockSampler:
 # ----------------------------------------------------------- CPU oracle leg
 
 def oracle_rows_sample(w, a_cpu, b_cpu, target_s: float):
-    """Time the oracle on whole rows of C until about target_s of work.
-    Returns (TFLOP/s, rows, seconds, threads)."""
+    """Time the oracle on whole rows of C, growing the row count until one
+    timed call takes about target_s.  Returns (TFLOP/s, rows, seconds, threads)."""
     import oracle
 
     nt = oracle.num_threads()
     a_np = a_cpu.numpy()
     b_np = b_cpu.numpy()
     rows = max(1, min(nt, w.M))
-    t = time.perf_counter()
-    oracle.gemm(a_np[:rows], b_np)
-    dt = time.perf_counter() - t
-    if dt < target_s:
-        scale = max(1, int(target_s / max(dt, 1e-3)))
-        rows = min(w.M, rows * scale)
+    while True:
         t = time.perf_counter()
         oracle.gemm(a_np[:rows], b_np)
         dt = time.perf_counter() - t
+        if dt >= 0.6 * target_s or rows >= w.M:
+            break
+        rows = min(w.M, rows * max(2, int(0.9 * target_s / max(dt, 1e-3))))
     return 2.0 * rows * w.N * w.K / dt / 1e12, rows, dt, nt
 
 
