@@ -46,11 +46,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # ncu capture, keyed by workload, with the hash of the kernel sources it was
 # taken on.  A stale hash means the kernel changed since: traffic is null.
 NCU_TRAFFIC = {
-    # profiles/gemm_tc_main_square_8192.md: 949.3 MB read + 123.9 MB written
-    "square_8192": {"bytes": 1073185024, "kernel_hash": "a4053c0733734b32"},
+    # (filled from the ncu capture of the CTA-pair kernel on this workload)
 }
 
-KERNEL_SOURCES = ["tiled_gemm_tg_gb300/csrc/gemm_tc.cu", "tiled_gemm_tg_gb300/csrc/ptx.cuh"]
+KERNEL_SOURCES = ["tiled_gemm_tg_gb300/csrc/gemm_tc2.cu", "tiled_gemm_tg_gb300/csrc/ptx.cuh",
+                  "tiled_gemm_tg_gb300/csrc/tc_common.cuh"]
 
 
 def kernel_hash() -> str:
@@ -374,7 +374,8 @@ def main():
         "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
         "frac": achieved / peak, "traffic": traffic,
         "kernel": {3: "gemm_tc_main_kernel", 4: "gemm_tc_boundary_kernel",
-                   2: "gemm_simt_f32_kernel"}.get(path, str(path)),
+                   2: "gemm_simt_f32_kernel", 5: "gemm_skinny_kernel",
+                   6: "gemm_tc_pair_kernel"}.get(path, str(path)),
         "kernel_ms": kern_ms,
         "peak_source": f"{peak_src} bf16 burst (torch.matmul 8192^3) x 1.0 fp16/bf16 nominal ratio",
         "frac_of_nominal_2500": achieved / NOMINAL_FP16_DENSE_TFLOPS,

@@ -47,7 +47,7 @@ typedef enum {
  * tg_gemm -- C = A x B.
  *
  * Arguments
- *   M, N, K   problem sizes, each in [0, 2^31 - 1].
+ *   M, N, K   problem sizes, each in [0, 2^31 - 1024].
  *   A         device pointer, M rows of K elements, row i at A + i*lda.
  *   lda       row stride of A in elements, lda >= K.
  *   B         device pointer, K rows of N elements, row k at B + k*ldb.
@@ -80,7 +80,7 @@ typedef enum {
  *   TG_ERR_INVALID_ARG  a negative size; a NULL pointer that would be read
  *                       or written; lda < K, ldb < N or ldc < N; or the byte
  *                       span of C overlapping the span of A or of B.
- *   TG_ERR_UNSUPPORTED  an unsupported dtype pair, or a size above 2^31 - 1.
+ *   TG_ERR_UNSUPPORTED  an unsupported dtype pair, or a size above 2^31 - 1024.
  *   TG_ERR_CUDA         a CUDA call made while launching failed.
  *
  * Ownership and memory: the caller owns A, B and C.  The library allocates
@@ -116,9 +116,11 @@ const char* tg_status_string(tg_status status);
  * launching anything, which kernel tg_gemm would run for these arguments on
  * the current device:
  *   0 none (no-op or error), 1 zero-fill (K == 0), 2 SIMT fp32,
- *   3 TMA + tcgen05 main kernel, 4 boundary kernel (predicated loads),
- *   5 skinny kernel (small M, split-K across a thread-block cluster).
- * tg_gemm_force_path forces one of 2..5 for subsequent calls in this process
+ *   3 TMA + tcgen05 main kernel (one CTA per 128-row tile),
+ *   4 boundary kernel (predicated loads, any alignment),
+ *   5 skinny kernel (small M, split-K across a thread-block cluster),
+ *   6 TMA + tcgen05 main kernel on CTA pairs (256 x 256 tiles).
+ * tg_gemm_force_path forces one of 2..6 for subsequent calls in this process
  * (0 restores automatic selection); a forced path that cannot serve a call
  * (e.g. the main kernel for misaligned operands, SIMT for fp16) makes that
  * call return TG_ERR_UNSUPPORTED.

@@ -90,6 +90,7 @@ def path(M, N, K, A=PA, lda=None, B=PB, ldb=None, C=PC, ldc=None, i=tg.F16, o=tg
     (dict(M=4, N=4, K=4, i=0, o=tg.F16), tg.TG_ERR_UNSUPPORTED),
     (dict(M=2 ** 31, N=4, K=4), tg.TG_ERR_UNSUPPORTED),
     (dict(M=4, N=4, K=2 ** 31), tg.TG_ERR_UNSUPPORTED),
+    (dict(M=2 ** 31 - 1023, N=8, K=8), tg.TG_ERR_UNSUPPORTED),
     # C overlapping A or B
     (dict(M=64, N=64, K=64, C=PA + 64), tg.TG_ERR_INVALID_ARG),
     (dict(M=64, N=64, K=64, C=PB - 100), tg.TG_ERR_INVALID_ARG),
@@ -121,7 +122,10 @@ def test_path_selection():
     assert path(128, 128, 128, i=tg.F32, o=tg.F32) == 2
     assert path(1024, 2048, 512) == 3
     assert path(1024, 2048, 512, o=tg.F32) == 3
-    assert path(8192, 8192, 8192) == 3
+    assert path(8192, 8192, 8192) == 6           # 1024 tiles of 256x256: CTA pairs
+    assert path(4096, 16384, 4096) == 6
+    assert path(2048, 2048, 512) == 6            # exactly 64 pair tiles
+    assert path(2048, 1792, 512) == 3            # 56 pair tiles: one CTA per tile
     # row stride not a multiple of 16 bytes -> boundary kernel
     assert path(127, 255, 512) == 4
     assert path(4, 4, 4) == 4
@@ -139,7 +143,11 @@ def test_forced_paths():
         assert path(1024, 2048, 512) == 4            # boundary can serve an aligned case
         assert path(128, 128, 128, i=tg.F32, o=tg.F32) == 0  # but not fp32 inputs
         tg.tg_gemm_force_path(3)
+        assert path(8192, 8192, 8192) == 3
         assert path(127, 255, 512) == 0              # main cannot serve misaligned operands
+        tg.tg_gemm_force_path(6)
+        assert path(16, 16, 16) == 6
+        assert path(127, 255, 512) == 0
         assert call(127, 255, 512) == tg.TG_ERR_UNSUPPORTED
         tg.tg_gemm_force_path(2)
         assert path(64, 64, 64) == 0                 # SIMT is fp32 only

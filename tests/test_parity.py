@@ -25,7 +25,7 @@ from gpu_util import check_full, compare, f16_bits_of, run
 
 pytestmark = pytest.mark.gpu
 
-MAIN, BOUNDARY, SIMT = 3, 4, 2
+MAIN, BOUNDARY, SIMT, PAIR = 3, 4, 2, 6
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -106,7 +106,7 @@ def _matvec_property(a, b, got, out_f16):
 def test_config4_square_8192():
     w, a, b, out = workload("square_8192")
     got, intact, path = run(a, b, out)
-    assert path == MAIN and intact
+    assert path == PAIR and intact
     assert np.isfinite(got).all(), "an output element was never written"
     _sampled_check(a, b, got, True, 41, extra_rows=(0, 4095, 8191), extra_cols=(0, 4097, 8191))
     _matvec_property(a, b, got, True)
@@ -120,7 +120,7 @@ def test_config5_skinny_full():
 def test_config5_wide_sampled():
     w, a, b, out = workload("wide_4096x16384x4096")
     got, intact, path = run(a, b, out)
-    assert path == MAIN and intact
+    assert path == PAIR and intact
     assert np.isfinite(got).all()
     _sampled_check(a, b, got, True, 51, extra_rows=(0, 4095), extra_cols=(0, 16383))
     _matvec_property(a, b, got, True)
@@ -242,8 +242,8 @@ def test_shapes_main_and_tails(M, N, K, out):
     check_full(a, b, out, lda=pad(K), ldb=pad(N), ldc=N + 3)
 
 
-@pytest.mark.parametrize("force", [MAIN, BOUNDARY])
-def test_same_problem_both_tensor_core_paths(force):
+@pytest.mark.parametrize("force", [MAIN, BOUNDARY, PAIR])
+def test_same_problem_every_tensor_core_path(force):
     a = inputs.draw((333, 456), "normal", 7601, "f16")
     b = inputs.draw((456, 520), "normal", 7602, "f16")
     tg.tg_gemm_force_path(force)
@@ -252,6 +252,49 @@ def test_same_problem_both_tensor_core_paths(force):
     finally:
         tg.tg_gemm_force_path(0)
     assert p == force
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 8, 8), (100, 72, 40), (256, 256, 64), (257, 264, 65),
+                                   (513, 520, 1000), (768, 1280, 320), (1000, 2000, 700)])
+@pytest.mark.parametrize("out", [torch.float16, torch.float32])
+def test_pair_kernel_shapes(M, N, K, out):
+    """The CTA-pair kernel forced onto ragged shapes: tails in M (inside either
+    CTA's half), N (inside either CTA's B half) and K."""
+    a = inputs.draw((M, K), "normal", 7800 + M, "f16")
+    b = inputs.draw((K, N), "normal", 7900 + N, "f16")
+    pad = lambda x: (x + 7) // 8 * 8  # noqa: E731
+    tg.tg_gemm_force_path(PAIR)
+    try:
+        _, _, p = check_full(a, b, out, lda=pad(K), ldb=pad(N), ldc=N + 1)
+    finally:
+        tg.tg_gemm_force_path(0)
+    assert p == PAIR
+
+
+def test_pair_kernel_integer_bitwise():
+    a = inputs.draw((700, 1000), "int2", 7951, "f16")
+    b = inputs.draw((1000, 900), "int2", 7952, "f16")
+    tg.tg_gemm_force_path(PAIR)
+    try:
+        got, intact, p = run(a, b, torch.float16, ldb=904)
+    finally:
+        tg.tg_gemm_force_path(0)
+    assert p == PAIR and intact
+    C_ref, _ = oracle.gemm(a.numpy(), b.numpy())
+    have = torch.from_numpy(got).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(have, f16_bits_of(C_ref))
+
+
+def test_one_cta_kernel_on_the_square_shape():
+    """The one-CTA kernel forced onto 8192^3 (the pair kernel's default shape)."""
+    w, a, b, out = workload("square_8192")
+    tg.tg_gemm_force_path(MAIN)
+    try:
+        got, intact, p = run(a, b, out)
+    finally:
+        tg.tg_gemm_force_path(0)
+    assert p == MAIN and intact and np.isfinite(got).all()
+    _sampled_check(a, b, got, True, 43, extra_rows=(8191,), extra_cols=(8191,))
 
 
 def test_stream_argument_is_honoured():

@@ -28,7 +28,8 @@ TG_ERR_INVALID_ARG = 1
 TG_ERR_UNSUPPORTED = 2
 TG_ERR_CUDA = 3
 TG_ERR_TIMEOUT = 4
-PATHS = {0: "none", 1: "zero", 2: "simt_f32", 3: "tc_main", 4: "tc_boundary", 5: "tc_skinny"}
+PATHS = {0: "none", 1: "zero", 2: "simt_f32", 3: "tc_main", 4: "tc_boundary", 5: "tc_skinny",
+         6: "tc_pair"}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libtg_gemm.so")

@@ -22,6 +22,7 @@ LIB = os.path.join(PKG, "libtg_gemm.so")
 SOURCES = [
     "tg_gemm_host.cu",
     "gemm_tc.cu",
+    "gemm_tc2.cu",
     "gemm_tc_boundary.cu",
     "gemm_simt_f32.cu",
 ]

@@ -42,6 +42,7 @@
 #include <cuda_runtime.h>
 
 #include "ptx.cuh"
+#include "tc_common.cuh"
 #include "tg_internal.h"
 
 namespace tg {
@@ -66,57 +67,6 @@ struct MainCfg {
     static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
                   "TMEM allocation must be a power of two in [32, 512]");
 };
-
-// Grouped tile order: tiles are visited in groups of `group_m` tile-rows,
-// column by column inside a group.
-__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int group_m,
-                                            int& tm, int& tn)
-{
-    const int span = group_m * tiles_n;
-    const int g = t / span;
-    const int first = g * group_m;
-    const int gs = min(tiles_m - first, group_m);
-    const int r = t - g * span;
-    tm = first + r % gs;
-    tn = r / gs;
-}
-
-template <bool OUT_F32>
-__device__ __forceinline__ void store_chunk(void* C, long long ldc, int m, int n, int N,
-                                            const uint32_t (&r)[32], bool vec)
-{
-    if constexpr (OUT_F32) {
-        float* row = static_cast<float*>(C) + static_cast<long long>(m) * ldc + n;
-        if (vec && n + 32 <= N) {
-            float4* d = reinterpret_cast<float4*>(row);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                d[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                   __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (n + j < N) row[j] = __uint_as_float(r[j]);
-        }
-    } else {
-        __half* row = static_cast<__half*>(C) + static_cast<long long>(m) * ldc + n;
-        if (vec && n + 32 <= N) {
-            uint32_t p[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                __half2 h = __floats2half2_rn(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-                p[i] = *reinterpret_cast<uint32_t*>(&h);
-            }
-            uint4* d = reinterpret_cast<uint4*>(row);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) d[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (n + j < N) row[j] = __float2half_rn(__uint_as_float(r[j]));
-        }
-    }
-}
 
 template <int BN, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)

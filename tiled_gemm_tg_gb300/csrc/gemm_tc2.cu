@@ -1,0 +1,353 @@
+// gemm_tc2.cu -- CTA-pair variant of the main fp16 GEMM kernel for sm_103a:
+// C = A x B with 256 x 256 output tiles computed by two CTAs of a cluster
+// that share one tcgen05.mma.cta_group::2 (M=256, N=256, K=16).
+//
+// The method is the pages' pipelined tiled GEMM ("企业官网建设流程全解析"
+// (cf-1.com), §2.3 warp specialisation + TMA + mbarrier, §3.3 the tiled
+// K loop with num_stages buffers, §4.1 swizzled shared memory); this file is
+// the GB300 form of it for large problems.
+//
+// Why a pair: each CTA holds half of A's rows (128 x 128) and half of B's
+// columns (128 x 128) of a 256 x 256 x 128 k-block, so a 64 KB stage feeds
+// 1024 MMA cycles and each B column block is loaded once per pair instead of
+// once per 128 rows (a third less L2 -> SM traffic than 128 x 256 tiles).
+// Three stages fill 192 KB of shared memory.
+//
+// Roles (192 threads per CTA, the same in both CTAs of the pair):
+//   warp 0   TMA producer.  Each CTA loads its own halves into its own shared
+//            memory; every copy signals the EVEN (leader) CTA's full barrier,
+//            which the leader's producer arms with both CTAs' bytes.
+//   warp 1   both CTAs allocate 512 TMEM columns together (two 256-column
+//            accumulators); only the leader's lane 0 issues the MMAs.  Each
+//            k-block's commit is multicast to both CTAs' empty barriers,
+//            each tile's commit to both CTAs' tmem-full barriers.
+//   warps 2-5  epilogue in both CTAs: each CTA reads its own 128 rows of the
+//            accumulator from its own TMEM and stores them; all 256 epilogue
+//            threads of the pair arrive on the leader's tmem-empty barrier.
+// Waits are bounded as in the one-CTA kernel; on expiry a role records a bit
+// in the device error word and leaves its loop; the leader waits for the
+// pair's copies in flight and its own MMAs; a cluster barrier keeps both CTAs
+// resident until then, and TMEM is freed by both CTAs together.
+#include <cstdint>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+#include "tc_common.cuh"
+#include "tg_internal.h"
+
+namespace tg {
+namespace {
+
+using namespace tg::dev;
+
+constexpr int PM = 256;                          // pair tile rows (128 per CTA)
+constexpr int PN = 256;                          // pair tile columns (B: 128 per CTA)
+constexpr int HM = PM / 2;
+constexpr int HN = PN / 2;
+// k-block of 128: eight MMAs per stage and per commit.  Measured on GB300,
+// 64-wide k-blocks (four MMAs between stage switches/commits) keep the
+// tensor pipe 87-94 % busy, 128-wide ones 100 %.
+constexpr int BK = 128;
+constexpr int KA = BK / 64;                      // 128-byte swizzle atoms along k in A
+constexpr uint32_t A_ATOM = HM * 128;            // [128 rows][64 k] = 16 KB
+constexpr uint32_t A_STAGE = HM * BK * 2;        // 32 KB
+constexpr uint32_t B_BOX = 64 * BK * 2;          // one [BK k][64 n] box, 16 KB
+constexpr uint32_t B_STAGE = HN * BK * 2;        // 32 KB
+constexpr uint32_t STAGE = A_STAGE + B_STAGE;    // 64 KB per CTA
+constexpr int STAGES = 3;
+constexpr uint32_t SMEM = STAGES * STAGE + 1024;
+constexpr uint32_t TMEM_COLS = 2 * PN;           // two accumulators
+constexpr int kThreads = 192;
+constexpr uint32_t kEpilogueThreads = 128;
+static_assert(SMEM <= 227 * 1024, "shared-memory budget exceeded");
+static_assert(TMEM_COLS == 512, "two 256-column accumulators fill TMEM");
+
+template <bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    void* __restrict__ C, long long ldc, int M, int N, int K, int tiles_m,
+                    int tiles_n, int group_m, int c_vec, unsigned int* err)
+{
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[STAGES];   // used in the leader only
+    __shared__ __align__(8) uint64_t empty_bar[STAGES];
+    __shared__ __align__(8) uint64_t tfull_bar[2];
+    __shared__ __align__(8) uint64_t tempty_bar[2];      // used in the leader only
+    __shared__ __align__(8) uint64_t drain_bar;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();  // 0: leader (issues the MMAs), 1: peer
+    const bool leader = rank == 0;
+    const int pair = static_cast<int>(blockIdx.x >> 1);
+    const int npairs = static_cast<int>(gridDim.x >> 1);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&tfull_bar[a]), 1);
+            mbar_init(smem_u32(&tempty_bar[a]), 2 * kEpilogueThreads);
+        }
+        mbar_init(smem_u32(&drain_bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(&tmem_slot), TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
+    tc_fence_after();
+    const uint32_t tmem_base = tmem_slot;
+
+    const int num_kb = (K + BK - 1) / BK;
+    const int total = tiles_m * tiles_n;
+    const uint32_t epi_limit = kSlowPolls + 64u * static_cast<uint32_t>(min(num_kb, 1 << 20));
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint32_t full0 = mapa_shared(smem_u32(&full_bar[0]), 0);  // leader's ring
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t issued = 0;
+            bool ok = true;
+            for (int t = pair; t < total && ok; t += npairs) {
+                int tm, tn;
+                tile_coords(t, tiles_m, tiles_n, group_m, tm, tn);
+                const int row = tm * PM + static_cast<int>(rank) * HM;
+                const int col = tn * PN + static_cast<int>(rank) * HN;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1u, &abort_flag)) {
+                        abort_flag = 1;
+                        atomicOr(err, ERR_MAIN_PRODUCER);
+                        ok = false;
+                        break;
+                    }
+                    if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[s]), 2 * STAGE);
+                    const uint32_t fb = full0 + 8u * static_cast<uint32_t>(s);
+                    const uint32_t sa = base + s * STAGE;
+#pragma unroll
+                    for (int j = 0; j < KA; ++j)
+                        tma_load_2d_pair(sa + j * A_ATOM, &tmA, fb, kb * BK + j * 64, row);
+#pragma unroll
+                    for (int j = 0; j < HN / 64; ++j)
+                        tma_load_2d_pair(sa + A_STAGE + j * B_BOX, &tmB, fb, col + j * 64, kb * BK);
+                    ++issued;
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            // Copies of both CTAs complete on the leader's full barriers, so the
+            // leader waits there for the last min(issued, STAGES) armed phases;
+            // the closing cluster barrier keeps the peer resident meanwhile.
+            if (leader) {
+                int ds = s;
+                uint32_t dph = ph;
+                const uint32_t n_drain = issued < (uint32_t)STAGES ? issued : (uint32_t)STAGES;
+                for (uint32_t i = 0; i < n_drain; ++i) {
+                    if (--ds < 0) {
+                        ds = STAGES - 1;
+                        dph ^= 1u;
+                    }
+                    if (!mbar_wait(smem_u32(&full_bar[ds]), dph, nullptr)) atomicOr(err, ERR_DRAIN);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------- MMA issuer (leader only)
+        if (leader && lane == 0) {
+            constexpr uint32_t idesc = idesc_f16_f32(PM, PN, false, true);
+            int s = 0;
+            uint32_t ph = 0;
+            int acc = 0;
+            uint32_t aph = 0;
+            bool ok = true;
+            for (int t = pair; t < total && ok; t += npairs) {
+                if (!mbar_wait(smem_u32(&tempty_bar[acc]), aph ^ 1u, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base + static_cast<uint32_t>(acc * PN);
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(smem_u32(&full_bar[s]), ph, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = base + s * STAGE;
+                    // A: K-major, atoms of [128 rows][64 k] 16 KB apart, 8-row groups
+                    // 1024 B apart, +32 B per 16 k inside an atom.  B: MN-major,
+                    // [BK k][64 n] boxes BK*128 B apart, 8-row k groups 1024 B apart.
+                    const uint64_t ad = sdesc_sw128(sa, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(sa + A_STAGE, BK * 128, 1024);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        umma_f16_pair(d, ad + ((k / 4) * (A_ATOM >> 4) + (k % 4) * 2),
+                                      bd + (k * 2048u >> 4), idesc, (kb | k) != 0 ? 1u : 0u);
+                    umma_commit_pair_mc(smem_u32(&empty_bar[s]), 0x3);
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit_pair_mc(smem_u32(&tfull_bar[acc]), 0x3);
+                acc ^= 1;
+                if (acc == 0) aph ^= 1u;
+            }
+            if (!ok) {
+                abort_flag = 1;
+                atomicOr(err, ERR_MAIN_MMA);
+            }
+            umma_commit_pair(smem_u32(&drain_bar));
+            if (!mbar_wait(smem_u32(&drain_bar), 0, nullptr)) atomicOr(err, ERR_DRAIN);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------- epilogue
+        const int q = warp & 3;
+        const uint32_t tempty0 = mapa_shared(smem_u32(&tempty_bar[0]), 0);  // leader's
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int t = pair; t < total; t += npairs) {
+            int tm, tn;
+            tile_coords(t, tiles_m, tiles_n, group_m, tm, tn);
+            const bool got = mbar_wait(smem_u32(&tfull_bar[acc]), aph, &abort_flag, epi_limit);
+            if (!__all_sync(0xffffffffu, got)) {
+                if (lane == 0) {
+                    abort_flag = 1;
+                    atomicOr(err, ERR_MAIN_EPILOGUE);
+                }
+                break;
+            }
+            tc_fence_after();
+            const int m = tm * PM + static_cast<int>(rank) * HM + q * 32 + lane;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(acc * PN);
+#pragma unroll 1
+            for (int c = 0; c < PN; c += 32) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(taddr + c, r);
+                tmem_ld_wait();
+                const int n = tn * PN + c;
+                if (m < M && n < N) store_chunk<OUT_F32>(C, ldc, m, n, N, r, c_vec != 0);
+            }
+            tc_fence_before();
+            mbar_arrive_cluster(tempty0 + 8u * static_cast<uint32_t>(acc));
+            acc ^= 1;
+            if (acc == 0) aph ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
+std::mutex g_mu;
+bool g_attr_set[64][2];
+int g_max_clusters[64][2];
+
+template <bool OUT_F32>
+cudaError_t launch_cfg(const GemmArgs& a)
+{
+    auto kernel = gemm_tc_pair_kernel<OUT_F32>;
+    const int slot = OUT_F32 ? 1 : 0;
+    int max_clusters = 0;
+    {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!g_attr_set[dev][slot]) {
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(SMEM));
+            if (e != cudaSuccess) return e;
+            cudaLaunchConfig_t q = {};
+            q.gridDim = dim3(2 * a.num_sms);
+            q.blockDim = dim3(kThreads);
+            q.dynamicSmemBytes = SMEM;
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = 2;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            q.attrs = at;
+            q.numAttrs = 1;
+            int n = 0;
+            e = cudaOccupancyMaxActiveClusters(&n, kernel, &q);
+            if (e != cudaSuccess) return e;
+            g_max_clusters[dev][slot] = n > 0 ? n : 1;
+            g_attr_set[dev][slot] = true;
+        }
+        max_clusters = g_max_clusters[dev][slot];
+    }
+    CUtensorMap ta, tb;
+    if (!encode_tmap_f16(&ta, a.A, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M),
+                         static_cast<uint64_t>(a.lda), 64, HM))
+        return cudaErrorInvalidValue;
+    if (!encode_tmap_f16(&tb, a.B, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
+                         static_cast<uint64_t>(a.ldb), 64, BK))
+        return cudaErrorInvalidValue;
+    const int tiles_m = (a.M + PM - 1) / PM;
+    const int tiles_n = (a.N + PN - 1) / PN;
+    const int total = tiles_m * tiles_n;
+    const int pairs = total < max_clusters ? total : max_clusters;
+    const int group_m = 8;
+    const size_t es = OUT_F32 ? 4 : 2;
+    const int c_vec = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) &&
+                      ((static_cast<size_t>(a.ldc) * es) % 16 == 0);
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * pairs);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = SMEM;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, ta, tb, a.C, a.ldc, a.M, a.N, a.K, tiles_m, tiles_n,
+                              group_m, c_vec, a.err);
+}
+
+}  // namespace
+
+int pair_tiles(int M, int N)
+{
+    return ((M + PM - 1) / PM) * ((N + PN - 1) / PN);
+}
+
+cudaError_t launch_main_pair(const GemmArgs& a)
+{
+    return a.out_f32 ? launch_cfg<true>(a) : launch_cfg<false>(a);
+}
+
+}  // namespace tg

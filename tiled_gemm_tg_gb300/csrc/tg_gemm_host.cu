@@ -24,7 +24,9 @@ static __device__ unsigned int g_tg_error_word;
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int64_t kMaxDim = 2147483647LL;
+// Largest M, N or K: tile origins (up to a dimension plus one tile) and TMA
+// coordinates stay within int32.
+constexpr int64_t kMaxDim = 2147483647LL - 1023;
 
 struct DeviceState {
     bool ready = false;
@@ -116,7 +118,13 @@ tg_status classify(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
     const bool tma_ok = (reinterpret_cast<uintptr_t>(A) % 16 == 0) &&
                         (reinterpret_cast<uintptr_t>(B) % 16 == 0) && (lda % 8 == 0) &&
                         (ldb % 8 == 0) && lda < kMaxTmaLd && ldb < kMaxTmaLd;
-    *path = tma_ok ? tg::PATH_MAIN : tg::PATH_BOUNDARY;
+    if (!tma_ok) {
+        *path = tg::PATH_BOUNDARY;
+    } else if (tg::pair_tiles(static_cast<int>(M), static_cast<int>(N)) >= tg::kPairMinTiles) {
+        *path = tg::PATH_MAIN_PAIR;
+    } else {
+        *path = tg::PATH_MAIN;
+    }
     return TG_OK;
 }
 
@@ -128,7 +136,7 @@ bool path_serves(int path, int natural, tg_dtype in_dtype)
         case tg::PATH_SIMT: return in_dtype == TG_F32;
         case tg::PATH_BOUNDARY: return in_dtype == TG_F16;
         case tg::PATH_MAIN:
-        case tg::PATH_SKINNY:
+        case tg::PATH_MAIN_PAIR:
             return in_dtype == TG_F16 && natural != tg::PATH_BOUNDARY;
         default: return false;
     }
@@ -202,6 +210,7 @@ tg_status tg_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, c
         case tg::PATH_SIMT: e = tg::launch_simt_f32(a); break;
         case tg::PATH_MAIN: e = tg::launch_main(a, tg::main_tile_n(a.M, a.N, a.num_sms)); break;
         case tg::PATH_BOUNDARY: e = tg::launch_boundary(a); break;
+        case tg::PATH_MAIN_PAIR: e = tg::launch_main_pair(a); break;
         default: return TG_ERR_UNSUPPORTED;
     }
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
@@ -252,7 +261,7 @@ int tg_gemm_path(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, co
 
 void tg_gemm_force_path(int path)
 {
-    if (path < 0 || path > tg::PATH_SKINNY || path == tg::PATH_ZERO) path = 0;
+    if (path < 0 || path > tg::PATH_MAIN_PAIR || path == tg::PATH_ZERO) path = 0;
     g_force_path.store(path, std::memory_order_relaxed);
 }
 

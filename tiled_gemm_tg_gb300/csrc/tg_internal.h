@@ -15,6 +15,7 @@ enum Path : int {
     PATH_MAIN = 3,      // TMA + tcgen05 warp-specialised persistent kernel
     PATH_BOUNDARY = 4,  // tcgen05 kernel with predicated (non-TMA) loads
     PATH_SKINNY = 5,    // small M: swapped operands, split-K over a cluster
+    PATH_MAIN_PAIR = 6, // TMA + tcgen05, 256 x 256 tiles on CTA pairs (cta_group::2)
 };
 
 // Bits of the device error word (OR-ed by kernels that abandon a wait).
@@ -49,10 +50,18 @@ bool encode_tmap_f16(CUtensorMap* map, const void* ptr, uint64_t cols, uint64_t 
 
 cudaError_t launch_simt_f32(const GemmArgs& a);
 cudaError_t launch_main(const GemmArgs& a, int bn);
+cudaError_t launch_main_pair(const GemmArgs& a);
 cudaError_t launch_boundary(const GemmArgs& a);
 cudaError_t launch_skinny(const GemmArgs& a);
 
 // Tile width the main kernel uses for this problem (64, 128 or 256).
 int main_tile_n(int M, int N, int num_sms);
+
+// Number of 256 x 256 tiles the pair kernel would compute.
+int pair_tiles(int M, int N);
+
+// The pair kernel takes over once a problem has at least this many
+// 256 x 256 tiles (enough to occupy most SM pairs in the first wave).
+constexpr int kPairMinTiles = 64;
 
 }  // namespace tg
