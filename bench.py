@@ -46,7 +46,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # ncu capture, keyed by workload, with the hash of the kernel sources it was
 # taken on.  A stale hash means the kernel changed since: traffic is null.
 NCU_TRAFFIC = {
-    # (filled from the ncu capture of the CTA-pair kernel on this workload)
+    # profiles/gemm_tc_pair_square_8192.md: 1047.0 MB read + 125.3 MB written
+    "square_8192": {"bytes": 1172230656, "kernel_hash": "55a52ca72b3fb54c"},
 }
 
 KERNEL_SOURCES = ["tiled_gemm_tg_gb300/csrc/gemm_tc2.cu", "tiled_gemm_tg_gb300/csrc/ptx.cuh",
