@@ -113,9 +113,10 @@ def test_degenerate_sizes_are_noops():
 
 def test_adjacent_operands_are_not_overlap():
     # C starts exactly where A's span ends: legal
-    M, N, K = 4, 8, 8
+    M, N, K = 128, 8, 8
     end_a = PA + ((M - 1) * K + K) * 2
     assert path(M, N, K, C=end_a) == 3
+    assert path(M, N, K, C=end_a - 2) == 0       # one element of overlap
 
 
 def test_path_selection():
@@ -130,6 +131,11 @@ def test_path_selection():
     assert path(127, 255, 512) == 4
     assert path(4, 4, 4) == 4
     assert path(1, 255, 17) == 4
+    # small M with TMA-addressable operands -> skinny split-K kernel
+    assert path(16, 4096, 4096) == 5
+    assert path(64, 4096, 4096) == 5
+    assert path(65, 4096, 4096) == 3
+    assert path(1, 8, 8) == 5
     # base pointer not 16-byte aligned -> boundary kernel
     assert path(128, 256, 512, A=PA + 2) == 4
     assert path(128, 256, 512, B=PB + 8) == 4
@@ -147,6 +153,9 @@ def test_forced_paths():
         assert path(127, 255, 512) == 0              # main cannot serve misaligned operands
         tg.tg_gemm_force_path(6)
         assert path(16, 16, 16) == 6
+        tg.tg_gemm_force_path(5)
+        assert path(64, 512, 512) == 5
+        assert path(65, 512, 512) == 0              # skinny serves M <= 64 only
         assert path(127, 255, 512) == 0
         assert call(127, 255, 512) == tg.TG_ERR_UNSUPPORTED
         tg.tg_gemm_force_path(2)

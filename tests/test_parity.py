@@ -25,7 +25,7 @@ from gpu_util import check_full, compare, f16_bits_of, run
 
 pytestmark = pytest.mark.gpu
 
-MAIN, BOUNDARY, SIMT, PAIR = 3, 4, 2, 6
+MAIN, BOUNDARY, SIMT, PAIR, SKINNY = 3, 4, 2, 6, 5
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -114,7 +114,31 @@ def test_config4_square_8192():
 
 def test_config5_skinny_full():
     w, a, b, out = workload("skinny_16x4096x4096")
-    check_full(a, b, out)
+    _, _, path = check_full(a, b, out)
+    assert path == SKINNY
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 8, 8), (1, 4096, 4096), (5, 300, 1000), (16, 128, 128),
+                                   (17, 1000, 2100), (31, 4104, 600), (32, 256, 8192),
+                                   (48, 2048, 1024), (63, 520, 3000), (64, 16384, 512)])
+@pytest.mark.parametrize("out", [torch.float16, torch.float32])
+def test_skinny_kernel_shapes(M, N, K, out):
+    """Split-K over a cluster with the DSMEM reduction, ragged M, N and K."""
+    a = inputs.draw((M, K), "normal_0.02", 8100 + M, "f16")
+    b = inputs.draw((K, N), "normal_0.02", 8200 + N, "f16")
+    pad = lambda x: (x + 7) // 8 * 8  # noqa: E731
+    _, _, p = check_full(a, b, out, lda=pad(K), ldb=pad(N), ldc=N + 2)
+    assert p == SKINNY
+
+
+def test_skinny_integer_bitwise():
+    a = inputs.draw((24, 3000), "int2", 8301, "f16")
+    b = inputs.draw((3000, 1032), "int2", 8302, "f16")
+    got, intact, p = run(a, b, torch.float16)
+    assert p == SKINNY and intact
+    C_ref, _ = oracle.gemm(a.numpy(), b.numpy())
+    have = torch.from_numpy(got).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(have, f16_bits_of(C_ref))
 
 
 def test_config5_wide_sampled():
@@ -192,10 +216,15 @@ def test_transpose_invariant():
     assert np.array_equal(c1, c2.T)
 
 
-def test_8x8_ones_page_example():
+@pytest.mark.parametrize("force", [0, MAIN, PAIR, BOUNDARY])
+def test_8x8_ones_page_example(force):
     a = torch.ones((8, 8), dtype=torch.float16)
-    got, intact, p = run(a, a, torch.float16)
-    assert intact and p == MAIN and np.all(got == 8)
+    tg.tg_gemm_force_path(force)
+    try:
+        got, intact, p = run(a, a, torch.float16)
+    finally:
+        tg.tg_gemm_force_path(0)
+    assert intact and p == (force or SKINNY) and np.all(got == 8)
 
 
 # ----------------------------------------------------------- degenerate sizes
@@ -244,6 +273,7 @@ def test_shapes_main_and_tails(M, N, K, out):
 
 @pytest.mark.parametrize("force", [MAIN, BOUNDARY, PAIR])
 def test_same_problem_every_tensor_core_path(force):
+    """(The skinny kernel serves M <= 64 only; it has its own shape tests.)"""
     a = inputs.draw((333, 456), "normal", 7601, "f16")
     b = inputs.draw((456, 520), "normal", 7602, "f16")
     tg.tg_gemm_force_path(force)

@@ -24,6 +24,7 @@ SOURCES = [
     "gemm_tc.cu",
     "gemm_tc2.cu",
     "gemm_tc_boundary.cu",
+    "gemm_skinny.cu",
     "gemm_simt_f32.cu",
 ]
 

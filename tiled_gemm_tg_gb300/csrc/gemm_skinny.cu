@@ -1,0 +1,326 @@
+// gemm_skinny.cu -- fp16 GEMM for small M (M <= 64), the decode-like shapes
+// where C = A x B is bound by streaming B from HBM, not by the tensor cores
+// (16 x 4096 x 4096: 15.9 FLOP per byte).
+//
+// It computes the same product as the pages' tiled GEMM ("企业官网建设流程全
+// 解析" (cf-1.com) §3.3; "TileLang实战" (gsyq.cn) §3.1), arranged so that B
+// streams through every SM:
+//   * operands swapped: C^T[N, M] = B^T[N, K] x A^T[K, M].  The MMA's M = 128
+//     runs over N (B^T is MN-major in shared memory: B's rows are contiguous
+//     in n), the MMA's N = Mp (M rounded up to 16) runs over M (A is K-major);
+//     the accumulator holds 128 n-lanes x Mp fp32 columns in TMEM;
+//   * split-K over a thread-block cluster of S CTAs (S = 1, 2, 4 or 8): CTA r
+//     of the cluster owns the same 128 columns of C and k-blocks
+//     [r*nkb/S, (r+1)*nkb/S), so n_tiles * S CTAs stream disjoint parts of B;
+//   * the S fp32 partials meet in distributed shared memory: each CTA writes
+//     its partial (read from TMEM) into its own shared memory, the cluster
+//     synchronises, and CTA r sums, in rank order, rows n in
+//     [r*128/S, (r+1)*128/S) of all S partials, rounds to the output type and
+//     stores them.  No global workspace, one launch.
+// Warp roles as in the main kernel: warp 0 TMA producer (k-block 128, four
+// stages), warp 1 TMEM allocation + single-thread tcgen05.mma issue, warps
+// 2-5 read the accumulator.  Waits are bounded; on expiry the kernel records
+// a bit in the device error word, stops issuing, waits for its own copies and
+// MMAs, and still reaches the cluster barriers so no CTA waits on a missing
+// peer.
+#include <cstdint>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+#include "tg_internal.h"
+
+namespace tg {
+namespace {
+
+using namespace tg::dev;
+
+constexpr int BNT = 128;                       // n per CTA (the MMA's M)
+constexpr int BK = 128;                        // k-block: eight MMAs per stage
+constexpr uint32_t BT_BOX = 64 * BK * 2;       // [BK k][64 n] box of B^T, 16 KB
+constexpr uint32_t BT_STAGE = BNT * BK * 2;    // 32 KB
+constexpr int STAGES = 4;
+constexpr int kThreads = 192;
+constexpr int kMaxSplit = 8;
+
+template <int MP>
+struct SkinnyCfg {
+    static constexpr uint32_t A_ATOM = MP * 128;          // [MP rows][64 k]
+    static constexpr uint32_t A_STAGE = MP * BK * 2;
+    static constexpr uint32_t STAGE = BT_STAGE + A_STAGE;
+    static constexpr uint32_t SMEM = STAGES * STAGE + 1024;
+    static constexpr uint32_t TMEM_COLS = MP <= 32 ? 32 : 64;
+    static constexpr uint32_t RED_BYTES = MP * BNT * 4;  // fp32 partial [MP][128]
+    static_assert(SMEM <= 227 * 1024, "shared-memory budget exceeded");
+    static_assert(RED_BYTES <= STAGES * STAGE, "reduction buffer must fit in the stages");
+};
+
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr)
+{
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
+template <int MP, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmBT,
+                   void* __restrict__ C, long long ldc, int M, int N, int K, int split,
+                   unsigned int* err)
+{
+    using Cfg = SkinnyCfg<MP>;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[STAGES];
+    __shared__ __align__(8) uint64_t empty_bar[STAGES];
+    __shared__ __align__(8) uint64_t tfull_bar;
+    __shared__ __align__(8) uint64_t drain_bar;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    float* const red = reinterpret_cast<float*>(smem_raw + (base - smem_u32(smem_raw)));
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int rank = static_cast<int>(cluster_ctarank());  // == blockIdx.x (cluster spans x)
+    const int n0 = blockIdx.y * BNT;
+    const int nkb = (K + BK - 1) / BK;
+    const int kb0 = static_cast<int>(static_cast<long long>(rank) * nkb / split);
+    const int kb1 = static_cast<int>(static_cast<long long>(rank + 1) * nkb / split);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), 1);
+        }
+        mbar_init(smem_u32(&tfull_bar), 1);
+        mbar_init(smem_u32(&drain_bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmBT);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&tmem_slot), Cfg::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = tmem_slot;
+    const uint32_t epi_limit = kSlowPolls + 64u * static_cast<uint32_t>(min(kb1 - kb0, 1 << 20));
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t issued = 0;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1u, &abort_flag)) {
+                    abort_flag = 1;
+                    atomicOr(err, ERR_SKINNY);
+                    break;
+                }
+                const uint32_t fb = smem_u32(&full_bar[s]);
+                const uint32_t sa = base + s * Cfg::STAGE;
+                mbar_arrive_expect_tx(fb, Cfg::STAGE);
+#pragma unroll
+                for (int j = 0; j < BNT / 64; ++j)
+                    tma_load_2d(sa + j * BT_BOX, &tmBT, fb, n0 + j * 64, kb * BK);
+#pragma unroll
+                for (int j = 0; j < BK / 64; ++j)
+                    tma_load_2d(sa + BT_STAGE + j * Cfg::A_ATOM, &tmA, fb, kb * BK + j * 64, 0);
+                ++issued;
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            int ds = s;
+            uint32_t dph = ph;
+            const uint32_t n_drain = issued < (uint32_t)STAGES ? issued : (uint32_t)STAGES;
+            for (uint32_t i = 0; i < n_drain; ++i) {
+                if (--ds < 0) {
+                    ds = STAGES - 1;
+                    dph ^= 1u;
+                }
+                if (!mbar_wait(smem_u32(&full_bar[ds]), dph, nullptr)) atomicOr(err, ERR_DRAIN);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // A operand = B^T tile (MN-major), B operand = A tile (K-major).
+            constexpr uint32_t idesc = idesc_f16_f32(BNT, MP, true, false);
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!mbar_wait(smem_u32(&full_bar[s]), ph, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sa = base + s * Cfg::STAGE;
+                const uint64_t btd = sdesc_sw128(sa, BK * 128, 1024);
+                const uint64_t ad = sdesc_sw128(sa + BT_STAGE, 16, 1024);
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k)
+                    umma_f16(tmem_base, btd + (k * 2048u >> 4),
+                             ad + ((k / 4) * (Cfg::A_ATOM >> 4) + (k % 4) * 2), idesc,
+                             (kb != kb0 || k != 0) ? 1u : 0u);
+                umma_commit(smem_u32(&empty_bar[s]));
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok) {
+                abort_flag = 1;
+                atomicOr(err, ERR_SKINNY);
+            } else {
+                umma_commit(smem_u32(&tfull_bar));
+            }
+            umma_commit(smem_u32(&drain_bar));
+            if (!mbar_wait(smem_u32(&drain_bar), 0, nullptr)) atomicOr(err, ERR_DRAIN);
+        }
+        __syncwarp();
+    } else {
+        // Accumulator -> this CTA's fp32 partial in shared memory, [MP][128]:
+        // lane n of warp quadrant q holds the MP values of row n = 32q + lane.
+        const int q = warp & 3;
+        const bool got = mbar_wait(smem_u32(&tfull_bar), 0, &abort_flag, epi_limit);
+        if (__all_sync(0xffffffffu, got)) {
+            tc_fence_after();
+            const int nl = q * 32 + lane;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll
+            for (int c = 0; c < MP; c += 16) {
+                uint32_t r[16];
+                tmem_ld_32x32b_x16(taddr + c, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    red[(c + j) * BNT + nl] = (kb1 > kb0) ? __uint_as_float(r[j]) : 0.0f;
+            }
+        } else if (lane == 0) {
+            abort_flag = 1;
+            atomicOr(err, ERR_SKINNY);
+        }
+        tc_fence_before();
+    }
+
+    // All partials of the cluster are in shared memory after this barrier.
+    cluster_sync();
+
+    {
+        const int span = BNT / split;  // rows n this CTA reduces
+        const uint32_t red_local = smem_u32(red);
+        for (int idx = threadIdx.x; idx < span * M; idx += kThreads) {
+            const int m = idx / span;
+            const int nl = rank * span + (idx - m * span);
+            const int n = n0 + nl;
+            if (n >= N) continue;
+            const uint32_t off = static_cast<uint32_t>((m * BNT + nl) * 4);
+            float sum = 0.0f;
+            for (int r = 0; r < split; ++r)
+                sum += ld_dsmem_f32(mapa_shared(red_local + off, static_cast<uint32_t>(r)));
+            if constexpr (OUT_F32)
+                static_cast<float*>(C)[static_cast<long long>(m) * ldc + n] = sum;
+            else
+                static_cast<__half*>(C)[static_cast<long long>(m) * ldc + n] = __float2half_rn(sum);
+        }
+    }
+
+    // No CTA may leave while a peer can still read its shared memory.
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+std::mutex g_mu;
+bool g_attr_set[64][8];
+
+template <int MP, bool OUT_F32>
+cudaError_t launch_cfg(const GemmArgs& a, int split)
+{
+    using Cfg = SkinnyCfg<MP>;
+    auto kernel = gemm_skinny_kernel<MP, OUT_F32>;
+    {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        const int slot = (MP / 16 - 1) * 2 + (OUT_F32 ? 1 : 0);
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!g_attr_set[dev][slot]) {
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(Cfg::SMEM));
+            if (e != cudaSuccess) return e;
+            g_attr_set[dev][slot] = true;
+        }
+    }
+    CUtensorMap ta, tbt;
+    if (!encode_tmap_f16(&ta, a.A, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M),
+                         static_cast<uint64_t>(a.lda), 64, MP))
+        return cudaErrorInvalidValue;
+    if (!encode_tmap_f16(&tbt, a.B, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
+                         static_cast<uint64_t>(a.ldb), 64, BK))
+        return cudaErrorInvalidValue;
+    const int n_tiles = (a.N + BNT - 1) / BNT;
+    if (n_tiles > 65535) return cudaErrorInvalidConfiguration;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(split, n_tiles);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Cfg::SMEM;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = split;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, ta, tbt, a.C, a.ldc, a.M, a.N, a.K, split, a.err);
+}
+
+}  // namespace
+
+int skinny_split(int M, int N, int K, int num_sms)
+{
+    (void)M;
+    const long long n_tiles = (N + BNT - 1) / BNT;
+    const int nkb = (K + BK - 1) / BK;
+    int s = 1;
+    while (s < kMaxSplit && n_tiles * (2 * s) <= num_sms && nkb >= 2 * (2 * s)) s *= 2;
+    return s;
+}
+
+cudaError_t launch_skinny(const GemmArgs& a)
+{
+    if (a.M > kSkinnyMaxM) return cudaErrorInvalidValue;
+    const int split = skinny_split(a.M, a.N, a.K, a.num_sms);
+    const int mp = (a.M + 15) / 16 * 16;
+    if (a.out_f32) {
+        switch (mp) {
+            case 16: return launch_cfg<16, true>(a, split);
+            case 32: return launch_cfg<32, true>(a, split);
+            case 48: return launch_cfg<48, true>(a, split);
+            default: return launch_cfg<64, true>(a, split);
+        }
+    }
+    switch (mp) {
+        case 16: return launch_cfg<16, false>(a, split);
+        case 32: return launch_cfg<32, false>(a, split);
+        case 48: return launch_cfg<48, false>(a, split);
+        default: return launch_cfg<64, false>(a, split);
+    }
+}
+
+}  // namespace tg

@@ -120,6 +120,8 @@ tg_status classify(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
                         (ldb % 8 == 0) && lda < kMaxTmaLd && ldb < kMaxTmaLd;
     if (!tma_ok) {
         *path = tg::PATH_BOUNDARY;
+    } else if (M <= tg::kSkinnyMaxM) {
+        *path = tg::PATH_SKINNY;
     } else if (tg::pair_tiles(static_cast<int>(M), static_cast<int>(N)) >= tg::kPairMinTiles) {
         *path = tg::PATH_MAIN_PAIR;
     } else {
@@ -128,7 +130,7 @@ tg_status classify(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
     return TG_OK;
 }
 
-bool path_serves(int path, int natural, tg_dtype in_dtype)
+bool path_serves(int path, int natural, tg_dtype in_dtype, int64_t M)
 {
     if (path == natural) return true;
     if (natural == tg::PATH_ZERO || natural == tg::PATH_NONE) return false;
@@ -138,6 +140,8 @@ bool path_serves(int path, int natural, tg_dtype in_dtype)
         case tg::PATH_MAIN:
         case tg::PATH_MAIN_PAIR:
             return in_dtype == TG_F16 && natural != tg::PATH_BOUNDARY;
+        case tg::PATH_SKINNY:
+            return in_dtype == TG_F16 && natural != tg::PATH_BOUNDARY && M <= tg::kSkinnyMaxM;
         default: return false;
     }
 }
@@ -182,7 +186,7 @@ tg_status tg_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, c
     }
     const int forced = g_force_path.load(std::memory_order_relaxed);
     if (forced != 0) {
-        if (!path_serves(forced, path, in_dtype)) return TG_ERR_UNSUPPORTED;
+        if (!path_serves(forced, path, in_dtype, M)) return TG_ERR_UNSUPPORTED;
         path = forced;
     }
 
@@ -211,6 +215,7 @@ tg_status tg_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, c
         case tg::PATH_MAIN: e = tg::launch_main(a, tg::main_tile_n(a.M, a.N, a.num_sms)); break;
         case tg::PATH_BOUNDARY: e = tg::launch_boundary(a); break;
         case tg::PATH_MAIN_PAIR: e = tg::launch_main_pair(a); break;
+        case tg::PATH_SKINNY: e = tg::launch_skinny(a); break;
         default: return TG_ERR_UNSUPPORTED;
     }
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
@@ -255,7 +260,7 @@ int tg_gemm_path(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, co
         return tg::PATH_NONE;
     const int forced = g_force_path.load(std::memory_order_relaxed);
     if (forced != 0 && path != tg::PATH_ZERO && path != tg::PATH_NONE)
-        return path_serves(forced, path, in_dtype) ? forced : tg::PATH_NONE;
+        return path_serves(forced, path, in_dtype, M) ? forced : tg::PATH_NONE;
     return path;
 }
 
