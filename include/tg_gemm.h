@@ -132,6 +132,19 @@ int tg_gemm_path(int64_t M, int64_t N, int64_t K,
                  tg_dtype in_dtype, tg_dtype out_dtype);
 void tg_gemm_force_path(int path);
 
+/*
+ * Test hook for failure detection, off (0) by default.  With hook 1, every
+ * subsequent tensor-core launch leaves one pipeline stage unfilled (or, in
+ * the boundary kernel, one MMA group uncommitted): nothing ever signals the
+ * barrier that the kernel then waits on, so its bounded wait runs out after
+ * about a second, the kernel records the expiry in the device error word,
+ * releases what it holds and returns, and tg_gemm_check reports
+ * TG_ERR_TIMEOUT.  C is undefined for those calls.  Nothing faults, traps
+ * or hangs.  Any other value turns the hook off.  Process-wide, not
+ * thread-specific; the SIMT fp32 path has no waits and ignores it.
+ */
+void tg_gemm_test_hook(int hook);
+
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int tg_gemm_version(void);
 

@@ -38,7 +38,7 @@ def declared_functions():
 def test_header_declares_the_abi():
     names = declared_functions()
     for must in ["tg_gemm", "tg_gemm_check", "tg_status_string", "tg_gemm_path",
-                 "tg_gemm_force_path", "tg_gemm_version"]:
+                 "tg_gemm_force_path", "tg_gemm_test_hook", "tg_gemm_version"]:
         assert must in names
 
 

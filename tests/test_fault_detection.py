@@ -1,0 +1,78 @@
+"""Failure detection without a GPU fault.
+
+The test hook (tg_gemm_test_hook) makes a tensor-core kernel wait on a
+barrier that nothing signals.  The bounded wait must run out in about a
+second, the kernel must record it in the device error word and return, and
+tg_gemm_check must report TG_ERR_TIMEOUT; the CUDA context must stay usable,
+so the same path run again without the hook matches the oracle.
+"""
+import time
+
+import pytest
+import torch
+
+import tiled_gemm_tg_gb300 as tg
+from tiled_gemm_tg_gb300 import inputs
+
+from gpu_util import DevMatrix, DevOutput, check_full
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    yield
+    tg.tg_gemm_test_hook(0)
+    tg.tg_gemm_force_path(0)
+
+
+# (path, M, N, K, pad_ld): K spans several k-blocks so every kernel waits on
+# the unfilled stage (or uncommitted group) before finishing.
+CASES = [(3, 300, 520, 1024, True), (6, 512, 768, 1024, True), (5, 16, 1024, 2048, True),
+         (4, 127, 255, 512, False)]
+
+
+@pytest.mark.parametrize("path,M,N,K,pad", CASES, ids=lambda v: str(v))
+def test_bounded_wait_expiry_is_reported(path, M, N, K, pad):
+    a = inputs.draw((M, K), "normal", 9100 + path, "f16")
+    b = inputs.draw((K, N), "normal", 9200 + path, "f16")
+    lda = (K + 7) // 8 * 8 if pad else K
+    ldb = (N + 7) // 8 * 8 if pad else N
+    A = DevMatrix(a, lda, 0, "cuda")
+    B = DevMatrix(b, ldb, 0, "cuda")
+    C = DevOutput(M, N, N, 0, torch.float16, "cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    assert tg.tg_gemm_check(s) == tg.TG_OK
+    tg.tg_gemm_force_path(path)
+    tg.tg_gemm_test_hook(1)
+    try:
+        assert tg.tg_gemm_path(M, N, K, A.ptr, lda, B.ptr, ldb, C.ptr, N, tg.F16, tg.F16) == path
+        t0 = time.time()
+        st = tg.tg_gemm(M, N, K, A.ptr, lda, B.ptr, ldb, C.ptr, N, tg.F16, tg.F16, s)
+        assert st == tg.TG_OK
+        assert tg.tg_gemm_check(s) == tg.TG_ERR_TIMEOUT
+        elapsed = time.time() - t0
+    finally:
+        tg.tg_gemm_test_hook(0)
+    try:
+        assert 0.5 < elapsed < 30.0, elapsed
+        # the word was cleared and the context still works: same path, no hook
+        assert tg.tg_gemm_check(s) == tg.TG_OK
+        check_full(a, b, torch.float16, lda=lda, ldb=ldb)
+    finally:
+        tg.tg_gemm_force_path(0)
+
+
+def test_simt_path_ignores_the_hook():
+    a = inputs.draw((64, 64), "normal", 9301, "f32")
+    b = inputs.draw((64, 64), "normal", 9302, "f32")
+    tg.tg_gemm_test_hook(1)
+    try:
+        check_full(a, b, torch.float32)
+    finally:
+        tg.tg_gemm_test_hook(0)

@@ -69,7 +69,7 @@ template <int MP, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmBT,
                    void* __restrict__ C, long long ldc, int M, int N, int K, int split,
-                   unsigned int* err)
+                   int hook, unsigned int* err)
 {
     using Cfg = SkinnyCfg<MP>;
     extern __shared__ uint8_t smem_raw[];
@@ -124,6 +124,15 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                     abort_flag = 1;
                     atomicOr(err, ERR_SKINNY);
                     break;
+                }
+                if (hook == 1 && kb == kb0) {
+                    // test hook: leave this stage unfilled, so the MMA
+                    // thread's bounded wait on it runs out
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                    continue;
                 }
                 const uint32_t fb = smem_u32(&full_bar[s]);
                 const uint32_t sa = base + s * Cfg::STAGE;
@@ -287,7 +296,7 @@ cudaError_t launch_cfg(const GemmArgs& a, int split)
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, ta, tbt, a.C, a.ldc, a.M, a.N, a.K, split, a.err);
+    return cudaLaunchKernelEx(&cfg, kernel, ta, tbt, a.C, a.ldc, a.M, a.N, a.K, split, a.hook, a.err);
 }
 
 }  // namespace

@@ -72,7 +72,7 @@ template <int BN, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     void* __restrict__ C, long long ldc, int M, int N, int K, int tiles_m,
-                    int tiles_n, int group_m, int c_vec, unsigned int* err)
+                    int tiles_n, int group_m, int c_vec, int hook, unsigned int* err)
 {
     using Cfg = MainCfg<BN>;
     constexpr int STAGES = Cfg::STAGES;
@@ -138,6 +138,15 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         atomicOr(err, ERR_MAIN_PRODUCER);
                         ok = false;
                         break;
+                    }
+                    if (hook == 1 && t == static_cast<int>(blockIdx.x) && kb == 0) {
+                        // test hook: leave this stage unfilled, so the MMA
+                        // thread's bounded wait on it runs out
+                        if (++s == STAGES) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                        continue;
                     }
                     const uint32_t fb = smem_u32(&full_bar[s]);
                     const uint32_t sa = base + s * Cfg::STAGE;
@@ -299,7 +308,7 @@ cudaError_t launch_cfg(const GemmArgs& a)
     const int c_vec = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) &&
                       ((static_cast<size_t>(a.ldc) * es) % 16 == 0);
     kernel<<<grid, kThreads, Cfg::SMEM, a.stream>>>(ta, tb, a.C, a.ldc, a.M, a.N, a.K, tiles_m,
-                                                     tiles_n, group_m, c_vec, a.err);
+                                                     tiles_n, group_m, c_vec, a.hook, a.err);
     return cudaGetLastError();
 }
 

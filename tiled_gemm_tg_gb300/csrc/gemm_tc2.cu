@@ -70,7 +70,7 @@ template <bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     void* __restrict__ C, long long ldc, int M, int N, int K, int tiles_m,
-                    int tiles_n, int group_m, int c_vec, unsigned int* err)
+                    int tiles_n, int group_m, int c_vec, int hook, unsigned int* err)
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[STAGES];   // used in the leader only
@@ -138,6 +138,15 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         atomicOr(err, ERR_MAIN_PRODUCER);
                         ok = false;
                         break;
+                    }
+                    if (hook == 1 && leader && t == pair && kb == 0) {
+                        // test hook: the leader never arms this stage, so the
+                        // MMA thread's bounded wait on it runs out
+                        if (++s == STAGES) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                        continue;
                     }
                     if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[s]), 2 * STAGE);
                     const uint32_t fb = full0 + 8u * static_cast<uint32_t>(s);
@@ -335,7 +344,7 @@ cudaError_t launch_cfg(const GemmArgs& a)
     cfg.attrs = at;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, ta, tb, a.C, a.ldc, a.M, a.N, a.K, tiles_m, tiles_n,
-                              group_m, c_vec, a.err);
+                              group_m, c_vec, a.hook, a.err);
 }
 
 }  // namespace

@@ -55,7 +55,7 @@ template <bool OUT_F32>
 __global__ void __launch_bounds__(kThreads)
 gemm_tc_boundary_kernel(const __half* __restrict__ A, long long lda, const __half* __restrict__ B,
                         long long ldb, void* __restrict__ C, long long ldc, int M, int N, int K,
-                        unsigned int* err)
+                        int hook, unsigned int* err)
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t mma_bar[2];
@@ -133,7 +133,8 @@ gemm_tc_boundary_kernel(const __half* __restrict__ A, long long lda, const __hal
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k)
                 umma_f16(tmem_base, ad + 2ull * k, bd + 128ull * k, idesc, (kb | k) != 0 ? 1u : 0u);
-            umma_commit(smem_u32(&mma_bar[s]));
+            // test hook: skip the first commit, so the bounded wait on it runs out
+            if (!(hook == 1 && kb == 0)) umma_commit(smem_u32(&mma_bar[s]));
         }
     }
 
@@ -207,7 +208,7 @@ cudaError_t launch_cfg(const GemmArgs& a)
     if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
     kernel<<<grid, kThreads, SMEM, a.stream>>>(
         static_cast<const __half*>(a.A), a.lda, static_cast<const __half*>(a.B), a.ldb, a.C, a.ldc,
-        a.M, a.N, a.K, a.err);
+        a.M, a.N, a.K, a.hook, a.err);
     return cudaGetLastError();
 }
 

@@ -37,6 +37,7 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 std::atomic<int> g_force_path{0};
+std::atomic<int> g_test_hook{0};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 tg_status device_state(DeviceState** out)
@@ -206,6 +207,7 @@ tg_status tg_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, c
     a.ldc = ldc;
     a.out_f32 = (out_dtype == TG_F32);
     a.err = ds->err;
+    a.hook = g_test_hook.load(std::memory_order_relaxed);
     a.num_sms = ds->num_sms;
     a.stream = s;
 
@@ -269,6 +271,8 @@ void tg_gemm_force_path(int path)
     if (path < 0 || path > tg::PATH_MAIN_PAIR || path == tg::PATH_ZERO) path = 0;
     g_force_path.store(path, std::memory_order_relaxed);
 }
+
+void tg_gemm_test_hook(int hook) { g_test_hook.store(hook == 1 ? 1 : 0, std::memory_order_relaxed); }
 
 int tg_gemm_version(void) { return 100; }
 

@@ -38,6 +38,7 @@ struct GemmArgs {
     long long ldc;
     bool out_f32;
     unsigned int* err;  // device error word
+    int hook;           // test hook (0 = off), see tg_gemm_test_hook
     int num_sms;
     cudaStream_t stream;
 };
