@@ -65,6 +65,10 @@ constexpr int kThreads = 192;
 constexpr uint32_t kEpilogueThreads = 128;
 static_assert(SMEM <= 227 * 1024, "shared-memory budget exceeded");
 static_assert(TMEM_COLS == 512, "two 256-column accumulators fill TMEM");
+#ifndef TG_PAIR_L2_HINTS
+#define TG_PAIR_L2_HINTS 1
+#endif
+constexpr int L2_HINTS = TG_PAIR_L2_HINTS;  // bit 0: A evict_last, bit 1: B evict_first
 
 template <bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -123,6 +127,10 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             const uint32_t full0 = mapa_shared(smem_u32(&full_bar[0]), 0);  // leader's ring
+            // L2 priorities: a group's A row blocks are reused by every wave of
+            // the group, each B column block only by the tiles of one wave.
+            const uint64_t pol_a = L2_HINTS & 1 ? policy_evict_last() : policy_evict_normal();
+            const uint64_t pol_b = L2_HINTS & 2 ? policy_evict_first() : policy_evict_normal();
             int s = 0;
             uint32_t ph = 0;
             uint32_t issued = 0;
@@ -153,10 +161,12 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const uint32_t sa = base + s * STAGE;
 #pragma unroll
                     for (int j = 0; j < KA; ++j)
-                        tma_load_2d_pair(sa + j * A_ATOM, &tmA, fb, kb * BK + j * 64, row);
+                        tma_load_2d_pair_hint(sa + j * A_ATOM, &tmA, fb, kb * BK + j * 64, row,
+                                              pol_a);
 #pragma unroll
                     for (int j = 0; j < HN / 64; ++j)
-                        tma_load_2d_pair(sa + A_STAGE + j * B_BOX, &tmB, fb, col + j * 64, kb * BK);
+                        tma_load_2d_pair_hint(sa + A_STAGE + j * B_BOX, &tmB, fb, col + j * 64,
+                                              kb * BK, pol_b);
                     ++issued;
                     if (++s == STAGES) {
                         s = 0;
