@@ -34,7 +34,9 @@ def built():
 # (path, M, N, K, pad_ld): K spans several k-blocks so every kernel waits on
 # the unfilled stage (or uncommitted group) before finishing.
 CASES = [(3, 300, 520, 1024, True), (6, 512, 768, 1024, True), (5, 16, 1024, 2048, True),
-         (4, 127, 255, 512, False)]
+         (4, 127, 255, 512, False),
+         # 77 pair tiles: one cluster stalls while the others run two tiles
+         (6, 1792, 2816, 1024, True)]
 
 
 @pytest.mark.parametrize("path,M,N,K,pad", CASES, ids=lambda v: str(v))

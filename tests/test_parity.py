@@ -315,6 +315,50 @@ def test_pair_kernel_integer_bitwise():
     assert np.array_equal(have, f16_bits_of(C_ref))
 
 
+# Pair-tile counts around multiples of the cluster count (76 pairs on GB300):
+# whole waves only, one tile past a wave, a partial last wave, ragged M/N/K.
+@pytest.mark.parametrize("M,N,K", [(2048, 2048, 512), (4864, 1024, 1024), (1792, 2816, 2048),
+                                   (2560, 2560, 1000), (2000, 2600, 1000), (2304, 4352, 768),
+                                   (4096, 4096, 4096)])
+def test_pair_kernel_wave_tails(M, N, K):
+    a = inputs.draw((M, K), "normal_rsqrtk", 8400 + M, "f16", k=K)
+    b = inputs.draw((K, N), "normal", 8500 + N, "f16")
+    pad = lambda x: (x + 7) // 8 * 8  # noqa: E731
+    got, intact, p = run(a, b, torch.float16, lda=pad(K), ldb=pad(N))
+    assert p == PAIR and intact and np.isfinite(got).all()
+    _sampled_check(a, b, got, True, 8600 + M, extra_rows=(M - 1,), extra_cols=(N - 1,))
+    _matvec_property(a, b, got, True)
+
+
+@pytest.mark.parametrize("out", [torch.float16, torch.float32])
+def test_pair_kernel_integer_bitwise_77_tiles(out):
+    """77 pair tiles (one past a full wave), small integers: a unique result."""
+    M, N, K = 1792, 2816, 2048
+    a = inputs.draw((M, K), "int2", 8701, "f16")
+    b = inputs.draw((K, N), "int2", 8702, "f16")
+    got, intact, p = run(a, b, out)
+    assert p == PAIR and intact
+    C_ref, _ = oracle.gemm(a.numpy(), b.numpy())
+    if out == torch.float16:
+        have = torch.from_numpy(got).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(have, f16_bits_of(C_ref))
+    else:
+        assert np.array_equal(got, C_ref)
+
+
+def test_pair_kernel_repeated_calls_agree():
+    """Back-to-back calls on one stream give the same exact result."""
+    M, N, K = 1792, 2816, 1024
+    a = inputs.draw((M, K), "int2", 8801, "f16")
+    b = inputs.draw((K, N), "int2", 8802, "f16")
+    C_ref, _ = oracle.gemm(a.numpy(), b.numpy())
+    want = f16_bits_of(C_ref)
+    for _ in range(3):
+        got, intact, p = run(a, b, torch.float16)
+        have = torch.from_numpy(got).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+        assert p == PAIR and intact and np.array_equal(have, want)
+
+
 def test_one_cta_kernel_on_the_square_shape():
     """The one-CTA kernel forced onto 8192^3 (the pair kernel's default shape)."""
     w, a, b, out = workload("square_8192")
