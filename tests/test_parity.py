@@ -120,7 +120,8 @@ def test_config5_skinny_full():
 
 @pytest.mark.parametrize("M,N,K", [(1, 8, 8), (1, 4096, 4096), (5, 300, 1000), (16, 128, 128),
                                    (17, 1000, 2100), (31, 4104, 600), (32, 256, 8192),
-                                   (48, 2048, 1024), (63, 520, 3000), (64, 16384, 512)])
+                                   (48, 2048, 1024), (63, 520, 3000), (64, 16384, 512),
+                                   (16, 2048, 4096), (8, 1024, 8192)])
 @pytest.mark.parametrize("out", [torch.float16, torch.float32])
 def test_skinny_kernel_shapes(M, N, K, out):
     """Split-K over a cluster with the DSMEM reduction, ragged M, N and K."""

@@ -9,7 +9,8 @@
 //     runs over N (B^T is MN-major in shared memory: B's rows are contiguous
 //     in n), the MMA's N = Mp (M rounded up to 16) runs over M (A is K-major);
 //     the accumulator holds 128 n-lanes x Mp fp32 columns in TMEM;
-//   * split-K over a thread-block cluster of S CTAs (S = 1, 2, 4 or 8): CTA r
+//   * split-K over a thread-block cluster of S CTAs (S = 1, 2, 4 or 8, the
+//     largest that keeps every cluster of the grid co-resident): CTA r
 //     of the cluster owns the same 128 columns of C and k-blocks
 //     [r*nkb/S, (r+1)*nkb/S), so n_tiles * S CTAs stream disjoint parts of B;
 //   * the S fp32 partials meet in distributed shared memory: each CTA writes
@@ -255,12 +256,31 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 
 std::mutex g_mu;
 bool g_attr_set[64][8];
+// Clusters of 2, 4 and 8 CTAs that can be resident at once, per device and
+// kernel instance (large clusters need whole free groups of SMs).
+int g_max_clusters[64][8][3];
+
+// Largest split s (1, 2, 4 or 8) such that n_tiles * s CTAs run as one wave
+// of co-resident clusters and every CTA keeps at least two k-blocks.
+int choose_split(long long n_tiles, int nkb, int num_sms, const int (&max_clusters)[3])
+{
+    int s = 1;
+    for (int i = 0; i < 3; ++i) {
+        const int t = 2 << i;
+        if (t > kMaxSplit || n_tiles * t > num_sms || n_tiles > max_clusters[i] ||
+            nkb < 2 * t)
+            break;
+        s = t;
+    }
+    return s;
+}
 
 template <int MP, bool OUT_F32>
-cudaError_t launch_cfg(const GemmArgs& a, int split)
+cudaError_t launch_cfg(const GemmArgs& a)
 {
     using Cfg = SkinnyCfg<MP>;
     auto kernel = gemm_skinny_kernel<MP, OUT_F32>;
+    int split = 1;
     {
         int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
@@ -272,8 +292,29 @@ cudaError_t launch_cfg(const GemmArgs& a, int split)
             e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(Cfg::SMEM));
             if (e != cudaSuccess) return e;
+            for (int i = 0; i < 3; ++i) {
+                cudaLaunchConfig_t q = {};
+                q.gridDim = dim3(2 << i, 1);
+                q.blockDim = dim3(kThreads);
+                q.dynamicSmemBytes = Cfg::SMEM;
+                cudaLaunchAttribute at[1];
+                at[0].id = cudaLaunchAttributeClusterDimension;
+                at[0].val.clusterDim.x = 2 << i;
+                at[0].val.clusterDim.y = 1;
+                at[0].val.clusterDim.z = 1;
+                q.attrs = at;
+                q.numAttrs = 1;
+                int n = 0;
+                if (cudaOccupancyMaxActiveClusters(&n, kernel, &q) != cudaSuccess) {
+                    cudaGetLastError();
+                    n = 0;
+                }
+                g_max_clusters[dev][slot][i] = n;
+            }
             g_attr_set[dev][slot] = true;
         }
+        split = choose_split((a.N + BNT - 1) / BNT, (a.K + BK - 1) / BK, a.num_sms,
+                             g_max_clusters[dev][slot]);
     }
     CUtensorMap ta, tbt;
     if (!encode_tmap_f16(&ta, a.A, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M),
@@ -301,34 +342,23 @@ cudaError_t launch_cfg(const GemmArgs& a, int split)
 
 }  // namespace
 
-int skinny_split(int M, int N, int K, int num_sms)
-{
-    (void)M;
-    const long long n_tiles = (N + BNT - 1) / BNT;
-    const int nkb = (K + BK - 1) / BK;
-    int s = 1;
-    while (s < kMaxSplit && n_tiles * (2 * s) <= num_sms && nkb >= 2 * (2 * s)) s *= 2;
-    return s;
-}
-
 cudaError_t launch_skinny(const GemmArgs& a)
 {
     if (a.M > kSkinnyMaxM) return cudaErrorInvalidValue;
-    const int split = skinny_split(a.M, a.N, a.K, a.num_sms);
     const int mp = (a.M + 15) / 16 * 16;
     if (a.out_f32) {
         switch (mp) {
-            case 16: return launch_cfg<16, true>(a, split);
-            case 32: return launch_cfg<32, true>(a, split);
-            case 48: return launch_cfg<48, true>(a, split);
-            default: return launch_cfg<64, true>(a, split);
+            case 16: return launch_cfg<16, true>(a);
+            case 32: return launch_cfg<32, true>(a);
+            case 48: return launch_cfg<48, true>(a);
+            default: return launch_cfg<64, true>(a);
         }
     }
     switch (mp) {
-        case 16: return launch_cfg<16, false>(a, split);
-        case 32: return launch_cfg<32, false>(a, split);
-        case 48: return launch_cfg<48, false>(a, split);
-        default: return launch_cfg<64, false>(a, split);
+        case 16: return launch_cfg<16, false>(a);
+        case 32: return launch_cfg<32, false>(a);
+        case 48: return launch_cfg<48, false>(a);
+        default: return launch_cfg<64, false>(a);
     }
 }
 

@@ -58,9 +58,8 @@ cudaError_t launch_skinny(const GemmArgs& a);
 // Tile width the main kernel uses for this problem (64, 128 or 256).
 int main_tile_n(int M, int N, int num_sms);
 
-// Largest M the skinny kernel serves, and its split-K factor (cluster size).
+// Largest M the skinny kernel serves.
 constexpr int kSkinnyMaxM = 64;
-int skinny_split(int M, int N, int K, int num_sms);
 
 // Number of 256 x 256 tiles the pair kernel would compute.
 int pair_tiles(int M, int N);
