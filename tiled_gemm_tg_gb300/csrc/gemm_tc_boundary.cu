@@ -9,8 +9,9 @@
 // and zero-filled, written by the threads themselves into the same 128-byte
 // swizzled shared-memory layout the TMA path produces, and fed to the same
 // tcgen05.mma (M=128, N=BN, K=16) with an fp32 accumulator in tensor memory.
-// Two shared-memory stages let the loads of k-block i+1 overlap the MMAs of
-// k-block i.  One CTA per 128 x BN output tile; 4 warps; stores predicated.
+// Each thread issues all its loads of k-block i+1 into registers while the
+// tensor core runs k-block i; two shared-memory stages.  One CTA per
+// 128 x BN output tile; 4 warps; stores predicated.
 #include <cstdint>
 #include <mutex>
 
@@ -35,20 +36,102 @@ constexpr uint32_t SMEM = 2 * STAGE + 1024;
 constexpr uint32_t TMEM_COLS = BN;
 constexpr int kThreads = 128;
 
-// 8 consecutive fp16 elements starting at p, with columns at or past `limit`
-// (relative index) read as zero.  Uses one 16-byte load when it can.
-__device__ __forceinline__ uint4 load8(const __half* p, int valid)
+// One k-block of operands held in registers: each thread's 8 chunks of the
+// A tile (128 rows x 8 chunks of 8 k) and 8 chunks of the B tile (64 k-rows x
+// BN/8 chunks of 8 n).  A chunk is either one 16-byte load (operand 16-byte
+// aligned, chunk in range) or eight 2-byte loads, each in its own register.
+// Every load of the k-block is issued before any value is used: the GPU
+// issues in order, so packing a value right after its load would stall the
+// thread before the next chunk's loads went out.
+constexpr int kChunksA = BM * (BK / 8) / kThreads;
+constexpr int kChunksB = BK * (BN / 8) / kThreads;
+static_assert(kChunksA * kThreads == BM * (BK / 8) && kChunksB * kThreads == BK * (BN / 8),
+              "tile chunks must divide evenly over the threads");
+
+struct Frag {
+    uint32_t a[kChunksA][8];
+    uint32_t b[kChunksB][8];
+    uint32_t wide;  // bit j: A chunk j was one 16-byte load; bit 8 + j: B chunk j
+};
+
+__device__ __forceinline__ void load_chunk(const __half* p, int valid, bool vec, uint32_t (&e)[8],
+                                           uint32_t& wide, uint32_t bit)
 {
-    if (valid >= 8 && (reinterpret_cast<uintptr_t>(p) & 15u) == 0)
-        return __ldg(reinterpret_cast<const uint4*>(p));
-    const unsigned short* q = reinterpret_cast<const unsigned short*>(p);
-    uint32_t w[4] = {0, 0, 0, 0};
+    if (vec && valid >= 8) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+        e[0] = v.x;
+        e[1] = v.y;
+        e[2] = v.z;
+        e[3] = v.w;
+        wide |= bit;
+    } else {
+        const unsigned short* q = reinterpret_cast<const unsigned short*>(p);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint32_t v = (i < valid) ? static_cast<uint32_t>(__ldg(q + i)) : 0u;
-        w[i >> 1] |= v << ((i & 1) * 16);
+        for (int i = 0; i < 8; ++i) e[i] = (i < valid) ? static_cast<uint32_t>(__ldg(q + i)) : 0u;
     }
-    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ uint4 pack_chunk(const uint32_t (&e)[8], bool wide)
+{
+    if (wide) return make_uint4(e[0], e[1], e[2], e[3]);
+    return make_uint4(e[0] | (e[1] << 16), e[2] | (e[3] << 16), e[4] | (e[5] << 16),
+                      e[6] | (e[7] << 16));
+}
+
+__device__ __forceinline__ void fetch(Frag& f, const __half* __restrict__ A, long long lda,
+                                      bool a_vec, const __half* __restrict__ B, long long ldb,
+                                      bool b_vec, int M, int N, int K, int m0, int n0, int k0,
+                                      int tid)
+{
+    f.wide = 0;
+#pragma unroll
+    for (int j = 0; j < kChunksA; ++j) {
+        const int i = tid + j * kThreads;
+        const int r = i >> 3, c = i & 7;
+        const int m = m0 + r, k = k0 + c * 8;
+        if (m < M && k < K) {
+            load_chunk(A + static_cast<long long>(m) * lda + k, K - k, a_vec, f.a[j], f.wide,
+                       1u << j);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f.a[j][e] = 0;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < kChunksB; ++j) {
+        const int i = tid + j * kThreads;
+        const int kr = i / (BN / 8), c = i % (BN / 8);
+        const int k = k0 + kr, n = n0 + c * 8;
+        if (k < K && n < N) {
+            load_chunk(B + static_cast<long long>(k) * ldb + n, N - n, b_vec, f.b[j], f.wide,
+                       1u << (8 + j));
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f.b[j][e] = 0;
+        }
+    }
+}
+
+// Registers -> one stage, in the 128-byte swizzled layouts the TMA path
+// produces: A chunk (r, c) at row r, 16-byte slot c ^ (r % 8); B chunk
+// (kr, c) in 64-column box c / 8 (8 KB apart), row kr, slot (c % 8) ^ (kr % 8).
+__device__ __forceinline__ void stash(const Frag& f, uint8_t* sA, uint8_t* sB, int tid)
+{
+#pragma unroll
+    for (int j = 0; j < kChunksA; ++j) {
+        const int i = tid + j * kThreads;
+        const int r = i >> 3, c = i & 7;
+        *reinterpret_cast<uint4*>(sA + r * 128 + ((c ^ (r & 7)) << 4)) =
+            pack_chunk(f.a[j], (f.wide >> j) & 1u);
+    }
+#pragma unroll
+    for (int j = 0; j < kChunksB; ++j) {
+        const int i = tid + j * kThreads;
+        const int kr = i / (BN / 8), c = i % (BN / 8);
+        *reinterpret_cast<uint4*>(sB + (c >> 3) * (64 * 128) + kr * 128 +
+                                  (((c & 7) ^ (kr & 7)) << 4)) =
+            pack_chunk(f.b[j], (f.wide >> (8 + j)) & 1u);
+    }
 }
 
 template <bool OUT_F32>
@@ -57,6 +140,10 @@ gemm_tc_boundary_kernel(const __half* __restrict__ A, long long lda, const __hal
                         long long ldb, void* __restrict__ C, long long ldc, int M, int N, int K,
                         int hook, unsigned int* err)
 {
+    // An operand whose base and row stride are both 16-byte multiples is read
+    // with 16-byte loads (at most one of A and B is, or the TMA path serves).
+    const bool a_vec = (reinterpret_cast<uintptr_t>(A) & 15u) == 0 && (lda & 7) == 0;
+    const bool b_vec = (reinterpret_cast<uintptr_t>(B) & 15u) == 0 && (ldb & 7) == 0;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t mma_bar[2];
     __shared__ __align__(8) uint64_t drain_bar;
@@ -89,6 +176,9 @@ gemm_tc_boundary_kernel(const __half* __restrict__ A, long long lda, const __hal
     const int num_kb = (K + BK - 1) / BK;
     bool aborted = false;
 
+    // Registers carry k-block kb+1 while the tensor core works on k-block kb.
+    Frag f;
+    fetch(f, A, lda, a_vec, B, ldb, b_vec, M, N, K, m0, n0, 0, tid);
     for (int kb = 0; kb < num_kb; ++kb) {
         const int s = kb & 1;
         if (kb >= 2) {
@@ -100,29 +190,7 @@ gemm_tc_boundary_kernel(const __half* __restrict__ A, long long lda, const __hal
             }
         }
         uint8_t* sA = gbase + s * STAGE;
-        uint8_t* sB = sA + A_STAGE;
-        const int k0 = kb * BK;
-        // A tile: 128 rows x 8 chunks of 8 k; chunk (r, c) goes to row r of the
-        // K-major atom column, 16-byte slot c ^ (r % 8).
-#pragma unroll 2
-        for (int i = tid; i < BM * (BK / 8); i += kThreads) {
-            const int r = i >> 3, c = i & 7;
-            const int m = m0 + r, k = k0 + c * 8;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (m < M && k < K) v = load8(A + static_cast<long long>(m) * lda + k, K - k);
-            *reinterpret_cast<uint4*>(sA + r * 128 + ((c ^ (r & 7)) << 4)) = v;
-        }
-        // B tile: 64 k-rows x (BN/8) chunks of 8 n; 64-column box j = c / 8 sits
-        // at j * 8 KB, row kr at kr * 128 B, 16-byte slot (c % 8) ^ (kr % 8).
-#pragma unroll 2
-        for (int i = tid; i < BK * (BN / 8); i += kThreads) {
-            const int kr = i / (BN / 8), c = i % (BN / 8);
-            const int k = k0 + kr, n = n0 + c * 8;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (k < K && n < N) v = load8(B + static_cast<long long>(k) * ldb + n, N - n);
-            *reinterpret_cast<uint4*>(sB + (c >> 3) * (64 * 128) + kr * 128 +
-                                      (((c & 7) ^ (kr & 7)) << 4)) = v;
-        }
+        stash(f, sA, sA + A_STAGE, tid);
         fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
         __syncthreads();
         if (tid == 0) {
@@ -136,6 +204,8 @@ gemm_tc_boundary_kernel(const __half* __restrict__ A, long long lda, const __hal
             // test hook: skip the first commit, so the bounded wait on it runs out
             if (!(hook == 1 && kb == 0)) umma_commit(smem_u32(&mma_bar[s]));
         }
+        if (kb + 1 < num_kb)
+            fetch(f, A, lda, a_vec, B, ldb, b_vec, M, N, K, m0, n0, (kb + 1) * BK, tid);
     }
 
     if (!aborted) {
