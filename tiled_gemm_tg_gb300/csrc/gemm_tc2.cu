@@ -69,6 +69,10 @@ static_assert(TMEM_COLS == 512, "two 256-column accumulators fill TMEM");
 #define TG_PAIR_L2_HINTS 1
 #endif
 constexpr int L2_HINTS = TG_PAIR_L2_HINTS;  // bit 0: A evict_last, bit 1: B evict_first
+#ifndef TG_PAIR_EPI_COLS
+#define TG_PAIR_EPI_COLS 32
+#endif
+constexpr int EPI_COLS = TG_PAIR_EPI_COLS;  // accumulator columns per tcgen05.ld
 
 template <bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -264,12 +268,17 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * PN);
 #pragma unroll 1
-            for (int c = 0; c < PN; c += 32) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(taddr + c, r);
+            for (int c = 0; c < PN; c += EPI_COLS) {
+                uint32_t r[EPI_COLS];
+                if constexpr (EPI_COLS == 128) tmem_ld_32x32b_x128(taddr + c, r);
+                else if constexpr (EPI_COLS == 64) tmem_ld_32x32b_x64(taddr + c, r);
+                else tmem_ld_32x32b_x32(taddr + c, *reinterpret_cast<uint32_t(*)[32]>(r));
                 tmem_ld_wait();
-                const int n = tn * PN + c;
-                if (m < M && n < N) store_chunk<OUT_F32>(C, ldc, m, n, N, r, c_vec != 0);
+#pragma unroll
+                for (int j = 0; j < EPI_COLS; j += 32) {
+                    const int n = tn * PN + c + j;
+                    if (m < M && n < N) store_chunk<OUT_F32>(C, ldc, m, n, N, r + j, c_vec != 0);
+                }
             }
             tc_fence_before();
             mbar_arrive_cluster(tempty0 + 8u * static_cast<uint32_t>(acc));

@@ -23,9 +23,11 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
     tn = r / gs;
 }
 
+// Stores 32 consecutive fp32 accumulator values r[0..31] of row m, columns
+// n..n+31, converted to the output type; columns >= N are skipped.
 template <bool OUT_F32>
 __device__ __forceinline__ void store_chunk(void* C, long long ldc, int m, int n, int N,
-                                            const uint32_t (&r)[32], bool vec)
+                                            const uint32_t* r, bool vec)
 {
     if constexpr (OUT_F32) {
         float* row = static_cast<float*>(C) + static_cast<long long>(m) * ldc + n;
