@@ -145,6 +145,19 @@ void tg_gemm_force_path(int path);
  */
 void tg_gemm_test_hook(int hook);
 
+/*
+ * Tiling override, for configuration sweeps, tests and benchmarks (the
+ * pages' tuning harness: block sizes and rasterisation, screened per shape).
+ *   bn       tile width of the one-CTA kernel (path 3): 64, 128 or 256
+ *            (with 8, 6 or 4 pipeline stages); 0 = chosen per problem.
+ *   group_m  height, in tile rows, of the grouped tile order of the one-CTA
+ *            and pair kernels (1..64); 0 = each kernel's default (16 for
+ *            128-row tiles, 8 for 256-row pair tiles).
+ * Process-wide; stays in force until changed.  Returns TG_ERR_INVALID_ARG
+ * (and changes nothing) for any other value.
+ */
+tg_status tg_gemm_force_tiling(int bn, int group_m);
+
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int tg_gemm_version(void);
 

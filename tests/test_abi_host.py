@@ -38,7 +38,8 @@ def declared_functions():
 def test_header_declares_the_abi():
     names = declared_functions()
     for must in ["tg_gemm", "tg_gemm_check", "tg_status_string", "tg_gemm_path",
-                 "tg_gemm_force_path", "tg_gemm_test_hook", "tg_gemm_version"]:
+                 "tg_gemm_force_path", "tg_gemm_force_tiling", "tg_gemm_test_hook",
+                 "tg_gemm_version"]:
         assert must in names
 
 
@@ -164,6 +165,16 @@ def test_forced_paths():
     finally:
         tg.tg_gemm_force_path(0)
     assert path(1024, 2048, 512) == 3
+
+
+def test_force_tiling_validates():
+    try:
+        for bn, g in [(0, 0), (64, 1), (128, 8), (256, 64)]:
+            assert tg.tg_gemm_force_tiling(bn, g) == tg.TG_OK
+        for bn, g in [(96, 0), (512, 0), (-1, 0), (0, -1), (0, 65)]:
+            assert tg.tg_gemm_force_tiling(bn, g) == tg.TG_ERR_INVALID_ARG
+    finally:
+        assert tg.tg_gemm_force_tiling(0, 0) == tg.TG_OK
 
 
 def test_product_path_never_imports_oracle():

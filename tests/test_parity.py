@@ -372,6 +372,26 @@ def test_one_cta_kernel_on_the_square_shape():
     _sampled_check(a, b, got, True, 43, extra_rows=(8191,), extra_cols=(8191,))
 
 
+@pytest.mark.parametrize("path,bn,group", [(MAIN, 64, 1), (MAIN, 128, 3), (MAIN, 256, 64),
+                                           (PAIR, 0, 1), (PAIR, 0, 5), (PAIR, 0, 64)])
+def test_forced_tilings(path, bn, group):
+    """Every tile width and raster height the sweep can choose computes the
+    same product (ragged shape, several tiles in each direction)."""
+    a = inputs.draw((1100, 700), "int2", 8901, "f16")
+    b = inputs.draw((700, 1400), "int2", 8902, "f16")
+    tg.tg_gemm_force_path(path)
+    assert tg.tg_gemm_force_tiling(bn, group) == tg.TG_OK
+    try:
+        got, intact, p = run(a, b, torch.float16, lda=704, ldb=1400)
+    finally:
+        tg.tg_gemm_force_path(0)
+        tg.tg_gemm_force_tiling(0, 0)
+    assert p == path and intact
+    C_ref, _ = oracle.gemm(a.numpy(), b.numpy())
+    have = torch.from_numpy(got).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(have, f16_bits_of(C_ref))
+
+
 def test_stream_argument_is_honoured():
     s = torch.cuda.Stream()
     a = inputs.draw((640, 384), "normal", 7701, "f16")

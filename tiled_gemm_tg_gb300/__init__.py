@@ -17,7 +17,8 @@ import threading
 __all__ = [
     "F16", "F32", "TG_OK", "TG_ERR_INVALID_ARG", "TG_ERR_UNSUPPORTED", "TG_ERR_CUDA",
     "TG_ERR_TIMEOUT", "PATHS", "TgError", "lib", "library_path", "tg_gemm", "tg_gemm_check",
-    "tg_status_string", "tg_gemm_path", "tg_gemm_force_path", "tg_gemm_test_hook",
+    "tg_status_string", "tg_gemm_path", "tg_gemm_force_path", "tg_gemm_force_tiling",
+    "tg_gemm_test_hook",
     "tg_gemm_version", "gemm",
     "check",
 ]
@@ -70,6 +71,8 @@ def lib() -> ctypes.CDLL:
         L.tg_gemm_path.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, i32]
         L.tg_gemm_force_path.restype = None
         L.tg_gemm_force_path.argtypes = [i32]
+        L.tg_gemm_force_tiling.restype = i32
+        L.tg_gemm_force_tiling.argtypes = [i32, i32]
         L.tg_gemm_test_hook.restype = None
         L.tg_gemm_test_hook.argtypes = [i32]
         L.tg_gemm_version.restype = i32
@@ -100,6 +103,10 @@ def tg_gemm_path(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype) -> int:
 
 def tg_gemm_force_path(path: int) -> None:
     lib().tg_gemm_force_path(int(path))
+
+
+def tg_gemm_force_tiling(bn: int, group_m: int) -> int:
+    return int(lib().tg_gemm_force_tiling(int(bn), int(group_m)))
 
 
 def tg_gemm_test_hook(hook: int) -> None:

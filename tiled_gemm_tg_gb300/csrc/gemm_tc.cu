@@ -303,7 +303,7 @@ cudaError_t launch_cfg(const GemmArgs& a)
     const int tiles_n = (a.N + BN - 1) / BN;
     const int total = tiles_m * tiles_n;
     const int grid = total < a.num_sms ? total : a.num_sms;
-    const int group_m = 16;
+    const int group_m = a.group_m > 0 ? a.group_m : 16;
     const size_t es = OUT_F32 ? 4 : 2;
     const int c_vec = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) &&
                       ((static_cast<size_t>(a.ldc) * es) % 16 == 0);

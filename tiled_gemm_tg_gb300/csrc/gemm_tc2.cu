@@ -345,7 +345,7 @@ cudaError_t launch_cfg(const GemmArgs& a)
     const int tiles_n = (a.N + PN - 1) / PN;
     const int total = tiles_m * tiles_n;
     const int pairs = total < max_clusters ? total : max_clusters;
-    const int group_m = 8;
+    const int group_m = a.group_m > 0 ? a.group_m : 8;
     const size_t es = OUT_F32 ? 4 : 2;
     const int c_vec = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) &&
                       ((static_cast<size_t>(a.ldc) * es) % 16 == 0);

@@ -38,6 +38,8 @@ std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 std::atomic<int> g_force_path{0};
 std::atomic<int> g_test_hook{0};
+std::atomic<int> g_force_bn{0};
+std::atomic<int> g_force_group{0};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 tg_status device_state(DeviceState** out)
@@ -208,13 +210,18 @@ tg_status tg_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, c
     a.out_f32 = (out_dtype == TG_F32);
     a.err = ds->err;
     a.hook = g_test_hook.load(std::memory_order_relaxed);
+    a.group_m = g_force_group.load(std::memory_order_relaxed);
     a.num_sms = ds->num_sms;
     a.stream = s;
 
     cudaError_t e = cudaSuccess;
     switch (path) {
         case tg::PATH_SIMT: e = tg::launch_simt_f32(a); break;
-        case tg::PATH_MAIN: e = tg::launch_main(a, tg::main_tile_n(a.M, a.N, a.num_sms)); break;
+        case tg::PATH_MAIN: {
+            const int bn = g_force_bn.load(std::memory_order_relaxed);
+            e = tg::launch_main(a, bn != 0 ? bn : tg::main_tile_n(a.M, a.N, a.num_sms));
+            break;
+        }
         case tg::PATH_BOUNDARY: e = tg::launch_boundary(a); break;
         case tg::PATH_MAIN_PAIR: e = tg::launch_main_pair(a); break;
         case tg::PATH_SKINNY: e = tg::launch_skinny(a); break;
@@ -273,6 +280,15 @@ void tg_gemm_force_path(int path)
 }
 
 void tg_gemm_test_hook(int hook) { g_test_hook.store(hook == 1 ? 1 : 0, std::memory_order_relaxed); }
+
+tg_status tg_gemm_force_tiling(int bn, int group_m)
+{
+    if (!(bn == 0 || bn == 64 || bn == 128 || bn == 256)) return TG_ERR_INVALID_ARG;
+    if (group_m < 0 || group_m > 64) return TG_ERR_INVALID_ARG;
+    g_force_bn.store(bn, std::memory_order_relaxed);
+    g_force_group.store(group_m, std::memory_order_relaxed);
+    return TG_OK;
+}
 
 int tg_gemm_version(void) { return 100; }
 

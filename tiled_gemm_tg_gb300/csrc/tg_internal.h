@@ -39,6 +39,7 @@ struct GemmArgs {
     bool out_f32;
     unsigned int* err;  // device error word
     int hook;           // test hook (0 = off), see tg_gemm_test_hook
+    int group_m;        // grouped tile-order height, 0 = the kernel's default
     int num_sms;
     cudaStream_t stream;
 };

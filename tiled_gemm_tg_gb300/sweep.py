@@ -1,0 +1,147 @@
+"""Configuration sweep: time every kernel configuration the library can run
+for given GEMM shapes and report the fastest (the tuning harness of the
+pages: block sizes, pipeline depth and rasterisation screened per shape).
+
+Configurations: the CTA-pair kernel (256 x 256 tiles, k-block 128, three
+stages) with grouped tile orders of 2..32 tile rows; the one-CTA kernel with
+128 x 64 / 128 x 128 / 128 x 256 tiles (8 / 6 / 4 stages of k-block 64) and
+group heights 4..32; the skinny kernel when M <= 64.  Each configuration is
+forced through tg_gemm_force_path / tg_gemm_force_tiling, launched `reps`
+times from one CUDA graph over operand sets rotated past L2, and timed with
+CUDA events.
+
+    python -m tiled_gemm_tg_gb300.sweep --shapes 1024x1024x1024,8192x8192x8192
+"""
+from __future__ import annotations
+
+import argparse
+import json
+
+import tiled_gemm_tg_gb300 as tg
+
+PAIR, MAIN, SKINNY = 6, 3, 5
+L2_BYTES = 129 * 2**20
+
+
+def candidates(M: int, N: int, K: int):
+    out = [(PAIR, 0, g) for g in (2, 4, 8, 16, 32)]
+    out += [(MAIN, bn, g) for bn in (64, 128, 256) for g in (4, 8, 16, 32)]
+    if M <= 64:
+        out.append((SKINNY, 0, 0))
+    return out
+
+
+def time_config(M, N, K, path, bn, group, reps=50, sets=None):
+    """Microseconds per launch (CUDA-graph replay), or None if not served."""
+    import torch
+
+    if sets is None:
+        sets = make_sets(M, N, K)
+    a0, b0, c0 = sets[0]
+    tg.tg_gemm_force_path(path)
+    if tg.tg_gemm_force_tiling(bn, group) != tg.TG_OK:
+        tg.tg_gemm_force_path(0)
+        return None
+    try:
+        if tg.tg_gemm_path(M, N, K, a0.data_ptr(), K, b0.data_ptr(), N, c0.data_ptr(), N,
+                           tg.F16, tg.F16) != path:
+            return None
+
+        def launch(i, h):
+            a, b, c = sets[i % len(sets)]
+            st = tg.tg_gemm(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N,
+                            tg.F16, tg.F16, h)
+            if st != tg.TG_OK:
+                raise tg.TgError(st)
+
+        h = torch.cuda.current_stream().cuda_stream
+        for i in range(3):
+            launch(i, h)
+        tg.check()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            hc = torch.cuda.current_stream().cuda_stream
+            for i in range(reps):
+                launch(i, hc)
+        g.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        tg.check()
+        return e0.elapsed_time(e1) * 1e3 / reps
+    finally:
+        tg.tg_gemm_force_path(0)
+        tg.tg_gemm_force_tiling(0, 0)
+
+
+def make_sets(M, N, K):
+    import torch
+
+    dev = torch.device("cuda")
+    set_bytes = (M * K + K * N + M * N) * 2
+    n = max(2, min(64, -(-3 * L2_BYTES // set_bytes)))
+    g = torch.Generator(device=dev).manual_seed(7)
+    return [((torch.rand(M, K, device=dev, generator=g) * 2 - 1).half(),
+             (torch.rand(K, N, device=dev, generator=g) * 2 - 1).half(),
+             torch.empty(M, N, dtype=torch.half, device=dev)) for _ in range(n)]
+
+
+def sweep(shapes, reps=50):
+    import torch
+
+    torch.cuda.set_device(0)
+    results = []
+    for (M, N, K) in shapes:
+        sets = make_sets(M, N, K)
+        a0, b0, c0 = sets[0]
+        auto_path = tg.tg_gemm_path(M, N, K, a0.data_ptr(), K, b0.data_ptr(), N, c0.data_ptr(),
+                                    N, tg.F16, tg.F16)
+        auto_us = time_config(M, N, K, auto_path, 0, 0, reps, sets)
+        rows = []
+        for path, bn, group in candidates(M, N, K):
+            us = time_config(M, N, K, path, bn, group, reps, sets)
+            if us is not None:
+                rows.append({"path": path, "bn": bn, "group_m": group, "us": us,
+                             "tflops": 2.0 * M * N * K / (us * 1e-6) / 1e12})
+        best = min(rows, key=lambda r: r["us"])
+        results.append({"shape": [M, N, K], "auto_path": auto_path, "auto_us": auto_us,
+                        "best": best, "configs": rows})
+        del sets
+        torch.cuda.empty_cache()
+    return results
+
+
+def parse_shapes(text: str):
+    return [tuple(int(v) for v in s.lower().split("x")) for s in text.split(",") if s]
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--shapes", default="1024x1024x1024,1024x2048x512,4096x4096x4096,"
+                                        "8192x8192x8192,4096x16384x4096")
+    ap.add_argument("--reps", type=int, default=50)
+    ap.add_argument("--json", default="")
+    args = ap.parse_args()
+    res = sweep(parse_shapes(args.shapes), args.reps)
+    names = {PAIR: "pair 256x256", MAIN: "one-CTA 128x{bn}", SKINNY: "skinny"}
+    for r in res:
+        M, N, K = r["shape"]
+        print(f"\n{M}x{N}x{K}: automatic path {r['auto_path']} {r['auto_us']:.1f} us; "
+              f"best {names[r['best']['path']].format(bn=r['best']['bn'])} "
+              f"group {r['best']['group_m']} {r['best']['us']:.1f} us")
+        print("| config | group_m | us | TFLOP/s |")
+        print("|---|---|---|---|")
+        for c in sorted(r["configs"], key=lambda c: c["us"]):
+            print(f"| {names[c['path']].format(bn=c['bn'])} | {c['group_m'] or '-'} | "
+                  f"{c['us']:.1f} | {c['tflops']:.0f} |")
+    if args.json:
+        with open(args.json, "w") as f:
+            json.dump(res, f, indent=1)
+
+
+if __name__ == "__main__":
+    main()
