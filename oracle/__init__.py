@@ -58,6 +58,9 @@ def _bind(path: str):
     lib.tgo_gemm.restype = ctypes.c_int
     lib.tgo_gemm.argtypes = [i64, i64, i64, vp, i64, vp, i64, ctypes.c_int,
                              vp, vp, ctypes.c_int]
+    lib.tgo_epilogue.restype = ctypes.c_int
+    lib.tgo_epilogue.argtypes = [i64, i64, vp, ctypes.c_double, ctypes.c_double, vp, i64,
+                                 ctypes.c_int, vp, ctypes.c_int, vp]
     lib.tgo_gemm_at.restype = ctypes.c_int
     lib.tgo_gemm_at.argtypes = [i64, i64, i64, vp, i64, vp, i64, ctypes.c_int,
                                 i64, vp, vp, vp, vp, ctypes.c_int]
@@ -155,6 +158,25 @@ class Oracle:
         return C, S
 
 
+    def epilogue(self, C: np.ndarray, alpha=1.0, beta=0.0, cin=None, bias=None, act=0):
+        """act(alpha * C + beta * Cin + bias[j]) in fp64 (C: the oracle's M x N
+        product; cin: M x N fp16/fp32 array or None; bias: N values or None)."""
+        C = np.ascontiguousarray(C, dtype=np.float64)
+        M, N = C.shape
+        out = np.empty((M, N), dtype=np.float64)
+        cin_ptr, ldcin, code = None, max(N, 1), F32
+        if cin is not None:
+            cin, code, ldcin = _operand(cin)
+            cin_ptr = cin.ctypes.data
+        b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+        rc = self.lib.tgo_epilogue(M, N, C.ctypes.data, float(alpha), float(beta), cin_ptr,
+                                   ldcin, code, None if b is None else b.ctypes.data, int(act),
+                                   out.ctypes.data)
+        if rc != 0:
+            raise RuntimeError("oracle rejected its arguments")
+        return out
+
+
 def _default() -> Oracle:
     global _lib
     with _lock:
@@ -183,6 +205,10 @@ def gemm_at(a, b, rows, cols, nthreads: int = 0):
     return _default().gemm_at(a, b, rows, cols, nthreads)
 
 
+def epilogue(C, alpha=1.0, beta=0.0, cin=None, bias=None, act=0):
+    return _default().epilogue(C, alpha, beta, cin, bias, act)
+
+
 def tolerance(C_ref: np.ndarray, S: np.ndarray, out_f16: bool) -> np.ndarray:
     """Per-element acceptance bound for a kernel result against the oracle.
 
@@ -194,3 +220,19 @@ def tolerance(C_ref: np.ndarray, S: np.ndarray, out_f16: bool) -> np.ndarray:
     if out_f16:
         tol = tol + 1e-2 * np.abs(C_ref)
     return tol
+
+
+def epilogue_tolerance(out_ref, S, alpha, beta, cin, bias, out_f16: bool):
+    """Bound for a fused result act(alpha*AB + beta*Cin + bias): the product's
+    bound scaled by |alpha|, fp32 rounding of the other terms, all carried
+    through an activation whose slope is at most 1.13 (ReLU 1, GELU
+    max d/dx x*Phi(x) = 1.129), plus 1e-2 relative for an fp16 output."""
+    t = abs(alpha) * (2e-3 * S + 1e-5)
+    if cin is not None and beta != 0.0:
+        t = t + 1e-6 * np.abs(beta * np.asarray(cin, dtype=np.float64))
+    if bias is not None:
+        t = t + 1e-6 * np.abs(np.asarray(bias, dtype=np.float64))[None, :]
+    t = 1.13 * t + 1e-6
+    if out_f16:
+        t = t + 1e-2 * np.abs(out_ref)
+    return t

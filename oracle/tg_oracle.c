@@ -32,7 +32,10 @@
  * 4x4 integer example (tests/golden), the 8x8 all-ones example of the
  * TileLang实战 page §6.2, closed forms (identity, all-ones, diagonal), the
  * transpose invariant (AB)^T = B^T A^T bitwise, and NumPy fp64 matmul on
- * exactly representable inputs.
+ * exactly representable inputs.  The fused epilogue is pinned by the block
+ * identity alpha*AB + beta*D + 1 bias^T = [alpha*A | beta*I | 1] [B; D; bias^T]
+ * evaluated by NumPy, by x * Phi(x) against SciPy's normal distribution
+ * function, and by the odd-part identities f(x) - f(-x) = x of ReLU and GELU.
  */
 #include <math.h>
 #include <stdint.h>
@@ -202,5 +205,40 @@ int tgo_gemm_at(int64_t M, int64_t N, int64_t K,
         S[t] = s;
     }
     (void)nthreads;
+    return 0;
+}
+
+/*
+ * Fused epilogue, applied to a product computed above:
+ *     out[i,j] = act(alpha * C[i,j] + beta * Cin[i,j] + bias[j])
+ * with act = identity (0), ReLU max(x, 0) (1), or GELU (2) in its defining
+ * form x * Phi(x) = 0.5 * x * (1 + erf(x / sqrt(2))), Phi the standard
+ * normal distribution function.  This is the multi-operator fusion that
+ * "企业官网建设流程全解析" (cf-1.com), §6.2, lists as the next direction after
+ * the plain GEMM kernel (merging operators into one kernel to save launches
+ * and memory round trips).  The pages give no formula for it, so the terms
+ * are the usual GEMM epilogue ones with their textbook definitions, applied
+ * in the order written.  C is dense M x N fp64 (the oracle's product); Cin is
+ * M x N of element type cin_dtype with row stride ldcin (may be NULL when
+ * beta == 0, and is then never read); bias holds N fp32 values (or NULL).
+ * Everything is evaluated in fp64.  Returns 0, or -1 on a bad argument.
+ */
+int tgo_epilogue(int64_t M, int64_t N, const double* C, double alpha, double beta,
+                 const void* Cin, int64_t ldcin, int cin_dtype, const float* bias, int act,
+                 double* out)
+{
+    if (M < 0 || N < 0 || act < 0 || act > 2) return -1;
+    if (beta != 0.0 && (!Cin || ldcin < N || (cin_dtype != TGO_F16 && cin_dtype != TGO_F32)))
+        return -1;
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            double y = alpha * C[i * N + j];
+            if (beta != 0.0) y += beta * load_elem(Cin, i * ldcin + j, cin_dtype);
+            if (bias) y += (double)bias[j];
+            if (act == 1) y = y > 0.0 ? y : 0.0;
+            else if (act == 2) y = 0.5 * y * (1.0 + erf(y / sqrt(2.0)));
+            out[i * N + j] = y;
+        }
+    }
     return 0;
 }

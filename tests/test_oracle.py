@@ -203,10 +203,73 @@ def pin_degenerate(o: Oracle):
     assert C.shape == (0, 5)
 
 
+# ----------------------------------------------------- fused epilogue pins
+
+def pin_epilogue_plain(o: Oracle):
+    # alpha 1, beta 0, no bias, no activation: the product itself, bit for bit
+    rng = np.random.default_rng(8)
+    C = rng.standard_normal((9, 14))
+    assert np.array_equal(o.epilogue(C), C)
+
+
+def pin_epilogue_block_identity(o: Oracle):
+    # alpha*A@B + beta*D + 1 bias^T is the product of the block matrices
+    # [alpha*A | beta*I_M | 1] and [B; D; bias^T]; with small integers and
+    # power-of-two scales every term is exact in fp64.  M != N, so a bias
+    # indexed by row or a transposed D cannot pass; D is a strided view.
+    rng = np.random.default_rng(9)
+    M, N, K = 11, 17, 23
+    a = rng.integers(-3, 4, (M, K)).astype(np.float16)
+    b = rng.integers(-3, 4, (K, N)).astype(np.float16)
+    big = rng.integers(-4, 5, (M + 2, N + 9)).astype(np.float16)
+    d = big[1:M + 1, 4:N + 4]
+    bias = rng.integers(-5, 6, N).astype(np.float32)
+    alpha, beta = 0.75, -1.5
+    C, _ = o.gemm(a, b)
+    got = o.epilogue(C, alpha, beta, d, bias, act=0)
+    left = np.hstack([alpha * a.astype(np.float64), beta * np.eye(M), np.ones((M, 1))])
+    right = np.vstack([b.astype(np.float64), d.astype(np.float64), bias[None, :].astype(np.float64)])
+    assert np.array_equal(got, left @ right)
+    # the same with an fp32 D and no bias: the bias row drops out
+    d32 = rng.integers(-4, 5, (M, N)).astype(np.float32)
+    got = o.epilogue(C, alpha, beta, d32, None, act=0)
+    assert np.array_equal(got, np.hstack([alpha * a.astype(np.float64), beta * np.eye(M)]) @
+                          np.vstack([b.astype(np.float64), d32.astype(np.float64)]))
+
+
+def pin_gelu_normal_cdf(o: Oracle):
+    # GELU(x) = x * Phi(x); Phi from SciPy's ndtr (an independent routine).
+    # Phi(0) = 1/2 exactly, so GELU(0) = 0; Phi(1) = 0.8413447460685429...
+    special = pytest.importorskip("scipy.special")
+    x = np.concatenate([np.linspace(-8, 8, 161), [-1.0, 0.0, 1.0, 1.959963984540054]])
+    got = o.epilogue(x[None, :], act=2)[0]
+    want = x * special.ndtr(x)
+    assert np.all(np.abs(got - want) <= 1e-15 * np.abs(x) + 1e-300)
+    assert got[-3] == 0.0
+    assert abs(got[-2] - 0.8413447460685429) < 1e-15
+
+
+def pin_activation_odd_parts(o: Oracle):
+    # Phi(x) + Phi(-x) = 1 gives GELU(x) - GELU(-x) = x; ReLU(x) - ReLU(-x) = x
+    # and ReLU(x) >= 0.  A flipped sign or a wrong erf scale breaks these.
+    rng = np.random.default_rng(10)
+    x = rng.standard_normal(500) * 3
+    for act in (1, 2):
+        p = o.epilogue(x[None, :], act=act)[0]
+        n = o.epilogue(-x[None, :], act=act)[0]
+        assert np.allclose(p - n, x, rtol=0, atol=1e-14 * (1 + np.abs(x)).max())
+    r = o.epilogue(x[None, :], act=1)[0]
+    assert np.all(r >= 0) and np.array_equal(r[x > 0], x[x > 0])
+    # GELU lies between min(x, 0) and max(x, 0)
+    g = o.epilogue(x[None, :], act=2)[0]
+    assert np.all(g <= np.maximum(x, 0) + 1e-15) and np.all(g >= np.minimum(x, 0) - 1e-15)
+
+
 PINS = [pin_decode_exhaustive, pin_decode_by_hand, pin_encode_ties, pin_encode_vs_numpy,
         pin_roundtrip, pin_gemm_4x4, pin_gemm_8x8_ones, pin_closed_forms, pin_transpose,
         pin_vs_numpy_exact, pin_vs_numpy_random, pin_leading_dims, pin_sampled,
-        pin_degenerate]
+        pin_degenerate, pin_epilogue_plain, pin_epilogue_block_identity, pin_gelu_normal_cdf,
+        pin_activation_odd_parts]
 
 
 @pytest.fixture(scope="module")
@@ -224,6 +287,18 @@ def test_tolerance_formula():
     S = np.array([3.0, 4.0, 5.0])
     assert np.allclose(oracle.tolerance(C, S, False), 2e-3 * S + 1e-5)
     assert np.allclose(oracle.tolerance(C, S, True), 2e-3 * S + 1e-5 + 1e-2 * np.abs(C))
+
+
+def test_epilogue_tolerance_terms():
+    out = np.array([[2.0, -1.0]])
+    S = np.array([[4.0, 8.0]])
+    plain = oracle.epilogue_tolerance(out, S, 1.0, 0.0, None, None, False)
+    assert np.allclose(plain, 1.13 * (2e-3 * S + 1e-5) + 1e-6)
+    scaled = oracle.epilogue_tolerance(out, S, -2.0, 0.5, np.array([[4.0, 0.0]]),
+                                       np.array([1.0, 3.0]), True)
+    want = 1.13 * (2.0 * (2e-3 * S + 1e-5) + 1e-6 * np.array([[2.0, 0.0]]) +
+                   1e-6 * np.array([[1.0, 3.0]])) + 1e-6 + 1e-2 * np.abs(out)
+    assert np.allclose(scaled, want)
 
 
 def test_threads_reported(o):
@@ -244,6 +319,15 @@ MUTANTS = {
     "ignored_lda": ("double a = load_elem(A, i * lda + k, in_dtype);",
                     "double a = load_elem(A, i * K + k, in_dtype);"),
     "missing_abs": ("s[j] += fabs(p);", "s[j] += p;"),
+    "epilogue_alpha_dropped": ("double y = alpha * C[i * N + j];", "double y = C[i * N + j];"),
+    "epilogue_beta_sign": ("y += beta * load_elem(", "y -= beta * load_elem("),
+    "epilogue_ignored_ldcin": ("load_elem(Cin, i * ldcin + j, cin_dtype)",
+                               "load_elem(Cin, i * N + j, cin_dtype)"),
+    "epilogue_bias_by_row": ("y += (double)bias[j];", "y += (double)bias[i % N];"),
+    "epilogue_relu_min": ("y = y > 0.0 ? y : 0.0;", "y = y < 0.0 ? y : 0.0;"),
+    "epilogue_gelu_scale": ("erf(y / sqrt(2.0))", "erf(y * sqrt(2.0))"),
+    "epilogue_gelu_tanh": ("0.5 * y * (1.0 + erf(y / sqrt(2.0)))",
+                           "0.5 * y * (1.0 + tanh(0.7978845608 * (y + 0.044715 * y * y * y)))"),
     "transposed_b": ("Bd[k * N + j] = load_elem(B, k * ldb + j, in_dtype);",
                      "Bd[k * N + j] = load_elem(B, (j % K) * ldb + (k % N), in_dtype);"),
 }
