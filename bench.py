@@ -216,6 +216,14 @@ def run_reference(args, w):
     return 0
 
 
+# Fused epilogues the bench can time (tg_gemm_ex): C = act(alpha*AB + beta*D + bias).
+EPILOGUES = {
+    "none": None,
+    "bias_relu": dict(alpha=1.0, beta=0.0, bias=True, act=1),
+    "axpby_bias_gelu": dict(alpha=0.5, beta=1.0, bias=True, act=2),
+}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -226,6 +234,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--epilogue", default="none", choices=sorted(EPILOGUES),
+                    help="time tg_gemm_ex with this fused epilogue instead of tg_gemm")
     ap.add_argument("--graph", action="store_true",
                     help="replay the timed launches from one CUDA graph (for us-scale shapes)")
     args = ap.parse_args()
@@ -258,8 +268,15 @@ def main():
     out_code = tg.F16 if w.out_dtype == "f16" else tg.F32
     # Rotate enough operand sets that one pass over them is at least three
     # times the 129 MB L2 (two sets for the large shapes).
-    set_bytes = (w.M * w.K + w.K * w.N) * a_cpu.element_size() + w.M * w.N * (
-        2 if w.out_dtype == "f16" else 4)
+    epi = EPILOGUES[args.epilogue]
+    use_d = epi is not None and epi["beta"] != 0.0
+    use_bias = epi is not None and epi["bias"]
+    out_es = 2 if w.out_dtype == "f16" else 4
+    set_bytes = (w.M * w.K + w.K * w.N) * a_cpu.element_size() + w.M * w.N * out_es * (
+        2 if use_d else 1)
+    # D and bias for a fused epilogue, drawn on the host like the operands
+    d_cpu = inputs.draw((w.M, w.N), "normal", w.seed_base + 7, w.out_dtype) if use_d else None
+    bias_cpu = inputs.draw((1, w.N), "normal", w.seed_base + 8, "f32")[0] if use_bias else None
     n_sets = max(2, min(64, -(-3 * 129 * 2**20 // set_bytes)))
     sets = []
     for i in range(n_sets):
@@ -269,17 +286,27 @@ def main():
             a = a.clone()
             b = b.clone()
         c = torch.empty((w.M, w.N), dtype=out_dt, device=dev)
-        sets.append((a, b, c))
+        d = d_cpu.to(dev) if use_d else None
+        bias = bias_cpu.to(dev) if use_bias else None
+        sets.append((a, b, c, d, bias))
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
     M, N, K = w.M, w.N, w.K
 
-    def step(i, handle=None):
-        a, b, c = sets[i % n_sets]
-        st = tg.tg_gemm(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N, in_code,
-                        out_code, sh if handle is None else handle)
+    def call(a, b, c, d, bias, handle):
+        if epi is None:
+            st = tg.tg_gemm(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N, in_code,
+                            out_code, handle)
+        else:
+            st = tg.tg_gemm_ex(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N,
+                               in_code, out_code, epi["alpha"], epi["beta"],
+                               d.data_ptr() if use_d else 0, N,
+                               bias.data_ptr() if use_bias else 0, epi["act"], handle)
         if st != tg.TG_OK:
             raise tg.TgError(st)
+
+    def step(i, handle=None):
+        call(*sets[i % n_sets], sh if handle is None else handle)
 
     path = tg.tg_gemm_path(M, N, K, sets[0][0].data_ptr(), K, sets[0][1].data_ptr(), N,
                            sets[0][2].data_ptr(), N, in_code, out_code)
@@ -355,6 +382,8 @@ def main():
     a_h = a_cpu.pin_memory()
     b_h = b_cpu.pin_memory()
     c_h = [torch.empty((M, N), dtype=out_dt).pin_memory() for _ in range(2)]
+    d_h = d_cpu.pin_memory() if use_d else None
+    bias_h = bias_cpu.pin_memory() if use_bias else None
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     s_mm = stream
     ev = {name: [torch.cuda.Event() for _ in range(2)] for name in ("in", "mm", "out")}
@@ -362,20 +391,21 @@ def main():
 
     def e2e_step(i):
         slot = i % 2
-        a_d, b_d, c_d = sets[slot]
+        a_d, b_d, c_d, d_d, bias_d = sets[slot]
         if started[slot]:
             s_in.wait_event(ev["mm"][slot])  # the slot's previous GEMM has read A, B
         with torch.cuda.stream(s_in):
             a_d.copy_(a_h, non_blocking=True)
             b_d.copy_(b_h, non_blocking=True)
+            if use_d:
+                d_d.copy_(d_h, non_blocking=True)
+            if use_bias:
+                bias_d.copy_(bias_h, non_blocking=True)
         ev["in"][slot].record(s_in)
         s_mm.wait_event(ev["in"][slot])
         if started[slot]:
             s_mm.wait_event(ev["out"][slot])  # the slot's previous C has been read out
-        st = tg.tg_gemm(M, N, K, a_d.data_ptr(), K, b_d.data_ptr(), N, c_d.data_ptr(), N,
-                        in_code, out_code, s_mm.cuda_stream)
-        if st != tg.TG_OK:
-            raise tg.TgError(st)
+        call(a_d, b_d, c_d, d_d, bias_d, s_mm.cuda_stream)
         ev["mm"][slot].record(s_mm)
         s_out.wait_event(ev["mm"][slot])
         with torch.cuda.stream(s_out):
@@ -404,7 +434,7 @@ def main():
         e2e_ms = float(t.item())
     e2e_value = ws * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
     ein = a_cpu.element_size()
-    h2d = (M * K + K * N) * ein
+    h2d = (M * K + K * N) * ein + (M * N * out_es if use_d else 0) + (N * 4 if use_bias else 0)
     d2h = M * N * c_h[0].element_size()
 
     sampler.stop()
@@ -413,8 +443,10 @@ def main():
     peaks, peak_src = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     achieved = flops / (kern_ms * 1e-3) / 1e12
+    alg_bytes = w.algorithmic_bytes() + (M * N * out_es if use_d else 0) + (
+        N * 4 if use_bias else 0)
     traffic = None
-    rec = NCU_TRAFFIC.get(w.name)
+    rec = NCU_TRAFFIC.get(w.name) if epi is None else None
     if rec and rec.get("kernel_hash") == kernel_hash():
         traffic = rec["bytes"]
     roofline = {
@@ -426,8 +458,8 @@ def main():
         "kernel_ms": kern_ms,
         "peak_source": f"{peak_src} bf16 burst (torch.matmul 8192^3) x 1.0 fp16/bf16 nominal ratio",
         "frac_of_nominal_2500": achieved / NOMINAL_FP16_DENSE_TFLOPS,
-        "algorithmic_bytes": w.algorithmic_bytes(),
-        "achieved_gbs": w.algorithmic_bytes() / (kern_ms * 1e-3) / 1e9,
+        "algorithmic_bytes": alg_bytes,
+        "achieved_gbs": alg_bytes / (kern_ms * 1e-3) / 1e9,
     }
 
     cpu = None
@@ -446,6 +478,8 @@ def main():
             "config": {"workload": w.name, "M": M, "N": N, "K": K, "in_dtype": w.in_dtype,
                        "accum": "f32", "out_dtype": w.out_dtype, "dist": w.dist,
                        "path": tg.PATHS.get(path, str(path)),
+                       "epilogue": args.epilogue if epi is None else
+                       f"{args.epilogue}: C = act(alpha*AB + beta*D + bias), {epi}",
                        "l2": f"{n_sets} rotating A/B/C sets, {n_sets * set_bytes / 2**20:.0f} MB "
                              "per pass (> L2)",
                        "timing": "CUDA graph replay" if graph is not None else "stream launches",
@@ -453,7 +487,8 @@ def main():
             "clocks": clocks,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                    "pipeline": "H2D / tg_gemm / D2H on three streams, two device buffer sets"},
+                    "pipeline": "H2D / tg_gemm{} / D2H on three streams, two device buffer "
+                                "sets".format("" if epi is None else "_ex")},
             "gpu_launches": args.steps,
             "roofline": roofline,
             "cpu_baseline": cpu,

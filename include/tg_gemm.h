@@ -78,8 +78,9 @@ typedef enum {
  * Errors (checked on the host before anything is enqueued; nothing is
  * written when an error is returned):
  *   TG_ERR_INVALID_ARG  a negative size; a NULL pointer that would be read
- *                       or written; lda < K, ldb < N or ldc < N; or the byte
- *                       span of C overlapping the span of A or of B.
+ *                       or written; a pointer that is not a multiple of its
+ *                       element size; lda < K, ldb < N or ldc < N; or the
+ *                       byte span of C overlapping the span of A or of B.
  *   TG_ERR_UNSUPPORTED  an unsupported dtype pair, or a size above 2^31 - 1024.
  *   TG_ERR_CUDA         a CUDA call made while launching failed.
  *
@@ -99,6 +100,61 @@ tg_status tg_gemm(int64_t M, int64_t N, int64_t K,
                   void* C, int64_t ldc,
                   tg_dtype in_dtype, tg_dtype out_dtype,
                   tg_stream_t stream);
+
+/* Activation of the fused epilogue (tg_gemm_ex). */
+typedef enum {
+    TG_ACT_NONE = 0, /* identity */
+    TG_ACT_RELU = 1, /* max(x, 0) */
+    TG_ACT_GELU = 2  /* x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)), Phi the
+                        standard normal distribution function (exact form,
+                        not the tanh approximation) */
+} tg_activation;
+
+/*
+ * tg_gemm_ex -- C = act(alpha * (A x B) + beta * D + bias), a GEMM with a
+ * fused epilogue.
+ *
+ * Source: "企业官网建设流程全解析" (cf-1.com, a TileLang article), §6.2, names
+ * multi-operator fusion -- merging several operators into one kernel to save
+ * launches and memory round trips -- as the next direction after the GEMM
+ * kernel of its §3.3.  The pages give no formula, so the terms are the usual
+ * GEMM epilogue ones with their textbook definitions.
+ *
+ * Arguments M..out_dtype and stream are those of tg_gemm; in addition
+ *   alpha  scale of the product (fp32).
+ *   beta   scale of D (fp32).  D is read only when beta != 0.
+ *   D      device pointer, M rows of N elements of out_dtype, row i at
+ *          D + i*ldd.  May be C itself (D == C and ldd == ldc: an in-place
+ *          C = alpha*AB + beta*C); may be NULL when beta == 0.
+ *   ldd    row stride of D in elements, ldd >= N when beta != 0.
+ *   bias   device pointer to N fp32 values added to every row (bias[j] to
+ *          column j), or NULL for none.
+ *   act    TG_ACT_NONE, TG_ACT_RELU or TG_ACT_GELU, applied last.
+ *
+ * Semantics: for every output element, y = alpha * acc + bias[j] + beta *
+ * D[i,j] in fp32, with acc the fp32-accumulated product; then act(y) is
+ * rounded to out_dtype (to nearest even for fp16).  A and B are read even
+ * when alpha == 0.  With alpha == 1, beta == 0, bias NULL and TG_ACT_NONE
+ * the call is tg_gemm, bit for bit.  K == 0 gives C = act(beta*D + bias).
+ * The epilogue runs in the same kernel as the product, on the accumulator
+ * before the output conversion, in every path (see tg_gemm_path: the path
+ * does not depend on the epilogue).
+ *
+ * Errors: those of tg_gemm, plus TG_ERR_INVALID_ARG for an act outside the
+ * enum; beta != 0 with D NULL, ldd < N, or D not a multiple of its element
+ * size; D overlapping C other than exactly in place; bias not 4-byte
+ * aligned or overlapping C.  Ownership, asynchrony and thread safety are as
+ * for tg_gemm; the library keeps no pointer after the call returns.
+ */
+tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K,
+                     const void* A, int64_t lda,
+                     const void* B, int64_t ldb,
+                     void* C, int64_t ldc,
+                     tg_dtype in_dtype, tg_dtype out_dtype,
+                     float alpha, float beta,
+                     const void* D, int64_t ldd,
+                     const float* bias, tg_activation act,
+                     tg_stream_t stream);
 
 /*
  * tg_gemm_check -- synchronize `stream`, then read and clear the current

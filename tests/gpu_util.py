@@ -114,3 +114,69 @@ def check_full(a, b, out_dtype=torch.float16, **kw):
 
 def f16_bits_of(x: np.ndarray) -> np.ndarray:
     return oracle.f64_to_f16_bits(x)
+
+
+class DevVector:
+    """n fp32 values at element offset `off` of a device buffer."""
+
+    def __init__(self, x: np.ndarray, off: int, device):
+        buf = torch.zeros(off + max(len(x), 1) + 16, dtype=torch.float32)
+        buf[off:off + len(x)] = torch.from_numpy(np.asarray(x, dtype=np.float32))
+        self.buf = buf.to(device)
+        self.ptr = self.buf.data_ptr() + off * 4
+
+
+def run_ex(a: torch.Tensor, b: torch.Tensor, out_dtype, alpha=1.0, beta=0.0, d=None,
+           bias=None, act=0, lda=None, ldb=None, ldc=None, ldd=None, offs=(0, 0, 0),
+           d_off=0, bias_off=0, in_place=False, device="cuda"):
+    """Run tg_gemm_ex through the C ABI: C = act(alpha*AB + beta*D + bias).
+
+    d: an M x N CPU tensor of the output dtype (or None); with in_place the
+    output buffer is first filled with d and passed as both C and D.
+    Returns (C float64, canaries intact, path)."""
+    M, K = a.shape
+    N = b.shape[1]
+    lda = K if lda is None else lda
+    ldb = N if ldb is None else ldb
+    ldc = N if ldc is None else ldc
+    A = DevMatrix(a, max(lda, 1), offs[0], device)
+    B = DevMatrix(b, max(ldb, 1), offs[1], device)
+    C = DevOutput(M, N, max(ldc, 1), offs[2], out_dtype, device)
+    d_ptr, ldd_v, keep = 0, max(N, 1), []
+    if d is not None:
+        if in_place:
+            body = C.buf[C.off + GUARD:C.off + GUARD + M * ldc].view(M, ldc)
+            body[:, :N] = d.to(device)
+            d_ptr, ldd_v = C.ptr, ldc
+        else:
+            ldd_v = N if ldd is None else ldd
+            D = DevMatrix(d, max(ldd_v, 1), d_off, device)
+            keep.append(D)
+            d_ptr = D.ptr
+    b_ptr = 0
+    if bias is not None:
+        bv = DevVector(bias, bias_off, device)
+        keep.append(bv)
+        b_ptr = bv.ptr
+    s = torch.cuda.current_stream()
+    path = tg.tg_gemm_path(M, N, K, A.ptr, lda, B.ptr, ldb, C.ptr, ldc, code(a.dtype),
+                           code(out_dtype))
+    st = tg.tg_gemm_ex(M, N, K, A.ptr, lda, B.ptr, ldb, C.ptr, ldc, code(a.dtype),
+                       code(out_dtype), alpha, beta, d_ptr, ldd_v, b_ptr, act, s.cuda_stream)
+    assert st == tg.TG_OK, tg.tg_status_string(st)
+    assert tg.tg_gemm_check(s.cuda_stream) == tg.TG_OK
+    got, intact = C.result()
+    return got, intact, path
+
+
+def compare_ex(got, out_ref, S, alpha, beta, d, bias, out_f16, what=""):
+    """Fused-epilogue acceptance (oracle.epilogue_tolerance)."""
+    tol = oracle.epilogue_tolerance(out_ref, S, alpha, beta,
+                                    None if d is None else d.double().numpy(), bias, out_f16)
+    err = np.abs(got - out_ref)
+    bad = ~(err <= tol)
+    if bad.any():
+        i = tuple(int(v) for v in np.argwhere(bad)[0])
+        raise AssertionError(f"{what}: {int(bad.sum())}/{bad.size} elements outside tolerance; "
+                             f"first at {i}: got {got[i]!r} want {out_ref[i]!r} tol {tol[i]!r}")
+    return float(np.max(err)) if err.size else 0.0

@@ -37,7 +37,7 @@ def declared_functions():
 
 def test_header_declares_the_abi():
     names = declared_functions()
-    for must in ["tg_gemm", "tg_gemm_check", "tg_status_string", "tg_gemm_path",
+    for must in ["tg_gemm", "tg_gemm_ex", "tg_gemm_check", "tg_status_string", "tg_gemm_path",
                  "tg_gemm_force_path", "tg_gemm_force_tiling", "tg_gemm_test_hook",
                  "tg_gemm_version"]:
         assert must in names
@@ -97,10 +97,56 @@ def path(M, N, K, A=PA, lda=None, B=PB, ldb=None, C=PC, ldc=None, i=tg.F16, o=tg
     (dict(M=64, N=64, K=64, C=PB - 100), tg.TG_ERR_INVALID_ARG),
     # a span that would wrap past the end of the address space
     (dict(M=2 ** 30, N=8, K=8, ldc=2 ** 40), tg.TG_ERR_INVALID_ARG),
+    # pointers that are not a multiple of their element size
+    (dict(M=64, N=64, K=64, A=PA + 1), tg.TG_ERR_INVALID_ARG),
+    (dict(M=64, N=64, K=64, B=PB + 3), tg.TG_ERR_INVALID_ARG),
+    (dict(M=64, N=64, K=64, C=PC + 1), tg.TG_ERR_INVALID_ARG),
+    (dict(M=64, N=64, K=64, C=PC + 2, o=tg.F32), tg.TG_ERR_INVALID_ARG),
+    (dict(M=64, N=64, K=64, A=PA + 2, i=tg.F32, o=tg.F32), tg.TG_ERR_INVALID_ARG),
+    (dict(M=64, N=64, K=0, C=PC + 1), tg.TG_ERR_INVALID_ARG),
 ])
 def test_invalid_arguments_rejected_on_host(args, status):
     assert call(**args) == status
     assert path(**args) == 0
+
+
+PD, PBIAS = 0x7F3000000000, 0x7F4000000000
+
+
+def call_ex(M, N, K, A=PA, B=PB, C=PC, ldc=None, i=tg.F16, o=tg.F16, alpha=1.0, beta=0.0, D=0,
+            ldd=None, bias=0, act=tg.ACT_NONE):
+    ldc = N if ldc is None else ldc
+    ldd = N if ldd is None else ldd
+    return tg.tg_gemm_ex(M, N, K, A, K, B, N, C, ldc, i, o, alpha, beta, D, ldd, bias, act, 0)
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(M=4, N=4, K=4, act=3), tg.TG_ERR_INVALID_ARG),
+    (dict(M=4, N=4, K=4, act=-1), tg.TG_ERR_INVALID_ARG),
+    (dict(M=0, N=4, K=4, act=7), tg.TG_ERR_INVALID_ARG),
+    (dict(M=4, N=4, K=4, beta=1.0, D=0), tg.TG_ERR_INVALID_ARG),
+    (dict(M=4, N=8, K=4, beta=1.0, D=PD, ldd=7), tg.TG_ERR_INVALID_ARG),
+    (dict(M=4, N=4, K=4, beta=1.0, D=PD + 1), tg.TG_ERR_INVALID_ARG),
+    (dict(M=4, N=4, K=4, beta=1.0, D=PD + 2, o=tg.F32), tg.TG_ERR_INVALID_ARG),
+    # D overlapping C other than exactly in place
+    (dict(M=64, N=64, K=64, beta=1.0, D=PC + 128), tg.TG_ERR_INVALID_ARG),
+    (dict(M=64, N=64, K=64, beta=1.0, D=PC, ldd=72, ldc=64), tg.TG_ERR_INVALID_ARG),
+    (dict(M=64, N=64, K=0, beta=1.0, D=PC - 2), tg.TG_ERR_INVALID_ARG),
+    # bias misaligned or inside C
+    (dict(M=4, N=4, K=4, bias=PBIAS + 2), tg.TG_ERR_INVALID_ARG),
+    (dict(M=64, N=64, K=64, bias=PC + 64), tg.TG_ERR_INVALID_ARG),
+    # the plain call's own checks come first
+    (dict(M=4, N=4, K=4, i=tg.F32, o=tg.F16, beta=1.0, D=PD), tg.TG_ERR_UNSUPPORTED),
+    (dict(M=64, N=64, K=64, C=PA + 64, beta=1.0, D=PD), tg.TG_ERR_INVALID_ARG),
+])
+def test_epilogue_arguments_rejected_on_host(args, status):
+    assert call_ex(**args) == status
+
+
+def test_epilogue_degenerate_sizes_are_noops():
+    # M == 0 or N == 0 returns before any CUDA call, even with NULL pointers
+    assert call_ex(0, 5, 7, A=0, B=0, C=0, beta=2.0, D=0, act=tg.ACT_GELU) == tg.TG_OK
+    assert call_ex(5, 0, 7, A=0, B=0, C=0, alpha=3.0, act=tg.ACT_RELU) == tg.TG_OK
 
 
 def test_degenerate_sizes_are_noops():

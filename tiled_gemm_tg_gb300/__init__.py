@@ -2,7 +2,8 @@
 
 The library computes C[M,N] = A[M,K] x B[K,N] (row-major; fp16 or fp32
 inputs, fp32 accumulation, fp16 or fp32 output) with hand-written CUDA
-kernels for sm_103a.  This module only marshals arguments: the entry points
+kernels for sm_103a, optionally with a fused epilogue
+C = act(alpha*AB + beta*D + bias) (``tg_gemm_ex``).  This module only marshals arguments: the entry points
 carry the names of the C ABI in include/tg_gemm.h, and ``gemm`` is a
 convenience that takes torch tensors, allocates the output with torch and
 calls ``tg_gemm``.  There is no fallback: if the compiled library is missing
@@ -18,7 +19,7 @@ __all__ = [
     "F16", "F32", "TG_OK", "TG_ERR_INVALID_ARG", "TG_ERR_UNSUPPORTED", "TG_ERR_CUDA",
     "TG_ERR_TIMEOUT", "PATHS", "TgError", "lib", "library_path", "tg_gemm", "tg_gemm_check",
     "tg_status_string", "tg_gemm_path", "tg_gemm_force_path", "tg_gemm_force_tiling",
-    "tg_gemm_test_hook",
+    "tg_gemm_test_hook", "tg_gemm_ex", "ACT_NONE", "ACT_RELU", "ACT_GELU",
     "tg_gemm_version", "gemm",
     "check",
 ]
@@ -30,6 +31,9 @@ TG_ERR_INVALID_ARG = 1
 TG_ERR_UNSUPPORTED = 2
 TG_ERR_CUDA = 3
 TG_ERR_TIMEOUT = 4
+ACT_NONE = 0
+ACT_RELU = 1
+ACT_GELU = 2
 PATHS = {0: "none", 1: "zero", 2: "simt_f32", 3: "tc_main", 4: "tc_boundary", 5: "tc_skinny",
          6: "tc_pair"}
 
@@ -63,6 +67,9 @@ def lib() -> ctypes.CDLL:
         i64, vp, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
         L.tg_gemm.restype = i32
         L.tg_gemm.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, i32, vp]
+        L.tg_gemm_ex.restype = i32
+        L.tg_gemm_ex.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, i32,
+                                 ctypes.c_float, ctypes.c_float, vp, i64, vp, i32, vp]
         L.tg_gemm_check.restype = i32
         L.tg_gemm_check.argtypes = [vp]
         L.tg_status_string.restype = ctypes.c_char_p
@@ -86,6 +93,15 @@ def lib() -> ctypes.CDLL:
 def tg_gemm(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, stream=0) -> int:
     """Enqueue C = A x B on `stream`; pointers are integers (device addresses)."""
     return int(lib().tg_gemm(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, stream))
+
+
+def tg_gemm_ex(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, alpha, beta, D, ldd,
+               bias, act, stream=0) -> int:
+    """Enqueue C = act(alpha * A x B + beta * D + bias) on `stream` (D and bias
+    are device addresses or 0/None)."""
+    return int(lib().tg_gemm_ex(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype,
+                                float(alpha), float(beta), D or None, ldd, bias or None,
+                                int(act), stream))
 
 
 def tg_gemm_check(stream=0) -> int:
@@ -143,9 +159,12 @@ def _stream_handle(stream) -> int:
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def gemm(a, b, out=None, out_dtype=None, stream=None):
-    """C = A x B for 2-D CUDA tensors (row-major rows; row strides may exceed
-    the row length).  Allocates C with torch unless `out` is given."""
+def gemm(a, b, out=None, out_dtype=None, stream=None, alpha=1.0, beta=0.0, d=None, bias=None,
+         act=ACT_NONE):
+    """C = act(alpha * A x B + beta * D + bias) for 2-D CUDA tensors (row-major
+    rows; row strides may exceed the row length); the defaults give C = A x B.
+    `d` has the output's dtype and may be `out` itself; `bias` is N fp32
+    values.  Allocates C with torch unless `out` is given."""
     import torch
     if not (a.is_cuda and b.is_cuda):
         raise ValueError("operands must be CUDA tensors")
@@ -156,8 +175,25 @@ def gemm(a, b, out=None, out_dtype=None, stream=None):
     if out is None:
         od = out_dtype if out_dtype is not None else a.dtype
         out = torch.empty((M, N), dtype=od, device=a.device)
-    st = tg_gemm(M, N, K, a.data_ptr(), _ld(a), b.data_ptr(), _ld(b), out.data_ptr(), _ld(out),
-                 _code(a.dtype), _code(out.dtype), _stream_handle(stream))
+    fused = alpha != 1.0 or beta != 0.0 or bias is not None or act != ACT_NONE
+    if not fused:
+        st = tg_gemm(M, N, K, a.data_ptr(), _ld(a), b.data_ptr(), _ld(b), out.data_ptr(),
+                     _ld(out), _code(a.dtype), _code(out.dtype), _stream_handle(stream))
+    else:
+        d_ptr, ldd = 0, N
+        if beta != 0.0:
+            if d is None or d.dtype != out.dtype or tuple(d.shape) != (M, N) or not d.is_cuda:
+                raise ValueError("beta != 0 needs d: an M x N CUDA tensor of the output dtype")
+            d_ptr, ldd = d.data_ptr(), _ld(d)
+        b_ptr = 0
+        if bias is not None:
+            if bias.dtype != torch.float32 or bias.numel() != N or not bias.is_cuda or \
+                    not bias.is_contiguous():
+                raise ValueError("bias must be N contiguous fp32 CUDA values")
+            b_ptr = bias.data_ptr()
+        st = tg_gemm_ex(M, N, K, a.data_ptr(), _ld(a), b.data_ptr(), _ld(b), out.data_ptr(),
+                        _ld(out), _code(a.dtype), _code(out.dtype), alpha, beta, d_ptr, ldd,
+                        b_ptr, act, _stream_handle(stream))
     if st != TG_OK:
         raise TgError(st)
     return out

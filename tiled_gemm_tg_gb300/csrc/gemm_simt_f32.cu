@@ -1,5 +1,6 @@
 // gemm_simt_f32.cu -- fp32 GEMM on the CUDA cores (fp32 in, fp32 accumulate,
-// fp32 out).
+// fp32 out), and the elementwise kernel of a fused epilogue over an empty
+// product (K == 0).
 //
 // This serves the fp32 128x128x128 example of "TileLang实战：用Python DSL自动
 // 生成高性能GPU计算内核" (gsyq.cn), §3.1 (the triple loop C[i,j] += A[i,k] *
@@ -16,12 +17,16 @@
 // M, N, K and row strides work.
 #include <cstdint>
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include "tc_common.cuh"
 #include "tg_internal.h"
 
 namespace tg {
 namespace {
+
+using namespace tg::dev;
 
 constexpr int BM = 64;
 constexpr int BN = 64;
@@ -32,7 +37,7 @@ constexpr int kThreads = (BM / TM) * (BN / TN);  // 256
 
 __global__ void __launch_bounds__(kThreads)
 gemm_simt_f32_kernel(const float* __restrict__ A, long long lda, const float* __restrict__ B,
-                     long long ldb, float* __restrict__ C, long long ldc, int M, int N, int K)
+                     long long ldb, float* C, long long ldc, int M, int N, int K, Epilogue epi)
 {
     __shared__ __align__(16) float As[2][BK][BM + 4];  // +4: fewer bank conflicts on the transposing store
     __shared__ __align__(16) float Bs[2][BK][BN];
@@ -101,12 +106,44 @@ gemm_simt_f32_kernel(const float* __restrict__ A, long long lda, const float* __
 #pragma unroll
         for (int j = 0; j < TN; ++j) {
             const int n = n0 + tx * TN + j;
-            if (n < N) C[static_cast<long long>(m) * ldc + n] = acc[i][j];
+            if (n < N)
+                C[static_cast<long long>(m) * ldc + n] =
+                    epi.on ? epilogue_elem<true>(acc[i][j], m, n, epi) : acc[i][j];
         }
     }
 }
 
+// K == 0 with a fused epilogue: the product is the empty sum, so each element
+// is act(beta * D + bias).  One thread per column, rows strided over grid.y.
+template <bool OUT_F32>
+__global__ void __launch_bounds__(256)
+epilogue_only_kernel(void* C, long long ldc, int M, int N, Epilogue epi)
+{
+    const int n = blockIdx.x * 256 + static_cast<int>(threadIdx.x);
+    if (n >= N) return;
+    for (int m = blockIdx.y; m < M; m += gridDim.y) {
+        const float y = epilogue_elem<OUT_F32>(0.0f, m, n, epi);
+        const long long i = static_cast<long long>(m) * ldc + n;
+        if constexpr (OUT_F32)
+            static_cast<float*>(C)[i] = y;
+        else
+            static_cast<__half*>(C)[i] = __float2half_rn(y);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_epilogue_only(const GemmArgs& a)
+{
+    const unsigned gx = static_cast<unsigned>((static_cast<long long>(a.N) + 255) / 256);
+    const unsigned gy = static_cast<unsigned>(a.M < 65535 ? a.M : 65535);
+    const dim3 grid(gx, gy);
+    if (a.out_f32)
+        epilogue_only_kernel<true><<<grid, 256, 0, a.stream>>>(a.C, a.ldc, a.M, a.N, a.epi);
+    else
+        epilogue_only_kernel<false><<<grid, 256, 0, a.stream>>>(a.C, a.ldc, a.M, a.N, a.epi);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_simt_f32(const GemmArgs& a)
 {
@@ -114,7 +151,7 @@ cudaError_t launch_simt_f32(const GemmArgs& a)
     if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
     gemm_simt_f32_kernel<<<grid, kThreads, 0, a.stream>>>(
         static_cast<const float*>(a.A), a.lda, static_cast<const float*>(a.B), a.ldb,
-        static_cast<float*>(a.C), a.ldc, a.M, a.N, a.K);
+        static_cast<float*>(a.C), a.ldc, a.M, a.N, a.K, a.epi);
     return cudaGetLastError();
 }
 

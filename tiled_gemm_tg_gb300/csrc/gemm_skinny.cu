@@ -32,6 +32,7 @@
 #include <cuda_runtime.h>
 
 #include "ptx.cuh"
+#include "tc_common.cuh"
 #include "tg_internal.h"
 
 namespace tg {
@@ -69,8 +70,8 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr)
 template <int MP, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmBT,
-                   void* __restrict__ C, long long ldc, int M, int N, int K, int split,
-                   int hook, unsigned int* err)
+                   void* C, long long ldc, int M, int N, int K, int split,
+                   int hook, unsigned int* err, Epilogue epi)
 {
     using Cfg = SkinnyCfg<MP>;
     extern __shared__ uint8_t smem_raw[];
@@ -239,6 +240,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             float sum = 0.0f;
             for (int r = 0; r < split; ++r)
                 sum += ld_dsmem_f32(mapa_shared(red_local + off, static_cast<uint32_t>(r)));
+            if (epi.on) sum = epilogue_elem<OUT_F32>(sum, m, n, epi);
             if constexpr (OUT_F32)
                 static_cast<float*>(C)[static_cast<long long>(m) * ldc + n] = sum;
             else
@@ -337,7 +339,8 @@ cudaError_t launch_cfg(const GemmArgs& a)
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, ta, tbt, a.C, a.ldc, a.M, a.N, a.K, split, a.hook, a.err);
+    return cudaLaunchKernelEx(&cfg, kernel, ta, tbt, a.C, a.ldc, a.M, a.N, a.K, split, a.hook, a.err,
+                              a.epi);
 }
 
 }  // namespace

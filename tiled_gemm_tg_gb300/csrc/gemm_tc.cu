@@ -71,8 +71,9 @@ struct MainCfg {
 template <int BN, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    void* __restrict__ C, long long ldc, int M, int N, int K, int tiles_m,
-                    int tiles_n, int group_m, int c_vec, int hook, unsigned int* err)
+                    void* C, long long ldc, int M, int N, int K, int tiles_m,
+                    int tiles_n, int group_m, int c_vec, int hook, unsigned int* err,
+                    Epilogue epi)
 {
     using Cfg = MainCfg<BN>;
     constexpr int STAGES = Cfg::STAGES;
@@ -253,7 +254,10 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 tmem_ld_32x32b_x32(taddr + c, r);
                 tmem_ld_wait();
                 const int n = tn * BN + c;
-                if (m < M && n < N) store_chunk<OUT_F32>(C, ldc, m, n, N, r, c_vec != 0);
+                if (m < M && n < N) {
+                    if (epi.on) epilogue_chunk<OUT_F32>(r, m, n, N, epi);
+                    store_chunk<OUT_F32>(C, ldc, m, n, N, r, c_vec != 0);
+                }
             }
             tc_fence_before();
             mbar_arrive(smem_u32(&tempty_bar[acc]));
@@ -308,7 +312,8 @@ cudaError_t launch_cfg(const GemmArgs& a)
     const int c_vec = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) &&
                       ((static_cast<size_t>(a.ldc) * es) % 16 == 0);
     kernel<<<grid, kThreads, Cfg::SMEM, a.stream>>>(ta, tb, a.C, a.ldc, a.M, a.N, a.K, tiles_m,
-                                                     tiles_n, group_m, c_vec, a.hook, a.err);
+                                                     tiles_n, group_m, c_vec, a.hook, a.err,
+                                                     a.epi);
     return cudaGetLastError();
 }
 

@@ -77,8 +77,9 @@ constexpr int EPI_COLS = TG_PAIR_EPI_COLS;  // accumulator columns per tcgen05.l
 template <bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    void* __restrict__ C, long long ldc, int M, int N, int K, int tiles_m,
-                    int tiles_n, int group_m, int c_vec, int hook, unsigned int* err)
+                    void* C, long long ldc, int M, int N, int K, int tiles_m,
+                    int tiles_n, int group_m, int c_vec, int hook, unsigned int* err,
+                    Epilogue epi)
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[STAGES];   // used in the leader only
@@ -277,7 +278,10 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 #pragma unroll
                 for (int j = 0; j < EPI_COLS; j += 32) {
                     const int n = tn * PN + c + j;
-                    if (m < M && n < N) store_chunk<OUT_F32>(C, ldc, m, n, N, r + j, c_vec != 0);
+                    if (m < M && n < N) {
+                        if (epi.on) epilogue_chunk<OUT_F32>(r + j, m, n, N, epi);
+                        store_chunk<OUT_F32>(C, ldc, m, n, N, r + j, c_vec != 0);
+                    }
                 }
             }
             tc_fence_before();
@@ -363,7 +367,7 @@ cudaError_t launch_cfg(const GemmArgs& a)
     cfg.attrs = at;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, ta, tb, a.C, a.ldc, a.M, a.N, a.K, tiles_m, tiles_n,
-                              group_m, c_vec, a.hook, a.err);
+                              group_m, c_vec, a.hook, a.err, a.epi);
 }
 
 }  // namespace

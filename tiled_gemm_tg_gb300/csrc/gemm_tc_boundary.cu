@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 
 #include "ptx.cuh"
+#include "tc_common.cuh"
 #include "tg_internal.h"
 
 namespace tg {
@@ -137,8 +138,8 @@ __device__ __forceinline__ void stash(const Frag& f, uint8_t* sA, uint8_t* sB, i
 template <bool OUT_F32>
 __global__ void __launch_bounds__(kThreads)
 gemm_tc_boundary_kernel(const __half* __restrict__ A, long long lda, const __half* __restrict__ B,
-                        long long ldb, void* __restrict__ C, long long ldc, int M, int N, int K,
-                        int hook, unsigned int* err)
+                        long long ldb, void* C, long long ldc, int M, int N, int K,
+                        int hook, unsigned int* err, Epilogue epi)
 {
     // An operand whose base and row stride are both 16-byte multiples is read
     // with 16-byte loads (at most one of A and B is, or the TMA path serves).
@@ -224,6 +225,7 @@ gemm_tc_boundary_kernel(const __half* __restrict__ A, long long lda, const __hal
             tmem_ld_wait();
             const int n = n0 + c;
             if (m < M && n < N) {
+                if (epi.on) epilogue_chunk<OUT_F32>(r, m, n, N, epi);
                 if constexpr (OUT_F32) {
                     float* row = static_cast<float*>(C) + static_cast<long long>(m) * ldc + n;
 #pragma unroll
@@ -278,7 +280,7 @@ cudaError_t launch_cfg(const GemmArgs& a)
     if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
     kernel<<<grid, kThreads, SMEM, a.stream>>>(
         static_cast<const __half*>(a.A), a.lda, static_cast<const __half*>(a.B), a.ldb, a.C, a.ldc,
-        a.M, a.N, a.K, a.hook, a.err);
+        a.M, a.N, a.K, a.hook, a.err, a.epi);
     return cudaGetLastError();
 }
 

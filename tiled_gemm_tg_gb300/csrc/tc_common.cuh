@@ -1,10 +1,12 @@
-// tc_common.cuh -- device helpers shared by the TMA + tcgen05 GEMM kernels:
-// the grouped tile order and the epilogue's row-chunk store.
+// tc_common.cuh -- device helpers shared by the GEMM kernels: the grouped
+// tile order, the fused epilogue and the epilogue's row-chunk store.
 #pragma once
 
 #include <cstdint>
 
 #include <cuda_fp16.h>
+
+#include "tg_internal.h"
 
 namespace tg {
 namespace dev {
@@ -21,6 +23,107 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
     const int r = t - g * span;
     tm = first + r % gs;
     tn = r / gs;
+}
+
+// Activation of the fused epilogue.  GELU is x * Phi(x) with Phi the standard
+// normal distribution function, written as 0.5 * x * erfc(-x / sqrt(2)) so the
+// negative tail keeps its relative accuracy.  fmaxf maps NaN to 0, as
+// "x > 0 ? x : 0" does.
+__device__ __forceinline__ float act_apply(float y, int act)
+{
+    if (act == ACT_RELU) return fmaxf(y, 0.0f);
+    if (act == ACT_GELU) return 0.5f * y * erfcf(-0.70710678118654752f * y);
+    return y;
+}
+
+// One output element of the fused epilogue: act(alpha*acc + bias[n] + beta*D[m,n]).
+template <bool OUT_F32>
+__device__ __forceinline__ float epilogue_elem(float acc, int m, int n, const Epilogue& e)
+{
+    float y = e.alpha * acc;
+    if (e.bias) y += __ldg(e.bias + n);
+    if (e.beta != 0.0f) {
+        const long long i = static_cast<long long>(m) * e.ldd + n;
+        const float d = OUT_F32 ? static_cast<const float*>(e.D)[i]
+                                : __half2float(static_cast<const __half*>(e.D)[i]);
+        y = fmaf(e.beta, d, y);
+    }
+    return act_apply(y, e.act);
+}
+
+// The fused epilogue over 32 accumulators r[0..31] (fp32 bit patterns) of row
+// m, columns n..n+31, in place; columns >= N are left as they are (the store
+// skips them).  D is read with plain loads, never through the read-only
+// path, because it may be C itself.
+template <bool OUT_F32>
+__device__ __forceinline__ void epilogue_chunk(uint32_t* r, int m, int n, int N, const Epilogue& e)
+{
+    const bool full = n + 32 <= N;
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = e.alpha * __uint_as_float(r[j]);
+    if (e.bias) {
+        if (e.bias_vec && full) {
+            const float4* b = reinterpret_cast<const float4*>(e.bias + n);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 q = __ldg(b + i);
+                v[4 * i] += q.x;
+                v[4 * i + 1] += q.y;
+                v[4 * i + 2] += q.z;
+                v[4 * i + 3] += q.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (n + j < N) v[j] += __ldg(e.bias + n + j);
+        }
+    }
+    if (e.beta != 0.0f) {
+        const long long row = static_cast<long long>(m) * e.ldd + n;
+        if constexpr (OUT_F32) {
+            const float* d = static_cast<const float*>(e.D) + row;
+            if (e.d_vec && full) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 q = reinterpret_cast<const float4*>(d)[i];
+                    v[4 * i] = fmaf(e.beta, q.x, v[4 * i]);
+                    v[4 * i + 1] = fmaf(e.beta, q.y, v[4 * i + 1]);
+                    v[4 * i + 2] = fmaf(e.beta, q.z, v[4 * i + 2]);
+                    v[4 * i + 3] = fmaf(e.beta, q.w, v[4 * i + 3]);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (n + j < N) v[j] = fmaf(e.beta, d[j], v[j]);
+            }
+        } else {
+            const __half* d = static_cast<const __half*>(e.D) + row;
+            if (e.d_vec && full) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 q = reinterpret_cast<const uint4*>(d)[i];
+                    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+                        v[8 * i + 2 * k] = fmaf(e.beta, f.x, v[8 * i + 2 * k]);
+                        v[8 * i + 2 * k + 1] = fmaf(e.beta, f.y, v[8 * i + 2 * k + 1]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (n + j < N) v[j] = fmaf(e.beta, __half2float(d[j]), v[j]);
+            }
+        }
+    }
+    if (e.act != ACT_NONE) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = act_apply(v[j], e.act);
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(v[j]);
 }
 
 // Stores 32 consecutive fp32 accumulator values r[0..31] of row m, columns

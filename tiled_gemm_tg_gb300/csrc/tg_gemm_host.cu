@@ -98,11 +98,17 @@ tg_status classify(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
     if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return TG_ERR_UNSUPPORTED;
     if (M == 0 || N == 0) return TG_OK;
     if (C == nullptr || ldc < N) return TG_ERR_INVALID_ARG;
+    // Every element access is naturally aligned: a pointer that is not a
+    // multiple of its element size is rejected rather than handed to a kernel.
+    if (reinterpret_cast<uintptr_t>(C) % esize(out_dtype) != 0) return TG_ERR_INVALID_ARG;
     if (K == 0) {
         *path = tg::PATH_ZERO;
         return TG_OK;
     }
     if (A == nullptr || B == nullptr || lda < K || ldb < N) return TG_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(A) % esize(in_dtype) != 0 ||
+        reinterpret_cast<uintptr_t>(B) % esize(in_dtype) != 0)
+        return TG_ERR_INVALID_ARG;
     u128 c0, c1, a0, a1, b0, b1;
     span(C, M, N, ldc, esize(out_dtype), &c0, &c1);
     span(A, M, K, lda, esize(in_dtype), &a0, &a1);
@@ -149,6 +155,106 @@ bool path_serves(int path, int natural, tg_dtype in_dtype, int64_t M)
     }
 }
 
+// Validates the fused-epilogue arguments of tg_gemm_ex against C (M, N >= 1,
+// C already validated) and fills *e.  D may be C itself (same base and row
+// stride: an in-place update); any other overlap of D or bias with C is an
+// error, as is a pointer that is not a multiple of its element size.
+tg_status classify_epilogue(int64_t M, int64_t N, void* C, int64_t ldc, tg_dtype out_dtype,
+                            float alpha, float beta, const void* D, int64_t ldd,
+                            const float* bias, int act, tg::Epilogue* e)
+{
+    if (act != tg::ACT_NONE && act != tg::ACT_RELU && act != tg::ACT_GELU) return TG_ERR_INVALID_ARG;
+    const size_t es = esize(out_dtype);
+    u128 c0, c1;
+    span(C, M, N, ldc, es, &c0, &c1);
+    const u128 top = static_cast<u128>(1) << 64;
+    if (beta != 0.0f) {
+        if (D == nullptr || ldd < N || reinterpret_cast<uintptr_t>(D) % es != 0)
+            return TG_ERR_INVALID_ARG;
+        u128 d0, d1;
+        span(D, M, N, ldd, es, &d0, &d1);
+        if (d1 > top) return TG_ERR_INVALID_ARG;
+        const bool in_place = (D == C && ldd == ldc);
+        if (!in_place && overlaps(c0, c1, d0, d1)) return TG_ERR_INVALID_ARG;
+    }
+    if (bias != nullptr) {
+        if (reinterpret_cast<uintptr_t>(bias) % 4 != 0) return TG_ERR_INVALID_ARG;
+        u128 b0, b1;
+        span(bias, 1, N, N, 4, &b0, &b1);
+        if (b1 > top || overlaps(c0, c1, b0, b1)) return TG_ERR_INVALID_ARG;
+    }
+    e->alpha = alpha;
+    e->beta = beta;
+    e->D = beta != 0.0f ? D : nullptr;
+    e->ldd = beta != 0.0f ? ldd : 0;
+    e->bias = bias;
+    e->act = act;
+    e->on = !(alpha == 1.0f && beta == 0.0f && bias == nullptr && act == tg::ACT_NONE);
+    e->d_vec = beta != 0.0f && reinterpret_cast<uintptr_t>(D) % 16 == 0 &&
+               (static_cast<size_t>(ldd) * es) % 16 == 0;
+    e->bias_vec = bias != nullptr && reinterpret_cast<uintptr_t>(bias) % 16 == 0;
+    return TG_OK;
+}
+
+// The body of tg_gemm and tg_gemm_ex once the arguments have been classified.
+tg_status run(int path, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+              const void* B, int64_t ldb, void* C, int64_t ldc, tg_dtype in_dtype,
+              tg_dtype out_dtype, const tg::Epilogue& epi, tg_stream_t stream)
+{
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (path == tg::PATH_ZERO && !epi.on) {
+        const size_t es = esize(out_dtype);
+        cudaError_t e = cudaMemset2DAsync(C, static_cast<size_t>(ldc) * es, 0,
+                                          static_cast<size_t>(N) * es, static_cast<size_t>(M), s);
+        return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+    }
+    if (path != tg::PATH_ZERO) {
+        const int forced = g_force_path.load(std::memory_order_relaxed);
+        if (forced != 0) {
+            if (!path_serves(forced, path, in_dtype, M)) return TG_ERR_UNSUPPORTED;
+            path = forced;
+        }
+    }
+
+    DeviceState* ds = nullptr;
+    tg_status st = device_state(&ds);
+    if (st != TG_OK) return st;
+
+    tg::GemmArgs a;
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.A = A;
+    a.lda = lda;
+    a.B = B;
+    a.ldb = ldb;
+    a.C = C;
+    a.ldc = ldc;
+    a.out_f32 = (out_dtype == TG_F32);
+    a.err = ds->err;
+    a.hook = g_test_hook.load(std::memory_order_relaxed);
+    a.group_m = g_force_group.load(std::memory_order_relaxed);
+    a.num_sms = ds->num_sms;
+    a.stream = s;
+    a.epi = epi;
+
+    cudaError_t e = cudaSuccess;
+    switch (path) {
+        case tg::PATH_ZERO: e = tg::launch_epilogue_only(a); break;
+        case tg::PATH_SIMT: e = tg::launch_simt_f32(a); break;
+        case tg::PATH_MAIN: {
+            const int bn = g_force_bn.load(std::memory_order_relaxed);
+            e = tg::launch_main(a, bn != 0 ? bn : tg::main_tile_n(a.M, a.N, a.num_sms));
+            break;
+        }
+        case tg::PATH_BOUNDARY: e = tg::launch_boundary(a); break;
+        case tg::PATH_MAIN_PAIR: e = tg::launch_main_pair(a); break;
+        case tg::PATH_SKINNY: e = tg::launch_skinny(a); break;
+        default: return TG_ERR_UNSUPPORTED;
+    }
+    return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+}
+
 }  // namespace
 
 namespace tg {
@@ -179,55 +285,23 @@ tg_status tg_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, c
     int path = tg::PATH_NONE;
     tg_status st = classify(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, &path);
     if (st != TG_OK || path == tg::PATH_NONE) return st;
+    return run(path, M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, tg::Epilogue{}, stream);
+}
 
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (path == tg::PATH_ZERO) {
-        const size_t es = esize(out_dtype);
-        cudaError_t e = cudaMemset2DAsync(C, static_cast<size_t>(ldc) * es, 0,
-                                          static_cast<size_t>(N) * es, static_cast<size_t>(M), s);
-        return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
-    }
-    const int forced = g_force_path.load(std::memory_order_relaxed);
-    if (forced != 0) {
-        if (!path_serves(forced, path, in_dtype, M)) return TG_ERR_UNSUPPORTED;
-        path = forced;
-    }
-
-    DeviceState* ds = nullptr;
-    st = device_state(&ds);
+tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                     int64_t ldb, void* C, int64_t ldc, tg_dtype in_dtype, tg_dtype out_dtype,
+                     float alpha, float beta, const void* D, int64_t ldd, const float* bias,
+                     tg_activation act, tg_stream_t stream)
+{
+    if (act != TG_ACT_NONE && act != TG_ACT_RELU && act != TG_ACT_GELU) return TG_ERR_INVALID_ARG;
+    int path = tg::PATH_NONE;
+    tg_status st = classify(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, &path);
+    if (st != TG_OK || path == tg::PATH_NONE) return st;
+    tg::Epilogue epi;
+    st = classify_epilogue(M, N, C, ldc, out_dtype, alpha, beta, D, ldd, bias,
+                           static_cast<int>(act), &epi);
     if (st != TG_OK) return st;
-
-    tg::GemmArgs a;
-    a.M = static_cast<int>(M);
-    a.N = static_cast<int>(N);
-    a.K = static_cast<int>(K);
-    a.A = A;
-    a.lda = lda;
-    a.B = B;
-    a.ldb = ldb;
-    a.C = C;
-    a.ldc = ldc;
-    a.out_f32 = (out_dtype == TG_F32);
-    a.err = ds->err;
-    a.hook = g_test_hook.load(std::memory_order_relaxed);
-    a.group_m = g_force_group.load(std::memory_order_relaxed);
-    a.num_sms = ds->num_sms;
-    a.stream = s;
-
-    cudaError_t e = cudaSuccess;
-    switch (path) {
-        case tg::PATH_SIMT: e = tg::launch_simt_f32(a); break;
-        case tg::PATH_MAIN: {
-            const int bn = g_force_bn.load(std::memory_order_relaxed);
-            e = tg::launch_main(a, bn != 0 ? bn : tg::main_tile_n(a.M, a.N, a.num_sms));
-            break;
-        }
-        case tg::PATH_BOUNDARY: e = tg::launch_boundary(a); break;
-        case tg::PATH_MAIN_PAIR: e = tg::launch_main_pair(a); break;
-        case tg::PATH_SKINNY: e = tg::launch_skinny(a); break;
-        default: return TG_ERR_UNSUPPORTED;
-    }
-    return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+    return run(path, M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, epi, stream);
 }
 
 tg_status tg_gemm_check(tg_stream_t stream)

@@ -28,6 +28,24 @@ enum ErrBits : unsigned int {
     ERR_DRAIN = 1u << 5,
 };
 
+// Fused epilogue  C = act(alpha * acc + beta * D + bias[n]), applied to the
+// fp32 accumulator before the output conversion.  `on` is 0 for the plain
+// store (alpha 1, beta 0, no bias, no activation); kernels then take exactly
+// the code path of the unfused call.
+enum Act : int { ACT_NONE = 0, ACT_RELU = 1, ACT_GELU = 2 };
+
+struct Epilogue {
+    float alpha = 1.0f;
+    float beta = 0.0f;
+    const void* D = nullptr;     // M x N, the output's element type; read only if beta != 0
+    long long ldd = 0;           // row stride of D in elements
+    const float* bias = nullptr; // N values, or null
+    int act = ACT_NONE;
+    int on = 0;
+    int d_vec = 0;     // D's base and row stride allow 16-byte loads
+    int bias_vec = 0;  // bias is 16-byte aligned
+};
+
 struct GemmArgs {
     int M, N, K;
     const void* A;
@@ -42,6 +60,7 @@ struct GemmArgs {
     int group_m;        // grouped tile-order height, 0 = the kernel's default
     int num_sms;
     cudaStream_t stream;
+    Epilogue epi;
 };
 
 // Encodes a 2-D row-major fp16 tensor map (inner extent `cols`, `rows` rows,
@@ -55,6 +74,8 @@ cudaError_t launch_main(const GemmArgs& a, int bn);
 cudaError_t launch_main_pair(const GemmArgs& a);
 cudaError_t launch_boundary(const GemmArgs& a);
 cudaError_t launch_skinny(const GemmArgs& a);
+// K == 0 with a fused epilogue: C = act(beta * D + bias) elementwise.
+cudaError_t launch_epilogue_only(const GemmArgs& a);
 
 // Tile width the main kernel uses for this problem (64, 128 or 256).
 int main_tile_n(int M, int N, int num_sms);
