@@ -220,6 +220,7 @@ def run_reference(args, w):
 EPILOGUES = {
     "none": None,
     "bias_relu": dict(alpha=1.0, beta=0.0, bias=True, act=1),
+    "axpby_bias": dict(alpha=0.5, beta=1.0, bias=True, act=0),
     "axpby_bias_gelu": dict(alpha=0.5, beta=1.0, bias=True, act=2),
 }
 

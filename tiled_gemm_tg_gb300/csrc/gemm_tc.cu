@@ -54,7 +54,11 @@ constexpr int BM = 128;
 constexpr int BK = 64;                 // fp16: 128 bytes per row = one swizzle atom
 constexpr uint32_t A_STAGE = BM * BK * 2;
 constexpr uint32_t B_BOX = 64 * BK * 2; // one [64 k][64 n] box, 8 KB
-constexpr int kThreads = 192;
+// Two epilogue warps per TMEM lane quadrant, each draining half of the
+// accumulator's columns: a long fused epilogue (GELU) then keeps up with the
+// MMAs instead of holding the accumulator buffer.
+constexpr int kEpilogueWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpilogueWarps;
 
 template <int BN>
 struct MainCfg {
@@ -98,7 +102,7 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&tfull_bar[a]), 1);
-            mbar_init(smem_u32(&tempty_bar[a]), 128);
+            mbar_init(smem_u32(&tempty_bar[a]), 32 * kEpilogueWarps);
         }
         mbar_init(smem_u32(&drain_bar), 1);
         abort_flag = 0;
@@ -231,6 +235,8 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     } else {
         // ------------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        constexpr int span = BN / (kEpilogueWarps / 4);  // accumulator columns per warp
+        const int c_lo = ((warp - 2) >> 2) * span;
         int acc = 0;
         uint32_t aph = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -249,7 +255,7 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
+            for (int c = c_lo; c < c_lo + span; c += 32) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(taddr + c, r);
                 tmem_ld_wait();
