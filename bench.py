@@ -182,6 +182,8 @@ def run_reference(args, w):
     from tiled_gemm_tg_gb300 import inputs
 
     a, b = inputs.operands(w)
+    if w.batch > 1:  # rows of the first product of the batch
+        a, b = a[0], b[0]
     nt = oracle.num_threads()
     a_np, b_np = a.numpy(), b.numpy()
     # size one step so that warmup + steps stay within ~2-3 minutes
@@ -273,8 +275,11 @@ def main():
     use_d = epi is not None and epi["beta"] != 0.0
     use_bias = epi is not None and epi["bias"]
     out_es = 2 if w.out_dtype == "f16" else 4
-    set_bytes = (w.M * w.K + w.K * w.N) * a_cpu.element_size() + w.M * w.N * out_es * (
-        2 if use_d else 1)
+    NB = w.batch
+    if NB > 1 and epi is not None:
+        ap.error("--epilogue applies to single products, not to a strided batch")
+    set_bytes = NB * ((w.M * w.K + w.K * w.N) * a_cpu.element_size() + w.M * w.N * out_es * (
+        2 if use_d else 1))
     # D and bias for a fused epilogue, drawn on the host like the operands
     d_cpu = inputs.draw((w.M, w.N), "normal", w.seed_base + 7, w.out_dtype) if use_d else None
     bias_cpu = inputs.draw((1, w.N), "normal", w.seed_base + 8, "f32")[0] if use_bias else None
@@ -286,7 +291,7 @@ def main():
         if i:  # distinct buffers with the same values (rotated for L2)
             a = a.clone()
             b = b.clone()
-        c = torch.empty((w.M, w.N), dtype=out_dt, device=dev)
+        c = torch.empty(((NB,) if NB > 1 else ()) + (w.M, w.N), dtype=out_dt, device=dev)
         d = d_cpu.to(dev) if use_d else None
         bias = bias_cpu.to(dev) if use_bias else None
         sets.append((a, b, c, d, bias))
@@ -295,7 +300,10 @@ def main():
     M, N, K = w.M, w.N, w.K
 
     def call(a, b, c, d, bias, handle):
-        if epi is None:
+        if NB > 1:
+            st = tg.tg_gemm_batched(NB, M, N, K, a.data_ptr(), K, M * K, b.data_ptr(), N, K * N,
+                                    c.data_ptr(), N, M * N, in_code, out_code, handle)
+        elif epi is None:
             st = tg.tg_gemm(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N, in_code,
                             out_code, handle)
         else:
@@ -309,8 +317,9 @@ def main():
     def step(i, handle=None):
         call(*sets[i % n_sets], sh if handle is None else handle)
 
-    path = tg.tg_gemm_path(M, N, K, sets[0][0].data_ptr(), K, sets[0][1].data_ptr(), N,
-                           sets[0][2].data_ptr(), N, in_code, out_code)
+    path = tg.tg_gemm_batched_path(NB, M, N, K, sets[0][0].data_ptr(), K, M * K,
+                                   sets[0][1].data_ptr(), N, K * N, sets[0][2].data_ptr(), N,
+                                   M * N, in_code, out_code)
 
     gpu_id = None
     try:
@@ -372,7 +381,7 @@ def main():
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         elapsed_ms = float(t.item())
 
-    flops = 2.0 * M * N * K
+    flops = 2.0 * NB * M * N * K
     value = ws * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
 
     # --- end to end through the C ABI from pinned host buffers.  Every step
@@ -382,7 +391,8 @@ def main():
     e2e_steps = args.e2e_steps or max(3, min(args.steps, 20))
     a_h = a_cpu.pin_memory()
     b_h = b_cpu.pin_memory()
-    c_h = [torch.empty((M, N), dtype=out_dt).pin_memory() for _ in range(2)]
+    c_h = [torch.empty(((NB,) if NB > 1 else ()) + (M, N), dtype=out_dt).pin_memory()
+           for _ in range(2)]
     d_h = d_cpu.pin_memory() if use_d else None
     bias_h = bias_cpu.pin_memory() if use_bias else None
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
@@ -435,8 +445,9 @@ def main():
         e2e_ms = float(t.item())
     e2e_value = ws * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
     ein = a_cpu.element_size()
-    h2d = (M * K + K * N) * ein + (M * N * out_es if use_d else 0) + (N * 4 if use_bias else 0)
-    d2h = M * N * c_h[0].element_size()
+    h2d = NB * (M * K + K * N) * ein + (M * N * out_es if use_d else 0) + (
+        N * 4 if use_bias else 0)
+    d2h = NB * M * N * c_h[0].element_size()
 
     sampler.stop()
     clocks = sampler.summary(host_t0, host_t1)
@@ -450,22 +461,38 @@ def main():
     rec = NCU_TRAFFIC.get(w.name) if epi is None else None
     if rec and rec.get("kernel_hash") == kernel_hash():
         traffic = rec["bytes"]
+    # The bound is the roofline's: a workload whose FLOP per algorithmic byte
+    # lies below the ridge (measured tensor peak / measured HBM bandwidth) is
+    # bound by HBM and is reported in GB/s against the copy bandwidth.
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    achieved_gbs = alg_bytes / (kern_ms * 1e-3) / 1e9
+    ridge = peak * 1e12 / (hbm * 1e9)
+    hbm_bound = flops / alg_bytes < ridge
     roofline = {
-        "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-        "frac": achieved / peak, "traffic": traffic,
+        "bound": "hbm" if hbm_bound else "tensor",
+        "achieved": achieved_gbs if hbm_bound else achieved,
+        "peak": hbm if hbm_bound else peak,
+        "unit": "GB/s" if hbm_bound else "TFLOP/s",
+        "frac": achieved_gbs / hbm if hbm_bound else achieved / peak,
+        "traffic": traffic,
         "kernel": {3: "gemm_tc_main_kernel", 4: "gemm_tc_boundary_kernel",
                    2: "gemm_simt_f32_kernel", 5: "gemm_skinny_kernel",
                    6: "gemm_tc_pair_kernel"}.get(path, str(path)),
         "kernel_ms": kern_ms,
-        "peak_source": f"{peak_src} bf16 burst (torch.matmul 8192^3) x 1.0 fp16/bf16 nominal ratio",
+        "peak_source": (f"{peak_src} STREAM-style copy bandwidth" if hbm_bound else
+                        f"{peak_src} bf16 burst (torch.matmul 8192^3) x 1.0 fp16/bf16 "
+                        "nominal ratio"),
+        "flop_per_byte": flops / alg_bytes, "ridge_flop_per_byte": ridge,
+        "achieved_tflops": achieved,
         "frac_of_nominal_2500": achieved / NOMINAL_FP16_DENSE_TFLOPS,
         "algorithmic_bytes": alg_bytes,
-        "achieved_gbs": alg_bytes / (kern_ms * 1e-3) / 1e9,
+        "achieved_gbs": achieved_gbs,
     }
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        v, rows, secs, nt = oracle_rows_sample(w, a_cpu, b_cpu, args.cpu_seconds)
+        v, rows, secs, nt = oracle_rows_sample(w, a_cpu[0] if NB > 1 else a_cpu,
+                                               b_cpu[0] if NB > 1 else b_cpu, args.cpu_seconds)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": nt, "kind": "oracle",
                "sample": f"{rows} of {M} rows of C (full N={N}, K={K}), {secs:.1f} s"}
 
@@ -476,7 +503,8 @@ def main():
             "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f16",
             "data": "synthetic",
-            "config": {"workload": w.name, "M": M, "N": N, "K": K, "in_dtype": w.in_dtype,
+            "config": {"workload": w.name, "batch": NB, "M": M, "N": N, "K": K,
+                       "in_dtype": w.in_dtype,
                        "accum": "f32", "out_dtype": w.out_dtype, "dist": w.dist,
                        "path": tg.PATHS.get(path, str(path)),
                        "epilogue": args.epilogue if epi is None else

@@ -101,6 +101,44 @@ tg_status tg_gemm(int64_t M, int64_t N, int64_t K,
                   tg_dtype in_dtype, tg_dtype out_dtype,
                   tg_stream_t stream);
 
+/*
+ * tg_gemm_batched -- C_b = A_b x B_b for b = 0 .. batch-1, a strided batch of
+ * independent products in one launch.
+ *
+ * Source: the pages' GEMM (as for tg_gemm) has no batch; a batch is the
+ * independent-problem form of the same operation, each product exactly the
+ * one tg_gemm computes.  The matrices of one call share M, N, K, the row
+ * strides and the dtypes.
+ *
+ * Arguments are those of tg_gemm plus
+ *   batch    number of products, 0 .. 65535 (0 is a no-op).
+ *   strideA  elements from A_b to A_(b+1): A_b = A + b*strideA.  0 uses one
+ *            A for every b (broadcast).  Likewise strideB.
+ *   strideC  elements from C_b to C_(b+1); with batch > 1 the C matrices
+ *            must not overlap: strideC >= (M-1)*ldc + N.
+ *
+ * Semantics per product: those of tg_gemm (overwrite, fp32 accumulation,
+ * RNE output rounding; K == 0 writes zeros).  Strides are in elements and
+ * must be >= 0.  Operand strides that are multiples of 16 bytes and at least
+ * one whole matrix (or 0) run on the TMA kernels, which walk every tile of
+ * every product in one persistent launch; other strides (overlapping
+ * operand matrices, odd strides) run on the predicated-load kernel.  The
+ * path is chosen as for tg_gemm, counting the tiles of all products.
+ *
+ * Errors: those of tg_gemm, with the byte spans taken over the whole batch
+ * (C's span, from C_0 to the end of C_(batch-1), may overlap neither A's nor
+ * B's), plus TG_ERR_INVALID_ARG for a negative batch or stride or for
+ * overlapping C matrices, and TG_ERR_UNSUPPORTED for batch > 65535 or more
+ * than 2^31 tiles of 128 x 64 in the whole batch.  Ownership, asynchrony
+ * and thread safety are as for tg_gemm.
+ */
+tg_status tg_gemm_batched(int64_t batch, int64_t M, int64_t N, int64_t K,
+                          const void* A, int64_t lda, int64_t strideA,
+                          const void* B, int64_t ldb, int64_t strideB,
+                          void* C, int64_t ldc, int64_t strideC,
+                          tg_dtype in_dtype, tg_dtype out_dtype,
+                          tg_stream_t stream);
+
 /* Activation of the fused epilogue (tg_gemm_ex). */
 typedef enum {
     TG_ACT_NONE = 0, /* identity */
@@ -186,6 +224,12 @@ int tg_gemm_path(int64_t M, int64_t N, int64_t K,
                  const void* B, int64_t ldb,
                  void* C, int64_t ldc,
                  tg_dtype in_dtype, tg_dtype out_dtype);
+/* The path tg_gemm_batched would take for these arguments (same codes). */
+int tg_gemm_batched_path(int64_t batch, int64_t M, int64_t N, int64_t K,
+                         const void* A, int64_t lda, int64_t strideA,
+                         const void* B, int64_t ldb, int64_t strideB,
+                         void* C, int64_t ldc, int64_t strideC,
+                         tg_dtype in_dtype, tg_dtype out_dtype);
 void tg_gemm_force_path(int path);
 
 /*

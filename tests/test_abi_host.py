@@ -232,3 +232,64 @@ def test_product_path_never_imports_oracle():
                 text = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 for needle in ("import oracle", "from oracle", "tg_oracle", "tgo_"):
                     assert needle not in text, f"{f} mentions {needle}"
+
+
+# ------------------------------------------------------------ strided batch
+
+def bpath(batch, M, N, K, sA=None, sB=None, sC=None, A=PA, B=PB, C=PC, lda=None, ldb=None,
+          ldc=None, i=tg.F16, o=tg.F16):
+    lda = K if lda is None else lda
+    ldb = N if ldb is None else ldb
+    ldc = N if ldc is None else ldc
+    sA = M * lda if sA is None else sA
+    sB = K * ldb if sB is None else sB
+    sC = M * ldc if sC is None else sC
+    return tg.tg_gemm_batched_path(batch, M, N, K, A, lda, sA, B, ldb, sB, C, ldc, sC, i, o)
+
+
+def bcall(batch, M, N, K, sA=None, sB=None, sC=None, A=PA, B=PB, C=PC, i=tg.F16, o=tg.F16):
+    sA = M * K if sA is None else sA
+    sB = K * N if sB is None else sB
+    sC = M * N if sC is None else sC
+    return tg.tg_gemm_batched(batch, M, N, K, A, K, sA, B, N, sB, C, N, sC, i, o, 0)
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(batch=-1, M=4, N=4, K=4), tg.TG_ERR_INVALID_ARG),
+    (dict(batch=2, M=4, N=4, K=4, sA=-16), tg.TG_ERR_INVALID_ARG),
+    (dict(batch=2, M=4, N=4, K=4, sC=-16), tg.TG_ERR_INVALID_ARG),
+    (dict(batch=65536, M=4, N=4, K=4), tg.TG_ERR_UNSUPPORTED),
+    # C matrices overlapping one another
+    (dict(batch=2, M=4, N=8, K=4, sC=3 * 8 + 7), tg.TG_ERR_INVALID_ARG),
+    (dict(batch=3, M=4, N=8, K=4, sC=0), tg.TG_ERR_INVALID_ARG),
+    # C's span over the batch reaching into A's (fake A after C: C=PA - 8 KB)
+    (dict(batch=64, M=16, N=16, K=16, C=PA - 8192), tg.TG_ERR_INVALID_ARG),
+    # more than 2^31 tiles in the whole batch
+    (dict(batch=65535, M=2 ** 20, N=2 ** 20, K=8), tg.TG_ERR_UNSUPPORTED),
+])
+def test_batched_arguments_rejected_on_host(args, status):
+    assert bcall(**args) == status
+    b = dict(args)
+    assert bpath(b.pop("batch"), b.pop("M"), b.pop("N"), b.pop("K"), **b) == 0
+
+
+def test_batched_degenerate_sizes_are_noops():
+    assert bcall(0, 4, 4, 4, A=0, B=0, C=0) == tg.TG_OK
+    assert bcall(3, 0, 4, 4, A=0, B=0, C=0) == tg.TG_OK
+    assert bpath(3, 5, 7, 0, A=0, B=0) == 1        # K == 0: zeros in every C_b
+
+
+def test_batched_path_selection():
+    assert bpath(1, 8192, 8192, 8192) == 6
+    assert bpath(16, 512, 512, 256) == 6            # 4 pair tiles x 16 = 64
+    assert bpath(15, 512, 512, 256) == 3            # 60 pair tiles
+    assert bpath(8, 16, 4096, 4096) == 5            # skinny, one cluster row per matrix
+    assert bpath(4, 128, 128, 128, i=tg.F32, o=tg.F32) == 2
+    assert bpath(4, 256, 256, 256, sA=0) == 3       # broadcast A: TMA map of one matrix
+    assert bpath(4, 256, 256, 256, sB=0) == 3
+    assert bpath(4, 256, 256, 256, sA=256 * 256 + 8) == 3   # padded stride
+    # strides the TMA engine cannot walk: odd, or overlapping operand matrices
+    assert bpath(4, 256, 256, 256, sA=256 * 256 + 4) == 4
+    assert bpath(4, 256, 256, 256, sB=128 * 256) == 4
+    # a single matrix ignores the strides
+    assert bpath(1, 256, 256, 256, sA=5, sB=3, sC=1) == 3

@@ -19,8 +19,8 @@ __all__ = [
     "F16", "F32", "TG_OK", "TG_ERR_INVALID_ARG", "TG_ERR_UNSUPPORTED", "TG_ERR_CUDA",
     "TG_ERR_TIMEOUT", "PATHS", "TgError", "lib", "library_path", "tg_gemm", "tg_gemm_check",
     "tg_status_string", "tg_gemm_path", "tg_gemm_force_path", "tg_gemm_force_tiling",
-    "tg_gemm_test_hook", "tg_gemm_ex", "ACT_NONE", "ACT_RELU", "ACT_GELU",
-    "tg_gemm_version", "gemm",
+    "tg_gemm_test_hook", "tg_gemm_ex", "tg_gemm_batched", "tg_gemm_batched_path", "ACT_NONE", "ACT_RELU", "ACT_GELU",
+    "tg_gemm_version", "gemm", "bmm",
     "check",
 ]
 
@@ -70,6 +70,12 @@ def lib() -> ctypes.CDLL:
         L.tg_gemm_ex.restype = i32
         L.tg_gemm_ex.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, i32,
                                  ctypes.c_float, ctypes.c_float, vp, i64, vp, i32, vp]
+        L.tg_gemm_batched.restype = i32
+        L.tg_gemm_batched.argtypes = [i64, i64, i64, i64, vp, i64, i64, vp, i64, i64, vp, i64, i64,
+                                      i32, i32, vp]
+        L.tg_gemm_batched_path.restype = i32
+        L.tg_gemm_batched_path.argtypes = [i64, i64, i64, i64, vp, i64, i64, vp, i64, i64, vp,
+                                           i64, i64, i32, i32]
         L.tg_gemm_check.restype = i32
         L.tg_gemm_check.argtypes = [vp]
         L.tg_status_string.restype = ctypes.c_char_p
@@ -102,6 +108,19 @@ def tg_gemm_ex(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, alpha, beta
     return int(lib().tg_gemm_ex(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype,
                                 float(alpha), float(beta), D or None, ldd, bias or None,
                                 int(act), stream))
+
+
+def tg_gemm_batched(batch, M, N, K, A, lda, sA, B, ldb, sB, C, ldc, sC, in_dtype, out_dtype,
+                    stream=0) -> int:
+    """Enqueue C_b = A_b x B_b, X_b = X + b*sX elements, for b < batch."""
+    return int(lib().tg_gemm_batched(batch, M, N, K, A, lda, sA, B, ldb, sB, C, ldc, sC,
+                                     in_dtype, out_dtype, stream))
+
+
+def tg_gemm_batched_path(batch, M, N, K, A, lda, sA, B, ldb, sB, C, ldc, sC, in_dtype,
+                         out_dtype) -> int:
+    return int(lib().tg_gemm_batched_path(batch, M, N, K, A, lda, sA, B, ldb, sB, C, ldc, sC,
+                                          in_dtype, out_dtype))
 
 
 def tg_gemm_check(stream=0) -> int:
@@ -196,6 +215,37 @@ def gemm(a, b, out=None, out_dtype=None, stream=None, alpha=1.0, beta=0.0, d=Non
                         b_ptr, act, _stream_handle(stream))
     if st != TG_OK:
         raise TgError(st)
+    return out
+
+
+def bmm(a, b, out=None, out_dtype=None, stream=None):
+    """C[i] = A[i] x B[i] for 3-D CUDA tensors (rows contiguous; a batch
+    stride of 0, as from expand(), broadcasts one matrix).  Allocates C with
+    torch unless `out` is given."""
+    import torch
+    if a.dim() != 3 or b.dim() != 3 or not (a.is_cuda and b.is_cuda):
+        raise ValueError("operands must be 3-D CUDA tensors")
+    batch, M, K = a.shape
+    b2, K2, N = b.shape
+    if K != K2 or batch != b2:
+        raise ValueError("batch or inner dimensions differ")
+    if out is None:
+        od = out_dtype if out_dtype is not None else a.dtype
+        out = torch.empty((batch, M, N), dtype=od, device=a.device)
+
+    def ld3(t):
+        if t.size(2) > 1 and t.stride(2) != 1:
+            raise ValueError("rows must be contiguous (row-major)")
+        ld = int(t.stride(1)) if t.size(1) > 1 else max(int(t.size(2)), 1)
+        sb = int(t.stride(0)) if t.size(0) > 1 else 0
+        return ld, sb
+
+    (lda, sa), (ldb, sb), (ldc, sc) = ld3(a), ld3(b), ld3(out)
+    st = tg_gemm_batched(batch, M, N, K, a.data_ptr(), lda, sa, b.data_ptr(), ldb, sb,
+                         out.data_ptr(), ldc, sc, _code(a.dtype), _code(out.dtype),
+                         _stream_handle(stream))
+    if st != TG_OK:
+        raise TgError(st, "tg_gemm_batched")
     return out
 
 

@@ -36,9 +36,15 @@ constexpr int TN = 4;
 constexpr int kThreads = (BM / TM) * (BN / TN);  // 256
 
 __global__ void __launch_bounds__(kThreads)
-gemm_simt_f32_kernel(const float* __restrict__ A, long long lda, const float* __restrict__ B,
-                     long long ldb, float* C, long long ldc, int M, int N, int K, Epilogue epi)
+gemm_simt_f32_kernel(const float* __restrict__ A0, long long lda, const float* __restrict__ B0,
+                     long long ldb, float* C0, long long ldc, int M, int N, int K, Epilogue epi,
+                     BatchArgs bt)
 {
+    // grid.z walks the matrices of a strided batch
+    const long long bz = blockIdx.z;
+    const float* const A = A0 + bz * bt.sA;
+    const float* const B = B0 + bz * bt.sB;
+    float* const C = C0 + bz * bt.sC;
     __shared__ __align__(16) float As[2][BK][BM + 4];  // +4: fewer bank conflicts on the transposing store
     __shared__ __align__(16) float Bs[2][BK][BN];
 
@@ -113,16 +119,18 @@ gemm_simt_f32_kernel(const float* __restrict__ A, long long lda, const float* __
     }
 }
 
-// K == 0 with a fused epilogue: the product is the empty sum, so each element
-// is act(beta * D + bias).  One thread per column, rows strided over grid.y.
+// K == 0: the product is the empty sum, so each element is act(beta * D +
+// bias), or 0 without an epilogue.  One thread per column, rows strided over
+// grid.y, the matrices of a strided batch over grid.z.
 template <bool OUT_F32>
 __global__ void __launch_bounds__(256)
-epilogue_only_kernel(void* C, long long ldc, int M, int N, Epilogue epi)
+epilogue_only_kernel(void* C0, long long ldc, int M, int N, Epilogue epi, long long sC)
 {
     const int n = blockIdx.x * 256 + static_cast<int>(threadIdx.x);
     if (n >= N) return;
+    void* const C = batch_ptr(C0, static_cast<int>(blockIdx.z), sC, OUT_F32 ? 4 : 2);
     for (int m = blockIdx.y; m < M; m += gridDim.y) {
-        const float y = epilogue_elem<OUT_F32>(0.0f, m, n, epi);
+        const float y = epi.on ? epilogue_elem<OUT_F32>(0.0f, m, n, epi) : 0.0f;
         const long long i = static_cast<long long>(m) * ldc + n;
         if constexpr (OUT_F32)
             static_cast<float*>(C)[i] = y;
@@ -137,21 +145,22 @@ cudaError_t launch_epilogue_only(const GemmArgs& a)
 {
     const unsigned gx = static_cast<unsigned>((static_cast<long long>(a.N) + 255) / 256);
     const unsigned gy = static_cast<unsigned>(a.M < 65535 ? a.M : 65535);
-    const dim3 grid(gx, gy);
+    if (a.batch > 65535) return cudaErrorInvalidConfiguration;
+    const dim3 grid(gx, gy, a.batch);
     if (a.out_f32)
-        epilogue_only_kernel<true><<<grid, 256, 0, a.stream>>>(a.C, a.ldc, a.M, a.N, a.epi);
+        epilogue_only_kernel<true><<<grid, 256, 0, a.stream>>>(a.C, a.ldc, a.M, a.N, a.epi, a.sC);
     else
-        epilogue_only_kernel<false><<<grid, 256, 0, a.stream>>>(a.C, a.ldc, a.M, a.N, a.epi);
+        epilogue_only_kernel<false><<<grid, 256, 0, a.stream>>>(a.C, a.ldc, a.M, a.N, a.epi, a.sC);
     return cudaGetLastError();
 }
 
 cudaError_t launch_simt_f32(const GemmArgs& a)
 {
-    const dim3 grid((a.N + BN - 1) / BN, (a.M + BM - 1) / BM);
-    if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
+    const dim3 grid((a.N + BN - 1) / BN, (a.M + BM - 1) / BM, a.batch);
+    if (grid.y > 65535u || grid.z > 65535u) return cudaErrorInvalidConfiguration;
     gemm_simt_f32_kernel<<<grid, kThreads, 0, a.stream>>>(
         static_cast<const float*>(a.A), a.lda, static_cast<const float*>(a.B), a.ldb,
-        static_cast<float*>(a.C), a.ldc, a.M, a.N, a.K, a.epi);
+        static_cast<float*>(a.C), a.ldc, a.M, a.N, a.K, a.epi, a.batch_args());
     return cudaGetLastError();
 }
 

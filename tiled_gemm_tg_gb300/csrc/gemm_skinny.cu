@@ -71,7 +71,7 @@ template <int MP, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmBT,
                    void* C, long long ldc, int M, int N, int K, int split,
-                   int hook, unsigned int* err, Epilogue epi)
+                   int hook, unsigned int* err, Epilogue epi, BatchArgs bt)
 {
     using Cfg = SkinnyCfg<MP>;
     extern __shared__ uint8_t smem_raw[];
@@ -88,6 +88,8 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     const int lane = threadIdx.x & 31;
     const int rank = static_cast<int>(cluster_ctarank());  // == blockIdx.x (cluster spans x)
     const int n0 = blockIdx.y * BNT;
+    const int bz = static_cast<int>(blockIdx.z);  // matrix of the batch
+    void* const Cb = batch_ptr(C, bz, bt.sC, OUT_F32 ? 4 : 2);
     const int nkb = (K + BK - 1) / BK;
     const int kb0 = static_cast<int>(static_cast<long long>(rank) * nkb / split);
     const int kb1 = static_cast<int>(static_cast<long long>(rank + 1) * nkb / split);
@@ -141,10 +143,11 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 mbar_arrive_expect_tx(fb, Cfg::STAGE);
 #pragma unroll
                 for (int j = 0; j < BNT / 64; ++j)
-                    tma_load_2d(sa + j * BT_BOX, &tmBT, fb, n0 + j * 64, kb * BK);
+                    tma_load_3d(sa + j * BT_BOX, &tmBT, fb, n0 + j * 64, kb * BK, bz * bt.zb);
 #pragma unroll
                 for (int j = 0; j < BK / 64; ++j)
-                    tma_load_2d(sa + BT_STAGE + j * Cfg::A_ATOM, &tmA, fb, kb * BK + j * 64, 0);
+                    tma_load_3d(sa + BT_STAGE + j * Cfg::A_ATOM, &tmA, fb, kb * BK + j * 64, 0,
+                                bz * bt.za);
                 ++issued;
                 if (++s == STAGES) {
                     s = 0;
@@ -242,9 +245,9 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 sum += ld_dsmem_f32(mapa_shared(red_local + off, static_cast<uint32_t>(r)));
             if (epi.on) sum = epilogue_elem<OUT_F32>(sum, m, n, epi);
             if constexpr (OUT_F32)
-                static_cast<float*>(C)[static_cast<long long>(m) * ldc + n] = sum;
+                static_cast<float*>(Cb)[static_cast<long long>(m) * ldc + n] = sum;
             else
-                static_cast<__half*>(C)[static_cast<long long>(m) * ldc + n] = __float2half_rn(sum);
+                static_cast<__half*>(Cb)[static_cast<long long>(m) * ldc + n] = __float2half_rn(sum);
         }
     }
 
@@ -315,20 +318,20 @@ cudaError_t launch_cfg(const GemmArgs& a)
             }
             g_attr_set[dev][slot] = true;
         }
-        split = choose_split((a.N + BNT - 1) / BNT, (a.K + BK - 1) / BK, a.num_sms,
-                             g_max_clusters[dev][slot]);
+        split = choose_split(static_cast<long long>((a.N + BNT - 1) / BNT) * a.batch,
+                             (a.K + BK - 1) / BK, a.num_sms, g_max_clusters[dev][slot]);
     }
     CUtensorMap ta, tbt;
     if (!encode_tmap_f16(&ta, a.A, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M),
-                         static_cast<uint64_t>(a.lda), 64, MP))
+                         static_cast<uint64_t>(a.lda), a.batch, a.sA, 64, MP))
         return cudaErrorInvalidValue;
     if (!encode_tmap_f16(&tbt, a.B, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
-                         static_cast<uint64_t>(a.ldb), 64, BK))
+                         static_cast<uint64_t>(a.ldb), a.batch, a.sB, 64, BK))
         return cudaErrorInvalidValue;
     const int n_tiles = (a.N + BNT - 1) / BNT;
-    if (n_tiles > 65535) return cudaErrorInvalidConfiguration;
+    if (n_tiles > 65535 || a.batch > 65535) return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(split, n_tiles);
+    cfg.gridDim = dim3(split, n_tiles, a.batch);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = Cfg::SMEM;
     cfg.stream = a.stream;
@@ -340,7 +343,7 @@ cudaError_t launch_cfg(const GemmArgs& a)
     cfg.attrs = at;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, ta, tbt, a.C, a.ldc, a.M, a.N, a.K, split, a.hook, a.err,
-                              a.epi);
+                              a.epi, a.batch_args());
 }
 
 }  // namespace

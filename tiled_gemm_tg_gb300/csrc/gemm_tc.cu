@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     void* C, long long ldc, int M, int N, int K, int tiles_m,
                     int tiles_n, int group_m, int c_vec, int hook, unsigned int* err,
-                    Epilogue epi)
+                    Epilogue epi, BatchArgs bt)
 {
     using Cfg = MainCfg<BN>;
     constexpr int STAGES = Cfg::STAGES;
@@ -122,7 +122,7 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const uint32_t tmem_base = tmem_slot;
 
     const int num_kb = (K + BK - 1) / BK;
-    const int total = tiles_m * tiles_n;
+    const int total = tiles_m * tiles_n * bt.count;
     // The epilogue waits for a whole tile's main loop; allow ~64 us per k-block
     // on top of the base limit so long-K problems never time out spuriously.
     const uint32_t epi_limit = kSlowPolls + 64u * static_cast<uint32_t>(min(num_kb, 1 << 20));
@@ -134,8 +134,9 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t ph = 0;
             uint32_t issued = 0;
             for (int t = blockIdx.x; t < total; t += gridDim.x) {
-                int tm, tn;
-                tile_coords(t, tiles_m, tiles_n, group_m, tm, tn);
+                int b, tm, tn;
+                batch_tile_coords(t, tiles_m, tiles_n, group_m, b, tm, tn);
+                const int za = b * bt.za, zb = b * bt.zb;
                 bool ok = true;
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1u, &abort_flag)) {
@@ -156,10 +157,11 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const uint32_t fb = smem_u32(&full_bar[s]);
                     const uint32_t sa = base + s * Cfg::STAGE;
                     mbar_arrive_expect_tx(fb, Cfg::STAGE);
-                    tma_load_2d(sa, &tmA, fb, kb * BK, tm * BM);
+                    tma_load_3d(sa, &tmA, fb, kb * BK, tm * BM, za);
 #pragma unroll
                     for (int j = 0; j < BN / 64; ++j)
-                        tma_load_2d(sa + A_STAGE + j * B_BOX, &tmB, fb, tn * BN + j * 64, kb * BK);
+                        tma_load_3d(sa + A_STAGE + j * B_BOX, &tmB, fb, tn * BN + j * 64, kb * BK,
+                                    zb);
                     ++issued;
                     if (++s == STAGES) {
                         s = 0;
@@ -240,8 +242,9 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         int acc = 0;
         uint32_t aph = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            int tm, tn;
-            tile_coords(t, tiles_m, tiles_n, group_m, tm, tn);
+            int b, tm, tn;
+            batch_tile_coords(t, tiles_m, tiles_n, group_m, b, tm, tn);
+            void* Cb = batch_ptr(C, b, bt.sC, OUT_F32 ? 4 : 2);
             const bool got = mbar_wait(smem_u32(&tfull_bar[acc]), aph, &abort_flag, epi_limit);
             if (!__all_sync(0xffffffffu, got)) {
                 if (lane == 0) {
@@ -262,7 +265,7 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const int n = tn * BN + c;
                 if (m < M && n < N) {
                     if (epi.on) epilogue_chunk<OUT_F32>(r, m, n, N, epi);
-                    store_chunk<OUT_F32>(C, ldc, m, n, N, r, c_vec != 0);
+                    store_chunk<OUT_F32>(Cb, ldc, m, n, N, r, c_vec != 0);
                 }
             }
             tc_fence_before();
@@ -304,30 +307,31 @@ cudaError_t launch_cfg(const GemmArgs& a)
     }
     CUtensorMap ta, tb;
     if (!encode_tmap_f16(&ta, a.A, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M),
-                         static_cast<uint64_t>(a.lda), BK, BM))
+                         static_cast<uint64_t>(a.lda), a.batch, a.sA, BK, BM))
         return cudaErrorInvalidValue;
     if (!encode_tmap_f16(&tb, a.B, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
-                         static_cast<uint64_t>(a.ldb), 64, BK))
+                         static_cast<uint64_t>(a.ldb), a.batch, a.sB, 64, BK))
         return cudaErrorInvalidValue;
     const int tiles_m = (a.M + BM - 1) / BM;
     const int tiles_n = (a.N + BN - 1) / BN;
-    const int total = tiles_m * tiles_n;
+    const int total = tiles_m * tiles_n * a.batch;
     const int grid = total < a.num_sms ? total : a.num_sms;
     const int group_m = a.group_m > 0 ? a.group_m : 16;
     const size_t es = OUT_F32 ? 4 : 2;
     const int c_vec = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) &&
-                      ((static_cast<size_t>(a.ldc) * es) % 16 == 0);
+                      ((static_cast<size_t>(a.ldc) * es) % 16 == 0) &&
+                      ((static_cast<size_t>(a.sC) * es) % 16 == 0);
     kernel<<<grid, kThreads, Cfg::SMEM, a.stream>>>(ta, tb, a.C, a.ldc, a.M, a.N, a.K, tiles_m,
                                                      tiles_n, group_m, c_vec, a.hook, a.err,
-                                                     a.epi);
+                                                     a.epi, a.batch_args());
     return cudaGetLastError();
 }
 
 }  // namespace
 
-int main_tile_n(int M, int N, int num_sms)
+int main_tile_n(int M, int N, int batch, int num_sms)
 {
-    const long long tm = (M + BM - 1) / BM;
+    const long long tm = static_cast<long long>((M + BM - 1) / BM) * batch;
     if (tm * ((N + 255) / 256) >= num_sms) return 256;
     if (tm * ((N + 127) / 128) >= num_sms / 2) return 128;
     return 64;

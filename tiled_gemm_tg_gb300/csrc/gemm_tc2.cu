@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     void* C, long long ldc, int M, int N, int K, int tiles_m,
                     int tiles_n, int group_m, int c_vec, int hook, unsigned int* err,
-                    Epilogue epi)
+                    Epilogue epi, BatchArgs bt)
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[STAGES];   // used in the leader only
@@ -135,7 +135,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const uint32_t tmem_base = tmem_slot;
 
     const int num_kb = (K + BK - 1) / BK;
-    const int total = tiles_m * tiles_n;
+    const int total = tiles_m * tiles_n * bt.count;
     const uint32_t epi_limit = kSlowPolls + 64u * static_cast<uint32_t>(min(num_kb, 1 << 20));
 
     if (warp == 0) {
@@ -151,8 +151,9 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t issued = 0;
             bool ok = true;
             for (int t = pair; t < total && ok; t += npairs) {
-                int tm, tn;
-                tile_coords(t, tiles_m, tiles_n, group_m, tm, tn);
+                int b, tm, tn;
+                batch_tile_coords(t, tiles_m, tiles_n, group_m, b, tm, tn);
+                const int za = b * bt.za, zb = b * bt.zb;
                 const int row = tm * PM + static_cast<int>(rank) * HM;
                 const int col = tn * PN + static_cast<int>(rank) * HN;
                 for (int kb = 0; kb < num_kb; ++kb) {
@@ -176,12 +177,12 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const uint32_t sa = base + s * STAGE;
 #pragma unroll
                     for (int j = 0; j < KA; ++j)
-                        tma_load_2d_pair_hint(sa + j * A_ATOM, &tmA, fb, kb * BK + j * 64, row,
-                                              pol_a);
+                        tma_load_3d_pair_hint(sa + j * A_ATOM, &tmA, fb, kb * BK + j * 64, row,
+                                              za, pol_a);
 #pragma unroll
                     for (int j = 0; j < HN / 64; ++j)
-                        tma_load_2d_pair_hint(sa + A_STAGE + j * B_BOX, &tmB, fb, col + j * 64,
-                                              kb * BK, pol_b);
+                        tma_load_3d_pair_hint(sa + A_STAGE + j * B_BOX, &tmB, fb, col + j * 64,
+                                              kb * BK, zb, pol_b);
                     ++issued;
                     if (++s == STAGES) {
                         s = 0;
@@ -265,8 +266,9 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         int acc = 0;
         uint32_t aph = 0;
         for (int t = pair; t < total; t += npairs) {
-            int tm, tn;
-            tile_coords(t, tiles_m, tiles_n, group_m, tm, tn);
+            int b, tm, tn;
+            batch_tile_coords(t, tiles_m, tiles_n, group_m, b, tm, tn);
+            void* Cb = batch_ptr(C, b, bt.sC, OUT_F32 ? 4 : 2);
             const bool got = mbar_wait(smem_u32(&tfull_bar[acc]), aph, &abort_flag, epi_limit);
             if (!__all_sync(0xffffffffu, got)) {
                 if (lane == 0) {
@@ -291,7 +293,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const int n = tn * PN + c + j;
                     if (m < M && n < N) {
                         if (epi.on) epilogue_chunk<OUT_F32>(r + j, m, n, N, epi);
-                        store_chunk<OUT_F32>(C, ldc, m, n, N, r + j, c_vec != 0);
+                        store_chunk<OUT_F32>(Cb, ldc, m, n, N, r + j, c_vec != 0);
                     }
                 }
             }
@@ -351,19 +353,20 @@ cudaError_t launch_cfg(const GemmArgs& a)
     }
     CUtensorMap ta, tb;
     if (!encode_tmap_f16(&ta, a.A, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M),
-                         static_cast<uint64_t>(a.lda), 64, HM))
+                         static_cast<uint64_t>(a.lda), a.batch, a.sA, 64, HM))
         return cudaErrorInvalidValue;
     if (!encode_tmap_f16(&tb, a.B, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
-                         static_cast<uint64_t>(a.ldb), 64, BK))
+                         static_cast<uint64_t>(a.ldb), a.batch, a.sB, 64, BK))
         return cudaErrorInvalidValue;
     const int tiles_m = (a.M + PM - 1) / PM;
     const int tiles_n = (a.N + PN - 1) / PN;
-    const int total = tiles_m * tiles_n;
+    const int total = tiles_m * tiles_n * a.batch;
     const int pairs = total < max_clusters ? total : max_clusters;
     const int group_m = a.group_m > 0 ? a.group_m : 8;
     const size_t es = OUT_F32 ? 4 : 2;
     const int c_vec = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) &&
-                      ((static_cast<size_t>(a.ldc) * es) % 16 == 0);
+                      ((static_cast<size_t>(a.ldc) * es) % 16 == 0) &&
+                      ((static_cast<size_t>(a.sC) * es) % 16 == 0);
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * pairs);
@@ -378,7 +381,7 @@ cudaError_t launch_cfg(const GemmArgs& a)
     cfg.attrs = at;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, ta, tb, a.C, a.ldc, a.M, a.N, a.K, tiles_m, tiles_n,
-                              group_m, c_vec, a.hook, a.err, a.epi);
+                              group_m, c_vec, a.hook, a.err, a.epi, a.batch_args());
 }
 
 }  // namespace

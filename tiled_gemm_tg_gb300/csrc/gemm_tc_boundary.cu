@@ -137,10 +137,15 @@ __device__ __forceinline__ void stash(const Frag& f, uint8_t* sA, uint8_t* sB, i
 
 template <bool OUT_F32>
 __global__ void __launch_bounds__(kThreads)
-gemm_tc_boundary_kernel(const __half* __restrict__ A, long long lda, const __half* __restrict__ B,
-                        long long ldb, void* C, long long ldc, int M, int N, int K,
-                        int hook, unsigned int* err, Epilogue epi)
+gemm_tc_boundary_kernel(const __half* __restrict__ A0, long long lda, const __half* __restrict__ B0,
+                        long long ldb, void* C0, long long ldc, int M, int N, int K,
+                        int hook, unsigned int* err, Epilogue epi, BatchArgs bt)
 {
+    // grid.z walks the matrices of a strided batch
+    const int bz = static_cast<int>(blockIdx.z);
+    const __half* const A = A0 + static_cast<long long>(bz) * bt.sA;
+    const __half* const B = B0 + static_cast<long long>(bz) * bt.sB;
+    void* const C = batch_ptr(C0, bz, bt.sC, OUT_F32 ? 4 : 2);
     // An operand whose base and row stride are both 16-byte multiples is read
     // with 16-byte loads (at most one of A and B is, or the TMA path serves).
     const bool a_vec = (reinterpret_cast<uintptr_t>(A) & 15u) == 0 && (lda & 7) == 0;
@@ -276,11 +281,11 @@ cudaError_t launch_cfg(const GemmArgs& a)
             g_attr_set[dev][OUT_F32 ? 1 : 0] = true;
         }
     }
-    const dim3 grid((a.N + BN - 1) / BN, (a.M + BM - 1) / BM);
-    if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
+    const dim3 grid((a.N + BN - 1) / BN, (a.M + BM - 1) / BM, a.batch);
+    if (grid.y > 65535u || grid.z > 65535u) return cudaErrorInvalidConfiguration;
     kernel<<<grid, kThreads, SMEM, a.stream>>>(
         static_cast<const __half*>(a.A), a.lda, static_cast<const __half*>(a.B), a.ldb, a.C, a.ldc,
-        a.M, a.N, a.K, a.hook, a.err, a.epi);
+        a.M, a.N, a.K, a.hook, a.err, a.epi, a.batch_args());
     return cudaGetLastError();
 }
 

@@ -83,28 +83,16 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// 2-D tiled bulk-tensor load global -> shared, completing on `bar` with the
-// box's byte count.  x is the innermost (contiguous) coordinate.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int32_t x, int32_t y)
+// 3-D tiled bulk-tensor load global -> shared, completing on `bar` with the
+// box's byte count.  x is the innermost (contiguous) coordinate, y the row,
+// z the matrix of a batch (0 for a single matrix).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t x, int32_t y, int32_t z)
 {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
-        : "memory");
-}
-
-// Same, with an L2 eviction-priority hint (a createpolicy cache policy).
-__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map,
-                                                 uint32_t bar, int32_t x, int32_t y,
-                                                 uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y),
-        "l"(policy)
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
         : "memory");
 }
 
@@ -271,25 +259,17 @@ __device__ __forceinline__ void cluster_sync()
 
 // TMA load into this CTA's shared memory whose completion is signalled on an
 // mbarrier that may live in the peer CTA (`bar` is a shared::cluster address).
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
-                                                 uint32_t bar, int32_t x, int32_t y)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile"
-        ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
-        : "memory");
-}
-
-// Same, with an L2 eviction-priority hint (a createpolicy cache policy).
-__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtensorMap* map,
+// With an L2 eviction-priority hint (a createpolicy cache policy); x, y, z
+// as for tma_load_3d.
+__device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const CUtensorMap* map,
                                                       uint32_t bar, int32_t x, int32_t y,
-                                                      uint64_t policy)
+                                                      int32_t z, uint64_t policy)
 {
     asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile"
-        ".mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile"
+        ".mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z),
+        "l"(policy)
         : "memory");
 }
 

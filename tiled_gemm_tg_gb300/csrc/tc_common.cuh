@@ -25,6 +25,22 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
     tn = r / gs;
 }
 
+// Tile t of a strided batch of matrices, each tiles_m x tiles_n tiles walked
+// in the grouped order: b is the matrix, (tm, tn) the tile inside it.
+__device__ __forceinline__ void batch_tile_coords(int t, int tiles_m, int tiles_n, int group_m,
+                                                  int& b, int& tm, int& tn)
+{
+    const int per = tiles_m * tiles_n;
+    b = t / per;
+    tile_coords(t - b * per, tiles_m, tiles_n, group_m, tm, tn);
+}
+
+// Matrix b of a strided batch of C (stride sC elements of es bytes).
+__device__ __forceinline__ void* batch_ptr(void* C, int b, long long sC, int es)
+{
+    return static_cast<char*>(C) + static_cast<long long>(b) * sC * es;
+}
+
 // GELU is x * Phi(x) with Phi the standard normal distribution function,
 // written as 0.5 * x * erfc(-x / sqrt(2)) so the negative tail keeps its
 // relative accuracy.  Kept out of line: the epilogue applies it to 32

@@ -27,6 +27,8 @@ constexpr int kMaxDevices = 64;
 // Largest M, N or K: tile origins (up to a dimension plus one tile) and TMA
 // coordinates stay within int32.
 constexpr int64_t kMaxDim = 2147483647LL - 1023;
+// Largest batch: the kernels that walk a batch over grid.z allow 65535.
+constexpr int64_t kMaxBatch = 65535;
 
 struct DeviceState {
     bool ready = false;
@@ -73,65 +75,103 @@ size_t esize(tg_dtype t) { return t == TG_F16 ? 2 : 4; }
 
 using u128 = unsigned __int128;
 
-// Byte span [lo, hi) touched by a rows x cols row-major matrix with stride ld
-// (rows, cols >= 1).  Computed in 128 bits so no product can wrap.
-void span(const void* p, int64_t rows, int64_t cols, int64_t ld, size_t es, u128* lo, u128* hi)
+// Byte span [lo, hi) touched by `batch` rows x cols row-major matrices with
+// row stride ld and matrix stride `stride` (rows, cols, batch >= 1).
+// Computed in 128 bits so no product can wrap.
+void span(const void* p, int64_t rows, int64_t cols, int64_t ld, size_t es, u128* lo, u128* hi,
+          int64_t batch = 1, int64_t stride = 0)
 {
     *lo = static_cast<u128>(reinterpret_cast<uintptr_t>(p));
-    *hi = *lo + (static_cast<u128>(rows - 1) * static_cast<u128>(ld) + static_cast<u128>(cols)) *
+    *hi = *lo + (static_cast<u128>(batch - 1) * static_cast<u128>(stride) +
+                 static_cast<u128>(rows - 1) * static_cast<u128>(ld) + static_cast<u128>(cols)) *
                     static_cast<u128>(es);
 }
 
 bool overlaps(u128 a0, u128 a1, u128 b0, u128 b1) { return a0 < b1 && b0 < a1; }
 
-// Validation shared by tg_gemm and tg_gemm_path.  On TG_OK, *path is the
-// path the arguments call for (ignoring any forced path).
-tg_status classify(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
-                   int64_t ldb, void* C, int64_t ldc, tg_dtype in_dtype, tg_dtype out_dtype,
-                   int* path)
+// One call's arguments: `batch` products C_b = A_b x B_b, X_b = X + b * sX
+// elements (batch 1 and strides 0 for tg_gemm).
+struct Problem {
+    int64_t batch, M, N, K;
+    const void* A;
+    int64_t lda, sA;
+    const void* B;
+    int64_t ldb, sB;
+    void* C;
+    int64_t ldc, sC;
+    tg_dtype in_dtype, out_dtype;
+};
+
+// The TMA engine addresses a batch of matrices through a 3-D tensor map:
+// a matrix stride that is a multiple of 16 bytes, below 2^40 bytes and at
+// least one whole matrix (or 0, one matrix broadcast to every b).
+bool tma_stride_ok(int64_t stride, int64_t rows, int64_t ld)
+{
+    if (stride == 0) return true;
+    return stride % 8 == 0 && stride < (int64_t(1) << 38) && stride >= rows * ld;
+}
+
+// Validation shared by every entry point.  On TG_OK, *path is the path the
+// arguments call for (ignoring any forced path).
+tg_status classify(const Problem& p, int* path)
 {
     *path = tg::PATH_NONE;
-    if (M < 0 || N < 0 || K < 0) return TG_ERR_INVALID_ARG;
-    const bool pair_ok = (in_dtype == TG_F16 && (out_dtype == TG_F16 || out_dtype == TG_F32)) ||
-                         (in_dtype == TG_F32 && out_dtype == TG_F32);
+    const int64_t M = p.M, N = p.N, K = p.K;
+    if (M < 0 || N < 0 || K < 0 || p.batch < 0) return TG_ERR_INVALID_ARG;
+    if (p.sA < 0 || p.sB < 0 || p.sC < 0) return TG_ERR_INVALID_ARG;
+    const bool pair_ok =
+        (p.in_dtype == TG_F16 && (p.out_dtype == TG_F16 || p.out_dtype == TG_F32)) ||
+        (p.in_dtype == TG_F32 && p.out_dtype == TG_F32);
     if (!pair_ok) return TG_ERR_UNSUPPORTED;
-    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return TG_ERR_UNSUPPORTED;
-    if (M == 0 || N == 0) return TG_OK;
-    if (C == nullptr || ldc < N) return TG_ERR_INVALID_ARG;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim || p.batch > kMaxBatch)
+        return TG_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0 || p.batch == 0) return TG_OK;
+    // every tile index of the whole batch fits in 32 bits
+    if (((M + 127) / 128) * ((N + 63) / 64) * p.batch >= (int64_t(1) << 31))
+        return TG_ERR_UNSUPPORTED;
+    if (p.C == nullptr || p.ldc < N) return TG_ERR_INVALID_ARG;
+    // the matrices of C are disjoint
+    if (p.batch > 1 && p.sC < (M - 1) * p.ldc + N) return TG_ERR_INVALID_ARG;
     // Every element access is naturally aligned: a pointer that is not a
     // multiple of its element size is rejected rather than handed to a kernel.
-    if (reinterpret_cast<uintptr_t>(C) % esize(out_dtype) != 0) return TG_ERR_INVALID_ARG;
+    const size_t ei = esize(p.in_dtype), eo = esize(p.out_dtype);
+    if (reinterpret_cast<uintptr_t>(p.C) % eo != 0) return TG_ERR_INVALID_ARG;
+    u128 c0, c1;
+    span(p.C, M, N, p.ldc, eo, &c0, &c1, p.batch, p.sC);
+    const u128 top = static_cast<u128>(1) << 64;  // a span past the address space cannot exist
+    if (c1 > top) return TG_ERR_INVALID_ARG;
     if (K == 0) {
         *path = tg::PATH_ZERO;
         return TG_OK;
     }
-    if (A == nullptr || B == nullptr || lda < K || ldb < N) return TG_ERR_INVALID_ARG;
-    if (reinterpret_cast<uintptr_t>(A) % esize(in_dtype) != 0 ||
-        reinterpret_cast<uintptr_t>(B) % esize(in_dtype) != 0)
+    if (p.A == nullptr || p.B == nullptr || p.lda < K || p.ldb < N) return TG_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(p.A) % ei != 0 || reinterpret_cast<uintptr_t>(p.B) % ei != 0)
         return TG_ERR_INVALID_ARG;
-    u128 c0, c1, a0, a1, b0, b1;
-    span(C, M, N, ldc, esize(out_dtype), &c0, &c1);
-    span(A, M, K, lda, esize(in_dtype), &a0, &a1);
-    span(B, K, N, ldb, esize(in_dtype), &b0, &b1);
-    const u128 top = static_cast<u128>(1) << 64;  // a span past the address space cannot exist
-    if (c1 > top || a1 > top || b1 > top) return TG_ERR_INVALID_ARG;
+    u128 a0, a1, b0, b1;
+    span(p.A, M, K, p.lda, ei, &a0, &a1, p.batch, p.sA);
+    span(p.B, K, N, p.ldb, ei, &b0, &b1, p.batch, p.sB);
+    if (a1 > top || b1 > top) return TG_ERR_INVALID_ARG;
     if (overlaps(c0, c1, a0, a1) || overlaps(c0, c1, b0, b1)) return TG_ERR_INVALID_ARG;
 
-    if (in_dtype == TG_F32) {
+    if (p.in_dtype == TG_F32) {
         *path = tg::PATH_SIMT;
         return TG_OK;
     }
     // The TMA engine needs 16-byte aligned bases and row strides that are
     // multiples of 16 bytes (and below 2^40 bytes).
     const int64_t kMaxTmaLd = int64_t(1) << 38;
-    const bool tma_ok = (reinterpret_cast<uintptr_t>(A) % 16 == 0) &&
-                        (reinterpret_cast<uintptr_t>(B) % 16 == 0) && (lda % 8 == 0) &&
-                        (ldb % 8 == 0) && lda < kMaxTmaLd && ldb < kMaxTmaLd;
+    const bool tma_ok = (reinterpret_cast<uintptr_t>(p.A) % 16 == 0) &&
+                        (reinterpret_cast<uintptr_t>(p.B) % 16 == 0) && (p.lda % 8 == 0) &&
+                        (p.ldb % 8 == 0) && p.lda < kMaxTmaLd && p.ldb < kMaxTmaLd &&
+                        (p.batch == 1 || (tma_stride_ok(p.sA, M, p.lda) &&
+                                          tma_stride_ok(p.sB, K, p.ldb)));
     if (!tma_ok) {
         *path = tg::PATH_BOUNDARY;
     } else if (M <= tg::kSkinnyMaxM) {
         *path = tg::PATH_SKINNY;
-    } else if (tg::pair_tiles(static_cast<int>(M), static_cast<int>(N)) >= tg::kPairMinTiles) {
+    } else if (static_cast<int64_t>(tg::pair_tiles(static_cast<int>(M), static_cast<int>(N))) *
+                   p.batch >=
+               tg::kPairMinTiles) {
         *path = tg::PATH_MAIN_PAIR;
     } else {
         *path = tg::PATH_MAIN;
@@ -196,22 +236,21 @@ tg_status classify_epilogue(int64_t M, int64_t N, void* C, int64_t ldc, tg_dtype
     return TG_OK;
 }
 
-// The body of tg_gemm and tg_gemm_ex once the arguments have been classified.
-tg_status run(int path, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
-              const void* B, int64_t ldb, void* C, int64_t ldc, tg_dtype in_dtype,
-              tg_dtype out_dtype, const tg::Epilogue& epi, tg_stream_t stream)
+// The body of every entry point once the arguments have been classified.
+tg_status run(int path, const Problem& p, const tg::Epilogue& epi, tg_stream_t stream)
 {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (path == tg::PATH_ZERO && !epi.on) {
-        const size_t es = esize(out_dtype);
-        cudaError_t e = cudaMemset2DAsync(C, static_cast<size_t>(ldc) * es, 0,
-                                          static_cast<size_t>(N) * es, static_cast<size_t>(M), s);
+    if (path == tg::PATH_ZERO && !epi.on && p.batch == 1) {
+        const size_t es = esize(p.out_dtype);
+        cudaError_t e = cudaMemset2DAsync(p.C, static_cast<size_t>(p.ldc) * es, 0,
+                                          static_cast<size_t>(p.N) * es,
+                                          static_cast<size_t>(p.M), s);
         return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
     }
     if (path != tg::PATH_ZERO) {
         const int forced = g_force_path.load(std::memory_order_relaxed);
         if (forced != 0) {
-            if (!path_serves(forced, path, in_dtype, M)) return TG_ERR_UNSUPPORTED;
+            if (!path_serves(forced, path, p.in_dtype, p.M)) return TG_ERR_UNSUPPORTED;
             path = forced;
         }
     }
@@ -221,16 +260,20 @@ tg_status run(int path, int64_t M, int64_t N, int64_t K, const void* A, int64_t 
     if (st != TG_OK) return st;
 
     tg::GemmArgs a;
-    a.M = static_cast<int>(M);
-    a.N = static_cast<int>(N);
-    a.K = static_cast<int>(K);
-    a.A = A;
-    a.lda = lda;
-    a.B = B;
-    a.ldb = ldb;
-    a.C = C;
-    a.ldc = ldc;
-    a.out_f32 = (out_dtype == TG_F32);
+    a.M = static_cast<int>(p.M);
+    a.N = static_cast<int>(p.N);
+    a.K = static_cast<int>(p.K);
+    a.batch = static_cast<int>(p.batch);
+    a.sA = p.batch > 1 ? p.sA : 0;
+    a.sB = p.batch > 1 ? p.sB : 0;
+    a.sC = p.batch > 1 ? p.sC : 0;
+    a.A = p.A;
+    a.lda = p.lda;
+    a.B = p.B;
+    a.ldb = p.ldb;
+    a.C = p.C;
+    a.ldc = p.ldc;
+    a.out_f32 = (p.out_dtype == TG_F32);
     a.err = ds->err;
     a.hook = g_test_hook.load(std::memory_order_relaxed);
     a.group_m = g_force_group.load(std::memory_order_relaxed);
@@ -244,7 +287,7 @@ tg_status run(int path, int64_t M, int64_t N, int64_t K, const void* A, int64_t 
         case tg::PATH_SIMT: e = tg::launch_simt_f32(a); break;
         case tg::PATH_MAIN: {
             const int bn = g_force_bn.load(std::memory_order_relaxed);
-            e = tg::launch_main(a, bn != 0 ? bn : tg::main_tile_n(a.M, a.N, a.num_sms));
+            e = tg::launch_main(a, bn != 0 ? bn : tg::main_tile_n(a.M, a.N, a.batch, a.num_sms));
             break;
         }
         case tg::PATH_BOUNDARY: e = tg::launch_boundary(a); break;
@@ -260,14 +303,20 @@ tg_status run(int path, int64_t M, int64_t N, int64_t K, const void* A, int64_t 
 namespace tg {
 
 bool encode_tmap_f16(CUtensorMap* map, const void* ptr, uint64_t cols, uint64_t rows, uint64_t ld,
-                     uint32_t box_cols, uint32_t box_rows)
+                     uint64_t batch, uint64_t stride, uint32_t box_cols, uint32_t box_rows)
 {
     if (!g_encode) return false;
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {ld * 2};
-    cuuint32_t box[2] = {box_cols, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims,
+    if (stride == 0) {
+        // one matrix: the third extent is 1 and its stride only has to be a
+        // legal value (a multiple of 16 bytes covering the matrix)
+        batch = 1;
+        stride = (rows * ld + 7) / 8 * 8;
+    }
+    cuuint64_t dims[3] = {cols, rows, batch};
+    cuuint64_t strides[2] = {ld * 2, stride * 2};
+    cuuint32_t box[3] = {box_cols, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(ptr), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -282,10 +331,24 @@ tg_status tg_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, c
                   int64_t ldb, void* C, int64_t ldc, tg_dtype in_dtype, tg_dtype out_dtype,
                   tg_stream_t stream)
 {
+    const Problem p{1, M, N, K, A, lda, 0, B, ldb, 0, C, ldc, 0, in_dtype, out_dtype};
     int path = tg::PATH_NONE;
-    tg_status st = classify(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, &path);
+    tg_status st = classify(p, &path);
     if (st != TG_OK || path == tg::PATH_NONE) return st;
-    return run(path, M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, tg::Epilogue{}, stream);
+    return run(path, p, tg::Epilogue{}, stream);
+}
+
+tg_status tg_gemm_batched(int64_t batch, int64_t M, int64_t N, int64_t K, const void* A,
+                          int64_t lda, int64_t strideA, const void* B, int64_t ldb,
+                          int64_t strideB, void* C, int64_t ldc, int64_t strideC,
+                          tg_dtype in_dtype, tg_dtype out_dtype, tg_stream_t stream)
+{
+    const Problem p{batch, M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc, strideC,
+                    in_dtype, out_dtype};
+    int path = tg::PATH_NONE;
+    tg_status st = classify(p, &path);
+    if (st != TG_OK || path == tg::PATH_NONE) return st;
+    return run(path, p, tg::Epilogue{}, stream);
 }
 
 tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
@@ -294,14 +357,15 @@ tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda
                      tg_activation act, tg_stream_t stream)
 {
     if (act != TG_ACT_NONE && act != TG_ACT_RELU && act != TG_ACT_GELU) return TG_ERR_INVALID_ARG;
+    const Problem p{1, M, N, K, A, lda, 0, B, ldb, 0, C, ldc, 0, in_dtype, out_dtype};
     int path = tg::PATH_NONE;
-    tg_status st = classify(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, &path);
+    tg_status st = classify(p, &path);
     if (st != TG_OK || path == tg::PATH_NONE) return st;
     tg::Epilogue epi;
     st = classify_epilogue(M, N, C, ldc, out_dtype, alpha, beta, D, ldd, bias,
                            static_cast<int>(act), &epi);
     if (st != TG_OK) return st;
-    return run(path, M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, epi, stream);
+    return run(path, p, epi, stream);
 }
 
 tg_status tg_gemm_check(tg_stream_t stream)
@@ -338,9 +402,18 @@ const char* tg_status_string(tg_status status)
 int tg_gemm_path(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                  int64_t ldb, void* C, int64_t ldc, tg_dtype in_dtype, tg_dtype out_dtype)
 {
+    return tg_gemm_batched_path(1, M, N, K, A, lda, 0, B, ldb, 0, C, ldc, 0, in_dtype, out_dtype);
+}
+
+int tg_gemm_batched_path(int64_t batch, int64_t M, int64_t N, int64_t K, const void* A,
+                         int64_t lda, int64_t strideA, const void* B, int64_t ldb,
+                         int64_t strideB, void* C, int64_t ldc, int64_t strideC,
+                         tg_dtype in_dtype, tg_dtype out_dtype)
+{
+    const Problem p{batch, M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc, strideC,
+                    in_dtype, out_dtype};
     int path = tg::PATH_NONE;
-    if (classify(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, &path) != TG_OK)
-        return tg::PATH_NONE;
+    if (classify(p, &path) != TG_OK) return tg::PATH_NONE;
     const int forced = g_force_path.load(std::memory_order_relaxed);
     if (forced != 0 && path != tg::PATH_ZERO && path != tg::PATH_NONE)
         return path_serves(forced, path, in_dtype, M) ? forced : tg::PATH_NONE;

@@ -46,8 +46,23 @@ struct Epilogue {
     int bias_vec = 0;  // bias is 16-byte aligned
 };
 
+// What a kernel needs to walk a strided batch: the number of matrices,
+// whether A and B advance with the batch index (1) or are broadcast (0), and
+// the matrix strides in elements (the TMA kernels read sA and sB from their
+// tensor maps instead).
+struct BatchArgs {
+    int count = 1;
+    int za = 0;
+    int zb = 0;
+    long long sA = 0, sB = 0, sC = 0;
+};
+
 struct GemmArgs {
     int M, N, K;
+    // Strided batch: matrix b of X starts at X + b * sX elements; a stride of
+    // 0 broadcasts one matrix to every b.  batch == 1 for a single GEMM.
+    int batch = 1;
+    long long sA = 0, sB = 0, sC = 0;
     const void* A;
     long long lda;
     const void* B;
@@ -61,24 +76,40 @@ struct GemmArgs {
     int num_sms;
     cudaStream_t stream;
     Epilogue epi;
+
+    BatchArgs batch_args() const
+    {
+        BatchArgs b;
+        b.count = batch;
+        b.za = sA != 0 ? 1 : 0;
+        b.zb = sB != 0 ? 1 : 0;
+        b.sA = sA;
+        b.sB = sB;
+        b.sC = sC;
+        return b;
+    }
 };
 
-// Encodes a 2-D row-major fp16 tensor map (inner extent `cols`, `rows` rows,
-// row stride `ld` elements) with a box of box_cols x box_rows and 128-byte
-// swizzle.  Returns false if the driver rejects it.
+// Encodes a 3-D tensor map over `batch` row-major matrices of fp16 elements
+// (inner extent `cols`, `rows` rows, row stride `ld` elements, matrix stride
+// `stride` elements; stride 0 maps a single matrix that every batch
+// coordinate must address as z = 0) with a box of box_cols x box_rows x 1 and
+// 128-byte swizzle.  Returns false if the driver rejects it.
 bool encode_tmap_f16(CUtensorMap* map, const void* ptr, uint64_t cols, uint64_t rows,
-                     uint64_t ld, uint32_t box_cols, uint32_t box_rows);
+                     uint64_t ld, uint64_t batch, uint64_t stride, uint32_t box_cols,
+                     uint32_t box_rows);
 
 cudaError_t launch_simt_f32(const GemmArgs& a);
 cudaError_t launch_main(const GemmArgs& a, int bn);
 cudaError_t launch_main_pair(const GemmArgs& a);
 cudaError_t launch_boundary(const GemmArgs& a);
 cudaError_t launch_skinny(const GemmArgs& a);
-// K == 0 with a fused epilogue: C = act(beta * D + bias) elementwise.
+// K == 0: C = act(beta * D + bias) elementwise (zeros without an epilogue),
+// for every matrix of a strided batch.
 cudaError_t launch_epilogue_only(const GemmArgs& a);
 
 // Tile width the main kernel uses for this problem (64, 128 or 256).
-int main_tile_n(int M, int N, int num_sms);
+int main_tile_n(int M, int N, int batch, int num_sms);
 
 // Largest M the skinny kernel serves.
 constexpr int kSkinnyMaxM = 64;

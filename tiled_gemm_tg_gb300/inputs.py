@@ -9,7 +9,8 @@ workload is ``seed_base + 1`` and the B seed ``seed_base + 2``.
 The shapes and distributions are the five workloads the GEMM is judged on:
 the fp32 128^3 triple-loop example, the fp16 edge set, the A[1024,512] x
 B[512,2048] tiling example, the 8192^3 compute-bound square and the two
-skinny/wide shapes.  The pages benchmark on no public dataset, so these
+skinny/wide shapes; and two strided batches (256 products of 256^3, 16 of
+2048^3).  The pages benchmark on no public dataset, so these
 synthetic draws are the whole input set.
 """
 from __future__ import annotations
@@ -30,16 +31,17 @@ class Workload:
     in_dtype: str      # "f16" or "f32"
     out_dtype: str     # "f16" or "f32"
     seed_base: int
+    batch: int = 1     # independent products of this shape (a strided batch)
 
     @property
     def flops(self) -> int:
-        return 2 * self.M * self.N * self.K
+        return 2 * self.batch * self.M * self.N * self.K
 
     def algorithmic_bytes(self) -> int:
-        """A and B read once, C written once."""
+        """A and B read once, C written once (every matrix of the batch)."""
         ein = 2 if self.in_dtype == "f16" else 4
         eout = 2 if self.out_dtype == "f16" else 4
-        return (self.M * self.K + self.K * self.N) * ein + self.M * self.N * eout
+        return self.batch * ((self.M * self.K + self.K * self.N) * ein + self.M * self.N * eout)
 
 
 WORKLOADS = {
@@ -54,6 +56,11 @@ WORKLOADS = {
         Workload("square_8192", 8192, 8192, 8192, "uniform", "f16", "f16", 4000),
         Workload("skinny_16x4096x4096", 16, 4096, 4096, "normal_0.02", "f16", "f16", 5000),
         Workload("wide_4096x16384x4096", 4096, 16384, 4096, "normal_0.02", "f16", "f16", 5100),
+        # strided batches: many small products in one launch, and a few large ones
+        Workload("batched_256x256x256x256", 256, 256, 256, "uniform", "f16", "f16", 6000,
+                 batch=256),
+        Workload("batched_16x2048x2048x2048", 2048, 2048, 2048, "uniform", "f16", "f16", 6100,
+                 batch=16),
     ]
 }
 
@@ -89,8 +96,10 @@ def draw(shape, dist: str, seed: int, dtype: str, k: int | None = None) -> torch
 
 
 def operands(w: Workload, dist: str | None = None):
-    """(A, B) on the CPU for a workload, from its own seeds."""
+    """(A, B) on the CPU for a workload, from its own seeds: M x K and K x N,
+    or batch x M x K and batch x K x N for a strided batch."""
     d = dist or w.dist
-    a = draw((w.M, w.K), d, w.seed_base + 1, w.in_dtype, k=w.K)
-    b = draw((w.K, w.N), d, w.seed_base + 2, w.in_dtype, k=w.K)
+    lead = (w.batch,) if w.batch > 1 else ()
+    a = draw(lead + (w.M, w.K), d, w.seed_base + 1, w.in_dtype, k=w.K)
+    b = draw(lead + (w.K, w.N), d, w.seed_base + 2, w.in_dtype, k=w.K)
     return a, b

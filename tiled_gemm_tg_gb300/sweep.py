@@ -11,6 +11,9 @@ times from one CUDA graph over operand sets rotated past L2, and timed with
 CUDA events.
 
     python -m tiled_gemm_tg_gb300.sweep --shapes 1024x1024x1024,8192x8192x8192
+
+A shape of four numbers, BxMxNxK, is a strided batch of B packed products
+(tg_gemm_batched).
 """
 from __future__ import annotations
 
@@ -31,26 +34,27 @@ def candidates(M: int, N: int, K: int):
     return out
 
 
-def time_config(M, N, K, path, bn, group, reps=50, sets=None):
+def time_config(M, N, K, path, bn, group, reps=50, sets=None, batch=1):
     """Microseconds per launch (CUDA-graph replay), or None if not served."""
     import torch
 
     if sets is None:
-        sets = make_sets(M, N, K)
+        sets = make_sets(M, N, K, batch)
     a0, b0, c0 = sets[0]
+    sa, sb, sc = M * K, K * N, M * N
     tg.tg_gemm_force_path(path)
     if tg.tg_gemm_force_tiling(bn, group) != tg.TG_OK:
         tg.tg_gemm_force_path(0)
         return None
     try:
-        if tg.tg_gemm_path(M, N, K, a0.data_ptr(), K, b0.data_ptr(), N, c0.data_ptr(), N,
-                           tg.F16, tg.F16) != path:
+        if tg.tg_gemm_batched_path(batch, M, N, K, a0.data_ptr(), K, sa, b0.data_ptr(), N, sb,
+                                   c0.data_ptr(), N, sc, tg.F16, tg.F16) != path:
             return None
 
         def launch(i, h):
             a, b, c = sets[i % len(sets)]
-            st = tg.tg_gemm(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N,
-                            tg.F16, tg.F16, h)
+            st = tg.tg_gemm_batched(batch, M, N, K, a.data_ptr(), K, sa, b.data_ptr(), N, sb,
+                                    c.data_ptr(), N, sc, tg.F16, tg.F16, h)
             if st != tg.TG_OK:
                 raise tg.TgError(st)
 
@@ -78,16 +82,16 @@ def time_config(M, N, K, path, bn, group, reps=50, sets=None):
         tg.tg_gemm_force_tiling(0, 0)
 
 
-def make_sets(M, N, K):
+def make_sets(M, N, K, batch=1):
     import torch
 
     dev = torch.device("cuda")
-    set_bytes = (M * K + K * N + M * N) * 2
+    set_bytes = batch * (M * K + K * N + M * N) * 2
     n = max(2, min(64, -(-3 * L2_BYTES // set_bytes)))
     g = torch.Generator(device=dev).manual_seed(7)
-    return [((torch.rand(M, K, device=dev, generator=g) * 2 - 1).half(),
-             (torch.rand(K, N, device=dev, generator=g) * 2 - 1).half(),
-             torch.empty(M, N, dtype=torch.half, device=dev)) for _ in range(n)]
+    return [((torch.rand(batch, M, K, device=dev, generator=g) * 2 - 1).half(),
+             (torch.rand(batch, K, N, device=dev, generator=g) * 2 - 1).half(),
+             torch.empty(batch, M, N, dtype=torch.half, device=dev)) for _ in range(n)]
 
 
 def sweep(shapes, reps=50):
@@ -95,20 +99,22 @@ def sweep(shapes, reps=50):
 
     torch.cuda.set_device(0)
     results = []
-    for (M, N, K) in shapes:
-        sets = make_sets(M, N, K)
+    for shape in shapes:
+        batch, (M, N, K) = (shape[0], shape[1:]) if len(shape) == 4 else (1, shape)
+        sets = make_sets(M, N, K, batch)
         a0, b0, c0 = sets[0]
-        auto_path = tg.tg_gemm_path(M, N, K, a0.data_ptr(), K, b0.data_ptr(), N, c0.data_ptr(),
-                                    N, tg.F16, tg.F16)
-        auto_us = time_config(M, N, K, auto_path, 0, 0, reps, sets)
+        auto_path = tg.tg_gemm_batched_path(batch, M, N, K, a0.data_ptr(), K, M * K,
+                                            b0.data_ptr(), N, K * N, c0.data_ptr(), N, M * N,
+                                            tg.F16, tg.F16)
+        auto_us = time_config(M, N, K, auto_path, 0, 0, reps, sets, batch)
         rows = []
         for path, bn, group in candidates(M, N, K):
-            us = time_config(M, N, K, path, bn, group, reps, sets)
+            us = time_config(M, N, K, path, bn, group, reps, sets, batch)
             if us is not None:
                 rows.append({"path": path, "bn": bn, "group_m": group, "us": us,
-                             "tflops": 2.0 * M * N * K / (us * 1e-6) / 1e12})
+                             "tflops": 2.0 * batch * M * N * K / (us * 1e-6) / 1e12})
         best = min(rows, key=lambda r: r["us"])
-        results.append({"shape": [M, N, K], "auto_path": auto_path, "auto_us": auto_us,
+        results.append({"shape": list(shape), "auto_path": auto_path, "auto_us": auto_us,
                         "best": best, "configs": rows})
         del sets
         torch.cuda.empty_cache()
@@ -129,8 +135,7 @@ def main():
     res = sweep(parse_shapes(args.shapes), args.reps)
     names = {PAIR: "pair 256x256", MAIN: "one-CTA 128x{bn}", SKINNY: "skinny"}
     for r in res:
-        M, N, K = r["shape"]
-        print(f"\n{M}x{N}x{K}: automatic path {r['auto_path']} {r['auto_us']:.1f} us; "
+        print(f"\n{'x'.join(str(v) for v in r['shape'])}: automatic path {r['auto_path']} {r['auto_us']:.1f} us; "
               f"best {names[r['best']['path']].format(bn=r['best']['bn'])} "
               f"group {r['best']['group_m']} {r['best']['us']:.1f} us")
         print("| config | group_m | us | TFLOP/s |")
