@@ -169,7 +169,7 @@ def test_batched_integer_bitwise(path):
 
 
 @pytest.mark.parametrize("batch,M,N,K,want", [
-    (16, 512, 512, 256, PAIR),      # 64 pair tiles over the batch
+    (16, 512, 512, 1024, PAIR),     # 64 pair tiles over the batch
     (6, 300, 200, 128, MAIN),
     (12, 16, 1024, 2048, SKINNY),
     (2, 1, 8, 8, SKINNY),

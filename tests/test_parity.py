@@ -325,7 +325,11 @@ def test_pair_kernel_wave_tails(M, N, K):
     a = inputs.draw((M, K), "normal_rsqrtk", 8400 + M, "f16", k=K)
     b = inputs.draw((K, N), "normal", 8500 + N, "f16")
     pad = lambda x: (x + 7) // 8 * 8  # noqa: E731
-    got, intact, p = run(a, b, torch.float16, lda=pad(K), ldb=pad(N))
+    tg.tg_gemm_force_path(PAIR)  # K < 1024 alone would select the one-CTA kernel
+    try:
+        got, intact, p = run(a, b, torch.float16, lda=pad(K), ldb=pad(N))
+    finally:
+        tg.tg_gemm_force_path(0)
     assert p == PAIR and intact and np.isfinite(got).all()
     _sampled_check(a, b, got, True, 8600 + M, extra_rows=(M - 1,), extra_cols=(N - 1,))
     _matvec_property(a, b, got, True)

@@ -170,8 +170,8 @@ tg_status classify(const Problem& p, int* path)
     } else if (M <= tg::kSkinnyMaxM) {
         *path = tg::PATH_SKINNY;
     } else if (static_cast<int64_t>(tg::pair_tiles(static_cast<int>(M), static_cast<int>(N))) *
-                   p.batch >=
-               tg::kPairMinTiles) {
+                       p.batch >= tg::kPairMinTiles &&
+               K >= tg::kPairMinK && M >= tg::kPairMinMN && N >= tg::kPairMinMN) {
         *path = tg::PATH_MAIN_PAIR;
     } else {
         *path = tg::PATH_MAIN;

@@ -117,8 +117,16 @@ constexpr int kSkinnyMaxM = 64;
 // Number of 256 x 256 tiles the pair kernel would compute.
 int pair_tiles(int M, int N);
 
-// The pair kernel takes over once a problem has at least this many
-// 256 x 256 tiles (enough to occupy most SM pairs in the first wave).
+// The pair kernel takes over once a problem (all products of a batch
+// together) has at least this many 256 x 256 tiles, enough to occupy most SM
+// pairs in the first wave, and each product is large enough for its 256 x 256
+// tiles and 128-deep k-blocks to pay: K >= 1024 and M, N >= 512.  Measured
+// with the configuration sweep: below these the one-CTA kernel's shorter
+// pipeline fill and finer tiles win (8192 x 8192 x 512: 71.5 against 80.3 us;
+// 256 products of 256^3: 19.7 against 25.9 us), above them the pair kernel
+// does (16 products of 2048^3: 169.8 against 180.2 us).
 constexpr int kPairMinTiles = 64;
+constexpr int kPairMinK = 1024;
+constexpr int kPairMinMN = 512;
 
 }  // namespace tg
