@@ -25,6 +25,7 @@ _lib = None
 
 F16 = 1
 F32 = 2
+E4M3 = 3
 
 
 def build(force: bool = False) -> str:
@@ -54,6 +55,7 @@ def _bind(path: str):
     lib.tgo_f64_to_f16.argtypes = [ctypes.c_double]
     lib.tgo_f16_to_f64_n.argtypes = [vp, vp, i64]
     lib.tgo_f64_to_f16_n.argtypes = [vp, vp, i64]
+    lib.tgo_e4m3_to_f64_n.argtypes = [vp, vp, i64]
     lib.tgo_num_threads.restype = ctypes.c_int
     lib.tgo_gemm.restype = ctypes.c_int
     lib.tgo_gemm.argtypes = [i64, i64, i64, vp, i64, vp, i64, ctypes.c_int,
@@ -70,7 +72,8 @@ def _bind(path: str):
 def _operand(x: np.ndarray):
     """Return (array, dtype code, row stride in elements) for a 2-D operand.
 
-    fp16 operands may be given as float16 or as uint16 bit patterns.  Rows
+    fp16 operands may be given as float16 or as uint16 bit patterns, FP8
+    E4M3 operands as uint8 bit patterns.  Rows
     must be unit-stride; the row stride (leading dimension) may exceed the
     row length, as with a sub-matrix view.
     """
@@ -80,6 +83,8 @@ def _operand(x: np.ndarray):
         x = x.view(np.uint16)
     if x.dtype == np.uint16:
         code = F16
+    elif x.dtype == np.uint8:
+        code = E4M3  # FP8 E4M3 bit patterns
     elif x.dtype == np.float32:
         code = F32
     else:
@@ -117,6 +122,13 @@ class Oracle:
         src = np.ascontiguousarray(bits, dtype=np.uint16)
         out = np.empty(src.shape, dtype=np.float64)
         self.lib.tgo_f16_to_f64_n(src.ctypes.data, out.ctypes.data, src.size)
+        return out
+
+    def e4m3_bits_to_f64(self, bits: np.ndarray) -> np.ndarray:
+        """Exact FP8 E4M3 -> binary64 decode of uint8 bit patterns."""
+        src = np.ascontiguousarray(bits, dtype=np.uint8)
+        out = np.empty(src.shape, dtype=np.float64)
+        self.lib.tgo_e4m3_to_f64_n(src.ctypes.data, out.ctypes.data, src.size)
         return out
 
     def f64_to_f16_bits(self, x: np.ndarray) -> np.ndarray:
@@ -195,6 +207,10 @@ def f16_bits_to_f64(bits):
 
 def f64_to_f16_bits(x):
     return _default().f64_to_f16_bits(x)
+
+
+def e4m3_bits_to_f64(bits):
+    return _default().e4m3_bits_to_f64(bits)
 
 
 def gemm(a, b, nthreads: int = 0):

@@ -13,6 +13,10 @@
  *     which the same page's §3.2 checks against a NumPy dot product.
  *   - Inputs are fp16 (or fp32 for the small example) and the pages accumulate
  *     in fp32 ("企业官网建设流程全解析" (cf-1.com), §3.3: accum_dtype float32).
+ *     The 8-bit variant takes FP8 E4M3 inputs (the pages discuss 8-bit
+ *     quantised GEMMs in "TileLang：GPU异构计算的声明式分块编程范式"
+ *     (kwkr.cn), §5.5, with INT8, which GB300's tensor cores do not offer
+ *     through tcgen05); they are decoded exactly like fp16.
  *     The oracle is stricter than that: every fp16 input is decoded exactly to
  *     binary64 from the IEEE-754 binary16 bit layout, every product of two
  *     fp16 values is exact in binary64, and the sum runs in binary64 in
@@ -32,7 +36,10 @@
  * 4x4 integer example (tests/golden), the 8x8 all-ones example of the
  * TileLang实战 page §6.2, closed forms (identity, all-ones, diagonal), the
  * transpose invariant (AB)^T = B^T A^T bitwise, and NumPy fp64 matmul on
- * exactly representable inputs.  The fused epilogue is pinned by the block
+ * exactly representable inputs.  The E4M3 decoder is pinned over all 256
+ * patterns against PyTorch's float8_e4m3fn conversion and by the format's
+ * defining values (448, 2^-6, 2^-9, the two NaNs, no infinities); an E4M3
+ * product of small integers equals NumPy's and the fp16 product.  The fused epilogue is pinned by the block
  * identity alpha*AB + beta*D + 1 bias^T = [alpha*A | beta*I | 1] [B; D; bias^T]
  * evaluated by NumPy, by x * Phi(x) against SciPy's normal distribution
  * function, and by the odd-part identities f(x) - f(-x) = x of ReLU and GELU.
@@ -47,6 +54,7 @@
 
 #define TGO_F16 1
 #define TGO_F32 2
+#define TGO_E4M3 3
 
 /* ---- binary16 decode (IEEE-754: 1 sign, 5 exponent bits biased by 15,
  *      10 fraction bits) ------------------------------------------------- */
@@ -100,6 +108,33 @@ uint16_t tgo_f64_to_f16(double x)
     return (uint16_t)(sign | (uint16_t)(((uint32_t)(E + 15) << 10) | (mant - 1024u)));
 }
 
+/* ---- FP8 E4M3 decode (the OCP 8-bit floating-point format's E4M3: 1 sign,
+ *      4 exponent bits biased by 7, 3 fraction bits; no infinities, and the
+ *      two patterns S.1111.111 are NaN, so the largest finite value is
+ *      1.75 * 2^8 = 448) ---------------------------------------------------- */
+double tgo_e4m3_to_f64(uint8_t q)
+{
+    int sign = (q >> 7) & 1;
+    int e = (q >> 3) & 0xf;
+    int f = q & 0x7;
+    double v;
+    if (e == 0xf && f == 0x7) {
+        v = NAN;
+    } else if (e == 0) {
+        /* zero and subnormals: 2^-6 * (f / 8) = f * 2^-9 */
+        v = ldexp((double)f, -9);
+    } else {
+        /* normals: 2^(e-7) * (1 + f/8) = (8 + f) * 2^(e-10) */
+        v = ldexp((double)(8 + f), e - 10);
+    }
+    return sign ? -v : v;
+}
+
+void tgo_e4m3_to_f64_n(const uint8_t* src, double* dst, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) dst[i] = tgo_e4m3_to_f64(src[i]);
+}
+
 /* Bulk helpers so the Python side need not loop element by element. */
 void tgo_f16_to_f64_n(const uint16_t* src, double* dst, int64_t n)
 {
@@ -114,7 +149,13 @@ void tgo_f64_to_f16_n(const double* src, uint16_t* dst, int64_t n)
 static double load_elem(const void* p, int64_t idx, int dtype)
 {
     if (dtype == TGO_F16) return tgo_f16_to_f64(((const uint16_t*)p)[idx]);
+    if (dtype == TGO_E4M3) return tgo_e4m3_to_f64(((const uint8_t*)p)[idx]);
     return (double)(((const float*)p)[idx]);
+}
+
+static int dtype_ok(int dtype)
+{
+    return dtype == TGO_F16 || dtype == TGO_F32 || dtype == TGO_E4M3;
 }
 
 int tgo_num_threads(void)
@@ -138,7 +179,7 @@ int tgo_gemm(int64_t M, int64_t N, int64_t K,
              int in_dtype, double* C, double* S, int nthreads)
 {
     if (M < 0 || N < 0 || K < 0) return -1;
-    if (in_dtype != TGO_F16 && in_dtype != TGO_F32) return -1;
+    if (!dtype_ok(in_dtype)) return -1;
     if (M == 0 || N == 0) return 0;
     if (K > 0 && (lda < K || ldb < N || !A || !B)) return -1;
 
@@ -186,7 +227,7 @@ int tgo_gemm_at(int64_t M, int64_t N, int64_t K,
                 const int64_t* cols, double* C, double* S, int nthreads)
 {
     if (M < 0 || N < 0 || K < 0 || n < 0) return -1;
-    if (in_dtype != TGO_F16 && in_dtype != TGO_F32) return -1;
+    if (!dtype_ok(in_dtype)) return -1;
     for (int64_t t = 0; t < n; ++t)
         if (rows[t] < 0 || rows[t] >= M || cols[t] < 0 || cols[t] >= N) return -1;
 #ifdef _OPENMP

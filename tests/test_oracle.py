@@ -203,6 +203,46 @@ def pin_degenerate(o: Oracle):
     assert C.shape == (0, 5)
 
 
+# ------------------------------------------------------------- FP8 E4M3 pins
+
+def pin_e4m3_decode_exhaustive(o: Oracle):
+    # all 256 patterns against PyTorch's own float8_e4m3fn conversion
+    torch = pytest.importorskip("torch")
+    bits = np.arange(256, dtype=np.uint8)
+    got = o.e4m3_bits_to_f64(bits)
+    ref = torch.from_numpy(bits).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan) and nan.sum() == 2
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def pin_e4m3_decode_by_hand(o: Oracle):
+    # the format's defining values: 1.0, the largest finite 448 = 1.75 * 2^8,
+    # the smallest normal 2^-6, the smallest subnormal 2^-9, signed zero
+    cases = {0x38: 1.0, 0x7E: 448.0, 0x08: 2.0 ** -6, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9,
+             0xC0: -2.0, 0x3C: 1.5, 0x00: 0.0}
+    got = o.e4m3_bits_to_f64(np.array(list(cases), dtype=np.uint8))
+    assert np.array_equal(got, np.array(list(cases.values())))
+    assert np.signbit(o.e4m3_bits_to_f64(np.array([0x80], np.uint8))[0])
+    assert np.isnan(o.e4m3_bits_to_f64(np.array([0x7F, 0xFF], np.uint8))).all()
+    assert o.e4m3_bits_to_f64(np.array([0x7C], np.uint8))[0] == 384.0  # no infinities
+
+
+def pin_e4m3_gemm_exact(o: Oracle):
+    # E4M3 operands with small-integer values: the product equals NumPy's on
+    # the decoded values exactly, and the same matrices in fp16 give the same C
+    rng = np.random.default_rng(12)
+    vals = np.array([0x00, 0x38, 0x40, 0xB8, 0xC0, 0x44, 0xC4], np.uint8)  # 0, 1, 2, -1, -2, 3, -3
+    a = vals[rng.integers(0, len(vals), (19, 37))]
+    b = vals[rng.integers(0, len(vals), (37, 23))]
+    C, S = o.gemm(a, b)
+    A, B = o.e4m3_bits_to_f64(a), o.e4m3_bits_to_f64(b)
+    assert set(np.unique(A)) <= {0.0, 1.0, 2.0, -1.0, -2.0, 3.0, -3.0}
+    assert np.array_equal(C, A @ B) and np.array_equal(S, np.abs(A) @ np.abs(B))
+    C16, _ = o.gemm(A.astype(np.float16), B.astype(np.float16))
+    assert np.array_equal(C, C16)
+
+
 # ----------------------------------------------------- fused epilogue pins
 
 def pin_epilogue_plain(o: Oracle):
@@ -268,7 +308,8 @@ def pin_activation_odd_parts(o: Oracle):
 PINS = [pin_decode_exhaustive, pin_decode_by_hand, pin_encode_ties, pin_encode_vs_numpy,
         pin_roundtrip, pin_gemm_4x4, pin_gemm_8x8_ones, pin_closed_forms, pin_transpose,
         pin_vs_numpy_exact, pin_vs_numpy_random, pin_leading_dims, pin_sampled,
-        pin_degenerate, pin_epilogue_plain, pin_epilogue_block_identity, pin_gelu_normal_cdf,
+        pin_degenerate, pin_e4m3_decode_exhaustive, pin_e4m3_decode_by_hand,
+        pin_e4m3_gemm_exact, pin_epilogue_plain, pin_epilogue_block_identity, pin_gelu_normal_cdf,
         pin_activation_odd_parts]
 
 
@@ -319,6 +360,9 @@ MUTANTS = {
     "ignored_lda": ("double a = load_elem(A, i * lda + k, in_dtype);",
                     "double a = load_elem(A, i * K + k, in_dtype);"),
     "missing_abs": ("s[j] += fabs(p);", "s[j] += p;"),
+    "e4m3_bias": ("(double)(8 + f), e - 10)", "(double)(8 + f), e - 11)"),
+    "e4m3_subnormal": ("v = ldexp((double)f, -9);", "v = ldexp((double)f, -10);"),
+    "e4m3_no_nan": ("if (e == 0xf && f == 0x7) {", "if (e == 0xf && f == 0x8) {"),
     "epilogue_alpha_dropped": ("double y = alpha * C[i * N + j];", "double y = C[i * N + j];"),
     "epilogue_beta_sign": ("y += beta * load_elem(", "y -= beta * load_elem("),
     "epilogue_ignored_ldcin": ("load_elem(Cin, i * ldcin + j, cin_dtype)",
