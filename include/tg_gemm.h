@@ -32,7 +32,9 @@ typedef void* tg_stream_t;
 
 typedef enum {
     TG_F16 = 1, /* IEEE-754 binary16 */
-    TG_F32 = 2  /* IEEE-754 binary32 */
+    TG_F32 = 2, /* IEEE-754 binary32 */
+    TG_E4M3 = 3 /* 8-bit float E4M3 (OCP FP8: bias 7, max 448, no infinities);
+                   an input type only */
 } tg_dtype;
 
 typedef enum {
@@ -65,11 +67,17 @@ typedef enum {
  * between column N and the row stride ldc are never written.
  *
  * Supported dtype pairs: (F16 -> F16) and (F16 -> F32) run on the tensor
- * cores; (F32 -> F32) runs on the SIMT fp32 path.  Any other pair returns
- * TG_ERR_UNSUPPORTED.  Pointer alignment and leading dimensions never cause
- * an error: operands that the TMA engine cannot address (base not 16-byte
+ * cores; (F32 -> F32) runs on the SIMT fp32 path; (E4M3 -> F16) and
+ * (E4M3 -> F32) run on the tensor cores (tcgen05 kind::f8f6f4, fp32
+ * accumulation).  Any other pair returns TG_ERR_UNSUPPORTED.  For fp16 and
+ * fp32 inputs, pointer alignment and leading dimensions never cause an
+ * error: operands that the TMA engine cannot address (base not 16-byte
  * aligned, or a row stride that is not a multiple of 16 bytes) go to a
- * predicated-load boundary kernel instead.
+ * predicated-load boundary kernel instead.  E4M3 inputs run on the TMA
+ * kernels only: their bases must be 16-byte aligned and lda, ldb multiples
+ * of 16, else TG_ERR_UNSUPPORTED.  The 8-bit path stands in for the INT8
+ * GEMM that "TileLang：GPU异构计算的声明式分块编程范式" (kwkr.cn), §5.5,
+ * discusses: GB300's tcgen05 has no integer MMA.
  *
  * Degenerate sizes: M == 0 or N == 0 is a no-op returning TG_OK (pointers
  * may then be NULL).  K == 0 writes zeros to C (the empty sum); A and B may
@@ -81,7 +89,8 @@ typedef enum {
  *                       or written; a pointer that is not a multiple of its
  *                       element size; lda < K, ldb < N or ldc < N; or the
  *                       byte span of C overlapping the span of A or of B.
- *   TG_ERR_UNSUPPORTED  an unsupported dtype pair, or a size above 2^31 - 1024.
+ *   TG_ERR_UNSUPPORTED  an unsupported dtype pair, a size above 2^31 - 1024,
+ *                       or E4M3 operands the TMA engine cannot address.
  *   TG_ERR_CUDA         a CUDA call made while launching failed.
  *
  * Ownership and memory: the caller owns A, B and C.  The library allocates

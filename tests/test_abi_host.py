@@ -298,3 +298,31 @@ def test_batched_path_selection():
     assert bpath(4, 256, 256, 256, sB=128 * 256) == 4
     # a single matrix ignores the strides
     assert bpath(1, 256, 256, 256, sA=5, sB=3, sC=1) == 3
+
+
+# ------------------------------------------------------------ FP8 E4M3 inputs
+
+def test_e4m3_path_selection():
+    E = tg.E4M3
+    assert path(8192, 8192, 8192, i=E) == 6
+    assert path(8192, 8192, 8192, i=E, o=tg.F32) == 6
+    assert path(256, 256, 256, i=E) == 3
+    assert path(16, 4096, 4096, i=E) == 3          # no skinny kernel for E4M3
+    assert bpath(8, 512, 512, 1024, i=E) == 3
+    # the TMA engine must address E4M3 operands: row strides of 16 bytes
+    assert path(256, 256, 100, i=E) == 0
+    assert call(256, 256, 100, i=E) == tg.TG_ERR_UNSUPPORTED
+    assert path(256, 256, 256, i=E, A=PA + 8) == 0
+    assert path(256, 256, 112, i=E) == 3
+    # E4M3 is an input type only
+    assert call(64, 64, 64, i=E, o=E) == tg.TG_ERR_UNSUPPORTED
+    assert call(64, 64, 64, i=tg.F16, o=E) == tg.TG_ERR_UNSUPPORTED
+    try:
+        tg.tg_gemm_force_path(4)
+        assert path(256, 256, 256, i=E) == 0        # no boundary kernel for E4M3
+        tg.tg_gemm_force_path(5)
+        assert path(16, 256, 256, i=E) == 0
+        tg.tg_gemm_force_path(6)
+        assert path(256, 256, 256, i=E) == 6
+    finally:
+        tg.tg_gemm_force_path(0)

@@ -16,7 +16,7 @@ import os
 import threading
 
 __all__ = [
-    "F16", "F32", "TG_OK", "TG_ERR_INVALID_ARG", "TG_ERR_UNSUPPORTED", "TG_ERR_CUDA",
+    "F16", "F32", "E4M3", "TG_OK", "TG_ERR_INVALID_ARG", "TG_ERR_UNSUPPORTED", "TG_ERR_CUDA",
     "TG_ERR_TIMEOUT", "PATHS", "TgError", "lib", "library_path", "tg_gemm", "tg_gemm_check",
     "tg_status_string", "tg_gemm_path", "tg_gemm_force_path", "tg_gemm_force_tiling",
     "tg_gemm_test_hook", "tg_gemm_ex", "tg_gemm_batched", "tg_gemm_batched_path", "ACT_NONE", "ACT_RELU", "ACT_GELU",
@@ -26,6 +26,7 @@ __all__ = [
 
 F16 = 1
 F32 = 2
+E4M3 = 3
 TG_OK = 0
 TG_ERR_INVALID_ARG = 1
 TG_ERR_UNSUPPORTED = 2
@@ -160,6 +161,8 @@ def _code(dtype) -> int:
         return F16
     if dtype == torch.float32:
         return F32
+    if dtype == torch.float8_e4m3fn:
+        return E4M3
     raise TypeError(f"unsupported dtype {dtype}")
 
 

@@ -322,10 +322,10 @@ cudaError_t launch_cfg(const GemmArgs& a)
                              (a.K + BK - 1) / BK, a.num_sms, g_max_clusters[dev][slot]);
     }
     CUtensorMap ta, tbt;
-    if (!encode_tmap_f16(&ta, a.A, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M),
+    if (!encode_tmap(&ta, a.A, 2, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M),
                          static_cast<uint64_t>(a.lda), a.batch, a.sA, 64, MP))
         return cudaErrorInvalidValue;
-    if (!encode_tmap_f16(&tbt, a.B, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
+    if (!encode_tmap(&tbt, a.B, 2, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
                          static_cast<uint64_t>(a.ldb), a.batch, a.sB, 64, BK))
         return cudaErrorInvalidValue;
     const int n_tiles = (a.N + BNT - 1) / BNT;

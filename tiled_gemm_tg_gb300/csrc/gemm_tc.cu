@@ -51,9 +51,16 @@ namespace {
 using namespace tg::dev;
 
 constexpr int BM = 128;
-constexpr int BK = 64;                 // fp16: 128 bytes per row = one swizzle atom
-constexpr uint32_t A_STAGE = BM * BK * 2;
-constexpr uint32_t B_BOX = 64 * BK * 2; // one [64 k][64 n] box, 8 KB
+// A k-block is 128 bytes of every row: one 128-byte swizzle atom, 64 fp16 or
+// 128 E4M3 elements (ES = element size in bytes), four MMAs of 32 bytes.
+template <int ES>
+struct KBlock {
+    static constexpr int BK = 128 / ES;             // k elements per k-block
+    static constexpr int NB = 128 / ES;             // n elements per B box (128 bytes)
+    static constexpr uint32_t B_BOX = BK * 128;     // one [BK k][NB n] box
+    static constexpr uint32_t B_KSTEP = 32 / ES * 128 / 16;  // 16-byte units per MMA k step
+};
+constexpr uint32_t A_STAGE = BM * 128;
 // Two epilogue warps per TMEM lane quadrant, each draining half of the
 // accumulator's columns: a long fused epilogue (GELU) then keeps up with the
 // MMAs instead of holding the accumulator buffer.
@@ -62,7 +69,7 @@ constexpr int kThreads = 64 + 32 * kEpilogueWarps;
 
 template <int BN>
 struct MainCfg {
-    static constexpr uint32_t B_STAGE = BN * BK * 2;
+    static constexpr uint32_t B_STAGE = BN * 128;
     static constexpr uint32_t STAGE = A_STAGE + B_STAGE;
     static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
     static constexpr uint32_t TMEM_COLS = 2 * BN;
@@ -72,7 +79,7 @@ struct MainCfg {
                   "TMEM allocation must be a power of two in [32, 512]");
 };
 
-template <int BN, bool OUT_F32>
+template <int BN, bool OUT_F32, int ES>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     void* C, long long ldc, int M, int N, int K, int tiles_m,
@@ -121,6 +128,10 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     tc_fence_after();
     const uint32_t tmem_base = tmem_slot;
 
+    constexpr int BK = KBlock<ES>::BK;
+    constexpr int NB = KBlock<ES>::NB;
+    constexpr uint32_t B_BOX = KBlock<ES>::B_BOX;
+    static_assert(BN % NB == 0, "B tile must be whole 128-byte boxes");
     const int num_kb = (K + BK - 1) / BK;
     const int total = tiles_m * tiles_n * bt.count;
     // The epilogue waits for a whole tile's main loop; allow ~64 us per k-block
@@ -159,8 +170,8 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     mbar_arrive_expect_tx(fb, Cfg::STAGE);
                     tma_load_3d(sa, &tmA, fb, kb * BK, tm * BM, za);
 #pragma unroll
-                    for (int j = 0; j < BN / 64; ++j)
-                        tma_load_3d(sa + A_STAGE + j * B_BOX, &tmB, fb, tn * BN + j * 64, kb * BK,
+                    for (int j = 0; j < BN / NB; ++j)
+                        tma_load_3d(sa + A_STAGE + j * B_BOX, &tmB, fb, tn * BN + j * NB, kb * BK,
                                     zb);
                     ++issued;
                     if (++s == STAGES) {
@@ -207,13 +218,15 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     }
                     tc_fence_after();
                     const uint32_t sa = base + s * Cfg::STAGE;
-                    // A: K-major, 8-row groups 1024 B apart.  B: MN-major,
-                    // 64-column boxes BK*128 B apart, 8-row k groups 1024 B apart.
+                    // A: K-major, 8-row groups 1024 B apart, +32 B per MMA.  B:
+                    // MN-major, 128-byte-wide boxes B_BOX apart, 8-row k groups
+                    // 1024 B apart, one MMA's k rows (16 fp16 / 32 E4M3) per step.
                     const uint64_t ad = sdesc_sw128(sa, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(sa + A_STAGE, BK * 128, 1024);
+                    const uint64_t bd = sdesc_sw128(sa + A_STAGE, B_BOX, 1024);
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)
-                        umma_f16(d, ad + 2ull * k, bd + 128ull * k, idesc, (kb | k) != 0 ? 1u : 0u);
+                    for (int k = 0; k < 4; ++k)
+                        umma<ES>(d, ad + 2ull * k, bd + KBlock<ES>::B_KSTEP * k, idesc,
+                                 (kb | k) != 0 ? 1u : 0u);
                     umma_commit(smem_u32(&empty_bar[s]));
                     if (++s == STAGES) {
                         s = 0;
@@ -284,18 +297,20 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 }
 
 std::mutex g_attr_mu;
-bool g_attr_set[64][6];
+bool g_attr_set[64][12];
 
-template <int BN, bool OUT_F32>
+template <int BN, bool OUT_F32, int ES>
 cudaError_t launch_cfg(const GemmArgs& a)
 {
     using Cfg = MainCfg<BN>;
-    auto kernel = gemm_tc_main_kernel<BN, OUT_F32>;
+    using KB = KBlock<ES>;
+    auto kernel = gemm_tc_main_kernel<BN, OUT_F32, ES>;
     {
         int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
-        const int slot = (BN == 256 ? 0 : BN == 128 ? 1 : 2) * 2 + (OUT_F32 ? 1 : 0);
+        const int slot =
+            ((BN == 256 ? 0 : BN == 128 ? 1 : 2) * 2 + (OUT_F32 ? 1 : 0)) * 2 + (ES == 1 ? 1 : 0);
         std::lock_guard<std::mutex> lock(g_attr_mu);
         if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
         if (!g_attr_set[dev][slot]) {
@@ -306,11 +321,11 @@ cudaError_t launch_cfg(const GemmArgs& a)
         }
     }
     CUtensorMap ta, tb;
-    if (!encode_tmap_f16(&ta, a.A, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M),
-                         static_cast<uint64_t>(a.lda), a.batch, a.sA, BK, BM))
+    if (!encode_tmap(&ta, a.A, ES, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M),
+                     static_cast<uint64_t>(a.lda), a.batch, a.sA, KB::BK, BM))
         return cudaErrorInvalidValue;
-    if (!encode_tmap_f16(&tb, a.B, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
-                         static_cast<uint64_t>(a.ldb), a.batch, a.sB, 64, BK))
+    if (!encode_tmap(&tb, a.B, ES, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
+                     static_cast<uint64_t>(a.ldb), a.batch, a.sB, KB::NB, KB::BK))
         return cudaErrorInvalidValue;
     const int tiles_m = (a.M + BM - 1) / BM;
     const int tiles_n = (a.N + BN - 1) / BN;
@@ -339,14 +354,19 @@ int main_tile_n(int M, int N, int batch, int num_sms)
 
 cudaError_t launch_main(const GemmArgs& a, int bn)
 {
-    if (a.out_f32) {
-        if (bn == 256) return launch_cfg<256, true>(a);
-        if (bn == 128) return launch_cfg<128, true>(a);
-        return launch_cfg<64, true>(a);
+    if (a.in_es == 1) {
+        // E4M3: B boxes are 128 elements wide, so tiles are 128 or 256 wide
+        if (a.out_f32) return bn == 256 ? launch_cfg<256, true, 1>(a) : launch_cfg<128, true, 1>(a);
+        return bn == 256 ? launch_cfg<256, false, 1>(a) : launch_cfg<128, false, 1>(a);
     }
-    if (bn == 256) return launch_cfg<256, false>(a);
-    if (bn == 128) return launch_cfg<128, false>(a);
-    return launch_cfg<64, false>(a);
+    if (a.out_f32) {
+        if (bn == 256) return launch_cfg<256, true, 2>(a);
+        if (bn == 128) return launch_cfg<128, true, 2>(a);
+        return launch_cfg<64, true, 2>(a);
+    }
+    if (bn == 256) return launch_cfg<256, false, 2>(a);
+    if (bn == 128) return launch_cfg<128, false, 2>(a);
+    return launch_cfg<64, false, 2>(a);
 }
 
 }  // namespace tg

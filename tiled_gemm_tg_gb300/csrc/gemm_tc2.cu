@@ -48,16 +48,25 @@ constexpr int PM = 256;                          // pair tile rows (128 per CTA)
 constexpr int PN = 256;                          // pair tile columns (B: 128 per CTA)
 constexpr int HM = PM / 2;
 constexpr int HN = PN / 2;
-// k-block of 128: eight MMAs per stage and per commit.  Measured on GB300,
-// 64-wide k-blocks (four MMAs between stage switches/commits) keep the
-// tensor pipe 87-94 % busy, 128-wide ones 100 %.
-constexpr int BK = 128;
-constexpr int KA = BK / 64;                      // 128-byte swizzle atoms along k in A
-constexpr uint32_t A_ATOM = HM * 128;            // [128 rows][64 k] = 16 KB
-constexpr uint32_t A_STAGE = HM * BK * 2;        // 32 KB
-constexpr uint32_t B_BOX = 64 * BK * 2;          // one [BK k][64 n] box, 16 KB
-constexpr uint32_t B_STAGE = HN * BK * 2;        // 32 KB
+// k-block of 256 bytes per row (128 fp16 or 256 E4M3 elements): eight MMAs
+// of 32 bytes per stage and per commit.  Measured on GB300, 64-element fp16
+// k-blocks (four MMAs between stage switches/commits) keep the tensor pipe
+// 87-94 % busy, 128-element ones 100 %.
+constexpr int KA = 2;                            // 128-byte swizzle atoms along k in A
+constexpr uint32_t A_ATOM = HM * 128;            // [128 rows][128 bytes of k] = 16 KB
+constexpr uint32_t A_STAGE = HM * 256;           // 32 KB
+constexpr uint32_t B_STAGE = HN * 256;           // 32 KB
 constexpr uint32_t STAGE = A_STAGE + B_STAGE;    // 64 KB per CTA
+
+// Element-size dependent geometry (ES = 2: fp16, 1: E4M3).
+template <int ES>
+struct PairK {
+    static constexpr int BK = 256 / ES;                  // k elements per k-block
+    static constexpr int AE = 128 / ES;                  // k elements per A atom
+    static constexpr int NB = 128 / ES;                  // n elements per B box
+    static constexpr uint32_t B_BOX = BK * 128;          // one [BK k][NB n] box
+    static constexpr uint32_t B_KSTEP = 32 / ES * 128 / 16;  // 16-byte units per MMA
+};
 constexpr int STAGES = 3;
 constexpr uint32_t SMEM = STAGES * STAGE + 1024;
 constexpr uint32_t TMEM_COLS = 2 * PN;           // two accumulators
@@ -84,7 +93,7 @@ constexpr int L2_HINTS = TG_PAIR_L2_HINTS;  // bit 0: A evict_last, bit 1: B evi
 #endif
 constexpr int EPI_COLS = TG_PAIR_EPI_COLS;  // accumulator columns per tcgen05.ld
 
-template <bool OUT_F32>
+template <bool OUT_F32, int ES>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     void* C, long long ldc, int M, int N, int K, int tiles_m,
@@ -134,6 +143,8 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     tc_fence_after();
     const uint32_t tmem_base = tmem_slot;
 
+    using KG = PairK<ES>;
+    constexpr int BK = KG::BK;
     const int num_kb = (K + BK - 1) / BK;
     const int total = tiles_m * tiles_n * bt.count;
     const uint32_t epi_limit = kSlowPolls + 64u * static_cast<uint32_t>(min(num_kb, 1 << 20));
@@ -177,12 +188,12 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const uint32_t sa = base + s * STAGE;
 #pragma unroll
                     for (int j = 0; j < KA; ++j)
-                        tma_load_3d_pair_hint(sa + j * A_ATOM, &tmA, fb, kb * BK + j * 64, row,
-                                              za, pol_a);
+                        tma_load_3d_pair_hint(sa + j * A_ATOM, &tmA, fb, kb * BK + j * KG::AE,
+                                              row, za, pol_a);
 #pragma unroll
-                    for (int j = 0; j < HN / 64; ++j)
-                        tma_load_3d_pair_hint(sa + A_STAGE + j * B_BOX, &tmB, fb, col + j * 64,
-                                              kb * BK, zb, pol_b);
+                    for (int j = 0; j < HN / KG::NB; ++j)
+                        tma_load_3d_pair_hint(sa + A_STAGE + j * KG::B_BOX, &tmB, fb,
+                                              col + j * KG::NB, kb * BK, zb, pol_b);
                     ++issued;
                     if (++s == STAGES) {
                         s = 0;
@@ -230,15 +241,16 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     }
                     tc_fence_after();
                     const uint32_t sa = base + s * STAGE;
-                    // A: K-major, atoms of [128 rows][64 k] 16 KB apart, 8-row groups
-                    // 1024 B apart, +32 B per 16 k inside an atom.  B: MN-major,
-                    // [BK k][64 n] boxes BK*128 B apart, 8-row k groups 1024 B apart.
+                    // A: K-major, atoms of [128 rows][128 B of k] 16 KB apart, 8-row
+                    // groups 1024 B apart, +32 B per MMA inside an atom.  B:
+                    // MN-major, [BK k][128 B of n] boxes B_BOX apart, 8-row k
+                    // groups 1024 B apart, one MMA's k rows per step.
                     const uint64_t ad = sdesc_sw128(sa, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(sa + A_STAGE, BK * 128, 1024);
+                    const uint64_t bd = sdesc_sw128(sa + A_STAGE, KG::B_BOX, 1024);
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)
-                        umma_f16_pair(d, ad + ((k / 4) * (A_ATOM >> 4) + (k % 4) * 2),
-                                      bd + (k * 2048u >> 4), idesc, (kb | k) != 0 ? 1u : 0u);
+                    for (int k = 0; k < 8; ++k)
+                        umma_pair<ES>(d, ad + ((k / 4) * (A_ATOM >> 4) + (k % 4) * 2),
+                                      bd + KG::B_KSTEP * k, idesc, (kb | k) != 0 ? 1u : 0u);
                     umma_commit_pair_mc(smem_u32(&empty_bar[s]), 0x3);
                     if (++s == STAGES) {
                         s = 0;
@@ -313,14 +325,15 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 }
 
 std::mutex g_mu;
-bool g_attr_set[64][2];
-int g_max_clusters[64][2];
+bool g_attr_set[64][4];
+int g_max_clusters[64][4];
 
-template <bool OUT_F32>
+template <bool OUT_F32, int ES>
 cudaError_t launch_cfg(const GemmArgs& a)
 {
-    auto kernel = gemm_tc_pair_kernel<OUT_F32>;
-    const int slot = OUT_F32 ? 1 : 0;
+    using KG = PairK<ES>;
+    auto kernel = gemm_tc_pair_kernel<OUT_F32, ES>;
+    const int slot = (OUT_F32 ? 1 : 0) + (ES == 1 ? 2 : 0);
     int max_clusters = 0;
     {
         int dev = 0;
@@ -352,11 +365,11 @@ cudaError_t launch_cfg(const GemmArgs& a)
         max_clusters = g_max_clusters[dev][slot];
     }
     CUtensorMap ta, tb;
-    if (!encode_tmap_f16(&ta, a.A, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M),
-                         static_cast<uint64_t>(a.lda), a.batch, a.sA, 64, HM))
+    if (!encode_tmap(&ta, a.A, ES, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M),
+                     static_cast<uint64_t>(a.lda), a.batch, a.sA, KG::AE, HM))
         return cudaErrorInvalidValue;
-    if (!encode_tmap_f16(&tb, a.B, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
-                         static_cast<uint64_t>(a.ldb), a.batch, a.sB, 64, BK))
+    if (!encode_tmap(&tb, a.B, ES, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
+                     static_cast<uint64_t>(a.ldb), a.batch, a.sB, KG::NB, KG::BK))
         return cudaErrorInvalidValue;
     const int tiles_m = (a.M + PM - 1) / PM;
     const int tiles_n = (a.N + PN - 1) / PN;
@@ -393,7 +406,8 @@ int pair_tiles(int M, int N)
 
 cudaError_t launch_main_pair(const GemmArgs& a)
 {
-    return a.out_f32 ? launch_cfg<true>(a) : launch_cfg<false>(a);
+    if (a.in_es == 1) return a.out_f32 ? launch_cfg<true, 1>(a) : launch_cfg<false, 1>(a);
+    return a.out_f32 ? launch_cfg<true, 2>(a) : launch_cfg<false, 2>(a);
 }
 
 }  // namespace tg

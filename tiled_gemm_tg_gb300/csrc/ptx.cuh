@@ -159,6 +159,30 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint6
         : "memory");
 }
 
+// D[tmem] (+)= A * B with FP8 E4M3 A and B (kind::f8f6f4, K = 32 per
+// instruction), fp32 accumulate.
+__device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// The MMA for an input element size: 2 bytes (fp16, K = 16 per instruction)
+// or 1 byte (E4M3, K = 32); either way one instruction consumes 32 bytes of
+// each operand row along k.
+template <int ES>
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                     uint32_t idesc, uint32_t accumulate)
+{
+    if constexpr (ES == 2) umma_f16(d_tmem, a_desc, b_desc, idesc, accumulate);
+    else umma_e4m3(d_tmem, a_desc, b_desc, idesc, accumulate);
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar)
@@ -307,6 +331,26 @@ __device__ __forceinline__ void umma_f16_pair(uint32_t d_tmem, uint64_t a_desc, 
         : "memory");
 }
 
+// The pair MMA with FP8 E4M3 operands (kind::f8f6f4, K = 32).
+__device__ __forceinline__ void umma_e4m3_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+template <int ES>
+__device__ __forceinline__ void umma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate)
+{
+    if constexpr (ES == 2) umma_f16_pair(d_tmem, a_desc, b_desc, idesc, accumulate);
+    else umma_e4m3_pair(d_tmem, a_desc, b_desc, idesc, accumulate);
+}
+
 // Arrive once, at the same shared-memory offset `bar` in every CTA of
 // `cta_mask`, when all tcgen05 operations this thread issued have completed.
 __device__ __forceinline__ void umma_commit_pair_mc(uint32_t bar, uint16_t cta_mask)
@@ -339,7 +383,8 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
 }
 
 // Instruction descriptor for kind::f16 with fp16 A and B, fp32 D.
-// a_mn / b_mn select the MN-major (transposed) operand layout.
+// a_mn / b_mn select the MN-major (transposed) operand layout.  The same
+// word serves kind::f8f6f4 with E4M3 A and B: format code 0 is E4M3 there.
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n, bool a_mn, bool b_mn)
 {
     return (1u << 4)                                   // D format: fp32

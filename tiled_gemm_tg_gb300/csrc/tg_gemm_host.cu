@@ -71,7 +71,7 @@ tg_status device_state(DeviceState** out)
     return TG_OK;
 }
 
-size_t esize(tg_dtype t) { return t == TG_F16 ? 2 : 4; }
+size_t esize(tg_dtype t) { return t == TG_F16 ? 2 : t == TG_E4M3 ? 1 : 4; }
 
 using u128 = unsigned __int128;
 
@@ -105,10 +105,11 @@ struct Problem {
 // The TMA engine addresses a batch of matrices through a 3-D tensor map:
 // a matrix stride that is a multiple of 16 bytes, below 2^40 bytes and at
 // least one whole matrix (or 0, one matrix broadcast to every b).
-bool tma_stride_ok(int64_t stride, int64_t rows, int64_t ld)
+bool tma_stride_ok(int64_t stride, int64_t rows, int64_t ld, int64_t es)
 {
     if (stride == 0) return true;
-    return stride % 8 == 0 && stride < (int64_t(1) << 38) && stride >= rows * ld;
+    return stride < (int64_t(1) << 39) / es && (stride * es) % 16 == 0 &&
+           static_cast<u128>(stride) >= static_cast<u128>(rows) * static_cast<u128>(ld);
 }
 
 // Validation shared by every entry point.  On TG_OK, *path is the path the
@@ -120,7 +121,8 @@ tg_status classify(const Problem& p, int* path)
     if (M < 0 || N < 0 || K < 0 || p.batch < 0) return TG_ERR_INVALID_ARG;
     if (p.sA < 0 || p.sB < 0 || p.sC < 0) return TG_ERR_INVALID_ARG;
     const bool pair_ok =
-        (p.in_dtype == TG_F16 && (p.out_dtype == TG_F16 || p.out_dtype == TG_F32)) ||
+        ((p.in_dtype == TG_F16 || p.in_dtype == TG_E4M3) &&
+         (p.out_dtype == TG_F16 || p.out_dtype == TG_F32)) ||
         (p.in_dtype == TG_F32 && p.out_dtype == TG_F32);
     if (!pair_ok) return TG_ERR_UNSUPPORTED;
     if (M > kMaxDim || N > kMaxDim || K > kMaxDim || p.batch > kMaxBatch)
@@ -159,15 +161,22 @@ tg_status classify(const Problem& p, int* path)
     }
     // The TMA engine needs 16-byte aligned bases and row strides that are
     // multiples of 16 bytes (and below 2^40 bytes).
-    const int64_t kMaxTmaLd = int64_t(1) << 38;
+    const int64_t e = static_cast<int64_t>(ei);
+    const int64_t kMaxTmaLdBytes = int64_t(1) << 39;
+    // (sizes are compared before they are multiplied, so nothing can overflow)
     const bool tma_ok = (reinterpret_cast<uintptr_t>(p.A) % 16 == 0) &&
-                        (reinterpret_cast<uintptr_t>(p.B) % 16 == 0) && (p.lda % 8 == 0) &&
-                        (p.ldb % 8 == 0) && p.lda < kMaxTmaLd && p.ldb < kMaxTmaLd &&
-                        (p.batch == 1 || (tma_stride_ok(p.sA, M, p.lda) &&
-                                          tma_stride_ok(p.sB, K, p.ldb)));
+                        (reinterpret_cast<uintptr_t>(p.B) % 16 == 0) &&
+                        p.lda < kMaxTmaLdBytes / e && p.ldb < kMaxTmaLdBytes / e &&
+                        (p.lda * e) % 16 == 0 && (p.ldb * e) % 16 == 0 &&
+                        (p.batch == 1 || (tma_stride_ok(p.sA, M, p.lda, e) &&
+                                          tma_stride_ok(p.sB, K, p.ldb, e)));
+    const bool e4m3 = p.in_dtype == TG_E4M3;
+    // E4M3 runs on the TMA kernels only (the skinny and boundary kernels are
+    // fp16): operands the TMA engine cannot address are not supported.
+    if (e4m3 && !tma_ok) return TG_ERR_UNSUPPORTED;
     if (!tma_ok) {
         *path = tg::PATH_BOUNDARY;
-    } else if (M <= tg::kSkinnyMaxM) {
+    } else if (M <= tg::kSkinnyMaxM && !e4m3) {
         *path = tg::PATH_SKINNY;
     } else if (static_cast<int64_t>(tg::pair_tiles(static_cast<int>(M), static_cast<int>(N))) *
                        p.batch >= tg::kPairMinTiles &&
@@ -183,6 +192,7 @@ bool path_serves(int path, int natural, tg_dtype in_dtype, int64_t M)
 {
     if (path == natural) return true;
     if (natural == tg::PATH_ZERO || natural == tg::PATH_NONE) return false;
+    if (in_dtype == TG_E4M3) return path == tg::PATH_MAIN || path == tg::PATH_MAIN_PAIR;
     switch (path) {
         case tg::PATH_SIMT: return in_dtype == TG_F32;
         case tg::PATH_BOUNDARY: return in_dtype == TG_F16;
@@ -274,6 +284,7 @@ tg_status run(int path, const Problem& p, const tg::Epilogue& epi, tg_stream_t s
     a.C = p.C;
     a.ldc = p.ldc;
     a.out_f32 = (p.out_dtype == TG_F32);
+    a.in_es = p.in_dtype == TG_E4M3 ? 1 : 2;
     a.err = ds->err;
     a.hook = g_test_hook.load(std::memory_order_relaxed);
     a.group_m = g_force_group.load(std::memory_order_relaxed);
@@ -302,21 +313,24 @@ tg_status run(int path, const Problem& p, const tg::Epilogue& epi, tg_stream_t s
 
 namespace tg {
 
-bool encode_tmap_f16(CUtensorMap* map, const void* ptr, uint64_t cols, uint64_t rows, uint64_t ld,
-                     uint64_t batch, uint64_t stride, uint32_t box_cols, uint32_t box_rows)
+bool encode_tmap(CUtensorMap* map, const void* ptr, int es, uint64_t cols, uint64_t rows,
+                 uint64_t ld, uint64_t batch, uint64_t stride, uint32_t box_cols,
+                 uint32_t box_rows)
 {
-    if (!g_encode) return false;
+    if (!g_encode || (es != 1 && es != 2)) return false;
     if (stride == 0) {
         // one matrix: the third extent is 1 and its stride only has to be a
         // legal value (a multiple of 16 bytes covering the matrix)
         batch = 1;
-        stride = (rows * ld + 7) / 8 * 8;
+        stride = (rows * ld * es + 15) / 16 * 16 / es;
     }
     cuuint64_t dims[3] = {cols, rows, batch};
-    cuuint64_t strides[2] = {ld * 2, stride * 2};
+    cuuint64_t strides[2] = {ld * es, stride * es};
     cuuint32_t box[3] = {box_cols, box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(ptr), dims,
+    const CUtensorMapDataType dt =
+        es == 2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    CUresult r = g_encode(map, dt, 3, const_cast<void*>(ptr), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

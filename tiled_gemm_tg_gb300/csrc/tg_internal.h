@@ -70,6 +70,7 @@ struct GemmArgs {
     void* C;
     long long ldc;
     bool out_f32;
+    int in_es = 2;      // input element size: 2 (fp16) or 1 (E4M3)
     unsigned int* err;  // device error word
     int hook;           // test hook (0 = off), see tg_gemm_test_hook
     int group_m;        // grouped tile-order height, 0 = the kernel's default
@@ -90,14 +91,15 @@ struct GemmArgs {
     }
 };
 
-// Encodes a 3-D tensor map over `batch` row-major matrices of fp16 elements
-// (inner extent `cols`, `rows` rows, row stride `ld` elements, matrix stride
-// `stride` elements; stride 0 maps a single matrix that every batch
-// coordinate must address as z = 0) with a box of box_cols x box_rows x 1 and
-// 128-byte swizzle.  Returns false if the driver rejects it.
-bool encode_tmap_f16(CUtensorMap* map, const void* ptr, uint64_t cols, uint64_t rows,
-                     uint64_t ld, uint64_t batch, uint64_t stride, uint32_t box_cols,
-                     uint32_t box_rows);
+// Encodes a 3-D tensor map over `batch` row-major matrices of `es`-byte
+// elements (2: fp16, 1: E4M3 bytes; inner extent `cols`, `rows` rows, row
+// stride `ld` elements, matrix stride `stride` elements; stride 0 maps a
+// single matrix that every batch coordinate must address as z = 0) with a box
+// of box_cols x box_rows x 1 and 128-byte swizzle.  Returns false if the
+// driver rejects it.
+bool encode_tmap(CUtensorMap* map, const void* ptr, int es, uint64_t cols, uint64_t rows,
+                 uint64_t ld, uint64_t batch, uint64_t stride, uint32_t box_cols,
+                 uint32_t box_rows);
 
 cudaError_t launch_simt_f32(const GemmArgs& a);
 cudaError_t launch_main(const GemmArgs& a, int bn);

@@ -9,8 +9,8 @@ workload is ``seed_base + 1`` and the B seed ``seed_base + 2``.
 The shapes and distributions are the five workloads the GEMM is judged on:
 the fp32 128^3 triple-loop example, the fp16 edge set, the A[1024,512] x
 B[512,2048] tiling example, the 8192^3 compute-bound square and the two
-skinny/wide shapes; and two strided batches (256 products of 256^3, 16 of
-2048^3).  The pages benchmark on no public dataset, so these
+skinny/wide shapes; two strided batches (256 products of 256^3, 16 of
+2048^3); and the 8192^3 square with 8-bit E4M3 inputs.  The pages benchmark on no public dataset, so these
 synthetic draws are the whole input set.
 """
 from __future__ import annotations
@@ -28,7 +28,7 @@ class Workload:
     N: int
     K: int
     dist: str          # "normal", "normal_rsqrtk", "uniform", "normal_0.02", "int2"
-    in_dtype: str      # "f16" or "f32"
+    in_dtype: str      # "f16", "f32" or "e4m3"
     out_dtype: str     # "f16" or "f32"
     seed_base: int
     batch: int = 1     # independent products of this shape (a strided batch)
@@ -39,7 +39,7 @@ class Workload:
 
     def algorithmic_bytes(self) -> int:
         """A and B read once, C written once (every matrix of the batch)."""
-        ein = 2 if self.in_dtype == "f16" else 4
+        ein = {"f16": 2, "e4m3": 1}.get(self.in_dtype, 4)
         eout = 2 if self.out_dtype == "f16" else 4
         return self.batch * ((self.M * self.K + self.K * self.N) * ein + self.M * self.N * eout)
 
@@ -61,6 +61,8 @@ WORKLOADS = {
                  batch=256),
         Workload("batched_16x2048x2048x2048", 2048, 2048, 2048, "uniform", "f16", "f16", 6100,
                  batch=16),
+        # the 8-bit variant of the compute-bound square: E4M3 in, fp16 out
+        Workload("square_8192_e4m3", 8192, 8192, 8192, "uniform", "e4m3", "f16", 7000),
     ]
 }
 
@@ -90,6 +92,10 @@ def draw(shape, dist: str, seed: int, dtype: str, k: int | None = None) -> torch
         raise ValueError(f"unknown distribution {dist}")
     if dtype == "f16":
         return x.to(torch.float16)
+    if dtype == "e4m3":
+        # round to nearest even into the 8-bit E4M3 format (|x| stays far
+        # below its largest finite value, 448, for every distribution here)
+        return x.to(torch.float8_e4m3fn)
     if dtype == "f32":
         return x
     raise ValueError(f"unknown dtype {dtype}")
