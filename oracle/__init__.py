@@ -60,6 +60,9 @@ def _bind(path: str):
     lib.tgo_gemm.restype = ctypes.c_int
     lib.tgo_gemm.argtypes = [i64, i64, i64, vp, i64, vp, i64, ctypes.c_int,
                              vp, vp, ctypes.c_int]
+    lib.tgo_attention.restype = ctypes.c_int
+    lib.tgo_attention.argtypes = [i64, i64, i64, i64, vp, i64, vp, i64, vp, i64, ctypes.c_int,
+                                  ctypes.c_double, vp, vp, vp, ctypes.c_int]
     lib.tgo_epilogue.restype = ctypes.c_int
     lib.tgo_epilogue.argtypes = [i64, i64, vp, ctypes.c_double, ctypes.c_double, vp, i64,
                                  ctypes.c_int, vp, ctypes.c_int, vp]
@@ -189,6 +192,31 @@ class Oracle:
         return out
 
 
+    def attention(self, q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float = 1.0,
+                  nthreads: int = 0):
+        """softmax(scale * Q K^T) V by its definition in fp64.  Returns (O, E, G):
+        O and E are Nq x dv, E[i,c] = sum_j w_ij |V[j,c]|; G[i] is the largest
+        |scale| * sum_d |Q[i,d] K[j,d]| over j."""
+        q, code, ldq = _operand(q)
+        k, code_k, ldk = _operand(k)
+        v, code_v, ldv = _operand(v)
+        if not (code == code_k == code_v):
+            raise TypeError("Q, K and V must share a dtype")
+        Nq, d = q.shape
+        Nk, dv = v.shape
+        if k.shape != (Nk, d):
+            raise ValueError("K must be Nk x d")
+        O = np.empty((Nq, dv), dtype=np.float64)
+        E = np.empty((Nq, dv), dtype=np.float64)
+        G = np.empty(Nq, dtype=np.float64)
+        rc = self.lib.tgo_attention(Nq, Nk, d, dv, q.ctypes.data, ldq, k.ctypes.data, ldk,
+                                    v.ctypes.data, ldv, code, float(scale), O.ctypes.data,
+                                    E.ctypes.data, G.ctypes.data, int(nthreads))
+        if rc != 0:
+            raise RuntimeError("oracle rejected its arguments")
+        return O, E, G
+
+
 def _default() -> Oracle:
     global _lib
     with _lock:
@@ -223,6 +251,25 @@ def gemm_at(a, b, rows, cols, nthreads: int = 0):
 
 def epilogue(C, alpha=1.0, beta=0.0, cin=None, bias=None, act=0):
     return _default().epilogue(C, alpha, beta, cin, bias, act)
+
+
+def attention(q, k, v, scale=1.0, nthreads: int = 0):
+    return _default().attention(q, k, v, scale, nthreads)
+
+
+def attention_tolerance(O, E, G, d: int, nk: int, out_f16: bool):
+    """Bound for a tensor-core attention forward against the fp64 definition:
+    logits from fp16 products summed in fp32 are off by at most about
+    (d + 8) * 2^-23 * G (G bounds every |logit| and its magnitude sum), which
+    moves each softmax weight by a factor within exp(+-2 * that), so O by
+    2.5 * dS * E; the probabilities rounded to fp16 for the P.V product and
+    summed in fp32 over nk keys add (2^-10 + nk * 2^-23) * E; plus 1e-5 and
+    the 1e-2 relative term for an fp16 output."""
+    dS = (d + 8) * 2.0 ** -23 * np.asarray(G, dtype=np.float64)[:, None]
+    t = E * (2.5 * dS + 2.0 ** -10 + nk * 2.0 ** -23) + 1e-5
+    if out_f16:
+        t = t + 1e-2 * np.abs(O)
+    return t
 
 
 def tolerance(C_ref: np.ndarray, S: np.ndarray, out_f16: bool) -> np.ndarray:

@@ -39,7 +39,12 @@
  * exactly representable inputs.  The E4M3 decoder is pinned over all 256
  * patterns against PyTorch's float8_e4m3fn conversion and by the format's
  * defining values (448, 2^-6, 2^-9, the two NaNs, no infinities); an E4M3
- * product of small integers equals NumPy's and the fp16 product.  The fused epilogue is pinned by the block
+ * product of small integers equals NumPy's and the fp16 product.  Attention
+ * is pinned against SciPy's softmax of NumPy's logits, by closed forms
+ * (identical keys give the mean of V exactly, a dominant key gives its V row
+ * exactly, V of ones gives ones), by invariants (a joint permutation of keys
+ * and values, a shift shared by all keys, row independence, strided views),
+ * and by the page's own blockwise running-max recurrence run in fp64.  The fused epilogue is pinned by the block
  * identity alpha*AB + beta*D + 1 bias^T = [alpha*A | beta*I | 1] [B; D; bias^T]
  * evaluated by NumPy, by x * Phi(x) against SciPy's normal distribution
  * function, and by the odd-part identities f(x) - f(-x) = x of ReLU and GELU.
@@ -282,4 +287,88 @@ int tgo_epilogue(int64_t M, int64_t N, const double* C, double alpha, double bet
         }
     }
     return 0;
+}
+
+/*
+ * Attention forward, by its definition:
+ *     O[i,c] = sum_j w_ij V[j,c],  w_ij = exp(s_ij - m_i) / sum_j' exp(s_ij' - m_i),
+ *     s_ij = scale * sum_d Q[i,d] K[j,d],  m_i = max_j s_ij.
+ * This is the softmax(Q K^T) V that "TileLang实战：用Python DSL自动生成高性能GPU
+ * 计算内核" (gsyq.cn), §4.1, states and its §4.2 computes blockwise with a
+ * running maximum M and normaliser L; the blockwise recurrence reaches the
+ * same value up to rounding, so the oracle is the definition.  The page's
+ * kernel applies no 1/sqrt(d) factor: `scale` is 1 for it.  Subtracting m_i
+ * is the usual overflow guard and cancels exactly in the ratio.
+ * Q is Nq x d (row stride ldq), K is Nk x d (ldk), V is Nk x dv (ldv), all of
+ * element type in_dtype.  O and E are dense Nq x dv fp64 with
+ * E[i,c] = sum_j w_ij |V[j,c]| (the scale the acceptance bound is written
+ * against), and G[i] = |scale| * max_j sum_d |Q[i,d] K[j,d]| (the largest
+ * logit magnitude a row's dot products can reach).  Everything in fp64.
+ * Returns 0, or -1 on a bad argument or failed allocation.
+ */
+int tgo_attention(int64_t Nq, int64_t Nk, int64_t d, int64_t dv, const void* Q, int64_t ldq,
+                  const void* K, int64_t ldk, const void* V, int64_t ldv, int in_dtype,
+                  double scale, double* O, double* E, double* G, int nthreads)
+{
+    if (Nq < 0 || Nk < 1 || d < 1 || dv < 1 || !dtype_ok(in_dtype)) return -1;
+    if (ldq < d || ldk < d || ldv < dv || !Q || !K || !V) return -1;
+    double* Kd = (double*)malloc(sizeof(double) * (size_t)Nk * (size_t)d);
+    double* Vd = (double*)malloc(sizeof(double) * (size_t)Nk * (size_t)dv);
+    if (!Kd || !Vd) {
+        free(Kd);
+        free(Vd);
+        return -1;
+    }
+    for (int64_t j = 0; j < Nk; ++j) {
+        for (int64_t c = 0; c < d; ++c) Kd[j * d + c] = load_elem(K, j * ldk + c, in_dtype);
+        for (int64_t c = 0; c < dv; ++c) Vd[j * dv + c] = load_elem(V, j * ldv + c, in_dtype);
+    }
+    int rc = 0;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (int64_t i = 0; i < Nq; ++i) {
+        double* s = (double*)malloc(sizeof(double) * (size_t)Nk);
+        double* q = (double*)malloc(sizeof(double) * (size_t)d);
+        if (!s || !q) {
+            free(s);
+            free(q);
+            rc = -1;
+            continue;
+        }
+        for (int64_t c = 0; c < d; ++c) q[c] = load_elem(Q, i * ldq + c, in_dtype);
+        double m = -INFINITY, g = 0.0;
+        for (int64_t j = 0; j < Nk; ++j) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t c = 0; c < d; ++c) {
+                acc += q[c] * Kd[j * d + c];
+                mag += fabs(q[c] * Kd[j * d + c]);
+            }
+            s[j] = scale * acc;
+            if (s[j] > m) m = s[j];
+            if (mag > g) g = mag;
+        }
+        double l = 0.0;
+        for (int64_t j = 0; j < Nk; ++j) {
+            s[j] = exp(s[j] - m); /* now the unnormalised weight */
+            l += s[j];
+        }
+        for (int64_t c = 0; c < dv; ++c) {
+            double o = 0.0, e = 0.0;
+            for (int64_t j = 0; j < Nk; ++j) {
+                o += s[j] * Vd[j * dv + c];
+                e += s[j] * fabs(Vd[j * dv + c]);
+            }
+            O[i * dv + c] = o / l;
+            E[i * dv + c] = e / l;
+        }
+        G[i] = fabs(scale) * g;
+        free(s);
+        free(q);
+    }
+    (void)nthreads;
+    free(Kd);
+    free(Vd);
+    return rc;
 }

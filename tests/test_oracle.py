@@ -243,6 +243,108 @@ def pin_e4m3_gemm_exact(o: Oracle):
     assert np.array_equal(C, C16)
 
 
+# ------------------------------------------------------------ attention pins
+
+def _softmax_rows(x):
+    x = x - x.max(axis=1, keepdims=True)
+    e = np.exp(x)
+    return e / e.sum(axis=1, keepdims=True)
+
+
+def pin_attention_vs_scipy(o: Oracle):
+    # SciPy's softmax of NumPy's logits, times V: an independent formulation
+    special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(20)
+    for (Nq, Nk, d, dv, scale) in [(9, 13, 16, 5, 0.25), (4, 70, 40, 24, 1.0)]:
+        q = rng.standard_normal((Nq, d)).astype(np.float16)
+        k = rng.standard_normal((Nk, d)).astype(np.float16)
+        v = rng.standard_normal((Nk, dv)).astype(np.float16)
+        O, E, G = o.attention(q, k, v, scale)
+        S = scale * (q.astype(np.float64) @ k.astype(np.float64).T)
+        W = special.softmax(S, axis=1)
+        assert np.allclose(O, W @ v.astype(np.float64), rtol=0, atol=1e-13)
+        assert np.allclose(E, W @ np.abs(v.astype(np.float64)), rtol=0, atol=1e-13)
+        assert np.allclose(G, np.abs(scale) * (np.abs(q.astype(np.float64)) @
+                                               np.abs(k.astype(np.float64)).T).max(axis=1))
+
+
+def pin_attention_closed_forms(o: Oracle):
+    rng = np.random.default_rng(21)
+    # all keys equal: uniform weights, O = mean of the V rows (exact: 8 keys)
+    q = rng.standard_normal((6, 32)).astype(np.float16)
+    k = np.tile(rng.standard_normal((1, 32)), (8, 1)).astype(np.float16)
+    v = rng.integers(-4, 5, (8, 5)).astype(np.float16)
+    O, E, _ = o.attention(q, k, v)
+    assert np.array_equal(O, np.tile(v.astype(np.float64).mean(axis=0), (6, 1)))
+    # one key dominates by a gap of ~1000 in the logit: O is that key's V row
+    k = np.zeros((9, 4), np.float16)
+    k[5] = [10, 10, 10, 10]
+    q = np.full((3, 4), 25, np.float16)
+    v = rng.standard_normal((9, 6)).astype(np.float16)
+    O, _, _ = o.attention(q, k, v)
+    assert np.array_equal(O, np.tile(v[5].astype(np.float64), (3, 1)))
+    # V of ones: the weights sum to one
+    q = rng.standard_normal((5, 8)).astype(np.float16)
+    k = rng.standard_normal((11, 8)).astype(np.float16)
+    O, E, _ = o.attention(q, k, np.ones((11, 3), np.float16), 2.0)
+    assert np.allclose(O, 1.0, atol=1e-14) and np.allclose(E, 1.0, atol=1e-14)
+
+
+def pin_attention_invariants(o: Oracle):
+    rng = np.random.default_rng(22)
+    q = rng.standard_normal((7, 12)).astype(np.float16)
+    k = rng.standard_normal((10, 12)).astype(np.float16)
+    v = rng.standard_normal((10, 4)).astype(np.float16)
+    O, _, _ = o.attention(q, k, v, 0.5)
+    # permuting the keys together with their values changes nothing
+    perm = rng.permutation(10)
+    Op, _, _ = o.attention(q, k[perm], v[perm], 0.5)
+    assert np.allclose(Op, O, atol=1e-14)
+    # a shift shared by every key moves each row's logits by a constant
+    # (integer keys and shift, so the shifted keys are exact in fp16)
+    ki = rng.integers(-3, 4, (10, 12)).astype(np.float16)
+    shift = np.array([1, -1, 2, 0, 0, 2, 0, 0, -3, 0, 1, 0], np.float16)
+    Oa, _, _ = o.attention(q, ki, v, 0.5)
+    Ob, _, _ = o.attention(q, ki + shift, v, 0.5)
+    assert np.allclose(Ob, Oa, atol=1e-13)
+    # rows are independent: one query row alone gives the same output row
+    O1, _, _ = o.attention(q[3:4], k, v, 0.5)
+    assert np.array_equal(O1[0], O[3])
+    # row strides larger than the rows (sub-matrix views) read the same values
+    big_q = rng.standard_normal((9, 20)).astype(np.float16)
+    big_k = rng.standard_normal((14, 17)).astype(np.float16)
+    big_v = rng.standard_normal((12, 9)).astype(np.float16)
+    qs, ks, vs = big_q[1:8, 2:14], big_k[2:12, 3:15], big_v[1:11, 4:8]
+    Os, _, _ = o.attention(qs, ks, vs, 0.5)
+    Oc, _, _ = o.attention(np.ascontiguousarray(qs), np.ascontiguousarray(ks),
+                           np.ascontiguousarray(vs), 0.5)
+    assert np.array_equal(Os, Oc)
+
+
+def pin_attention_page_recurrence(o: Oracle):
+    # The blockwise recurrence of the TileLang page (running maximum M and
+    # normaliser L, blocks of keys), carried out in fp64 in Python on the
+    # page's 1024-key shape reduced to 96 keys: it reaches the definition.
+    rng = np.random.default_rng(23)
+    Nq, Nk, d, blk = 5, 96, 24, 32
+    q = rng.standard_normal((Nq, d)).astype(np.float16)
+    k = rng.standard_normal((Nk, d)).astype(np.float16)
+    v = rng.standard_normal((Nk, 7)).astype(np.float16)
+    Q, K, V = (x.astype(np.float64) for x in (q, k, v))
+    Ob = np.zeros((Nq, 7))
+    L = np.zeros(Nq)
+    M = np.full(Nq, -1e9)
+    for b0 in range(0, Nk, blk):
+        S = Q @ K[b0:b0 + blk].T
+        m_new = np.maximum(M, S.max(axis=1))
+        l_new = L * np.exp(M - m_new) + np.exp(S - m_new[:, None]).sum(axis=1)
+        Ob = (Ob * (L * np.exp(M - m_new))[:, None] +
+              np.exp(S - m_new[:, None]) @ V[b0:b0 + blk]) / l_new[:, None]
+        L, M = l_new, m_new
+    O, _, _ = o.attention(q, k, v, 1.0)
+    assert np.allclose(O, Ob, rtol=0, atol=1e-12)
+
+
 # ----------------------------------------------------- fused epilogue pins
 
 def pin_epilogue_plain(o: Oracle):
@@ -309,7 +411,8 @@ PINS = [pin_decode_exhaustive, pin_decode_by_hand, pin_encode_ties, pin_encode_v
         pin_roundtrip, pin_gemm_4x4, pin_gemm_8x8_ones, pin_closed_forms, pin_transpose,
         pin_vs_numpy_exact, pin_vs_numpy_random, pin_leading_dims, pin_sampled,
         pin_degenerate, pin_e4m3_decode_exhaustive, pin_e4m3_decode_by_hand,
-        pin_e4m3_gemm_exact, pin_epilogue_plain, pin_epilogue_block_identity, pin_gelu_normal_cdf,
+        pin_e4m3_gemm_exact, pin_attention_vs_scipy, pin_attention_closed_forms,
+        pin_attention_invariants, pin_attention_page_recurrence, pin_epilogue_plain, pin_epilogue_block_identity, pin_gelu_normal_cdf,
         pin_activation_odd_parts]
 
 
@@ -363,6 +466,12 @@ MUTANTS = {
     "e4m3_bias": ("(double)(8 + f), e - 10)", "(double)(8 + f), e - 11)"),
     "e4m3_subnormal": ("v = ldexp((double)f, -9);", "v = ldexp((double)f, -10);"),
     "e4m3_no_nan": ("if (e == 0xf && f == 0x7) {", "if (e == 0xf && f == 0x8) {"),
+    "attention_no_scale": ("s[j] = scale * acc;", "s[j] = acc;"),
+    "attention_v_transposed": ("o += s[j] * Vd[j * dv + c];", "o += s[j] * Vd[(c % Nk) * dv + (j % dv)];"),
+    "attention_no_normalise": ("O[i * dv + c] = o / l;", "O[i * dv + c] = o;"),
+    "attention_max_not_subtracted": ("s[j] = exp(s[j] - m);", "s[j] = exp(s[j]);"),
+    "attention_k_row_stride": ("Kd[j * d + c] = load_elem(K, j * ldk + c, in_dtype);",
+                               "Kd[j * d + c] = load_elem(K, j * d + c, in_dtype);"),
     "epilogue_alpha_dropped": ("double y = alpha * C[i * N + j];", "double y = C[i * N + j];"),
     "epilogue_beta_sign": ("y += beta * load_elem(", "y -= beta * load_elem("),
     "epilogue_ignored_ldcin": ("load_elem(Cin, i * ldcin + j, cin_dtype)",
