@@ -204,6 +204,53 @@ tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K,
                      tg_stream_t stream);
 
 /*
+ * tg_attention -- attention forward, O_b = softmax(scale * Q_b K_b^T) V_b for
+ * b = 0 .. batch-1 (heads or sequences of a strided batch), row by row.
+ *
+ * Source: "TileLang实战：用Python DSL自动生成高性能GPU计算内核" (gsyq.cn), §4
+ * (FlashAttention): the product softmax(Q K^T) V of §4.1, computed by §4.2
+ * blockwise over the keys with a running maximum M and normaliser L per query
+ * row, so the Nq x Nk score matrix never exists in memory.  The page applies
+ * no 1/sqrt(d) factor: pass scale = 1 for its kernel (the usual 1/sqrt(d) for
+ * transformer attention); any finite scale is accepted.  Full (non-causal)
+ * attention, as on the page.
+ *
+ * Arguments (sizes >= 0; row strides and matrix strides in elements):
+ *   Q  batch x Nq x d,  row i of matrix b at Q + b*strideQ + i*ldq.
+ *   K  batch x Nk x d,  likewise with ldk, strideK.
+ *   V  batch x Nk x dv, likewise with ldv, strideV.
+ *   O  batch x Nq x dv, written; row i of matrix b at O + b*strideO + i*ldo.
+ *   A stride of 0 uses one matrix for every b (e.g. keys shared by all
+ *   heads); with batch > 1 the O matrices must not overlap.
+ *   in_dtype  TG_F16 (Q, K and V); out_dtype TG_F16 or TG_F32.
+ *
+ * Semantics: s_ij = scale * sum_d Q_id K_jd with fp16 products accumulated in
+ * fp32 on the tensor cores; probabilities 2^(s_ij log2(e) - m_i) rounded to
+ * fp16 for the P V product, accumulated in fp32; O = (P V) / L rounded to
+ * out_dtype.  Elements of O between column dv and ldo are never written.
+ *
+ * Errors (checked on the host before anything is enqueued):
+ *   TG_ERR_INVALID_ARG  a negative size or stride; Nk == 0 or d == 0 (no
+ *                       softmax to take) with work to do; a NULL pointer;
+ *                       ld < row length; O not aligned to its element size;
+ *                       overlapping O matrices; O overlapping Q, K or V.
+ *   TG_ERR_UNSUPPORTED  other dtypes; Q, K or V not 16-byte aligned, a row
+ *                       stride not a multiple of 8, or a nonzero matrix
+ *                       stride that is not a multiple of 8 or smaller than a
+ *                       whole matrix (the TMA engine reads them); batch >
+ *                       65535, dv > 65535 * 128, or a size above 2^31 - 1024.
+ * batch, Nq or dv == 0 is a no-op.  Ownership, asynchrony, the device error
+ * word and the test hook are as for tg_gemm.
+ */
+tg_status tg_attention(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                       const void* Q, int64_t ldq, int64_t strideQ,
+                       const void* K, int64_t ldk, int64_t strideK,
+                       const void* V, int64_t ldv, int64_t strideV,
+                       void* O, int64_t ldo, int64_t strideO,
+                       float scale, tg_dtype in_dtype, tg_dtype out_dtype,
+                       tg_stream_t stream);
+
+/*
  * tg_gemm_check -- synchronize `stream`, then read and clear the current
  * device's error word.  Returns TG_OK, TG_ERR_CUDA if the stream reported a
  * CUDA error, or TG_ERR_TIMEOUT if a kernel abandoned a bounded wait (its

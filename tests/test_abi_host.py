@@ -326,3 +326,53 @@ def test_e4m3_path_selection():
         assert path(256, 256, 256, i=E) == 6
     finally:
         tg.tg_gemm_force_path(0)
+
+
+# ------------------------------------------------------------------ attention
+
+PQ, PK, PV, PO = 0x7F5000000000, 0x7F6000000000, 0x7F7000000000, 0x7F8000000000
+
+
+def acall(batch=1, Nq=128, Nk=128, d=64, dv=64, Q=PQ, K=PK, V=PV, O=PO, ldq=None, ldk=None,
+          ldv=None, ldo=None, sQ=None, sK=None, sV=None, sO=None, i=tg.F16, o=tg.F16):
+    ldq = d if ldq is None else ldq
+    ldk = d if ldk is None else ldk
+    ldv = dv if ldv is None else ldv
+    ldo = dv if ldo is None else ldo
+    sQ = Nq * ldq if sQ is None else sQ
+    sK = Nk * ldk if sK is None else sK
+    sV = Nk * ldv if sV is None else sV
+    sO = Nq * ldo if sO is None else sO
+    return tg.tg_attention(batch, Nq, Nk, d, dv, Q, ldq, sQ, K, ldk, sK, V, ldv, sV, O, ldo, sO,
+                           1.0, i, o, 0)
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(Nq=-1), tg.TG_ERR_INVALID_ARG),
+    (dict(batch=-1), tg.TG_ERR_INVALID_ARG),
+    (dict(Nk=0), tg.TG_ERR_INVALID_ARG),
+    (dict(d=0), tg.TG_ERR_INVALID_ARG),
+    (dict(Q=0), tg.TG_ERR_INVALID_ARG),
+    (dict(O=0), tg.TG_ERR_INVALID_ARG),
+    (dict(ldq=32), tg.TG_ERR_INVALID_ARG),
+    (dict(ldo=32), tg.TG_ERR_INVALID_ARG),
+    (dict(O=PO + 1), tg.TG_ERR_INVALID_ARG),
+    (dict(O=PQ + 64), tg.TG_ERR_INVALID_ARG),            # O inside Q
+    (dict(batch=2, sO=100), tg.TG_ERR_INVALID_ARG),       # overlapping O matrices
+    (dict(sQ=-8), tg.TG_ERR_INVALID_ARG),
+    (dict(i=tg.F32, o=tg.F32), tg.TG_ERR_UNSUPPORTED),
+    (dict(i=tg.E4M3), tg.TG_ERR_UNSUPPORTED),
+    (dict(o=tg.E4M3), tg.TG_ERR_UNSUPPORTED),
+    (dict(Q=PQ + 8), tg.TG_ERR_UNSUPPORTED),              # not TMA-addressable
+    (dict(ldk=68), tg.TG_ERR_UNSUPPORTED),
+    (dict(batch=2, sV=64 * 64 - 8), tg.TG_ERR_UNSUPPORTED),  # overlapping V matrices
+    (dict(batch=65536), tg.TG_ERR_UNSUPPORTED),
+])
+def test_attention_arguments_rejected_on_host(args, status):
+    assert acall(**args) == status
+
+
+def test_attention_degenerate_sizes_are_noops():
+    assert acall(batch=0, Q=0, K=0, V=0, O=0) == tg.TG_OK
+    assert acall(Nq=0, Q=0, K=0, V=0, O=0) == tg.TG_OK
+    assert acall(dv=0, Q=0, K=0, V=0, O=0) == tg.TG_OK

@@ -1,0 +1,212 @@
+"""GPU parity of the attention forward, O = softmax(scale * Q K^T) V, through
+tg_attention, against the oracle's fp64 definition.
+
+Acceptance per element: oracle.attention_tolerance (logit error from fp32
+accumulation of exact fp16 products, bounded through G; fp16 rounding of the
+probabilities; fp32 accumulation over the keys; 1e-2 relative for an fp16
+output).  Structured inputs whose softmax is exact (identical keys: uniform
+weights; one dominant key: a one-hot row) must match bit for bit.  The
+page's own configuration (one head, 1024 positions, d_model 768, no 1/sqrt(d)
+factor, normal inputs) is checked in full.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tiled_gemm_tg_gb300 as tg
+from tiled_gemm_tg_gb300 import inputs
+
+from gpu_util import GUARD, bits, f16_bits_of
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    yield
+
+
+def _place(x, ld, off=0):
+    """rows x cols fp16 CPU tensor at element offset `off` of a device buffer
+    with row stride ld (a multiple of 8 keeps it TMA-addressable)."""
+    rows, cols = x.shape[-2:]
+    lead = x.shape[0] if x.dim() == 3 else 1
+    buf = torch.zeros(off + lead * rows * ld + 64, dtype=torch.float16)
+    view = buf[off:off + lead * rows * ld].view(lead, rows, ld)
+    view[:, :, :cols] = x.reshape(lead, rows, cols)
+    dev = buf.cuda()
+    return dev, dev.data_ptr() + off * 2
+
+
+def run_attn(q, k, v, scale, out_dtype=torch.float16, ldq=None, ldk=None, ldv=None, ldo=None,
+             share_kv=False):
+    """q: (b, Nq, d), k: (b or 1, Nk, d), v: (b or 1, Nk, dv) fp16 on the CPU.
+    Returns (O as float64 (b, Nq, dv), canaries intact)."""
+    batch, Nq, d = q.shape
+    Nk, dv = v.shape[-2], v.shape[-1]
+    ldq = ldq or (d + 7) // 8 * 8
+    ldk = ldk or (d + 7) // 8 * 8
+    ldv = ldv or (dv + 7) // 8 * 8
+    ldo = ldo or dv + 3
+    Qb, Qp = _place(q, ldq)
+    Kb, Kp = _place(k, ldk)
+    Vb, Vp = _place(v, ldv)
+    sQ = Nq * ldq
+    sK = 0 if share_kv else Nk * ldk
+    sV = 0 if share_kv else Nk * ldv
+    sO = Nq * ldo + 5
+    n = GUARD + (batch - 1) * sO + Nq * ldo + GUARD
+    Ob = torch.empty(n, dtype=out_dtype, device="cuda")
+    bits(Ob).fill_(0x7E5A if out_dtype == torch.float16 else 0x7FC0A5A5)
+    canary = bits(Ob[:1].clone()).item()
+    oc = tg.F16 if out_dtype == torch.float16 else tg.F32
+    Op = Ob.data_ptr() + GUARD * Ob.element_size()
+    s = torch.cuda.current_stream().cuda_stream
+    st = tg.tg_attention(batch, Nq, Nk, d, dv, Qp, ldq, sQ, Kp, ldk, sK, Vp, ldv, sV, Op, ldo, sO,
+                         scale, tg.F16, oc, s)
+    assert st == tg.TG_OK, tg.tg_status_string(st)
+    assert tg.tg_gemm_check(s) == tg.TG_OK
+    h = Ob.cpu()
+    hb = bits(h)
+    written = torch.zeros(n, dtype=torch.bool)
+    outs = []
+    for b in range(batch):
+        start = GUARD + b * sO
+        outs.append(h[start:start + Nq * ldo].view(Nq, ldo)[:, :dv].double().numpy())
+        written[start:start + Nq * ldo].view(Nq, ldo)[:, :dv] = True
+    intact = bool((hb[~written] == canary).all())
+    return np.stack(outs), intact
+
+
+def _check(q, k, v, scale, got, out_dtype, what):
+    for b in range(q.shape[0]):
+        kb = k[b if k.shape[0] > 1 else 0]
+        vb = v[b if v.shape[0] > 1 else 0]
+        O, E, G = oracle.attention(q[b].numpy(), kb.numpy(), vb.numpy(), scale)
+        tol = oracle.attention_tolerance(O, E, G, q.shape[2], kb.shape[0],
+                                         out_dtype == torch.float16)
+        err = np.abs(got[b] - O)
+        bad = ~(err <= tol)
+        if bad.any():
+            i = tuple(int(x) for x in np.argwhere(bad)[0])
+            raise AssertionError(f"{what} batch {b}: {int(bad.sum())}/{bad.size} outside the "
+                                 f"bound; first {i}: got {got[b][i]!r} want {O[i]!r} "
+                                 f"tol {tol[i]!r}")
+
+
+def _qkv(batch, Nq, Nk, d, dv, seed, std=1.0):
+    g = torch.Generator().manual_seed(seed)
+    q = (torch.randn(batch, Nq, d, generator=g) * std).half()
+    k = (torch.randn(batch, Nk, d, generator=g) * std).half()
+    v = torch.randn(batch, Nk, dv, generator=g).half()
+    return q, k, v
+
+
+@pytest.mark.parametrize("Nq,Nk,d,dv,scale", [
+    (128, 128, 64, 64, 0.125), (200, 300, 64, 64, 0.125), (1, 1, 64, 64, 1.0),
+    (130, 257, 128, 128, 1 / math.sqrt(128)), (300, 500, 96, 80, 0.1),
+    (64, 1000, 40, 300, 0.15), (256, 384, 768, 768, 1.0), (129, 131, 256, 256, 0.0625),
+])
+@pytest.mark.parametrize("out", [torch.float16, torch.float32])
+def test_attention_shapes(Nq, Nk, d, dv, scale, out):
+    q, k, v = _qkv(1, Nq, Nk, d, dv, 13000 + Nq + Nk + d)
+    got, intact = run_attn(q, k, v, scale, out)
+    assert intact
+    _check(q, k, v, scale, got, out, f"{Nq}x{Nk} d{d} dv{dv}")
+
+
+def test_attention_page_configuration():
+    """One head, 1024 positions, d_model 768, scale 1, N(0,1) inputs (the
+    TileLang page's FlashAttention test data), fp32 output."""
+    q, k, v = _qkv(1, 1024, 1024, 768, 768, 13100)
+    got, intact = run_attn(q, k, v, 1.0, torch.float32)
+    assert intact
+    _check(q, k, v, 1.0, got, torch.float32, "page configuration")
+
+
+def test_attention_batched_and_shared_kv():
+    """Four heads with their own K/V, then four queries sharing one K/V."""
+    q, k, v = _qkv(4, 150, 260, 64, 64, 13200)
+    got, intact = run_attn(q, k, v, 0.125)
+    assert intact
+    _check(q, k, v, 0.125, got, torch.float16, "batched")
+    got, intact = run_attn(q, k[:1], v[:1], 0.125, share_kv=True)
+    assert intact
+    _check(q, k[:1], v[:1], 0.125, got, torch.float16, "shared K/V")
+
+
+def test_attention_growing_logits_rescale():
+    """Logits that grow key by key: the running maximum is raised in every
+    block, so O in tensor memory is rescaled again and again."""
+    Nq, Nk, d, dv = 128, 1024, 64, 64
+    g = torch.Generator().manual_seed(13300)
+    u = torch.randn(d, generator=g)
+    u = u / u.norm()
+    q = (u * 4).expand(Nq, d).clone() + 0.01 * torch.randn(Nq, d, generator=g)
+    t = torch.linspace(-4, 4, Nk)
+    k = t[:, None] * u[None, :] + 0.01 * torch.randn(Nk, d, generator=g)
+    v = torch.randn(Nk, dv, generator=g)
+    q, k, v = q.half()[None], k.half()[None], v.half()[None]
+    got, intact = run_attn(q, k, v, 1.0, torch.float32)
+    assert intact
+    _check(q, k, v, 1.0, got, torch.float32, "growing logits")
+
+
+@pytest.mark.parametrize("out", [torch.float16, torch.float32])
+def test_attention_uniform_weights_exact(out):
+    """Identical keys: every probability is 2^0 = 1, O is the mean of V's
+    rows, exact for integer V and 256 keys."""
+    Nq, Nk, d, dv = 100, 256, 64, 96
+    g = torch.Generator().manual_seed(13400)
+    q = torch.randn(1, Nq, d, generator=g).half()
+    k = torch.randn(1, 1, d, generator=g).half().expand(1, Nk, d).contiguous()
+    v = torch.randint(-8, 9, (1, Nk, dv), generator=g).half()
+    got, intact = run_attn(q, k, v, 0.125, out)
+    assert intact
+    want = np.broadcast_to(v[0].double().numpy().mean(axis=0), (Nq, dv))
+    if out == torch.float16:
+        assert np.array_equal(f16_bits_of(got[0]), f16_bits_of(want))
+    else:
+        assert np.array_equal(got[0], want)
+
+
+def test_attention_one_hot_exact():
+    """Each query has one key whose logit exceeds all others by 369 in base 2:
+    the other probabilities flush to zero and O is exactly that key's V row."""
+    Nq, Nk, d, dv = 128, 640, 128, 64
+    g = torch.Generator().manual_seed(13500)
+    hot = torch.randint(0, Nk, (Nq,), generator=g)
+    q = torch.zeros(Nq, d)
+    k = torch.zeros(Nk, d)
+    for i in range(Nq):
+        q[i, i] = 16.0           # query i looks along axis i only
+        k[hot[i], i] = 16.0      # and only key hot[i] has a component there
+    v = torch.randn(Nk, dv, generator=g).half()
+    got, intact = run_attn(q.half()[None], k.half()[None], v[None], 1.0, torch.float32)
+    assert intact
+    want = v[hot].double().numpy()
+    assert np.array_equal(got[0], want)
+
+
+def test_attention_binding_sampled_large():
+    """tg.attention on 3-D torch tensors: 8 heads, 4096 positions, d 128,
+    scale 1/sqrt(d); sampled query rows checked against the oracle."""
+    batch, N, d = 8, 4096, 128
+    q, k, v = _qkv(batch, N, N, d, d, 13600)
+    o = tg.attention(q.cuda(), k.cuda(), v.cuda(), 1 / math.sqrt(d))
+    tg.check()
+    rows = np.array([0, 1, 127, 128, 2049, 4095])
+    for b in (0, batch - 1):
+        O, E, G = oracle.attention(q[b].numpy()[rows], k[b].numpy(), v[b].numpy(),
+                                   1 / math.sqrt(d))
+        tol = oracle.attention_tolerance(O, E, G, d, N, True)
+        got = o[b].double().cpu().numpy()[rows]
+        assert np.all(np.abs(got - O) <= tol), f"head {b}"

@@ -19,7 +19,8 @@ __all__ = [
     "F16", "F32", "E4M3", "TG_OK", "TG_ERR_INVALID_ARG", "TG_ERR_UNSUPPORTED", "TG_ERR_CUDA",
     "TG_ERR_TIMEOUT", "PATHS", "TgError", "lib", "library_path", "tg_gemm", "tg_gemm_check",
     "tg_status_string", "tg_gemm_path", "tg_gemm_force_path", "tg_gemm_force_tiling",
-    "tg_gemm_test_hook", "tg_gemm_ex", "tg_gemm_batched", "tg_gemm_batched_path", "ACT_NONE", "ACT_RELU", "ACT_GELU",
+    "tg_gemm_test_hook", "tg_gemm_ex", "tg_gemm_batched", "tg_gemm_batched_path",
+    "tg_attention", "attention", "ACT_NONE", "ACT_RELU", "ACT_GELU",
     "tg_gemm_version", "gemm", "bmm",
     "check",
 ]
@@ -77,6 +78,9 @@ def lib() -> ctypes.CDLL:
         L.tg_gemm_batched_path.restype = i32
         L.tg_gemm_batched_path.argtypes = [i64, i64, i64, i64, vp, i64, i64, vp, i64, i64, vp,
                                            i64, i64, i32, i32]
+        L.tg_attention.restype = i32
+        L.tg_attention.argtypes = [i64, i64, i64, i64, i64, vp, i64, i64, vp, i64, i64, vp, i64,
+                                   i64, vp, i64, i64, ctypes.c_float, i32, i32, vp]
         L.tg_gemm_check.restype = i32
         L.tg_gemm_check.argtypes = [vp]
         L.tg_status_string.restype = ctypes.c_char_p
@@ -122,6 +126,13 @@ def tg_gemm_batched_path(batch, M, N, K, A, lda, sA, B, ldb, sB, C, ldc, sC, in_
                          out_dtype) -> int:
     return int(lib().tg_gemm_batched_path(batch, M, N, K, A, lda, sA, B, ldb, sB, C, ldc, sC,
                                           in_dtype, out_dtype))
+
+
+def tg_attention(batch, Nq, Nk, d, dv, Q, ldq, sQ, K, ldk, sK, V, ldv, sV, O, ldo, sO, scale,
+                 in_dtype, out_dtype, stream=0) -> int:
+    """Enqueue O_b = softmax(scale * Q_b K_b^T) V_b for b < batch."""
+    return int(lib().tg_attention(batch, Nq, Nk, d, dv, Q, ldq, sQ, K, ldk, sK, V, ldv, sV, O,
+                                  ldo, sO, float(scale), in_dtype, out_dtype, stream))
 
 
 def tg_gemm_check(stream=0) -> int:
@@ -250,6 +261,43 @@ def bmm(a, b, out=None, out_dtype=None, stream=None):
     if st != TG_OK:
         raise TgError(st, "tg_gemm_batched")
     return out
+
+
+def attention(q, k, v, scale=1.0, out=None, out_dtype=None, stream=None):
+    """softmax(scale * Q K^T) V for 2-D (Nq x d, Nk x d, Nk x dv) or 3-D
+    (batch first) fp16 CUDA tensors with contiguous rows; a batch stride of 0,
+    as from expand(), shares one matrix.  Allocates O with torch unless `out`
+    is given."""
+    import torch
+    squeeze = q.dim() == 2
+    if squeeze:
+        q, k, v = q.unsqueeze(0), k.unsqueeze(0), v.unsqueeze(0)
+        if out is not None:
+            out = out.unsqueeze(0)
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3 or not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be 2-D or 3-D CUDA tensors")
+    batch, Nq, d = q.shape
+    bk, Nk, dk = k.shape
+    bv, Nv, dv = v.shape
+    if dk != d or Nv != Nk or not (bk == bv == batch):
+        raise ValueError("shapes do not match: q (b, Nq, d), k (b, Nk, d), v (b, Nk, dv)")
+    if out is None:
+        od = out_dtype if out_dtype is not None else q.dtype
+        out = torch.empty((batch, Nq, dv), dtype=od, device=q.device)
+
+    def ld3(t):
+        if t.size(2) > 1 and t.stride(2) != 1:
+            raise ValueError("rows must be contiguous (row-major)")
+        ld = int(t.stride(1)) if t.size(1) > 1 else max(int(t.size(2)), 1)
+        return ld, (int(t.stride(0)) if t.size(0) > 1 else 0)
+
+    (ldq, sq), (ldk, sk), (ldv, sv), (ldo, so) = ld3(q), ld3(k), ld3(v), ld3(out)
+    st = tg_attention(batch, Nq, Nk, d, dv, q.data_ptr(), ldq, sq, k.data_ptr(), ldk, sk,
+                      v.data_ptr(), ldv, sv, out.data_ptr(), ldo, so, scale, _code(q.dtype),
+                      _code(out.dtype), _stream_handle(stream))
+    if st != TG_OK:
+        raise TgError(st, "tg_attention")
+    return out[0] if squeeze else out
 
 
 def check(stream=None) -> None:

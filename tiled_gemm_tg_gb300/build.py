@@ -26,6 +26,7 @@ SOURCES = [
     "gemm_tc_boundary.cu",
     "gemm_skinny.cu",
     "gemm_simt_f32.cu",
+    "attention_fwd.cu",
 ]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -382,6 +382,73 @@ tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda
     return run(path, p, epi, stream);
 }
 
+tg_status tg_attention(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                       const void* Q, int64_t ldq, int64_t strideQ, const void* K, int64_t ldk,
+                       int64_t strideK, const void* V, int64_t ldv, int64_t strideV, void* O,
+                       int64_t ldo, int64_t strideO, float scale, tg_dtype in_dtype,
+                       tg_dtype out_dtype, tg_stream_t stream)
+{
+    if (batch < 0 || Nq < 0 || Nk < 0 || d < 0 || dv < 0) return TG_ERR_INVALID_ARG;
+    if (strideQ < 0 || strideK < 0 || strideV < 0 || strideO < 0) return TG_ERR_INVALID_ARG;
+    if (in_dtype != TG_F16 || (out_dtype != TG_F16 && out_dtype != TG_F32))
+        return TG_ERR_UNSUPPORTED;
+    if (Nq > kMaxDim || Nk > kMaxDim || d > kMaxDim || dv > 65535LL * 128 || batch > kMaxBatch)
+        return TG_ERR_UNSUPPORTED;
+    if (batch == 0 || Nq == 0 || dv == 0) return TG_OK;
+    // softmax over no keys, or over all-zero logits of an empty dot product,
+    // is not an attention problem
+    if (Nk == 0 || d == 0) return TG_ERR_INVALID_ARG;
+    if (!Q || !K || !V || !O || ldq < d || ldk < d || ldv < dv || ldo < dv)
+        return TG_ERR_INVALID_ARG;
+    const size_t eo = esize(out_dtype);
+    if (reinterpret_cast<uintptr_t>(O) % eo != 0) return TG_ERR_INVALID_ARG;
+    if (batch > 1 && strideO < (Nq - 1) * ldo + dv) return TG_ERR_INVALID_ARG;
+    u128 o0, o1, q0, q1, k0, k1, v0, v1;
+    span(O, Nq, dv, ldo, eo, &o0, &o1, batch, strideO);
+    span(Q, Nq, d, ldq, 2, &q0, &q1, batch, strideQ);
+    span(K, Nk, d, ldk, 2, &k0, &k1, batch, strideK);
+    span(V, Nk, dv, ldv, 2, &v0, &v1, batch, strideV);
+    const u128 top = static_cast<u128>(1) << 64;
+    if (o1 > top || q1 > top || k1 > top || v1 > top) return TG_ERR_INVALID_ARG;
+    if (overlaps(o0, o1, q0, q1) || overlaps(o0, o1, k0, k1) || overlaps(o0, o1, v0, v1))
+        return TG_ERR_INVALID_ARG;
+    // Q, K and V are read by the TMA engine only
+    auto tma_ok = [&](const void* p, int64_t ld, int64_t stride, int64_t rows) {
+        return reinterpret_cast<uintptr_t>(p) % 16 == 0 && ld % 8 == 0 &&
+               ld < (int64_t(1) << 38) && (batch == 1 || tma_stride_ok(stride, rows, ld, 2));
+    };
+    if (!tma_ok(Q, ldq, strideQ, Nq) || !tma_ok(K, ldk, strideK, Nk) || !tma_ok(V, ldv, strideV, Nk))
+        return TG_ERR_UNSUPPORTED;
+
+    DeviceState* ds = nullptr;
+    tg_status st = device_state(&ds);
+    if (st != TG_OK) return st;
+    tg::AttnArgs a;
+    a.batch = static_cast<int>(batch);
+    a.Nq = static_cast<int>(Nq);
+    a.Nk = static_cast<int>(Nk);
+    a.d = static_cast<int>(d);
+    a.dv = static_cast<int>(dv);
+    a.Q = Q;
+    a.ldq = ldq;
+    a.sQ = batch > 1 ? strideQ : 0;
+    a.K = K;
+    a.ldk = ldk;
+    a.sK = batch > 1 ? strideK : 0;
+    a.V = V;
+    a.ldv = ldv;
+    a.sV = batch > 1 ? strideV : 0;
+    a.O = O;
+    a.ldo = ldo;
+    a.sO = batch > 1 ? strideO : 0;
+    a.out_f32 = out_dtype == TG_F32;
+    a.scale = scale;
+    a.err = ds->err;
+    a.hook = g_test_hook.load(std::memory_order_relaxed);
+    a.stream = static_cast<cudaStream_t>(stream);
+    return tg::launch_attention(a) == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+}
+
 tg_status tg_gemm_check(tg_stream_t stream)
 {
     cudaStream_t s = static_cast<cudaStream_t>(stream);

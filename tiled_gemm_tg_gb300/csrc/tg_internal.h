@@ -26,6 +26,7 @@ enum ErrBits : unsigned int {
     ERR_BOUNDARY = 1u << 3,
     ERR_SKINNY = 1u << 4,
     ERR_DRAIN = 1u << 5,
+    ERR_ATTENTION = 1u << 6,
 };
 
 // Fused epilogue  C = act(alpha * acc + beta * D + bias[n]), applied to the
@@ -109,6 +110,27 @@ cudaError_t launch_skinny(const GemmArgs& a);
 // K == 0: C = act(beta * D + bias) elementwise (zeros without an epilogue),
 // for every matrix of a strided batch.
 cudaError_t launch_epilogue_only(const GemmArgs& a);
+
+// Attention forward O_b = softmax(scale * Q_b K_b^T) V_b for a strided batch
+// (fp16 Q, K, V; fp16 or fp32 O).  Strides and row strides in elements.
+struct AttnArgs {
+    int batch, Nq, Nk, d, dv;
+    const void* Q;
+    long long ldq, sQ;
+    const void* K;
+    long long ldk, sK;
+    const void* V;
+    long long ldv, sV;
+    void* O;
+    long long ldo, sO;
+    bool out_f32;
+    float scale;
+    unsigned int* err;
+    int hook;
+    cudaStream_t stream;
+};
+
+cudaError_t launch_attention(const AttnArgs& a);
 
 // Tile width the main kernel uses for this problem (64, 128 or 256).
 int main_tile_n(int M, int N, int batch, int num_sms);
