@@ -236,6 +236,209 @@ EPILOGUES = {
 }
 
 
+def attn_cpu_sample(w, q, k, v, target_s: float):
+    """Time the oracle on whole query rows of head 0, growing the row count
+    until one call takes about target_s.  Returns (TFLOP/s, rows, s, threads)."""
+    import oracle
+
+    nt = oracle.num_threads()
+    qn, kn, vn = q[0].numpy(), k[0].numpy(), v[0].numpy()
+    rows = max(1, min(nt, w.Nq))
+    while True:
+        t = time.perf_counter()
+        oracle.attention(qn[:rows], kn, vn, w.scale)
+        dt = time.perf_counter() - t
+        if dt >= 0.6 * target_s or rows >= w.Nq:
+            break
+        rows = min(w.Nq, rows * max(2, int(0.9 * target_s / max(dt, 1e-3))))
+    return 2.0 * rows * w.Nk * (w.d + w.dv) / dt / 1e12, rows, dt, nt
+
+
+def run_reference_attention(args, w):
+    """The reference arm for an attention workload: the oracle on host cores."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from tiled_gemm_tg_gb300 import inputs
+
+    q, k, v = inputs.attn_operands(w)
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    v0, rows, dt, nt = attn_cpu_sample(w, q, k, v, min(budget, 5.0))
+    import oracle
+
+    qn, kn, vn = q[0].numpy()[:rows], k[0].numpy(), v[0].numpy()
+    for _ in range(args.warmup):
+        oracle.attention(qn, kn, vn, w.scale)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.attention(qn, kn, vn, w.scale)
+    el = time.perf_counter() - t0
+    value = 2.0 * rows * w.Nk * (w.d + w.dv) * args.steps / el / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+                   "dv": w.dv, "scale": w.scale},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nt, "kind": "oracle",
+                         "sample": f"{rows} of {w.Nq} query rows of head 0 per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main_attention(args, w):
+    """Attention forward, O = softmax(scale * Q K^T) V, timed like the GEMM:
+    device-resident inputs rotated past L2, CUDA events per launch, clocks
+    sampled, an end-to-end leg through the C ABI from pinned host buffers."""
+    import torch
+
+    import tiled_gemm_tg_gb300 as tg
+    from tiled_gemm_tg_gb300 import inputs
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    tg.lib()
+    q_cpu, k_cpu, v_cpu = inputs.attn_operands(w)
+    out_dt = torch.float16 if w.out_dtype == "f16" else torch.float32
+    oc = tg.F16 if w.out_dtype == "f16" else tg.F32
+    set_bytes = w.algorithmic_bytes()
+    n_sets = max(2, min(64, -(-3 * 129 * 2**20 // set_bytes)))
+    sets = []
+    for i in range(n_sets):
+        sets.append((q_cpu.to(dev), k_cpu.to(dev), v_cpu.to(dev),
+                     torch.empty((w.batch, w.Nq, w.dv), dtype=out_dt, device=dev)))
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    B, Nq, Nk, d, dv = w.batch, w.Nq, w.Nk, w.d, w.dv
+
+    def call(q, k, v, o, handle):
+        st = tg.tg_attention(B, Nq, Nk, d, dv, q.data_ptr(), d, Nq * d, k.data_ptr(), d, Nk * d,
+                             v.data_ptr(), dv, Nk * dv, o.data_ptr(), dv, Nq * dv, w.scale,
+                             tg.F16, oc, handle)
+        if st != tg.TG_OK:
+            raise tg.TgError(st, "tg_attention")
+
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = None
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.3)
+    for i in range(args.warmup):
+        call(*sets[i % n_sets], sh)
+    tg.check(stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    host_t0 = time.time()
+    t_start.record(stream)
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        call(*sets[i % n_sets], sh)
+        evs[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    host_t1 = time.time()
+    if ws > 1:
+        torch.distributed.barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    kern_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    if tg.tg_gemm_check(sh) != tg.TG_OK:
+        raise RuntimeError("a kernel abandoned a bounded wait during the timed region")
+    if ws > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    flops = float(w.flops)
+    value = ws * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
+
+    # end to end: Q, K, V in from pinned host memory, O out, every step
+    e2e_steps = args.e2e_steps or max(3, min(args.steps, 20))
+    qh, kh, vh = q_cpu.pin_memory(), k_cpu.pin_memory(), v_cpu.pin_memory()
+    oh = torch.empty((B, Nq, dv), dtype=out_dt).pin_memory()
+    qd, kd, vd, od = sets[0]
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        call(qd, kd, vd, od, sh)
+        oh.copy_(od, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if tg.tg_gemm_check(sh) != tg.TG_OK:
+        raise RuntimeError("a kernel abandoned a bounded wait during the e2e region")
+    e2e_value = ws * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    sampler.stop()
+    clocks = sampler.summary(host_t0, host_t1)
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = flops / (kern_ms * 1e-3) / 1e12
+    alg_bytes = w.algorithmic_bytes()
+    roofline = {
+        "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+        "frac": achieved / peak, "traffic": None, "kernel": "attention_fwd_kernel",
+        "kernel_ms": kern_ms,
+        "peak_source": f"{peak_src} bf16 burst (torch.matmul 8192^3) x 1.0 fp16/bf16 nominal ratio",
+        "flop_per_byte": flops / alg_bytes, "algorithmic_bytes": alg_bytes,
+        "achieved_gbs": alg_bytes / (kern_ms * 1e-3) / 1e9,
+        "tensor_flops_executed": 2.0 * B * Nq * Nk * (d * -(-dv // 256) + dv),
+    }
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        v0, rows, secs, nt = attn_cpu_sample(w, q_cpu, k_cpu, v_cpu, args.cpu_seconds)
+        cpu = {"value": v0, "unit": "TFLOP/s", "cores": nt, "kind": "oracle",
+               "sample": f"{rows} of {Nq} query rows of head 0, {secs:.1f} s"}
+    if rank == 0:
+        line = {
+            "metric": "attention forward TFLOP/s (4 Nq Nk d per head) and % of GB300 dense "
+                      "FP16 tensor peak (1 GPU)",
+            "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "batch": B, "Nq": Nq, "Nk": Nk, "d": d, "dv": dv,
+                       "scale": w.scale, "out_dtype": w.out_dtype, "accum": "f32",
+                       "l2": f"{n_sets} rotating Q/K/V/O sets, "
+                             f"{n_sets * set_bytes / 2**20:.0f} MB per pass",
+                       "timing": "stream launches",
+                       "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+            "clocks": clocks,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": B * (Nq * d + Nk * (d + dv)) * 2,
+                    "d2h_bytes_per_step": B * Nq * dv * oh.element_size(), "steps": e2e_steps,
+                    "pipeline": "H2D / tg_attention / D2H on one stream"},
+            "gpu_launches": args.steps,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -255,6 +458,11 @@ def main():
         ap.error("--warmup must be at least 3")
 
     from tiled_gemm_tg_gb300 import inputs
+    if args.workload in inputs.ATTN_WORKLOADS:
+        wa = inputs.ATTN_WORKLOADS[args.workload]
+        if args.impl == "reference":
+            return run_reference_attention(args, wa)
+        return main_attention(args, wa)
     w = inputs.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)

@@ -69,6 +69,52 @@ WORKLOADS = {
 EDGE_SET = ["edge_4x4x4", "edge_128x256x512", "edge_127x255x512", "edge_1x255x17"]
 
 
+@dataclass(frozen=True)
+class AttnWorkload:
+    """softmax(scale * Q K^T) V for `batch` independent heads."""
+    name: str
+    batch: int
+    Nq: int
+    Nk: int
+    d: int
+    dv: int
+    scale: float
+    out_dtype: str     # "f16" or "f32"
+    seed_base: int
+
+    @property
+    def flops(self) -> int:
+        """Q K^T and P V: 2 Nq Nk d + 2 Nq Nk dv per head."""
+        return 2 * self.batch * self.Nq * self.Nk * (self.d + self.dv)
+
+    def algorithmic_bytes(self) -> int:
+        """Q, K, V read once (fp16), O written once."""
+        eout = 2 if self.out_dtype == "f16" else 4
+        return self.batch * ((self.Nq * self.d + self.Nk * (self.d + self.dv)) * 2 +
+                             self.Nq * self.dv * eout)
+
+
+ATTN_WORKLOADS = {
+    w.name: w
+    for w in [
+        # the TileLang page's FlashAttention test: one head, seq_len 1024,
+        # d_model 768, N(0,1) data, no 1/sqrt(d) factor (fp16 in, fp32 out)
+        AttnWorkload("attn_page_1x1024x768", 1, 1024, 1024, 768, 768, 1.0, "f32", 8000),
+        # the page's largest length, 2048, as heads of the usual width
+        AttnWorkload("attn_16x2048x128", 16, 2048, 2048, 128, 128, 128 ** -0.5, "f16", 8100),
+        AttnWorkload("attn_16x4096x128", 16, 4096, 4096, 128, 128, 128 ** -0.5, "f16", 8200),
+    ]
+}
+
+
+def attn_operands(w: AttnWorkload):
+    """(Q, K, V) fp16 on the CPU, batch x rows x width, N(0,1) draws."""
+    q = draw((w.batch, w.Nq, w.d), "normal", w.seed_base + 1, "f16")
+    k = draw((w.batch, w.Nk, w.d), "normal", w.seed_base + 2, "f16")
+    v = draw((w.batch, w.Nk, w.dv), "normal", w.seed_base + 3, "f16")
+    return q, k, v
+
+
 def draw(shape, dist: str, seed: int, dtype: str, k: int | None = None) -> torch.Tensor:
     """One seeded operand on the CPU, row-major and contiguous."""
     g = torch.Generator().manual_seed(int(seed))
