@@ -32,6 +32,7 @@
 // the device error word, raises the CTA's abort flag and winds down.
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -305,27 +306,38 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 break;
             }
             tc_fence_after();
-            float sv[BN];
+            // S_t row r: four 32-column loads in flight, one wait
+            uint32_t raw[BN];
 #pragma unroll
-            for (int i = 0; i < BN / 32; ++i) {
-                uint32_t raw[32];
-                tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(sb * BN + 32 * i), raw);
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) sv[32 * i + j] = __uint_as_float(raw[j]);
-            }
+            for (int i = 0; i < BN / 32; ++i)
+                tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(sb * BN + 32 * i),
+                                   *reinterpret_cast<uint32_t(*)[32]>(raw + 32 * i));
+            tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(smem_u32(&s_empty[sb]));
 
-            // logits in base 2; keys past Nk (zero-filled by TMA) are masked
+            // block maximum of the base-2 logits; keys past Nk (zero-filled by
+            // TMA) are masked, which only the last block can need
             const int valid = min(BN, Nk - t * BN);
-            float mx = -INFINITY;
+            if (valid < BN) {
 #pragma unroll
-            for (int j = 0; j < BN; ++j) {
-                const float x = j < valid ? sv[j] * scale_log2 : -INFINITY;
-                sv[j] = x;
-                mx = fmaxf(mx, x);
+                for (int j = 0; j < BN; ++j)
+                    if (j >= valid) raw[j] = __float_as_uint(scale_log2 >= 0.0f ? -INFINITY : INFINITY);
             }
+            // (four independent chains keep the reduction short)
+            float mc[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) mc[c] = __uint_as_float(raw[c]);
+            if (scale_log2 >= 0.0f) {
+#pragma unroll
+                for (int j = 4; j < BN; ++j) mc[j & 3] = fmaxf(mc[j & 3], __uint_as_float(raw[j]));
+            } else {
+#pragma unroll
+                for (int j = 4; j < BN; ++j) mc[j & 3] = fminf(mc[j & 3], __uint_as_float(raw[j]));
+            }
+            const float mraw = scale_log2 >= 0.0f ? fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]))
+                                                  : fminf(fminf(mc[0], mc[1]), fminf(mc[2], mc[3]));
+            const float mx = mraw * scale_log2;
             const bool raise = mx > m_run + kRescaleLog2;
             float alpha = 1.0f;
             if (raise) {
@@ -333,6 +345,7 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 l_run *= alpha;
                 m_run = mx;
             }
+            const float neg_m = -m_run;
 
             // the P buffer must be free: the MMAs of block t - 2 have read it
             const bool got_p = mbar_wait(smem_u32(&p_empty[sb]), ((t >> 1) & 1) ^ 1u, &abort_flag,
@@ -363,23 +376,39 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 tmem_st_wait();
             }
 
-            // P = 2^(logit - m) in fp16, row r of the swizzled K-major tile
+            // P = 2^(s * scale * log2 e - m) in fp16, row r of the swizzled
+            // K-major tile; the row sum in two chains.  Masked keys (the last
+            // block only) get probability 0 whatever the scale.
             const uint32_t prow = p_base + sb * P_BUF + static_cast<uint32_t>(r) * 128u;
+            float l0 = 0.0f, l1 = 0.0f;
+            auto write_p = [&](auto masked) {
 #pragma unroll
-            for (int ch = 0; ch < BN / 8; ++ch) {
-                uint32_t w[4];
+                for (int ch = 0; ch < BN / 8; ++ch) {
+                    uint32_t w[4];
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const float p0 = ex2_approx(sv[8 * ch + 2 * h] - m_run);
-                    const float p1 = ex2_approx(sv[8 * ch + 2 * h + 1] - m_run);
-                    l_run += p0 + p1;
-                    __half2 v2 = __floats2half2_rn(p0, p1);
-                    w[h] = *reinterpret_cast<uint32_t*>(&v2);
+                    for (int h = 0; h < 4; ++h) {
+                        const int j = 8 * ch + 2 * h;
+                        float a0 = fmaf(__uint_as_float(raw[j]), scale_log2, neg_m);
+                        float a1 = fmaf(__uint_as_float(raw[j + 1]), scale_log2, neg_m);
+                        if constexpr (decltype(masked)::value) {
+                            if (j >= valid) a0 = -INFINITY;
+                            if (j + 1 >= valid) a1 = -INFINITY;
+                        }
+                        const float p0 = ex2_approx(a0);
+                        const float p1 = ex2_approx(a1);
+                        l0 += p0;
+                        l1 += p1;
+                        __half2 v2 = __floats2half2_rn(p0, p1);
+                        w[h] = *reinterpret_cast<uint32_t*>(&v2);
+                    }
+                    const uint32_t atom = static_cast<uint32_t>(ch >> 3);
+                    const uint32_t pos = static_cast<uint32_t>((ch & 7) ^ (r & 7));
+                    st_shared_v4(prow + atom * P_ATOM + pos * 16u, w[0], w[1], w[2], w[3]);
                 }
-                const uint32_t atom = static_cast<uint32_t>(ch >> 3);
-                const uint32_t pos = static_cast<uint32_t>((ch & 7) ^ (r & 7));
-                st_shared_v4(prow + atom * P_ATOM + pos * 16u, w[0], w[1], w[2], w[3]);
-            }
+            };
+            if (valid < BN) write_p(std::true_type{});
+            else write_p(std::false_type{});
+            l_run += l0 + l1;
             fence_proxy_async_smem();  // generic-proxy P writes -> visible to the tensor core
             tc_fence_before();
             mbar_arrive(smem_u32(&p_full[sb]));
