@@ -18,17 +18,19 @@
 //                      128-byte-swizzled K-major layout the MMA reads;
 //   O += P_t V_t       tcgen05.mma, M=128 N=DVS K=128, V MN-major from TMA,
 //                      accumulating in TMEM columns 256 .. 256+DVS.
-// The MMA issuer computes S_(t+1) before P_t V_t, so the tensor core works
-// on the next scores while the softmax warps turn S_t into P_t.  The running
+// Two threads issue the MMAs: one the scores (up to two blocks ahead, into
+// alternating S buffers), the other P_t V_t as soon as P_t is written, so
+// the tensor core works on the next scores while the softmax warps turn S_t
+// into P_t and neither stream waits behind the other's barriers.  The running
 // maximum is raised only when a block's maximum exceeds it by more than 8 (in
 // base 2): then O (in TMEM) and L are scaled by 2^(m_old - m_new); otherwise
 // the stale maximum stays, the probabilities stay below 2^8, and the final
 // O / L is the same quotient.  Outputs wider than 256 columns take several
 // CTAs, each recomputing S for its own slice of V.
 //
-// Warp roles (256 threads): 0 TMA for Q and K, 1 TMEM allocation and MMA
-// issue, 2 TMA for V, 4-7 softmax and output (warp w reads TMEM lane
-// quadrant w % 4).  Every wait is bounded: on expiry a role records it in
+// Warp roles (384 threads): 0 TMA for Q and K, 1 TMEM allocation and the
+// S MMAs, 2 TMA for V, 3 the P V MMAs, 4-11 softmax and output (warp w reads
+// TMEM lane quadrant w % 4; two warps per quadrant split the keys).  Every wait is bounded: on expiry a role records it in
 // the device error word, raises the CTA's abort flag and winds down.
 #include <cstdint>
 #include <mutex>
@@ -50,54 +52,74 @@ using namespace tg::dev;
 constexpr int BM = 128;                       // query rows per CTA
 constexpr int BN = 128;                       // keys per block
 constexpr int DC = 64;                        // d per chunk: 128 bytes of fp16
-constexpr int QK_STAGES = 3;
 constexpr uint32_t Q_CHUNK = BM * DC * 2;     // 16 KB
 constexpr uint32_t K_CHUNK = BN * DC * 2;     // 16 KB
-constexpr uint32_t QK_STAGE = Q_CHUNK + K_CHUNK;
 constexpr uint32_t P_ATOM = BM * 128;         // [128 rows][64 keys] fp16, 16 KB
 constexpr uint32_t P_BUF = 2 * P_ATOM;        // 128 keys
 constexpr uint32_t V_BOX = BN * 128;          // [128 keys][64 columns] fp16, 16 KB
 constexpr uint32_t TMEM_COLS = 512;           // S0, S1 (128 each), O (<= 256)
 constexpr uint32_t O_COL = 256;
-constexpr int kThreads = 256;
-constexpr uint32_t kSoftmaxThreads = 128;
+constexpr int kThreads = 384;                 // 4 role warps + 8 softmax warps
+constexpr uint32_t kSoftmaxThreads = 256;
 constexpr float kRescaleLog2 = 8.0f;          // raise the running max past 2^8 growth
 
-template <int DVS>
+// QMODE: the number of 64-wide Q chunks kept resident in shared memory for
+// the whole CTA (2: d <= 128, 4: d <= 256), so the ring carries K chunks
+// only; or 0: Q is streamed with K, chunk by chunk, for any d.  The ring gets
+// whatever shared memory the fixed parts leave.
+template <int DVS, int QMODE>
 struct AttnCfg {
     static_assert(DVS == 128 || DVS == 256, "an output slice is 128 or 256 columns");
+    static_assert(QMODE == 0 || QMODE == 2 || QMODE == 4, "resident Q of 0, 2 or 4 chunks");
+#ifdef TG_ATTN_V_STAGES
+    static constexpr int V_STAGES = DVS == 128 ? (QMODE == 2 ? TG_ATTN_V_STAGES : 2) : 1;
+#else
     static constexpr int V_STAGES = DVS == 128 ? 2 : 1;
+#endif
     static constexpr uint32_t V_STAGE = BN * DVS * 2;
-    static constexpr uint32_t SMEM =
-        QK_STAGES * QK_STAGE + V_STAGES * V_STAGE + 2 * P_BUF + 1024;
-    static_assert(SMEM <= 227 * 1024, "shared-memory budget exceeded");
+    static constexpr uint32_t Q_RES = QMODE * Q_CHUNK;
+    static constexpr uint32_t STAGE = QMODE ? K_CHUNK : Q_CHUNK + K_CHUNK;
+    static constexpr uint32_t FIXED = Q_RES + V_STAGES * V_STAGE + P_BUF + 1024;
+    // 227 KB per CTA covers static shared memory too: keep 4 KB for it
+    static constexpr uint32_t BUDGET = 227 * 1024 - 4096;
+    static constexpr int STAGES = static_cast<int>((BUDGET - FIXED) / STAGE);
+    static constexpr uint32_t SMEM = FIXED + STAGES * STAGE;
+    static_assert(STAGES >= 3, "too few pipeline stages");
+    static_assert(SMEM <= BUDGET, "shared-memory budget exceeded");
 };
 
-template <int DVS, bool OUT_F32>
+template <int DVS, bool OUT_F32, int QMODE>
 __global__ void __launch_bounds__(kThreads, 1)
 attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, void* O, long long ldo, long long sO,
                      int Nq, int Nk, int dv, int n_chunks, float scale_log2, int o_vec, int zq,
                      int zk, int zv, int hook, unsigned int* err)
 {
-    using Cfg = AttnCfg<DVS>;
+    using Cfg = AttnCfg<DVS, QMODE>;
     constexpr int VS = Cfg::V_STAGES;
+    constexpr int QK_STAGES = Cfg::STAGES;
+    constexpr uint32_t QK_STAGE = Cfg::STAGE;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t qk_full[QK_STAGES];
     __shared__ __align__(8) uint64_t qk_empty[QK_STAGES];
+    __shared__ __align__(8) uint64_t q_full;              // the resident Q (QMODE > 0)
     __shared__ __align__(8) uint64_t v_full[VS];
     __shared__ __align__(8) uint64_t v_empty[VS];
     __shared__ __align__(8) uint64_t s_full[2];
     __shared__ __align__(8) uint64_t s_empty[2];
-    __shared__ __align__(8) uint64_t p_full[2];
-    __shared__ __align__(8) uint64_t p_empty[2];
+    __shared__ __align__(8) uint64_t p_full;              // one P buffer
+    __shared__ __align__(8) uint64_t p_empty;
     __shared__ __align__(8) uint64_t drain_bar;
+    __shared__ __align__(8) uint64_t drain_bar2;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
+    __shared__ float red[2][2][BM];   // per-row partial maxima of the two halves, by block parity
+    __shared__ float lsum[2][BM];     // per-row partial normalisers of the two halves
 
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-    const uint32_t qk_base = base;
-    const uint32_t v_base = base + QK_STAGES * QK_STAGE;
+    const uint32_t q_res = base;                       // resident Q chunks
+    const uint32_t qk_base = base + Cfg::Q_RES;        // the ring
+    const uint32_t v_base = qk_base + QK_STAGES * QK_STAGE;
     const uint32_t p_base = v_base + VS * Cfg::V_STAGE;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -118,10 +140,12 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&s_full[b]), 1);
             mbar_init(smem_u32(&s_empty[b]), kSoftmaxThreads);
-            mbar_init(smem_u32(&p_full[b]), kSoftmaxThreads);
-            mbar_init(smem_u32(&p_empty[b]), 1);
         }
+        mbar_init(smem_u32(&q_full), 1);
+        mbar_init(smem_u32(&p_full), kSoftmaxThreads);
+        mbar_init(smem_u32(&p_empty), 1);
         mbar_init(smem_u32(&drain_bar), 1);
+        mbar_init(smem_u32(&drain_bar2), 1);
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -148,6 +172,13 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             int s = 0;
             uint32_t ph = 0, issued = 0;
             bool ok = true;
+            if constexpr (QMODE > 0) {
+                // the CTA's Q tile, once
+                const uint32_t qb = smem_u32(&q_full);
+                mbar_arrive_expect_tx(qb, static_cast<uint32_t>(n_chunks) * Q_CHUNK);
+                for (int c = 0; c < n_chunks; ++c)
+                    tma_load_3d(q_res + c * Q_CHUNK, &tmQ, qb, c * DC, q0, bz * zq);
+            }
             for (int t = 0; t < n_kv && ok; ++t) {
                 for (int c = 0; c < n_chunks; ++c) {
                     if (!mbar_wait(smem_u32(&qk_empty[s]), ph ^ 1u, &abort_flag)) {
@@ -160,8 +191,12 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                         const uint32_t fb = smem_u32(&qk_full[s]);
                         const uint32_t sa = qk_base + s * QK_STAGE;
                         mbar_arrive_expect_tx(fb, QK_STAGE);
-                        tma_load_3d(sa, &tmQ, fb, c * DC, q0, bz * zq);
-                        tma_load_3d(sa + Q_CHUNK, &tmK, fb, c * DC, t * BN, bz * zk);
+                        if constexpr (QMODE == 0) {
+                            tma_load_3d(sa, &tmQ, fb, c * DC, q0, bz * zq);
+                            tma_load_3d(sa + Q_CHUNK, &tmK, fb, c * DC, t * BN, bz * zk);
+                        } else {
+                            tma_load_3d(sa, &tmK, fb, c * DC, t * BN, bz * zk);
+                        }
                         ++issued;
                     }
                     if (++s == QK_STAGES) {
@@ -177,6 +212,9 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                     ph ^= 1u;
                 }
                 if (!mbar_wait(smem_u32(&qk_full[s]), ph, nullptr)) atomicOr(err, ERR_DRAIN);
+            }
+            if constexpr (QMODE > 0) {
+                if (!mbar_wait(smem_u32(&q_full), 0, nullptr)) atomicOr(err, ERR_DRAIN);
             }
         }
         __syncwarp();
@@ -213,130 +251,172 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         }
         __syncwarp();
     } else if (warp == 1) {
-        // --------------------------------------------------- MMA issuer
+        // ------------------------------------------ MMA issuer: S = Q K^T
+        // (a second issuer, warp 3, does O += P V, so that neither stream
+        // of MMAs waits behind the other's barriers)
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_f16_f32(BM, BN, false, false);
-            constexpr uint32_t idesc_o = idesc_f16_f32(BM, DVS, false, true);
-            int s = 0, vs = 0;
-            uint32_t ph = 0, vph = 0;
+            int s = 0;
+            uint32_t ph = 0;
             bool ok = true;
-            for (int t = 0; t <= n_kv && ok; ++t) {
-                if (t < n_kv) {
-                    // S_t = Q K_t^T into S buffer t % 2, once the softmax has
-                    // read S_(t-2) from it
-                    const int sb = t & 1;
-                    if (!mbar_wait(smem_u32(&s_empty[sb]), ((t >> 1) & 1) ^ 1u, &abort_flag,
-                                   long_limit)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t d_s = tmem_base + static_cast<uint32_t>(sb * BN);
-                    for (int c = 0; c < n_chunks; ++c) {
-                        if (!mbar_wait(smem_u32(&qk_full[s]), ph, &abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t sa = qk_base + s * QK_STAGE;
-                        // both operands K-major: 8-row groups 1024 B apart, +32 B per 16 of d
-                        const uint64_t ad = sdesc_sw128(sa, 16, 1024);
-                        const uint64_t bd = sdesc_sw128(sa + Q_CHUNK, 16, 1024);
-#pragma unroll
-                        for (int k = 0; k < DC / 16; ++k)
-                            umma_f16(d_s, ad + 2ull * k, bd + 2ull * k, idesc_s,
-                                     (c | k) != 0 ? 1u : 0u);
-                        umma_commit(smem_u32(&qk_empty[s]));
-                        if (++s == QK_STAGES) {
-                            s = 0;
-                            ph ^= 1u;
-                        }
-                    }
-                    if (!ok) break;
-                    umma_commit(smem_u32(&s_full[sb]));
+            if constexpr (QMODE > 0) {
+                ok = mbar_wait(smem_u32(&q_full), 0, &abort_flag);
+                tc_fence_after();
+            }
+            for (int t = 0; t < n_kv && ok; ++t) {
+                // S_t into S buffer t % 2, once the softmax has read S_(t-2) from it
+                const int sb = t & 1;
+                if (!mbar_wait(smem_u32(&s_empty[sb]), ((t >> 1) & 1) ^ 1u, &abort_flag,
+                               long_limit)) {
+                    ok = false;
+                    break;
                 }
-                if (t >= 1) {
-                    // O += P_u V_u for the previous block u
-                    const int u = t - 1;
-                    const int pb = u & 1;
-                    if (!mbar_wait(smem_u32(&p_full[pb]), (u >> 1) & 1, &abort_flag, long_limit) ||
-                        !mbar_wait(smem_u32(&v_full[vs]), vph, &abort_flag, long_limit)) {
+                tc_fence_after();
+                const uint32_t d_s = tmem_base + static_cast<uint32_t>(sb * BN);
+                for (int c = 0; c < n_chunks; ++c) {
+                    if (!mbar_wait(smem_u32(&qk_full[s]), ph, &abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    // P: K-major, two 64-key atoms 16 KB apart.  V: MN-major,
-                    // 64-column boxes 16 KB apart, 16 keys = 2048 B per step.
-                    const uint64_t ad = sdesc_sw128(p_base + pb * P_BUF, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(v_base + vs * Cfg::V_STAGE, V_BOX, 1024);
+                    const uint32_t sa = qk_base + s * QK_STAGE;
+                    const uint32_t qa = QMODE > 0 ? q_res + c * Q_CHUNK : sa;
+                    const uint32_t ka = QMODE > 0 ? sa : sa + Q_CHUNK;
+                    // both operands K-major: 8-row groups 1024 B apart, +32 B per 16 of d
+                    const uint64_t ad = sdesc_sw128(qa, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(ka, 16, 1024);
 #pragma unroll
-                    for (int k = 0; k < BN / 16; ++k)
-                        umma_f16(tmem_base + O_COL, ad + ((k / 4) * (P_ATOM >> 4) + (k % 4) * 2),
-                                 bd + 128ull * k, idesc_o, (u | k) != 0 ? 1u : 0u);
-                    umma_commit(smem_u32(&v_empty[vs]));
-                    umma_commit(smem_u32(&p_empty[pb]));
-                    if (++vs == VS) {
-                        vs = 0;
-                        vph ^= 1u;
+                    for (int k = 0; k < DC / 16; ++k)
+                        umma_f16(d_s, ad + 2ull * k, bd + 2ull * k, idesc_s, (c | k) != 0 ? 1u : 0u);
+                    umma_commit(smem_u32(&qk_empty[s]));
+                    if (++s == QK_STAGES) {
+                        s = 0;
+                        ph ^= 1u;
                     }
+                }
+                if (!ok) break;
+                umma_commit(smem_u32(&s_full[sb]));
+            }
+            if (!ok) {
+                abort_flag = 1;
+                atomicOr(err, ERR_ATTENTION);
+            }
+            // every MMA this thread issued must finish before TMEM is freed
+            umma_commit(smem_u32(&drain_bar));
+            if (!mbar_wait(smem_u32(&drain_bar), 0, nullptr)) atomicOr(err, ERR_DRAIN);
+        }
+        __syncwarp();
+    } else if (warp == 3) {
+        // ------------------------------------------ MMA issuer: O += P V
+        if (lane == 0) {
+            constexpr uint32_t idesc_o = idesc_f16_f32(BM, DVS, false, true);
+            int vs = 0;
+            uint32_t vph = 0;
+            bool ok = true;
+            for (int u = 0; u < n_kv; ++u) {
+                if (!mbar_wait(smem_u32(&p_full), u & 1, &abort_flag, long_limit) ||
+                    !mbar_wait(smem_u32(&v_full[vs]), vph, &abort_flag, long_limit)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // P: K-major, two 64-key atoms 16 KB apart.  V: MN-major,
+                // 64-column boxes 16 KB apart, 16 keys = 2048 B per step.
+                const uint64_t ad = sdesc_sw128(p_base, 16, 1024);
+                const uint64_t bd = sdesc_sw128(v_base + vs * Cfg::V_STAGE, V_BOX, 1024);
+#pragma unroll
+                for (int k = 0; k < BN / 16; ++k)
+                    umma_f16(tmem_base + O_COL, ad + ((k / 4) * (P_ATOM >> 4) + (k % 4) * 2),
+                             bd + 128ull * k, idesc_o, (u | k) != 0 ? 1u : 0u);
+                umma_commit(smem_u32(&v_empty[vs]));
+                umma_commit(smem_u32(&p_empty));
+                if (++vs == VS) {
+                    vs = 0;
+                    vph ^= 1u;
                 }
             }
             if (!ok) {
                 abort_flag = 1;
                 atomicOr(err, ERR_ATTENTION);
             }
-            // every MMA issued must finish before TMEM is freed
-            umma_commit(smem_u32(&drain_bar));
-            if (!mbar_wait(smem_u32(&drain_bar), 0, nullptr)) atomicOr(err, ERR_DRAIN);
+            umma_commit(smem_u32(&drain_bar2));
+            if (!mbar_wait(smem_u32(&drain_bar2), 0, nullptr)) atomicOr(err, ERR_DRAIN);
         }
         __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------- softmax and output
+        // Two warps per TMEM lane quadrant: warp h of the pair takes keys
+        // h*64 .. h*64+63 of each block and output columns h*DVS/2 ..; the
+        // pair agrees on each row's maximum (and, at the end, its sum)
+        // through shared memory and a 64-thread named barrier.
         const int q = warp & 3;
+        const int h = (warp - 4) >> 2;
         const int r = q * 32 + lane;  // this thread's query row in the tile
         const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        constexpr int HK = BN / 2;    // keys per warp
+        constexpr int HO = DVS / 2;   // output columns per warp
         float m_run = -INFINITY;      // running maximum, base-2 scaled logits
-        float l_run = 0.0f;           // running normaliser
+        float l_run = 0.0f;           // this half's share of the running normaliser
         bool ok = true;
-        for (int t = 0; t < n_kv && ok; ++t) {
+        // Every iteration passes exactly one pair barrier, also after a
+        // failed wait (the work is then skipped), so the two warps of a pair
+        // always meet; a failure raises the abort flag at once so that every
+        // other role's bounded waits end too.
+        auto fail = [&]() {
+            ok = false;
+            if (lane == 0) {
+                abort_flag = 1;
+                atomicOr(err, ERR_ATTENTION);
+            }
+        };
+        for (int t = 0; t < n_kv; ++t) {
             const int sb = t & 1;
-            const bool got = mbar_wait(smem_u32(&s_full[sb]), (t >> 1) & 1, &abort_flag, long_limit);
-            if (!__all_sync(0xffffffffu, got)) {
-                ok = false;
-                break;
+            uint32_t raw[HK];
+            float mine = 0.0f;
+            const int valid = min(BN, Nk - t * BN) - h * HK;
+            const bool pos_scale = scale_log2 >= 0.0f;
+            if (ok) {
+                const bool got =
+                    mbar_wait(smem_u32(&s_full[sb]), (t >> 1) & 1, &abort_flag, long_limit);
+                if (!__all_sync(0xffffffffu, got)) fail();
             }
-            tc_fence_after();
-            // S_t row r: four 32-column loads in flight, one wait
-            uint32_t raw[BN];
+            if (ok) {
+                tc_fence_after();
+                // this half of S_t row r: two 32-column loads in flight, one wait
 #pragma unroll
-            for (int i = 0; i < BN / 32; ++i)
-                tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(sb * BN + 32 * i),
-                                   *reinterpret_cast<uint32_t(*)[32]>(raw + 32 * i));
-            tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(smem_u32(&s_empty[sb]));
+                for (int i = 0; i < HK / 32; ++i)
+                    tmem_ld_32x32b_x32(t_lane + static_cast<uint32_t>(sb * BN + h * HK + 32 * i),
+                                       *reinterpret_cast<uint32_t(*)[32]>(raw + 32 * i));
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(smem_u32(&s_empty[sb]));
+                // keys past Nk (zero-filled by TMA) are masked; only the last
+                // block can have them
+                if (valid < HK) {
+#pragma unroll
+                    for (int j = 0; j < HK; ++j)
+                        if (j >= valid) raw[j] = __float_as_uint(pos_scale ? -INFINITY : INFINITY);
+                }
+                // the extreme raw score of this half, in four chains
+                float mc[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) mc[c] = __uint_as_float(raw[c]);
+                if (pos_scale) {
+#pragma unroll
+                    for (int j = 4; j < HK; ++j) mc[j & 3] = fmaxf(mc[j & 3], __uint_as_float(raw[j]));
+                } else {
+#pragma unroll
+                    for (int j = 4; j < HK; ++j) mc[j & 3] = fminf(mc[j & 3], __uint_as_float(raw[j]));
+                }
+                mine = pos_scale ? fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]))
+                                 : fminf(fminf(mc[0], mc[1]), fminf(mc[2], mc[3]));
+            }
+            red[sb][h][r] = mine;
+            named_bar_sync(1 + q, 64);
+            const float other = red[sb][h ^ 1][r];
+            if (!ok) continue;
 
-            // block maximum of the base-2 logits; keys past Nk (zero-filled by
-            // TMA) are masked, which only the last block can need
-            const int valid = min(BN, Nk - t * BN);
-            if (valid < BN) {
-#pragma unroll
-                for (int j = 0; j < BN; ++j)
-                    if (j >= valid) raw[j] = __float_as_uint(scale_log2 >= 0.0f ? -INFINITY : INFINITY);
-            }
-            // (four independent chains keep the reduction short)
-            float mc[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) mc[c] = __uint_as_float(raw[c]);
-            if (scale_log2 >= 0.0f) {
-#pragma unroll
-                for (int j = 4; j < BN; ++j) mc[j & 3] = fmaxf(mc[j & 3], __uint_as_float(raw[j]));
-            } else {
-#pragma unroll
-                for (int j = 4; j < BN; ++j) mc[j & 3] = fminf(mc[j & 3], __uint_as_float(raw[j]));
-            }
-            const float mraw = scale_log2 >= 0.0f ? fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]))
-                                                  : fminf(fminf(mc[0], mc[1]), fminf(mc[2], mc[3]));
+            const float mraw = pos_scale ? fmaxf(mine, other) : fminf(mine, other);
             const float mx = mraw * scale_log2;
             const bool raise = mx > m_run + kRescaleLog2;
             float alpha = 1.0f;
@@ -347,97 +427,98 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             }
             const float neg_m = -m_run;
 
-            // the P buffer must be free: the MMAs of block t - 2 have read it
-            const bool got_p = mbar_wait(smem_u32(&p_empty[sb]), ((t >> 1) & 1) ^ 1u, &abort_flag,
-                                         long_limit);
-            if (!__all_sync(0xffffffffu, got_p)) {
-                ok = false;
-                break;
-            }
-            if (t > 0 && __any_sync(0xffffffffu, raise)) {
-                // O *= alpha, after the MMAs of block t - 1 have finished
-                const int u = t - 1;
-                const bool got_o = mbar_wait(smem_u32(&p_empty[u & 1]), (u >> 1) & 1, &abort_flag,
-                                             long_limit);
-                if (!__all_sync(0xffffffffu, got_o)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-#pragma unroll 1
-                for (int c = 0; c < DVS; c += 32) {
-                    uint32_t o[32];
-                    tmem_ld_32x32b_x32(t_lane + O_COL + static_cast<uint32_t>(c), o);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-                    tmem_st_32x32b_x32(t_lane + O_COL + static_cast<uint32_t>(c), o);
-                }
-                tmem_st_wait();
-            }
-
-            // P = 2^(s * scale * log2 e - m) in fp16, row r of the swizzled
-            // K-major tile; the row sum in two chains.  Masked keys (the last
-            // block only) get probability 0 whatever the scale.
-            const uint32_t prow = p_base + sb * P_BUF + static_cast<uint32_t>(r) * 128u;
+            // P = 2^(s * scale * log2 e - m) in fp16 (packed pairs, in
+            // registers while the previous block's P V may still run)
+            uint32_t pw[HK / 2];
             float l0 = 0.0f, l1 = 0.0f;
-            auto write_p = [&](auto masked) {
+            auto make_p = [&](auto masked) {
 #pragma unroll
-                for (int ch = 0; ch < BN / 8; ++ch) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const int j = 8 * ch + 2 * h;
-                        float a0 = fmaf(__uint_as_float(raw[j]), scale_log2, neg_m);
-                        float a1 = fmaf(__uint_as_float(raw[j + 1]), scale_log2, neg_m);
-                        if constexpr (decltype(masked)::value) {
-                            if (j >= valid) a0 = -INFINITY;
-                            if (j + 1 >= valid) a1 = -INFINITY;
-                        }
-                        const float p0 = ex2_approx(a0);
-                        const float p1 = ex2_approx(a1);
-                        l0 += p0;
-                        l1 += p1;
-                        __half2 v2 = __floats2half2_rn(p0, p1);
-                        w[h] = *reinterpret_cast<uint32_t*>(&v2);
+                for (int j = 0; j < HK; j += 2) {
+                    float a0 = fmaf(__uint_as_float(raw[j]), scale_log2, neg_m);
+                    float a1 = fmaf(__uint_as_float(raw[j + 1]), scale_log2, neg_m);
+                    if constexpr (decltype(masked)::value) {
+                        if (j >= valid) a0 = -INFINITY;
+                        if (j + 1 >= valid) a1 = -INFINITY;
                     }
-                    const uint32_t atom = static_cast<uint32_t>(ch >> 3);
-                    const uint32_t pos = static_cast<uint32_t>((ch & 7) ^ (r & 7));
-                    st_shared_v4(prow + atom * P_ATOM + pos * 16u, w[0], w[1], w[2], w[3]);
+                    const float p0 = ex2_approx(a0);
+                    const float p1 = ex2_approx(a1);
+                    l0 += p0;
+                    l1 += p1;
+                    __half2 v2 = __floats2half2_rn(p0, p1);
+                    pw[j / 2] = *reinterpret_cast<uint32_t*>(&v2);
                 }
             };
-            if (valid < BN) write_p(std::true_type{});
-            else write_p(std::false_type{});
+            if (valid < HK) make_p(std::true_type{});
+            else make_p(std::false_type{});
             l_run += l0 + l1;
+
+            if (t > 0) {
+                // the P buffer and O are free once the MMAs of block t - 1 are done
+                const int u = t - 1;
+                const bool got_o = mbar_wait(smem_u32(&p_empty), u & 1, &abort_flag, long_limit);
+                if (!__all_sync(0xffffffffu, got_o)) {
+                    fail();
+                    continue;
+                }
+                if (__any_sync(0xffffffffu, raise)) {
+                    // this warp's half of O *= alpha (1 in rows that kept their maximum)
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < HO; c += 32) {
+                        const uint32_t col = O_COL + static_cast<uint32_t>(h * HO + c);
+                        uint32_t o[32];
+                        tmem_ld_32x32b_x32(t_lane + col, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                        tmem_st_32x32b_x32(t_lane + col, o);
+                    }
+                    tmem_st_wait();
+                }
+            }
+
+            // row r of this half's 64-key atom of the swizzled K-major P tile:
+            // 16-byte chunk ch of the row sits at chunk ch ^ (r % 8)
+            const uint32_t prow = p_base + static_cast<uint32_t>(h) * P_ATOM +
+                                  static_cast<uint32_t>(r) * 128u;
+#pragma unroll
+            for (int ch = 0; ch < HK / 8; ++ch) {
+                const uint32_t pos = static_cast<uint32_t>(ch ^ (r & 7));
+                st_shared_v4(prow + pos * 16u, pw[4 * ch], pw[4 * ch + 1], pw[4 * ch + 2],
+                             pw[4 * ch + 3]);
+            }
             fence_proxy_async_smem();  // generic-proxy P writes -> visible to the tensor core
             tc_fence_before();
-            mbar_arrive(smem_u32(&p_full[sb]));
+            mbar_arrive(smem_u32(&p_full));
         }
         if (ok) {
-            // the last block's MMAs complete O; normalise and store
+            // the last block's MMAs complete O
             const int u = n_kv - 1;
-            const bool got = mbar_wait(smem_u32(&p_empty[u & 1]), (u >> 1) & 1, &abort_flag,
-                                       long_limit);
-            ok = __all_sync(0xffffffffu, got);
+            const bool got = mbar_wait(smem_u32(&p_empty), u & 1, &abort_flag, long_limit);
+            if (!__all_sync(0xffffffffu, got)) fail();
         }
+        // both halves of the row's normaliser (every softmax thread reaches
+        // this barrier exactly once)
+        lsum[h][r] = l_run;
+        named_bar_sync(1 + q, 64);
+        const float l_row = lsum[0][r] + lsum[1][r];
         if (ok) {
             tc_fence_after();
-            const float inv_l = 1.0f / l_run;
+            const float inv_l = 1.0f / l_row;
             const int m = q0 + r;
             void* Ob = batch_ptr(O, bz, sO, OUT_F32 ? 4 : 2);
 #pragma unroll 1
-            for (int c = 0; c < DVS; c += 32) {
+            for (int c = 0; c < HO; c += 32) {
+                const int cc = h * HO + c;
                 uint32_t o[32];
-                tmem_ld_32x32b_x32(t_lane + O_COL + static_cast<uint32_t>(c), o);
+                tmem_ld_32x32b_x32(t_lane + O_COL + static_cast<uint32_t>(cc), o);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * inv_l);
-                const int n = dv0 + c;
+                const int n = dv0 + cc;
                 if (m < Nq && n < dv) store_chunk<OUT_F32>(Ob, ldo, m, n, dv, o, o_vec != 0);
             }
-        } else if (lane == 0) {
-            abort_flag = 1;
-            atomicOr(err, ERR_ATTENTION);
         }
     }
 
@@ -450,18 +531,18 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 }
 
 std::mutex g_attr_mu;
-bool g_attr_set[64][4];
+bool g_attr_set[64][12];
 
-template <int DVS, bool OUT_F32>
+template <int DVS, bool OUT_F32, int QMODE>
 cudaError_t launch_cfg(const AttnArgs& a)
 {
-    using Cfg = AttnCfg<DVS>;
-    auto kernel = attention_fwd_kernel<DVS, OUT_F32>;
+    using Cfg = AttnCfg<DVS, QMODE>;
+    auto kernel = attention_fwd_kernel<DVS, OUT_F32, QMODE>;
     {
         int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
-        const int slot = (DVS == 256 ? 2 : 0) + (OUT_F32 ? 1 : 0);
+        const int slot = ((DVS == 256 ? 2 : 0) + (OUT_F32 ? 1 : 0)) * 3 + QMODE / 2;
         std::lock_guard<std::mutex> lock(g_attr_mu);
         if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
         if (!g_attr_set[dev][slot]) {
@@ -494,12 +575,20 @@ cudaError_t launch_cfg(const AttnArgs& a)
     return cudaGetLastError();
 }
 
+template <int DVS, bool OUT_F32>
+cudaError_t launch_q(const AttnArgs& a)
+{
+    if (a.d <= 128) return launch_cfg<DVS, OUT_F32, 2>(a);
+    if (a.d <= 256) return launch_cfg<DVS, OUT_F32, 4>(a);
+    return launch_cfg<DVS, OUT_F32, 0>(a);
+}
+
 }  // namespace
 
 cudaError_t launch_attention(const AttnArgs& a)
 {
-    if (a.dv <= 128) return a.out_f32 ? launch_cfg<128, true>(a) : launch_cfg<128, false>(a);
-    return a.out_f32 ? launch_cfg<256, true>(a) : launch_cfg<256, false>(a);
+    if (a.dv <= 128) return a.out_f32 ? launch_q<128, true>(a) : launch_q<128, false>(a);
+    return a.out_f32 ? launch_q<256, true>(a) : launch_q<256, false>(a);
 }
 
 }  // namespace tg
