@@ -71,19 +71,25 @@ template <int DVS, int QMODE>
 struct AttnCfg {
     static_assert(DVS == 128 || DVS == 256, "an output slice is 128 or 256 columns");
     static_assert(QMODE == 0 || QMODE == 2 || QMODE == 4, "resident Q of 0, 2 or 4 chunks");
-#ifdef TG_ATTN_V_STAGES
-    static constexpr int V_STAGES = DVS == 128 ? (QMODE == 2 ? TG_ATTN_V_STAGES : 2) : 1;
-#else
-    static constexpr int V_STAGES = DVS == 128 ? 2 : 1;
-#endif
     static constexpr uint32_t V_STAGE = BN * DVS * 2;
     static constexpr uint32_t Q_RES = QMODE * Q_CHUNK;
     static constexpr uint32_t STAGE = QMODE ? K_CHUNK : Q_CHUNK + K_CHUNK;
-    static constexpr uint32_t FIXED = Q_RES + V_STAGES * V_STAGE + P_BUF + 1024;
     // 227 KB per CTA covers static shared memory too: keep 4 KB for it
     static constexpr uint32_t BUDGET = 227 * 1024 - 4096;
-    static constexpr int STAGES = static_cast<int>((BUDGET - FIXED) / STAGE);
-    static constexpr uint32_t SMEM = FIXED + STAGES * STAGE;
+    static constexpr int ring(int vs, int pb)
+    {
+        return static_cast<int>((BUDGET - (Q_RES + vs * V_STAGE + pb * P_BUF + 1024)) / STAGE);
+    }
+    // Two P buffers let the softmax write P_(t+1) while P_t V_t still runs;
+    // they are used whenever the ring keeps at least three stages (with two V
+    // stages for 128-column slices if possible, else one).
+    static constexpr int V_DEFAULT = DVS == 128 ? 2 : 1;
+    static constexpr bool TWO_P = ring(V_DEFAULT, 2) >= 3 || ring(1, 2) >= 3;
+    static constexpr int P_BUFS = TWO_P ? 2 : 1;
+    static constexpr int V_STAGES = ring(V_DEFAULT, P_BUFS) >= 3 ? V_DEFAULT : 1;
+    static constexpr int STAGES = ring(V_STAGES, P_BUFS);
+    static constexpr uint32_t SMEM = Q_RES + V_STAGES * V_STAGE + P_BUFS * P_BUF + 1024 +
+                                     STAGES * STAGE;
     static_assert(STAGES >= 3, "too few pipeline stages");
     static_assert(SMEM <= BUDGET, "shared-memory budget exceeded");
 };
@@ -107,8 +113,9 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     __shared__ __align__(8) uint64_t v_empty[VS];
     __shared__ __align__(8) uint64_t s_full[2];
     __shared__ __align__(8) uint64_t s_empty[2];
-    __shared__ __align__(8) uint64_t p_full;              // one P buffer
-    __shared__ __align__(8) uint64_t p_empty;
+    constexpr int PB = Cfg::P_BUFS;
+    __shared__ __align__(8) uint64_t p_full[PB];
+    __shared__ __align__(8) uint64_t p_empty[PB];
     __shared__ __align__(8) uint64_t drain_bar;
     __shared__ __align__(8) uint64_t drain_bar2;
     __shared__ uint32_t tmem_slot;
@@ -142,8 +149,10 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             mbar_init(smem_u32(&s_empty[b]), kSoftmaxThreads);
         }
         mbar_init(smem_u32(&q_full), 1);
-        mbar_init(smem_u32(&p_full), kSoftmaxThreads);
-        mbar_init(smem_u32(&p_empty), 1);
+        for (int b = 0; b < PB; ++b) {
+            mbar_init(smem_u32(&p_full[b]), kSoftmaxThreads);
+            mbar_init(smem_u32(&p_empty[b]), 1);
+        }
         mbar_init(smem_u32(&drain_bar), 1);
         mbar_init(smem_u32(&drain_bar2), 1);
         abort_flag = 0;
@@ -314,7 +323,9 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             uint32_t vph = 0;
             bool ok = true;
             for (int u = 0; u < n_kv; ++u) {
-                if (!mbar_wait(smem_u32(&p_full), u & 1, &abort_flag, long_limit) ||
+                const int pb = u % PB;
+                const uint32_t pph = static_cast<uint32_t>((u / PB) & 1);
+                if (!mbar_wait(smem_u32(&p_full[pb]), pph, &abort_flag, long_limit) ||
                     !mbar_wait(smem_u32(&v_full[vs]), vph, &abort_flag, long_limit)) {
                     ok = false;
                     break;
@@ -322,14 +333,14 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 tc_fence_after();
                 // P: K-major, two 64-key atoms 16 KB apart.  V: MN-major,
                 // 64-column boxes 16 KB apart, 16 keys = 2048 B per step.
-                const uint64_t ad = sdesc_sw128(p_base, 16, 1024);
+                const uint64_t ad = sdesc_sw128(p_base + pb * P_BUF, 16, 1024);
                 const uint64_t bd = sdesc_sw128(v_base + vs * Cfg::V_STAGE, V_BOX, 1024);
 #pragma unroll
                 for (int k = 0; k < BN / 16; ++k)
                     umma_f16(tmem_base + O_COL, ad + ((k / 4) * (P_ATOM >> 4) + (k % 4) * 2),
                              bd + 128ull * k, idesc_o, (u | k) != 0 ? 1u : 0u);
                 umma_commit(smem_u32(&v_empty[vs]));
-                umma_commit(smem_u32(&p_empty));
+                umma_commit(smem_u32(&p_empty[pb]));
                 if (++vs == VS) {
                     vs = 0;
                     vph ^= 1u;
@@ -452,36 +463,48 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             else make_p(std::false_type{});
             l_run += l0 + l1;
 
-            if (t > 0) {
-                // the P buffer and O are free once the MMAs of block t - 1 are done
-                const int u = t - 1;
-                const bool got_o = mbar_wait(smem_u32(&p_empty), u & 1, &abort_flag, long_limit);
-                if (!__all_sync(0xffffffffu, got_o)) {
+            // P buffer t % PB is free once the MMAs of block t - PB are done
+            // (with one buffer that is block t - 1, which also frees O)
+            if (t >= PB) {
+                const int u = t - PB;
+                const bool got_p = mbar_wait(smem_u32(&p_empty[u % PB]), (u / PB) & 1, &abort_flag,
+                                             long_limit);
+                if (!__all_sync(0xffffffffu, got_p)) {
                     fail();
                     continue;
                 }
-                if (__any_sync(0xffffffffu, raise)) {
-                    // this warp's half of O *= alpha (1 in rows that kept their maximum)
-                    tc_fence_after();
-#pragma unroll 1
-                    for (int c = 0; c < HO; c += 32) {
-                        const uint32_t col = O_COL + static_cast<uint32_t>(h * HO + c);
-                        uint32_t o[32];
-                        tmem_ld_32x32b_x32(t_lane + col, o);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-                        tmem_st_32x32b_x32(t_lane + col, o);
+            }
+            if (t > 0 && __any_sync(0xffffffffu, raise)) {
+                // O *= alpha (1 in rows that kept their maximum) once the MMAs
+                // of block t - 1 are done; with two P buffers that is one more
+                // wait, on the buffer of block t - 1
+                if (PB == 2) {
+                    const int u = t - 1;
+                    const bool got_o = mbar_wait(smem_u32(&p_empty[u % PB]), (u / PB) & 1,
+                                                 &abort_flag, long_limit);
+                    if (!__all_sync(0xffffffffu, got_o)) {
+                        fail();
+                        continue;
                     }
-                    tmem_st_wait();
                 }
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < HO; c += 32) {
+                    const uint32_t col = O_COL + static_cast<uint32_t>(h * HO + c);
+                    uint32_t o[32];
+                    tmem_ld_32x32b_x32(t_lane + col, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                    tmem_st_32x32b_x32(t_lane + col, o);
+                }
+                tmem_st_wait();
             }
 
             // row r of this half's 64-key atom of the swizzled K-major P tile:
             // 16-byte chunk ch of the row sits at chunk ch ^ (r % 8)
-            const uint32_t prow = p_base + static_cast<uint32_t>(h) * P_ATOM +
-                                  static_cast<uint32_t>(r) * 128u;
+            const uint32_t prow = p_base + static_cast<uint32_t>(t % PB) * P_BUF +
+                                  static_cast<uint32_t>(h) * P_ATOM + static_cast<uint32_t>(r) * 128u;
 #pragma unroll
             for (int ch = 0; ch < HK / 8; ++ch) {
                 const uint32_t pos = static_cast<uint32_t>(ch ^ (r & 7));
@@ -490,12 +513,13 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             }
             fence_proxy_async_smem();  // generic-proxy P writes -> visible to the tensor core
             tc_fence_before();
-            mbar_arrive(smem_u32(&p_full));
+            mbar_arrive(smem_u32(&p_full[t % PB]));
         }
         if (ok) {
             // the last block's MMAs complete O
             const int u = n_kv - 1;
-            const bool got = mbar_wait(smem_u32(&p_empty), u & 1, &abort_flag, long_limit);
+            const bool got = mbar_wait(smem_u32(&p_empty[u % PB]), (u / PB) & 1, &abort_flag,
+                                       long_limit);
             if (!__all_sync(0xffffffffu, got)) fail();
         }
         // both halves of the row's normaliser (every softmax thread reaches
