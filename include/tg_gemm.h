@@ -20,6 +20,7 @@
 #ifndef TG_GEMM_H
 #define TG_GEMM_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -249,6 +250,41 @@ tg_status tg_attention(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t
                        void* O, int64_t ldo, int64_t strideO,
                        float scale, tg_dtype in_dtype, tg_dtype out_dtype,
                        tg_stream_t stream);
+
+/*
+ * tg_attention_ws -- tg_attention with a caller-provided workspace.
+ *
+ * When the work of a call covers fewer CTAs than the GPU has SMs (few heads,
+ * short sequences, or the page's single 1024 x 768 head), the keys are split
+ * into ranges handled by separate CTAs, each writing an unnormalised partial
+ * output with its running maximum and normaliser to `workspace`; a second
+ * kernel merges them (the same merge of maxima and normalisers the blockwise
+ * pass applies between key blocks).  tg_attention_workspace_size reports the
+ * bytes this needs on the current device (0 when the call is large enough
+ * not to split).  A NULL or smaller workspace runs the single pass: the
+ * result is the same up to rounding order.
+ *
+ * Arguments: those of tg_attention, plus
+ *   workspace        device memory, 256-byte aligned, owned by the caller,
+ *                    not overlapping Q, K, V or O; its contents on entry do
+ *                    not matter and are undefined afterwards.
+ *   workspace_bytes  its size.
+ * Calls that share a workspace must not overlap in time (use one stream, or
+ * one workspace per stream).  Errors: those of tg_attention, plus
+ * TG_ERR_INVALID_ARG for a misaligned or overlapping workspace.
+ */
+tg_status tg_attention_ws(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                          const void* Q, int64_t ldq, int64_t strideQ,
+                          const void* K, int64_t ldk, int64_t strideK,
+                          const void* V, int64_t ldv, int64_t strideV,
+                          void* O, int64_t ldo, int64_t strideO,
+                          float scale, tg_dtype in_dtype, tg_dtype out_dtype,
+                          void* workspace, size_t workspace_bytes,
+                          tg_stream_t stream);
+
+/* Workspace bytes tg_attention_ws uses for these sizes on the current device
+ * (0: no split, or invalid sizes, or no device). */
+size_t tg_attention_workspace_size(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv);
 
 /*
  * tg_gemm_check -- synchronize `stream`, then read and clear the current

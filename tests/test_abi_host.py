@@ -376,3 +376,13 @@ def test_attention_degenerate_sizes_are_noops():
     assert acall(batch=0, Q=0, K=0, V=0, O=0) == tg.TG_OK
     assert acall(Nq=0, Q=0, K=0, V=0, O=0) == tg.TG_OK
     assert acall(dv=0, Q=0, K=0, V=0, O=0) == tg.TG_OK
+
+
+def test_attention_workspace_checks_on_host():
+    # a workspace that is not 256-byte aligned is rejected before any CUDA call
+    st = tg.tg_attention_ws(1, 128, 128, 64, 64, PQ, 64, 0, PK, 64, 0, PV, 64, 0, PO, 64, 0, 1.0,
+                            tg.F16, tg.F16, 0x7F9000000010, 1 << 20, 0)
+    assert st == tg.TG_ERR_INVALID_ARG
+    # sizes with no work, or invalid ones, need no workspace
+    assert tg.tg_attention_workspace_size(0, 128, 128, 64, 64) == 0
+    assert tg.tg_attention_workspace_size(1, 128, -1, 64, 64) == 0

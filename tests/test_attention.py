@@ -210,3 +210,32 @@ def test_attention_binding_sampled_large():
         tol = oracle.attention_tolerance(O, E, G, d, N, True)
         got = o[b].double().cpu().numpy()[rows]
         assert np.all(np.abs(got - O) <= tol), f"head {b}"
+
+
+@pytest.mark.parametrize("B,Nq,Nk,d,dv,scale", [
+    (1, 1024, 1024, 768, 768, 1.0),        # the page's configuration: 24 CTAs without a split
+    (1, 200, 1000, 64, 64, 0.125),         # ragged last key block inside the last split
+    (2, 130, 2000, 128, 96, 0.09),
+    (1, 1, 640, 64, 200, 0.2),
+])
+@pytest.mark.parametrize("out", [torch.float16, torch.float32])
+def test_attention_split_keys(B, Nq, Nk, d, dv, scale, out):
+    """Few CTAs: the keys are split over more CTAs through the workspace and
+    merged by the combine kernel; the result matches the oracle and the
+    single-pass result."""
+    ws_bytes = tg.tg_attention_workspace_size(B, Nq, Nk, d, dv)
+    assert ws_bytes > 0, "a call this small should split the keys"
+    q, k, v = _qkv(B, Nq, Nk, d, dv, 13700 + Nk + d)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    o_split = tg.attention(qd, kd, vd, scale, out_dtype=out, workspace=ws)
+    o_plain = tg.attention(qd, kd, vd, scale, out_dtype=out)
+    tg.check()
+    got = o_split.double().cpu().numpy()
+    _check(q, k, v, scale, got, out, f"split {B}x{Nq}x{Nk} d{d} dv{dv}")
+    # both ways within the bound of each other's reference, and close
+    assert np.allclose(got, o_plain.double().cpu().numpy(), rtol=2e-2, atol=2e-3)
+
+
+def test_attention_large_call_needs_no_workspace():
+    assert tg.tg_attention_workspace_size(16, 4096, 4096, 128, 128) == 0

@@ -20,7 +20,7 @@ __all__ = [
     "TG_ERR_TIMEOUT", "PATHS", "TgError", "lib", "library_path", "tg_gemm", "tg_gemm_check",
     "tg_status_string", "tg_gemm_path", "tg_gemm_force_path", "tg_gemm_force_tiling",
     "tg_gemm_test_hook", "tg_gemm_ex", "tg_gemm_batched", "tg_gemm_batched_path",
-    "tg_attention", "attention", "ACT_NONE", "ACT_RELU", "ACT_GELU",
+    "tg_attention", "tg_attention_ws", "tg_attention_workspace_size", "attention", "ACT_NONE", "ACT_RELU", "ACT_GELU",
     "tg_gemm_version", "gemm", "bmm",
     "check",
 ]
@@ -81,6 +81,12 @@ def lib() -> ctypes.CDLL:
         L.tg_attention.restype = i32
         L.tg_attention.argtypes = [i64, i64, i64, i64, i64, vp, i64, i64, vp, i64, i64, vp, i64,
                                    i64, vp, i64, i64, ctypes.c_float, i32, i32, vp]
+        L.tg_attention_ws.restype = i32
+        L.tg_attention_ws.argtypes = [i64, i64, i64, i64, i64, vp, i64, i64, vp, i64, i64, vp,
+                                      i64, i64, vp, i64, i64, ctypes.c_float, i32, i32, vp,
+                                      ctypes.c_size_t, vp]
+        L.tg_attention_workspace_size.restype = ctypes.c_size_t
+        L.tg_attention_workspace_size.argtypes = [i64, i64, i64, i64, i64]
         L.tg_gemm_check.restype = i32
         L.tg_gemm_check.argtypes = [vp]
         L.tg_status_string.restype = ctypes.c_char_p
@@ -133,6 +139,17 @@ def tg_attention(batch, Nq, Nk, d, dv, Q, ldq, sQ, K, ldk, sK, V, ldv, sV, O, ld
     """Enqueue O_b = softmax(scale * Q_b K_b^T) V_b for b < batch."""
     return int(lib().tg_attention(batch, Nq, Nk, d, dv, Q, ldq, sQ, K, ldk, sK, V, ldv, sV, O,
                                   ldo, sO, float(scale), in_dtype, out_dtype, stream))
+
+
+def tg_attention_ws(batch, Nq, Nk, d, dv, Q, ldq, sQ, K, ldk, sK, V, ldv, sV, O, ldo, sO, scale,
+                    in_dtype, out_dtype, workspace, workspace_bytes, stream=0) -> int:
+    return int(lib().tg_attention_ws(batch, Nq, Nk, d, dv, Q, ldq, sQ, K, ldk, sK, V, ldv, sV, O,
+                                     ldo, sO, float(scale), in_dtype, out_dtype, workspace or None,
+                                     workspace_bytes, stream))
+
+
+def tg_attention_workspace_size(batch, Nq, Nk, d, dv) -> int:
+    return int(lib().tg_attention_workspace_size(batch, Nq, Nk, d, dv))
 
 
 def tg_gemm_check(stream=0) -> int:
@@ -263,11 +280,12 @@ def bmm(a, b, out=None, out_dtype=None, stream=None):
     return out
 
 
-def attention(q, k, v, scale=1.0, out=None, out_dtype=None, stream=None):
+def attention(q, k, v, scale=1.0, out=None, out_dtype=None, stream=None, workspace=None):
     """softmax(scale * Q K^T) V for 2-D (Nq x d, Nk x d, Nk x dv) or 3-D
     (batch first) fp16 CUDA tensors with contiguous rows; a batch stride of 0,
     as from expand(), shares one matrix.  Allocates O with torch unless `out`
-    is given."""
+    is given.  `workspace` (a CUDA tensor of tg_attention_workspace_size
+    bytes) lets small calls split the keys over more CTAs."""
     import torch
     squeeze = q.dim() == 2
     if squeeze:
@@ -292,9 +310,12 @@ def attention(q, k, v, scale=1.0, out=None, out_dtype=None, stream=None):
         return ld, (int(t.stride(0)) if t.size(0) > 1 else 0)
 
     (ldq, sq), (ldk, sk), (ldv, sv), (ldo, so) = ld3(q), ld3(k), ld3(v), ld3(out)
-    st = tg_attention(batch, Nq, Nk, d, dv, q.data_ptr(), ldq, sq, k.data_ptr(), ldk, sk,
-                      v.data_ptr(), ldv, sv, out.data_ptr(), ldo, so, scale, _code(q.dtype),
-                      _code(out.dtype), _stream_handle(stream))
+    ws_ptr, ws_bytes = 0, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    st = tg_attention_ws(batch, Nq, Nk, d, dv, q.data_ptr(), ldq, sq, k.data_ptr(), ldk, sk,
+                         v.data_ptr(), ldv, sv, out.data_ptr(), ldo, so, scale, _code(q.dtype),
+                         _code(out.dtype), ws_ptr, ws_bytes, _stream_handle(stream))
     if st != TG_OK:
         raise TgError(st, "tg_attention")
     return out[0] if squeeze else out

@@ -99,7 +99,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, void* O, long long ldo, long long sO,
                      int Nq, int Nk, int dv, int n_chunks, float scale_log2, int o_vec, int zq,
-                     int zk, int zv, int hook, unsigned int* err)
+                     int zk, int zv, int dv_slices, int kv_per_split, float* ws_o, float* ws_ml,
+                     int hook, unsigned int* err)
 {
     using Cfg = AttnCfg<DVS, QMODE>;
     constexpr int VS = Cfg::V_STAGES;
@@ -131,9 +132,14 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int q0 = blockIdx.x * BM;
-    const int dv0 = blockIdx.y * DVS;
+    // grid.y walks the output slices and, for a split over the keys, the
+    // splits: this CTA takes key blocks kv0 .. kv0 + n_kv - 1
+    const int slice = static_cast<int>(blockIdx.y) % dv_slices;
+    const int split = static_cast<int>(blockIdx.y) / dv_slices;
+    const int dv0 = slice * DVS;
     const int bz = static_cast<int>(blockIdx.z);
-    const int n_kv = (Nk + BN - 1) / BN;
+    const int kv0 = split * kv_per_split;
+    const int n_kv = min((Nk + BN - 1) / BN - kv0, kv_per_split);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < QK_STAGES; ++s) {
@@ -202,9 +208,9 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                         mbar_arrive_expect_tx(fb, QK_STAGE);
                         if constexpr (QMODE == 0) {
                             tma_load_3d(sa, &tmQ, fb, c * DC, q0, bz * zq);
-                            tma_load_3d(sa + Q_CHUNK, &tmK, fb, c * DC, t * BN, bz * zk);
+                            tma_load_3d(sa + Q_CHUNK, &tmK, fb, c * DC, (kv0 + t) * BN, bz * zk);
                         } else {
-                            tma_load_3d(sa, &tmK, fb, c * DC, t * BN, bz * zk);
+                            tma_load_3d(sa, &tmK, fb, c * DC, (kv0 + t) * BN, bz * zk);
                         }
                         ++issued;
                     }
@@ -243,7 +249,7 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 mbar_arrive_expect_tx(fb, Cfg::V_STAGE);
 #pragma unroll
                 for (int i = 0; i < DVS / 64; ++i)
-                    tma_load_3d(sv + i * V_BOX, &tmV, fb, dv0 + i * 64, t * BN, bz * zv);
+                    tma_load_3d(sv + i * V_BOX, &tmV, fb, dv0 + i * 64, (kv0 + t) * BN, bz * zv);
                 ++issued;
                 if (++s == VS) {
                     s = 0;
@@ -384,7 +390,7 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             const int sb = t & 1;
             uint32_t raw[HK];
             float mine = 0.0f;
-            const int valid = min(BN, Nk - t * BN) - h * HK;
+            const int valid = min(BN, Nk - (kv0 + t) * BN) - h * HK;
             const bool pos_scale = scale_log2 >= 0.0f;
             if (ok) {
                 const bool got =
@@ -527,7 +533,7 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         lsum[h][r] = l_run;
         named_bar_sync(1 + q, 64);
         const float l_row = lsum[0][r] + lsum[1][r];
-        if (ok) {
+        if (ok && ws_o == nullptr) {
             tc_fence_after();
             const float inv_l = 1.0f / l_row;
             const int m = q0 + r;
@@ -543,6 +549,26 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 const int n = dv0 + cc;
                 if (m < Nq && n < dv) store_chunk<OUT_F32>(Ob, ldo, m, n, dv, o, o_vec != 0);
             }
+        } else if (ok) {
+            // one split of the keys: the unnormalised O, the running maximum
+            // (base 2) and the normaliser go to the workspace for the combine
+            tc_fence_after();
+            const int m = q0 + r;
+            const long long row = (static_cast<long long>(split) * gridDim.z + bz) * Nq + m;
+            const int ldw = (dv + 3) & ~3;  // workspace rows padded to 16 bytes
+#pragma unroll 1
+            for (int c = 0; c < HO; c += 32) {
+                const int cc = h * HO + c;
+                uint32_t o[32];
+                tmem_ld_32x32b_x32(t_lane + O_COL + static_cast<uint32_t>(cc), o);
+                tmem_ld_wait();
+                const int n = dv0 + cc;
+                if (m < Nq && n < dv) store_chunk<true>(ws_o + row * ldw, 0, 0, n, dv, o, true);
+            }
+            if (m < Nq && slice == 0 && h == 0) {
+                ws_ml[2 * row] = m_run;
+                ws_ml[2 * row + 1] = l_row;
+            }
         }
     }
 
@@ -551,6 +577,40 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// The combine step of a split over the keys: per output element,
+// O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s with M = max_s m_s, the
+// same merge of running maxima and normalisers the blockwise pass applies.
+template <bool OUT_F32>
+__global__ void __launch_bounds__(128)
+attention_combine_kernel(const float* ws_o, const float* ws_ml, void* O, long long ldo,
+                         long long sO, int Nq, int dv, int n_split)
+{
+    const int n = blockIdx.x * 128 + static_cast<int>(threadIdx.x);
+    if (n >= dv) return;
+    const int b = static_cast<int>(blockIdx.z);
+    const int batch = static_cast<int>(gridDim.z);
+    const int ldw = (dv + 3) & ~3;
+    void* Ob = batch_ptr(O, b, sO, OUT_F32 ? 4 : 2);
+    for (int m = blockIdx.y; m < Nq; m += gridDim.y) {
+        float M = -INFINITY;
+        for (int sp = 0; sp < n_split; ++sp)
+            M = fmaxf(M, ws_ml[2 * ((static_cast<long long>(sp) * batch + b) * Nq + m)]);
+        float num = 0.0f, den = 0.0f;
+        for (int sp = 0; sp < n_split; ++sp) {
+            const long long row = (static_cast<long long>(sp) * batch + b) * Nq + m;
+            const float w = ex2_approx(ws_ml[2 * row] - M);
+            num = fmaf(w, ws_o[row * ldw + n], num);
+            den = fmaf(w, ws_ml[2 * row + 1], den);
+        }
+        const float y = num / den;
+        const long long i = static_cast<long long>(m) * ldo + n;
+        if constexpr (OUT_F32)
+            static_cast<float*>(Ob)[i] = y;
+        else
+            static_cast<__half*>(Ob)[i] = __float2half_rn(y);
     }
 }
 
@@ -588,14 +648,25 @@ cudaError_t launch_cfg(const AttnArgs& a)
     const int o_vec = (reinterpret_cast<uintptr_t>(a.O) % 16 == 0) &&
                       ((static_cast<size_t>(a.ldo) * es) % 16 == 0) &&
                       ((static_cast<size_t>(a.sO) * es) % 16 == 0);
-    const dim3 grid((a.Nq + BM - 1) / BM, (a.dv + DVS - 1) / DVS, a.batch);
+    const int dv_slices = (a.dv + DVS - 1) / DVS;
+    const int n_kv = (a.Nk + BN - 1) / BN;
+    const int n_split = a.n_split > 1 ? a.n_split : 1;
+    const int kv_per_split = (n_kv + n_split - 1) / n_split;
+    const dim3 grid((a.Nq + BM - 1) / BM, dv_slices * n_split, a.batch);
     if (grid.y > 65535u || grid.z > 65535u) return cudaErrorInvalidConfiguration;
+    float* ws_o = n_split > 1 ? static_cast<float*>(a.ws) : nullptr;
+    float* ws_ml = n_split > 1 ? ws_o + static_cast<long long>(attention_ws_o_floats(a.batch, a.Nq, a.dv, n_split)) : nullptr;
     const float scale_log2 = a.scale * 1.4426950408889634f;  // log2(e)
     const int n_chunks = (a.d + DC - 1) / DC;
     kernel<<<grid, kThreads, Cfg::SMEM, a.stream>>>(tq, tk, tv, a.O, a.ldo, a.sO, a.Nq, a.Nk,
                                                      a.dv, n_chunks, scale_log2, o_vec,
-                                                     a.sQ != 0, a.sK != 0, a.sV != 0, a.hook,
-                                                     a.err);
+                                                     a.sQ != 0, a.sK != 0, a.sV != 0, dv_slices,
+                                                     kv_per_split, ws_o, ws_ml, a.hook, a.err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || n_split == 1) return e;
+    const dim3 cgrid((a.dv + 127) / 128, a.Nq < 65535 ? a.Nq : 65535, a.batch);
+    attention_combine_kernel<OUT_F32><<<cgrid, 128, 0, a.stream>>>(ws_o, ws_ml, a.O, a.ldo, a.sO,
+                                                                   a.Nq, a.dv, n_split);
     return cudaGetLastError();
 }
 
@@ -608,6 +679,35 @@ cudaError_t launch_q(const AttnArgs& a)
 }
 
 }  // namespace
+
+long long attention_ws_o_floats(int batch, int Nq, int dv, int n_split)
+{
+    // the O partials (rows padded to 4 floats), rounded up to 64 floats so
+    // the maxima/normalisers that follow start 256-byte aligned
+    const long long n = static_cast<long long>(n_split) * batch * Nq * ((dv + 3) & ~3);
+    return (n + 63) / 64 * 64;
+}
+
+int attention_splits(int batch, int Nq, int Nk, int dv, int num_sms)
+{
+    const long long base = static_cast<long long>((Nq + BM - 1) / BM) *
+                           ((dv + (dv <= 128 ? 128 : 256) - 1) / (dv <= 128 ? 128 : 256)) * batch;
+    const int n_kv = (Nk + BN - 1) / BN;
+    if (2 * base > num_sms || n_kv < 2) return 1;
+    // as many splits as keep every CTA of the call in one wave
+    int want = static_cast<int>(num_sms / base);
+    if (want > n_kv) want = n_kv;
+    const int per = (n_kv + want - 1) / want;
+    return (n_kv + per - 1) / per;
+}
+
+size_t attention_ws_bytes(int batch, int Nq, int Nk, int dv, int num_sms)
+{
+    const int n_split = attention_splits(batch, Nq, Nk, dv, num_sms);
+    if (n_split <= 1) return 0;
+    return (static_cast<size_t>(attention_ws_o_floats(batch, Nq, dv, n_split)) +
+            2ull * n_split * batch * Nq) * sizeof(float);
+}
 
 cudaError_t launch_attention(const AttnArgs& a)
 {

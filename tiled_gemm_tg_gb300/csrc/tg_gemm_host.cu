@@ -382,11 +382,12 @@ tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda
     return run(path, p, epi, stream);
 }
 
-tg_status tg_attention(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
-                       const void* Q, int64_t ldq, int64_t strideQ, const void* K, int64_t ldk,
-                       int64_t strideK, const void* V, int64_t ldv, int64_t strideV, void* O,
-                       int64_t ldo, int64_t strideO, float scale, tg_dtype in_dtype,
-                       tg_dtype out_dtype, tg_stream_t stream)
+tg_status tg_attention_ws(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                          const void* Q, int64_t ldq, int64_t strideQ, const void* K, int64_t ldk,
+                          int64_t strideK, const void* V, int64_t ldv, int64_t strideV, void* O,
+                          int64_t ldo, int64_t strideO, float scale, tg_dtype in_dtype,
+                          tg_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                          tg_stream_t stream)
 {
     if (batch < 0 || Nq < 0 || Nk < 0 || d < 0 || dv < 0) return TG_ERR_INVALID_ARG;
     if (strideQ < 0 || strideK < 0 || strideV < 0 || strideO < 0) return TG_ERR_INVALID_ARG;
@@ -420,9 +421,25 @@ tg_status tg_attention(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t
     if (!tma_ok(Q, ldq, strideQ, Nq) || !tma_ok(K, ldk, strideK, Nk) || !tma_ok(V, ldv, strideV, Nk))
         return TG_ERR_UNSUPPORTED;
 
+    if (workspace != nullptr && reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+        return TG_ERR_INVALID_ARG;
+
     DeviceState* ds = nullptr;
     tg_status st = device_state(&ds);
     if (st != TG_OK) return st;
+    // a split over the keys when the grid is small and the caller's
+    // workspace holds its partial results
+    const size_t need = tg::attention_ws_bytes(static_cast<int>(batch), static_cast<int>(Nq),
+                                               static_cast<int>(Nk), static_cast<int>(dv),
+                                               ds->num_sms);
+    const bool split = need > 0 && workspace != nullptr && workspace_bytes >= need;
+    if (split) {
+        u128 w0 = static_cast<u128>(reinterpret_cast<uintptr_t>(workspace));
+        u128 w1 = w0 + need;
+        if (w1 > top || overlaps(w0, w1, o0, o1) || overlaps(w0, w1, q0, q1) ||
+            overlaps(w0, w1, k0, k1) || overlaps(w0, w1, v0, v1))
+            return TG_ERR_INVALID_ARG;
+    }
     tg::AttnArgs a;
     a.batch = static_cast<int>(batch);
     a.Nq = static_cast<int>(Nq);
@@ -446,7 +463,33 @@ tg_status tg_attention(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t
     a.err = ds->err;
     a.hook = g_test_hook.load(std::memory_order_relaxed);
     a.stream = static_cast<cudaStream_t>(stream);
+    if (split) {
+        a.n_split = tg::attention_splits(a.batch, a.Nq, a.Nk, a.dv, ds->num_sms);
+        a.ws = workspace;
+    }
     return tg::launch_attention(a) == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+}
+
+tg_status tg_attention(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                       const void* Q, int64_t ldq, int64_t strideQ, const void* K, int64_t ldk,
+                       int64_t strideK, const void* V, int64_t ldv, int64_t strideV, void* O,
+                       int64_t ldo, int64_t strideO, float scale, tg_dtype in_dtype,
+                       tg_dtype out_dtype, tg_stream_t stream)
+{
+    return tg_attention_ws(batch, Nq, Nk, d, dv, Q, ldq, strideQ, K, ldk, strideK, V, ldv,
+                           strideV, O, ldo, strideO, scale, in_dtype, out_dtype, nullptr, 0,
+                           stream);
+}
+
+size_t tg_attention_workspace_size(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv)
+{
+    if (batch <= 0 || Nq <= 0 || Nk <= 0 || d <= 0 || dv <= 0) return 0;
+    if (Nq > kMaxDim || Nk > kMaxDim || d > kMaxDim || dv > 65535LL * 128 || batch > kMaxBatch)
+        return 0;
+    DeviceState* ds = nullptr;
+    if (device_state(&ds) != TG_OK) return 0;
+    return tg::attention_ws_bytes(static_cast<int>(batch), static_cast<int>(Nq),
+                                  static_cast<int>(Nk), static_cast<int>(dv), ds->num_sms);
 }
 
 tg_status tg_gemm_check(tg_stream_t stream)

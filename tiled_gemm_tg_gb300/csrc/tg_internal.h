@@ -128,9 +128,19 @@ struct AttnArgs {
     unsigned int* err;
     int hook;
     cudaStream_t stream;
+    // a split over the keys (n_split > 1) writes partial results to `ws`
+    // (attention_ws_bytes of them) and merges them in a second kernel
+    int n_split = 1;
+    void* ws = nullptr;
 };
 
 cudaError_t launch_attention(const AttnArgs& a);
+// How many key splits the attention forward uses on `num_sms` SMs (1: none),
+// the workspace bytes they need, and the offset (in floats) of the
+// maxima/normalisers after the O partials.
+int attention_splits(int batch, int Nq, int Nk, int dv, int num_sms);
+size_t attention_ws_bytes(int batch, int Nq, int Nk, int dv, int num_sms);
+long long attention_ws_o_floats(int batch, int Nq, int dv, int n_split);
 
 // Tile width the main kernel uses for this problem (64, 128 or 256).
 int main_tile_n(int M, int N, int batch, int num_sms);
