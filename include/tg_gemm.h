@@ -287,6 +287,33 @@ tg_status tg_attention_ws(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int6
 size_t tg_attention_workspace_size(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv);
 
 /*
+ * tg_attention_noalloc -- tg_attention with the key split's partial results
+ * in the library's own file-scope device scratch instead of a caller
+ * workspace.  The pages have no counterpart of this entry point: it exists
+ * so that a caller can get the split without allocating anything.
+ *
+ * Arguments, semantics and errors are those of tg_attention, plus:
+ *   - the scratch is a fixed 16 MB static device array (per device, its
+ *     address looked up once); a call whose split needs more returns
+ *     TG_ERR_UNSUPPORTED (tg_attention_workspace_size tells the need), and a
+ *     call that needs no split runs the single pass;
+ *   - nothing in the scratch has to start at zero: every partial is written
+ *     before the combine kernel reads it;
+ *   - no device memory is allocated or freed, ever;
+ *   - all calls on a device share the scratch, so calls that overlap in time
+ *     (on different streams, or from different host threads without
+ *     ordering) race on it and give undefined results.  Serialise them, or
+ *     use tg_attention_ws with one workspace per stream.
+ */
+tg_status tg_attention_noalloc(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                               const void* Q, int64_t ldq, int64_t strideQ,
+                               const void* K, int64_t ldk, int64_t strideK,
+                               const void* V, int64_t ldv, int64_t strideV,
+                               void* O, int64_t ldo, int64_t strideO,
+                               float scale, tg_dtype in_dtype, tg_dtype out_dtype,
+                               tg_stream_t stream);
+
+/*
  * tg_gemm_check -- synchronize `stream`, then read and clear the current
  * device's error word.  Returns TG_OK, TG_ERR_CUDA if the stream reported a
  * CUDA error, or TG_ERR_TIMEOUT if a kernel abandoned a bounded wait (its

@@ -20,7 +20,8 @@ __all__ = [
     "TG_ERR_TIMEOUT", "PATHS", "TgError", "lib", "library_path", "tg_gemm", "tg_gemm_check",
     "tg_status_string", "tg_gemm_path", "tg_gemm_force_path", "tg_gemm_force_tiling",
     "tg_gemm_test_hook", "tg_gemm_ex", "tg_gemm_batched", "tg_gemm_batched_path",
-    "tg_attention", "tg_attention_ws", "tg_attention_workspace_size", "attention", "ACT_NONE", "ACT_RELU", "ACT_GELU",
+    "tg_attention", "tg_attention_ws", "tg_attention_workspace_size", "tg_attention_noalloc",
+    "attention", "ACT_NONE", "ACT_RELU", "ACT_GELU",
     "tg_gemm_version", "gemm", "bmm",
     "check",
 ]
@@ -85,6 +86,10 @@ def lib() -> ctypes.CDLL:
         L.tg_attention_ws.argtypes = [i64, i64, i64, i64, i64, vp, i64, i64, vp, i64, i64, vp,
                                       i64, i64, vp, i64, i64, ctypes.c_float, i32, i32, vp,
                                       ctypes.c_size_t, vp]
+        L.tg_attention_noalloc.restype = i32
+        L.tg_attention_noalloc.argtypes = [i64, i64, i64, i64, i64, vp, i64, i64, vp, i64, i64,
+                                           vp, i64, i64, vp, i64, i64, ctypes.c_float, i32, i32,
+                                           vp]
         L.tg_attention_workspace_size.restype = ctypes.c_size_t
         L.tg_attention_workspace_size.argtypes = [i64, i64, i64, i64, i64]
         L.tg_gemm_check.restype = i32
@@ -146,6 +151,15 @@ def tg_attention_ws(batch, Nq, Nk, d, dv, Q, ldq, sQ, K, ldk, sK, V, ldv, sV, O,
     return int(lib().tg_attention_ws(batch, Nq, Nk, d, dv, Q, ldq, sQ, K, ldk, sK, V, ldv, sV, O,
                                      ldo, sO, float(scale), in_dtype, out_dtype, workspace or None,
                                      workspace_bytes, stream))
+
+
+def tg_attention_noalloc(batch, Nq, Nk, d, dv, Q, ldq, sQ, K, ldk, sK, V, ldv, sV, O, ldo, sO,
+                         scale, in_dtype, out_dtype, stream=0) -> int:
+    """tg_attention with the key split's partials in the library's static
+    scratch (no allocation; overlapping calls race on it)."""
+    return int(lib().tg_attention_noalloc(batch, Nq, Nk, d, dv, Q, ldq, sQ, K, ldk, sK, V, ldv,
+                                          sV, O, ldo, sO, float(scale), in_dtype, out_dtype,
+                                          stream))
 
 
 def tg_attention_workspace_size(batch, Nq, Nk, d, dv) -> int:

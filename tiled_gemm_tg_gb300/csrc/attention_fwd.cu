@@ -680,6 +680,36 @@ cudaError_t launch_q(const AttnArgs& a)
 
 }  // namespace
 
+namespace {
+
+// Scratch for tg_attention_noalloc: file-scope device memory, so that entry
+// point allocates nothing.  16 MB holds the key-split partials of the
+// largest calls that split (for example the page's one 1024 x 768 head needs
+// 12.6 MB); larger needs are rejected.  Every call on a device uses the same
+// bytes.
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;
+__device__ __align__(256) unsigned char g_attn_scratch[kStaticScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_addr[64];
+
+}  // namespace
+
+void* attention_static_scratch(size_t* bytes)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (g_scratch_addr[dev] == nullptr) {
+        // the symbol's address on this device, looked up once
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess) return nullptr;
+        g_scratch_addr[dev] = p;
+    }
+    *bytes = kStaticScratchBytes;
+    return g_scratch_addr[dev];
+}
+
 long long attention_ws_o_floats(int batch, int Nq, int dv, int n_split)
 {
     // the O partials (rows padded to 4 floats), rounded up to 64 floats so

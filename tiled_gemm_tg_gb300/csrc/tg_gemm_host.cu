@@ -481,6 +481,26 @@ tg_status tg_attention(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t
                            stream);
 }
 
+tg_status tg_attention_noalloc(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                               const void* Q, int64_t ldq, int64_t strideQ, const void* K,
+                               int64_t ldk, int64_t strideK, const void* V, int64_t ldv,
+                               int64_t strideV, void* O, int64_t ldo, int64_t strideO, float scale,
+                               tg_dtype in_dtype, tg_dtype out_dtype, tg_stream_t stream)
+{
+    const size_t need = tg_attention_workspace_size(batch, Nq, Nk, d, dv);
+    if (need == 0)  // no split (or invalid arguments, which tg_attention_ws reports)
+        return tg_attention_ws(batch, Nq, Nk, d, dv, Q, ldq, strideQ, K, ldk, strideK, V, ldv,
+                               strideV, O, ldo, strideO, scale, in_dtype, out_dtype, nullptr, 0,
+                               stream);
+    size_t bytes = 0;
+    void* scratch = tg::attention_static_scratch(&bytes);
+    if (scratch == nullptr) return TG_ERR_CUDA;
+    if (need > bytes) return TG_ERR_UNSUPPORTED;  // the split needs more than the static scratch
+    return tg_attention_ws(batch, Nq, Nk, d, dv, Q, ldq, strideQ, K, ldk, strideK, V, ldv,
+                           strideV, O, ldo, strideO, scale, in_dtype, out_dtype, scratch, bytes,
+                           stream);
+}
+
 size_t tg_attention_workspace_size(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv)
 {
     if (batch <= 0 || Nq <= 0 || Nk <= 0 || d <= 0 || dv <= 0) return 0;

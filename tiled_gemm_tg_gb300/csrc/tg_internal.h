@@ -141,6 +141,9 @@ cudaError_t launch_attention(const AttnArgs& a);
 int attention_splits(int batch, int Nq, int Nk, int dv, int num_sms);
 size_t attention_ws_bytes(int batch, int Nq, int Nk, int dv, int num_sms);
 long long attention_ws_o_floats(int batch, int Nq, int dv, int n_split);
+// The current device's address of the file-scope attention scratch (looked
+// up once per device) and its size; nullptr on failure.
+void* attention_static_scratch(size_t* bytes);
 
 // Tile width the main kernel uses for this problem (64, 128 or 256).
 int main_tile_n(int M, int N, int batch, int num_sms);
