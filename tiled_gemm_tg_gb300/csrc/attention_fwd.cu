@@ -583,34 +583,72 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 // The combine step of a split over the keys: per output element,
 // O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s with M = max_s m_s, the
 // same merge of running maxima and normalisers the blockwise pass applies.
+// A CTA takes blockDim.y query rows of one batch entry; a thread takes four
+// columns at a time, and all loads of a row are issued before any is used.
+constexpr int kMaxSplit = 16;
+
 template <bool OUT_F32>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(256)
 attention_combine_kernel(const float* ws_o, const float* ws_ml, void* O, long long ldo,
                          long long sO, int Nq, int dv, int n_split)
 {
-    const int n = blockIdx.x * 128 + static_cast<int>(threadIdx.x);
-    if (n >= dv) return;
     const int b = static_cast<int>(blockIdx.z);
     const int batch = static_cast<int>(gridDim.z);
     const int ldw = (dv + 3) & ~3;
     void* Ob = batch_ptr(O, b, sO, OUT_F32 ? 4 : 2);
-    for (int m = blockIdx.y; m < Nq; m += gridDim.y) {
+    for (int m = blockIdx.y * blockDim.y + threadIdx.y; m < Nq; m += gridDim.y * blockDim.y) {
+        // the row's maxima and normalisers (the same for every column)
+        float mv[kMaxSplit], lv[kMaxSplit];
         float M = -INFINITY;
-        for (int sp = 0; sp < n_split; ++sp)
-            M = fmaxf(M, ws_ml[2 * ((static_cast<long long>(sp) * batch + b) * Nq + m)]);
-        float num = 0.0f, den = 0.0f;
-        for (int sp = 0; sp < n_split; ++sp) {
-            const long long row = (static_cast<long long>(sp) * batch + b) * Nq + m;
-            const float w = ex2_approx(ws_ml[2 * row] - M);
-            num = fmaf(w, ws_o[row * ldw + n], num);
-            den = fmaf(w, ws_ml[2 * row + 1], den);
+#pragma unroll
+        for (int sp = 0; sp < kMaxSplit; ++sp) {
+            if (sp < n_split) {
+                const long long row = (static_cast<long long>(sp) * batch + b) * Nq + m;
+                mv[sp] = ws_ml[2 * row];
+                lv[sp] = ws_ml[2 * row + 1];
+            }
         }
-        const float y = num / den;
-        const long long i = static_cast<long long>(m) * ldo + n;
-        if constexpr (OUT_F32)
-            static_cast<float*>(Ob)[i] = y;
-        else
-            static_cast<__half*>(Ob)[i] = __float2half_rn(y);
+#pragma unroll
+        for (int sp = 0; sp < kMaxSplit; ++sp)
+            if (sp < n_split) M = fmaxf(M, mv[sp]);
+        float den = 0.0f;
+#pragma unroll
+        for (int sp = 0; sp < kMaxSplit; ++sp) {
+            if (sp < n_split) {
+                mv[sp] = ex2_approx(mv[sp] - M);  // now the split's weight
+                den = fmaf(mv[sp], lv[sp], den);
+            }
+        }
+        const float inv = 1.0f / den;
+        for (int n = 4 * static_cast<int>(threadIdx.x); n < dv; n += 4 * static_cast<int>(blockDim.x)) {
+            float4 ov[kMaxSplit];
+#pragma unroll
+            for (int sp = 0; sp < kMaxSplit; ++sp)
+                if (sp < n_split)
+                    ov[sp] = *reinterpret_cast<const float4*>(
+                        ws_o + ((static_cast<long long>(sp) * batch + b) * Nq + m) * ldw + n);
+            float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int sp = 0; sp < kMaxSplit; ++sp) {
+                if (sp < n_split) {
+                    num.x = fmaf(mv[sp], ov[sp].x, num.x);
+                    num.y = fmaf(mv[sp], ov[sp].y, num.y);
+                    num.z = fmaf(mv[sp], ov[sp].z, num.z);
+                    num.w = fmaf(mv[sp], ov[sp].w, num.w);
+                }
+            }
+            const float y[4] = {num.x * inv, num.y * inv, num.z * inv, num.w * inv};
+            const long long i = static_cast<long long>(m) * ldo + n;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (n + j < dv) {
+                    if constexpr (OUT_F32)
+                        static_cast<float*>(Ob)[i + j] = y[j];
+                    else
+                        static_cast<__half*>(Ob)[i + j] = __float2half_rn(y[j]);
+                }
+            }
+        }
     }
 }
 
@@ -664,9 +702,15 @@ cudaError_t launch_cfg(const AttnArgs& a)
                                                      kv_per_split, ws_o, ws_ml, a.hook, a.err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || n_split == 1) return e;
-    const dim3 cgrid((a.dv + 127) / 128, a.Nq < 65535 ? a.Nq : 65535, a.batch);
-    attention_combine_kernel<OUT_F32><<<cgrid, 128, 0, a.stream>>>(ws_o, ws_ml, a.O, a.ldo, a.sO,
-                                                                   a.Nq, a.dv, n_split);
+    // 4 columns per thread across a row (at most 256 threads), the rest of the
+    // 256 threads of a CTA on further rows
+    int bx = ((a.dv + 3) / 4 + 31) / 32 * 32;
+    if (bx > 256) bx = 256;
+    const int by = 256 / bx;
+    const long long rows = (a.Nq + by - 1) / by;
+    const dim3 cgrid(1, static_cast<unsigned>(rows < 65535 ? rows : 65535), a.batch);
+    attention_combine_kernel<OUT_F32><<<cgrid, dim3(bx, by), 0, a.stream>>>(
+        ws_o, ws_ml, a.O, a.ldo, a.sO, a.Nq, a.dv, n_split);
     return cudaGetLastError();
 }
 
@@ -724,9 +768,10 @@ int attention_splits(int batch, int Nq, int Nk, int dv, int num_sms)
                            ((dv + (dv <= 128 ? 128 : 256) - 1) / (dv <= 128 ? 128 : 256)) * batch;
     const int n_kv = (Nk + BN - 1) / BN;
     if (2 * base > num_sms || n_kv < 2) return 1;
-    // as many splits as keep every CTA of the call in one wave
+    // as many splits as keep every CTA of the call in one wave (at most 16)
     int want = static_cast<int>(num_sms / base);
     if (want > n_kv) want = n_kv;
+    if (want > kMaxSplit) want = kMaxSplit;
     const int per = (n_kv + want - 1) / want;
     return (n_kv + per - 1) / per;
 }
