@@ -116,6 +116,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = tmem_slot;
+    pdl_wait();  // the previous kernel on the stream is complete from here on
     const uint32_t epi_limit = kSlowPolls + 64u * static_cast<uint32_t>(min(kb1 - kb0, 1 << 20));
 
     if (warp == 0) {
@@ -252,6 +253,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     }
 
     // No CTA may leave while a peer can still read its shared memory.
+    pdl_trigger();  // this CTA has issued all its global writes
     cluster_sync();
     if (warp == 1) {
         tc_fence_after();
@@ -335,13 +337,14 @@ cudaError_t launch_cfg(const GemmArgs& a)
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = Cfg::SMEM;
     cfg.stream = a.stream;
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = split;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
+    set_pdl_attr(at[1]);
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kernel, ta, tbt, a.C, a.ldc, a.M, a.N, a.K, split, a.hook, a.err,
                               a.epi, a.batch_args());
 }

@@ -127,6 +127,7 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = tmem_slot;
+    pdl_wait();  // the previous kernel on the stream is complete from here on
 
     constexpr int BK = KBlock<ES>::BK;
     constexpr int NB = KBlock<ES>::NB;
@@ -288,6 +289,7 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
     }
 
+    pdl_trigger();  // this CTA has issued all its global writes
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -336,10 +338,17 @@ cudaError_t launch_cfg(const GemmArgs& a)
     const int c_vec = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) &&
                       ((static_cast<size_t>(a.ldc) * es) % 16 == 0) &&
                       ((static_cast<size_t>(a.sC) * es) % 16 == 0);
-    kernel<<<grid, kThreads, Cfg::SMEM, a.stream>>>(ta, tb, a.C, a.ldc, a.M, a.N, a.K, tiles_m,
-                                                     tiles_n, group_m, c_vec, a.hook, a.err,
-                                                     a.epi, a.batch_args());
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Cfg::SMEM;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute at[1];
+    set_pdl_attr(at[0]);
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, ta, tb, a.C, a.ldc, a.M, a.N, a.K, tiles_m, tiles_n,
+                              group_m, c_vec, a.hook, a.err, a.epi, a.batch_args());
 }
 
 }  // namespace

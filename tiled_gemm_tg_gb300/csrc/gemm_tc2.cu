@@ -142,6 +142,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
     tc_fence_after();
     const uint32_t tmem_base = tmem_slot;
+    pdl_wait();  // the previous kernel on the stream is complete from here on
 
     using KG = PairK<ES>;
     constexpr int BK = KG::BK;
@@ -316,6 +317,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
     }
 
+    pdl_trigger();  // this CTA has issued all its global writes
     tc_fence_before();
     cluster_sync();
     if (warp == 1) {
@@ -386,13 +388,14 @@ cudaError_t launch_cfg(const GemmArgs& a)
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = SMEM;
     cfg.stream = a.stream;
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = 2;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
+    set_pdl_attr(at[1]);
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kernel, ta, tb, a.C, a.ldc, a.M, a.N, a.K, tiles_m, tiles_n,
                               group_m, c_vec, a.hook, a.err, a.epi, a.batch_args());
 }

@@ -177,6 +177,7 @@ gemm_tc_boundary_kernel(const __half* __restrict__ A0, long long lda, const __ha
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = tmem_slot;
+    pdl_wait();  // the previous kernel on the stream is complete from here on
 
     constexpr uint32_t idesc = idesc_f16_f32(BM, BN, false, true);
     const int num_kb = (K + BK - 1) / BK;
@@ -253,6 +254,7 @@ gemm_tc_boundary_kernel(const __half* __restrict__ A0, long long lda, const __ha
         umma_commit(smem_u32(&drain_bar));
         if (!mbar_wait(smem_u32(&drain_bar), 0, nullptr)) atomicOr(err, ERR_DRAIN);
     }
+    pdl_trigger();  // this CTA has issued all its global writes
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -283,10 +285,18 @@ cudaError_t launch_cfg(const GemmArgs& a)
     }
     const dim3 grid((a.N + BN - 1) / BN, (a.M + BM - 1) / BM, a.batch);
     if (grid.y > 65535u || grid.z > 65535u) return cudaErrorInvalidConfiguration;
-    kernel<<<grid, kThreads, SMEM, a.stream>>>(
-        static_cast<const __half*>(a.A), a.lda, static_cast<const __half*>(a.B), a.ldb, a.C, a.ldc,
-        a.M, a.N, a.K, a.hook, a.err, a.epi, a.batch_args());
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = SMEM;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute at[1];
+    set_pdl_attr(at[0]);
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<const __half*>(a.A), a.lda,
+                              static_cast<const __half*>(a.B), a.ldb, a.C, a.ldc, a.M, a.N, a.K,
+                              a.hook, a.err, a.epi, a.batch_args());
 }
 
 }  // namespace

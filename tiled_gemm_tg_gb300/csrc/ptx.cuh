@@ -274,6 +274,20 @@ __device__ __forceinline__ float ex2_approx(float x)
     return y;
 }
 
+// Programmatic dependent launch.  pdl_wait: block until the grid this one
+// depends on (launched before it on the stream with the programmatic
+// serialization attribute) has completed and its memory is visible; a no-op
+// otherwise.  pdl_trigger: allow the dependent grid to start its prologue.
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_trigger()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Named barrier `id` (1..15) over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(int id, int count)
 {

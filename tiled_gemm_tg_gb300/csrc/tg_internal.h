@@ -18,6 +18,20 @@ enum Path : int {
     PATH_MAIN_PAIR = 6, // TMA + tcgen05, 256 x 256 tiles on CTA pairs (cta_group::2)
 };
 
+// Programmatic dependent launch (on by default): a kernel's prologue (barrier
+// setup, TMEM allocation, descriptor prefetch) may overlap the end of the
+// kernel before it on the stream; the kernel waits for that grid's
+// completion (griddepcontrol.wait) before touching global memory.
+#ifndef TG_PDL
+#define TG_PDL 1
+#endif
+
+inline void set_pdl_attr(cudaLaunchAttribute& at)
+{
+    at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at.val.programmaticStreamSerializationAllowed = TG_PDL;
+}
+
 // Bits of the device error word (OR-ed by kernels that abandon a wait).
 enum ErrBits : unsigned int {
     ERR_MAIN_PRODUCER = 1u << 0,
