@@ -1,5 +1,6 @@
-// gemm_tc.cu -- the main fp16 GEMM kernel for sm_103a: C = A x B with fp32
-// accumulation in tensor memory.
+// gemm_tc.cu -- the one-CTA GEMM kernel for sm_103a: C = A x B (fp16 or
+// E4M3 inputs) with fp32 accumulation in tensor memory, for mid-size,
+// small-K and batched problems.
 //
 // What the pages describe ("企业官网建设流程全解析" (cf-1.com), §2.3 and §3.3):
 // a 2-D grid of 128x128 output tiles, A and B tiles staged in shared memory,
@@ -12,18 +13,22 @@
 //   * persistent grid of one CTA per SM walking a grouped tile order, so a
 //     wave of tiles shares A rows and B columns in L2 (the "block_wise"
 //     mapping of "TileLang：GPU异构计算的声明式分块编程范式" (kwkr.cn), §3.3);
-//   * tiles of 128 x BN (BN = 256, 128 or 64), k-blocks of 64 fp16, so one
-//     A row of a k-block is exactly one 128-byte swizzle atom;
-//   * warp 0: TMA producer.  A is loaded K-major ([128 rows][64 k]), B is
-//     loaded MN-major in BN/64 boxes of [64 k rows][64 n], all with the
-//     128-byte swizzle, into a ring of STAGES full/empty mbarrier pairs;
-//   * warp 1: allocates tensor memory and issues tcgen05.mma (M=128,
-//     N=BN, K=16, four per k-block) from one thread, accumulating in a
-//     double-buffered TMEM accumulator (2 x BN fp32 columns);
-//   * warps 2..5: epilogue.  Each thread owns one output row: tcgen05.ld
-//     of 32 columns at a time, fp32 -> fp16 round-to-nearest-even (or fp32
-//     as is), 16-byte vector stores, predicated at the M/N edges.  The
-//     epilogue of tile i overlaps the main loop of tile i+1.
+//   * tiles of 128 x BN (BN = 256, 128 or 64), k-blocks of 128 bytes per
+//     row (64 fp16 or 128 E4M3), so one A row of a k-block is exactly one
+//     128-byte swizzle atom; a strided batch walks every tile of every
+//     matrix through 3-D tensor maps;
+//   * warp 0: TMA producer.  A is loaded K-major ([128 rows][128 B]), B is
+//     loaded MN-major in 128-byte-wide boxes of [k rows][128 B of n], all
+//     with the 128-byte swizzle, into a ring of STAGES full/empty mbarrier
+//     pairs;
+//   * warp 1: allocates tensor memory and issues tcgen05.mma (M=128, N=BN,
+//     32 bytes of k each, four per k-block) from one thread, accumulating in
+//     a double-buffered TMEM accumulator (2 x BN fp32 columns);
+//   * warps 2..9: epilogue, two per TMEM lane quadrant (half of the columns
+//     each).  Each thread owns one output row: tcgen05.ld of 32 columns at a
+//     time, the fused epilogue if any, fp32 -> fp16 round-to-nearest-even
+//     (or fp32 as is), 16-byte vector stores, predicated at the M/N edges.
+//     The epilogue of tile i overlaps the main loop of tile i+1.
 // Out-of-range rows, columns and k are zero-filled by TMA, so any M, N, K
 // works as long as the operands are TMA-addressable (16-byte aligned bases,
 // row strides a multiple of 16 bytes); the host routes everything else to

@@ -1,19 +1,19 @@
-// gemm_tc2.cu -- CTA-pair variant of the main fp16 GEMM kernel for sm_103a:
-// C = A x B with 256 x 256 output tiles computed by two CTAs of a cluster
-// that share one tcgen05.mma.cta_group::2 (M=256, N=256, K=16).
+// gemm_tc2.cu -- CTA-pair GEMM kernel for sm_103a: C = A x B (fp16 or E4M3
+// inputs) with 256 x 256 output tiles computed by two CTAs of a cluster that
+// share one tcgen05.mma.cta_group::2 (M=256, N=256, 32 bytes of k).
 //
 // The method is the pages' pipelined tiled GEMM ("企业官网建设流程全解析"
 // (cf-1.com), §2.3 warp specialisation + TMA + mbarrier, §3.3 the tiled
 // K loop with num_stages buffers, §4.1 swizzled shared memory); this file is
 // the GB300 form of it for large problems.
 //
-// Why a pair: each CTA holds half of A's rows (128 x 128) and half of B's
-// columns (128 x 128) of a 256 x 256 x 128 k-block, so a 64 KB stage feeds
-// 1024 MMA cycles and each B column block is loaded once per pair instead of
-// once per 128 rows (a third less L2 -> SM traffic than 128 x 256 tiles).
-// Three stages fill 192 KB of shared memory.
+// Why a pair: each CTA holds half of A's rows (128 rows x 256 B) and half of
+// B's columns (256 B of k x 128 columns) of a 256 x 256 k-block, so a 64 KB
+// stage feeds 1024 MMA cycles and each B column block is loaded once per pair
+// instead of once per 128 rows (a third less L2 -> SM traffic than 128 x 256
+// tiles).  Three stages fill 192 KB of shared memory.
 //
-// Roles (192 threads per CTA, the same in both CTAs of the pair):
+// Roles (320 threads per CTA, the same in both CTAs of the pair):
 //   warp 0   TMA producer.  Each CTA loads its own halves into its own shared
 //            memory; every copy signals the EVEN (leader) CTA's full barrier,
 //            which the leader's producer arms with both CTAs' bytes.
@@ -21,8 +21,9 @@
 //            accumulators); only the leader's lane 0 issues the MMAs.  Each
 //            k-block's commit is multicast to both CTAs' empty barriers,
 //            each tile's commit to both CTAs' tmem-full barriers.
-//   warps 2-5  epilogue in both CTAs: each CTA reads its own 128 rows of the
-//            accumulator from its own TMEM and stores them; all 256 epilogue
+//   warps 2-9  epilogue in both CTAs, two per TMEM lane quadrant: each CTA
+//            reads its own 128 rows of the accumulator from its own TMEM
+//            (each warp half of the columns) and stores them; all epilogue
 //            threads of the pair arrive on the leader's tmem-empty barrier.
 // Waits are bounded as in the one-CTA kernel; on expiry a role records a bit
 // in the device error word and leaves its loop; the leader waits for the
