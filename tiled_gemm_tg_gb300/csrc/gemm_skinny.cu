@@ -18,9 +18,9 @@
 //     synchronises, and CTA r sums, in rank order, rows n in
 //     [r*128/S, (r+1)*128/S) of all S partials, rounds to the output type and
 //     stores them.  No global workspace, one launch.
-// Warp roles as in the main kernel: warp 0 TMA producer (k-block 128, four
+// Roles (192 threads per CTA): warp 0 TMA producer (k-block 128, four
 // stages), warp 1 TMEM allocation + single-thread tcgen05.mma issue, warps
-// 2-5 read the accumulator.  Waits are bounded; on expiry the kernel records
+// 2-5 read the accumulator, one per TMEM lane quadrant.  Waits are bounded; on expiry the kernel records
 // a bit in the device error word, stops issuing, waits for its own copies and
 // MMAs, and still reaches the cluster barriers so no CTA waits on a missing
 // peer.
