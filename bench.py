@@ -323,6 +323,12 @@ def main_attention(args, w):
     # a workspace lets calls with few CTAs split the keys (the library says how much)
     ws_bytes = tg.tg_attention_workspace_size(B, Nq, Nk, d, dv)
     workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    forced = {"auto": 0, "general": 1, "tmem_p": 3}[args.attn_kernel]
+    if tg.tg_attention_force_kernel(forced) != tg.TG_OK:
+        raise RuntimeError("attention kernel override refused")
+    kern = tg.tg_attention_kernel(B, Nq, Nk, d, dv, split_allowed=bool(ws_bytes))
+    kern_name = {1: "attention_fwd_kernel", 2: "attention_fwd_kernel (+ attention_combine_kernel)",
+                 3: "attention_fwd2_kernel"}.get(kern, "none")
 
     def call(q, k, v, o, handle):
         st = tg.tg_attention_ws(B, Nq, Nk, d, dv, q.data_ptr(), d, Nq * d, k.data_ptr(), d,
@@ -403,7 +409,7 @@ def main_attention(args, w):
     alg_bytes = w.algorithmic_bytes()
     roofline = {
         "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-        "frac": achieved / peak, "traffic": None, "kernel": "attention_fwd_kernel",
+        "frac": achieved / peak, "traffic": None, "kernel": kern_name,
         "kernel_ms": kern_ms,
         "peak_source": f"{peak_src} bf16 burst (torch.matmul 8192^3) x 1.0 fp16/bf16 nominal ratio",
         "flop_per_byte": flops / alg_bytes, "algorithmic_bytes": alg_bytes,
@@ -426,6 +432,8 @@ def main_attention(args, w):
             "config": {"workload": w.name, "batch": B, "Nq": Nq, "Nk": Nk, "d": d, "dv": dv,
                        "scale": w.scale, "out_dtype": w.out_dtype, "accum": "f32",
                        "key_split_workspace_bytes": ws_bytes,
+                       "kernel": {1: "general, P in shared memory", 2: "general, keys split",
+                                  3: "P in tensor memory"}.get(kern, "none"),
                        "l2": f"{n_sets} rotating Q/K/V/O sets, "
                              f"{n_sets * set_bytes / 2**20:.0f} MB per pass",
                        "timing": "stream launches",
@@ -435,7 +443,7 @@ def main_attention(args, w):
                     "h2d_bytes_per_step": B * (Nq * d + Nk * (d + dv)) * 2,
                     "d2h_bytes_per_step": B * Nq * dv * oh.element_size(), "steps": e2e_steps,
                     "pipeline": "H2D / tg_attention / D2H on one stream"},
-            "gpu_launches": args.steps * (2 if ws_bytes else 1),  # + the combine kernel
+            "gpu_launches": args.steps * (2 if kern == 2 else 1),  # + the combine kernel
             "roofline": roofline,
             "cpu_baseline": cpu,
         }
@@ -457,6 +465,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--epilogue", default="none", choices=sorted(EPILOGUES),
                     help="time tg_gemm_ex with this fused epilogue instead of tg_gemm")
+    ap.add_argument("--attn-kernel", default="auto", choices=["auto", "general", "tmem_p"],
+                    help="attention workloads: the library's choice of forward kernel, or one "
+                         "forced (tmem_p serves d <= 128, dv <= 128)")
     ap.add_argument("--graph", action="store_true",
                     help="replay the timed launches from one CUDA graph (for us-scale shapes)")
     args = ap.parse_args()

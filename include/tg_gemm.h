@@ -377,6 +377,28 @@ void tg_gemm_test_hook(int hook);
  */
 tg_status tg_gemm_force_tiling(int bn, int group_m);
 
+/*
+ * Attention kernel selection, for tests and benchmarks.  tg_attention_kernel
+ * reports, without launching anything, which forward kernel a call with these
+ * sizes would run on the current device: tg_attention (split_allowed = 0),
+ * or tg_attention_ws / tg_attention_noalloc given the workspace that
+ * tg_attention_workspace_size asks for (split_allowed = 1):
+ *   0 none (sizes out of range or empty; tg_attention reports the error),
+ *   1 the general kernel (any d and dv; P staged in shared memory),
+ *   2 the same with the keys split over several CTAs and a combine kernel
+ *     (calls with few query tiles, given the workspace),
+ *   3 the kernel that keeps P in tensor memory, with two score buffers
+ *     (heads with d <= 128 and dv <= 128).
+ * tg_attention_force_kernel(1) keeps later calls off kernel 3;
+ * tg_attention_force_kernel(3) runs kernel 3, with no key split, for every
+ * later call whose head sizes it serves (others choose automatically); 0
+ * restores automatic selection.  Process-wide.  Returns TG_ERR_INVALID_ARG
+ * (and changes nothing) for any other value.
+ */
+int tg_attention_kernel(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                        int split_allowed);
+tg_status tg_attention_force_kernel(int kernel);
+
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int tg_gemm_version(void);
 

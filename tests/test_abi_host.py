@@ -386,3 +386,19 @@ def test_attention_workspace_checks_on_host():
     # sizes with no work, or invalid ones, need no workspace
     assert tg.tg_attention_workspace_size(0, 128, 128, 64, 64) == 0
     assert tg.tg_attention_workspace_size(1, 128, -1, 64, 64) == 0
+
+
+def test_attention_kernel_selection_on_host():
+    """The kernel override accepts 0, 1 and 3 only; the kernel query reports
+    0 for sizes with no work or out of range, before touching a device."""
+    try:
+        for bad in (-1, 2, 4, 99):
+            assert tg.tg_attention_force_kernel(bad) == tg.TG_ERR_INVALID_ARG
+        for ok in (1, 3, 0):
+            assert tg.tg_attention_force_kernel(ok) == tg.TG_OK
+    finally:
+        tg.tg_attention_force_kernel(0)
+    assert tg.tg_attention_kernel(0, 128, 128, 64, 64) == 0
+    assert tg.tg_attention_kernel(1, 128, 0, 64, 64) == 0
+    assert tg.tg_attention_kernel(1, -5, 128, 64, 64) == 0
+    assert tg.tg_attention_kernel(65536, 128, 128, 64, 64) == 0

@@ -80,10 +80,12 @@ def test_simt_path_ignores_the_hook():
         tg.tg_gemm_test_hook(0)
 
 
-def test_attention_bounded_wait_expiry_is_reported():
-    """The attention kernel under the hook: its first Q/K stage stays empty,
-    the MMA issuer's wait runs out, every role winds down, and the next call
-    without the hook is correct."""
+@pytest.mark.parametrize("kernel", [1, 3])
+def test_attention_bounded_wait_expiry_is_reported(kernel):
+    """Each attention kernel under the hook (1: the general kernel, 3: the
+    one keeping P in tensor memory): its first K stage stays empty, the MMA
+    issuer's wait runs out, every role winds down, and the next call without
+    the hook is correct."""
     import numpy as np
 
     import oracle
@@ -95,18 +97,23 @@ def test_attention_bounded_wait_expiry_is_reported():
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     s = torch.cuda.current_stream().cuda_stream
     assert tg.tg_gemm_check(s) == tg.TG_OK
-    tg.tg_gemm_test_hook(1)
+    assert tg.tg_attention_force_kernel(kernel) == tg.TG_OK
     try:
-        t0 = time.time()
-        tg.attention(qd, kd, vd, 0.125)
-        assert tg.tg_gemm_check(s) == tg.TG_ERR_TIMEOUT
-        elapsed = time.time() - t0
+        assert tg.tg_attention_kernel(1, 200, 300, 64, 64) == kernel
+        tg.tg_gemm_test_hook(1)
+        try:
+            t0 = time.time()
+            tg.attention(qd, kd, vd, 0.125)
+            assert tg.tg_gemm_check(s) == tg.TG_ERR_TIMEOUT
+            elapsed = time.time() - t0
+        finally:
+            tg.tg_gemm_test_hook(0)
+        assert 0.5 < elapsed < 30.0, elapsed
+        assert tg.tg_gemm_check(s) == tg.TG_OK
+        o = tg.attention(qd, kd, vd, 0.125)
+        tg.check()
     finally:
-        tg.tg_gemm_test_hook(0)
-    assert 0.5 < elapsed < 30.0, elapsed
-    assert tg.tg_gemm_check(s) == tg.TG_OK
-    o = tg.attention(qd, kd, vd, 0.125)
-    tg.check()
+        tg.tg_attention_force_kernel(0)
     O, E, G = oracle.attention(q.numpy(), k.numpy(), v.numpy(), 0.125)
     tol = oracle.attention_tolerance(O, E, G, 64, 300, True)
     assert np.all(np.abs(o.double().cpu().numpy() - O) <= tol)

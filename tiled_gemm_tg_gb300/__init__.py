@@ -21,6 +21,7 @@ __all__ = [
     "tg_status_string", "tg_gemm_path", "tg_gemm_force_path", "tg_gemm_force_tiling",
     "tg_gemm_test_hook", "tg_gemm_ex", "tg_gemm_batched", "tg_gemm_batched_path",
     "tg_attention", "tg_attention_ws", "tg_attention_workspace_size", "tg_attention_noalloc",
+    "tg_attention_kernel", "tg_attention_force_kernel",
     "attention", "ACT_NONE", "ACT_RELU", "ACT_GELU",
     "tg_gemm_version", "gemm", "bmm",
     "check",
@@ -92,6 +93,10 @@ def lib() -> ctypes.CDLL:
                                            vp]
         L.tg_attention_workspace_size.restype = ctypes.c_size_t
         L.tg_attention_workspace_size.argtypes = [i64, i64, i64, i64, i64]
+        L.tg_attention_kernel.restype = i32
+        L.tg_attention_kernel.argtypes = [i64, i64, i64, i64, i64, i32]
+        L.tg_attention_force_kernel.restype = i32
+        L.tg_attention_force_kernel.argtypes = [i32]
         L.tg_gemm_check.restype = i32
         L.tg_gemm_check.argtypes = [vp]
         L.tg_status_string.restype = ctypes.c_char_p
@@ -177,6 +182,14 @@ def tg_status_string(status: int) -> str:
 
 def tg_gemm_path(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype) -> int:
     return int(lib().tg_gemm_path(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype))
+
+
+def tg_attention_kernel(batch, Nq, Nk, d, dv, split_allowed: bool = False) -> int:
+    return int(lib().tg_attention_kernel(batch, Nq, Nk, d, dv, 1 if split_allowed else 0))
+
+
+def tg_attention_force_kernel(kernel: int) -> int:
+    return int(lib().tg_attention_force_kernel(int(kernel)))
 
 
 def tg_gemm_force_path(path: int) -> None:

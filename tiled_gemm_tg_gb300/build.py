@@ -27,6 +27,7 @@ SOURCES = [
     "gemm_skinny.cu",
     "gemm_simt_f32.cu",
     "attention_fwd.cu",
+    "attention_fwd2.cu",
 ]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -457,12 +457,12 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                         if (j >= valid) a0 = -INFINITY;
                         if (j + 1 >= valid) a1 = -INFINITY;
                     }
-                    const float p0 = ex2_approx(a0);
-                    const float p1 = ex2_approx(a1);
-                    l0 += p0;
-                    l1 += p1;
-                    __half2 v2 = __floats2half2_rn(p0, p1);
-                    pw[j / 2] = *reinterpret_cast<uint32_t*>(&v2);
+                    const __half2 v2 = __floats2half2_rn(ex2_approx(a0), ex2_approx(a1));
+                    // the normaliser sums the weights the MMA uses: the fp16 ones
+                    const float2 r2 = __half22float2(v2);
+                    l0 += r2.x;
+                    l1 += r2.y;
+                    pw[j / 2] = *reinterpret_cast<const uint32_t*>(&v2);
                 }
             };
             if (valid < HK) make_p(std::true_type{});
@@ -784,8 +784,18 @@ size_t attention_ws_bytes(int batch, int Nq, int Nk, int dv, int num_sms)
             2ull * n_split * batch * Nq) * sizeof(float);
 }
 
+int attention_kernel_choice(int batch, int Nq, int Nk, int d, int dv, int num_sms, bool split_ok,
+                            int forced)
+{
+    const bool tmem_ok = attention_tmem_p_serves(d, dv);
+    if (forced == 3 && tmem_ok) return 3;
+    if (split_ok && attention_splits(batch, Nq, Nk, dv, num_sms) > 1) return 2;
+    return forced == 1 || !tmem_ok ? 1 : 3;
+}
+
 cudaError_t launch_attention(const AttnArgs& a)
 {
+    if (a.tmem_p) return launch_attention_tmem_p(a);
     if (a.dv <= 128) return a.out_f32 ? launch_q<128, true>(a) : launch_q<128, false>(a);
     return a.out_f32 ? launch_q<256, true>(a) : launch_q<256, false>(a);
 }

@@ -1,0 +1,525 @@
+// attention_fwd2.cu -- attention forward O = softmax(scale * Q K^T) V for heads
+// with d <= 128 and dv <= 128, the probabilities kept in tensor memory.
+//
+// The operation and its blockwise evaluation are those of "TileLang实战：用
+// Python DSL自动生成高性能GPU计算内核" (gsyq.cn), §4 (FlashAttention): keys and
+// values are consumed in blocks, each query row keeps its running maximum M
+// and normaliser L, and the output is rescaled when M grows.  The general
+// kernel (attention_fwd.cu) computes the same thing for any d and dv; this
+// one is laid out for the common head sizes.
+//
+// GB300 design.  A CTA owns 128 query rows and walks the keys in blocks of
+// 128, with two TMEM score buffers b = t % 2:
+//   S_t = Q K_t^T      tcgen05.mma M=128 N=128, K = d (Q resident, the key
+//                      block one TMA stage), into TMEM columns 128b..128b+127;
+//   P_t = exp2(S_t * scale * log2 e - m)   two threads per query row (64
+//                      scores each, one tcgen05.ld) agree on the row maximum
+//                      and write P as fp16 pairs over the first 64 of those
+//                      columns;
+//   O += P_t V_t       tcgen05.mma with A = P_t from TMEM, B = V_t from shared
+//                      memory (MN-major), accumulating in TMEM columns
+//                      256 .. 383.
+// S_(t+1) goes to the other buffer, so the tensor core computes it while the
+// softmax turns S_t into P_t; S_(t+2) reuses buffer b once P_t V_t has
+// completed.  P never leaves tensor memory: no shared-memory round trip and
+// no proxy fence between the softmax and the MMA.  Each tcgen05.commit ends
+// a whole block of MMAs: a commit after a few MMAs leaves the pipe idle.
+// The running maximum is raised only when a block's maximum exceeds it by
+// more than 8 (base 2); then the row of O (in TMEM) and L are scaled by
+// 2^(m_old - m_new) before P_t V_t is issued.
+//
+// Warp roles (384 threads): 0 TMA for Q (once) and K, 1 TMEM allocation and
+// the S MMAs, 2 TMA for V, 3 the P V MMAs, 4-11 softmax and output (warp w
+// reads TMEM lane quadrant w % 4; two warps per quadrant split the keys).
+// Every wait is bounded: on expiry a role records it in the device error
+// word, raises the CTA's abort flag and winds down.
+#include <cstdint>
+#include <mutex>
+#include <type_traits>
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+#include "tc_common.cuh"
+#include "tg_internal.h"
+
+namespace tg {
+namespace {
+
+using namespace tg::dev;
+
+constexpr int BM = 128;                        // query rows per CTA
+constexpr int BN = 128;                        // keys per block
+constexpr int DC = 64;                         // d per chunk: 128 bytes of fp16
+constexpr int QC = 2;                          // Q chunks (d <= 128)
+constexpr uint32_t Q_CHUNK = BM * DC * 2;      // 16 KB
+constexpr uint32_t K_CHUNK = BN * DC * 2;      // 16 KB
+constexpr uint32_t K_BLK = QC * K_CHUNK;       // a key block: one stage, one release
+constexpr uint32_t V_BOX = BN * 128;           // [128 keys][64 columns] fp16, 16 KB
+constexpr uint32_t V_STAGE = 2 * V_BOX;        // 128 output columns
+constexpr uint32_t Q_RES = QC * Q_CHUNK;       // 32 KB
+constexpr int V_STAGES = 2;
+// 227 KB per CTA covers static shared memory too: keep 4 KB for it
+constexpr uint32_t BUDGET = 227 * 1024 - 4096;
+constexpr int K_STAGES =
+    static_cast<int>((BUDGET - 1024 - Q_RES - V_STAGES * V_STAGE) / K_BLK);
+constexpr uint32_t SMEM = 1024 + Q_RES + V_STAGES * V_STAGE + K_STAGES * K_BLK;
+static_assert(K_STAGES >= 2, "too few key stages");
+static_assert(SMEM <= BUDGET, "shared-memory budget exceeded");
+constexpr uint32_t TMEM_COLS = 512;            // S/P buffers 0 and 1, then O
+constexpr uint32_t O_COL = 256;
+constexpr int kThreads = 384;                  // 4 role warps + 8 softmax warps
+constexpr int HK = BN / 2;                     // keys per softmax warp
+constexpr float kRescaleLog2 = 8.0f;
+
+template <bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, void* O, long long ldo, long long sO,
+                      int Nq, int Nk, int dv, int n_chunks, float scale_log2, int o_vec, int zq,
+                      int zk, int zv, int hook, unsigned int* err)
+{
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t k_full[K_STAGES];
+    __shared__ __align__(8) uint64_t k_empty[K_STAGES];
+    __shared__ __align__(8) uint64_t q_full;
+    __shared__ __align__(8) uint64_t v_full[V_STAGES];
+    __shared__ __align__(8) uint64_t v_empty[V_STAGES];
+    __shared__ __align__(8) uint64_t s_full[2];    // S of the buffer's block is in TMEM
+    __shared__ __align__(8) uint64_t p_full[2];    // P written over it (256 arrivals)
+    __shared__ __align__(8) uint64_t pv_done[2];   // the buffer's P V MMAs are complete
+    __shared__ __align__(8) uint64_t drain_s;
+    __shared__ __align__(8) uint64_t drain_o;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    __shared__ float red[2][2][BM];   // per-row partial maxima of the two halves, by buffer
+    __shared__ float lsum[2][BM];     // per-row partial normalisers of the two halves
+
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t q_res = base;
+    const uint32_t k_base = base + Q_RES;
+    const uint32_t v_base = k_base + K_STAGES * K_BLK;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int q0 = static_cast<int>(blockIdx.x) * BM;
+    const int bz = static_cast<int>(blockIdx.z);
+    const int n_kv = (Nk + BN - 1) / BN;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < K_STAGES; ++s) {
+            mbar_init(smem_u32(&k_full[s]), 1);
+            mbar_init(smem_u32(&k_empty[s]), 1);
+        }
+        for (int s = 0; s < V_STAGES; ++s) {
+            mbar_init(smem_u32(&v_full[s]), 1);
+            mbar_init(smem_u32(&v_empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&s_full[b]), 1);
+            mbar_init(smem_u32(&p_full[b]), 2 * BM);
+            mbar_init(smem_u32(&pv_done[b]), 1);
+        }
+        mbar_init(smem_u32(&q_full), 1);
+        mbar_init(smem_u32(&drain_s), 1);
+        mbar_init(smem_u32(&drain_o), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = tmem_slot;
+    // a softmax step waits for a whole block of MMAs; allow ~64 us per chunk
+    const uint32_t long_limit =
+        kSlowPolls + 64u * static_cast<uint32_t>(min(n_chunks + 8, 1 << 20));
+
+    if (warp == 0) {
+        // --------------------------------------------------- TMA: Q and K
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0, issued = 0;
+            const uint32_t qb = smem_u32(&q_full);
+            mbar_arrive_expect_tx(qb, static_cast<uint32_t>(n_chunks) * Q_CHUNK);
+            for (int c = 0; c < n_chunks; ++c)
+                tma_load_3d(q_res + c * Q_CHUNK, &tmQ, qb, c * DC, q0, bz * zq);
+            for (int t = 0; t < n_kv; ++t) {
+                if (!mbar_wait(smem_u32(&k_empty[s]), ph ^ 1u, &abort_flag, long_limit)) {
+                    abort_flag = 1;
+                    atomicOr(err, ERR_ATTENTION);
+                    break;
+                }
+                if (!(hook == 1 && t == 0)) {  // test hook: leave the first stage empty
+                    const uint32_t fb = smem_u32(&k_full[s]);
+                    mbar_arrive_expect_tx(fb, static_cast<uint32_t>(n_chunks) * K_CHUNK);
+                    for (int c = 0; c < n_chunks; ++c)
+                        tma_load_3d(k_base + s * K_BLK + c * K_CHUNK, &tmK, fb, c * DC, t * BN, bz * zk);
+                    ++issued;
+                }
+                if (++s == K_STAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            // wait for this thread's copies still in flight before leaving
+            for (uint32_t i = 0; i < min(issued, static_cast<uint32_t>(K_STAGES)); ++i) {
+                if (--s < 0) {
+                    s = K_STAGES - 1;
+                    ph ^= 1u;
+                }
+                if (!mbar_wait(smem_u32(&k_full[s]), ph, nullptr)) atomicOr(err, ERR_DRAIN);
+            }
+            if (!mbar_wait(qb, 0, nullptr)) atomicOr(err, ERR_DRAIN);
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // ------------------------------------------------------- TMA: V
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0, issued = 0;
+            for (int t = 0; t < n_kv; ++t) {
+                if (!mbar_wait(smem_u32(&v_empty[s]), ph ^ 1u, &abort_flag, long_limit)) {
+                    abort_flag = 1;
+                    atomicOr(err, ERR_ATTENTION);
+                    break;
+                }
+                const uint32_t fb = smem_u32(&v_full[s]);
+                const uint32_t sv = v_base + s * V_STAGE;
+                mbar_arrive_expect_tx(fb, V_STAGE);
+                tma_load_3d(sv, &tmV, fb, 0, t * BN, bz * zv);
+                tma_load_3d(sv + V_BOX, &tmV, fb, 64, t * BN, bz * zv);
+                ++issued;
+                if (++s == V_STAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            for (uint32_t i = 0; i < min(issued, static_cast<uint32_t>(V_STAGES)); ++i) {
+                if (--s < 0) {
+                    s = V_STAGES - 1;
+                    ph ^= 1u;
+                }
+                if (!mbar_wait(smem_u32(&v_full[s]), ph, nullptr)) atomicOr(err, ERR_DRAIN);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------ MMA issuer: S = Q K^T
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_f16_f32(BM, BN, false, false);
+            int ks = 0;
+            uint32_t kph = 0;
+            bool ok = mbar_wait(smem_u32(&q_full), 0, &abort_flag);
+            for (int t = 0; t < n_kv && ok; ++t) {
+                const int b = t & 1;
+                // buffer b held P_(t-2): reuse it once P_(t-2) V has completed
+                if (t >= 2 && !mbar_wait(smem_u32(&pv_done[b]), static_cast<uint32_t>(((t >> 1) - 1) & 1),
+                                         &abort_flag, long_limit)) {
+                    ok = false;
+                    break;
+                }
+                if (!mbar_wait(smem_u32(&k_full[ks]), kph, &abort_flag, long_limit)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_s = tmem_base + static_cast<uint32_t>(b * BN);
+                for (int c = 0; c < n_chunks; ++c) {
+                    // both operands K-major: 8-row groups 1024 B apart, +32 B per 16 of d
+                    const uint64_t ad = sdesc_sw128(q_res + c * Q_CHUNK, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(k_base + ks * K_BLK + c * K_CHUNK, 16, 1024);
+#pragma unroll
+                    for (int k = 0; k < DC / 16; ++k)
+                        umma_f16(d_s, ad + 2ull * k, bd + 2ull * k, idesc_s, (c | k) != 0 ? 1u : 0u);
+                }
+                umma_commit(smem_u32(&s_full[b]));
+                umma_commit(smem_u32(&k_empty[ks]));
+                if (++ks == K_STAGES) {
+                    ks = 0;
+                    kph ^= 1u;
+                }
+            }
+            if (!ok) {
+                abort_flag = 1;
+                atomicOr(err, ERR_ATTENTION);
+            }
+            // every MMA this thread issued must finish before TMEM is freed
+            umma_commit(smem_u32(&drain_s));
+            if (!mbar_wait(smem_u32(&drain_s), 0, nullptr)) atomicOr(err, ERR_DRAIN);
+        }
+        __syncwarp();
+    } else if (warp == 3) {
+        // ------------------------------------------ MMA issuer: O += P V
+        if (lane == 0) {
+            // A = P from TMEM (K-major), B = V from shared memory (MN-major)
+            constexpr uint32_t idesc_o = idesc_f16_f32(BM, 128, false, true);
+            int vs = 0;
+            uint32_t vph = 0;
+            bool ok = true;
+            for (int t = 0; t < n_kv; ++t) {
+                const int b = t & 1;
+                if (!mbar_wait(smem_u32(&p_full[b]), static_cast<uint32_t>((t >> 1) & 1), &abort_flag,
+                               long_limit) ||
+                    !mbar_wait(smem_u32(&v_full[vs]), vph, &abort_flag, long_limit)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // V: 64-column boxes 16 KB apart, 16 keys = 2048 B per step
+                const uint64_t bd = sdesc_sw128(v_base + vs * V_STAGE, V_BOX, 1024);
+                const uint32_t a_tm = tmem_base + static_cast<uint32_t>(b * BN);
+#pragma unroll
+                for (int k = 0; k < BN / 16; ++k)
+                    umma_f16_ts(tmem_base + O_COL, a_tm + 8u * k, bd + 128ull * k, idesc_o,
+                                (t | k) != 0 ? 1u : 0u);
+                umma_commit(smem_u32(&pv_done[b]));
+                umma_commit(smem_u32(&v_empty[vs]));
+                if (++vs == V_STAGES) {
+                    vs = 0;
+                    vph ^= 1u;
+                }
+            }
+            if (!ok) {
+                abort_flag = 1;
+                atomicOr(err, ERR_ATTENTION);
+            }
+            umma_commit(smem_u32(&drain_o));
+            if (!mbar_wait(smem_u32(&drain_o), 0, nullptr)) atomicOr(err, ERR_DRAIN);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------- softmax and output
+        // Two warps per TMEM lane quadrant: warp h of the pair takes keys
+        // h*64 .. h*64+63 of each block (and output columns h*64 ..); the
+        // pair agrees on each row's maximum (and, at the end, its sum)
+        // through shared memory and a 64-thread named barrier.
+        const int qd = warp & 3;          // TMEM lane quadrant
+        const int h = (warp - 4) >> 2;    // which half of the keys
+        const int r = qd * 32 + lane;     // this thread's query row
+        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(qd * 32) << 16);
+        const bool pos_scale = scale_log2 >= 0.0f;
+        float m_run = -INFINITY;          // running maximum, base-2 scaled logits
+        float l_run = 0.0f;               // this half's share of the running normaliser
+        bool ok = true;
+        // Every iteration passes exactly one pair barrier, also after a
+        // failed wait (the work is then skipped), so the two warps of a pair
+        // always meet; a failure raises the abort flag at once so that every
+        // other role's bounded waits end too.
+        auto fail = [&]() {
+            ok = false;
+            if (lane == 0) {
+                abort_flag = 1;
+                atomicOr(err, ERR_ATTENTION);
+            }
+        };
+        for (int t = 0; t < n_kv; ++t) {
+            const int b = t & 1;
+            const uint32_t s_col = static_cast<uint32_t>(b * BN);
+            uint32_t raw[HK];
+            float mine = 0.0f;
+            const int valid = min(BN, Nk - t * BN) - h * HK;
+            if (ok) {
+                const bool got = mbar_wait(smem_u32(&s_full[b]), static_cast<uint32_t>((t >> 1) & 1),
+                                           &abort_flag, long_limit);
+                if (!__all_sync(0xffffffffu, got)) fail();
+            }
+            if (ok) {
+                tc_fence_after();
+                tmem_ld_32x32b_x64(t_lane + s_col + static_cast<uint32_t>(h * HK), raw);
+                tmem_ld_wait();
+                // keys past Nk (zero-filled by TMA) are masked; only the last
+                // block can have them
+                if (valid < HK) {
+#pragma unroll
+                    for (int j = 0; j < HK; ++j)
+                        if (j >= valid) raw[j] = __float_as_uint(pos_scale ? -INFINITY : INFINITY);
+                }
+                // the extreme raw score of this half, in four chains
+                float mc[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) mc[c] = __uint_as_float(raw[c]);
+                if (pos_scale) {
+#pragma unroll
+                    for (int j = 4; j < HK; ++j) mc[j & 3] = fmaxf(mc[j & 3], __uint_as_float(raw[j]));
+                } else {
+#pragma unroll
+                    for (int j = 4; j < HK; ++j) mc[j & 3] = fminf(mc[j & 3], __uint_as_float(raw[j]));
+                }
+                mine = pos_scale ? fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]))
+                                 : fminf(fminf(mc[0], mc[1]), fminf(mc[2], mc[3]));
+            }
+            // the exchange also orders both halves' score loads before either
+            // half writes P over the buffer's first 64 columns
+            red[b][h][r] = mine;
+            named_bar_sync(1 + qd, 64);
+            const float other = red[b][h ^ 1][r];
+            if (!ok) continue;
+
+            const float mraw = pos_scale ? fmaxf(mine, other) : fminf(mine, other);
+            const float mx = mraw * scale_log2;
+            const bool raise = mx > m_run + kRescaleLog2;
+            float alpha = 1.0f;
+            if (raise) {
+                alpha = ex2_approx(m_run - mx);  // 0 for the first block
+                l_run *= alpha;
+                m_run = mx;
+            }
+            const float neg_m = -m_run;
+
+            // P = 2^(s * scale * log2 e - m) as fp16 pairs: this half's 64
+            // keys go to columns h*32 .. h*32+31 of the buffer
+            uint32_t pw[HK / 2];
+            float l0 = 0.0f, l1 = 0.0f;
+            auto make_p = [&](auto masked) {
+#pragma unroll
+                for (int j = 0; j < HK; j += 2) {
+                    float a0 = fmaf(__uint_as_float(raw[j]), scale_log2, neg_m);
+                    float a1 = fmaf(__uint_as_float(raw[j + 1]), scale_log2, neg_m);
+                    if constexpr (decltype(masked)::value) {
+                        if (j >= valid) a0 = -INFINITY;
+                        if (j + 1 >= valid) a1 = -INFINITY;
+                    }
+                    const __half2 v2 = __floats2half2_rn(ex2_approx(a0), ex2_approx(a1));
+                    // the normaliser sums the weights the MMA uses: the fp16 ones
+                    const float2 r2 = __half22float2(v2);
+                    l0 += r2.x;
+                    l1 += r2.y;
+                    pw[j / 2] = *reinterpret_cast<const uint32_t*>(&v2);
+                }
+            };
+            if (valid < HK) make_p(std::true_type{});
+            else make_p(std::false_type{});
+            l_run += l0 + l1;
+            tmem_st_32x32b_x32(t_lane + s_col + static_cast<uint32_t>(h * (HK / 2)), pw);
+            if (t > 0 && __any_sync(0xffffffffu, raise)) {
+                // then this half of O *= alpha (1 in rows that kept their
+                // maximum), once P_(t-1) V has completed; P_t V waits for
+                // this block's P
+                const int u = t - 1;
+                const bool got_o = mbar_wait(smem_u32(&pv_done[u & 1]), static_cast<uint32_t>((u >> 1) & 1),
+                                             &abort_flag, long_limit);
+                if (!__all_sync(0xffffffffu, got_o)) {
+                    tmem_st_wait();
+                    fail();
+                    continue;
+                }
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < HK; c += 32) {
+                    const uint32_t col = O_COL + static_cast<uint32_t>(h * HK + c);
+                    uint32_t o[32];
+                    tmem_ld_32x32b_x32(t_lane + col, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                    tmem_st_32x32b_x32(t_lane + col, o);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&p_full[b]));
+        }
+        if (ok && n_kv > 0) {
+            // the last block's MMAs complete O
+            const int u = n_kv - 1;
+            const bool got = mbar_wait(smem_u32(&pv_done[u & 1]), static_cast<uint32_t>((u >> 1) & 1),
+                                       &abort_flag, long_limit);
+            if (!__all_sync(0xffffffffu, got)) fail();
+        }
+        // both halves of the row's normaliser (every softmax thread reaches
+        // this barrier exactly once)
+        lsum[h][r] = l_run;
+        named_bar_sync(1 + qd, 64);
+        const float l_row = lsum[0][r] + lsum[1][r];
+        if (ok) {
+            tc_fence_after();
+            const float inv_l = 1.0f / l_row;
+            const int m = q0 + r;
+            void* Ob = batch_ptr(O, bz, sO, OUT_F32 ? 4 : 2);
+#pragma unroll 1
+            for (int c = 0; c < HK; c += 32) {
+                const int n = h * HK + c;
+                uint32_t o[32];
+                tmem_ld_32x32b_x32(t_lane + O_COL + static_cast<uint32_t>(n), o);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * inv_l);
+                if (m < Nq && n < dv) store_chunk<OUT_F32>(Ob, ldo, m, n, dv, o, o_vec != 0);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+std::mutex g_attr_mu;
+bool g_attr_set[64][2];
+
+template <bool OUT_F32>
+cudaError_t launch_cfg(const AttnArgs& a)
+{
+    auto kernel = attention_fwd2_kernel<OUT_F32>;
+    {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        std::lock_guard<std::mutex> lock(g_attr_mu);
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        if (!g_attr_set[dev][OUT_F32 ? 1 : 0]) {
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(SMEM));
+            if (e != cudaSuccess) return e;
+            g_attr_set[dev][OUT_F32 ? 1 : 0] = true;
+        }
+    }
+    CUtensorMap tq, tk, tv;
+    if (!encode_tmap(&tq, a.Q, 2, static_cast<uint64_t>(a.d), static_cast<uint64_t>(a.Nq),
+                     static_cast<uint64_t>(a.ldq), a.batch, a.sQ, DC, BM) ||
+        !encode_tmap(&tk, a.K, 2, static_cast<uint64_t>(a.d), static_cast<uint64_t>(a.Nk),
+                     static_cast<uint64_t>(a.ldk), a.batch, a.sK, DC, BN) ||
+        !encode_tmap(&tv, a.V, 2, static_cast<uint64_t>(a.dv), static_cast<uint64_t>(a.Nk),
+                     static_cast<uint64_t>(a.ldv), a.batch, a.sV, 64, BN))
+        return cudaErrorInvalidValue;
+    const size_t es = OUT_F32 ? 4 : 2;
+    const int o_vec = (reinterpret_cast<uintptr_t>(a.O) % 16 == 0) &&
+                      ((static_cast<size_t>(a.ldo) * es) % 16 == 0) &&
+                      ((static_cast<size_t>(a.sO) * es) % 16 == 0);
+    const dim3 grid((a.Nq + BM - 1) / BM, 1, a.batch);
+    if (grid.z > 65535u) return cudaErrorInvalidConfiguration;
+    const float scale_log2 = a.scale * 1.4426950408889634f;  // log2(e)
+    const int n_chunks = (a.d + DC - 1) / DC;
+    kernel<<<grid, kThreads, SMEM, a.stream>>>(tq, tk, tv, a.O, a.ldo, a.sO, a.Nq, a.Nk, a.dv,
+                                               n_chunks, scale_log2, o_vec, a.sQ != 0, a.sK != 0,
+                                               a.sV != 0, a.hook, a.err);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool attention_tmem_p_serves(int d, int dv)
+{
+    return d >= 1 && d <= DC * QC && dv >= 1 && dv <= 128;
+}
+
+cudaError_t launch_attention_tmem_p(const AttnArgs& a)
+{
+    if (!attention_tmem_p_serves(a.d, a.dv) || a.Nk < 1) return cudaErrorInvalidValue;
+    return a.out_f32 ? launch_cfg<true>(a) : launch_cfg<false>(a);
+}
+
+}  // namespace tg

@@ -42,6 +42,7 @@ std::atomic<int> g_force_path{0};
 std::atomic<int> g_test_hook{0};
 std::atomic<int> g_force_bn{0};
 std::atomic<int> g_force_group{0};
+std::atomic<int> g_force_attn{0};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 tg_status device_state(DeviceState** out)
@@ -432,7 +433,11 @@ tg_status tg_attention_ws(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int6
     const size_t need = tg::attention_ws_bytes(static_cast<int>(batch), static_cast<int>(Nq),
                                                static_cast<int>(Nk), static_cast<int>(dv),
                                                ds->num_sms);
-    const bool split = need > 0 && workspace != nullptr && workspace_bytes >= need;
+    const bool ws_ok = need > 0 && workspace != nullptr && workspace_bytes >= need;
+    const int choice = tg::attention_kernel_choice(
+        static_cast<int>(batch), static_cast<int>(Nq), static_cast<int>(Nk), static_cast<int>(d),
+        static_cast<int>(dv), ds->num_sms, ws_ok, g_force_attn.load(std::memory_order_relaxed));
+    const bool split = choice == 2;
     if (split) {
         u128 w0 = static_cast<u128>(reinterpret_cast<uintptr_t>(workspace));
         u128 w1 = w0 + need;
@@ -467,6 +472,7 @@ tg_status tg_attention_ws(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int6
         a.n_split = tg::attention_splits(a.batch, a.Nq, a.Nk, a.dv, ds->num_sms);
         a.ws = workspace;
     }
+    a.tmem_p = choice == 3;
     return tg::launch_attention(a) == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 
@@ -510,6 +516,31 @@ size_t tg_attention_workspace_size(int64_t batch, int64_t Nq, int64_t Nk, int64_
     if (device_state(&ds) != TG_OK) return 0;
     return tg::attention_ws_bytes(static_cast<int>(batch), static_cast<int>(Nq),
                                   static_cast<int>(Nk), static_cast<int>(dv), ds->num_sms);
+}
+
+int tg_attention_kernel(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                        int split_allowed)
+{
+    if (batch <= 0 || Nq <= 0 || Nk <= 0 || d <= 0 || dv <= 0) return 0;
+    if (Nq > kMaxDim || Nk > kMaxDim || d > kMaxDim || dv > 65535LL * 128 || batch > kMaxBatch)
+        return 0;
+    DeviceState* ds = nullptr;
+    if (device_state(&ds) != TG_OK) return 0;
+    const bool ws_ok = split_allowed != 0 &&
+                       tg::attention_ws_bytes(static_cast<int>(batch), static_cast<int>(Nq),
+                                              static_cast<int>(Nk), static_cast<int>(dv),
+                                              ds->num_sms) > 0;
+    return tg::attention_kernel_choice(static_cast<int>(batch), static_cast<int>(Nq),
+                                       static_cast<int>(Nk), static_cast<int>(d),
+                                       static_cast<int>(dv), ds->num_sms, ws_ok,
+                                       g_force_attn.load(std::memory_order_relaxed));
+}
+
+tg_status tg_attention_force_kernel(int kernel)
+{
+    if (!(kernel == 0 || kernel == 1 || kernel == 3)) return TG_ERR_INVALID_ARG;
+    g_force_attn.store(kernel, std::memory_order_relaxed);
+    return TG_OK;
 }
 
 tg_status tg_gemm_check(tg_stream_t stream)

@@ -146,6 +146,9 @@ struct AttnArgs {
     // (attention_ws_bytes of them) and merges them in a second kernel
     int n_split = 1;
     void* ws = nullptr;
+    // the kernel that keeps P in tensor memory (attention_fwd2.cu); needs
+    // d <= 128, dv <= 128 and no key split
+    bool tmem_p = false;
 };
 
 cudaError_t launch_attention(const AttnArgs& a);
@@ -158,6 +161,16 @@ long long attention_ws_o_floats(int batch, int Nq, int dv, int n_split);
 // The current device's address of the file-scope attention scratch (looked
 // up once per device) and its size; nullptr on failure.
 void* attention_static_scratch(size_t* bytes);
+// The forward kernel that keeps P in tensor memory: whether it serves these
+// head sizes, and its launch.
+bool attention_tmem_p_serves(int d, int dv);
+cudaError_t launch_attention_tmem_p(const AttnArgs& a);
+// Which forward kernel a call runs: 1 the general kernel (any d, dv), 2 the
+// same with the keys split over CTAs (only when `split_ok`: the caller's
+// workspace holds the partials), 3 the kernel that keeps P in tensor memory
+// (d <= 128, dv <= 128).  `forced` is 0 (automatic), 1 or 3.
+int attention_kernel_choice(int batch, int Nq, int Nk, int d, int dv, int num_sms, bool split_ok,
+                            int forced);
 
 // Tile width the main kernel uses for this problem (64, 128 or 256).
 int main_tile_n(int M, int N, int batch, int num_sms);
