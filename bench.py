@@ -56,9 +56,20 @@ KERNEL_SOURCES = ["tiled_gemm_tg_gb300/csrc/gemm_tc2.cu", "tiled_gemm_tg_gb300/c
                   "tiled_gemm_tg_gb300/csrc/tc_common.cuh", "tiled_gemm_tg_gb300/csrc/tg_internal.h"]
 
 
-def kernel_hash() -> str:
+ATTN_KERNEL_SOURCES = ["tiled_gemm_tg_gb300/csrc/attention_fwd2.cu", "tiled_gemm_tg_gb300/csrc/ptx.cuh",
+                       "tiled_gemm_tg_gb300/csrc/tc_common.cuh", "tiled_gemm_tg_gb300/csrc/tg_internal.h"]
+
+# DRAM traffic per launch of the attention kernel that keeps P in tensor
+# memory, from one ncu capture, valid while its sources hash the same
+ATTN_NCU_TRAFFIC = {
+    # profiles/attention_fwd2_16x4096x128.md: 50.4 MB read + 0.5 MB written
+    "attn_16x4096x128": {"bytes": 50953728, "kernel_hash": "80416652c795028d"},
+}
+
+
+def kernel_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
+    for p in sources or KERNEL_SOURCES:
         with open(os.path.join(ROOT, p), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -407,9 +418,11 @@ def main_attention(args, w):
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     achieved = flops / (kern_ms * 1e-3) / 1e12
     alg_bytes = w.algorithmic_bytes()
+    rec = ATTN_NCU_TRAFFIC.get(w.name) if kern == 3 else None
+    attn_traffic = rec["bytes"] if rec and rec.get("kernel_hash") == kernel_hash(ATTN_KERNEL_SOURCES) else None
     roofline = {
         "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-        "frac": achieved / peak, "traffic": None, "kernel": kern_name,
+        "frac": achieved / peak, "traffic": attn_traffic, "kernel": kern_name,
         "kernel_ms": kern_ms,
         "peak_source": f"{peak_src} bf16 burst (torch.matmul 8192^3) x 1.0 fp16/bf16 nominal ratio",
         "flop_per_byte": flops / alg_bytes, "algorithmic_bytes": alg_bytes,

@@ -9,7 +9,7 @@
 // one is laid out for the common head sizes.
 //
 // GB300 design.  A CTA owns 128 query rows and walks the keys in blocks of
-// 128, with two TMEM score buffers b = t % 2:
+// 128, with three TMEM score buffers b = t % 3:
 //   S_t = Q K_t^T      tcgen05.mma M=128 N=128, K = d (Q resident, the key
 //                      block one TMA stage), into TMEM columns 128b..128b+127;
 //   P_t = exp2(S_t * scale * log2 e - m)   two threads per query row (64
@@ -18,10 +18,11 @@
 //                      columns;
 //   O += P_t V_t       tcgen05.mma with A = P_t from TMEM, B = V_t from shared
 //                      memory (MN-major), accumulating in TMEM columns
-//                      256 .. 383.
-// S_(t+1) goes to the other buffer, so the tensor core computes it while the
-// softmax turns S_t into P_t; S_(t+2) reuses buffer b once P_t V_t has
-// completed.  P never leaves tensor memory: no shared-memory round trip and
+//                      384 .. 511.
+// S_(t+1) goes to the next buffer, so the tensor core computes it while the
+// softmax turns S_t into P_t; S_(t+3) reuses buffer b once P_t V_t has
+// completed (with two buffers, S_(t+2) waiting on P_t V_t put the softmax,
+// the P V MMAs and the next S MMAs of a buffer on one serial chain).  P never leaves tensor memory: no shared-memory round trip and
 // no proxy fence between the softmax and the MMA.  Each tcgen05.commit ends
 // a whole block of MMAs: a commit after a few MMAs leaves the pipe idle.
 // The running maximum is raised only when a block's maximum exceeds it by
@@ -61,15 +62,18 @@ constexpr uint32_t V_BOX = BN * 128;           // [128 keys][64 columns] fp16, 1
 constexpr uint32_t V_STAGE = 2 * V_BOX;        // 128 output columns
 constexpr uint32_t Q_RES = QC * Q_CHUNK;       // 32 KB
 constexpr int V_STAGES = 2;
-// 227 KB per CTA covers static shared memory too: keep 4 KB for it
-constexpr uint32_t BUDGET = 227 * 1024 - 4096;
+// 227 KB per CTA covers static shared memory too (barriers and the row
+// exchange arrays, about 4.3 KB): keep 8 KB for it
+constexpr uint32_t BUDGET = 227 * 1024 - 8192;
 constexpr int K_STAGES =
     static_cast<int>((BUDGET - 1024 - Q_RES - V_STAGES * V_STAGE) / K_BLK);
 constexpr uint32_t SMEM = 1024 + Q_RES + V_STAGES * V_STAGE + K_STAGES * K_BLK;
 static_assert(K_STAGES >= 2, "too few key stages");
 static_assert(SMEM <= BUDGET, "shared-memory budget exceeded");
-constexpr uint32_t TMEM_COLS = 512;            // S/P buffers 0 and 1, then O
-constexpr uint32_t O_COL = 256;
+constexpr int NBUF = 3;                        // TMEM score buffers
+constexpr uint32_t TMEM_COLS = 512;            // S/P buffers 0..2, then O
+constexpr uint32_t O_COL = NBUF * BN;
+static_assert(O_COL + 128 <= TMEM_COLS, "tensor memory exceeded");
 constexpr int kThreads = 384;                  // 4 role warps + 8 softmax warps
 constexpr int HK = BN / 2;                     // keys per softmax warp
 constexpr float kRescaleLog2 = 8.0f;
@@ -87,14 +91,14 @@ attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
     __shared__ __align__(8) uint64_t q_full;
     __shared__ __align__(8) uint64_t v_full[V_STAGES];
     __shared__ __align__(8) uint64_t v_empty[V_STAGES];
-    __shared__ __align__(8) uint64_t s_full[2];    // S of the buffer's block is in TMEM
-    __shared__ __align__(8) uint64_t p_full[2];    // P written over it (256 arrivals)
-    __shared__ __align__(8) uint64_t pv_done[2];   // the buffer's P V MMAs are complete
+    __shared__ __align__(8) uint64_t s_full[NBUF]; // S of the buffer's block is in TMEM
+    __shared__ __align__(8) uint64_t p_full[NBUF]; // P written over it (256 arrivals)
+    __shared__ __align__(8) uint64_t pv_done[NBUF];  // the buffer's P V MMAs are complete
     __shared__ __align__(8) uint64_t drain_s;
     __shared__ __align__(8) uint64_t drain_o;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
-    __shared__ float red[2][2][BM];   // per-row partial maxima of the two halves, by buffer
+    __shared__ float red[NBUF][2][BM];  // per-row partial maxima of the two halves, by buffer
     __shared__ float lsum[2][BM];     // per-row partial normalisers of the two halves
 
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -116,7 +120,7 @@ attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
             mbar_init(smem_u32(&v_full[s]), 1);
             mbar_init(smem_u32(&v_empty[s]), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NBUF; ++b) {
             mbar_init(smem_u32(&s_full[b]), 1);
             mbar_init(smem_u32(&p_full[b]), 2 * BM);
             mbar_init(smem_u32(&pv_done[b]), 1);
@@ -221,10 +225,10 @@ attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
             uint32_t kph = 0;
             bool ok = mbar_wait(smem_u32(&q_full), 0, &abort_flag);
             for (int t = 0; t < n_kv && ok; ++t) {
-                const int b = t & 1;
-                // buffer b held P_(t-2): reuse it once P_(t-2) V has completed
-                if (t >= 2 && !mbar_wait(smem_u32(&pv_done[b]), static_cast<uint32_t>(((t >> 1) - 1) & 1),
-                                         &abort_flag, long_limit)) {
+                const int b = t % NBUF;
+                // buffer b held P_(t-NBUF): reuse it once that block's P V has completed
+                if (t >= NBUF && !mbar_wait(smem_u32(&pv_done[b]), static_cast<uint32_t>((t / NBUF - 1) & 1),
+                                            &abort_flag, long_limit)) {
                     ok = false;
                     break;
                 }
@@ -267,8 +271,8 @@ attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
             uint32_t vph = 0;
             bool ok = true;
             for (int t = 0; t < n_kv; ++t) {
-                const int b = t & 1;
-                if (!mbar_wait(smem_u32(&p_full[b]), static_cast<uint32_t>((t >> 1) & 1), &abort_flag,
+                const int b = t % NBUF;
+                if (!mbar_wait(smem_u32(&p_full[b]), static_cast<uint32_t>((t / NBUF) & 1), &abort_flag,
                                long_limit) ||
                     !mbar_wait(smem_u32(&v_full[vs]), vph, &abort_flag, long_limit)) {
                     ok = false;
@@ -323,13 +327,13 @@ attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
             }
         };
         for (int t = 0; t < n_kv; ++t) {
-            const int b = t & 1;
+            const int b = t % NBUF;
             const uint32_t s_col = static_cast<uint32_t>(b * BN);
             uint32_t raw[HK];
             float mine = 0.0f;
             const int valid = min(BN, Nk - t * BN) - h * HK;
             if (ok) {
-                const bool got = mbar_wait(smem_u32(&s_full[b]), static_cast<uint32_t>((t >> 1) & 1),
+                const bool got = mbar_wait(smem_u32(&s_full[b]), static_cast<uint32_t>((t / NBUF) & 1),
                                            &abort_flag, long_limit);
                 if (!__all_sync(0xffffffffu, got)) fail();
             }
@@ -406,7 +410,7 @@ attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
                 // maximum), once P_(t-1) V has completed; P_t V waits for
                 // this block's P
                 const int u = t - 1;
-                const bool got_o = mbar_wait(smem_u32(&pv_done[u & 1]), static_cast<uint32_t>((u >> 1) & 1),
+                const bool got_o = mbar_wait(smem_u32(&pv_done[u % NBUF]), static_cast<uint32_t>((u / NBUF) & 1),
                                              &abort_flag, long_limit);
                 if (!__all_sync(0xffffffffu, got_o)) {
                     tmem_st_wait();
@@ -432,7 +436,7 @@ attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
         if (ok && n_kv > 0) {
             // the last block's MMAs complete O
             const int u = n_kv - 1;
-            const bool got = mbar_wait(smem_u32(&pv_done[u & 1]), static_cast<uint32_t>((u >> 1) & 1),
+            const bool got = mbar_wait(smem_u32(&pv_done[u % NBUF]), static_cast<uint32_t>((u / NBUF) & 1),
                                        &abort_flag, long_limit);
             if (!__all_sync(0xffffffffu, got)) fail();
         }
