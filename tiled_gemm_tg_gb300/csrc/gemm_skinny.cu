@@ -60,10 +60,13 @@ struct SkinnyCfg {
     static_assert(RED_BYTES <= STAGES * STAGE, "reduction buffer must fit in the stages");
 };
 
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr)
+__device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t cluster_addr)
 {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
     return v;
 }
 
@@ -233,22 +236,42 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     cluster_sync();
 
     {
-        const int span = BNT / split;  // rows n this CTA reduces
+        // rows n this CTA reduces, four at a time: every CTA's partial of the
+        // four is loaded (16 bytes each, all loads in flight together) before
+        // they are added, in rank order
+        const int span = BNT / split;
+        const int quads = span / 4;
         const uint32_t red_local = smem_u32(red);
-        for (int idx = threadIdx.x; idx < span * M; idx += kThreads) {
-            const int m = idx / span;
-            const int nl = rank * span + (idx - m * span);
-            const int n = n0 + nl;
-            if (n >= N) continue;
+        for (int idx = threadIdx.x; idx < quads * M; idx += kThreads) {
+            const int m = idx / quads;
+            const int nl = rank * span + 4 * (idx - m * quads);
+            if (n0 + nl >= N) continue;
             const uint32_t off = static_cast<uint32_t>((m * BNT + nl) * 4);
-            float sum = 0.0f;
-            for (int r = 0; r < split; ++r)
-                sum += ld_dsmem_f32(mapa_shared(red_local + off, static_cast<uint32_t>(r)));
-            if (epi.on) sum = epilogue_elem<OUT_F32>(sum, m, n, epi);
-            if constexpr (OUT_F32)
-                static_cast<float*>(Cb)[static_cast<long long>(m) * ldc + n] = sum;
-            else
-                static_cast<__half*>(Cb)[static_cast<long long>(m) * ldc + n] = __float2half_rn(sum);
+            float4 part[kMaxSplit];
+#pragma unroll
+            for (int r = 0; r < kMaxSplit; ++r)
+                if (r < split) part[r] = ld_dsmem_f32x4(mapa_shared(red_local + off, static_cast<uint32_t>(r)));
+            float sum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int r = 0; r < kMaxSplit; ++r) {
+                if (r < split) {
+                    sum[0] += part[r].x;
+                    sum[1] += part[r].y;
+                    sum[2] += part[r].z;
+                    sum[3] += part[r].w;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int n = n0 + nl + j;
+                if (n >= N) break;
+                float y = sum[j];
+                if (epi.on) y = epilogue_elem<OUT_F32>(y, m, n, epi);
+                if constexpr (OUT_F32)
+                    static_cast<float*>(Cb)[static_cast<long long>(m) * ldc + n] = y;
+                else
+                    static_cast<__half*>(Cb)[static_cast<long long>(m) * ldc + n] = __float2half_rn(y);
+            }
         }
     }
 
