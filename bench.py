@@ -761,6 +761,16 @@ def main():
                                                b_cpu[0] if NB > 1 else b_cpu, args.cpu_seconds)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": nt, "kind": "oracle",
                "sample": f"{rows} of {M} rows of C (full N={N}, K={K}), {secs:.1f} s"}
+        # small products: the whole product on one core as well
+        if 2.0 * M * N * K <= 4.4e9:
+            import oracle
+            a1 = host_array(a_cpu[0] if NB > 1 else a_cpu)
+            b1 = host_array(b_cpu[0] if NB > 1 else b_cpu)
+            t1 = time.perf_counter()
+            oracle.gemm(a1, b1, nthreads=1)
+            s1 = time.perf_counter() - t1
+            cpu["single_thread"] = {"value": 2.0 * M * N * K / s1 / 1e12, "unit": "TFLOP/s",
+                                    "sample": f"all of C, one thread, {s1:.2f} s"}
 
     if rank == 0:
         line = {
