@@ -193,6 +193,25 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, ws: int, device) -> float:
+    """The largest x over all ranks of the process group (x itself on one
+    rank): the job is as slow as its slowest replica."""
+    if ws <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank_step: float, ws: int, steps: int, elapsed_ms: float) -> float:
+    """Whole-job throughput in tera-units per second: the units every rank
+    processed over `steps` steps, divided by the slowest rank's time."""
+    return ws * units_per_rank_step * steps / (elapsed_ms * 1e-3) / 1e12
+
+
 def run_reference(args, w):
     """The reference arm: the CPU oracle, timed on the host's cores."""
     ws, rank, _ = dist_env()
@@ -399,12 +418,9 @@ def main_attention(args, w):
     kern_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
     if tg.tg_gemm_check(sh) != tg.TG_OK:
         raise RuntimeError("a kernel abandoned a bounded wait during the timed region")
-    if ws > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, ws, dev)
     flops = float(w.flops)
-    value = ws * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
+    value = job_throughput(flops, ws, args.steps, elapsed_ms)
 
     # end to end: Q, K, V in from pinned host memory, O out, every step
     e2e_steps = args.e2e_steps or max(3, min(args.steps, 20))
@@ -414,6 +430,8 @@ def main_attention(args, w):
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        torch.distributed.barrier()
     e0.record(stream)
     for _ in range(e2e_steps):
         qd.copy_(qh, non_blocking=True)
@@ -426,7 +444,8 @@ def main_attention(args, w):
     e2e_ms = e0.elapsed_time(e1)
     if tg.tg_gemm_check(sh) != tg.TG_OK:
         raise RuntimeError("a kernel abandoned a bounded wait during the e2e region")
-    e2e_value = ws * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e2e_ms, ws, dev)
+    e2e_value = job_throughput(flops, ws, e2e_steps, e2e_ms)
     sampler.stop()
     clocks = sampler.summary(host_t0, host_t1)
 
@@ -639,13 +658,9 @@ def main():
     if tg.tg_gemm_check(sh) != tg.TG_OK:
         raise RuntimeError("a kernel abandoned a bounded wait during the timed region")
 
-    if ws > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-
+    elapsed_ms = max_over_ranks(elapsed_ms, ws, dev)
     flops = 2.0 * NB * M * N * K
-    value = ws * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
+    value = job_throughput(flops, ws, args.steps, elapsed_ms)
 
     # --- end to end through the C ABI from pinned host buffers.  Every step
     # copies its A and B in, runs tg_gemm and copies C out; steps are
@@ -702,11 +717,8 @@ def main():
     e2e_ms = e0.elapsed_time(e1)
     if tg.tg_gemm_check(s_mm.cuda_stream) != tg.TG_OK:
         raise RuntimeError("a kernel abandoned a bounded wait during the e2e region")
-    if ws > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = ws * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e2e_ms, ws, dev)
+    e2e_value = job_throughput(flops, ws, e2e_steps, e2e_ms)
     ein = a_cpu.element_size()
     h2d = NB * (M * K + K * N) * ein + (M * N * out_es if use_d else 0) + (
         N * 4 if use_bias else 0)
