@@ -422,24 +422,49 @@ def main_attention(args, w):
     flops = float(w.flops)
     value = job_throughput(flops, ws, args.steps, elapsed_ms)
 
-    # end to end: Q, K, V in from pinned host memory, O out, every step
+    # end to end: Q, K, V in from pinned host memory, O out, every step;
+    # steps are pipelined over three streams (H2D, attention, D2H) and two
+    # device buffer sets, so step i's transfers overlap the kernels of steps
+    # i-1 and i+1
     e2e_steps = args.e2e_steps or max(3, min(args.steps, 20))
     qh, kh, vh = q_cpu.pin_memory(), k_cpu.pin_memory(), v_cpu.pin_memory()
-    oh = torch.empty((B, Nq, dv), dtype=out_dt).pin_memory()
-    qd, kd, vd, od = sets[0]
+    oh = [torch.empty((B, Nq, dv), dtype=out_dt).pin_memory() for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = {name: [torch.cuda.Event() for _ in range(2)] for name in ("in", "mm", "out")}
+    started = [False, False]
+
+    def e2e_step(i):
+        slot = i % 2
+        qd, kd, vd, od = sets[slot]
+        if started[slot]:
+            s_in.wait_event(ev["mm"][slot])  # the slot's previous call has read Q, K, V
+        with torch.cuda.stream(s_in):
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+        ev["in"][slot].record(s_in)
+        stream.wait_event(ev["in"][slot])
+        if started[slot]:
+            stream.wait_event(ev["out"][slot])  # the slot's previous O has been read out
+        call(qd, kd, vd, od, sh)
+        ev["mm"][slot].record(stream)
+        s_out.wait_event(ev["mm"][slot])
+        with torch.cuda.stream(s_out):
+            oh[slot].copy_(od, non_blocking=True)
+        ev["out"][slot].record(s_out)
+        started[slot] = True
+
+    for i in range(2):
+        e2e_step(i)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     if ws > 1:
         torch.distributed.barrier()
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        qd.copy_(qh, non_blocking=True)
-        kd.copy_(kh, non_blocking=True)
-        vd.copy_(vh, non_blocking=True)
-        call(qd, kd, vd, od, sh)
-        oh.copy_(od, non_blocking=True)
-    e1.record(stream)
+    e0.record(s_in)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e1.record(s_out)  # after the last D2H, which follows every earlier step's work
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
     if tg.tg_gemm_check(sh) != tg.TG_OK:
@@ -489,8 +514,8 @@ def main_attention(args, w):
             "clocks": clocks,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": B * (Nq * d + Nk * (d + dv)) * 2,
-                    "d2h_bytes_per_step": B * Nq * dv * oh.element_size(), "steps": e2e_steps,
-                    "pipeline": "H2D / tg_attention / D2H on one stream"},
+                    "d2h_bytes_per_step": B * Nq * dv * oh[0].element_size(), "steps": e2e_steps,
+                    "pipeline": "H2D / tg_attention / D2H on three streams, two device buffer sets"},
             "gpu_launches": args.steps * (2 if kern == 2 else 1),  # + the combine kernel
             "roofline": roofline,
             "cpu_baseline": cpu,
