@@ -9,24 +9,26 @@
 // one is laid out for the common head sizes.
 //
 // GB300 design.  A CTA owns 128 query rows and walks the keys in blocks of
-// 128, with three TMEM score buffers b = t % 3:
+// 128, with two TMEM score buffers b = t % 2:
 //   S_t = Q K_t^T      tcgen05.mma M=128 N=128, K = d (Q resident, the key
 //                      block one TMA stage), into TMEM columns 128b..128b+127;
 //   P_t = exp2(S_t * scale * log2 e - m)   two threads per query row (64
 //                      scores each, one tcgen05.ld) agree on the row maximum
 //                      and write P as fp16 pairs over the first 64 of those
 //                      columns;
-//   O += P_t V_t       tcgen05.mma with A = P_t from TMEM, B = V_t from shared
-//                      memory (MN-major), accumulating in TMEM columns
-//                      384 .. 511.
-// S_(t+1) goes to the next buffer, so the tensor core computes it while the
-// softmax turns S_t into P_t; S_(t+3) reuses buffer b once P_t V_t has
-// completed (with two buffers, S_(t+2) waiting on P_t V_t put the softmax,
-// the P V MMAs and the next S MMAs of a buffer on one serial chain).  P never leaves tensor memory: no shared-memory round trip and
+//   [O | L] += P_t [V_t | 1]   tcgen05.mma M=128 N=144 with A = P_t from
+//                      TMEM, B = V_t from shared memory (MN-major) followed
+//                      by a box of ones, accumulating in TMEM columns 256 ..
+//                      399: columns 128.. of the product are the normaliser
+//                      L = sum_k p_k of exactly the fp16 weights the MMA
+//                      used, so the softmax threads never sum P themselves.
+// S_(t+1) goes to the other buffer, so the tensor core computes it while the
+// softmax turns S_t into P_t; S_(t+2) reuses buffer b once P_t V_t has
+// completed.  P never leaves tensor memory: no shared-memory round trip and
 // no proxy fence between the softmax and the MMA.  Each tcgen05.commit ends
 // a whole block of MMAs: a commit after a few MMAs leaves the pipe idle.
 // The running maximum is raised only when a block's maximum exceeds it by
-// more than 8 (base 2); then the row of O (in TMEM) and L are scaled by
+// more than 8 (base 2); then the row of [O | L] (in TMEM) is scaled by
 // 2^(m_old - m_new) before P_t V_t is issued.
 //
 // Warp roles (384 threads): 0 TMA for Q (once) and K, 1 TMEM allocation and
@@ -59,7 +61,9 @@ constexpr uint32_t Q_CHUNK = BM * DC * 2;      // 16 KB
 constexpr uint32_t K_CHUNK = BN * DC * 2;      // 16 KB
 constexpr uint32_t K_BLK = QC * K_CHUNK;       // a key block: one stage, one release
 constexpr uint32_t V_BOX = BN * 128;           // [128 keys][64 columns] fp16, 16 KB
-constexpr uint32_t V_STAGE = 2 * V_BOX;        // 128 output columns
+// a V stage: two boxes of V (128 output columns) and a box of ones, so that
+// the P V MMA's columns 128.. accumulate the normaliser sum_k p_k
+constexpr uint32_t V_STAGE = 3 * V_BOX;
 constexpr uint32_t Q_RES = QC * Q_CHUNK;       // 32 KB
 constexpr int V_STAGES = 2;
 // 227 KB per CTA covers static shared memory too (barriers and the row
@@ -70,10 +74,11 @@ constexpr int K_STAGES =
 constexpr uint32_t SMEM = 1024 + Q_RES + V_STAGES * V_STAGE + K_STAGES * K_BLK;
 static_assert(K_STAGES >= 2, "too few key stages");
 static_assert(SMEM <= BUDGET, "shared-memory budget exceeded");
-constexpr int NBUF = 3;                        // TMEM score buffers
-constexpr uint32_t TMEM_COLS = 512;            // S/P buffers 0..2, then O
+constexpr int NBUF = 2;                        // TMEM score buffers
+constexpr uint32_t TMEM_COLS = 512;            // S/P buffers 0 and 1, then O
 constexpr uint32_t O_COL = NBUF * BN;
-static_assert(O_COL + 128 <= TMEM_COLS, "tensor memory exceeded");
+constexpr int O_N = 144;                       // O: 128 output columns, then the normaliser
+static_assert(O_COL + O_N <= TMEM_COLS, "tensor memory exceeded");
 constexpr int kThreads = 384;                  // 4 role warps + 8 softmax warps
 constexpr int HK = BN / 2;                     // keys per softmax warp
 constexpr float kRescaleLog2 = 8.0f;
@@ -99,7 +104,6 @@ attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     __shared__ float red[NBUF][2][BM];  // per-row partial maxima of the two halves, by buffer
-    __shared__ float lsum[2][BM];     // per-row partial normalisers of the two halves
 
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t q_res = base;
@@ -140,6 +144,14 @@ attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
         tmem_alloc(smem_u32(&tmem_slot), TMEM_COLS);
         tmem_relinquish();
     }
+    // the third box of every V stage holds ones (fp16 1.0): TMA never writes it
+    for (int i = threadIdx.x; i < V_STAGES * static_cast<int>(V_BOX / 16); i += kThreads) {
+        const int st = i / static_cast<int>(V_BOX / 16);
+        const int j = i - st * static_cast<int>(V_BOX / 16);
+        st_shared_v4(v_base + st * V_STAGE + 2 * V_BOX + 16u * j, 0x3c003c00u, 0x3c003c00u, 0x3c003c00u,
+                     0x3c003c00u);
+    }
+    fence_proxy_async_smem();  // generic-proxy stores -> visible to the tensor core
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -199,7 +211,7 @@ attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
                 }
                 const uint32_t fb = smem_u32(&v_full[s]);
                 const uint32_t sv = v_base + s * V_STAGE;
-                mbar_arrive_expect_tx(fb, V_STAGE);
+                mbar_arrive_expect_tx(fb, 2 * V_BOX);  // the two V boxes (the third is ones)
                 tma_load_3d(sv, &tmV, fb, 0, t * BN, bz * zv);
                 tma_load_3d(sv + V_BOX, &tmV, fb, 64, t * BN, bz * zv);
                 ++issued;
@@ -266,7 +278,7 @@ attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
         // ------------------------------------------ MMA issuer: O += P V
         if (lane == 0) {
             // A = P from TMEM (K-major), B = V from shared memory (MN-major)
-            constexpr uint32_t idesc_o = idesc_f16_f32(BM, 128, false, true);
+            constexpr uint32_t idesc_o = idesc_f16_f32(BM, O_N, false, true);
             int vs = 0;
             uint32_t vph = 0;
             bool ok = true;
@@ -279,7 +291,8 @@ attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
                     break;
                 }
                 tc_fence_after();
-                // V: 64-column boxes 16 KB apart, 16 keys = 2048 B per step
+                // V: 64-column boxes 16 KB apart (the third one ones), 16 keys =
+                // 2048 B per step
                 const uint64_t bd = sdesc_sw128(v_base + vs * V_STAGE, V_BOX, 1024);
                 const uint32_t a_tm = tmem_base + static_cast<uint32_t>(b * BN);
 #pragma unroll
@@ -313,7 +326,6 @@ attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
         const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(qd * 32) << 16);
         const bool pos_scale = scale_log2 >= 0.0f;
         float m_run = -INFINITY;          // running maximum, base-2 scaled logits
-        float l_run = 0.0f;               // this half's share of the running normaliser
         bool ok = true;
         // Every iteration passes exactly one pair barrier, also after a
         // failed wait (the work is then skipped), so the two warps of a pair
@@ -375,7 +387,6 @@ attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
             float alpha = 1.0f;
             if (raise) {
                 alpha = ex2_approx(m_run - mx);  // 0 for the first block
-                l_run *= alpha;
                 m_run = mx;
             }
             const float neg_m = -m_run;
@@ -383,7 +394,6 @@ attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
             // P = 2^(s * scale * log2 e - m) as fp16 pairs: this half's 64
             // keys go to columns h*32 .. h*32+31 of the buffer
             uint32_t pw[HK / 2];
-            float l0 = 0.0f, l1 = 0.0f;
             auto make_p = [&](auto masked) {
 #pragma unroll
                 for (int j = 0; j < HK; j += 2) {
@@ -394,16 +404,11 @@ attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
                         if (j + 1 >= valid) a1 = -INFINITY;
                     }
                     const __half2 v2 = __floats2half2_rn(ex2_approx(a0), ex2_approx(a1));
-                    // the normaliser sums the weights the MMA uses: the fp16 ones
-                    const float2 r2 = __half22float2(v2);
-                    l0 += r2.x;
-                    l1 += r2.y;
                     pw[j / 2] = *reinterpret_cast<const uint32_t*>(&v2);
                 }
             };
             if (valid < HK) make_p(std::true_type{});
             else make_p(std::false_type{});
-            l_run += l0 + l1;
             tmem_st_32x32b_x32(t_lane + s_col + static_cast<uint32_t>(h * (HK / 2)), pw);
             if (t > 0 && __any_sync(0xffffffffu, raise)) {
                 // then this half of O *= alpha (1 in rows that kept their
@@ -428,6 +433,15 @@ attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
                     for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
                     tmem_st_32x32b_x32(t_lane + col, o);
                 }
+                if (h == 1) {
+                    // the normaliser columns
+                    uint32_t o[16];
+                    tmem_ld_32x32b_x16(t_lane + O_COL + 128u, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                    tmem_st_32x32b_x16(t_lane + O_COL + 128u, o);
+                }
             }
             tmem_st_wait();
             tc_fence_before();
@@ -440,14 +454,14 @@ attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
                                        &abort_flag, long_limit);
             if (!__all_sync(0xffffffffu, got)) fail();
         }
-        // both halves of the row's normaliser (every softmax thread reaches
-        // this barrier exactly once)
-        lsum[h][r] = l_run;
-        named_bar_sync(1 + qd, 64);
-        const float l_row = lsum[0][r] + lsum[1][r];
         if (ok) {
             tc_fence_after();
-            const float inv_l = 1.0f / l_row;
+            // the row's normaliser: column 128 of O, the weights (the fp16
+            // ones the MMA used) summed by the P V MMA against the ones
+            uint32_t lw[16];
+            tmem_ld_32x32b_x16(t_lane + O_COL + 128u, lw);
+            tmem_ld_wait();
+            const float inv_l = 1.0f / __uint_as_float(lw[0]);
             const int m = q0 + r;
             void* Ob = batch_ptr(O, bz, sO, OUT_F32 ? 4 : 2);
 #pragma unroll 1
