@@ -67,7 +67,7 @@ constexpr uint32_t V_STAGE = 3 * V_BOX;
 constexpr uint32_t Q_RES = QC * Q_CHUNK;       // 32 KB
 constexpr int V_STAGES = 2;
 // 227 KB per CTA covers static shared memory too (barriers and the row
-// exchange arrays, about 4.3 KB): keep 8 KB for it
+// exchange array, about 2.2 KB): keep 8 KB for it
 constexpr uint32_t BUDGET = 227 * 1024 - 8192;
 constexpr int K_STAGES =
     static_cast<int>((BUDGET - 1024 - Q_RES - V_STAGES * V_STAGE) / K_BLK);
@@ -318,8 +318,8 @@ attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
         // ------------------------------------------- softmax and output
         // Two warps per TMEM lane quadrant: warp h of the pair takes keys
         // h*64 .. h*64+63 of each block (and output columns h*64 ..); the
-        // pair agrees on each row's maximum (and, at the end, its sum)
-        // through shared memory and a 64-thread named barrier.
+        // pair agrees on each row's maximum through shared memory and a
+        // 64-thread named barrier.  The row's sum comes from the MMA.
         const int qd = warp & 3;          // TMEM lane quadrant
         const int h = (warp - 4) >> 2;    // which half of the keys
         const int r = qd * 32 + lane;     // this thread's query row
