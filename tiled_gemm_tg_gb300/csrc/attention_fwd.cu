@@ -584,7 +584,9 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 // O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s with M = max_s m_s, the
 // same merge of running maxima and normalisers the blockwise pass applies.
 // A CTA takes blockDim.y query rows of one batch entry; a thread takes four
-// columns at a time, and all loads of a row are issued before any is used.
+// columns at a time.  Two short passes over the splits (the maximum, then
+// the weighted sums in split order) keep the registers few, so that many
+// rows are in flight per SM.
 constexpr int kMaxSplit = 16;
 
 template <bool OUT_F32>
@@ -597,46 +599,26 @@ attention_combine_kernel(const float* ws_o, const float* ws_ml, void* O, long lo
     const int ldw = (dv + 3) & ~3;
     void* Ob = batch_ptr(O, b, sO, OUT_F32 ? 4 : 2);
     for (int m = blockIdx.y * blockDim.y + threadIdx.y; m < Nq; m += gridDim.y * blockDim.y) {
-        // the row's maxima and normalisers (the same for every column)
-        float mv[kMaxSplit], lv[kMaxSplit];
+        // the row's largest maximum over the splits
         float M = -INFINITY;
-#pragma unroll
-        for (int sp = 0; sp < kMaxSplit; ++sp) {
-            if (sp < n_split) {
-                const long long row = (static_cast<long long>(sp) * batch + b) * Nq + m;
-                mv[sp] = ws_ml[2 * row];
-                lv[sp] = ws_ml[2 * row + 1];
-            }
-        }
-#pragma unroll
-        for (int sp = 0; sp < kMaxSplit; ++sp)
-            if (sp < n_split) M = fmaxf(M, mv[sp]);
-        float den = 0.0f;
-#pragma unroll
-        for (int sp = 0; sp < kMaxSplit; ++sp) {
-            if (sp < n_split) {
-                mv[sp] = ex2_approx(mv[sp] - M);  // now the split's weight
-                den = fmaf(mv[sp], lv[sp], den);
-            }
-        }
-        const float inv = 1.0f / den;
+#pragma unroll 4
+        for (int sp = 0; sp < n_split; ++sp)
+            M = fmaxf(M, ws_ml[2 * ((static_cast<long long>(sp) * batch + b) * Nq + m)]);
         for (int n = 4 * static_cast<int>(threadIdx.x); n < dv; n += 4 * static_cast<int>(blockDim.x)) {
-            float4 ov[kMaxSplit];
-#pragma unroll
-            for (int sp = 0; sp < kMaxSplit; ++sp)
-                if (sp < n_split)
-                    ov[sp] = *reinterpret_cast<const float4*>(
-                        ws_o + ((static_cast<long long>(sp) * batch + b) * Nq + m) * ldw + n);
+            float den = 0.0f;
             float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int sp = 0; sp < kMaxSplit; ++sp) {
-                if (sp < n_split) {
-                    num.x = fmaf(mv[sp], ov[sp].x, num.x);
-                    num.y = fmaf(mv[sp], ov[sp].y, num.y);
-                    num.z = fmaf(mv[sp], ov[sp].z, num.z);
-                    num.w = fmaf(mv[sp], ov[sp].w, num.w);
-                }
+#pragma unroll 4
+            for (int sp = 0; sp < n_split; ++sp) {
+                const long long row = (static_cast<long long>(sp) * batch + b) * Nq + m;
+                const float w = ex2_approx(ws_ml[2 * row] - M);  // the split's weight
+                den = fmaf(w, ws_ml[2 * row + 1], den);
+                const float4 ov = *reinterpret_cast<const float4*>(ws_o + row * ldw + n);
+                num.x = fmaf(w, ov.x, num.x);
+                num.y = fmaf(w, ov.y, num.y);
+                num.z = fmaf(w, ov.z, num.z);
+                num.w = fmaf(w, ov.w, num.w);
             }
+            const float inv = 1.0f / den;
             const float y[4] = {num.x * inv, num.y * inv, num.z * inv, num.w * inv};
             const long long i = static_cast<long long>(m) * ldo + n;
 #pragma unroll
