@@ -396,6 +396,15 @@ def main_attention(args, w):
     for i in range(args.warmup):
         call(*sets[i % n_sets], sh)
     tg.check(stream)
+    graph = None
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            h = torch.cuda.current_stream().cuda_stream
+            for i in range(args.steps):
+                call(*sets[i % n_sets], h)
+        graph.replay()  # warm replay
+        tg.check(stream)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
@@ -405,18 +414,26 @@ def main_attention(args, w):
     torch.cuda.synchronize()
     host_t0 = time.time()
     t_start.record(stream)
-    for i in range(args.steps):
-        evs[i][0].record(stream)
-        call(*sets[i % n_sets], sh)
-        evs[i][1].record(stream)
+    if graph is not None:
+        # all K calls replayed from one CUDA graph: no host gaps between them
+        graph.replay()
+    else:
+        for i in range(args.steps):
+            evs[i][0].record(stream)
+            call(*sets[i % n_sets], sh)
+            evs[i][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     host_t1 = time.time()
     if ws > 1:
         torch.distributed.barrier()
     elapsed_ms = t_start.elapsed_time(t_end)
-    per_launch = sorted(a.elapsed_time(b) for a, b in evs)
-    kern_ms = sum(per_launch) / args.steps
+    if graph is not None:
+        per_launch = []  # one graph replay: only the mean per call is known
+        kern_ms = elapsed_ms / args.steps
+    else:
+        per_launch = sorted(a.elapsed_time(b) for a, b in evs)
+        kern_ms = sum(per_launch) / args.steps
     if tg.tg_gemm_check(sh) != tg.TG_OK:
         raise RuntimeError("a kernel abandoned a bounded wait during the timed region")
     elapsed_ms = max_over_ranks(elapsed_ms, ws, dev)
@@ -508,11 +525,11 @@ def main_attention(args, w):
             "config": {"workload": w.name, "batch": B, "Nq": Nq, "Nk": Nk, "d": d, "dv": dv,
                        "scale": w.scale, "out_dtype": w.out_dtype, "accum": "f32",
                        "key_split_workspace_bytes": ws_bytes,
+                       "timing": "CUDA graph replay" if graph is not None else "stream launches",
                        "kernel": {1: "general, P in shared memory", 2: "general, keys split",
                                   3: "P in tensor memory"}.get(kern, "none"),
                        "l2": f"{n_sets} rotating Q/K/V/O sets, "
                              f"{n_sets * set_bytes / 2**20:.0f} MB per pass",
-                       "timing": "stream launches",
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
             "clocks": clocks,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s",
