@@ -259,10 +259,18 @@ tg_status tg_attention(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t
  * into ranges handled by separate CTAs, each writing an unnormalised partial
  * output with its running maximum and normaliser to `workspace`; a second
  * kernel merges them (the same merge of maxima and normalisers the blockwise
- * pass applies between key blocks).  tg_attention_workspace_size reports the
- * bytes this needs on the current device (0 when the call is large enough
- * not to split).  A NULL or smaller workspace runs the single pass: the
- * result is the same up to rounding order.
+ * pass applies between key blocks).  For heads with d <= 128 and dv <= 128
+ * the workspace serves a second purpose: when the query tiles fill the SMs
+ * more than once and leave the last wave at most 45 % full, each tile of
+ * that wave is cut into 2 or 4 ranges of at least four key blocks, run by
+ * separate CTAs, and the range that finishes last merges all partial
+ * results (the same merge, in the order of the ranges, so that the result
+ * does not depend on which one merges) in the kernel; the workspace holds
+ * the partials and one counter per tile, zeroed by a small kernel the call
+ * launches first.  tg_attention_workspace_size reports the bytes either use
+ * on the current device (0 when neither applies).  A NULL or smaller
+ * workspace runs the single pass: the result is the same up to rounding
+ * order.
  *
  * Arguments: those of tg_attention, plus
  *   workspace        device memory, 256-byte aligned, owned by the caller,
@@ -283,7 +291,8 @@ tg_status tg_attention_ws(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int6
                           tg_stream_t stream);
 
 /* Workspace bytes tg_attention_ws uses for these sizes on the current device
- * (0: no split, or invalid sizes, or no device). */
+ * (0: no key split and no split of the last wave, or invalid sizes, or no
+ * device). */
 size_t tg_attention_workspace_size(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv);
 
 /*
@@ -294,8 +303,9 @@ size_t tg_attention_workspace_size(int64_t batch, int64_t Nq, int64_t Nk, int64_
  *
  * Arguments, semantics and errors are those of tg_attention, plus:
  *   - the scratch is a fixed 16 MB static device array (per device, its
- *     address looked up once); a call whose split needs more returns
- *     TG_ERR_UNSUPPORTED (tg_attention_workspace_size tells the need), and a
+ *     address looked up once); a call whose key split needs more returns
+ *     TG_ERR_UNSUPPORTED (tg_attention_workspace_size tells the need), a
+ *     call whose split of the last wave needs more runs without it, and a
  *     call that needs no split runs the single pass;
  *   - nothing in the scratch has to start at zero: every partial is written
  *     before the combine kernel reads it;

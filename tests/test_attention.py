@@ -237,5 +237,19 @@ def test_attention_split_keys(B, Nq, Nk, d, dv, scale, out):
     assert np.allclose(got, o_plain.double().cpu().numpy(), rtol=2e-2, atol=2e-3)
 
 
-def test_attention_large_call_needs_no_workspace():
-    assert tg.tg_attention_workspace_size(16, 4096, 4096, 128, 128) == 0
+def test_attention_large_call_workspace():
+    """Many query tiles: no key split.  The P-in-TMEM kernel asks for a
+    workspace only when its tiles fill the SMs more than once, the last wave
+    holds at most 45 % of the SMs' worth of tiles, and the keys make at
+    least two pieces of four blocks (on 152 SMs: 16 x 4096, 56 tiles in the
+    fourth wave, and 4 x 5504, 20 in the second, do; 16 x 2048, 104 of 256
+    in the second wave, 19 x 4096, whole waves, and 4 x 5504 with 800 keys
+    do not).  The general kernel's 768-wide heads need none."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for B, N, Nk, d in [(16, 4096, 4096, 128), (4, 5504, 5504, 128), (16, 2048, 2048, 128),
+                        (19, 4096, 4096, 128), (4, 5504, 800, 128), (16, 2048, 2048, 768)]:
+        tiles = B * ((N + 127) // 128)
+        waves = (tiles + sms - 1) // sms
+        tail = tiles - (waves - 1) * sms
+        want = d <= 128 and waves > 1 and tail * 100 <= sms * 45 and (Nk + 127) // 128 >= 8
+        assert (tg.tg_attention_workspace_size(B, N, Nk, d, d) > 0) == want, (B, N, Nk, d)

@@ -220,3 +220,81 @@ def test_tmem_p_binding_sampled_large():
         tol = oracle.attention_tolerance(O, E, G, d, N, True)
         got = o[b].double().cpu().numpy()[rows]
         assert np.all(np.abs(got - O) <= tol), f"head {b}"
+
+
+def _num_sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def _tail_case(Nq, extra):
+    """A batch count whose query tiles fill the SMs once and leave `extra`
+    tiles (up to one tile row more) in a last, short wave."""
+    q_blocks = (Nq + 127) // 128
+    batch = (_num_sms() + extra + q_blocks - 1) // q_blocks
+    tiles = batch * q_blocks
+    assert _num_sms() < tiles <= _num_sms() * 3 // 2
+    return batch
+
+
+def _attn_ws(qd, kd, vd, scale, out, ws):
+    o = tg.attention(qd, kd, vd, scale, out_dtype=out, workspace=ws)
+    tg.check()
+    return o.double().cpu().numpy()
+
+
+@pytest.mark.parametrize("Nq,Nk,d,dv,scale,fill", [
+    (128, 1000, 128, 128, 0.09, 0.05),  # eight blocks, the last one ragged: 2 pieces of 4
+    (200, 1100, 64, 64, 0.125, 0.05),   # ragged queries; nine blocks: pieces of 4 and 5
+    (256, 1500, 96, 80, 0.1, 0.05),     # twelve blocks: 3 pieces; d, dv not multiples of 64
+    (130, 2100, 64, 48, 0.125, 0.05),   # seventeen blocks: 4 pieces of 4, 4, 4, 5
+    (128, 2100, 128, 128, 0.09, 0.3),   # a third of a wave left: 2 pieces of 8 and 9
+])
+@pytest.mark.parametrize("out", [torch.float16, torch.float32])
+def test_tmem_p_wave_tail_split(Nq, Nk, d, dv, scale, fill, out):
+    """A short last wave: its tiles are cut into pieces along the keys,
+    merged in the kernel through the workspace.  Every row against the
+    oracle, the same call without a workspace close by, and a second call on
+    the same workspace bit for bit equal (the merge order is fixed)."""
+    batch = _tail_case(Nq, int(fill * _num_sms()))
+    assert tg.tg_attention_kernel(batch, Nq, Nk, d, dv) == 3
+    need = tg.tg_attention_workspace_size(batch, Nq, Nk, d, dv)
+    assert need > 0, "a short last wave should ask for the tail workspace"
+    q, k, v = _qkv(batch, Nq, Nk, d, dv, 14800 + Nq + Nk + d)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    ws = torch.full((need,), 0xA5, dtype=torch.uint8, device="cuda")  # contents do not matter
+    got = _attn_ws(qd, kd, vd, scale, out, ws)
+    _check(q, k, v, scale, got, out, f"tail split {batch}x{Nq}x{Nk} d{d} dv{dv}")
+    plain = tg.attention(qd, kd, vd, scale, out_dtype=out).double().cpu().numpy()
+    tg.check()
+    assert np.allclose(got, plain, rtol=2e-2, atol=2e-3)
+    again = _attn_ws(qd, kd, vd, scale, out, ws)
+    assert np.array_equal(got, again)
+
+
+@pytest.mark.parametrize("peak_piece", [0, 2, 3])
+def test_tmem_p_wave_tail_split_far_apart_maxima(peak_piece):
+    """The pieces' row maxima differ by far more than the rescale threshold:
+    one key per row dominates (score 60 against |score| < 1), in the first,
+    a middle or the last of four pieces of the keys, so the other pieces'
+    merge weights are 2^-86 and every other probability rounds to zero in
+    fp16.  The output is that key's value row exactly (fp32 output)."""
+    Nq, Nk, d, dv = 128, 2048, 64, 64    # sixteen key blocks: four pieces of 512 keys
+    batch = _tail_case(Nq, 6)
+    g = torch.Generator().manual_seed(14900 + peak_piece)
+    # row r points along axis r % d; each axis has one hot key per batch entry
+    hot = torch.randint(0, Nk // 4, (batch, d), generator=g) + peak_piece * (Nk // 4)
+    q = torch.zeros(batch, Nq, d)
+    q[:, torch.arange(Nq), torch.arange(Nq) % d] = 8.0
+    k = torch.randn(batch, Nk, d, generator=g) * 0.01
+    for b in range(batch):
+        k[b, hot[b], torch.arange(d)] = 7.5
+    v = torch.randn(batch, Nk, dv, generator=g)
+    q, k, v = q.half(), k.half(), v.half()
+    need = tg.tg_attention_workspace_size(batch, Nq, Nk, d, dv)
+    assert need > 0
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    got = _attn_ws(q.cuda(), k.cuda(), v.cuda(), 1.0, torch.float32, ws)
+    _check(q, k, v, 1.0, got, torch.float32, f"tail split, peak in piece {peak_piece}")
+    rows = torch.arange(Nq) % d
+    want = np.stack([v[b, hot[b][rows]].double().numpy() for b in range(batch)])
+    assert np.array_equal(got, want)

@@ -82,13 +82,22 @@ static_assert(O_COL + O_N <= TMEM_COLS, "tensor memory exceeded");
 constexpr int kThreads = 384;                  // 4 role warps + 8 softmax warps
 constexpr int HK = BN / 2;                     // keys per softmax warp
 constexpr float kRescaleLog2 = 8.0f;
+// Tail split: the tiles of a last wave that holds at most kTailFill4
+// percent of the SMs' worth of tiles are cut into 4 pieces along the keys,
+// of at most kTailFill2 percent into 2, each piece at least kTailMinBlocks
+// key blocks.
+constexpr int kMaxPieces = 4;
+constexpr int kTailFill4 = 20;
+constexpr int kTailFill2 = 45;
+constexpr int kTailMinBlocks = 4;
 
 template <bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
 attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, void* O, long long ldo, long long sO,
                       int Nq, int Nk, int dv, int n_chunks, float scale_log2, int o_vec, int zq,
-                      int zk, int zv, int hook, unsigned int* err)
+                      int zk, int zv, int q_blocks, int units_full, int pieces, float* tws_o, float* tws_ml,
+                      unsigned int* tws_cnt, int hook, unsigned int* err)
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t k_full[K_STAGES];
@@ -103,6 +112,7 @@ attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
     __shared__ __align__(8) uint64_t drain_o;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
+    __shared__ unsigned int tail_old;
     __shared__ float red[NBUF][2][BM];  // per-row partial maxima of the two halves, by buffer
 
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -111,9 +121,22 @@ attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
     const uint32_t v_base = k_base + K_STAGES * K_BLK;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int q0 = static_cast<int>(blockIdx.x) * BM;
-    const int bz = static_cast<int>(blockIdx.z);
-    const int n_kv = (Nk + BN - 1) / BN;
+    // Work units: units 0 .. units_full-1 are whole tiles (128 query rows of
+    // one batch entry, all keys); each tile after them, a tile of the last,
+    // partial wave, is cut into `pieces` consecutive ranges of key blocks,
+    // one unit per range, merged by whichever unit of the tile ends last.
+    const int unit = static_cast<int>(blockIdx.x);
+    int tile = unit;
+    int part = -1;
+    if (unit >= units_full) {
+        tile = units_full + (unit - units_full) / pieces;
+        part = (unit - units_full) % pieces;
+    }
+    const int q0 = (tile % q_blocks) * BM;
+    const int bz = tile / q_blocks;
+    const int n_kv_all = (Nk + BN - 1) / BN;
+    const int kv0 = part < 0 ? 0 : part * n_kv_all / pieces;
+    const int n_kv = (part < 0 ? n_kv_all : (part + 1) * n_kv_all / pieces) - kv0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < K_STAGES; ++s) {
@@ -179,7 +202,8 @@ attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
                     const uint32_t fb = smem_u32(&k_full[s]);
                     mbar_arrive_expect_tx(fb, static_cast<uint32_t>(n_chunks) * K_CHUNK);
                     for (int c = 0; c < n_chunks; ++c)
-                        tma_load_3d(k_base + s * K_BLK + c * K_CHUNK, &tmK, fb, c * DC, t * BN, bz * zk);
+                        tma_load_3d(k_base + s * K_BLK + c * K_CHUNK, &tmK, fb, c * DC, (kv0 + t) * BN,
+                                    bz * zk);
                     ++issued;
                 }
                 if (++s == K_STAGES) {
@@ -212,8 +236,8 @@ attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
                 const uint32_t fb = smem_u32(&v_full[s]);
                 const uint32_t sv = v_base + s * V_STAGE;
                 mbar_arrive_expect_tx(fb, 2 * V_BOX);  // the two V boxes (the third is ones)
-                tma_load_3d(sv, &tmV, fb, 0, t * BN, bz * zv);
-                tma_load_3d(sv + V_BOX, &tmV, fb, 64, t * BN, bz * zv);
+                tma_load_3d(sv, &tmV, fb, 0, (kv0 + t) * BN, bz * zv);
+                tma_load_3d(sv + V_BOX, &tmV, fb, 64, (kv0 + t) * BN, bz * zv);
                 ++issued;
                 if (++s == V_STAGES) {
                     s = 0;
@@ -343,7 +367,7 @@ attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
             const uint32_t s_col = static_cast<uint32_t>(b * BN);
             uint32_t raw[HK];
             float mine = 0.0f;
-            const int valid = min(BN, Nk - t * BN) - h * HK;
+            const int valid = min(BN, Nk - (kv0 + t) * BN) - h * HK;
             if (ok) {
                 const bool got = mbar_wait(smem_u32(&s_full[b]), static_cast<uint32_t>((t / NBUF) & 1),
                                            &abort_flag, long_limit);
@@ -456,23 +480,106 @@ attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
         }
         if (ok) {
             tc_fence_after();
-            // the row's normaliser: column 128 of O, the weights (the fp16
-            // ones the MMA used) summed by the P V MMA against the ones
-            uint32_t lw[16];
-            tmem_ld_32x32b_x16(t_lane + O_COL + 128u, lw);
-            tmem_ld_wait();
-            const float inv_l = 1.0f / __uint_as_float(lw[0]);
-            const int m = q0 + r;
-            void* Ob = batch_ptr(O, bz, sO, OUT_F32 ? 4 : 2);
-#pragma unroll 1
-            for (int c = 0; c < HK; c += 32) {
-                const int n = h * HK + c;
-                uint32_t o[32];
-                tmem_ld_32x32b_x32(t_lane + O_COL + static_cast<uint32_t>(n), o);
+        }
+        const int m = q0 + r;
+        void* Ob = batch_ptr(O, bz, sO, OUT_F32 ? 4 : 2);
+        if (part < 0) {
+            if (ok) {
+                // the row's normaliser: column 128 of O, the weights (the
+                // fp16 ones the MMA used) summed by the P V MMA against the ones
+                uint32_t lw[16];
+                tmem_ld_32x32b_x16(t_lane + O_COL + 128u, lw);
                 tmem_ld_wait();
+                const float inv_l = 1.0f / __uint_as_float(lw[0]);
+#pragma unroll 1
+                for (int c = 0; c < HK; c += 32) {
+                    const int n = h * HK + c;
+                    uint32_t o[32];
+                    tmem_ld_32x32b_x32(t_lane + O_COL + static_cast<uint32_t>(n), o);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * inv_l);
-                if (m < Nq && n < dv) store_chunk<OUT_F32>(Ob, ldo, m, n, dv, o, o_vec != 0);
+                    for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * inv_l);
+                    if (m < Nq && n < dv) store_chunk<OUT_F32>(Ob, ldo, m, n, dv, o, o_vec != 0);
+                }
+            }
+        } else {
+            // One piece of a tail tile: its unnormalised O, running maximum
+            // and normaliser go to the workspace; the piece that ends last
+            // merges them all, O = sum_p w_p O_p / sum_p w_p L_p with
+            // w_p = 2^(m_p - max_p m_p), in the order of the pieces whichever
+            // unit merges, so that every call rounds alike.  A piece's O is
+            // stored column by column (128 rows of a column contiguous), so
+            // that a warp's 32 rows make one 128-byte line per access.
+            const int ti = tile - units_full;
+            const size_t slot0 = static_cast<size_t>(ti) * pieces;  // piece p: slot0 + p
+            const size_t slot_self = slot0 + static_cast<size_t>(part);
+            if (ok) {
+                uint32_t lw[16];
+                tmem_ld_32x32b_x16(t_lane + O_COL + 128u, lw);
+                tmem_ld_wait();
+#pragma unroll 1
+                for (int c = 0; c < HK; c += 32) {
+                    const int n = h * HK + c;
+                    uint32_t o[32];
+                    tmem_ld_32x32b_x32(t_lane + O_COL + static_cast<uint32_t>(n), o);
+                    tmem_ld_wait();
+                    float* dst = tws_o + (slot_self * 128 + static_cast<size_t>(n)) * BM + r;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) dst[static_cast<size_t>(e) * BM] = __uint_as_float(o[e]);
+                }
+                if (h == 0) {
+                    tws_ml[2 * (slot_self * BM + r)] = m_run;
+                    tws_ml[2 * (slot_self * BM + r) + 1] = __uint_as_float(lw[0]);
+                }
+            }
+            __threadfence();  // this thread's partial is visible before the count
+            named_bar_sync(5, 2 * BM);
+            if (warp == 4 && lane == 0) {
+                pdl_wait();  // the counters were zeroed by the kernel before this one
+                tail_old = abort_flag == 0 ? atomicAdd(&tws_cnt[ti], 1u) : 0xffffffffu;
+            }
+            named_bar_sync(5, 2 * BM);
+            if (ok && tail_old == static_cast<unsigned int>(pieces - 1)) {
+                __threadfence();  // the other pieces, counted before this one, are visible
+                // read through L2: the other pieces' lines were written by other SMs
+                const float* ml = tws_ml + 2 * (slot0 * BM + r);  // piece p: ml[2 * p * BM]
+                float mm = -INFINITY;
+#pragma unroll 1
+                for (int p = 0; p < pieces; ++p) mm = fmaxf(mm, __ldcg(ml + 2 * p * BM));
+                float lsum = 0.0f;
+#pragma unroll 1
+                for (int p = 0; p < pieces; ++p)
+                    lsum = fmaf(ex2_approx(__ldcg(ml + 2 * p * BM) - mm), __ldcg(ml + 2 * p * BM + 1), lsum);
+                const float inv = 1.0f / lsum;
+#pragma unroll 1
+                for (int c = 0; c < HK; c += 32) {
+                    const int n = h * HK + c;
+                    float acc[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) acc[e] = 0.0f;
+                    // two pieces' columns in flight at a time (pieces >= 2)
+#pragma unroll 1
+                    for (int p = 0; p < pieces; p += 2) {
+                        const int p1 = p + 1 < pieces ? p + 1 : p;
+                        const float w0 = ex2_approx(__ldcg(ml + 2 * p * BM) - mm);
+                        const float w1 = p1 != p ? ex2_approx(__ldcg(ml + 2 * p1 * BM) - mm) : 0.0f;
+                        const float* s0 = tws_o + ((slot0 + p) * 128 + static_cast<size_t>(n)) * BM + r;
+                        const float* s1 = tws_o + ((slot0 + p1) * 128 + static_cast<size_t>(n)) * BM + r;
+                        float v0[32], v1[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            v0[e] = __ldcg(s0 + static_cast<size_t>(e) * BM);
+                            v1[e] = __ldcg(s1 + static_cast<size_t>(e) * BM);
+                        }
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) acc[e] = fmaf(w1, v1[e], fmaf(w0, v0[e], acc[e]));
+                    }
+                    uint32_t o[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(acc[e] * inv);
+                    if (m < Nq && n < dv) store_chunk<OUT_F32>(Ob, ldo, m, n, dv, o, o_vec != 0);
+                }
+                if (warp == 4 && lane == 0) tws_cnt[ti] = 0u;  // ready for the next call
             }
         }
     }
@@ -483,6 +590,15 @@ attention_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
     }
+}
+
+// Zeroes the tail tiles' counters; lets the attention kernel, launched as
+// its programmatic dependent, start at once (only the tail units wait for
+// this grid, just before they count).
+__global__ void __launch_bounds__(256) tail_zero_kernel(unsigned int* cnt, int n)
+{
+    pdl_trigger();
+    for (int i = static_cast<int>(threadIdx.x); i < n; i += static_cast<int>(blockDim.x)) cnt[i] = 0u;
 }
 
 std::mutex g_attr_mu;
@@ -517,17 +633,95 @@ cudaError_t launch_cfg(const AttnArgs& a)
     const int o_vec = (reinterpret_cast<uintptr_t>(a.O) % 16 == 0) &&
                       ((static_cast<size_t>(a.ldo) * es) % 16 == 0) &&
                       ((static_cast<size_t>(a.sO) * es) % 16 == 0);
-    const dim3 grid((a.Nq + BM - 1) / BM, 1, a.batch);
-    if (grid.z > 65535u) return cudaErrorInvalidConfiguration;
+    const int q_blocks = (a.Nq + BM - 1) / BM;
+    const long long tiles = static_cast<long long>(q_blocks) * a.batch;
+    const int tail = a.tail_tiles;  // tiles of the last wave cut into pieces along the keys
+    const int pieces = tail > 0 ? a.tail_pieces : 1;
+    if (tail < 0 || tail > tiles || (tail > 0 && a.ws == nullptr) || pieces < 1 ||
+        pieces > kMaxPieces || (tail > 0 && (pieces < 2 || pieces > (a.Nk + BN - 1) / BN)))
+        return cudaErrorInvalidValue;
+    const long long units = tiles - tail + static_cast<long long>(tail) * pieces;
+    if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const dim3 grid(static_cast<unsigned>(units), 1, 1);
+    float* tws_o = nullptr;
+    float* tws_ml = nullptr;
+    unsigned int* tws_cnt = nullptr;
+    if (tail > 0) {
+        tws_o = static_cast<float*>(a.ws);
+        tws_ml = tws_o + attention_tail_o_floats(tail, pieces);
+        tws_cnt = reinterpret_cast<unsigned int*>(tws_ml + attention_tail_ml_floats(tail, pieces));
+        tail_zero_kernel<<<1, 256, 0, a.stream>>>(tws_cnt, tail);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     const float scale_log2 = a.scale * 1.4426950408889634f;  // log2(e)
     const int n_chunks = (a.d + DC - 1) / DC;
-    kernel<<<grid, kThreads, SMEM, a.stream>>>(tq, tk, tv, a.O, a.ldo, a.sO, a.Nq, a.Nk, a.dv,
-                                               n_chunks, scale_log2, o_vec, a.sQ != 0, a.sK != 0,
-                                               a.sV != 0, a.hook, a.err);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = SMEM;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute at[1];
+    set_pdl_attr(at[0]);
+    cfg.attrs = at;
+    cfg.numAttrs = tail > 0 ? 1 : 0;  // only behind the counter-zeroing kernel
+    return cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, a.O, a.ldo, a.sO, a.Nq, a.Nk, a.dv, n_chunks,
+                              scale_log2, o_vec, static_cast<int>(a.sQ != 0),
+                              static_cast<int>(a.sK != 0), static_cast<int>(a.sV != 0), q_blocks,
+                              static_cast<int>(tiles - tail), pieces, tws_o, tws_ml, tws_cnt, a.hook,
+                              a.err);
 }
 
 }  // namespace
+
+long long attention_tail_o_floats(int tail, int pieces)
+{
+    // fp32 [tail][pieces][128 columns][128 rows], 256-byte aligned after it
+    return (static_cast<long long>(tail) * pieces * BM * 128 + 63) / 64 * 64;
+}
+
+long long attention_tail_ml_floats(int tail, int pieces)
+{
+    // fp32 [tail][pieces][128 rows][maximum, normaliser]
+    return (static_cast<long long>(tail) * pieces * BM * 2 + 63) / 64 * 64;
+}
+
+int attention_tail_plan(int batch, int Nq, int Nk, int num_sms, int* pieces)
+{
+    // Tiles go to the SMs in waves.  When the tiles fill the SMs more than
+    // once and the last wave is short, each tile of that wave is cut into
+    // pieces along the keys; the dispatcher hands the short pieces to SMs as
+    // they free up, so that the SMs end closer together.  Each piece costs
+    // its own start (Q load, pipeline fill), a partial write, and a share of
+    // the merge, which outweighs the gain once the last wave is about half
+    // full: the thresholds are measured ones.
+    *pieces = 0;
+    if (batch <= 0 || Nq <= 0 || Nk <= 0 || num_sms <= 0) return 0;
+    const long long tiles = static_cast<long long>((Nq + BM - 1) / BM) * batch;
+    const int n_kv = (Nk + BN - 1) / BN;
+    if (tiles <= num_sms) return 0;
+    const long long waves = (tiles + num_sms - 1) / num_sms;
+    const long long tail = tiles - (waves - 1) * num_sms;
+    int p = 0;
+    if (tail * 100 <= static_cast<long long>(num_sms) * kTailFill4) p = 4;
+    else if (tail * 100 <= static_cast<long long>(num_sms) * kTailFill2) p = 2;
+    if (p > n_kv / kTailMinBlocks) p = n_kv / kTailMinBlocks;
+    if (p > kMaxPieces) p = kMaxPieces;
+    if (p < 2) return 0;
+    *pieces = p;
+    return static_cast<int>(tail);
+}
+
+size_t attention_tail_ws_bytes(int batch, int Nq, int Nk, int num_sms)
+{
+    int pieces = 0;
+    const int tail = attention_tail_plan(batch, Nq, Nk, num_sms, &pieces);
+    if (tail == 0) return 0;
+    return static_cast<size_t>(attention_tail_o_floats(tail, pieces) +
+                               attention_tail_ml_floats(tail, pieces)) *
+               sizeof(float) +
+           static_cast<size_t>(tail) * sizeof(unsigned int);
+}
 
 bool attention_tmem_p_serves(int d, int dv)
 {

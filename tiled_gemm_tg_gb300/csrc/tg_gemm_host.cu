@@ -438,9 +438,18 @@ tg_status tg_attention_ws(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int6
         static_cast<int>(batch), static_cast<int>(Nq), static_cast<int>(Nk), static_cast<int>(d),
         static_cast<int>(dv), ds->num_sms, ws_ok, g_force_attn.load(std::memory_order_relaxed));
     const bool split = choice == 2;
-    if (split) {
+    // the P-in-TMEM kernel cuts the tiles of a short last wave in two along
+    // the keys when the workspace holds the halves' partial results
+    size_t need_tail = 0;
+    if (choice == 3 && workspace != nullptr) {
+        need_tail = tg::attention_tail_ws_bytes(static_cast<int>(batch), static_cast<int>(Nq),
+                                                static_cast<int>(Nk), ds->num_sms);
+        if (workspace_bytes < need_tail) need_tail = 0;
+    }
+    const size_t used = split ? need : need_tail;
+    if (used > 0) {
         u128 w0 = static_cast<u128>(reinterpret_cast<uintptr_t>(workspace));
-        u128 w1 = w0 + need;
+        u128 w1 = w0 + used;
         if (w1 > top || overlaps(w0, w1, o0, o1) || overlaps(w0, w1, q0, q1) ||
             overlaps(w0, w1, k0, k1) || overlaps(w0, w1, v0, v1))
             return TG_ERR_INVALID_ARG;
@@ -473,6 +482,10 @@ tg_status tg_attention_ws(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int6
         a.ws = workspace;
     }
     a.tmem_p = choice == 3;
+    if (need_tail > 0) {
+        a.tail_tiles = tg::attention_tail_plan(a.batch, a.Nq, a.Nk, ds->num_sms, &a.tail_pieces);
+        a.ws = workspace;
+    }
     return tg::launch_attention(a) == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 
@@ -501,7 +514,14 @@ tg_status tg_attention_noalloc(int64_t batch, int64_t Nq, int64_t Nk, int64_t d,
     size_t bytes = 0;
     void* scratch = tg::attention_static_scratch(&bytes);
     if (scratch == nullptr) return TG_ERR_CUDA;
-    if (need > bytes) return TG_ERR_UNSUPPORTED;  // the split needs more than the static scratch
+    if (need > bytes) {
+        // the key split needs more than the static scratch; a split of the
+        // last wave only saves time, and the call runs without it
+        if (tg_attention_kernel(batch, Nq, Nk, d, dv, 1) != 3) return TG_ERR_UNSUPPORTED;
+        return tg_attention_ws(batch, Nq, Nk, d, dv, Q, ldq, strideQ, K, ldk, strideK, V, ldv,
+                               strideV, O, ldo, strideO, scale, in_dtype, out_dtype, nullptr, 0,
+                               stream);
+    }
     return tg_attention_ws(batch, Nq, Nk, d, dv, Q, ldq, strideQ, K, ldk, strideK, V, ldv,
                            strideV, O, ldo, strideO, scale, in_dtype, out_dtype, scratch, bytes,
                            stream);
@@ -514,8 +534,17 @@ size_t tg_attention_workspace_size(int64_t batch, int64_t Nq, int64_t Nk, int64_
         return 0;
     DeviceState* ds = nullptr;
     if (device_state(&ds) != TG_OK) return 0;
-    return tg::attention_ws_bytes(static_cast<int>(batch), static_cast<int>(Nq),
-                                  static_cast<int>(Nk), static_cast<int>(dv), ds->num_sms);
+    const size_t split = tg::attention_ws_bytes(static_cast<int>(batch), static_cast<int>(Nq),
+                                                static_cast<int>(Nk), static_cast<int>(dv),
+                                                ds->num_sms);
+    const int choice = tg::attention_kernel_choice(
+        static_cast<int>(batch), static_cast<int>(Nq), static_cast<int>(Nk), static_cast<int>(d),
+        static_cast<int>(dv), ds->num_sms, split > 0, g_force_attn.load(std::memory_order_relaxed));
+    if (choice == 2) return split;
+    if (choice == 3)
+        return tg::attention_tail_ws_bytes(static_cast<int>(batch), static_cast<int>(Nq),
+                                           static_cast<int>(Nk), ds->num_sms);
+    return 0;
 }
 
 int tg_attention_kernel(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,

@@ -149,6 +149,11 @@ struct AttnArgs {
     // the kernel that keeps P in tensor memory (attention_fwd2.cu); needs
     // d <= 128, dv <= 128 and no key split
     bool tmem_p = false;
+    // with tmem_p: the tiles of the last wave each cut into `tail_pieces`
+    // ranges of the keys and merged in the kernel, through `ws`
+    // (attention_tail_plan, attention_tail_ws_bytes)
+    int tail_tiles = 0;
+    int tail_pieces = 0;
 };
 
 cudaError_t launch_attention(const AttnArgs& a);
@@ -165,6 +170,13 @@ void* attention_static_scratch(size_t* bytes);
 // head sizes, and its launch.
 bool attention_tmem_p_serves(int d, int dv);
 cudaError_t launch_attention_tmem_p(const AttnArgs& a);
+// Its tail split: how many tiles of a last, partial wave are cut in two
+// (0: none), the workspace that needs, and the workspace's layout (O rows,
+// then maxima and normalisers, then one counter per tail tile).
+int attention_tail_plan(int batch, int Nq, int Nk, int num_sms, int* pieces);
+size_t attention_tail_ws_bytes(int batch, int Nq, int Nk, int num_sms);
+long long attention_tail_o_floats(int tail, int pieces);
+long long attention_tail_ml_floats(int tail, int pieces);
 // Which forward kernel a call runs: 1 the general kernel (any d, dv), 2 the
 // same with the keys split over CTAs (only when `split_ok`: the caller's
 // workspace holds the partials), 3 the kernel that keeps P in tensor memory
