@@ -46,9 +46,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # ncu capture, keyed by workload, with the hash of the kernel sources it was
 # taken on.  A stale hash means the kernel changed since: traffic is null.
 NCU_TRAFFIC = {
-    # profiles/gemm_tc_pair_square_8192.md: 994.1 MB read + 124.8 MB written
-    "square_8192": {"bytes": 1118886400, "kernel_hash": "b29e0f161ce798af"},
-    # same file, E4M3 inputs: 336.9 MB read + 115.3 MB written
+    # the pair kernel's ncu summary under profiles/: 991.5 MB read + 124.1 MB written
+    "square_8192": {"bytes": 1115573504, "kernel_hash": "1a413666d8be47c8"},
+    # same summary, E4M3 inputs: 336.9 MB read + 115.3 MB written
     "square_8192_e4m3": {"bytes": 452197376, "kernel_hash": "b29e0f161ce798af"},
 }
 
@@ -62,8 +62,8 @@ ATTN_KERNEL_SOURCES = ["tiled_gemm_tg_gb300/csrc/attention_fwd2.cu", "tiled_gemm
 # DRAM traffic per launch of the attention kernel that keeps P in tensor
 # memory, from one ncu capture, valid while its sources hash the same
 ATTN_NCU_TRAFFIC = {
-    # profiles/attention_fwd2_16x4096x128.md: 50.4 MB read + 0.5 MB written
-    "attn_16x4096x128": {"bytes": 50846208, "kernel_hash": "17e648aa7dbc8aa2"},
+    # the kernel's ncu summary under profiles/: 50.4 MB read + 1.4 MB written
+    "attn_16x4096x128": {"bytes": 51794176, "kernel_hash": "7adf12e0ed838ea7"},
 }
 
 
@@ -366,7 +366,9 @@ def main_attention(args, w):
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
     B, Nq, Nk, d, dv = w.batch, w.Nq, w.Nk, w.d, w.dv
-    # a workspace lets calls with few CTAs split the keys (the library says how much)
+    # a workspace lets calls with few CTAs split the keys, and calls whose
+    # last wave of tiles is short split that wave's tiles (the library says
+    # how much)
     ws_bytes = tg.tg_attention_workspace_size(B, Nq, Nk, d, dv)
     workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     forced = {"auto": 0, "general": 1, "tmem_p": 3}[args.attn_kernel]
@@ -374,7 +376,11 @@ def main_attention(args, w):
         raise RuntimeError("attention kernel override refused")
     kern = tg.tg_attention_kernel(B, Nq, Nk, d, dv, split_allowed=bool(ws_bytes))
     kern_name = {1: "attention_fwd_kernel", 2: "attention_fwd_kernel (+ attention_combine_kernel)",
-                 3: "attention_fwd2_kernel"}.get(kern, "none")
+                 3: "attention_fwd2_kernel" + (" (+ tail_zero_kernel)" if ws_bytes else "")
+                 }.get(kern, "none")
+    # kernels per call: the combine kernel after a key split; the counters'
+    # zeroing kernel before a split of the last wave
+    per_call = 2 if kern == 2 or (kern == 3 and ws_bytes) else 1
 
     def call(q, k, v, o, handle):
         st = tg.tg_attention_ws(B, Nq, Nk, d, dv, q.data_ptr(), d, Nq * d, k.data_ptr(), d,
@@ -524,7 +530,9 @@ def main_attention(args, w):
             "data": "synthetic",
             "config": {"workload": w.name, "batch": B, "Nq": Nq, "Nk": Nk, "d": d, "dv": dv,
                        "scale": w.scale, "out_dtype": w.out_dtype, "accum": "f32",
-                       "key_split_workspace_bytes": ws_bytes,
+                       "workspace_bytes": ws_bytes,
+                       "workspace_use": ("key split" if kern == 2 else
+                                         "last-wave split" if ws_bytes else "none"),
                        "timing": "CUDA graph replay" if graph is not None else "stream launches",
                        "kernel": {1: "general, P in shared memory", 2: "general, keys split",
                                   3: "P in tensor memory"}.get(kern, "none"),
@@ -536,7 +544,7 @@ def main_attention(args, w):
                     "h2d_bytes_per_step": B * (Nq * d + Nk * (d + dv)) * 2,
                     "d2h_bytes_per_step": B * Nq * dv * oh[0].element_size(), "steps": e2e_steps,
                     "pipeline": "H2D / tg_attention / D2H on three streams, two device buffer sets"},
-            "gpu_launches": args.steps * (2 if kern == 2 else 1),  # + the combine kernel
+            "gpu_launches": args.steps * per_call,
             "roofline": roofline,
             "cpu_baseline": cpu,
         }
