@@ -409,6 +409,22 @@ int tg_attention_kernel(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_
                         int split_allowed);
 tg_status tg_attention_force_kernel(int kernel);
 
+/*
+ * tg_attention_tail_plan -- the split of a short last wave (tg_attention_ws)
+ * that kernel 3 would make for these sizes on a GPU with `num_sms` SMs,
+ * computed on the host alone (no device needed).  The kernel gives each CTA
+ * 128 query rows of one head; tiles = ceil(Nq / 128) * batch go to the SMs in
+ * waves of num_sms.  When there are more tiles than SMs and the last wave
+ * holds at most 45 % of num_sms tiles, each of its tiles is cut into 2 ranges
+ * of key blocks (4 when it holds at most 20 %), fewer if that would leave a
+ * range under four blocks of 128 keys, and none below two ranges.
+ * Returns the number of tiles cut (0: no split; also for sizes kernel 3 does
+ * not serve, d or dv above 128, or out of range) and stores the ranges per
+ * tile in *pieces (0 with no split); `pieces` may be NULL.
+ */
+int tg_attention_tail_plan(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                           int num_sms, int* pieces);
+
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int tg_gemm_version(void);
 

@@ -402,3 +402,61 @@ def test_attention_kernel_selection_on_host():
     assert tg.tg_attention_kernel(1, 128, 0, 64, 64) == 0
     assert tg.tg_attention_kernel(1, -5, 128, 64, 64) == 0
     assert tg.tg_attention_kernel(65536, 128, 128, 64, 64) == 0
+
+
+def test_attention_tail_plan_on_host():
+    """The last-wave split of kernel 3 is host logic: tiles of 128 query
+    rows per head, waves of num_sms, a split only of a last wave holding at
+    most 45 % of num_sms tiles (4 key ranges up to 20 %), every range at
+    least four 128-key blocks."""
+    plan = tg.tg_attention_tail_plan
+    # 16 heads x 4096: 512 tiles, 56 in the fourth wave on 152 SMs (37 %)
+    assert plan(16, 4096, 4096, 128, 128, 152) == (56, 2)
+    # on 148 SMs the fourth wave holds 68 tiles (46 %): no split
+    assert plan(16, 4096, 4096, 128, 128, 148) == (0, 0)
+    # 4 x 5504 queries: 172 tiles, 20 in the second wave (13 %)
+    assert plan(4, 5504, 5504, 128, 128, 152) == (20, 4)
+    # fewer key blocks, fewer ranges: 8 -> 2, 12 or 13 -> 3, 16 -> 4, 7 -> none
+    assert plan(4, 5504, 1024, 128, 128, 152) == (20, 2)
+    assert plan(4, 5504, 1536, 128, 128, 152) == (20, 3)
+    assert plan(4, 5504, 1537, 128, 128, 152) == (20, 3)
+    assert plan(4, 5504, 2048, 64, 32, 152) == (20, 4)
+    assert plan(4, 5504, 800, 128, 128, 152) == (0, 0)
+    # a last wave 68 % full, an exact number of waves, one wave or less
+    assert plan(16, 2048, 2048, 128, 128, 152) == (0, 0)
+    assert plan(19, 4096, 4096, 128, 128, 152) == (0, 0)
+    assert plan(1, 128 * 152, 4096, 64, 64, 152) == (0, 0)
+    assert plan(1, 128 * 152 + 1, 4096, 64, 64, 152) == (1, 4)
+    # the thresholds on 100 SMs: 20 and 45 tiles left are in, 21 and 46 not
+    assert plan(120, 100, 4096, 64, 64, 100) == (20, 4)
+    assert plan(121, 100, 4096, 64, 64, 100) == (21, 2)
+    assert plan(145, 100, 4096, 64, 64, 100) == (45, 2)
+    assert plan(146, 100, 4096, 64, 64, 100) == (0, 0)
+    # heads kernel 3 does not serve, and sizes with no work
+    assert plan(4, 5504, 5504, 160, 128, 152) == (0, 0)
+    assert plan(4, 5504, 5504, 128, 256, 152) == (0, 0)
+    for args in [(0, 4096, 4096, 128, 128, 152), (16, -1, 4096, 128, 128, 152),
+                 (16, 4096, 0, 128, 128, 152), (16, 4096, 4096, 128, 128, 0)]:
+        assert plan(*args) == (0, 0), args
+
+
+def test_attention_tail_plan_invariants():
+    """Over a grid of shapes and SM counts: a split takes exactly the tiles
+    of the last wave, into 2 to 4 ranges of at least four key blocks, and
+    leaves a last wave of at most 45 % of the SMs."""
+    for sms in (100, 132, 148, 152, 160):
+        for batch in (1, 3, 16, 40):
+            for Nq in (1, 128, 1000, 4096, 5504):
+                for Nk in (1, 512, 1023, 1024, 3000, 8192):
+                    tail, pieces = tg.tg_attention_tail_plan(batch, Nq, Nk, 128, 128, sms)
+                    tiles = batch * ((Nq + 127) // 128)
+                    n_kv = (Nk + 127) // 128
+                    if tail == 0:
+                        assert pieces == 0
+                        continue
+                    waves = (tiles + sms - 1) // sms
+                    assert waves >= 2
+                    assert tail == tiles - (waves - 1) * sms
+                    assert 100 * tail <= 45 * sms
+                    assert 2 <= pieces <= 4 and 4 * pieces <= n_kv
+                    assert pieces < 4 or 100 * tail <= 20 * sms

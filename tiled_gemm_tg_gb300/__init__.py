@@ -21,7 +21,7 @@ __all__ = [
     "tg_status_string", "tg_gemm_path", "tg_gemm_force_path", "tg_gemm_force_tiling",
     "tg_gemm_test_hook", "tg_gemm_ex", "tg_gemm_batched", "tg_gemm_batched_path",
     "tg_attention", "tg_attention_ws", "tg_attention_workspace_size", "tg_attention_noalloc",
-    "tg_attention_kernel", "tg_attention_force_kernel",
+    "tg_attention_kernel", "tg_attention_force_kernel", "tg_attention_tail_plan",
     "attention", "ACT_NONE", "ACT_RELU", "ACT_GELU",
     "tg_gemm_version", "gemm", "bmm",
     "check",
@@ -95,6 +95,9 @@ def lib() -> ctypes.CDLL:
         L.tg_attention_workspace_size.argtypes = [i64, i64, i64, i64, i64]
         L.tg_attention_kernel.restype = i32
         L.tg_attention_kernel.argtypes = [i64, i64, i64, i64, i64, i32]
+        L.tg_attention_tail_plan.restype = i32
+        L.tg_attention_tail_plan.argtypes = [i64, i64, i64, i64, i64, i32,
+                                             ctypes.POINTER(ctypes.c_int)]
         L.tg_attention_force_kernel.restype = i32
         L.tg_attention_force_kernel.argtypes = [i32]
         L.tg_gemm_check.restype = i32
@@ -186,6 +189,13 @@ def tg_gemm_path(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype) -> int:
 
 def tg_attention_kernel(batch, Nq, Nk, d, dv, split_allowed: bool = False) -> int:
     return int(lib().tg_attention_kernel(batch, Nq, Nk, d, dv, 1 if split_allowed else 0))
+
+
+def tg_attention_tail_plan(batch, Nq, Nk, d, dv, num_sms):
+    """(tiles of the last wave that are split, key ranges per tile)."""
+    p = ctypes.c_int(-1)
+    tail = int(lib().tg_attention_tail_plan(batch, Nq, Nk, d, dv, num_sms, ctypes.byref(p)))
+    return tail, int(p.value)
 
 
 def tg_attention_force_kernel(kernel: int) -> int:

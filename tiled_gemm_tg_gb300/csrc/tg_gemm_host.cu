@@ -565,6 +565,20 @@ int tg_attention_kernel(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_
                                        g_force_attn.load(std::memory_order_relaxed));
 }
 
+int tg_attention_tail_plan(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                           int num_sms, int* pieces)
+{
+    int p = 0;
+    int tail = 0;
+    if (batch > 0 && Nq > 0 && Nk > 0 && d > 0 && dv > 0 && num_sms > 0 && Nq <= kMaxDim &&
+        Nk <= kMaxDim && batch <= kMaxBatch &&
+        tg::attention_tmem_p_serves(static_cast<int>(d), static_cast<int>(dv)))
+        tail = tg::attention_tail_plan(static_cast<int>(batch), static_cast<int>(Nq),
+                                       static_cast<int>(Nk), num_sms, &p);
+    if (pieces != nullptr) *pieces = tail > 0 ? p : 0;
+    return tail;
+}
+
 tg_status tg_attention_force_kernel(int kernel)
 {
     if (!(kernel == 0 || kernel == 1 || kernel == 3)) return TG_ERR_INVALID_ARG;
