@@ -117,3 +117,49 @@ def test_attention_bounded_wait_expiry_is_reported(kernel):
     O, E, G = oracle.attention(q.numpy(), k.numpy(), v.numpy(), 0.125)
     tol = oracle.attention_tolerance(O, E, G, 64, 300, True)
     assert np.all(np.abs(o.double().cpu().numpy() - O) <= tol)
+
+
+def test_attention_tail_split_expiry_then_clean_call():
+    """The P-in-TMEM kernel with its last wave split through a workspace:
+    under the hook every CTA's wait runs out, no range merges and the tile
+    counters are left as the aborted ranges left them; the next call on the
+    same workspace (its zeroing kernel resets them) matches the oracle on
+    every head, and a third call matches the second bit for bit."""
+    import numpy as np
+
+    import oracle
+
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    batch, Nq, Nk, d = sms + 6, 128, 1024, 64   # six tiles left over: two ranges of 4 blocks
+    assert tg.tg_attention_kernel(batch, Nq, Nk, d, d, split_allowed=True) == 3
+    assert tg.tg_attention_tail_plan(batch, Nq, Nk, d, d, sms) == (6, 2)
+    need = tg.tg_attention_workspace_size(batch, Nq, Nk, d, d)
+    assert need > 0
+    g = torch.Generator().manual_seed(9500)
+    q = torch.randn(batch, Nq, d, generator=g).half()
+    k = torch.randn(batch, Nk, d, generator=g).half()
+    v = torch.randn(batch, Nk, d, generator=g).half()
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    assert tg.tg_gemm_check(s) == tg.TG_OK
+    tg.tg_gemm_test_hook(1)
+    try:
+        t0 = time.time()
+        tg.attention(qd, kd, vd, 0.125, workspace=ws)
+        assert tg.tg_gemm_check(s) == tg.TG_ERR_TIMEOUT
+        elapsed = time.time() - t0
+    finally:
+        tg.tg_gemm_test_hook(0)
+    assert 0.5 < elapsed < 60.0, elapsed
+    assert tg.tg_gemm_check(s) == tg.TG_OK
+    o = tg.attention(qd, kd, vd, 0.125, workspace=ws)
+    tg.check()
+    got = o.double().cpu().numpy()
+    for b in range(batch):
+        O, E, G = oracle.attention(q[b].numpy(), k[b].numpy(), v[b].numpy(), 0.125)
+        tol = oracle.attention_tolerance(O, E, G, d, Nk, True)
+        assert np.all(np.abs(got[b] - O) <= tol), f"head {b}"
+    again = tg.attention(qd, kd, vd, 0.125, workspace=ws)
+    tg.check()
+    assert torch.equal(again.view(torch.int16), o.view(torch.int16))
