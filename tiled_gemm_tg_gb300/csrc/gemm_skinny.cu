@@ -31,6 +31,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include "l2_prefetch.cuh"
 #include "ptx.cuh"
 #include "tc_common.cuh"
 #include "tg_internal.h"
@@ -110,6 +111,13 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmBT);
+        // this CTA's first stages into L2 while the previous kernel finishes
+        for (int kb = kb0; kb < kb1 && kb < kb0 + min(STAGES, kPrefetchStagesSingle); ++kb) {
+            for (int j = 0; j < BNT / 64; ++j)
+                tma_prefetch_l2_3d(&tmBT, n0 + j * 64, kb * BK, bz * bt.zb);
+            for (int j = 0; j < BK / 64; ++j)
+                tma_prefetch_l2_3d(&tmA, kb * BK + j * 64, 0, bz * bt.za);
+        }
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&tmem_slot), Cfg::TMEM_COLS);

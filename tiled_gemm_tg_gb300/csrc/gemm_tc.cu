@@ -46,6 +46,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include "l2_prefetch.cuh"
 #include "ptx.cuh"
 #include "tc_common.cuh"
 #include "tg_internal.h"
@@ -120,9 +121,27 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         abort_flag = 0;
         fence_mbar_init();
     }
+    constexpr int BK = KBlock<ES>::BK;
+    constexpr int NB = KBlock<ES>::NB;
+    constexpr uint32_t B_BOX = KBlock<ES>::B_BOX;
+    static_assert(BN % NB == 0, "B tile must be whole 128-byte boxes");
+    const int num_kb = (K + BK - 1) / BK;
+    const int total = tiles_m * tiles_n * bt.count;
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        // the first tile's first stages into L2 while the previous kernel finishes
+        if (static_cast<int>(blockIdx.x) < total) {
+            int b, tm, tn;
+            batch_tile_coords(static_cast<int>(blockIdx.x), tiles_m, tiles_n, group_m, b, tm, tn);
+            const int pf = total > static_cast<int>(gridDim.x) ? STAGES
+                                                                : min(STAGES, kPrefetchStagesSingle);
+            for (int kb = 0; kb < num_kb && kb < pf; ++kb) {
+                tma_prefetch_l2_3d(&tmA, kb * BK, tm * BM, b * bt.za);
+                for (int j = 0; j < BN / NB; ++j)
+                    tma_prefetch_l2_3d(&tmB, tn * BN + j * NB, kb * BK, b * bt.zb);
+            }
+        }
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&tmem_slot), Cfg::TMEM_COLS);
@@ -134,12 +153,6 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const uint32_t tmem_base = tmem_slot;
     pdl_wait();  // the previous kernel on the stream is complete from here on
 
-    constexpr int BK = KBlock<ES>::BK;
-    constexpr int NB = KBlock<ES>::NB;
-    constexpr uint32_t B_BOX = KBlock<ES>::B_BOX;
-    static_assert(BN % NB == 0, "B tile must be whole 128-byte boxes");
-    const int num_kb = (K + BK - 1) / BK;
-    const int total = tiles_m * tiles_n * bt.count;
     // The epilogue waits for a whole tile's main loop; allow ~64 us per k-block
     // on top of the base limit so long-K problems never time out spuriously.
     const uint32_t epi_limit = kSlowPolls + 64u * static_cast<uint32_t>(min(num_kb, 1 << 20));
