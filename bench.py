@@ -63,7 +63,9 @@ ATTN_KERNEL_SOURCES = ["tiled_gemm_tg_gb300/csrc/attention_fwd2.cu", "tiled_gemm
 # memory, from one ncu capture, valid while its sources hash the same
 ATTN_NCU_TRAFFIC = {
     # the kernel's ncu summary under profiles/: 50.4 MB read + 1.4 MB written
-    "attn_16x4096x128": {"bytes": 51794176, "kernel_hash": "7adf12e0ed838ea7"},
+    # (taken on 7adf12e0ed838ea7; the source has changed since in its header
+    # comment only)
+    "attn_16x4096x128": {"bytes": 51794176, "kernel_hash": "81e5a2daac910ddb"},
 }
 
 

@@ -36,6 +36,16 @@
 // reads TMEM lane quadrant w % 4; two warps per quadrant split the keys).
 // Every wait is bounded: on expiry a role records it in the device error
 // word, raises the CTA's abort flag and winds down.
+//
+// The grid is one CTA per tile (128 query rows of one batch entry), issued
+// in waves of one tile per SM.  Given a workspace, the tiles of a short last
+// wave are each cut into 2 or 4 consecutive ranges of key blocks, one CTA
+// per range (attention_tail_plan says which): a range writes its
+// unnormalised O, maximum and normaliser to the workspace, counts itself on
+// the tile's counter, and the range that counts last merges all of them in
+// range order, the same merge the blockwise pass applies between blocks.  A
+// one-CTA kernel zeroes the counters first.  The dispatcher hands the short
+// ranges to SMs as they free up, so the SMs finish closer together.
 #include <cstdint>
 #include <mutex>
 #include <type_traits>
