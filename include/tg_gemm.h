@@ -95,8 +95,13 @@ typedef enum {
  *   TG_ERR_CUDA         a CUDA call made while launching failed.
  *
  * Ownership and memory: the caller owns A, B and C.  The library allocates
- * no device memory per call; it keeps only per-device launch attributes and
- * a 4-byte device error word for bounded-wait failures.
+ * no device memory per call; it keeps only per-device launch attributes, a
+ * 4-byte device error word for bounded-wait failures (its address looked up
+ * on the first call on each device), and a host-side cache of encoded TMA
+ * descriptors keyed by pointer, sizes and strides (a repeated call with the
+ * same operands skips the encoding).  This per-device state belongs to the
+ * device's primary context: after cudaDeviceReset on a device, do not call
+ * the library on that device again in the same process.
  *
  * Asynchrony: the call only enqueues work on `stream` and returns; it never
  * synchronizes.  A kernel that times out on a bounded wait records that in
@@ -296,24 +301,34 @@ tg_status tg_attention_ws(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int6
 size_t tg_attention_workspace_size(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv);
 
 /*
- * tg_attention_noalloc -- tg_attention with the key split's partial results
- * in the library's own file-scope device scratch instead of a caller
- * workspace.  The pages have no counterpart of this entry point: it exists
- * so that a caller can get the split without allocating anything.
+ * tg_attention_noalloc -- tg_attention_ws with the partial results of its
+ * splits (the key split, and the split of a short last wave) in the
+ * library's own file-scope device scratch instead of a caller workspace.
+ * The pages have no counterpart of this entry point: it exists for callers
+ * that cannot allocate device memory at call time (code running under a
+ * memory pool or allocator they do not own, or inside a region where an
+ * allocation would synchronise the device).
  *
  * Arguments, semantics and errors are those of tg_attention, plus:
- *   - the scratch is a fixed 16 MB static device array (per device, its
- *     address looked up once); a call whose key split needs more returns
- *     TG_ERR_UNSUPPORTED (tg_attention_workspace_size tells the need), a
- *     call whose split of the last wave needs more runs without it, and a
- *     call that needs no split runs the single pass;
- *   - nothing in the scratch has to start at zero: every partial is written
- *     before the combine kernel reads it;
+ *   - the scratch is a fixed 16 MB static device array, held by every GPU
+ *     that loads the library until the process exits; a call whose key
+ *     split needs more returns TG_ERR_UNSUPPORTED
+ *     (tg_attention_workspace_size tells the need), a call whose split of
+ *     the last wave would need more runs without it, and a call that needs
+ *     no split runs the single pass;
+ *   - the first call on a device looks up the scratch's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first
+ *     call before any stream capture on the device;
+ *   - the key split writes every partial before the combine kernel reads
+ *     it, and the last-wave split's per-tile counters are zeroed by a small
+ *     kernel in every call, so nothing left in the scratch by an earlier
+ *     call is read;
  *   - no device memory is allocated or freed, ever;
  *   - all calls on a device share the scratch, so calls that overlap in time
  *     (on different streams, or from different host threads without
  *     ordering) race on it and give undefined results.  Serialise them, or
  *     use tg_attention_ws with one workspace per stream.
+ *   - tg_attention_force_kernel is read once per call.
  */
 tg_status tg_attention_noalloc(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
                                const void* Q, int64_t ldq, int64_t strideQ,

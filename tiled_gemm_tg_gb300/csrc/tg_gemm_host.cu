@@ -314,6 +314,63 @@ tg_status run(int path, const Problem& p, const tg::Epilogue& epi, tg_stream_t s
 
 namespace tg {
 
+namespace {
+
+// Encoded tensor maps, keyed by every argument of encode_tmap (the encoded
+// bytes depend on nothing else: the swizzle, L2 promotion and fill mode are
+// fixed).  A call that repeats a previous call's operands (the usual case:
+// the same buffers every step) copies 128 bytes instead of encoding again.
+// Direct-mapped; a colliding key replaces the entry.  Guarded by a mutex.
+struct TmapKey {
+    const void* ptr;
+    uint64_t cols, rows, ld, batch, stride;
+    uint32_t box_cols, box_rows;
+    int es;
+    bool operator==(const TmapKey& o) const
+    {
+        return ptr == o.ptr && cols == o.cols && rows == o.rows && ld == o.ld &&
+               batch == o.batch && stride == o.stride && box_cols == o.box_cols &&
+               box_rows == o.box_rows && es == o.es;
+    }
+};
+
+struct TmapEntry {
+    bool used = false;
+    TmapKey key{};
+    CUtensorMap map{};
+};
+
+constexpr int kTmapCacheSize = 1024;
+std::mutex g_tmap_mu;
+TmapEntry g_tmap_cache[kTmapCacheSize];
+
+uint64_t mix(uint64_t h, uint64_t v)
+{
+    // splitmix64 finaliser over the running hash
+    h ^= v + 0x9e3779b97f4a7c15ULL + (h << 6) + (h >> 2);
+    h ^= h >> 30;
+    h *= 0xbf58476d1ce4e5b9ULL;
+    h ^= h >> 27;
+    h *= 0x94d049bb133111ebULL;
+    h ^= h >> 31;
+    return h;
+}
+
+int tmap_slot(const TmapKey& k)
+{
+    uint64_t h = reinterpret_cast<uintptr_t>(k.ptr);
+    h = mix(h, k.cols);
+    h = mix(h, k.rows);
+    h = mix(h, k.ld);
+    h = mix(h, k.batch);
+    h = mix(h, k.stride);
+    h = mix(h, (static_cast<uint64_t>(k.box_cols) << 32) | k.box_rows);
+    h = mix(h, static_cast<uint64_t>(k.es));
+    return static_cast<int>(h % kTmapCacheSize);
+}
+
+}  // namespace
+
 bool encode_tmap(CUtensorMap* map, const void* ptr, int es, uint64_t cols, uint64_t rows,
                  uint64_t ld, uint64_t batch, uint64_t stride, uint32_t box_cols,
                  uint32_t box_rows)
@@ -325,6 +382,16 @@ bool encode_tmap(CUtensorMap* map, const void* ptr, int es, uint64_t cols, uint6
         batch = 1;
         stride = (rows * ld * es + 15) / 16 * 16 / es;
     }
+    const TmapKey key{ptr, cols, rows, ld, batch, stride, box_cols, box_rows, es};
+    const int slot = tmap_slot(key);
+    {
+        std::lock_guard<std::mutex> lock(g_tmap_mu);
+        const TmapEntry& e = g_tmap_cache[slot];
+        if (e.used && e.key == key) {
+            *map = e.map;
+            return true;
+        }
+    }
     cuuint64_t dims[3] = {cols, rows, batch};
     cuuint64_t strides[2] = {ld * es, stride * es};
     cuuint32_t box[3] = {box_cols, box_rows, 1};
@@ -335,7 +402,13 @@ bool encode_tmap(CUtensorMap* map, const void* ptr, int es, uint64_t cols, uint6
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    if (r != CUDA_SUCCESS) return false;
+    std::lock_guard<std::mutex> lock(g_tmap_mu);
+    TmapEntry& e = g_tmap_cache[slot];
+    e.used = true;
+    e.key = key;
+    e.map = *map;
+    return true;
 }
 
 }  // namespace tg
@@ -383,12 +456,18 @@ tg_status tg_gemm_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda
     return run(path, p, epi, stream);
 }
 
-tg_status tg_attention_ws(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
-                          const void* Q, int64_t ldq, int64_t strideQ, const void* K, int64_t ldk,
-                          int64_t strideK, const void* V, int64_t ldv, int64_t strideV, void* O,
-                          int64_t ldo, int64_t strideO, float scale, tg_dtype in_dtype,
-                          tg_dtype out_dtype, void* workspace, size_t workspace_bytes,
-                          tg_stream_t stream)
+}  // extern "C"
+
+namespace {
+
+// tg_attention_ws with the kernel override passed in (read once by the
+// caller, so that every decision of one call sees the same value).
+tg_status attention_impl(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                         const void* Q, int64_t ldq, int64_t strideQ, const void* K, int64_t ldk,
+                         int64_t strideK, const void* V, int64_t ldv, int64_t strideV, void* O,
+                         int64_t ldo, int64_t strideO, float scale, tg_dtype in_dtype,
+                         tg_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                         tg_stream_t stream, int forced)
 {
     if (batch < 0 || Nq < 0 || Nk < 0 || d < 0 || dv < 0) return TG_ERR_INVALID_ARG;
     if (strideQ < 0 || strideK < 0 || strideV < 0 || strideO < 0) return TG_ERR_INVALID_ARG;
@@ -436,7 +515,7 @@ tg_status tg_attention_ws(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int6
     const bool ws_ok = need > 0 && workspace != nullptr && workspace_bytes >= need;
     const int choice = tg::attention_kernel_choice(
         static_cast<int>(batch), static_cast<int>(Nq), static_cast<int>(Nk), static_cast<int>(d),
-        static_cast<int>(dv), ds->num_sms, ws_ok, g_force_attn.load(std::memory_order_relaxed));
+        static_cast<int>(dv), ds->num_sms, ws_ok, forced);
     const bool split = choice == 2;
     // the P-in-TMEM kernel cuts the tiles of a short last wave in two along
     // the keys when the workspace holds the halves' partial results
@@ -489,6 +568,65 @@ tg_status tg_attention_ws(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int6
     return tg::launch_attention(a) == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
 
+bool attention_sizes_ok(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv)
+{
+    if (batch <= 0 || Nq <= 0 || Nk <= 0 || d <= 0 || dv <= 0) return false;
+    return !(Nq > kMaxDim || Nk > kMaxDim || d > kMaxDim || dv > 65535LL * 128 ||
+             batch > kMaxBatch);
+}
+
+// tg_attention_workspace_size with the kernel override passed in.
+size_t workspace_size_impl(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                           int forced)
+{
+    if (!attention_sizes_ok(batch, Nq, Nk, d, dv)) return 0;
+    DeviceState* ds = nullptr;
+    if (device_state(&ds) != TG_OK) return 0;
+    const size_t split = tg::attention_ws_bytes(static_cast<int>(batch), static_cast<int>(Nq),
+                                                static_cast<int>(Nk), static_cast<int>(dv),
+                                                ds->num_sms);
+    const int choice = tg::attention_kernel_choice(
+        static_cast<int>(batch), static_cast<int>(Nq), static_cast<int>(Nk), static_cast<int>(d),
+        static_cast<int>(dv), ds->num_sms, split > 0, forced);
+    if (choice == 2) return split;
+    if (choice == 3)
+        return tg::attention_tail_ws_bytes(static_cast<int>(batch), static_cast<int>(Nq),
+                                           static_cast<int>(Nk), ds->num_sms);
+    return 0;
+}
+
+// tg_attention_kernel with the kernel override passed in.
+int kernel_choice_impl(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                       int split_allowed, int forced)
+{
+    if (!attention_sizes_ok(batch, Nq, Nk, d, dv)) return 0;
+    DeviceState* ds = nullptr;
+    if (device_state(&ds) != TG_OK) return 0;
+    const bool ws_ok = split_allowed != 0 &&
+                       tg::attention_ws_bytes(static_cast<int>(batch), static_cast<int>(Nq),
+                                              static_cast<int>(Nk), static_cast<int>(dv),
+                                              ds->num_sms) > 0;
+    return tg::attention_kernel_choice(static_cast<int>(batch), static_cast<int>(Nq),
+                                       static_cast<int>(Nk), static_cast<int>(d),
+                                       static_cast<int>(dv), ds->num_sms, ws_ok, forced);
+}
+
+}  // namespace
+
+extern "C" {
+
+tg_status tg_attention_ws(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
+                          const void* Q, int64_t ldq, int64_t strideQ, const void* K, int64_t ldk,
+                          int64_t strideK, const void* V, int64_t ldv, int64_t strideV, void* O,
+                          int64_t ldo, int64_t strideO, float scale, tg_dtype in_dtype,
+                          tg_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                          tg_stream_t stream)
+{
+    return attention_impl(batch, Nq, Nk, d, dv, Q, ldq, strideQ, K, ldk, strideK, V, ldv, strideV,
+                          O, ldo, strideO, scale, in_dtype, out_dtype, workspace, workspace_bytes,
+                          stream, g_force_attn.load(std::memory_order_relaxed));
+}
+
 tg_status tg_attention(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
                        const void* Q, int64_t ldq, int64_t strideQ, const void* K, int64_t ldk,
                        int64_t strideK, const void* V, int64_t ldv, int64_t strideV, void* O,
@@ -506,63 +644,40 @@ tg_status tg_attention_noalloc(int64_t batch, int64_t Nq, int64_t Nk, int64_t d,
                                int64_t strideV, void* O, int64_t ldo, int64_t strideO, float scale,
                                tg_dtype in_dtype, tg_dtype out_dtype, tg_stream_t stream)
 {
-    const size_t need = tg_attention_workspace_size(batch, Nq, Nk, d, dv);
-    if (need == 0)  // no split (or invalid arguments, which tg_attention_ws reports)
-        return tg_attention_ws(batch, Nq, Nk, d, dv, Q, ldq, strideQ, K, ldk, strideK, V, ldv,
-                               strideV, O, ldo, strideO, scale, in_dtype, out_dtype, nullptr, 0,
-                               stream);
+    // one read of the override: the need, the choice below and the launch
+    // all see the same kernel selection
+    const int forced = g_force_attn.load(std::memory_order_relaxed);
+    const size_t need = workspace_size_impl(batch, Nq, Nk, d, dv, forced);
+    if (need == 0)  // no split (or invalid arguments, which attention_impl reports)
+        return attention_impl(batch, Nq, Nk, d, dv, Q, ldq, strideQ, K, ldk, strideK, V, ldv,
+                              strideV, O, ldo, strideO, scale, in_dtype, out_dtype, nullptr, 0,
+                              stream, forced);
     size_t bytes = 0;
     void* scratch = tg::attention_static_scratch(&bytes);
     if (scratch == nullptr) return TG_ERR_CUDA;
     if (need > bytes) {
         // the key split needs more than the static scratch; a split of the
         // last wave only saves time, and the call runs without it
-        if (tg_attention_kernel(batch, Nq, Nk, d, dv, 1) != 3) return TG_ERR_UNSUPPORTED;
-        return tg_attention_ws(batch, Nq, Nk, d, dv, Q, ldq, strideQ, K, ldk, strideK, V, ldv,
-                               strideV, O, ldo, strideO, scale, in_dtype, out_dtype, nullptr, 0,
-                               stream);
+        if (kernel_choice_impl(batch, Nq, Nk, d, dv, 1, forced) != 3) return TG_ERR_UNSUPPORTED;
+        return attention_impl(batch, Nq, Nk, d, dv, Q, ldq, strideQ, K, ldk, strideK, V, ldv,
+                              strideV, O, ldo, strideO, scale, in_dtype, out_dtype, nullptr, 0,
+                              stream, forced);
     }
-    return tg_attention_ws(batch, Nq, Nk, d, dv, Q, ldq, strideQ, K, ldk, strideK, V, ldv,
-                           strideV, O, ldo, strideO, scale, in_dtype, out_dtype, scratch, bytes,
-                           stream);
+    return attention_impl(batch, Nq, Nk, d, dv, Q, ldq, strideQ, K, ldk, strideK, V, ldv, strideV,
+                          O, ldo, strideO, scale, in_dtype, out_dtype, scratch, bytes, stream,
+                          forced);
 }
 
 size_t tg_attention_workspace_size(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv)
 {
-    if (batch <= 0 || Nq <= 0 || Nk <= 0 || d <= 0 || dv <= 0) return 0;
-    if (Nq > kMaxDim || Nk > kMaxDim || d > kMaxDim || dv > 65535LL * 128 || batch > kMaxBatch)
-        return 0;
-    DeviceState* ds = nullptr;
-    if (device_state(&ds) != TG_OK) return 0;
-    const size_t split = tg::attention_ws_bytes(static_cast<int>(batch), static_cast<int>(Nq),
-                                                static_cast<int>(Nk), static_cast<int>(dv),
-                                                ds->num_sms);
-    const int choice = tg::attention_kernel_choice(
-        static_cast<int>(batch), static_cast<int>(Nq), static_cast<int>(Nk), static_cast<int>(d),
-        static_cast<int>(dv), ds->num_sms, split > 0, g_force_attn.load(std::memory_order_relaxed));
-    if (choice == 2) return split;
-    if (choice == 3)
-        return tg::attention_tail_ws_bytes(static_cast<int>(batch), static_cast<int>(Nq),
-                                           static_cast<int>(Nk), ds->num_sms);
-    return 0;
+    return workspace_size_impl(batch, Nq, Nk, d, dv, g_force_attn.load(std::memory_order_relaxed));
 }
 
 int tg_attention_kernel(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
                         int split_allowed)
 {
-    if (batch <= 0 || Nq <= 0 || Nk <= 0 || d <= 0 || dv <= 0) return 0;
-    if (Nq > kMaxDim || Nk > kMaxDim || d > kMaxDim || dv > 65535LL * 128 || batch > kMaxBatch)
-        return 0;
-    DeviceState* ds = nullptr;
-    if (device_state(&ds) != TG_OK) return 0;
-    const bool ws_ok = split_allowed != 0 &&
-                       tg::attention_ws_bytes(static_cast<int>(batch), static_cast<int>(Nq),
-                                              static_cast<int>(Nk), static_cast<int>(dv),
-                                              ds->num_sms) > 0;
-    return tg::attention_kernel_choice(static_cast<int>(batch), static_cast<int>(Nq),
-                                       static_cast<int>(Nk), static_cast<int>(d),
-                                       static_cast<int>(dv), ds->num_sms, ws_ok,
-                                       g_force_attn.load(std::memory_order_relaxed));
+    return kernel_choice_impl(batch, Nq, Nk, d, dv, split_allowed,
+                              g_force_attn.load(std::memory_order_relaxed));
 }
 
 int tg_attention_tail_plan(int64_t batch, int64_t Nq, int64_t Nk, int64_t d, int64_t dv,
