@@ -403,6 +403,31 @@ void tg_gemm_test_hook(int hook);
 tg_status tg_gemm_force_tiling(int bn, int group_m);
 
 /*
+ * Last-wave override of the CTA-pair kernel (path 6), for tests and
+ * benchmarks.  The pair kernel hands its 256 x 256 tiles to the CTA pairs
+ * in waves; when the last wave is at most half full, it cuts each of that
+ * wave's tiles into two 256 x 128 halves so that twice as many pairs share
+ * it (fp16 inputs; E4M3 calls never cut).
+ *   tiles  -1: automatic (the rule above); 0: never cut; k > 0: cut the
+ *          last k tiles of every call (capped at the call's tile count),
+ *          whatever the wave shape.
+ * Process-wide; stays in force until changed.  Returns TG_ERR_INVALID_ARG
+ * (and changes nothing) for tiles < -1.  Results are the same either way.
+ */
+tg_status tg_gemm_force_split_tail(int tiles);
+
+/*
+ * The automatic rule above, computed on the host alone (no device needed):
+ * how many of `tiles` 256 x 256 tiles (all products of a call together) the
+ * pair kernel cuts in two on a GPU that holds `max_pairs` CTA pairs at once
+ * (half the SM count when the kernel fills every SM).  The last wave holds
+ * last = tiles - max_pairs * floor((tiles - 1) / max_pairs) tiles; they are
+ * all cut when 2 * last <= max_pairs, else none.  0 for non-positive
+ * arguments.
+ */
+int tg_gemm_pair_split_tail(int64_t tiles, int max_pairs);
+
+/*
  * Attention kernel selection, for tests and benchmarks.  tg_attention_kernel
  * reports, without launching anything, which forward kernel a call with these
  * sizes would run on the current device: tg_attention (split_allowed = 0),

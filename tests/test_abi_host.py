@@ -460,3 +460,26 @@ def test_attention_tail_plan_invariants():
                     assert 100 * tail <= 45 * sms
                     assert 2 <= pieces <= 4 and 4 * pieces <= n_kv
                     assert pieces < 4 or 100 * tail <= 20 * sms
+
+
+@pytest.mark.parametrize("tiles,pairs,want", [
+    (1024, 76, 36),    # 8192^3: 13 whole waves and 36 tiles, cut into 72 halves
+    (1024, 74, 0),     # 13 waves and 62 tiles: more than half a wave, none cut
+    (77, 76, 1), (152, 76, 0), (153, 76, 1), (100, 76, 24), (114, 76, 38), (115, 76, 0),
+    (64, 76, 0),       # one wave, 128 halves would not fit
+    (38, 76, 38), (39, 76, 0), (1, 76, 1), (1, 1, 0), (5, 2, 1),
+    (0, 76, 0), (10, 0, 0), (-3, 76, 0),
+])
+def test_pair_split_tail_rule(tiles, pairs, want):
+    """The short-last-wave rule of the pair kernel, on the host."""
+    got = tg.tg_gemm_pair_split_tail(tiles, pairs)
+    assert got == want
+    if got:
+        last = tiles - pairs * ((tiles - 1) // pairs)
+        assert got == last and 2 * last <= pairs
+
+
+def test_force_split_tail_arguments():
+    assert tg.tg_gemm_force_split_tail(-2) == tg.TG_ERR_INVALID_ARG
+    for v in (0, 5, -1):
+        assert tg.tg_gemm_force_split_tail(v) == tg.TG_OK

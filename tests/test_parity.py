@@ -375,6 +375,52 @@ def test_pair_kernel_integer_bitwise_77_tiles(out):
         assert np.array_equal(got, C_ref)
 
 
+@pytest.mark.parametrize("M,N,K,split", [(512, 768, 1024, 6), (700, 1000, 640, 3),
+                                         (1792, 2816, 2048, -1), (2000, 2600, 1000, -1),
+                                         (256, 200, 300, 1), (300, 136, 520, 2)])
+@pytest.mark.parametrize("out", [torch.float16, torch.float32])
+def test_pair_kernel_half_tiles_bitwise(M, N, K, split, out):
+    """Tiles cut into two 256 x 128 halves (the short last wave, forced onto
+    small shapes, or chosen by the rule: 77 and 88 tiles on 76 pairs), ragged
+    halves and halves wholly past N included: bit for bit equal to the
+    oracle on integer inputs, and to the same call with no tile cut."""
+    a = inputs.draw((M, K), "int2", 9001 + M, "f16")
+    b = inputs.draw((K, N), "int2", 9002 + N, "f16")
+    pad = lambda x: (x + 7) // 8 * 8  # noqa: E731
+    tg.tg_gemm_force_path(PAIR)
+    try:
+        assert tg.tg_gemm_force_split_tail(split) == tg.TG_OK
+        got, intact, p = run(a, b, out, lda=pad(K), ldb=pad(N), ldc=N + 1)
+        assert tg.tg_gemm_force_split_tail(0) == tg.TG_OK
+        plain, intact2, _ = run(a, b, out, lda=pad(K), ldb=pad(N), ldc=N + 1)
+    finally:
+        tg.tg_gemm_force_split_tail(-1)
+        tg.tg_gemm_force_path(0)
+    assert p == PAIR and intact and intact2
+    C_ref, _ = oracle.gemm(a.numpy(), b.numpy())
+    if out == torch.float16:
+        have = torch.from_numpy(got).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(have, f16_bits_of(C_ref))
+    else:
+        assert np.array_equal(got, C_ref)
+    assert np.array_equal(got, plain)
+
+
+def test_pair_kernel_half_tiles_random():
+    """Random fp16 inputs with every tile of the call cut (sampled rows of a
+    4-tile problem with ragged M and N), against the oracle's bound."""
+    a = inputs.draw((600, 1200), "normal", 9101, "f16")
+    b = inputs.draw((1200, 700), "normal", 9102, "f16")
+    tg.tg_gemm_force_path(PAIR)
+    try:
+        assert tg.tg_gemm_force_split_tail(1 << 20) == tg.TG_OK
+        _, _, p = check_full(a, b, torch.float16, ldb=704)
+    finally:
+        tg.tg_gemm_force_split_tail(-1)
+        tg.tg_gemm_force_path(0)
+    assert p == PAIR
+
+
 def test_pair_kernel_repeated_calls_agree():
     """Back-to-back calls on one stream give the same exact result."""
     M, N, K = 1792, 2816, 1024

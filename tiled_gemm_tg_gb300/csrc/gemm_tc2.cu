@@ -94,12 +94,34 @@ constexpr int L2_HINTS = TG_PAIR_L2_HINTS;  // bit 0: A evict_last, bit 1: B evi
 #endif
 constexpr int EPI_COLS = TG_PAIR_EPI_COLS;  // accumulator columns per tcgen05.ld
 
+// Work item t of the pair kernel: tile t in the grouped order over the
+// whole batch (half = -1), or, among the last `split_tail` tiles, one half
+// of a tile: items past the whole tiles go two to a tile, half 0 for its
+// columns 0..127 and half 1 for 128..255.  fp16 only (an E4M3 half would
+// need a 64-byte-wide B box).
+template <int ES>
+__device__ __forceinline__ void work_item(int t, int tiles_m, int tiles_n, int group_m, int whole,
+                                          int split_tail, int& b, int& tm, int& tn, int& half)
+{
+    half = -1;
+    int tile = t;
+    if (ES == 2 && split_tail > 0) {
+        const int first = whole - split_tail;  // the first tile cut in two
+        if (t >= first) {
+            const int h = t - first;
+            tile = first + (h >> 1);
+            half = h & 1;
+        }
+    }
+    batch_tile_coords(tile, tiles_m, tiles_n, group_m, b, tm, tn);
+}
+
 template <bool OUT_F32, int ES>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     void* C, long long ldc, int M, int N, int K, int tiles_m,
-                    int tiles_n, int group_m, int c_vec, int hook, unsigned int* err,
-                    Epilogue epi, BatchArgs bt)
+                    int tiles_n, int group_m, int split_tail, int c_vec, int hook,
+                    unsigned int* err, Epilogue epi, BatchArgs bt)
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[STAGES];   // used in the leader only
@@ -148,7 +170,11 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     using KG = PairK<ES>;
     constexpr int BK = KG::BK;
     const int num_kb = (K + BK - 1) / BK;
-    const int total = tiles_m * tiles_n * bt.count;
+    // Work items: the tiles in the grouped order, except that the last
+    // split_tail tiles (a short last wave) are each cut into two 256 x 128
+    // halves, two items each, so that twice as many pairs share that wave.
+    const int whole = tiles_m * tiles_n * bt.count;
+    const int total = whole + (ES == 2 ? split_tail : 0);
     const uint32_t epi_limit = kSlowPolls + 64u * static_cast<uint32_t>(min(num_kb, 1 << 20));
 
     if (warp == 0) {
@@ -164,11 +190,15 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t issued = 0;
             bool ok = true;
             for (int t = pair; t < total && ok; t += npairs) {
-                int b, tm, tn;
-                batch_tile_coords(t, tiles_m, tiles_n, group_m, b, tm, tn);
+                int b, tm, tn, half;
+                work_item<ES>(t, tiles_m, tiles_n, group_m, whole, split_tail, b, tm, tn, half);
                 const int za = b * bt.za, zb = b * bt.zb;
                 const int row = tm * PM + static_cast<int>(rank) * HM;
-                const int col = tn * PN + static_cast<int>(rank) * HN;
+                // a half item: each CTA holds 64 of its 128 columns (one box)
+                const int col = half < 0 ? tn * PN + static_cast<int>(rank) * HN
+                                         : tn * PN + half * HN + static_cast<int>(rank) * (HN / 2);
+                const int nbox = half < 0 ? HN / KG::NB : 1;
+                const uint32_t stage_bytes = A_STAGE + static_cast<uint32_t>(nbox) * KG::B_BOX;
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1u, &abort_flag)) {
                         abort_flag = 1;
@@ -185,15 +215,14 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         }
                         continue;
                     }
-                    if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[s]), 2 * STAGE);
+                    if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[s]), 2 * stage_bytes);
                     const uint32_t fb = full0 + 8u * static_cast<uint32_t>(s);
                     const uint32_t sa = base + s * STAGE;
 #pragma unroll
                     for (int j = 0; j < KA; ++j)
                         tma_load_3d_pair_hint(sa + j * A_ATOM, &tmA, fb, kb * BK + j * KG::AE,
                                               row, za, pol_a);
-#pragma unroll
-                    for (int j = 0; j < HN / KG::NB; ++j)
+                    for (int j = 0; j < nbox; ++j)
                         tma_load_3d_pair_hint(sa + A_STAGE + j * KG::B_BOX, &tmB, fb,
                                               col + j * KG::NB, kb * BK, zb, pol_b);
                     ++issued;
@@ -223,13 +252,17 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     } else if (warp == 1) {
         // ------------------------------------------- MMA issuer (leader only)
         if (leader && lane == 0) {
-            constexpr uint32_t idesc = idesc_f16_f32(PM, PN, false, true);
+            constexpr uint32_t idesc_full = idesc_f16_f32(PM, PN, false, true);
+            constexpr uint32_t idesc_half = idesc_f16_f32(PM, PN / 2, false, true);
             int s = 0;
             uint32_t ph = 0;
             int acc = 0;
             uint32_t aph = 0;
             bool ok = true;
             for (int t = pair; t < total && ok; t += npairs) {
+                int b, tm, tn, half;
+                work_item<ES>(t, tiles_m, tiles_n, group_m, whole, split_tail, b, tm, tn, half);
+                const uint32_t idesc = half < 0 ? idesc_full : idesc_half;
                 if (!mbar_wait(smem_u32(&tempty_bar[acc]), aph ^ 1u, &abort_flag)) {
                     ok = false;
                     break;
@@ -275,14 +308,19 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     } else {
         // ------------------------------------------------------- epilogue
         const int q = warp & 3;                       // TMEM lane quadrant of this warp
-        const int c_lo = ((warp - 2) >> 2) * EPI_SPAN;  // its first accumulator column
+        const int wcol = (warp - 2) >> 2;             // which share of the columns
         const uint32_t tempty0 = mapa_shared(smem_u32(&tempty_bar[0]), 0);  // leader's
         int acc = 0;
         uint32_t aph = 0;
         for (int t = pair; t < total; t += npairs) {
-            int b, tm, tn;
-            batch_tile_coords(t, tiles_m, tiles_n, group_m, b, tm, tn);
+            int b, tm, tn, half;
+            work_item<ES>(t, tiles_m, tiles_n, group_m, whole, split_tail, b, tm, tn, half);
             void* Cb = batch_ptr(C, b, bt.sC, OUT_F32 ? 4 : 2);
+            // a half item's accumulator has 128 columns, for output columns
+            // from tn * 256 + half * 128
+            const int span = half < 0 ? EPI_SPAN : EPI_SPAN / 2;
+            const int c_lo = wcol * span;
+            const int n0 = tn * PN + (half < 0 ? 0 : half * HN);
             const bool got = mbar_wait(smem_u32(&tfull_bar[acc]), aph, &abort_flag, epi_limit);
             if (!__all_sync(0xffffffffu, got)) {
                 if (lane == 0) {
@@ -296,7 +334,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * PN);
 #pragma unroll 1
-            for (int c = c_lo; c < c_lo + EPI_SPAN; c += EPI_COLS) {
+            for (int c = c_lo; c < c_lo + span; c += EPI_COLS) {
                 uint32_t r[EPI_COLS];
                 if constexpr (EPI_COLS == 128) tmem_ld_32x32b_x128(taddr + c, r);
                 else if constexpr (EPI_COLS == 64) tmem_ld_32x32b_x64(taddr + c, r);
@@ -304,7 +342,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < EPI_COLS; j += 32) {
-                    const int n = tn * PN + c + j;
+                    const int n = n0 + c + j;
                     if (m < M && n < N) {
                         if (epi.on) epilogue_chunk<OUT_F32>(r + j, m, n, N, epi);
                         store_chunk<OUT_F32>(Cb, ldc, m, n, N, r + j, c_vec != 0);
@@ -377,7 +415,9 @@ cudaError_t launch_cfg(const GemmArgs& a)
     const int tiles_m = (a.M + PM - 1) / PM;
     const int tiles_n = (a.N + PN - 1) / PN;
     const int total = tiles_m * tiles_n * a.batch;
-    const int pairs = total < max_clusters ? total : max_clusters;
+    const int split_tail = ES == 2 ? pair_split_tail(total, max_clusters, a.split_tail) : 0;
+    const int items = total + split_tail;
+    const int pairs = items < max_clusters ? items : max_clusters;
     const int group_m = a.group_m > 0 ? a.group_m : 8;
     const size_t es = OUT_F32 ? 4 : 2;
     const int c_vec = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) &&
@@ -398,10 +438,23 @@ cudaError_t launch_cfg(const GemmArgs& a)
     cfg.attrs = at;
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kernel, ta, tb, a.C, a.ldc, a.M, a.N, a.K, tiles_m, tiles_n,
-                              group_m, c_vec, a.hook, a.err, a.epi, a.batch_args());
+                              group_m, split_tail, c_vec, a.hook, a.err, a.epi, a.batch_args());
 }
 
 }  // namespace
+
+int pair_split_tail(int total, int max_pairs, int forced)
+{
+    if (total <= 0 || max_pairs <= 0) return 0;
+    if (forced >= 0) return forced < total ? forced : total;
+    // Tiles go to the pairs in waves of max_pairs.  The last wave holds
+    // `last` tiles; when twice that many fit in one wave, each of them is
+    // cut into two 256 x 128 halves.  An M = 256, N = 128 pair MMA costs
+    // ~98 cycles against ~128 for N = 256 (measured), so the wave then takes
+    // ~0.77 of a whole-tile wave, on twice as many pairs.
+    const int last = total - max_pairs * ((total - 1) / max_pairs);
+    return 2 * last <= max_pairs ? last : 0;
+}
 
 int pair_tiles(int M, int N)
 {

@@ -43,6 +43,7 @@ std::atomic<int> g_test_hook{0};
 std::atomic<int> g_force_bn{0};
 std::atomic<int> g_force_group{0};
 std::atomic<int> g_force_attn{0};
+std::atomic<int> g_force_split_tail{-1};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 tg_status device_state(DeviceState** out)
@@ -289,6 +290,7 @@ tg_status run(int path, const Problem& p, const tg::Epilogue& epi, tg_stream_t s
     a.err = ds->err;
     a.hook = g_test_hook.load(std::memory_order_relaxed);
     a.group_m = g_force_group.load(std::memory_order_relaxed);
+    a.split_tail = g_force_split_tail.load(std::memory_order_relaxed);
     a.num_sms = ds->num_sms;
     a.stream = s;
     a.epi = epi;
@@ -768,6 +770,19 @@ tg_status tg_gemm_force_tiling(int bn, int group_m)
     g_force_bn.store(bn, std::memory_order_relaxed);
     g_force_group.store(group_m, std::memory_order_relaxed);
     return TG_OK;
+}
+
+tg_status tg_gemm_force_split_tail(int tiles)
+{
+    if (tiles < -1) return TG_ERR_INVALID_ARG;
+    g_force_split_tail.store(tiles, std::memory_order_relaxed);
+    return TG_OK;
+}
+
+int tg_gemm_pair_split_tail(int64_t tiles, int max_pairs)
+{
+    if (tiles <= 0 || max_pairs <= 0 || tiles >= (int64_t(1) << 31)) return 0;
+    return tg::pair_split_tail(static_cast<int>(tiles), max_pairs, -1);
 }
 
 int tg_gemm_version(void) { return 100; }

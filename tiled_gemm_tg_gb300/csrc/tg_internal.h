@@ -89,6 +89,7 @@ struct GemmArgs {
     unsigned int* err;  // device error word
     int hook;           // test hook (0 = off), see tg_gemm_test_hook
     int group_m;        // grouped tile-order height, 0 = the kernel's default
+    int split_tail = -1;  // pair kernel: tiles of the last wave cut in two, -1 = automatic
     int num_sms;
     cudaStream_t stream;
     Epilogue epi;
@@ -192,6 +193,11 @@ constexpr int kSkinnyMaxM = 64;
 
 // Number of 256 x 256 tiles the pair kernel would compute.
 int pair_tiles(int M, int N);
+// How many of the pair kernel's `total` tiles (the last ones) it cuts into
+// two 256 x 128 halves on `max_pairs` co-resident CTA pairs: the whole last
+// wave when twice its tiles fit in one wave, else none; `forced` >= 0
+// overrides the choice (capped at total).
+int pair_split_tail(int total, int max_pairs, int forced);
 
 // The pair kernel takes over once a problem (all products of a batch
 // together) has at least this many 256 x 256 tiles, enough to occupy most SM
