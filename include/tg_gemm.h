@@ -403,6 +403,19 @@ void tg_gemm_test_hook(int hook);
 tg_status tg_gemm_force_tiling(int bn, int group_m);
 
 /*
+ * Pipeline-depth override, for configuration sweeps (the pages' num_stages,
+ * tuned separately from the tile size): the number of shared-memory stages
+ * in the TMA load ring of the one-CTA kernel (path 3; at most 4, 6 or 8 for
+ * tiles 256, 128 or 64 wide, the default) and of the CTA-pair kernel (path
+ * 6; at most 3, the default).
+ *   stages  0: each kernel's default; 2..8: that many stages.
+ * Process-wide; stays in force until changed.  Returns TG_ERR_INVALID_ARG
+ * (and changes nothing) for other values.  A later call whose kernel holds
+ * fewer stages returns TG_ERR_UNSUPPORTED; other paths ignore it.
+ */
+tg_status tg_gemm_force_stages(int stages);
+
+/*
  * Last-wave override of the CTA-pair kernel (path 6), for tests and
  * benchmarks.  The pair kernel hands its 256 x 256 tiles to the CTA pairs
  * in waves; when the last wave is at most half full, it cuts each of that

@@ -483,3 +483,10 @@ def test_force_split_tail_arguments():
     assert tg.tg_gemm_force_split_tail(-2) == tg.TG_ERR_INVALID_ARG
     for v in (0, 5, -1):
         assert tg.tg_gemm_force_split_tail(v) == tg.TG_OK
+
+
+def test_force_stages_arguments():
+    for bad in (-1, 1, 9, 100):
+        assert tg.tg_gemm_force_stages(bad) == tg.TG_ERR_INVALID_ARG
+    for ok in (2, 3, 8, 0):
+        assert tg.tg_gemm_force_stages(ok) == tg.TG_OK

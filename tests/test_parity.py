@@ -166,6 +166,113 @@ def test_skinny_integer_bitwise():
     assert np.array_equal(have, f16_bits_of(C_ref))
 
 
+@pytest.mark.parametrize("N", [16384, 8192, 4096, 2048])
+@pytest.mark.parametrize("M", [16, 3])
+def test_skinny_splits_integer_bitwise(M, N):
+    """M <= 16 on every split of the cluster (1, 2, 4 and 8 CTAs per 128
+    columns for 128, 64, 32 and 16 column tiles): the partials pushed to the
+    reducing CTA and added in rank order give the exact result."""
+    a = inputs.draw((M, 2048), "int2", 8311 + M, "f16")
+    b = inputs.draw((2048, N), "int2", 8312 + N, "f16")
+    got, intact, p = run(a, b, torch.float16, ldc=N + 8)
+    assert p == SKINNY and intact
+    C_ref, _ = oracle.gemm(a.numpy(), b.numpy())
+    have = torch.from_numpy(got).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(have, f16_bits_of(C_ref))
+
+
+def test_skinny_chain_reads_the_previous_output():
+    """Back-to-back skinny calls on one stream where each call's A is the
+    previous call's C (a decode-like chain), launched with no host sync in
+    between, and again replayed from a CUDA graph: the next call, which may
+    start and prefetch its operands while the previous one still runs, must
+    read the previous call's final output.  Each step is checked against the
+    oracle on the step's own input."""
+    dev = torch.device("cuda")
+    widths = [4096, 2048, 4096, 1024, 4096, 3072]
+    ws = [inputs.draw((widths[i], widths[i + 1]), "normal_0.02", 8400 + i, "f16")
+          for i in range(len(widths) - 1)]
+    x0 = inputs.draw((16, widths[0]), "normal", 8399, "f16")
+    s = torch.cuda.current_stream()
+    wd = [w.to(dev) for w in ws]
+    acts = [x0.to(dev)] + [torch.empty((16, widths[i + 1]), dtype=torch.float16, device=dev)
+                           for i in range(len(ws))]
+
+    def chain(h):
+        for i, w in enumerate(wd):
+            K, N = w.shape
+            st = tg.tg_gemm(16, N, K, acts[i].data_ptr(), K, w.data_ptr(), N,
+                            acts[i + 1].data_ptr(), N, tg.F16, tg.F16, h)
+            assert st == tg.TG_OK
+
+    def check():
+        for i, w in enumerate(ws):
+            x = acts[i].cpu()
+            C_ref, S = oracle.gemm(x.numpy(), w.numpy())
+            compare(acts[i + 1].double().cpu().numpy(), C_ref, S, True, f"chain step {i}")
+
+    assert tg.tg_gemm_path(16, 2048, 4096, acts[0].data_ptr(), 4096, wd[0].data_ptr(), 2048,
+                           acts[1].data_ptr(), 2048, tg.F16, tg.F16) == SKINNY
+    chain(s.cuda_stream)
+    assert tg.tg_gemm_check(s.cuda_stream) == tg.TG_OK
+    check()
+    for a in acts[1:]:
+        a.fill_(float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        chain(torch.cuda.current_stream().cuda_stream)
+    g.replay()
+    g.replay()
+    assert tg.tg_gemm_check(s.cuda_stream) == tg.TG_OK
+    check()
+
+
+@pytest.mark.parametrize("M,widths,path", [(512, [768, 1024, 512, 640], MAIN),
+                                            (2048, [2048, 2048, 2048], PAIR)])
+def test_chain_reads_the_previous_output(M, widths, path):
+    """Back-to-back calls where each call's A is the previous call's C, with
+    no host sync in between and again from a CUDA graph: a call whose
+    prologue overlaps the previous call (programmatic dependent launch) and
+    whose C leaves through TMA stores must read the previous call's final
+    output.  Each step against the oracle on the step's own input."""
+    dev = torch.device("cuda")
+    ws = [inputs.draw((widths[i], widths[i + 1]), "normal_rsqrtk", 8450 + i, "f16",
+                      k=widths[i]) for i in range(len(widths) - 1)]
+    x0 = inputs.draw((M, widths[0]), "normal", 8449, "f16")
+    s = torch.cuda.current_stream()
+    wd = [w.to(dev) for w in ws]
+    acts = [x0.to(dev)] + [torch.empty((M, widths[i + 1]), dtype=torch.float16, device=dev)
+                           for i in range(len(ws))]
+
+    def chain(h):
+        for i, w in enumerate(wd):
+            K, N = w.shape
+            st = tg.tg_gemm(M, N, K, acts[i].data_ptr(), K, w.data_ptr(), N,
+                            acts[i + 1].data_ptr(), N, tg.F16, tg.F16, h)
+            assert st == tg.TG_OK
+
+    def check():
+        for i, w in enumerate(ws):
+            C_ref, S = oracle.gemm(acts[i].cpu().numpy(), w.numpy())
+            compare(acts[i + 1].double().cpu().numpy(), C_ref, S, True, f"chain step {i}")
+
+    K0, N0 = ws[0].shape
+    assert tg.tg_gemm_path(M, N0, K0, acts[0].data_ptr(), K0, wd[0].data_ptr(), N0,
+                           acts[1].data_ptr(), N0, tg.F16, tg.F16) == path
+    chain(s.cuda_stream)
+    assert tg.tg_gemm_check(s.cuda_stream) == tg.TG_OK
+    check()
+    for a in acts[1:]:
+        a.fill_(float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        chain(torch.cuda.current_stream().cuda_stream)
+    g.replay()
+    g.replay()
+    assert tg.tg_gemm_check(s.cuda_stream) == tg.TG_OK
+    check()
+
+
 def test_config5_wide_full():
     """All 67 M outputs of 4096 x 16384 x 4096 against the oracle."""
     w, a, b, out = workload("wide_4096x16384x4096")
@@ -294,6 +401,22 @@ def test_shapes_main_and_tails(M, N, K, out):
     b = inputs.draw((K, N), "normal", 7500 + N, "f16")
     pad = lambda x: (x + 7) // 8 * 8  # noqa: E731  keep TMA-legal strides
     check_full(a, b, out, lda=pad(K), ldb=pad(N), ldc=N + 3)
+
+
+@pytest.mark.parametrize("M,N,ldc,out", [(129, 129, 132, torch.float32), (129, 129, 136, torch.float16),
+                                         (200, 136, 144, torch.float16), (129, 132, 140, torch.float32),
+                                         (300, 264, 272, torch.float16), (70, 40, 48, torch.float32)])
+def test_row_gap_untouched_by_tma_stores(M, N, ldc, out):
+    """C rows padded to a 16-byte-aligned stride, with N itself on or off a
+    16-byte boundary: the columns between N and the stride keep their
+    canaries (a TMA store writes whole 16-byte units at the right edge, so
+    the one-CTA kernel stores through TMA only when rows end on a 16-byte
+    boundary) and every element of C matches the oracle."""
+    a = inputs.draw((M, 192), "normal", 7150 + M, "f16")
+    b = inputs.draw((192, N), "normal", 7151 + N, "f16")
+    pad = lambda x: (x + 7) // 8 * 8  # noqa: E731
+    _, _, p = check_full(a, b, out, ldb=pad(N), ldc=ldc)
+    assert p == MAIN
 
 
 @pytest.mark.parametrize("force", [MAIN, BOUNDARY, PAIR])
@@ -464,6 +587,49 @@ def test_forced_tilings(path, bn, group):
     C_ref, _ = oracle.gemm(a.numpy(), b.numpy())
     have = torch.from_numpy(got).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(have, f16_bits_of(C_ref))
+
+
+@pytest.mark.parametrize("path,bn,stages", [(MAIN, 64, 2), (MAIN, 64, 5), (MAIN, 64, 8),
+                                            (MAIN, 128, 2), (MAIN, 128, 3), (MAIN, 128, 6),
+                                            (MAIN, 256, 2), (MAIN, 256, 3), (PAIR, 0, 2),
+                                            (PAIR, 0, 3)])
+def test_forced_stages(path, bn, stages):
+    """Every pipeline depth the sweep can choose computes the same exact
+    product (more k-blocks than stages, so the ring wraps many times)."""
+    a = inputs.draw((700, 1500), "int2", 8911, "f16")
+    b = inputs.draw((1500, 900), "int2", 8912, "f16")
+    tg.tg_gemm_force_path(path)
+    assert tg.tg_gemm_force_tiling(bn, 0) == tg.TG_OK
+    assert tg.tg_gemm_force_stages(stages) == tg.TG_OK
+    try:
+        got, intact, p = run(a, b, torch.float16, lda=1504, ldb=904)
+    finally:
+        tg.tg_gemm_force_stages(0)
+        tg.tg_gemm_force_path(0)
+        tg.tg_gemm_force_tiling(0, 0)
+    assert p == path and intact
+    C_ref, _ = oracle.gemm(a.numpy(), b.numpy())
+    have = torch.from_numpy(got).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(have, f16_bits_of(C_ref))
+
+
+def test_forced_stages_beyond_the_kernel_are_refused():
+    dev = torch.device("cuda")
+    a = torch.ones((512, 1024), dtype=torch.float16, device=dev)
+    b = torch.ones((1024, 512), dtype=torch.float16, device=dev)
+    c = torch.full((512, 512), 7.0, dtype=torch.float16, device=dev)
+    s = torch.cuda.current_stream().cuda_stream
+    tg.tg_gemm_force_path(PAIR)
+    assert tg.tg_gemm_force_stages(4) == tg.TG_OK
+    try:
+        st = tg.tg_gemm(512, 512, 1024, a.data_ptr(), 1024, b.data_ptr(), 512, c.data_ptr(), 512,
+                        tg.F16, tg.F16, s)
+    finally:
+        tg.tg_gemm_force_stages(0)
+        tg.tg_gemm_force_path(0)
+    assert st == tg.TG_ERR_UNSUPPORTED
+    assert tg.tg_gemm_check(s) == tg.TG_OK
+    assert torch.all(c == 7.0)
 
 
 def test_stream_argument_is_honoured():

@@ -19,7 +19,7 @@ __all__ = [
     "F16", "F32", "E4M3", "TG_OK", "TG_ERR_INVALID_ARG", "TG_ERR_UNSUPPORTED", "TG_ERR_CUDA",
     "TG_ERR_TIMEOUT", "PATHS", "TgError", "lib", "library_path", "tg_gemm", "tg_gemm_check",
     "tg_status_string", "tg_gemm_path", "tg_gemm_force_path", "tg_gemm_force_tiling",
-    "tg_gemm_force_split_tail", "tg_gemm_pair_split_tail",
+    "tg_gemm_force_split_tail", "tg_gemm_pair_split_tail", "tg_gemm_force_stages",
     "tg_gemm_test_hook", "tg_gemm_ex", "tg_gemm_batched", "tg_gemm_batched_path",
     "tg_attention", "tg_attention_ws", "tg_attention_workspace_size", "tg_attention_noalloc",
     "tg_attention_kernel", "tg_attention_force_kernel", "tg_attention_tail_plan",
@@ -115,6 +115,8 @@ def lib() -> ctypes.CDLL:
         L.tg_gemm_force_split_tail.argtypes = [i32]
         L.tg_gemm_pair_split_tail.restype = i32
         L.tg_gemm_pair_split_tail.argtypes = [i64, i32]
+        L.tg_gemm_force_stages.restype = i32
+        L.tg_gemm_force_stages.argtypes = [i32]
         L.tg_gemm_test_hook.restype = None
         L.tg_gemm_test_hook.argtypes = [i32]
         L.tg_gemm_version.restype = i32
@@ -217,6 +219,10 @@ def tg_gemm_force_tiling(bn: int, group_m: int) -> int:
 
 def tg_gemm_force_split_tail(tiles: int) -> int:
     return int(lib().tg_gemm_force_split_tail(int(tiles)))
+
+
+def tg_gemm_force_stages(stages: int) -> int:
+    return int(lib().tg_gemm_force_stages(int(stages)))
 
 
 def tg_gemm_pair_split_tail(tiles: int, max_pairs: int) -> int:

@@ -27,8 +27,11 @@
 //   * warps 2..9: epilogue, two per TMEM lane quadrant (half of the columns
 //     each).  Each thread owns one output row: tcgen05.ld of 32 columns at a
 //     time, the fused epilogue if any, fp32 -> fp16 round-to-nearest-even
-//     (or fp32 as is), 16-byte vector stores, predicated at the M/N edges.
-//     The epilogue of tile i overlaps the main loop of tile i+1.
+//     (or fp32 as is).  When C is TMA-addressable and its rows end on
+//     16-byte boundaries the warp's 32 x 32 chunk goes through a 4 KB
+//     shared-memory staging buffer per warp and leaves as one TMA store (the
+//     TMA engine clips it at the M/N edges); otherwise each thread writes
+//     its row with 16-byte vector stores, predicated at the edges.  The epilogue of tile i overlaps the main loop of tile i+1.
 // Out-of-range rows, columns and k are zero-filled by TMA, so any M, N, K
 // works as long as the operands are TMA-addressable (16-byte aligned bases,
 // row strides a multiple of 16 bytes); the host routes everything else to
@@ -40,6 +43,7 @@
 // flight, the MMA thread waits for its own MMAs, and tensor memory is freed
 // before the CTA exits.
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 
 #include <cuda.h>
@@ -72,15 +76,25 @@ constexpr uint32_t A_STAGE = BM * 128;
 // MMAs instead of holding the accumulator buffer.
 constexpr int kEpilogueWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpilogueWarps;
+// Output staging for TMA stores: 4 KB per epilogue warp, one 32 x 32 fp32
+// chunk or two fp16 chunks (double-buffered).
+constexpr uint32_t kStageC = 4096;
+constexpr uint32_t kStageCBytes = kEpilogueWarps * kStageC;
 
 template <int BN>
 struct MainCfg {
     static constexpr uint32_t B_STAGE = BN * 128;
     static constexpr uint32_t STAGE = A_STAGE + B_STAGE;
+    // the most stages that fit (the default); a ring of 2..STAGES can be
+    // requested (tg_gemm_force_stages), shared memory is sized to it
     static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
     static constexpr uint32_t TMEM_COLS = 2 * BN;
     static constexpr uint32_t SMEM = STAGES * STAGE + 1024;  // + alignment slack
-    static_assert(SMEM <= 227 * 1024, "shared-memory budget exceeded");
+    static constexpr uint32_t smem(int stages, bool c_tma)
+    {
+        return stages * STAGE + (c_tma ? kStageCBytes : 0u) + 1024;
+    }
+    static_assert(SMEM + kStageCBytes <= 227 * 1024, "shared-memory budget exceeded");
     static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
                   "TMEM allocation must be a power of two in [32, 512]");
 };
@@ -88,12 +102,12 @@ struct MainCfg {
 template <int BN, bool OUT_F32, int ES>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    void* C, long long ldc, int M, int N, int K, int tiles_m,
-                    int tiles_n, int group_m, int c_vec, int hook, unsigned int* err,
-                    Epilogue epi, BatchArgs bt)
+                    const __grid_constant__ CUtensorMap tmC, void* C, long long ldc, int M,
+                    int N, int K, int tiles_m, int tiles_n, int group_m, int stages, int c_vec,
+                    int c_tma, int hook, unsigned int* err, Epilogue epi, BatchArgs bt)
 {
     using Cfg = MainCfg<BN>;
-    constexpr int STAGES = Cfg::STAGES;
+    constexpr int STAGES = Cfg::STAGES;  // the most stages; `stages` are in use
 
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[STAGES];
@@ -134,8 +148,8 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         if (static_cast<int>(blockIdx.x) < total) {
             int b, tm, tn;
             batch_tile_coords(static_cast<int>(blockIdx.x), tiles_m, tiles_n, group_m, b, tm, tn);
-            const int pf = total > static_cast<int>(gridDim.x) ? STAGES
-                                                                : min(STAGES, kPrefetchStagesSingle);
+            const int pf = total > static_cast<int>(gridDim.x) ? stages
+                                                                : min(stages, kPrefetchStagesSingle);
             for (int kb = 0; kb < num_kb && kb < pf; ++kb) {
                 tma_prefetch_l2_3d(&tmA, kb * BK, tm * BM, b * bt.za);
                 for (int j = 0; j < BN / NB; ++j)
@@ -178,7 +192,7 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     if (hook == 1 && t == static_cast<int>(blockIdx.x) && kb == 0) {
                         // test hook: leave this stage unfilled, so the MMA
                         // thread's bounded wait on it runs out
-                        if (++s == STAGES) {
+                        if (++s == stages) {
                             s = 0;
                             ph ^= 1u;
                         }
@@ -193,7 +207,7 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         tma_load_3d(sa + A_STAGE + j * B_BOX, &tmB, fb, tn * BN + j * NB, kb * BK,
                                     zb);
                     ++issued;
-                    if (++s == STAGES) {
+                    if (++s == stages) {
                         s = 0;
                         ph ^= 1u;
                     }
@@ -201,13 +215,13 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 if (!ok) break;
             }
             // Wait for this thread's own copies still in flight: the most
-            // recent arming of each of the last min(issued, STAGES) stages.
+            // recent arming of each of the last min(issued, stages) stages.
             int ds = s;
             uint32_t dph = ph;
-            const uint32_t n_drain = issued < (uint32_t)STAGES ? issued : (uint32_t)STAGES;
+            const uint32_t n_drain = issued < (uint32_t)stages ? issued : (uint32_t)stages;
             for (uint32_t i = 0; i < n_drain; ++i) {
                 if (--ds < 0) {
-                    ds = STAGES - 1;
+                    ds = stages - 1;
                     dph ^= 1u;
                 }
                 if (!mbar_wait(smem_u32(&full_bar[ds]), dph, nullptr)) atomicOr(err, ERR_DRAIN);
@@ -247,7 +261,7 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         umma<ES>(d, ad + 2ull * k, bd + KBlock<ES>::B_KSTEP * k, idesc,
                                  (kb | k) != 0 ? 1u : 0u);
                     umma_commit(smem_u32(&empty_bar[s]));
-                    if (++s == STAGES) {
+                    if (++s == stages) {
                         s = 0;
                         ph ^= 1u;
                     }
@@ -271,6 +285,9 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         constexpr int span = BN / (kEpilogueWarps / 4);  // accumulator columns per warp
         const int c_lo = ((warp - 2) >> 2) * span;
+        const uint32_t stage_c = base + static_cast<uint32_t>(stages) * Cfg::STAGE +
+                                 static_cast<uint32_t>(warp - 2) * kStageC;
+        uint32_t chunk = 0;  // staged chunks so far (fp16 alternates two 2 KB halves)
         int acc = 0;
         uint32_t aph = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -286,7 +303,8 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 break;
             }
             tc_fence_after();
-            const int m = tm * BM + q * 32 + lane;
+            const int m0 = tm * BM + q * 32;  // this warp's first row
+            const int m = m0 + lane;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
@@ -295,7 +313,22 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 tmem_ld_32x32b_x32(taddr + c, r);
                 tmem_ld_wait();
                 const int n = tn * BN + c;
-                if (m < M && n < N) {
+                if (c_tma) {
+                    if (m0 < M && n < N) {  // warp-uniform
+                        if (epi.on && m < M) epilogue_chunk<OUT_F32>(r, m, n, N, epi);
+                        // the staging buffer half (fp16) or whole (fp32) this
+                        // chunk takes is free once the store that used it
+                        // last has read it
+                        if (lane == 0) {
+                            if constexpr (OUT_F32) bulk_wait_read<0>();
+                            else bulk_wait_read<1>();
+                        }
+                        __syncwarp();
+                        const uint32_t slot = OUT_F32 ? stage_c : stage_c + (chunk & 1u) * (kStageC / 2);
+                        stage_store_chunk<OUT_F32>(&tmC, slot, r, n, m0, b, lane);
+                        ++chunk;
+                    }
+                } else if (m < M && n < N) {
                     if (epi.on) epilogue_chunk<OUT_F32>(r, m, n, N, epi);
                     store_chunk<OUT_F32>(Cb, ldc, m, n, N, r, c_vec != 0);
                 }
@@ -305,6 +338,10 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             acc ^= 1;
             if (acc == 0) aph ^= 1u;
         }
+        // the TMA stores have read their staging buffers before the CTA
+        // ends (their writes to C complete with the grid)
+        if (c_tma && lane == 0) bulk_wait_read<0>();
+        __syncwarp();
     }
 
     pdl_trigger();  // this CTA has issued all its global writes
@@ -335,7 +372,7 @@ cudaError_t launch_cfg(const GemmArgs& a)
         if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
         if (!g_attr_set[dev][slot]) {
             e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(Cfg::SMEM));
+                                     static_cast<int>(Cfg::SMEM + kStageCBytes));
             if (e != cudaSuccess) return e;
             g_attr_set[dev][slot] = true;
         }
@@ -356,20 +393,41 @@ cudaError_t launch_cfg(const GemmArgs& a)
     const int c_vec = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) &&
                       ((static_cast<size_t>(a.ldc) * es) % 16 == 0) &&
                       ((static_cast<size_t>(a.sC) * es) % 16 == 0);
+    // C written by TMA stores when the TMA engine can address it and each
+    // row of C ends on a 16-byte boundary: at the right edge of C a TMA
+    // store writes whole 16-byte units (measured: a box clipped at N = 129
+    // fp32 columns also wrote columns 129..131 of the row stride), and the
+    // ABI leaves columns N..ldc-1 untouched
+    CUtensorMap tc;
+    std::memset(&tc, 0, sizeof(tc));
+    const int c_tma = c_vec && (static_cast<size_t>(a.N) * es) % 16 == 0 &&
+                      encode_tmap_store(&tc, a.C, static_cast<int>(es),
+                                                 static_cast<uint64_t>(a.N),
+                                                 static_cast<uint64_t>(a.M),
+                                                 static_cast<uint64_t>(a.ldc), a.batch, a.sC,
+                                                 32, 32);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = Cfg::SMEM;
+    const int stages = a.stages > 0 ? a.stages : Cfg::STAGES;
+    if (stages < 2 || stages > Cfg::STAGES) return cudaErrorInvalidValue;
+    cfg.dynamicSmemBytes = Cfg::smem(stages, c_tma != 0);
     cfg.stream = a.stream;
     cudaLaunchAttribute at[1];
     set_pdl_attr(at[0]);
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, ta, tb, a.C, a.ldc, a.M, a.N, a.K, tiles_m, tiles_n,
-                              group_m, c_vec, a.hook, a.err, a.epi, a.batch_args());
+    return cudaLaunchKernelEx(&cfg, kernel, ta, tb, tc, a.C, a.ldc, a.M, a.N, a.K, tiles_m,
+                              tiles_n, group_m, stages, c_vec, c_tma, a.hook, a.err, a.epi,
+                              a.batch_args());
 }
 
 }  // namespace
+
+int main_max_stages(int bn)
+{
+    return bn == 256 ? MainCfg<256>::STAGES : bn == 128 ? MainCfg<128>::STAGES : MainCfg<64>::STAGES;
+}
 
 int main_tile_n(int M, int N, int batch, int num_sms)
 {

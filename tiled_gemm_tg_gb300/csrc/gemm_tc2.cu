@@ -23,13 +23,17 @@
 //            each tile's commit to both CTAs' tmem-full barriers.
 //   warps 2-9  epilogue in both CTAs, two per TMEM lane quadrant: each CTA
 //            reads its own 128 rows of the accumulator from its own TMEM
-//            (each warp half of the columns) and stores them; all epilogue
-//            threads of the pair arrive on the leader's tmem-empty barrier.
+//            (each warp half of the columns) and stores them, 32 x 32 chunks
+//            staged in shared memory and written by TMA stores when C allows
+//            (16-byte aligned, rows ending on 16-byte boundaries), else
+//            16-byte stores per row; all epilogue threads of the pair arrive
+//            on the leader's tmem-empty barrier.
 // Waits are bounded as in the one-CTA kernel; on expiry a role records a bit
 // in the device error word and leaves its loop; the leader waits for the
 // pair's copies in flight and its own MMAs; a cluster barrier keeps both CTAs
 // resident until then, and TMEM is freed by both CTAs together.
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 
 #include <cuda.h>
@@ -68,8 +72,13 @@ struct PairK {
     static constexpr uint32_t B_BOX = BK * 128;          // one [BK k][NB n] box
     static constexpr uint32_t B_KSTEP = 32 / ES * 128 / 16;  // 16-byte units per MMA
 };
+// three 64 KB stages fit (the default); two can be requested
+// (tg_gemm_force_stages), shared memory is sized to the ring
 constexpr int STAGES = 3;
 constexpr uint32_t SMEM = STAGES * STAGE + 1024;
+// Output staging for TMA stores: 4 KB per epilogue warp (one 32 x 32 fp32
+// chunk, or two fp16 chunks double-buffered), after the stages.
+constexpr uint32_t kStageC = 4096;
 constexpr uint32_t TMEM_COLS = 2 * PN;           // two accumulators
 #ifndef TG_PAIR_EPI_WARPS
 #define TG_PAIR_EPI_WARPS 8
@@ -83,7 +92,8 @@ static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "4 or 8 epilogue warps");
 constexpr uint32_t kEpilogueThreads = 32 * EPI_WARPS;
 constexpr int kThreads = 64 + static_cast<int>(kEpilogueThreads);
 constexpr int EPI_SPAN = PN / (EPI_WARPS / 4);  // accumulator columns per epilogue warp
-static_assert(SMEM <= 227 * 1024, "shared-memory budget exceeded");
+constexpr uint32_t kStageCBytes = (kThreads / 32 - 2) * kStageC;
+static_assert(SMEM + kStageCBytes <= 227 * 1024, "shared-memory budget exceeded");
 static_assert(TMEM_COLS == 512, "two 256-column accumulators fill TMEM");
 #ifndef TG_PAIR_L2_HINTS
 #define TG_PAIR_L2_HINTS 1
@@ -119,9 +129,10 @@ __device__ __forceinline__ void work_item(int t, int tiles_m, int tiles_n, int g
 template <bool OUT_F32, int ES>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    void* C, long long ldc, int M, int N, int K, int tiles_m,
-                    int tiles_n, int group_m, int split_tail, int c_vec, int hook,
-                    unsigned int* err, Epilogue epi, BatchArgs bt)
+                    const __grid_constant__ CUtensorMap tmC, void* C, long long ldc, int M,
+                    int N, int K, int tiles_m, int tiles_n, int group_m, int split_tail,
+                    int stages, int c_vec, int c_tma, int hook, unsigned int* err, Epilogue epi,
+                    BatchArgs bt)
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[STAGES];   // used in the leader only
@@ -209,7 +220,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     if (hook == 1 && leader && t == pair && kb == 0) {
                         // test hook: the leader never arms this stage, so the
                         // MMA thread's bounded wait on it runs out
-                        if (++s == STAGES) {
+                        if (++s == stages) {
                             s = 0;
                             ph ^= 1u;
                         }
@@ -226,22 +237,22 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         tma_load_3d_pair_hint(sa + A_STAGE + j * KG::B_BOX, &tmB, fb,
                                               col + j * KG::NB, kb * BK, zb, pol_b);
                     ++issued;
-                    if (++s == STAGES) {
+                    if (++s == stages) {
                         s = 0;
                         ph ^= 1u;
                     }
                 }
             }
             // Copies of both CTAs complete on the leader's full barriers, so the
-            // leader waits there for the last min(issued, STAGES) armed phases;
+            // leader waits there for the last min(issued, stages) armed phases;
             // the closing cluster barrier keeps the peer resident meanwhile.
             if (leader) {
                 int ds = s;
                 uint32_t dph = ph;
-                const uint32_t n_drain = issued < (uint32_t)STAGES ? issued : (uint32_t)STAGES;
+                const uint32_t n_drain = issued < (uint32_t)stages ? issued : (uint32_t)stages;
                 for (uint32_t i = 0; i < n_drain; ++i) {
                     if (--ds < 0) {
-                        ds = STAGES - 1;
+                        ds = stages - 1;
                         dph ^= 1u;
                     }
                     if (!mbar_wait(smem_u32(&full_bar[ds]), dph, nullptr)) atomicOr(err, ERR_DRAIN);
@@ -287,7 +298,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         umma_pair<ES>(d, ad + ((k / 4) * (A_ATOM >> 4) + (k % 4) * 2),
                                       bd + KG::B_KSTEP * k, idesc, (kb | k) != 0 ? 1u : 0u);
                     umma_commit_pair_mc(smem_u32(&empty_bar[s]), 0x3);
-                    if (++s == STAGES) {
+                    if (++s == stages) {
                         s = 0;
                         ph ^= 1u;
                     }
@@ -310,6 +321,9 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const int q = warp & 3;                       // TMEM lane quadrant of this warp
         const int wcol = (warp - 2) >> 2;             // which share of the columns
         const uint32_t tempty0 = mapa_shared(smem_u32(&tempty_bar[0]), 0);  // leader's
+        const uint32_t stage_c = base + static_cast<uint32_t>(stages) * STAGE +
+                                 static_cast<uint32_t>(warp - 2) * kStageC;
+        uint32_t chunk = 0;  // staged chunks so far (fp16 alternates two 2 KB halves)
         int acc = 0;
         uint32_t aph = 0;
         for (int t = pair; t < total; t += npairs) {
@@ -330,7 +344,8 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 break;
             }
             tc_fence_after();
-            const int m = tm * PM + static_cast<int>(rank) * HM + q * 32 + lane;
+            const int m0 = tm * PM + static_cast<int>(rank) * HM + q * 32;  // this warp's first row
+            const int m = m0 + lane;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * PN);
 #pragma unroll 1
@@ -343,7 +358,22 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 #pragma unroll
                 for (int j = 0; j < EPI_COLS; j += 32) {
                     const int n = n0 + c + j;
-                    if (m < M && n < N) {
+                    if (c_tma) {
+                        if (m0 < M && n < N) {  // warp-uniform
+                            if (epi.on && m < M) epilogue_chunk<OUT_F32>(r + j, m, n, N, epi);
+                            // the staging slot is free once the store that
+                            // used it last has read it
+                            if (lane == 0) {
+                                if constexpr (OUT_F32) bulk_wait_read<0>();
+                                else bulk_wait_read<1>();
+                            }
+                            __syncwarp();
+                            const uint32_t slot =
+                                OUT_F32 ? stage_c : stage_c + (chunk & 1u) * (kStageC / 2);
+                            stage_store_chunk<OUT_F32>(&tmC, slot, r + j, n, m0, b, lane);
+                            ++chunk;
+                        }
+                    } else if (m < M && n < N) {
                         if (epi.on) epilogue_chunk<OUT_F32>(r + j, m, n, N, epi);
                         store_chunk<OUT_F32>(Cb, ldc, m, n, N, r + j, c_vec != 0);
                     }
@@ -354,6 +384,10 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             acc ^= 1;
             if (acc == 0) aph ^= 1u;
         }
+        // the TMA stores have read their staging buffers before the CTA
+        // ends (their writes to C complete with the grid)
+        if (c_tma && lane == 0) bulk_wait_read<0>();
+        __syncwarp();
     }
 
     pdl_trigger();  // this CTA has issued all its global writes
@@ -384,12 +418,12 @@ cudaError_t launch_cfg(const GemmArgs& a)
         std::lock_guard<std::mutex> lock(g_mu);
         if (!g_attr_set[dev][slot]) {
             e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(SMEM));
+                                     static_cast<int>(SMEM + kStageCBytes));
             if (e != cudaSuccess) return e;
             cudaLaunchConfig_t q = {};
             q.gridDim = dim3(2 * a.num_sms);
             q.blockDim = dim3(kThreads);
-            q.dynamicSmemBytes = SMEM;
+            q.dynamicSmemBytes = SMEM + kStageCBytes;
             cudaLaunchAttribute at[1];
             at[0].id = cudaLaunchAttributeClusterDimension;
             at[0].val.clusterDim.x = 2;
@@ -423,11 +457,22 @@ cudaError_t launch_cfg(const GemmArgs& a)
     const int c_vec = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) &&
                       ((static_cast<size_t>(a.ldc) * es) % 16 == 0) &&
                       ((static_cast<size_t>(a.sC) * es) % 16 == 0);
+    // C written by TMA stores when the TMA engine can address it and its
+    // rows end on a 16-byte boundary (at the right edge a TMA store writes
+    // whole 16-byte units; columns N..ldc-1 stay untouched)
+    CUtensorMap tc;
+    std::memset(&tc, 0, sizeof(tc));
+    const int c_tma = c_vec && (static_cast<size_t>(a.N) * es) % 16 == 0 &&
+                      encode_tmap_store(&tc, a.C, static_cast<int>(es),
+                                        static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.M),
+                                        static_cast<uint64_t>(a.ldc), a.batch, a.sC, 32, 32);
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * pairs);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = SMEM;
+    const int stages = a.stages > 0 ? a.stages : STAGES;
+    if (stages < 2 || stages > STAGES) return cudaErrorInvalidValue;
+    cfg.dynamicSmemBytes = stages * STAGE + (c_tma ? kStageCBytes : 0u) + 1024;
     cfg.stream = a.stream;
     cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
@@ -437,8 +482,9 @@ cudaError_t launch_cfg(const GemmArgs& a)
     set_pdl_attr(at[1]);
     cfg.attrs = at;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kernel, ta, tb, a.C, a.ldc, a.M, a.N, a.K, tiles_m, tiles_n,
-                              group_m, split_tail, c_vec, a.hook, a.err, a.epi, a.batch_args());
+    return cudaLaunchKernelEx(&cfg, kernel, ta, tb, tc, a.C, a.ldc, a.M, a.N, a.K, tiles_m,
+                              tiles_n, group_m, split_tail, stages, c_vec, c_tma, a.hook, a.err,
+                              a.epi, a.batch_args());
 }
 
 }  // namespace
@@ -455,6 +501,8 @@ int pair_split_tail(int total, int max_pairs, int forced)
     const int last = total - max_pairs * ((total - 1) / max_pairs);
     return 2 * last <= max_pairs ? last : 0;
 }
+
+int pair_max_stages() { return STAGES; }
 
 int pair_tiles(int M, int N)
 {

@@ -6,6 +6,7 @@
 
 #include <cuda_fp16.h>
 
+#include "ptx.cuh"
 #include "tg_internal.h"
 
 namespace tg {
@@ -186,6 +187,44 @@ __device__ __forceinline__ void store_chunk(void* C, long long ldc, int m, int n
             for (int j = 0; j < 32; ++j)
                 if (n + j < N) row[j] = __float2half_rn(__uint_as_float(r[j]));
         }
+    }
+}
+
+// One epilogue warp's 32 x 32 chunk of C (rows m0..m0+31, lane = row,
+// columns n..n+31, r[] the lane's fp32 accumulators after the fused
+// epilogue) through shared memory and one TMA store: the lane writes its
+// row, converted, into the warp's staging buffer `slot` (64 B per row for
+// fp16, 128 B for fp32), and lane 0 stores the box [32 cols][32 rows] at
+// (n, m0, z) of `tmC`; the TMA engine writes only the part inside C.  The
+// warp's 32 rows then leave as one bulk copy instead of 32-row scattered
+// 16-byte stores.  The caller keeps `slot` untouched until the store has
+// read it (bulk_wait_read in lane 0, then __syncwarp).
+template <bool OUT_F32>
+__device__ __forceinline__ void stage_store_chunk(const CUtensorMap* tmC, uint32_t slot,
+                                                  const uint32_t* r, int n, int m0, int z,
+                                                  int lane)
+{
+    if constexpr (OUT_F32) {
+        const uint32_t row = slot + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            st_shared_v4(row + 16u * i, r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+    } else {
+        uint32_t p[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            __half2 h = __floats2half2_rn(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+            p[i] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        const uint32_t row = slot + static_cast<uint32_t>(lane) * 64u;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) st_shared_v4(row + 16u * i, p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+    }
+    fence_proxy_async_smem();  // the rows are visible to the TMA engine
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_3d(tmC, slot, n, m0, z);
+        bulk_commit();
     }
 }
 

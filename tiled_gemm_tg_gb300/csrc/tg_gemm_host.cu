@@ -44,6 +44,7 @@ std::atomic<int> g_force_bn{0};
 std::atomic<int> g_force_group{0};
 std::atomic<int> g_force_attn{0};
 std::atomic<int> g_force_split_tail{-1};
+std::atomic<int> g_force_stages{0};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 tg_status device_state(DeviceState** out)
@@ -291,6 +292,7 @@ tg_status run(int path, const Problem& p, const tg::Epilogue& epi, tg_stream_t s
     a.hook = g_test_hook.load(std::memory_order_relaxed);
     a.group_m = g_force_group.load(std::memory_order_relaxed);
     a.split_tail = g_force_split_tail.load(std::memory_order_relaxed);
+    a.stages = g_force_stages.load(std::memory_order_relaxed);
     a.num_sms = ds->num_sms;
     a.stream = s;
     a.epi = epi;
@@ -300,12 +302,17 @@ tg_status run(int path, const Problem& p, const tg::Epilogue& epi, tg_stream_t s
         case tg::PATH_ZERO: e = tg::launch_epilogue_only(a); break;
         case tg::PATH_SIMT: e = tg::launch_simt_f32(a); break;
         case tg::PATH_MAIN: {
-            const int bn = g_force_bn.load(std::memory_order_relaxed);
-            e = tg::launch_main(a, bn != 0 ? bn : tg::main_tile_n(a.M, a.N, a.batch, a.num_sms));
+            const int forced_bn = g_force_bn.load(std::memory_order_relaxed);
+            const int bn = forced_bn != 0 ? forced_bn : tg::main_tile_n(a.M, a.N, a.batch, a.num_sms);
+            if (a.stages != 0 && a.stages > tg::main_max_stages(bn)) return TG_ERR_UNSUPPORTED;
+            e = tg::launch_main(a, bn);
             break;
         }
         case tg::PATH_BOUNDARY: e = tg::launch_boundary(a); break;
-        case tg::PATH_MAIN_PAIR: e = tg::launch_main_pair(a); break;
+        case tg::PATH_MAIN_PAIR:
+            if (a.stages != 0 && a.stages > tg::pair_max_stages()) return TG_ERR_UNSUPPORTED;
+            e = tg::launch_main_pair(a);
+            break;
         case tg::PATH_SKINNY: e = tg::launch_skinny(a); break;
         default: return TG_ERR_UNSUPPORTED;
     }
@@ -328,11 +335,12 @@ struct TmapKey {
     uint64_t cols, rows, ld, batch, stride;
     uint32_t box_cols, box_rows;
     int es;
+    int kind;  // 0: operand load map (128-byte swizzle), 1: output store map (no swizzle)
     bool operator==(const TmapKey& o) const
     {
         return ptr == o.ptr && cols == o.cols && rows == o.rows && ld == o.ld &&
                batch == o.batch && stride == o.stride && box_cols == o.box_cols &&
-               box_rows == o.box_rows && es == o.es;
+               box_rows == o.box_rows && es == o.es && kind == o.kind;
     }
 };
 
@@ -367,24 +375,25 @@ int tmap_slot(const TmapKey& k)
     h = mix(h, k.batch);
     h = mix(h, k.stride);
     h = mix(h, (static_cast<uint64_t>(k.box_cols) << 32) | k.box_rows);
-    h = mix(h, static_cast<uint64_t>(k.es));
+    h = mix(h, static_cast<uint64_t>(k.es) | (static_cast<uint64_t>(k.kind) << 8));
     return static_cast<int>(h % kTmapCacheSize);
 }
 
-}  // namespace
-
-bool encode_tmap(CUtensorMap* map, const void* ptr, int es, uint64_t cols, uint64_t rows,
-                 uint64_t ld, uint64_t batch, uint64_t stride, uint32_t box_cols,
-                 uint32_t box_rows)
+// Encodes (or finds in the cache) a 3-D map; kind 0: an operand load map
+// (fp16 or byte elements, 128-byte swizzle, 256-byte L2 promotion), kind 1:
+// an output store map (fp16 or fp32 elements, no swizzle).
+bool encode_map(CUtensorMap* map, int kind, const void* ptr, int es, uint64_t cols, uint64_t rows,
+                uint64_t ld, uint64_t batch, uint64_t stride, uint32_t box_cols, uint32_t box_rows)
 {
-    if (!g_encode || (es != 1 && es != 2)) return false;
+    if (!g_encode) return false;
+    if (kind == 0 ? (es != 1 && es != 2) : (es != 2 && es != 4)) return false;
     if (stride == 0) {
         // one matrix: the third extent is 1 and its stride only has to be a
         // legal value (a multiple of 16 bytes covering the matrix)
         batch = 1;
         stride = (rows * ld * es + 15) / 16 * 16 / es;
     }
-    const TmapKey key{ptr, cols, rows, ld, batch, stride, box_cols, box_rows, es};
+    const TmapKey key{ptr, cols, rows, ld, batch, stride, box_cols, box_rows, es, kind};
     const int slot = tmap_slot(key);
     {
         std::lock_guard<std::mutex> lock(g_tmap_mu);
@@ -398,11 +407,14 @@ bool encode_tmap(CUtensorMap* map, const void* ptr, int es, uint64_t cols, uint6
     cuuint64_t strides[2] = {ld * es, stride * es};
     cuuint32_t box[3] = {box_cols, box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    const CUtensorMapDataType dt =
-        es == 2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-    CUresult r = g_encode(map, dt, 3, const_cast<void*>(ptr), dims,
-                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    const CUtensorMapDataType dt = es == 4   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : es == 2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                             : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    CUresult r = g_encode(map, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          kind == 0 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          kind == 0 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                    : CU_TENSOR_MAP_L2_PROMOTION_NONE,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
     std::lock_guard<std::mutex> lock(g_tmap_mu);
@@ -411,6 +423,22 @@ bool encode_tmap(CUtensorMap* map, const void* ptr, int es, uint64_t cols, uint6
     e.key = key;
     e.map = *map;
     return true;
+}
+
+}  // namespace
+
+bool encode_tmap(CUtensorMap* map, const void* ptr, int es, uint64_t cols, uint64_t rows,
+                 uint64_t ld, uint64_t batch, uint64_t stride, uint32_t box_cols,
+                 uint32_t box_rows)
+{
+    return encode_map(map, 0, ptr, es, cols, rows, ld, batch, stride, box_cols, box_rows);
+}
+
+bool encode_tmap_store(CUtensorMap* map, const void* ptr, int es, uint64_t cols, uint64_t rows,
+                       uint64_t ld, uint64_t batch, uint64_t stride, uint32_t box_cols,
+                       uint32_t box_rows)
+{
+    return encode_map(map, 1, ptr, es, cols, rows, ld, batch, stride, box_cols, box_rows);
 }
 
 }  // namespace tg
@@ -769,6 +797,13 @@ tg_status tg_gemm_force_tiling(int bn, int group_m)
     if (group_m < 0 || group_m > 64) return TG_ERR_INVALID_ARG;
     g_force_bn.store(bn, std::memory_order_relaxed);
     g_force_group.store(group_m, std::memory_order_relaxed);
+    return TG_OK;
+}
+
+tg_status tg_gemm_force_stages(int stages)
+{
+    if (stages != 0 && (stages < 2 || stages > 8)) return TG_ERR_INVALID_ARG;
+    g_force_stages.store(stages, std::memory_order_relaxed);
     return TG_OK;
 }
 

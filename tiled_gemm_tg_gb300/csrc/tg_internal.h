@@ -90,6 +90,7 @@ struct GemmArgs {
     int hook;           // test hook (0 = off), see tg_gemm_test_hook
     int group_m;        // grouped tile-order height, 0 = the kernel's default
     int split_tail = -1;  // pair kernel: tiles of the last wave cut in two, -1 = automatic
+    int stages = 0;       // TMA kernels: pipeline stages in the ring, 0 = the kernel's most
     int num_sms;
     cudaStream_t stream;
     Epilogue epi;
@@ -116,6 +117,12 @@ struct GemmArgs {
 bool encode_tmap(CUtensorMap* map, const void* ptr, int es, uint64_t cols, uint64_t rows,
                  uint64_t ld, uint64_t batch, uint64_t stride, uint32_t box_cols,
                  uint32_t box_rows);
+
+// The same for an output written by TMA stores: es = 2 (fp16) or 4 (fp32),
+// no swizzle, box_cols x box_rows x 1.
+bool encode_tmap_store(CUtensorMap* map, const void* ptr, int es, uint64_t cols, uint64_t rows,
+                       uint64_t ld, uint64_t batch, uint64_t stride, uint32_t box_cols,
+                       uint32_t box_rows);
 
 cudaError_t launch_simt_f32(const GemmArgs& a);
 cudaError_t launch_main(const GemmArgs& a, int bn);
@@ -187,6 +194,10 @@ int attention_kernel_choice(int batch, int Nq, int Nk, int d, int dv, int num_sm
 
 // Tile width the main kernel uses for this problem (64, 128 or 256).
 int main_tile_n(int M, int N, int batch, int num_sms);
+// The most pipeline stages (the default ring) of the one-CTA kernel with
+// tile width bn, and of the pair kernel.
+int main_max_stages(int bn);
+int pair_max_stages();
 
 // Largest M the skinny kernel serves.
 constexpr int kSkinnyMaxM = 64;

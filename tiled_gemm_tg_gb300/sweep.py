@@ -2,13 +2,16 @@
 for given GEMM shapes and report the fastest (the tuning harness of the
 pages: block sizes, pipeline depth and rasterisation screened per shape).
 
-Configurations: the CTA-pair kernel (256 x 256 tiles, k-block 128, three
-stages) with grouped tile orders of 2..32 tile rows; the one-CTA kernel with
-128 x 64 / 128 x 128 / 128 x 256 tiles (8 / 6 / 4 stages of k-block 64) and
-group heights 4..32; the skinny kernel when M <= 64.  Each configuration is
-forced through tg_gemm_force_path / tg_gemm_force_tiling, launched `reps`
-times from one CUDA graph over operand sets rotated past L2, and timed with
-CUDA events.
+Configurations, two axes at a time as the pages tune them: the CTA-pair
+kernel (256 x 256 tiles, k-block 128) with grouped tile orders of 2..32
+tile rows at its default three stages, and with 2 or 3 stages at its
+default group; the one-CTA kernel with 128 x 64 / 128 x 128 / 128 x 256
+tiles (at most 8 / 6 / 4 stages of k-block 64) with group heights 4..32 at
+the most stages, and with every depth from 2 stages up at the default
+group; the skinny kernel when M <= 64.  Each configuration is forced
+through tg_gemm_force_path / tg_gemm_force_tiling / tg_gemm_force_stages,
+launched `reps` times from one CUDA graph over operand sets rotated past
+L2, and timed with CUDA events.
 
     python -m tiled_gemm_tg_gb300.sweep --shapes 1024x1024x1024,8192x8192x8192
 
@@ -26,15 +29,22 @@ PAIR, MAIN, SKINNY = 6, 3, 5
 L2_BYTES = 129 * 2**20
 
 
+MAX_STAGES = {(PAIR, 0): 3, (MAIN, 64): 8, (MAIN, 128): 6, (MAIN, 256): 4}
+
+
 def candidates(M: int, N: int, K: int):
-    out = [(PAIR, 0, g) for g in (2, 4, 8, 16, 32)]
-    out += [(MAIN, bn, g) for bn in (64, 128, 256) for g in (4, 8, 16, 32)]
+    """(path, tile width, group height, stages); 0 = the kernel's default."""
+    out = [(PAIR, 0, g, 0) for g in (2, 4, 8, 16, 32)]
+    out += [(PAIR, 0, 0, st) for st in range(2, MAX_STAGES[(PAIR, 0)])]
+    for bn in (64, 128, 256):
+        out += [(MAIN, bn, g, 0) for g in (4, 8, 16, 32)]
+        out += [(MAIN, bn, 0, st) for st in range(2, MAX_STAGES[(MAIN, bn)])]
     if M <= 64:
-        out.append((SKINNY, 0, 0))
+        out.append((SKINNY, 0, 0, 0))
     return out
 
 
-def time_config(M, N, K, path, bn, group, reps=50, sets=None, batch=1):
+def time_config(M, N, K, path, bn, group, reps=50, sets=None, batch=1, stages=0):
     """Microseconds per launch (CUDA-graph replay), or None if not served."""
     import torch
 
@@ -43,8 +53,9 @@ def time_config(M, N, K, path, bn, group, reps=50, sets=None, batch=1):
     a0, b0, c0 = sets[0]
     sa, sb, sc = M * K, K * N, M * N
     tg.tg_gemm_force_path(path)
-    if tg.tg_gemm_force_tiling(bn, group) != tg.TG_OK:
+    if tg.tg_gemm_force_tiling(bn, group) != tg.TG_OK or tg.tg_gemm_force_stages(stages) != tg.TG_OK:
         tg.tg_gemm_force_path(0)
+        tg.tg_gemm_force_stages(0)
         return None
     try:
         if tg.tg_gemm_batched_path(batch, M, N, K, a0.data_ptr(), K, sa, b0.data_ptr(), N, sb,
@@ -80,6 +91,7 @@ def time_config(M, N, K, path, bn, group, reps=50, sets=None, batch=1):
     finally:
         tg.tg_gemm_force_path(0)
         tg.tg_gemm_force_tiling(0, 0)
+        tg.tg_gemm_force_stages(0)
 
 
 def make_sets(M, N, K, batch=1):
@@ -108,10 +120,11 @@ def sweep(shapes, reps=50):
                                             tg.F16, tg.F16)
         auto_us = time_config(M, N, K, auto_path, 0, 0, reps, sets, batch)
         rows = []
-        for path, bn, group in candidates(M, N, K):
-            us = time_config(M, N, K, path, bn, group, reps, sets, batch)
+        for path, bn, group, stages in candidates(M, N, K):
+            us = time_config(M, N, K, path, bn, group, reps, sets, batch, stages)
             if us is not None:
-                rows.append({"path": path, "bn": bn, "group_m": group, "us": us,
+                rows.append({"path": path, "bn": bn, "group_m": group, "stages": stages,
+                             "us": us,
                              "tflops": 2.0 * batch * M * N * K / (us * 1e-6) / 1e12})
         best = min(rows, key=lambda r: r["us"])
         results.append({"shape": list(shape), "auto_path": auto_path, "auto_us": auto_us,
@@ -137,12 +150,14 @@ def main():
     for r in res:
         print(f"\n{'x'.join(str(v) for v in r['shape'])}: automatic path {r['auto_path']} {r['auto_us']:.1f} us; "
               f"best {names[r['best']['path']].format(bn=r['best']['bn'])} "
-              f"group {r['best']['group_m']} {r['best']['us']:.1f} us")
-        print("| config | group_m | us | TFLOP/s |")
-        print("|---|---|---|---|")
+              f"group {r['best']['group_m']} stages {r['best']['stages']} "
+              f"{r['best']['us']:.1f} us")
+        print("| config | group_m | stages | us | TFLOP/s |")
+        print("|---|---|---|---|---|")
         for c in sorted(r["configs"], key=lambda c: c["us"]):
-            print(f"| {names[c['path']].format(bn=c['bn'])} | {c['group_m'] or '-'} | "
-                  f"{c['us']:.1f} | {c['tflops']:.0f} |")
+            st = c["stages"] or MAX_STAGES.get((c["path"], c["bn"]), "-")
+            print(f"| {names[c['path']].format(bn=c['bn'])} | {c['group_m'] or 'default'} | "
+                  f"{st} | {c['us']:.1f} | {c['tflops']:.0f} |")
     if args.json:
         with open(args.json, "w") as f:
             json.dump(res, f, indent=1)
