@@ -44,31 +44,45 @@ METRIC = "GEMM TFLOP/s and % of GB300 dense FP16 tensor peak (1 GPU), vs CPU ora
 SPEC_FP16_DENSE_TFLOPS = 2500.0
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM traffic (read + write bytes per launch) of the main kernel from one
-# ncu capture, keyed by workload, with the hash of the kernel sources it was
-# taken on.  A stale hash means the kernel changed since: traffic is null.
-NCU_TRAFFIC = {
-    # the pair kernel's ncu summary under profiles/: 991.5 MB read + 124.1 MB written
-    "square_8192": {"bytes": 1115573504, "kernel_hash": "1a413666d8be47c8"},
-    # same summary, E4M3 inputs: 335.5 MB read + 115.1 MB written
-    "square_8192_e4m3": {"bytes": 450589440, "kernel_hash": "1a413666d8be47c8"},
-}
-
-KERNEL_SOURCES = ["tiled_gemm_tg_gb300/csrc/gemm_tc2.cu", "tiled_gemm_tg_gb300/csrc/ptx.cuh",
-                  "tiled_gemm_tg_gb300/csrc/tc_common.cuh", "tiled_gemm_tg_gb300/csrc/tg_internal.h"]
-
-
+# DRAM traffic (read + write bytes per launch) of a workload's kernel from
+# one ncu capture, with the hash of the kernel's sources it was taken on.  A
+# stale hash means the kernel changed since: traffic is then null.
+PAIR_SOURCES = ["tiled_gemm_tg_gb300/csrc/gemm_tc2.cu", "tiled_gemm_tg_gb300/csrc/ptx.cuh",
+                "tiled_gemm_tg_gb300/csrc/tc_common.cuh", "tiled_gemm_tg_gb300/csrc/tg_internal.h"]
+MAIN_SOURCES = ["tiled_gemm_tg_gb300/csrc/gemm_tc.cu", "tiled_gemm_tg_gb300/csrc/ptx.cuh",
+                "tiled_gemm_tg_gb300/csrc/tc_common.cuh", "tiled_gemm_tg_gb300/csrc/tg_internal.h",
+                "tiled_gemm_tg_gb300/csrc/l2_prefetch.cuh"]
+KERNEL_SOURCES = PAIR_SOURCES
 ATTN_KERNEL_SOURCES = ["tiled_gemm_tg_gb300/csrc/attention_fwd2.cu", "tiled_gemm_tg_gb300/csrc/ptx.cuh",
                        "tiled_gemm_tg_gb300/csrc/tc_common.cuh", "tiled_gemm_tg_gb300/csrc/tg_internal.h"]
+
+NCU_TRAFFIC = {
+    # the pair kernel's ncu summary under profiles/: 1027.8 MB read + 127.0 MB written
+    "square_8192": {"bytes": 1154789376, "kernel_hash": "4b14134fef017164",
+                    "sources": PAIR_SOURCES},
+    # the one-CTA kernel on the tiling example: 3.22 MB read, C still in L2 at exit
+    "tile_1024x2048x512": {"bytes": 3220224, "kernel_hash": "89fd4b9c0eb66a3e", "sources": MAIN_SOURCES},
+    # the one-CTA kernel on 256 products of 256^3: 67.2 MB read + 3.3 MB written
+    "batched_256x256x256x256": {"bytes": 70494208, "kernel_hash": "89fd4b9c0eb66a3e",
+                                "sources": MAIN_SOURCES},
+}
 
 # DRAM traffic per launch of the attention kernel that keeps P in tensor
 # memory, from one ncu capture, valid while its sources hash the same
 ATTN_NCU_TRAFFIC = {
-    # the kernel's ncu summary under profiles/: 50.4 MB read + 1.4 MB written
-    # (taken on 7adf12e0ed838ea7; the source has changed since in its header
-    # comment only)
-    "attn_16x4096x128": {"bytes": 51794176, "kernel_hash": "81e5a2daac910ddb"},
+    # the kernel's ncu summary under profiles/: 50.4 MB read + 1.1 MB written
+    "attn_16x4096x128": {"bytes": 51529472, "kernel_hash": "ff90030c6a44b06d",
+                         "sources": ATTN_KERNEL_SOURCES},
 }
+
+
+def traffic_of(table, name):
+    """The recorded DRAM bytes per launch for a workload, or None if there is
+    no record or the kernel's sources have changed since it was taken."""
+    rec = table.get(name)
+    if rec and rec.get("kernel_hash") == kernel_hash(rec.get("sources")):
+        return rec["bytes"]
+    return None
 
 
 def kernel_hash(sources=None) -> str:
@@ -506,8 +520,7 @@ def main_attention(args, w):
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     achieved = flops / (kern_ms * 1e-3) / 1e12
     alg_bytes = w.algorithmic_bytes()
-    rec = ATTN_NCU_TRAFFIC.get(w.name) if kern == 3 else None
-    attn_traffic = rec["bytes"] if rec and rec.get("kernel_hash") == kernel_hash(ATTN_KERNEL_SOURCES) else None
+    attn_traffic = traffic_of(ATTN_NCU_TRAFFIC, w.name) if kern == 3 else None
     roofline = {
         "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
         "frac": achieved / peak, "traffic": attn_traffic, "kernel": kern_name,
@@ -585,8 +598,9 @@ def roofline_of(flops: float, alg_bytes: float, seconds: float, peak_tflops: flo
 
 
 def measure_config(label, w, dev, launches, sampler, peaks, cpu_s, num_sms):
-    """One judged configuration: per-launch time stream-launched (CUDA events
-    around every launch) and replayed from one CUDA graph (no host gaps),
+    """One judged configuration: per-launch time stream-launched (launches
+    back to back from the host, CUDA events around the whole loop) and
+    replayed from one CUDA graph (no host gaps),
     operand sets rotated so one pass over them is at least 3x the L2; the
     roofline fraction of each; the clocks sampled meanwhile; the oracle's
     time on the host cores."""
@@ -620,15 +634,17 @@ def measure_config(label, w, dev, launches, sampler, peaks, cpu_s, num_sms):
         call(i, sh)
     tg.check(stream)
     t0 = time.time()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(launches)]
+    # stream-launched: back-to-back launches between two events (events
+    # around every launch would add their own host time to each gap)
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    s0.record(stream)
     for i in range(launches):
-        evs[i][0].record(stream)
         call(i, sh)
-        evs[i][1].record(stream)
+    s1.record(stream)
     torch.cuda.synchronize()
-    per = sorted(x.elapsed_time(y) * 1e3 for x, y in evs)
+    us_stream = s0.elapsed_time(s1) * 1e3 / launches
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         h = torch.cuda.current_stream().cuda_stream
@@ -646,7 +662,6 @@ def measure_config(label, w, dev, launches, sampler, peaks, cpu_s, num_sms):
     if tg.tg_gemm_check(sh) != tg.TG_OK:
         raise RuntimeError(f"{w.name}: a kernel abandoned a bounded wait")
     us_graph = g0.elapsed_time(g1) * 1e3 / launches
-    us_stream = sum(per) / len(per)
     del graph
 
     flops = float(w.flops)
@@ -665,8 +680,7 @@ def measure_config(label, w, dev, launches, sampler, peaks, cpu_s, num_sms):
         "in_dtype": w.in_dtype, "out_dtype": w.out_dtype, "dist": w.dist,
         "path": tg.PATHS.get(path, str(path)), "kernel": KERNEL_OF_PATH.get(path, str(path)),
         "launches": launches,
-        "us_stream_mean": us_stream, "us_stream_median": per[len(per) // 2],
-        "us_stream_best": per[0], "us_graph": us_graph,
+        "us_stream": us_stream, "us_graph": us_graph,
         "tflops_graph": flops / (us_graph * 1e-6) / 1e12,
         "tflops_stream": flops / (us_stream * 1e-6) / 1e12,
         "gbs_graph": set_bytes / (us_graph * 1e-6) / 1e9,
@@ -680,6 +694,7 @@ def measure_config(label, w, dev, launches, sampler, peaks, cpu_s, num_sms):
                         "measured bf16 burst (fp16 has the same nominal rate)"),
         "frac_graph": frac_graph, "frac_stream": frac_stream,
         "l2": f"{n_sets} rotating A/B/C sets, {n_sets * set_bytes / 2**20:.0f} MB per pass",
+        "traffic": traffic_of(NCU_TRAFFIC, w.name),
         "clocks": sampler.summary(t0, t1),
     }
     if cpu_s > 0:
@@ -940,10 +955,7 @@ def main():
     achieved = flops / (kern_ms * 1e-3) / 1e12
     alg_bytes = w.algorithmic_bytes() + (M * N * out_es if use_d else 0) + (
         N * 4 if use_bias else 0)
-    traffic = None
-    rec = NCU_TRAFFIC.get(w.name) if epi is None else None
-    if rec and rec.get("kernel_hash") == kernel_hash():
-        traffic = rec["bytes"]
+    traffic = traffic_of(NCU_TRAFFIC, w.name) if epi is None else None
     # The bound is the roofline's: a workload whose FLOP per algorithmic byte
     # lies below the ridge (measured tensor peak / measured HBM bandwidth) is
     # bound by HBM and is reported in GB/s against the copy bandwidth.
