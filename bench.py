@@ -734,6 +734,9 @@ def main():
                     help="skip the per-configuration records (configs 1, 2, 3, 5a, 5b)")
     ap.add_argument("--config-launches", type=int, default=200,
                     help="launches per judged configuration, stream-launched and in a graph")
+    ap.add_argument("--group-m", type=int, default=0,
+                    help="grouped tile-order height of the GEMM kernels (tg_gemm_force_tiling); "
+                         "0 = each kernel's default")
     ap.add_argument("--graph", action="store_true",
                     help="replay the timed launches from one CUDA graph (for us-scale shapes)")
     args = ap.parse_args()
@@ -763,6 +766,8 @@ def main():
         torch.cuda.set_device(0)
     dev = torch.device("cuda", torch.cuda.current_device())
     tg.lib()  # fail loudly if the library is missing
+    if args.group_m and tg.tg_gemm_force_tiling(0, args.group_m) != tg.TG_OK:
+        ap.error("--group-m must be 0..64")
 
     # operands: drawn on the host from the workload's seeds, copied to HBM
     a_cpu, b_cpu = inputs.operands(w)
@@ -1031,6 +1036,7 @@ def main():
                        "l2": f"{n_sets} rotating A/B/C sets, {n_sets * set_bytes / 2**20:.0f} MB "
                              "per pass (> L2)",
                        "timing": "CUDA graph replay" if graph is not None else "stream launches",
+                       "group_m": args.group_m or "default",
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
             "clocks": clocks,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
