@@ -28,10 +28,13 @@
 //     each).  Each thread owns one output row: tcgen05.ld of 32 columns at a
 //     time, the fused epilogue if any, fp32 -> fp16 round-to-nearest-even
 //     (or fp32 as is).  When C is TMA-addressable and its rows end on
-//     16-byte boundaries the warp's 32 x 32 chunk goes through a 4 KB
-//     shared-memory staging buffer per warp and leaves as one TMA store (the
-//     TMA engine clips it at the M/N edges); otherwise each thread writes
-//     its row with 16-byte vector stores, predicated at the edges.  The epilogue of tile i overlaps the main loop of tile i+1.
+//     16-byte boundaries the warp's 32 x 32 chunks go through a 4 KB
+//     shared-memory staging buffer per warp (two fp16 chunks double-
+//     buffered) and leave as one TMA store each (the TMA engine clips them
+//     at the M/N edges); otherwise each thread writes its row with 16-byte
+//     vector stores, predicated at the edges.  After its last TMEM read each
+//     epilogue warp arrives on a named barrier on which warp 1 waits to free
+//     TMEM, so the release overlaps the last stores.  The epilogue of tile i overlaps the main loop of tile i+1.
 // Out-of-range rows, columns and k are zero-filled by TMA, so any M, N, K
 // works as long as the operands are TMA-addressable (16-byte aligned bases,
 // row strides a multiple of 16 bytes); the host routes everything else to
@@ -80,6 +83,10 @@ constexpr int kThreads = 64 + 32 * kEpilogueWarps;
 // chunk or two fp16 chunks (double-buffered).
 constexpr uint32_t kStageC = 4096;
 constexpr uint32_t kStageCBytes = kEpilogueWarps * kStageC;
+// Named barrier on which the epilogue warps tell warp 1 that their last
+// TMEM read is done: the eight epilogue warps arrive, warp 1 waits.
+constexpr int kTmemFreeBar = 1;
+constexpr int kTmemFreeThreads = 32 * (kEpilogueWarps + 1);
 
 template <int BN>
 struct MainCfg {
@@ -141,13 +148,17 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     static_assert(BN % NB == 0, "B tile must be whole 128-byte boxes");
     const int num_kb = (K + BK - 1) / BK;
     const int total = tiles_m * tiles_n * bt.count;
+    // the producer's first tile, found before the wait for the previous
+    // kernel (the integer divisions of the tile order are on the critical
+    // path of a one-tile CTA otherwise)
+    int b0 = 0, tm0 = 0, tn0 = 0;
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
         // the first tile's first stages into L2 while the previous kernel finishes
         if (static_cast<int>(blockIdx.x) < total) {
-            int b, tm, tn;
-            batch_tile_coords(static_cast<int>(blockIdx.x), tiles_m, tiles_n, group_m, b, tm, tn);
+            batch_tile_coords(static_cast<int>(blockIdx.x), tiles_m, tiles_n, group_m, b0, tm0, tn0);
+            const int b = b0, tm = tm0, tn = tn0;
             const int pf = total > static_cast<int>(gridDim.x) ? stages
                                                                 : min(stages, kPrefetchStagesSingle);
             for (int kb = 0; kb < num_kb && kb < pf; ++kb) {
@@ -178,8 +189,9 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t ph = 0;
             uint32_t issued = 0;
             for (int t = blockIdx.x; t < total; t += gridDim.x) {
-                int b, tm, tn;
-                batch_tile_coords(t, tiles_m, tiles_n, group_m, b, tm, tn);
+                int b = b0, tm = tm0, tn = tn0;
+                if (t != static_cast<int>(blockIdx.x))
+                    batch_tile_coords(t, tiles_m, tiles_n, group_m, b, tm, tn);
                 const int za = b * bt.za, zb = b * bt.zb;
                 bool ok = true;
                 for (int kb = 0; kb < num_kb; ++kb) {
@@ -338,6 +350,10 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             acc ^= 1;
             if (acc == 0) aph ^= 1u;
         }
+        // every TMEM read of this warp is done: warp 1 may free TMEM now,
+        // while the last stores drain
+        tc_fence_before();
+        named_bar_arrive(kTmemFreeBar, kTmemFreeThreads);
         // the TMA stores have read their staging buffers before the CTA
         // ends (their writes to C complete with the grid)
         if (c_tma && lane == 0) bulk_wait_read<0>();
@@ -345,9 +361,10 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     }
 
     pdl_trigger();  // this CTA has issued all its global writes
-    tc_fence_before();
-    __syncthreads();
     if (warp == 1) {
+        // after the MMA thread's own MMAs (drained above) and every epilogue
+        // warp's last TMEM read
+        named_bar_sync(kTmemFreeBar, kTmemFreeThreads);
         tc_fence_after();
         tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
     }
@@ -393,19 +410,17 @@ cudaError_t launch_cfg(const GemmArgs& a)
     const int c_vec = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) &&
                       ((static_cast<size_t>(a.ldc) * es) % 16 == 0) &&
                       ((static_cast<size_t>(a.sC) * es) % 16 == 0);
-    // C written by TMA stores when the TMA engine can address it and each
-    // row of C ends on a 16-byte boundary: at the right edge of C a TMA
-    // store writes whole 16-byte units (measured: a box clipped at N = 129
-    // fp32 columns also wrote columns 129..131 of the row stride), and the
-    // ABI leaves columns N..ldc-1 untouched
+    // C written by TMA stores (32 x 32 boxes) when the TMA engine can
+    // address it and each row of C ends on a 16-byte boundary: at the right
+    // edge of C a TMA store writes whole 16-byte units (measured: a box
+    // clipped at N = 129 fp32 columns also wrote columns 129..131 of the row
+    // stride), and the ABI leaves columns N..ldc-1 untouched
     CUtensorMap tc;
     std::memset(&tc, 0, sizeof(tc));
     const int c_tma = c_vec && (static_cast<size_t>(a.N) * es) % 16 == 0 &&
                       encode_tmap_store(&tc, a.C, static_cast<int>(es),
-                                                 static_cast<uint64_t>(a.N),
-                                                 static_cast<uint64_t>(a.M),
-                                                 static_cast<uint64_t>(a.ldc), a.batch, a.sC,
-                                                 32, 32);
+                                        static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.M),
+                                        static_cast<uint64_t>(a.ldc), a.batch, a.sC, 32, 32);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);

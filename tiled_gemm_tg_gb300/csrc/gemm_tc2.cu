@@ -76,8 +76,8 @@ struct PairK {
 // (tg_gemm_force_stages), shared memory is sized to the ring
 constexpr int STAGES = 3;
 constexpr uint32_t SMEM = STAGES * STAGE + 1024;
-// Output staging for TMA stores: 4 KB per epilogue warp (one 32 x 32 fp32
-// chunk, or two fp16 chunks double-buffered), after the stages.
+// Output staging for TMA stores: 4 KB per epilogue warp (one box of 32 rows
+// x 128 bytes), after the stages.
 constexpr uint32_t kStageC = 4096;
 constexpr uint32_t TMEM_COLS = 2 * PN;           // two accumulators
 #ifndef TG_PAIR_EPI_WARPS
@@ -323,7 +323,6 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const uint32_t tempty0 = mapa_shared(smem_u32(&tempty_bar[0]), 0);  // leader's
         const uint32_t stage_c = base + static_cast<uint32_t>(stages) * STAGE +
                                  static_cast<uint32_t>(warp - 2) * kStageC;
-        uint32_t chunk = 0;  // staged chunks so far (fp16 alternates two 2 KB halves)
         int acc = 0;
         uint32_t aph = 0;
         for (int t = pair; t < total; t += npairs) {
@@ -348,34 +347,45 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const int m = m0 + lane;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * PN);
+            // columns per TMA store: one 128-byte row of the box
+            constexpr int G = OUT_F32 ? 32 : 64;
+            if (c_tma) {
 #pragma unroll 1
-            for (int c = c_lo; c < c_lo + span; c += EPI_COLS) {
-                uint32_t r[EPI_COLS];
-                if constexpr (EPI_COLS == 128) tmem_ld_32x32b_x128(taddr + c, r);
-                else if constexpr (EPI_COLS == 64) tmem_ld_32x32b_x64(taddr + c, r);
-                else tmem_ld_32x32b_x32(taddr + c, *reinterpret_cast<uint32_t(*)[32]>(r));
-                tmem_ld_wait();
+                for (int c = c_lo; c < c_lo + span; c += G) {
+                    uint32_t r[G];
+                    tmem_ld_32x32b_x32(taddr + c, *reinterpret_cast<uint32_t(*)[32]>(r));
+                    if constexpr (G == 64)
+                        tmem_ld_32x32b_x32(taddr + c + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+                    tmem_ld_wait();
+                    const int n = n0 + c;
+                    if (m0 < M && n < N) {  // warp-uniform
+                        if (epi.on && m < M) {
 #pragma unroll
-                for (int j = 0; j < EPI_COLS; j += 32) {
-                    const int n = n0 + c + j;
-                    if (c_tma) {
-                        if (m0 < M && n < N) {  // warp-uniform
-                            if (epi.on && m < M) epilogue_chunk<OUT_F32>(r + j, m, n, N, epi);
-                            // the staging slot is free once the store that
-                            // used it last has read it
-                            if (lane == 0) {
-                                if constexpr (OUT_F32) bulk_wait_read<0>();
-                                else bulk_wait_read<1>();
-                            }
-                            __syncwarp();
-                            const uint32_t slot =
-                                OUT_F32 ? stage_c : stage_c + (chunk & 1u) * (kStageC / 2);
-                            stage_store_chunk<OUT_F32>(&tmC, slot, r + j, n, m0, b, lane);
-                            ++chunk;
+                            for (int j = 0; j < G; j += 32)
+                                epilogue_chunk<OUT_F32>(r + j, m, n + j, N, epi);
                         }
-                    } else if (m < M && n < N) {
-                        if (epi.on) epilogue_chunk<OUT_F32>(r + j, m, n, N, epi);
-                        store_chunk<OUT_F32>(Cb, ldc, m, n, N, r + j, c_vec != 0);
+                        // the staging buffer is free once the previous store
+                        // has read it
+                        if (lane == 0) bulk_wait_read<0>();
+                        __syncwarp();
+                        stage_store_box<OUT_F32>(&tmC, stage_c, r, n, m0, b, lane);
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int c = c_lo; c < c_lo + span; c += EPI_COLS) {
+                    uint32_t r[EPI_COLS];
+                    if constexpr (EPI_COLS == 128) tmem_ld_32x32b_x128(taddr + c, r);
+                    else if constexpr (EPI_COLS == 64) tmem_ld_32x32b_x64(taddr + c, r);
+                    else tmem_ld_32x32b_x32(taddr + c, *reinterpret_cast<uint32_t(*)[32]>(r));
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < EPI_COLS; j += 32) {
+                        const int n = n0 + c + j;
+                        if (m < M && n < N) {
+                            if (epi.on) epilogue_chunk<OUT_F32>(r + j, m, n, N, epi);
+                            store_chunk<OUT_F32>(Cb, ldc, m, n, N, r + j, c_vec != 0);
+                        }
                     }
                 }
             }
@@ -465,7 +475,8 @@ cudaError_t launch_cfg(const GemmArgs& a)
     const int c_tma = c_vec && (static_cast<size_t>(a.N) * es) % 16 == 0 &&
                       encode_tmap_store(&tc, a.C, static_cast<int>(es),
                                         static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.M),
-                                        static_cast<uint64_t>(a.ldc), a.batch, a.sC, 32, 32);
+                                        static_cast<uint64_t>(a.ldc), a.batch, a.sC,
+                                        static_cast<uint32_t>(128 / es), 32);
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * pairs);

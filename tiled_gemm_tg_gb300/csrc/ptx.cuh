@@ -345,6 +345,13 @@ __device__ __forceinline__ void named_bar_sync(int id, int count)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Arrive on named barrier `id` without waiting (the threads that must wait
+// use named_bar_sync with the same count).
+__device__ __forceinline__ void named_bar_arrive(int id, int count)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // 16-byte shared-memory store.
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d)

@@ -228,5 +228,46 @@ __device__ __forceinline__ void stage_store_chunk(const CUtensorMap* tmC, uint32
     }
 }
 
+// One epilogue warp's 32-row x 128-byte box of C through shared memory and
+// one TMA store: rows m0..m0+31 (lane = row), 64 fp16 or 32 fp32 columns
+// from n, r[] the lane's fp32 accumulators after the fused epilogue (64 for
+// fp16 output, 32 for fp32).  The lane writes its row, converted, into the
+// warp's 4 KB staging buffer `slot` (128 bytes per row), and lane 0 stores
+// the box at (n, m0, z) of `tmC`; the TMA engine writes only the part
+// inside C.  The warp's rows then leave as one bulk copy instead of 32
+// scattered 16-byte stores per instruction.  The caller keeps `slot`
+// untouched until the store has read it (bulk_wait_read in lane 0, then
+// __syncwarp).
+template <bool OUT_F32>
+__device__ __forceinline__ void stage_store_box(const CUtensorMap* tmC, uint32_t slot,
+                                                const uint32_t* r, int n, int m0, int z,
+                                                int lane)
+{
+    const uint32_t row = slot + static_cast<uint32_t>(lane) * 128u;
+    if constexpr (OUT_F32) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            st_shared_v4(row + 16u * i, r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint32_t p[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                __half2 h = __floats2half2_rn(__uint_as_float(r[8 * i + 2 * j]),
+                                              __uint_as_float(r[8 * i + 2 * j + 1]));
+                p[j] = *reinterpret_cast<uint32_t*>(&h);
+            }
+            st_shared_v4(row + 16u * i, p[0], p[1], p[2], p[3]);
+        }
+    }
+    fence_proxy_async_smem();  // the rows are visible to the TMA engine
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_3d(tmC, slot, n, m0, z);
+        bulk_commit();
+    }
+}
+
 }  // namespace dev
 }  // namespace tg
