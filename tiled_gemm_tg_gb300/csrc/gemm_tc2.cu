@@ -11,7 +11,10 @@
 // B's columns (256 B of k x 128 columns) of a 256 x 256 k-block, so a 64 KB
 // stage feeds 1024 MMA cycles and each B column block is loaded once per pair
 // instead of once per 128 rows (a third less L2 -> SM traffic than 128 x 256
-// tiles).  Three stages fill 192 KB of shared memory.
+// tiles).  Three stages fill 192 KB of shared memory.  When the last wave of
+// tiles is at most half full, its tiles are cut into two 256 x 128 halves
+// (work_item), each pair loading one 64-column B box per CTA and issuing
+// N = 128 MMAs.
 //
 // Roles (320 threads per CTA, the same in both CTAs of the pair):
 //   warp 0   TMA producer.  Each CTA loads its own halves into its own shared
@@ -23,11 +26,11 @@
 //            each tile's commit to both CTAs' tmem-full barriers.
 //   warps 2-9  epilogue in both CTAs, two per TMEM lane quadrant: each CTA
 //            reads its own 128 rows of the accumulator from its own TMEM
-//            (each warp half of the columns) and stores them, 32 x 32 chunks
-//            staged in shared memory and written by TMA stores when C allows
-//            (16-byte aligned, rows ending on 16-byte boundaries), else
-//            16-byte stores per row; all epilogue threads of the pair arrive
-//            on the leader's tmem-empty barrier.
+//            (each warp half of the columns) and stores them, boxes of 32
+//            rows x 128 bytes staged in shared memory and written by TMA
+//            stores when C allows (16-byte aligned, rows ending on 16-byte
+//            boundaries), else 16-byte stores per row; all epilogue threads
+//            of the pair arrive on the leader's tmem-empty barrier.
 // Waits are bounded as in the one-CTA kernel; on expiry a role records a bit
 // in the device error word and leaves its loop; the leader waits for the
 // pair's copies in flight and its own MMAs; a cluster barrier keeps both CTAs
