@@ -57,21 +57,22 @@ ATTN_KERNEL_SOURCES = ["tiled_gemm_tg_gb300/csrc/attention_fwd2.cu", "tiled_gemm
                        "tiled_gemm_tg_gb300/csrc/tc_common.cuh", "tiled_gemm_tg_gb300/csrc/tg_internal.h"]
 
 NCU_TRAFFIC = {
-    # the pair kernel's ncu summary under profiles/: 1027.8 MB read + 127.0 MB written
-    "square_8192": {"bytes": 1154789376, "kernel_hash": "4b14134fef017164",
+    # the pair kernel's ncu summary under profiles/: 1020.1 MB read + 127.1 MB written
+    "square_8192": {"bytes": 1147142400, "kernel_hash": "613d64badb1afbff",
                     "sources": PAIR_SOURCES},
     # the one-CTA kernel on the tiling example: 3.22 MB read, C still in L2 at exit
-    "tile_1024x2048x512": {"bytes": 3220224, "kernel_hash": "89fd4b9c0eb66a3e", "sources": MAIN_SOURCES},
-    # the one-CTA kernel on 256 products of 256^3: 67.2 MB read + 3.3 MB written
-    "batched_256x256x256x256": {"bytes": 70494208, "kernel_hash": "89fd4b9c0eb66a3e",
+    "tile_1024x2048x512": {"bytes": 3220992, "kernel_hash": "b936f727f7d74405",
+                           "sources": MAIN_SOURCES},
+    # the one-CTA kernel on 256 products of 256^3: 67.2 MB read + 2.8 MB written
+    "batched_256x256x256x256": {"bytes": 69970944, "kernel_hash": "b936f727f7d74405",
                                 "sources": MAIN_SOURCES},
 }
 
 # DRAM traffic per launch of the attention kernel that keeps P in tensor
 # memory, from one ncu capture, valid while its sources hash the same
 ATTN_NCU_TRAFFIC = {
-    # the kernel's ncu summary under profiles/: 50.4 MB read + 1.1 MB written
-    "attn_16x4096x128": {"bytes": 51529472, "kernel_hash": "ff90030c6a44b06d",
+    # the kernel's ncu summary under profiles/: 50.4 MB read + 0.9 MB written
+    "attn_16x4096x128": {"bytes": 51322112, "kernel_hash": "9d37b1490dfb76de",
                          "sources": ATTN_KERNEL_SOURCES},
 }
 
@@ -105,8 +106,88 @@ def load_peaks():
 
 # ------------------------------------------------------------------- clocks
 
+class NvmlPoller:
+    """In-process NVML reads of the SM clock, its maximum, the clock-event
+    reasons and the power draw every `period_s`, so that a timed region of a
+    few milliseconds still holds samples (nvidia-smi's floor is 100 ms).
+    Only reads: nvmlDeviceGetClockInfo, nvmlDeviceGetMaxClockInfo,
+    nvmlDeviceGetCurrentClocksEventReasons, nvmlDeviceGetPowerUsage."""
+
+    NVML_CLOCK_SM = 1
+    # clock-event reason bits of the public NVML API
+    REASON_BITS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown",
+                   0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
+
+    def __init__(self, uuid: str | None, period_s: float = 0.002):
+        self.samples = []
+        self.period_s = period_s
+        self.ok = False
+        self._stop = threading.Event()
+        self.thread = None
+        if not uuid:
+            return
+        try:
+            import ctypes
+
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            dev = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(dev)) != 0:
+                return
+            reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self._ct, self._lib, self._dev, self._reasons = ctypes, lib, dev, reasons
+            self.ok = True
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def _one(self):
+        ct, lib, dev = self._ct, self._lib, self._dev
+        mhz, mx, mw = ct.c_uint(), ct.c_uint(), ct.c_uint()
+        mask = ct.c_ulonglong()
+        if lib.nvmlDeviceGetClockInfo(dev, self.NVML_CLOCK_SM, ct.byref(mhz)) != 0:
+            return None
+        lib.nvmlDeviceGetMaxClockInfo(dev, self.NVML_CLOCK_SM, ct.byref(mx))
+        self._reasons(dev, ct.byref(mask))
+        lib.nvmlDeviceGetPowerUsage(dev, ct.byref(mw))
+        return (float(mhz.value), float(mx.value), int(mask.value), mw.value / 1000.0)
+
+    def _loop(self):
+        while not self._stop.is_set():
+            r = self._one()
+            if r is not None:
+                self.samples.append((time.time(),) + r)
+            time.sleep(self.period_s)
+
+    def start(self):
+        if self.ok:
+            self._stop.clear()
+            self.thread = threading.Thread(target=self._loop, daemon=True)
+            self.thread.start()
+
+    def stop(self):
+        self._stop.set()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        inside = [x for x in self.samples if t0 <= x[0] <= t1]
+        if len(inside) < 3:
+            return None
+        sm = sorted(x[1] for x in inside)
+        reasons = sorted({name for x in inside for bit, name in self.REASON_BITS.items()
+                          if x[3] & bit})
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(x[2] for x in inside),
+                "sm_mhz_min": sm[0], "reasons": reasons, "samples": len(inside),
+                "window": f"timed (NVML every {self.period_s * 1e3:.0f} ms)",
+                "power_w_max": max(x[4] for x in inside)}
+
+
 class ClockSampler:
-    """nvidia-smi clock/throttle samples every 100 ms while running."""
+    """Clock/throttle samples while running: NVML polled in-process every
+    2 ms (the timed region is often shorter than nvidia-smi's 100 ms period),
+    with nvidia-smi every 100 ms beside it as the fallback."""
 
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -117,8 +198,10 @@ class ClockSampler:
         self.proc = None
         self.gpu_id = gpu_id
         self.thread = None
+        self.nvml = NvmlPoller(gpu_id)
 
     def start(self):
+        self.nvml.start()
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                "-lms", "100"]
         if self.gpu_id:
@@ -139,6 +222,7 @@ class ClockSampler:
                 self.samples.append((time.time(), parts))
 
     def stop(self):
+        self.nvml.stop()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -149,6 +233,9 @@ class ClockSampler:
             self.thread.join(timeout=5)
 
     def summary(self, t0: float, t1: float):
+        fine = self.nvml.summary(t0, t1)
+        if fine is not None:
+            return fine
         inside = [p for (t, p) in self.samples if t0 <= t <= t1]
         window = "timed"
         if len(inside) < 3:
