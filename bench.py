@@ -173,7 +173,7 @@ class NvmlPoller:
 
     def summary(self, t0: float, t1: float):
         inside = [x for x in self.samples if t0 <= x[0] <= t1]
-        if len(inside) < 3:
+        if not inside:
             return None
         sm = sorted(x[1] for x in inside)
         reasons = sorted({name for x in inside for bit, name in self.REASON_BITS.items()

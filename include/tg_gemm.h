@@ -441,6 +441,17 @@ tg_status tg_gemm_force_split_tail(int tiles);
 int tg_gemm_pair_split_tail(int64_t tiles, int max_pairs);
 
 /*
+ * The boundary kernel's split over K (the kernel that serves operands the TMA
+ * engine cannot address), computed on the host alone: a problem with `tiles`
+ * 128 x 128 output tiles (all products of a call together) and `kblocks`
+ * k-blocks of 64 is shared by clusters of S CTAs, S the largest of 2, 4 and 8
+ * with tiles * S <= num_sms and S <= kblocks, else 1.  On a device the
+ * library also requires that `tiles` clusters of S fit at once.  1 for
+ * non-positive arguments.
+ */
+int tg_gemm_boundary_split(int64_t tiles, int kblocks, int num_sms);
+
+/*
  * Attention kernel selection, for tests and benchmarks.  tg_attention_kernel
  * reports, without launching anything, which forward kernel a call with these
  * sizes would run on the current device: tg_attention (split_allowed = 0),

@@ -479,6 +479,25 @@ def test_pair_split_tail_rule(tiles, pairs, want):
         assert got == last and 2 * last <= pairs
 
 
+@pytest.mark.parametrize("tiles,kblocks,sms,want", [
+    (2, 8, 152, 8),        # 127 x 255 x 512: two tiles, one k-block per CTA
+    (15, 8, 152, 8), (19, 8, 152, 8), (20, 8, 152, 4), (38, 8, 152, 4), (39, 8, 152, 2),
+    (76, 8, 152, 2), (77, 8, 152, 1), (128, 16, 152, 1),
+    (1, 1, 152, 1), (1, 2, 152, 2), (1, 3, 152, 2), (1, 7, 152, 4), (1, 100, 152, 8),
+    (3, 8, 4, 1), (2, 8, 4, 2),
+    (0, 8, 152, 1), (5, 0, 152, 1), (5, 8, 0, 1), (-1, 8, 152, 1),
+])
+def test_boundary_split_rule(tiles, kblocks, sms, want):
+    """The boundary kernel's split over K, on the host: the largest cluster
+    of 2, 4 or 8 CTAs per output tile that keeps every CTA on its own SM and
+    gives each at least one k-block."""
+    got = tg.tg_gemm_boundary_split(tiles, kblocks, sms)
+    assert got == want
+    if got > 1:
+        assert tiles * got <= sms and got <= kblocks
+        assert got == 8 or tiles * 2 * got > sms or 2 * got > kblocks
+
+
 def test_force_split_tail_arguments():
     assert tg.tg_gemm_force_split_tail(-2) == tg.TG_ERR_INVALID_ARG
     for v in (0, 5, -1):

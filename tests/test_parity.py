@@ -307,6 +307,43 @@ def test_integer_inputs_bitwise(M, N, K, ld_pad, off, out, path):
         assert np.array_equal(got, C_ref)
 
 
+# (M, N, K): B's row stride is not a multiple of 16 bytes, so the boundary
+# kernel serves them; on 152 SMs the tile counts and k-blocks give clusters of 8 (one or
+# two k-blocks per CTA), 4 and 2 CTAs per output tile, and no split.
+BOUNDARY_SPLIT_SHAPES = [(127, 255, 512), (300, 700, 1000), (513, 520, 333), (129, 1000, 130),
+                         (100, 90, 300), (70, 33, 65), (1000, 2000, 700)]
+
+
+def _odd_ld(n: int) -> int:
+    """A row stride >= n that no TMA tensor map accepts (not a multiple of 8
+    fp16 elements)."""
+    return n + 1 if (n + 1) % 8 else n + 3
+
+
+@pytest.mark.parametrize("M,N,K", BOUNDARY_SPLIT_SHAPES)
+@pytest.mark.parametrize("out", [torch.float16, torch.float32])
+def test_boundary_split_k(M, N, K, out):
+    """The boundary kernel with its output tiles shared over K by a cluster:
+    every element against the oracle, canaries intact."""
+    a = inputs.draw((M, K), "normal", 7050 + M, "f16")
+    b = inputs.draw((K, N), "normal", 7060 + N, "f16")
+    _, _, p = check_full(a, b, out, ldb=_odd_ld(N), ldc=N + 1)
+    assert p == BOUNDARY
+
+
+@pytest.mark.parametrize("M,N,K", BOUNDARY_SPLIT_SHAPES[:4])
+def test_boundary_split_k_integer_bitwise(M, N, K):
+    """Integer inputs: every partial sum is exact in fp32, so the sum over
+    the cluster's partials equals the oracle bit for bit whatever the split."""
+    a = inputs.draw((M, K), "int2", 7070 + M, "f16")
+    b = inputs.draw((K, N), "int2", 7080 + N, "f16")
+    got, intact, p = run(a, b, torch.float16, ldb=_odd_ld(N), ldc=N + 3)
+    assert p == BOUNDARY and intact
+    C_ref, _ = oracle.gemm(a.numpy(), b.numpy())
+    have = torch.from_numpy(got).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(have, f16_bits_of(C_ref))
+
+
 def test_fp32_integer_inputs_exact():
     a = inputs.draw((77, 130), "int2", 7101, "f32")
     b = inputs.draw((130, 45), "int2", 7102, "f32")

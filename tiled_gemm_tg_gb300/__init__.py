@@ -20,6 +20,7 @@ __all__ = [
     "TG_ERR_TIMEOUT", "PATHS", "TgError", "lib", "library_path", "tg_gemm", "tg_gemm_check",
     "tg_status_string", "tg_gemm_path", "tg_gemm_force_path", "tg_gemm_force_tiling",
     "tg_gemm_force_split_tail", "tg_gemm_pair_split_tail", "tg_gemm_force_stages",
+    "tg_gemm_boundary_split",
     "tg_gemm_test_hook", "tg_gemm_ex", "tg_gemm_batched", "tg_gemm_batched_path",
     "tg_attention", "tg_attention_ws", "tg_attention_workspace_size", "tg_attention_noalloc",
     "tg_attention_kernel", "tg_attention_force_kernel", "tg_attention_tail_plan",
@@ -115,6 +116,8 @@ def lib() -> ctypes.CDLL:
         L.tg_gemm_force_split_tail.argtypes = [i32]
         L.tg_gemm_pair_split_tail.restype = i32
         L.tg_gemm_pair_split_tail.argtypes = [i64, i32]
+        L.tg_gemm_boundary_split.restype = i32
+        L.tg_gemm_boundary_split.argtypes = [i64, i32, i32]
         L.tg_gemm_force_stages.restype = i32
         L.tg_gemm_force_stages.argtypes = [i32]
         L.tg_gemm_test_hook.restype = None
@@ -227,6 +230,10 @@ def tg_gemm_force_stages(stages: int) -> int:
 
 def tg_gemm_pair_split_tail(tiles: int, max_pairs: int) -> int:
     return int(lib().tg_gemm_pair_split_tail(int(tiles), int(max_pairs)))
+
+
+def tg_gemm_boundary_split(tiles: int, kblocks: int, num_sms: int) -> int:
+    return int(lib().tg_gemm_boundary_split(int(tiles), int(kblocks), int(num_sms)))
 
 
 def tg_gemm_test_hook(hook: int) -> None:

@@ -10,8 +10,19 @@
 // swizzled shared-memory layout the TMA path produces, and fed to the same
 // tcgen05.mma (M=128, N=BN, K=16) with an fp32 accumulator in tensor memory.
 // Each thread issues all its loads of k-block i+1 into registers while the
-// tensor core runs k-block i; two shared-memory stages.  One CTA per
-// 128 x BN output tile; 4 warps; stores predicated.
+// tensor core runs k-block i; two shared-memory stages.  4 warps; stores
+// predicated.
+//
+// Loads that cannot be 16 bytes wide are latency-bound, so a problem with few
+// 128 x BN output tiles is also split over K: a cluster of S CTAs (S = 2, 4
+// or 8) shares one output tile, CTA r taking k-blocks [r*nkb/S, (r+1)*nkb/S).
+// Each CTA writes its fp32 partial tile into its own shared memory (rows
+// padded by four floats, so the writes from tensor-memory lanes do not
+// collide on banks), the cluster synchronises, and CTA r adds up, in rank
+// order, rows [r*128/S, (r+1)*128/S) of all S partials through distributed
+// shared memory, applies the epilogue and stores them.  With S = 1 (enough
+// tiles to fill the GPU) each CTA stores its tile straight from tensor
+// memory.
 #include <cstdint>
 #include <mutex>
 
@@ -33,7 +44,10 @@ constexpr int BK = 64;
 constexpr uint32_t A_STAGE = BM * BK * 2;   // 16 KB
 constexpr uint32_t B_STAGE = BN * BK * 2;   // 16 KB: two [64 k][64 n] atoms-columns
 constexpr uint32_t STAGE = A_STAGE + B_STAGE;
-constexpr uint32_t SMEM = 2 * STAGE + 1024;
+constexpr int RED_LD = BN + 4;                       // floats per partial row
+constexpr uint32_t RED_BYTES = BM * RED_LD * 4;      // fp32 partial tile, 66 KB
+constexpr uint32_t SMEM = (2 * STAGE > RED_BYTES ? 2 * STAGE : RED_BYTES) + 1024;
+constexpr int kMaxSplit = 8;
 constexpr uint32_t TMEM_COLS = BN;
 constexpr int kThreads = 128;
 
@@ -138,7 +152,7 @@ __device__ __forceinline__ void stash(const Frag& f, uint8_t* sA, uint8_t* sB, i
 template <bool OUT_F32>
 __global__ void __launch_bounds__(kThreads)
 gemm_tc_boundary_kernel(const __half* __restrict__ A0, long long lda, const __half* __restrict__ B0,
-                        long long ldb, void* C0, long long ldc, int M, int N, int K,
+                        long long ldb, void* C0, long long ldc, int M, int N, int K, int split,
                         int hook, unsigned int* err, Epilogue epi, BatchArgs bt)
 {
     // grid.z walks the matrices of a strided batch
@@ -161,7 +175,9 @@ gemm_tc_boundary_kernel(const __half* __restrict__ A0, long long lda, const __ha
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int m0 = blockIdx.y * BM;
-    const int n0 = blockIdx.x * BN;
+    // a cluster of `split` CTAs along x shares one output tile
+    const int rank = split > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    const int n0 = static_cast<int>(blockIdx.x / split) * BN;
 
     if (tid == 0) {
         mbar_init(smem_u32(&mma_bar[0]), 1);
@@ -180,12 +196,15 @@ gemm_tc_boundary_kernel(const __half* __restrict__ A0, long long lda, const __ha
     pdl_wait();  // the previous kernel on the stream is complete from here on
 
     constexpr uint32_t idesc = idesc_f16_f32(BM, BN, false, true);
-    const int num_kb = (K + BK - 1) / BK;
+    const int nkb_all = (K + BK - 1) / BK;
+    const int kb0 = static_cast<int>(static_cast<long long>(rank) * nkb_all / split);
+    const int num_kb = static_cast<int>(static_cast<long long>(rank + 1) * nkb_all / split) - kb0;
     bool aborted = false;
 
-    // Registers carry k-block kb+1 while the tensor core works on k-block kb.
+    // Registers carry k-block i+1 while the tensor core works on k-block i
+    // (i counts this CTA's k-blocks; kb0 + i is the k-block of the problem).
     Frag f;
-    fetch(f, A, lda, a_vec, B, ldb, b_vec, M, N, K, m0, n0, 0, tid);
+    if (num_kb > 0) fetch(f, A, lda, a_vec, B, ldb, b_vec, M, N, K, m0, n0, kb0 * BK, tid);
     for (int kb = 0; kb < num_kb; ++kb) {
         const int s = kb & 1;
         if (kb >= 2) {
@@ -212,15 +231,84 @@ gemm_tc_boundary_kernel(const __half* __restrict__ A0, long long lda, const __ha
             if (!(hook == 1 && kb == 0)) umma_commit(smem_u32(&mma_bar[s]));
         }
         if (kb + 1 < num_kb)
-            fetch(f, A, lda, a_vec, B, ldb, b_vec, M, N, K, m0, n0, (kb + 1) * BK, tid);
+            fetch(f, A, lda, a_vec, B, ldb, b_vec, M, N, K, m0, n0, (kb0 + kb + 1) * BK, tid);
     }
 
-    if (!aborted) {
+    if (!aborted && num_kb > 0) {
         const int last = num_kb - 1;
         const bool got = mbar_wait(smem_u32(&mma_bar[last & 1]), (last >> 1) & 1, nullptr);
         if (__syncthreads_or(got ? 0 : 1)) aborted = true;
     }
-    if (!aborted) {
+    if (split > 1) {
+        // This CTA's partial tile -> its shared memory (the stages are free:
+        // every MMA reading them has completed), row m_local at
+        // red[m_local * RED_LD]; a CTA without k-blocks contributes zeros.
+        float* const red = reinterpret_cast<float*>(gbase);
+        if (!aborted) {
+            tc_fence_after();
+            const int ml = warp * 32 + lane;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16);
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t r[32];
+                if (num_kb > 0) {
+                    tmem_ld_32x32b_x32(taddr + c, r);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = 0u;
+                }
+                float4* row = reinterpret_cast<float4*>(red + ml * RED_LD + c);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    row[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                         __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+            }
+        } else if (tid == 0) {
+            atomicOr(err, ERR_BOUNDARY);
+        }
+        // every partial of the cluster is in shared memory after this barrier
+        cluster_sync();
+        const int span = BM / split;
+        const uint32_t red_local = smem_u32(red);
+        for (int idx = tid; idx < span * (BN / 4); idx += kThreads) {
+            const int ml = rank * span + idx / (BN / 4);
+            const int nl = 4 * (idx % (BN / 4));
+            const int m = m0 + ml, n = n0 + nl;
+            if (m >= M || n >= N) continue;
+            const uint32_t off = static_cast<uint32_t>((ml * RED_LD + nl) * 4);
+            float4 part[kMaxSplit];
+#pragma unroll
+            for (int r = 0; r < kMaxSplit; ++r)
+                if (r < split) {
+                    const uint32_t ra = mapa_shared(red_local + off, static_cast<uint32_t>(r));
+                    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                 : "=f"(part[r].x), "=f"(part[r].y), "=f"(part[r].z), "=f"(part[r].w)
+                                 : "r"(ra)
+                                 : "memory");
+                }
+            float sum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int r = 0; r < kMaxSplit; ++r)
+                if (r < split) {
+                    sum[0] += part[r].x;
+                    sum[1] += part[r].y;
+                    sum[2] += part[r].z;
+                    sum[3] += part[r].w;
+                }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (n + j >= N) break;
+                float y = sum[j];
+                if (epi.on) y = epilogue_elem<OUT_F32>(y, m, n + j, epi);
+                if constexpr (OUT_F32)
+                    static_cast<float*>(C)[static_cast<long long>(m) * ldc + n + j] = y;
+                else
+                    static_cast<__half*>(C)[static_cast<long long>(m) * ldc + n + j] =
+                        __float2half_rn(y);
+            }
+        }
+    } else if (!aborted) {
         tc_fence_after();
         const int m = m0 + warp * 32 + lane;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(warp * 32) << 16);
@@ -255,6 +343,8 @@ gemm_tc_boundary_kernel(const __half* __restrict__ A0, long long lda, const __ha
         if (!mbar_wait(smem_u32(&drain_bar), 0, nullptr)) atomicOr(err, ERR_DRAIN);
     }
     pdl_trigger();  // this CTA has issued all its global writes
+    // no CTA may leave while a peer can still read its shared memory
+    if (split > 1) cluster_sync();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -265,38 +355,88 @@ gemm_tc_boundary_kernel(const __half* __restrict__ A0, long long lda, const __ha
 
 std::mutex g_attr_mu;
 bool g_attr_set[64][2];
+// Clusters of 2, 4 and 8 CTAs that can be resident at once, per device and
+// output type.
+int g_max_clusters[64][2][3];
+
+}  // namespace
+
+int boundary_split(long long tiles, int nkb, int num_sms, const int* max_clusters)
+{
+    int s = 1;
+    for (int i = 0; i < 3; ++i) {
+        const int t = 2 << i;
+        if (t > kMaxSplit || tiles * t > num_sms || nkb < t ||
+            (max_clusters != nullptr && tiles > max_clusters[i]))
+            break;
+        s = t;
+    }
+    return s;
+}
+
+namespace {
 
 template <bool OUT_F32>
 cudaError_t launch_cfg(const GemmArgs& a)
 {
     auto kernel = gemm_tc_boundary_kernel<OUT_F32>;
+    const int o = OUT_F32 ? 1 : 0;
+    int split = 1;
     {
         int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
         std::lock_guard<std::mutex> lock(g_attr_mu);
         if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-        if (!g_attr_set[dev][OUT_F32 ? 1 : 0]) {
+        if (!g_attr_set[dev][o]) {
             e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(SMEM));
             if (e != cudaSuccess) return e;
-            g_attr_set[dev][OUT_F32 ? 1 : 0] = true;
+            for (int i = 0; i < 3; ++i) {
+                cudaLaunchConfig_t q = {};
+                q.gridDim = dim3(2 << i, 1);
+                q.blockDim = dim3(kThreads);
+                q.dynamicSmemBytes = SMEM;
+                cudaLaunchAttribute at[1];
+                at[0].id = cudaLaunchAttributeClusterDimension;
+                at[0].val.clusterDim.x = 2 << i;
+                at[0].val.clusterDim.y = 1;
+                at[0].val.clusterDim.z = 1;
+                q.attrs = at;
+                q.numAttrs = 1;
+                int n = 0;
+                if (cudaOccupancyMaxActiveClusters(&n, kernel, &q) != cudaSuccess) {
+                    cudaGetLastError();
+                    n = 0;
+                }
+                g_max_clusters[dev][o][i] = n;
+            }
+            g_attr_set[dev][o] = true;
         }
+        const long long tiles = static_cast<long long>((a.N + BN - 1) / BN) *
+                                ((a.M + BM - 1) / BM) * a.batch;
+        split = boundary_split(tiles, (a.K + BK - 1) / BK, a.num_sms, g_max_clusters[dev][o]);
     }
-    const dim3 grid((a.N + BN - 1) / BN, (a.M + BM - 1) / BM, a.batch);
+    const long long gx = static_cast<long long>((a.N + BN - 1) / BN) * split;
+    if (gx > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const dim3 grid(static_cast<unsigned>(gx), (a.M + BM - 1) / BM, a.batch);
     if (grid.y > 65535u || grid.z > 65535u) return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = SMEM;
     cfg.stream = a.stream;
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     set_pdl_attr(at[0]);
+    at[1].id = cudaLaunchAttributeClusterDimension;
+    at[1].val.clusterDim.x = split;
+    at[1].val.clusterDim.y = 1;
+    at[1].val.clusterDim.z = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = split > 1 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<const __half*>(a.A), a.lda,
                               static_cast<const __half*>(a.B), a.ldb, a.C, a.ldc, a.M, a.N, a.K,
-                              a.hook, a.err, a.epi, a.batch_args());
+                              split, a.hook, a.err, a.epi, a.batch_args());
 }
 
 }  // namespace

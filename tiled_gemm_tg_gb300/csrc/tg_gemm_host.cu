@@ -820,6 +820,12 @@ int tg_gemm_pair_split_tail(int64_t tiles, int max_pairs)
     return tg::pair_split_tail(static_cast<int>(tiles), max_pairs, -1);
 }
 
+int tg_gemm_boundary_split(int64_t tiles, int kblocks, int num_sms)
+{
+    if (tiles <= 0 || kblocks <= 0 || num_sms <= 0) return 1;
+    return tg::boundary_split(tiles, kblocks, num_sms, nullptr);
+}
+
 int tg_gemm_version(void) { return 100; }
 
 }  // extern "C"
