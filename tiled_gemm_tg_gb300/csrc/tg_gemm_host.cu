@@ -441,6 +441,11 @@ bool encode_tmap_store(CUtensorMap* map, const void* ptr, int es, uint64_t cols,
     return encode_map(map, 1, ptr, es, cols, rows, ld, batch, stride, box_cols, box_rows);
 }
 
+// Defined beside the boundary kernel: clusters of S CTAs that share one boundary-kernel
+// output tile over K: the largest S of 2, 4, 8 with tiles * S <= num_sms,
+// S <= nkb and (given max_clusters[i], the clusters of 2 << i that fit at
+// once) `tiles` clusters resident together; else 1.
+int boundary_split(long long tiles, int nkb, int num_sms, const int* max_clusters);
 }  // namespace tg
 
 extern "C" {

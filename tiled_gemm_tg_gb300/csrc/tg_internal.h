@@ -199,12 +199,6 @@ int main_tile_n(int M, int N, int batch, int num_sms);
 int main_max_stages(int bn);
 int pair_max_stages();
 
-// Clusters of S CTAs that share one boundary-kernel output tile over K: the
-// largest S of 2, 4, 8 with tiles * S <= num_sms, S <= nkb and (given
-// max_clusters[i], the clusters of 2 << i that fit at once) tiles clusters
-// resident together; else 1.
-int boundary_split(long long tiles, int nkb, int num_sms, const int* max_clusters);
-
 // Largest M the skinny kernel serves.
 constexpr int kSkinnyMaxM = 64;
 
