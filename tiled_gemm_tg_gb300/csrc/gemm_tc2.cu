@@ -14,7 +14,10 @@
 // tiles).  Three stages fill 192 KB of shared memory.  When the last wave of
 // tiles is at most half full, its tiles are cut into two 256 x 128 halves
 // (work_item), each pair loading one 64-column B box per CTA and issuing
-// N = 128 MMAs.
+// N = 128 MMAs.  Each pair walks K forwards on its even-numbered tiles and
+// backwards on its odd-numbered ones: the pairs of one wave share A rows with
+// the wave before, whose last-read k-blocks are the ones still in L2 (8192^3:
+// 1020 -> 854 MB of DRAM reads per launch, ~1 % faster).
 //
 // Roles (320 threads per CTA, the same in both CTAs of the pair):
 //   warp 0   TMA producer.  Each CTA loads its own halves into its own shared
@@ -102,6 +105,7 @@ static_assert(TMEM_COLS == 512, "two 256-column accumulators fill TMEM");
 #define TG_PAIR_L2_HINTS 1
 #endif
 constexpr int L2_HINTS = TG_PAIR_L2_HINTS;  // bit 0: A evict_last, bit 1: B evict_first
+
 #ifndef TG_PAIR_EPI_COLS
 #define TG_PAIR_EPI_COLS 32
 #endif
@@ -203,9 +207,13 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t ph = 0;
             uint32_t issued = 0;
             bool ok = true;
-            for (int t = pair; t < total && ok; t += npairs) {
+            int wave = 0;
+            for (int t = pair; t < total && ok; t += npairs, ++wave) {
                 int b, tm, tn, half;
                 work_item<ES>(t, tiles_m, tiles_n, group_m, whole, split_tail, b, tm, tn, half);
+                // every other wave walks K backwards, starting on the k-blocks
+                // of the A rows the wave before it read last (still in L2)
+                const bool back = (wave & 1) != 0;
                 const int za = b * bt.za, zb = b * bt.zb;
                 const int row = tm * PM + static_cast<int>(rank) * HM;
                 // a half item: each CTA holds 64 of its 128 columns (one box)
@@ -220,6 +228,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         ok = false;
                         break;
                     }
+                    const int kk = back ? num_kb - 1 - kb : kb;
                     if (hook == 1 && leader && t == pair && kb == 0) {
                         // test hook: the leader never arms this stage, so the
                         // MMA thread's bounded wait on it runs out
@@ -234,11 +243,11 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const uint32_t sa = base + s * STAGE;
 #pragma unroll
                     for (int j = 0; j < KA; ++j)
-                        tma_load_3d_pair_hint(sa + j * A_ATOM, &tmA, fb, kb * BK + j * KG::AE,
+                        tma_load_3d_pair_hint(sa + j * A_ATOM, &tmA, fb, kk * BK + j * KG::AE,
                                               row, za, pol_a);
                     for (int j = 0; j < nbox; ++j)
                         tma_load_3d_pair_hint(sa + A_STAGE + j * KG::B_BOX, &tmB, fb,
-                                              col + j * KG::NB, kb * BK, zb, pol_b);
+                                              col + j * KG::NB, kk * BK, zb, pol_b);
                     ++issued;
                     if (++s == stages) {
                         s = 0;
