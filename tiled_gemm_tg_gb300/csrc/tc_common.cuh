@@ -13,7 +13,9 @@ namespace tg {
 namespace dev {
 
 // Grouped tile order: tiles are visited in groups of `group_m` tile-rows,
-// column by column inside a group.
+// column by column inside a group, left to right in even groups and right to
+// left in odd ones, so a group starts on the B columns its predecessor read
+// last.
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int group_m,
                                             int& tm, int& tn)
 {
@@ -23,7 +25,7 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
     const int gs = min(tiles_m - first, group_m);
     const int r = t - g * span;
     tm = first + r % gs;
-    tn = r / gs;
+    tn = (g & 1) ? tiles_n - 1 - r / gs : r / gs;
 }
 
 // Tile t of a strided batch of matrices, each tiles_m x tiles_n tiles walked
