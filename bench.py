@@ -57,22 +57,22 @@ ATTN_KERNEL_SOURCES = ["tiled_gemm_tg_gb300/csrc/attention_fwd2.cu", "tiled_gemm
                        "tiled_gemm_tg_gb300/csrc/tc_common.cuh", "tiled_gemm_tg_gb300/csrc/tg_internal.h"]
 
 NCU_TRAFFIC = {
-    # the pair kernel's ncu summary under profiles/: 1020.1 MB read + 127.1 MB written
-    "square_8192": {"bytes": 1147142400, "kernel_hash": "613d64badb1afbff",
+    # the pair kernel's ncu summary under profiles/: 773.2 MB read + 127.0 MB written
+    "square_8192": {"bytes": 900219904, "kernel_hash": "204d16ae8a623739",
                     "sources": PAIR_SOURCES},
     # the one-CTA kernel on the tiling example: 3.22 MB read, C still in L2 at exit
-    "tile_1024x2048x512": {"bytes": 3220992, "kernel_hash": "b936f727f7d74405",
+    "tile_1024x2048x512": {"bytes": 3220480, "kernel_hash": "b12d6de54d93c6c6",
                            "sources": MAIN_SOURCES},
-    # the one-CTA kernel on 256 products of 256^3: 67.2 MB read + 2.8 MB written
-    "batched_256x256x256x256": {"bytes": 69970944, "kernel_hash": "b936f727f7d74405",
+    # the one-CTA kernel on 256 products of 256^3: 67.2 MB read + 3.2 MB written
+    "batched_256x256x256x256": {"bytes": 70385408, "kernel_hash": "b12d6de54d93c6c6",
                                 "sources": MAIN_SOURCES},
 }
 
 # DRAM traffic per launch of the attention kernel that keeps P in tensor
 # memory, from one ncu capture, valid while its sources hash the same
 ATTN_NCU_TRAFFIC = {
-    # the kernel's ncu summary under profiles/: 50.4 MB read + 0.9 MB written
-    "attn_16x4096x128": {"bytes": 51322112, "kernel_hash": "9d37b1490dfb76de",
+    # the kernel's ncu summary under profiles/: 50.4 MB read + 1.1 MB written
+    "attn_16x4096x128": {"bytes": 51508480, "kernel_hash": "033b9c19083626e1",
                          "sources": ATTN_KERNEL_SOURCES},
 }
 
