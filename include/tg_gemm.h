@@ -416,6 +416,40 @@ tg_status tg_gemm_force_tiling(int bn, int group_m);
 tg_status tg_gemm_force_stages(int stages);
 
 /*
+ * Split over K of the one-CTA kernel (path 3), for tests and benchmarks.  A
+ * call whose 128 x BN output tiles (all products of a call together) leave
+ * at least half of the SMs idle can share each tile over K among a cluster
+ * of S CTAs: each CTA computes an fp32 partial over its range of k-blocks
+ * (64 fp16 or 128 E4M3 elements each) and the cluster adds the S partials
+ * in distributed shared memory, in rank order, before the epilogue.
+ *   split  0: automatic (tg_gemm_main_plan's choice, with every cluster
+ *          resident at once); 1: never; 2, 4 or 8: always that many CTAs
+ *          per tile (halved while it exceeds the k-blocks), at the default
+ *          or forced tile width.
+ * Process-wide; stays in force until changed.  Returns TG_ERR_INVALID_ARG
+ * (and changes nothing) for any other value.  Results can differ in the
+ * last bits between splits (another order of fp32 additions) and are exact
+ * for inputs whose partial sums are.
+ */
+tg_status tg_gemm_force_split_k(int split);
+
+/*
+ * The one-CTA kernel's automatic choice, computed on the host alone for an
+ * M x N x K call (batch products) of in_dtype (TG_F16 or TG_E4M3) on
+ * num_sms SMs: returns the split S (1: none) and writes the tile width
+ * (64, 128 or 256) to *bn.  The default width, unsplit, competes with every
+ * width whose tiles fill at most half of the SMs, at its largest split (2, 4
+ * or 8 with tiles * S <= num_sms and S <= k-blocks), by a time estimate
+ * measured on GB300: ~86 KB/us of A and B per CTA unsplit, ~95 KB/us split,
+ * plus 1.5, 2.5 or 4.0 us for a split of 64-, 128- or 256-column tiles.  On
+ * a device the library also requires every cluster to be resident at once
+ * (GB300 holds 15 clusters of 8 of these CTAs), which can change the choice.
+ * Returns 0 (and *bn = 0) for non-positive sizes or another dtype.
+ */
+int tg_gemm_main_plan(int64_t M, int64_t N, int64_t K, int64_t batch, tg_dtype in_dtype,
+                      int num_sms, int* bn);
+
+/*
  * Last-wave override of the CTA-pair kernel (path 6), for tests and
  * benchmarks.  The pair kernel hands its 256 x 256 tiles to the CTA pairs
  * in waves; when the last wave is at most half full, it cuts each of that

@@ -8,6 +8,7 @@ addresses (nothing is ever dereferenced or launched).
 import os
 import re
 
+import numpy as np
 import pytest
 
 import tiled_gemm_tg_gb300 as tg
@@ -496,6 +497,56 @@ def test_boundary_split_rule(tiles, kblocks, sms, want):
     if got > 1:
         assert tiles * got <= sms and got <= kblocks
         assert got == 8 or tiles * 2 * got > sms or 2 * got > kblocks
+
+
+@pytest.mark.parametrize("M,N,K,batch,want", [
+    # measured best on GB300 (tile width / split): the estimate picks them
+    ((128, 256, 512, 1, (64, 8))),
+    ((256, 256, 8192, 1, (64, 8))),
+    # 16 clusters of 8: more than GB300 holds at once, so on the device
+    # the library falls back to 64 / 4, the measured best
+    ((512, 512, 8192, 1, (128, 8))),
+    ((1024, 1024, 4096, 1, (256, 4))),
+    ((304, 520, 1024, 1, (64, 4))),
+    ((512, 1024, 2048, 1, (128, 4))),
+    ((256, 4096, 4096, 1, (256, 4))),
+    # no split: the tiles fill the GPU, or K is too short to pay for it
+    ((1024, 2048, 512, 1, (128, 1))),
+    ((1024, 1024, 1024, 1, (64, 1))),
+    ((2048, 1024, 512, 1, (128, 1))),
+    ((8192, 8192, 8192, 1, (256, 1))),
+    ((256, 256, 256, 256, (256, 1))),
+])
+def test_main_plan(M, N, K, batch, want):
+    """The one-CTA kernel's tile width and split over K, on the host."""
+    assert tg.tg_gemm_main_plan(M, N, K, batch, tg.F16, 152) == want
+
+
+def test_main_plan_rules():
+    """Whatever the estimate picks, a split keeps every CTA on its own SM,
+    at least one k-block each, and only for tiles that leave half the SMs
+    idle; E4M3 never gets 64-column tiles; bad arguments give (0, 0)."""
+    rng = np.random.default_rng(5)
+    for _ in range(400):
+        M, N = (int(v) for v in rng.integers(65, 4097, 2))
+        K = int(rng.integers(1, 20000))
+        batch = int(rng.integers(1, 4))
+        for dt, bk in ((tg.F16, 64), (tg.E4M3, 128)):
+            bn, split = tg.tg_gemm_main_plan(M, N, K, batch, dt, 152)
+            assert bn in ((128, 256) if dt == tg.E4M3 else (64, 128, 256))
+            assert split in (1, 2, 4, 8)
+            if split > 1:
+                tiles = -(-M // 128) * -(-N // bn) * batch
+                assert 2 * tiles <= 152 and tiles * split <= 152 and split <= -(-K // bk)
+    assert tg.tg_gemm_main_plan(0, 8, 8, 1, tg.F16, 152) == (0, 0)
+    assert tg.tg_gemm_main_plan(8, 8, 8, 1, tg.F32, 152) == (0, 0)
+
+
+def test_force_split_k_arguments():
+    for bad in (-1, 3, 5, 6, 16):
+        assert tg.tg_gemm_force_split_k(bad) == tg.TG_ERR_INVALID_ARG
+    for ok in (1, 2, 4, 8, 0):
+        assert tg.tg_gemm_force_split_k(ok) == tg.TG_OK
 
 
 def test_force_split_tail_arguments():

@@ -160,3 +160,22 @@ def test_e4m3_batched_and_epilogue():
     C0, _ = oracle.gemm(u8(a[0]), u8(b))
     ref = oracle.epilogue(C0, 2.0, 0.0, None, bias.numpy(), tg.ACT_RELU)
     assert np.array_equal(f16_bits_of(D.double().cpu().numpy()), f16_bits_of(ref))
+
+
+@pytest.mark.parametrize("split", [0, 1, 2, 8])
+@pytest.mark.parametrize("out", [torch.float16, torch.float32])
+def test_e4m3_split_k_bitwise(split, out):
+    """E4M3 through the one-CTA kernel with its tiles shared over K by a
+    cluster (0: the automatic choice, which splits this few-tile, deep-K
+    shape): integer-valued operands, exact whatever the split."""
+    M, N, K = 200, 272, 8192
+    a = int_e4m3((M, K), 12900)
+    b = int_e4m3((K, N), 12901)
+    assert tg.tg_gemm_force_split_k(split) == tg.TG_OK
+    try:
+        got, intact, p = run_e4m3(a, b, out, ldc=N + 8)
+    finally:
+        tg.tg_gemm_force_split_k(0)
+    assert p == MAIN and intact
+    C, _ = oracle.gemm(u8(a), u8(b))
+    _exact(got, C, out)

@@ -344,6 +344,60 @@ def test_boundary_split_k_integer_bitwise(M, N, K):
     assert np.array_equal(have, f16_bits_of(C_ref))
 
 
+# (M, N, K) served by the one-CTA kernel with few tiles: on 152 SMs the
+# rule gives clusters of 8, 4 and 2 CTAs per tile over K.
+MAIN_SPLIT_SHAPES = [(128, 256, 512), (300, 520, 1024), (200, 100, 4096), (129, 1000, 2000),
+                     (513, 1024, 768), (250, 70, 130)]
+
+
+@pytest.mark.parametrize("M,N,K", MAIN_SPLIT_SHAPES)
+@pytest.mark.parametrize("out", [torch.float16, torch.float32])
+@pytest.mark.parametrize("pad_c", [False, True])
+def test_main_split_k(M, N, K, out, pad_c):
+    """The one-CTA kernel with its tiles shared over K by a cluster: every
+    element against the oracle, canaries intact, with vector stores (C rows
+    16-byte aligned) and without."""
+    a = inputs.draw((M, K), "normal", 7250 + M, "f16")
+    b = inputs.draw((K, N), "normal", 7260 + N, "f16")
+    pad = lambda x: (x + 7) // 8 * 8  # noqa: E731
+    ldc = N + 3 if pad_c else pad(N)
+    _, _, p = check_full(a, b, out, lda=pad(K), ldb=pad(N), ldc=ldc)
+    assert p == MAIN
+
+
+@pytest.mark.parametrize("split", [1, 2, 4, 8])
+def test_main_split_k_forced_integer_bitwise(split):
+    """Every split size gives the exact product on integer inputs (each
+    partial sum is exact in fp32), ragged in M, N and K."""
+    M, N, K = 300, 264, 1000
+    a = inputs.draw((M, K), "int2", 7270, "f16")
+    b = inputs.draw((K, N), "int2", 7271, "f16")
+    assert tg.tg_gemm_force_split_k(split) == tg.TG_OK
+    try:
+        got, intact, p = run(a, b, torch.float16, lda=1000, ldb=264, ldc=264)
+    finally:
+        tg.tg_gemm_force_split_k(0)
+    assert p == MAIN and intact
+    C_ref, _ = oracle.gemm(a.numpy(), b.numpy())
+    have = torch.from_numpy(got).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(have, f16_bits_of(C_ref))
+
+
+@pytest.mark.parametrize("split", [1, 2, 4, 8])
+def test_main_split_k_forced_random(split):
+    """Forced splits on random inputs, more clusters than fit at once (a
+    forced split ignores the residency rule), against the oracle."""
+    M, N, K = 1100, 700, 1500
+    a = inputs.draw((M, K), "normal", 7280, "f16")
+    b = inputs.draw((K, N), "normal", 7281, "f16")
+    assert tg.tg_gemm_force_split_k(split) == tg.TG_OK
+    try:
+        _, _, p = check_full(a, b, torch.float16, lda=1504, ldb=704, ldc=700)
+    finally:
+        tg.tg_gemm_force_split_k(0)
+    assert p == MAIN
+
+
 def test_fp32_integer_inputs_exact():
     a = inputs.draw((77, 130), "int2", 7101, "f32")
     b = inputs.draw((130, 45), "int2", 7102, "f32")

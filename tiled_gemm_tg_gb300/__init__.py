@@ -20,7 +20,7 @@ __all__ = [
     "TG_ERR_TIMEOUT", "PATHS", "TgError", "lib", "library_path", "tg_gemm", "tg_gemm_check",
     "tg_status_string", "tg_gemm_path", "tg_gemm_force_path", "tg_gemm_force_tiling",
     "tg_gemm_force_split_tail", "tg_gemm_pair_split_tail", "tg_gemm_force_stages",
-    "tg_gemm_boundary_split",
+    "tg_gemm_boundary_split", "tg_gemm_force_split_k", "tg_gemm_main_plan",
     "tg_gemm_test_hook", "tg_gemm_ex", "tg_gemm_batched", "tg_gemm_batched_path",
     "tg_attention", "tg_attention_ws", "tg_attention_workspace_size", "tg_attention_noalloc",
     "tg_attention_kernel", "tg_attention_force_kernel", "tg_attention_tail_plan",
@@ -116,6 +116,10 @@ def lib() -> ctypes.CDLL:
         L.tg_gemm_force_split_tail.argtypes = [i32]
         L.tg_gemm_pair_split_tail.restype = i32
         L.tg_gemm_pair_split_tail.argtypes = [i64, i32]
+        L.tg_gemm_force_split_k.restype = i32
+        L.tg_gemm_force_split_k.argtypes = [i32]
+        L.tg_gemm_main_plan.restype = i32
+        L.tg_gemm_main_plan.argtypes = [i64, i64, i64, i64, i32, i32, ctypes.POINTER(i32)]
         L.tg_gemm_boundary_split.restype = i32
         L.tg_gemm_boundary_split.argtypes = [i64, i32, i32]
         L.tg_gemm_force_stages.restype = i32
@@ -230,6 +234,18 @@ def tg_gemm_force_stages(stages: int) -> int:
 
 def tg_gemm_pair_split_tail(tiles: int, max_pairs: int) -> int:
     return int(lib().tg_gemm_pair_split_tail(int(tiles), int(max_pairs)))
+
+
+def tg_gemm_force_split_k(split: int) -> int:
+    return int(lib().tg_gemm_force_split_k(int(split)))
+
+
+def tg_gemm_main_plan(M: int, N: int, K: int, batch: int, in_dtype: int, num_sms: int):
+    """(tile width, split over K) the one-CTA kernel would choose, host only."""
+    bn = ctypes.c_int(0)
+    split = int(lib().tg_gemm_main_plan(int(M), int(N), int(K), int(batch), int(in_dtype),
+                                        int(num_sms), ctypes.byref(bn)))
+    return bn.value, split
 
 
 def tg_gemm_boundary_split(tiles: int, kblocks: int, num_sms: int) -> int:

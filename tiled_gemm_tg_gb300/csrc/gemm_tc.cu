@@ -35,6 +35,14 @@
 //     vector stores, predicated at the edges.  After its last TMEM read each
 //     epilogue warp arrives on a named barrier on which warp 1 waits to free
 //     TMEM, so the release overlaps the last stores.  The epilogue of tile i overlaps the main loop of tile i+1.
+// A problem with few output tiles (at most half the SMs) is also split over
+// K: a cluster of S CTAs (2, 4 or 8) shares each tile, CTA r taking k-blocks
+// [r*nkb/S, (r+1)*nkb/S).  The epilogue warps then copy the accumulator into
+// the CTA's own shared memory (fp32, rows padded by four floats so the
+// copies from TMEM lanes do not collide on banks), the cluster
+// synchronises, and all 320 threads of CTA r add up rows [r*128/S,
+// (r+1)*128/S) of the S partials through distributed shared memory, in rank
+// order, apply the fused epilogue and store them.
 // Out-of-range rows, columns and k are zero-filled by TMA, so any M, N, K
 // works as long as the operands are TMA-addressable (16-byte aligned bases,
 // row strides a multiple of 16 bytes); the host routes everything else to
@@ -88,6 +96,24 @@ constexpr uint32_t kStageCBytes = kEpilogueWarps * kStageC;
 constexpr int kTmemFreeBar = 1;
 constexpr int kTmemFreeThreads = 32 * (kEpilogueWarps + 1);
 
+// fp32 partial tile of a split over K: BM rows of BN + 4 floats.
+template <int BN>
+struct RedCfg {
+    static constexpr int LD = BN + 4;
+    static constexpr uint32_t BYTES = BM * LD * 4;
+};
+constexpr int kMaxSplitK = 8;
+
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t cluster_addr)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
+}
+
 template <int BN>
 struct MainCfg {
     static constexpr uint32_t B_STAGE = BN * 128;
@@ -111,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, void* C, long long ldc, int M,
                     int N, int K, int tiles_m, int tiles_n, int group_m, int stages, int c_vec,
-                    int c_tma, int hook, unsigned int* err, Epilogue epi, BatchArgs bt)
+                    int c_tma, int split, int hook, unsigned int* err, Epilogue epi, BatchArgs bt)
 {
     using Cfg = MainCfg<BN>;
     constexpr int STAGES = Cfg::STAGES;  // the most stages; `stages` are in use
@@ -146,8 +172,16 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     constexpr int NB = KBlock<ES>::NB;
     constexpr uint32_t B_BOX = KBlock<ES>::B_BOX;
     static_assert(BN % NB == 0, "B tile must be whole 128-byte boxes");
-    const int num_kb = (K + BK - 1) / BK;
+    // a split over K: this CTA is rank r of a cluster of `split` sharing one
+    // tile, and takes k-blocks kb_lo .. kb_lo + num_kb - 1 of it
+    const int rank = split > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    const int nkb_all = (K + BK - 1) / BK;
+    const int kb_lo = static_cast<int>(static_cast<long long>(rank) * nkb_all / split);
+    const int num_kb = static_cast<int>(static_cast<long long>(rank + 1) * nkb_all / split) - kb_lo;
     const int total = tiles_m * tiles_n * bt.count;
+    // the tiles this CTA walks: t_first, t_first + t_step, ... (one tile when split)
+    const int t_first = static_cast<int>(blockIdx.x) / split;
+    const int t_step = split > 1 ? total : static_cast<int>(gridDim.x);
     // the producer's first tile, found before the wait for the previous
     // kernel (the integer divisions of the tile order are on the critical
     // path of a one-tile CTA otherwise)
@@ -156,15 +190,14 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
         // the first tile's first stages into L2 while the previous kernel finishes
-        if (static_cast<int>(blockIdx.x) < total) {
-            batch_tile_coords(static_cast<int>(blockIdx.x), tiles_m, tiles_n, group_m, b0, tm0, tn0);
+        if (t_first < total) {
+            batch_tile_coords(t_first, tiles_m, tiles_n, group_m, b0, tm0, tn0);
             const int b = b0, tm = tm0, tn = tn0;
-            const int pf = total > static_cast<int>(gridDim.x) ? stages
-                                                                : min(stages, kPrefetchStagesSingle);
+            const int pf = total > t_step ? stages : min(stages, kPrefetchStagesSingle);
             for (int kb = 0; kb < num_kb && kb < pf; ++kb) {
-                tma_prefetch_l2_3d(&tmA, kb * BK, tm * BM, b * bt.za);
+                tma_prefetch_l2_3d(&tmA, (kb_lo + kb) * BK, tm * BM, b * bt.za);
                 for (int j = 0; j < BN / NB; ++j)
-                    tma_prefetch_l2_3d(&tmB, tn * BN + j * NB, kb * BK, b * bt.zb);
+                    tma_prefetch_l2_3d(&tmB, tn * BN + j * NB, (kb_lo + kb) * BK, b * bt.zb);
             }
         }
     }
@@ -188,9 +221,9 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             int s = 0;
             uint32_t ph = 0;
             uint32_t issued = 0;
-            for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            for (int t = t_first; t < total; t += t_step) {
                 int b = b0, tm = tm0, tn = tn0;
-                if (t != static_cast<int>(blockIdx.x))
+                if (t != t_first)
                     batch_tile_coords(t, tiles_m, tiles_n, group_m, b, tm, tn);
                 const int za = b * bt.za, zb = b * bt.zb;
                 bool ok = true;
@@ -201,7 +234,7 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         ok = false;
                         break;
                     }
-                    if (hook == 1 && t == static_cast<int>(blockIdx.x) && kb == 0) {
+                    if (hook == 1 && t == t_first && kb == 0) {
                         // test hook: leave this stage unfilled, so the MMA
                         // thread's bounded wait on it runs out
                         if (++s == stages) {
@@ -213,11 +246,11 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const uint32_t fb = smem_u32(&full_bar[s]);
                     const uint32_t sa = base + s * Cfg::STAGE;
                     mbar_arrive_expect_tx(fb, Cfg::STAGE);
-                    tma_load_3d(sa, &tmA, fb, kb * BK, tm * BM, za);
+                    tma_load_3d(sa, &tmA, fb, (kb_lo + kb) * BK, tm * BM, za);
 #pragma unroll
                     for (int j = 0; j < BN / NB; ++j)
-                        tma_load_3d(sa + A_STAGE + j * B_BOX, &tmB, fb, tn * BN + j * NB, kb * BK,
-                                    zb);
+                        tma_load_3d(sa + A_STAGE + j * B_BOX, &tmB, fb, tn * BN + j * NB,
+                                    (kb_lo + kb) * BK, zb);
                     ++issued;
                     if (++s == stages) {
                         s = 0;
@@ -249,7 +282,7 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             int acc = 0;
             uint32_t aph = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            for (int t = t_first; t < total && ok; t += t_step) {
                 if (!mbar_wait(smem_u32(&tempty_bar[acc]), aph ^ 1u, &abort_flag)) {
                     ok = false;
                     break;
@@ -302,7 +335,39 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         uint32_t chunk = 0;  // staged chunks so far (fp16 alternates two 2 KB halves)
         int acc = 0;
         uint32_t aph = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        if (split > 1) {
+            // the accumulator (this CTA's k-range of its one tile) -> the fp32
+            // partial in shared memory, row q*32 + lane at red[row * LD]; the
+            // stages are free once every MMA is complete
+            const bool got = mbar_wait(smem_u32(&tfull_bar[0]), 0, &abort_flag, epi_limit);
+            if (__all_sync(0xffffffffu, got)) {
+                tc_fence_after();
+                float* const red = reinterpret_cast<float*>(smem_raw + (base - smem_u32(smem_raw)));
+                const int ml = q * 32 + lane;
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+                for (int c = c_lo; c < c_lo + span; c += 32) {
+                    uint32_t r[32];
+                    if (num_kb > 0) {
+                        tmem_ld_32x32b_x32(taddr + c, r);
+                        tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) r[j] = 0u;
+                    }
+                    float4* row = reinterpret_cast<float4*>(red + ml * RedCfg<BN>::LD + c);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        row[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                             __uint_as_float(r[4 * j + 2]),
+                                             __uint_as_float(r[4 * j + 3]));
+                }
+            } else if (lane == 0) {
+                abort_flag = 1;
+                atomicOr(err, ERR_MAIN_EPILOGUE);
+            }
+        }
+        for (int t = t_first; t < total && split == 1; t += t_step) {
             int b, tm, tn;
             batch_tile_coords(t, tiles_m, tiles_n, group_m, b, tm, tn);
             void* Cb = batch_ptr(C, b, bt.sC, OUT_F32 ? 4 : 2);
@@ -360,6 +425,95 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         __syncwarp();
     }
 
+    if (split > 1) {
+        if (warp == 1) {
+            named_bar_sync(kTmemFreeBar, kTmemFreeThreads);
+            tc_fence_after();
+            tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+        }
+        // every partial of the cluster is in shared memory after this barrier
+        cluster_sync();
+        if (t_first < total) {
+            int b, tm, tn;
+            batch_tile_coords(t_first, tiles_m, tiles_n, group_m, b, tm, tn);
+            void* Cb = batch_ptr(C, b, bt.sC, OUT_F32 ? 4 : 2);
+            // rows rank*rows .. of the tile, four columns per item, every
+            // thread of the CTA; the partials are added in rank order.  A
+            // thread issues the remote loads of kUnroll items before it adds
+            // any, so that several round trips overlap.
+            const int rows = BM / split;
+            constexpr int quads = BN / 4;
+            constexpr int kUnroll = 4;
+            const int items = rows * quads;
+            for (int i0 = threadIdx.x; i0 < items; i0 += kThreads * kUnroll) {
+                float4 part[kUnroll][kMaxSplitK];
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int idx = i0 + u * kThreads;
+                    if (idx >= items) break;
+                    const int ml = rank * rows + idx / quads;
+                    const int nl = 4 * (idx % quads);
+                    const uint32_t off = static_cast<uint32_t>((ml * RedCfg<BN>::LD + nl) * 4);
+#pragma unroll
+                    for (int r = 0; r < kMaxSplitK; ++r)
+                        if (r < split)
+                            part[u][r] = ld_cluster_f32x4(mapa_shared(base + off, static_cast<uint32_t>(r)));
+                }
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int idx = i0 + u * kThreads;
+                    if (idx >= items) break;
+                    const int ml = rank * rows + idx / quads;
+                    const int nl = 4 * (idx % quads);
+                    const int m = tm * BM + ml, n = tn * BN + nl;
+                    if (m >= M || n >= N) continue;
+                    float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                    for (int r = 0; r < kMaxSplitK; ++r) {
+                        if (r < split) {
+                            v[0] += part[u][r].x;
+                            v[1] += part[u][r].y;
+                            v[2] += part[u][r].z;
+                            v[3] += part[u][r].w;
+                        }
+                    }
+                    const bool full = n + 4 <= N;
+                    if (epi.on) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (n + j < N) v[j] = epilogue_elem<OUT_F32>(v[j], m, n + j, epi);
+                    }
+                    if constexpr (OUT_F32) {
+                        float* row = static_cast<float*>(Cb) + static_cast<long long>(m) * ldc + n;
+                        if (c_vec && full) {
+                            *reinterpret_cast<float4*>(row) = make_float4(v[0], v[1], v[2], v[3]);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                if (n + j < N) row[j] = v[j];
+                        }
+                    } else {
+                        __half* row = static_cast<__half*>(Cb) + static_cast<long long>(m) * ldc + n;
+                        if (c_vec && full) {
+                            const __half2 lo = __floats2half2_rn(v[0], v[1]);
+                            const __half2 hi = __floats2half2_rn(v[2], v[3]);
+                            *reinterpret_cast<uint2*>(row) =
+                                make_uint2(*reinterpret_cast<const uint32_t*>(&lo),
+                                           *reinterpret_cast<const uint32_t*>(&hi));
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                if (n + j < N) row[j] = __float2half_rn(v[j]);
+                        }
+                    }
+                }
+            }
+        }
+        pdl_trigger();  // this CTA has issued all its global writes
+        // no CTA may leave while a peer can still read its partial
+        cluster_sync();
+        return;
+    }
     pdl_trigger();  // this CTA has issued all its global writes
     if (warp == 1) {
         // after the MMA thread's own MMAs (drained above) and every epilogue
@@ -372,6 +526,150 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 
 std::mutex g_attr_mu;
 bool g_attr_set[64][12];
+// Clusters of 2, 4 and 8 CTAs that fit at once, per device and kernel
+// instance (with the default ring's shared memory).
+int g_max_clusters[64][12][3];
+
+// Clusters of S CTAs per tile for `tiles` tiles of nkb k-blocks: none when
+// the tiles fill more than half of the SMs; else the largest S of 2, 4, 8
+// with tiles * S <= num_sms, S <= nkb and (given max_clusters) all the
+// clusters resident at once.
+int main_split_k(long long tiles, long long nkb, int num_sms, const int* max_clusters)
+{
+    if (tiles * 2 > num_sms) return 1;
+    int s = 1;
+    for (int i = 0; i < 3; ++i) {
+        const int t = 2 << i;
+        if (tiles * t > num_sms || nkb < t || (max_clusters != nullptr && tiles > max_clusters[i]))
+            break;
+        s = t;
+    }
+    return s;
+}
+
+// The kernel instance's launch attributes, set once per device, and its
+// cluster residency: max_clusters[i] clusters of 2 << i CTAs fit at once.
+template <int BN, bool OUT_F32, int ES>
+cudaError_t init_instance(const int** max_clusters)
+{
+    using Cfg = MainCfg<BN>;
+    auto kernel = gemm_tc_main_kernel<BN, OUT_F32, ES>;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    const int slot =
+        ((BN == 256 ? 0 : BN == 128 ? 1 : 2) * 2 + (OUT_F32 ? 1 : 0)) * 2 + (ES == 1 ? 1 : 0);
+    std::lock_guard<std::mutex> lock(g_attr_mu);
+    if (!g_attr_set[dev][slot]) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(Cfg::SMEM + kStageCBytes));
+        if (e != cudaSuccess) return e;
+        for (int i = 0; i < 3; ++i) {
+            cudaLaunchConfig_t q = {};
+            q.gridDim = dim3(2 << i);
+            q.blockDim = dim3(kThreads);
+            q.dynamicSmemBytes = Cfg::SMEM;
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = 2 << i;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            q.attrs = at;
+            q.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, kernel, &q) != cudaSuccess) {
+                cudaGetLastError();
+                n = 0;
+            }
+            g_max_clusters[dev][slot][i] = n;
+        }
+        g_attr_set[dev][slot] = true;
+    }
+    *max_clusters = g_max_clusters[dev][slot];
+    return cudaSuccess;
+}
+
+template <bool OUT_F32, int ES>
+cudaError_t instance_clusters(int bn, const int** mc)
+{
+    if (bn == 256) return init_instance<256, OUT_F32, ES>(mc);
+    if constexpr (ES == 1) {
+        return init_instance<128, OUT_F32, ES>(mc);  // E4M3 tiles are 128 or 256 wide
+    } else {
+        if (bn == 128) return init_instance<128, OUT_F32, ES>(mc);
+        return init_instance<64, OUT_F32, ES>(mc);
+    }
+}
+
+cudaError_t clusters_of(const GemmArgs& a, int bn, const int** mc)
+{
+    if (a.in_es == 1)
+        return a.out_f32 ? instance_clusters<true, 1>(bn, mc) : instance_clusters<false, 1>(bn, mc);
+    return a.out_f32 ? instance_clusters<true, 2>(bn, mc) : instance_clusters<false, 2>(bn, mc);
+}
+
+// Estimated microseconds of a call with tile width bn split s ways over K,
+// from a sweep of every tile width and split on GB300 (CUDA-graph replay,
+// operands past L2): each CTA takes in A and B at ~86 KB/us on its own and
+// ~95 KB/us in a split, times the waves when the CTAs outnumber the SMs; a
+// split adds ~1.5, 2.5 or 4.0 us for 64, 128 or 256 columns (the partial
+// tile through distributed shared memory and the two cluster barriers).
+double main_cost_us(long long M, long long N, long long K, long long batch, int es, int num_sms,
+                    int bn, int s)
+{
+    const int bk = 128 / es;
+    const long long tiles = ((M + BM - 1) / BM) * ((N + bn - 1) / bn) * batch;
+    const long long waves = (tiles * s + num_sms - 1) / num_sms;
+    const long long nkb = (K + bk - 1) / bk;
+    const long long kper = (nkb + s - 1) / s * bk;
+    const long long rows = M < BM ? M : BM;
+    const long long n64 = (N + 63) / 64 * 64;
+    const long long cols = n64 < bn ? n64 : bn;
+    const double kbytes = static_cast<double>((rows + cols) * kper * es) / 1024.0;
+    if (s == 1) return static_cast<double>(waves) * kbytes / 86.0;
+    const double extra = bn == 64 ? 1.5 : bn == 128 ? 2.5 : 4.0;
+    return static_cast<double>(waves) * kbytes / 95.0 + extra;
+}
+
+// The tile width and split for a call (max_clusters(bn) gives the residency
+// of each instance, or null for the rule alone).  A forced split is used as
+// given (halved while it exceeds the k-blocks); otherwise the default tile
+// width, unsplit, competes with every tile width at its largest split by
+// estimated time.
+template <typename MC>
+void plan(long long M, long long N, long long K, long long batch, int es, int num_sms,
+          int forced_bn, int forced_split, MC max_clusters, int* bn_out, int* split_out)
+{
+    const int bk = 128 / es;
+    const long long nkb = (K + bk - 1) / bk;
+    int bn = forced_bn != 0 ? forced_bn
+                            : main_tile_n(static_cast<int>(M), static_cast<int>(N),
+                                          static_cast<int>(batch), num_sms);
+    if (es == 1 && bn == 64) bn = 128;  // E4M3 B boxes are 128 elements wide
+    int split = 1;
+    if (forced_split > 0) {
+        split = forced_split;
+        while (split > 1 && split > nkb) split >>= 1;
+    } else {
+        double best = main_cost_us(M, N, K, batch, es, num_sms, bn, 1);
+        const int widths[3] = {64, 128, 256};
+        for (int w : widths) {
+            if ((forced_bn != 0 && w != forced_bn) || (es == 1 && w == 64)) continue;
+            const long long tiles = ((M + BM - 1) / BM) * ((N + w - 1) / w) * batch;
+            const int sw = main_split_k(tiles, nkb, num_sms, max_clusters(w));
+            if (sw <= 1) continue;
+            const double c = main_cost_us(M, N, K, batch, es, num_sms, w, sw);
+            if (c < best) {
+                best = c;
+                bn = w;
+                split = sw;
+            }
+        }
+    }
+    *bn_out = bn;
+    *split_out = split;
+}
 
 template <int BN, bool OUT_F32, int ES>
 cudaError_t launch_cfg(const GemmArgs& a)
@@ -379,21 +677,12 @@ cudaError_t launch_cfg(const GemmArgs& a)
     using Cfg = MainCfg<BN>;
     using KB = KBlock<ES>;
     auto kernel = gemm_tc_main_kernel<BN, OUT_F32, ES>;
+    const int* mc = nullptr;
     {
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
+        const cudaError_t e = init_instance<BN, OUT_F32, ES>(&mc);
         if (e != cudaSuccess) return e;
-        const int slot =
-            ((BN == 256 ? 0 : BN == 128 ? 1 : 2) * 2 + (OUT_F32 ? 1 : 0)) * 2 + (ES == 1 ? 1 : 0);
-        std::lock_guard<std::mutex> lock(g_attr_mu);
-        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-        if (!g_attr_set[dev][slot]) {
-            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(Cfg::SMEM + kStageCBytes));
-            if (e != cudaSuccess) return e;
-            g_attr_set[dev][slot] = true;
-        }
     }
+    const int split = a.split_k > 1 ? a.split_k : 1;
     CUtensorMap ta, tb;
     if (!encode_tmap(&ta, a.A, ES, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M),
                      static_cast<uint64_t>(a.lda), a.batch, a.sA, KB::BK, BM))
@@ -417,27 +706,53 @@ cudaError_t launch_cfg(const GemmArgs& a)
     // stride), and the ABI leaves columns N..ldc-1 untouched
     CUtensorMap tc;
     std::memset(&tc, 0, sizeof(tc));
-    const int c_tma = c_vec && (static_cast<size_t>(a.N) * es) % 16 == 0 &&
+    // (a split over K stores from its reduction, without TMA)
+    const int c_tma = split == 1 && c_vec && (static_cast<size_t>(a.N) * es) % 16 == 0 &&
                       encode_tmap_store(&tc, a.C, static_cast<int>(es),
                                         static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.M),
                                         static_cast<uint64_t>(a.ldc), a.batch, a.sC, 32, 32);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
+    cfg.gridDim = dim3(split > 1 ? total * split : grid);
     cfg.blockDim = dim3(kThreads);
     const int stages = a.stages > 0 ? a.stages : Cfg::STAGES;
     if (stages < 2 || stages > Cfg::STAGES) return cudaErrorInvalidValue;
-    cfg.dynamicSmemBytes = Cfg::smem(stages, c_tma != 0);
+    uint32_t smem = Cfg::smem(stages, c_tma != 0);
+    if (split > 1 && smem < RedCfg<BN>::BYTES + 1024) smem = RedCfg<BN>::BYTES + 1024;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = a.stream;
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     set_pdl_attr(at[0]);
+    at[1].id = cudaLaunchAttributeClusterDimension;
+    at[1].val.clusterDim.x = split;
+    at[1].val.clusterDim.y = 1;
+    at[1].val.clusterDim.z = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = split > 1 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kernel, ta, tb, tc, a.C, a.ldc, a.M, a.N, a.K, tiles_m,
-                              tiles_n, group_m, stages, c_vec, c_tma, a.hook, a.err, a.epi,
+                              tiles_n, group_m, stages, c_vec, c_tma, split, a.hook, a.err, a.epi,
                               a.batch_args());
 }
 
 }  // namespace
+
+cudaError_t main_plan(const GemmArgs& a, int forced_bn, int forced_split, int* bn, int* split)
+{
+    cudaError_t err = cudaSuccess;
+    auto mc = [&](int w) -> const int* {
+        const int* p = nullptr;
+        const cudaError_t e = clusters_of(a, w, &p);
+        if (e != cudaSuccess) err = e;
+        return p;
+    };
+    plan(a.M, a.N, a.K, a.batch, a.in_es, a.num_sms, forced_bn, forced_split, mc, bn, split);
+    return err;
+}
+
+void main_plan_host(long long M, long long N, long long K, long long batch, int es, int num_sms,
+                    int* bn, int* split)
+{
+    plan(M, N, K, batch, es, num_sms, 0, 0, [](int) -> const int* { return nullptr; }, bn, split);
+}
 
 int main_max_stages(int bn)
 {

@@ -41,6 +41,7 @@ DeviceState g_dev[kMaxDevices];
 std::atomic<int> g_force_path{0};
 std::atomic<int> g_test_hook{0};
 std::atomic<int> g_force_bn{0};
+std::atomic<int> g_force_split_k{0};
 std::atomic<int> g_force_group{0};
 std::atomic<int> g_force_attn{0};
 std::atomic<int> g_force_split_tail{-1};
@@ -303,8 +304,12 @@ tg_status run(int path, const Problem& p, const tg::Epilogue& epi, tg_stream_t s
         case tg::PATH_SIMT: e = tg::launch_simt_f32(a); break;
         case tg::PATH_MAIN: {
             const int forced_bn = g_force_bn.load(std::memory_order_relaxed);
-            const int bn = forced_bn != 0 ? forced_bn : tg::main_tile_n(a.M, a.N, a.batch, a.num_sms);
+            int bn = 0, split = 1;
+            e = tg::main_plan(a, forced_bn, g_force_split_k.load(std::memory_order_relaxed), &bn,
+                              &split);
+            if (e != cudaSuccess) break;
             if (a.stages != 0 && a.stages > tg::main_max_stages(bn)) return TG_ERR_UNSUPPORTED;
+            a.split_k = split;
             e = tg::launch_main(a, bn);
             break;
         }
@@ -810,6 +815,29 @@ tg_status tg_gemm_force_stages(int stages)
     if (stages != 0 && (stages < 2 || stages > 8)) return TG_ERR_INVALID_ARG;
     g_force_stages.store(stages, std::memory_order_relaxed);
     return TG_OK;
+}
+
+tg_status tg_gemm_force_split_k(int split)
+{
+    if (split != 0 && split != 1 && split != 2 && split != 4 && split != 8)
+        return TG_ERR_INVALID_ARG;
+    g_force_split_k.store(split, std::memory_order_relaxed);
+    return TG_OK;
+}
+
+int tg_gemm_main_plan(int64_t M, int64_t N, int64_t K, int64_t batch, tg_dtype in_dtype,
+                      int num_sms, int* bn)
+{
+    if (M <= 0 || N <= 0 || K <= 0 || batch <= 0 || num_sms <= 0 || M > INT32_MAX ||
+        N > INT32_MAX || K > INT32_MAX || batch > INT32_MAX ||
+        (in_dtype != TG_F16 && in_dtype != TG_E4M3)) {
+        if (bn != nullptr) *bn = 0;
+        return 0;
+    }
+    int w = 0, split = 1;
+    tg::main_plan_host(M, N, K, batch, in_dtype == TG_E4M3 ? 1 : 2, num_sms, &w, &split);
+    if (bn != nullptr) *bn = w;
+    return split;
 }
 
 tg_status tg_gemm_force_split_tail(int tiles)

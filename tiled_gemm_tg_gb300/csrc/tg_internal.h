@@ -91,6 +91,7 @@ struct GemmArgs {
     int group_m;        // grouped tile-order height, 0 = the kernel's default
     int split_tail = -1;  // pair kernel: tiles of the last wave cut in two, -1 = automatic
     int stages = 0;       // TMA kernels: pipeline stages in the ring, 0 = the kernel's most
+    int split_k = 1;      // one-CTA kernel: CTAs sharing each tile over K (a cluster)
     int num_sms;
     cudaStream_t stream;
     Epilogue epi;
@@ -194,6 +195,15 @@ int attention_kernel_choice(int batch, int Nq, int Nk, int d, int dv, int num_sm
 
 // Tile width the main kernel uses for this problem (64, 128 or 256).
 int main_tile_n(int M, int N, int batch, int num_sms);
+// Tile width and split over K of the main kernel for the call `a`: a
+// forced tile width (0: automatic) and split (0: automatic), else the
+// default width unsplit or, when the tiles leave half the SMs idle, a wider
+// or equal tile split over a cluster if that is estimated faster (every
+// cluster resident at once).  main_plan_host: the same without the
+// residency check, on the host alone.
+cudaError_t main_plan(const GemmArgs& a, int forced_bn, int forced_split, int* bn, int* split);
+void main_plan_host(long long M, long long N, long long K, long long batch, int es, int num_sms,
+                    int* bn, int* split);
 // The most pipeline stages (the default ring) of the one-CTA kernel with
 // tile width bn, and of the pair kernel.
 int main_max_stages(int bn);
