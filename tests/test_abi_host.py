@@ -173,8 +173,11 @@ def test_path_selection():
     assert path(1024, 2048, 512, o=tg.F32) == 3
     assert path(8192, 8192, 8192) == 6           # 1024 tiles of 256x256: CTA pairs
     assert path(4096, 16384, 4096) == 6
-    assert path(2048, 2048, 1024) == 6           # exactly 64 pair tiles
-    assert path(2048, 1792, 1024) == 3           # 56 pair tiles: one CTA per tile
+    assert path(2048, 2048, 1024) == 3           # 64 pair tiles, K < 4096: one CTA per tile
+    assert path(2048, 2048, 4096) == 6           # 64 pair tiles, K = 4096: CTA pairs
+    assert path(2048, 1792, 4096) == 3           # 56 pair tiles: one CTA per tile
+    assert path(4096, 2048, 2048) == 3           # 128 pair tiles, K < 4096
+    assert path(3072, 3072, 1024) == 6           # 144 pair tiles
     assert path(2048, 2048, 512) == 3            # K < 1024: the one-CTA kernel
     assert path(8192, 8192, 512) == 3
     assert path(4096, 4096, 1024) == 6
@@ -285,8 +288,10 @@ def test_batched_degenerate_sizes_are_noops():
 
 def test_batched_path_selection():
     assert bpath(1, 8192, 8192, 8192) == 6
-    assert bpath(16, 512, 512, 1024) == 6           # 4 pair tiles x 16 = 64
-    assert bpath(15, 512, 512, 1024) == 3           # 60 pair tiles
+    assert bpath(16, 512, 512, 4096) == 6           # 4 pair tiles x 16 = 64, K = 4096
+    assert bpath(16, 512, 512, 1024) == 3           # 64 pair tiles, K < 4096
+    assert bpath(36, 512, 512, 1024) == 6           # 144 pair tiles
+    assert bpath(15, 512, 512, 4096) == 3           # 60 pair tiles
     assert bpath(16, 512, 512, 512) == 3            # K < 1024
     assert bpath(256, 256, 256, 4096) == 3          # products smaller than 512 x 512
     assert bpath(8, 16, 4096, 4096) == 5            # skinny, one cluster row per matrix

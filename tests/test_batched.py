@@ -169,7 +169,8 @@ def test_batched_integer_bitwise(path):
 
 
 @pytest.mark.parametrize("batch,M,N,K,want", [
-    (16, 512, 512, 1024, PAIR),     # 64 pair tiles over the batch
+    (16, 512, 512, 4096, PAIR),     # 64 pair tiles over the batch, K = 4096
+    (16, 512, 512, 1024, MAIN),     # 64 pair tiles with K < 4096
     (6, 300, 200, 128, MAIN),
     (12, 16, 1024, 2048, SKINNY),
     (2, 1, 8, 8, SKINNY),

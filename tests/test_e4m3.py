@@ -107,8 +107,8 @@ def test_e4m3_integer_bitwise(M, N, K, force, bn, out):
     _exact(got, C, out)
 
 
-@pytest.mark.parametrize("M,N,K,want", [(300, 520, 448, MAIN), (2048, 2048, 2048, PAIR),
-                                        (1792, 2816, 1024, PAIR)])
+@pytest.mark.parametrize("M,N,K,want", [(300, 520, 448, MAIN), (2048, 2048, 4096, PAIR),
+                                        (1792, 2816, 4096, PAIR), (2048, 2048, 2048, MAIN)])
 @pytest.mark.parametrize("out", [torch.float16, torch.float32])
 def test_e4m3_random(M, N, K, want, out):
     a = inputs.draw((M, K), "normal", 12200 + M, "e4m3")

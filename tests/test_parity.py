@@ -228,7 +228,7 @@ def test_skinny_chain_reads_the_previous_output():
 
 
 @pytest.mark.parametrize("M,widths,path", [(512, [768, 1024, 512, 640], MAIN),
-                                            (2048, [2048, 2048, 2048], PAIR)])
+                                            (2048, [4096, 2048, 4096], PAIR)])
 def test_chain_reads_the_previous_output(M, widths, path):
     """Back-to-back calls where each call's A is the previous call's C, with
     no host sync in between and again from a CUDA graph: a call whose
@@ -579,7 +579,11 @@ def test_pair_kernel_integer_bitwise_77_tiles(out):
     M, N, K = 1792, 2816, 2048
     a = inputs.draw((M, K), "int2", 8701, "f16")
     b = inputs.draw((K, N), "int2", 8702, "f16")
-    got, intact, p = run(a, b, out)
+    tg.tg_gemm_force_path(PAIR)  # 77 tiles with K < 4096 would take the one-CTA kernel
+    try:
+        got, intact, p = run(a, b, out)
+    finally:
+        tg.tg_gemm_force_path(0)
     assert p == PAIR and intact
     C_ref, _ = oracle.gemm(a.numpy(), b.numpy())
     if out == torch.float16:
@@ -637,7 +641,7 @@ def test_pair_kernel_half_tiles_random():
 
 def test_pair_kernel_repeated_calls_agree():
     """Back-to-back calls on one stream give the same exact result."""
-    M, N, K = 1792, 2816, 1024
+    M, N, K = 1792, 2816, 4096
     a = inputs.draw((M, K), "int2", 8801, "f16")
     b = inputs.draw((K, N), "int2", 8802, "f16")
     C_ref, _ = oracle.gemm(a.numpy(), b.numpy())

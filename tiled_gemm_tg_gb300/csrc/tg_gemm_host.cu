@@ -116,6 +116,13 @@ bool tma_stride_ok(int64_t stride, int64_t rows, int64_t ld, int64_t es)
            static_cast<u128>(stride) >= static_cast<u128>(rows) * static_cast<u128>(ld);
 }
 
+// Whether a problem with `tiles` 256 x 256 tiles and depth K goes to the
+// pair kernel (M, N and K already past their minimums).
+bool pair_worth(int64_t tiles, int64_t K)
+{
+    return tiles >= tg::kPairMinTilesShortK || (tiles >= tg::kPairMinTiles && K >= tg::kPairLongK);
+}
+
 // Validation shared by every entry point.  On TG_OK, *path is the path the
 // arguments call for (ignoring any forced path).
 tg_status classify(const Problem& p, int* path)
@@ -182,9 +189,10 @@ tg_status classify(const Problem& p, int* path)
         *path = tg::PATH_BOUNDARY;
     } else if (M <= tg::kSkinnyMaxM && !e4m3) {
         *path = tg::PATH_SKINNY;
-    } else if (static_cast<int64_t>(tg::pair_tiles(static_cast<int>(M), static_cast<int>(N))) *
-                       p.batch >= tg::kPairMinTiles &&
-               K >= tg::kPairMinK && M >= tg::kPairMinMN && N >= tg::kPairMinMN) {
+    } else if (M >= tg::kPairMinMN && N >= tg::kPairMinMN && K >= tg::kPairMinK &&
+               pair_worth(static_cast<int64_t>(tg::pair_tiles(static_cast<int>(M),
+                                                              static_cast<int>(N))) * p.batch,
+                          K)) {
         *path = tg::PATH_MAIN_PAIR;
     } else {
         *path = tg::PATH_MAIN;

@@ -221,14 +221,19 @@ int pair_tiles(int M, int N);
 int pair_split_tail(int total, int max_pairs, int forced);
 
 // The pair kernel takes over once a problem (all products of a batch
-// together) has at least this many 256 x 256 tiles, enough to occupy most SM
-// pairs in the first wave, and each product is large enough for its 256 x 256
-// tiles and 128-deep k-blocks to pay: K >= 1024 and M, N >= 512.  Measured
-// with the configuration sweep: below these the one-CTA kernel's shorter
-// pipeline fill and finer tiles win (8192 x 8192 x 512: 71.5 against 80.3 us;
-// 256 products of 256^3: 19.7 against 25.9 us), above them the pair kernel
-// does (16 products of 2048^3: 169.8 against 180.2 us).
+// together) has enough 256 x 256 tiles for its longer pipeline fill to pay:
+// at least kPairMinTiles with K >= kPairLongK, or kPairMinTilesShortK with
+// K >= kPairMinK, and M, N >= 512.  Measured with the configuration sweep
+// (CUDA-graph replay): the one-CTA kernel with 128 x 256 tiles wins at 64
+// and 128 pair tiles with K <= 2048 (2048 x 2048 x 1024: 10.9 against 12.8
+// us; 2048^3: 16.7 against 17.5; 4096 x 2048 x 1024: 17.6 against 18.1), the
+// pair kernel at 64 tiles with K = 4096 (2048 x 2048 x 4096: 26.4 against
+// 28.1) and from 144 tiles (3072 x 3072 x 2048: 28.0 against 29.7; 4096 x
+// 4096 x 1024: 27.1 against 31.2); below K = 1024 the one-CTA kernel's
+// shorter fill wins everywhere (8192 x 8192 x 512: 71.5 against 80.3 us).
 constexpr int kPairMinTiles = 64;
+constexpr int kPairMinTilesShortK = 144;
+constexpr int kPairLongK = 4096;
 constexpr int kPairMinK = 1024;
 constexpr int kPairMinMN = 512;
 

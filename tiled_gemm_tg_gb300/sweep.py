@@ -7,11 +7,12 @@ kernel (256 x 256 tiles, k-block 128) with grouped tile orders of 2..32
 tile rows at its default three stages, and with 2 or 3 stages at its
 default group; the one-CTA kernel with 128 x 64 / 128 x 128 / 128 x 256
 tiles (at most 8 / 6 / 4 stages of k-block 64) with group heights 4..32 at
-the most stages, and with every depth from 2 stages up at the default
-group; the skinny kernel when M <= 64.  Each configuration is forced
-through tg_gemm_force_path / tg_gemm_force_tiling / tg_gemm_force_stages,
-launched `reps` times from one CUDA graph over operand sets rotated past
-L2, and timed with CUDA events.
+the most stages, with every depth from 2 stages up at the default group,
+and unsplit or split over K by clusters of 2, 4 or 8 CTAs; the skinny
+kernel when M <= 64.  Each configuration is forced through
+tg_gemm_force_path / tg_gemm_force_tiling / tg_gemm_force_stages /
+tg_gemm_force_split_k, launched `reps` times from one CUDA graph over
+operand sets rotated past L2, and timed with CUDA events.
 
     python -m tiled_gemm_tg_gb300.sweep --shapes 1024x1024x1024,8192x8192x8192
 
@@ -33,18 +34,20 @@ MAX_STAGES = {(PAIR, 0): 3, (MAIN, 64): 8, (MAIN, 128): 6, (MAIN, 256): 4}
 
 
 def candidates(M: int, N: int, K: int):
-    """(path, tile width, group height, stages); 0 = the kernel's default."""
-    out = [(PAIR, 0, g, 0) for g in (2, 4, 8, 16, 32)]
-    out += [(PAIR, 0, 0, st) for st in range(2, MAX_STAGES[(PAIR, 0)])]
+    """(path, tile width, group height, stages, split over K); 0 = the
+    kernel's default (for the split: its own choice; 1 = unsplit)."""
+    out = [(PAIR, 0, g, 0, 0) for g in (2, 4, 8, 16, 32)]
+    out += [(PAIR, 0, 0, st, 0) for st in range(2, MAX_STAGES[(PAIR, 0)])]
     for bn in (64, 128, 256):
-        out += [(MAIN, bn, g, 0) for g in (4, 8, 16, 32)]
-        out += [(MAIN, bn, 0, st) for st in range(2, MAX_STAGES[(MAIN, bn)])]
+        out += [(MAIN, bn, g, 0, 1) for g in (4, 8, 16, 32)]
+        out += [(MAIN, bn, 0, st, 1) for st in range(2, MAX_STAGES[(MAIN, bn)])]
+        out += [(MAIN, bn, 0, 0, sp) for sp in (1, 2, 4, 8)]
     if M <= 64:
-        out.append((SKINNY, 0, 0, 0))
+        out.append((SKINNY, 0, 0, 0, 0))
     return out
 
 
-def time_config(M, N, K, path, bn, group, reps=50, sets=None, batch=1, stages=0):
+def time_config(M, N, K, path, bn, group, reps=50, sets=None, batch=1, stages=0, split=0):
     """Microseconds per launch (CUDA-graph replay), or None if not served."""
     import torch
 
@@ -53,9 +56,12 @@ def time_config(M, N, K, path, bn, group, reps=50, sets=None, batch=1, stages=0)
     a0, b0, c0 = sets[0]
     sa, sb, sc = M * K, K * N, M * N
     tg.tg_gemm_force_path(path)
-    if tg.tg_gemm_force_tiling(bn, group) != tg.TG_OK or tg.tg_gemm_force_stages(stages) != tg.TG_OK:
+    if (tg.tg_gemm_force_tiling(bn, group) != tg.TG_OK or tg.tg_gemm_force_stages(stages) != tg.TG_OK
+            or tg.tg_gemm_force_split_k(split) != tg.TG_OK):
         tg.tg_gemm_force_path(0)
+        tg.tg_gemm_force_tiling(0, 0)
         tg.tg_gemm_force_stages(0)
+        tg.tg_gemm_force_split_k(0)
         return None
     try:
         if tg.tg_gemm_batched_path(batch, M, N, K, a0.data_ptr(), K, sa, b0.data_ptr(), N, sb,
@@ -92,6 +98,7 @@ def time_config(M, N, K, path, bn, group, reps=50, sets=None, batch=1, stages=0)
         tg.tg_gemm_force_path(0)
         tg.tg_gemm_force_tiling(0, 0)
         tg.tg_gemm_force_stages(0)
+        tg.tg_gemm_force_split_k(0)
 
 
 def make_sets(M, N, K, batch=1):
@@ -120,11 +127,11 @@ def sweep(shapes, reps=50):
                                             tg.F16, tg.F16)
         auto_us = time_config(M, N, K, auto_path, 0, 0, reps, sets, batch)
         rows = []
-        for path, bn, group, stages in candidates(M, N, K):
-            us = time_config(M, N, K, path, bn, group, reps, sets, batch, stages)
+        for path, bn, group, stages, split in candidates(M, N, K):
+            us = time_config(M, N, K, path, bn, group, reps, sets, batch, stages, split)
             if us is not None:
                 rows.append({"path": path, "bn": bn, "group_m": group, "stages": stages,
-                             "us": us,
+                             "split": split, "us": us,
                              "tflops": 2.0 * batch * M * N * K / (us * 1e-6) / 1e12})
         best = min(rows, key=lambda r: r["us"])
         results.append({"shape": list(shape), "auto_path": auto_path, "auto_us": auto_us,
@@ -151,13 +158,14 @@ def main():
         print(f"\n{'x'.join(str(v) for v in r['shape'])}: automatic path {r['auto_path']} {r['auto_us']:.1f} us; "
               f"best {names[r['best']['path']].format(bn=r['best']['bn'])} "
               f"group {r['best']['group_m']} stages {r['best']['stages']} "
-              f"{r['best']['us']:.1f} us")
-        print("| config | group_m | stages | us | TFLOP/s |")
-        print("|---|---|---|---|---|")
+              f"split {r['best']['split'] or 'auto'} {r['best']['us']:.1f} us")
+        print("| config | group_m | stages | split over K | us | TFLOP/s |")
+        print("|---|---|---|---|---|---|")
         for c in sorted(r["configs"], key=lambda c: c["us"]):
             st = c["stages"] or MAX_STAGES.get((c["path"], c["bn"]), "-")
+            sp = c["split"] or ("auto" if c["path"] == MAIN else "-")
             print(f"| {names[c['path']].format(bn=c['bn'])} | {c['group_m'] or 'default'} | "
-                  f"{st} | {c['us']:.1f} | {c['tflops']:.0f} |")
+                  f"{st} | {sp} | {c['us']:.1f} | {c['tflops']:.0f} |")
     if args.json:
         with open(args.json, "w") as f:
             json.dump(res, f, indent=1)
