@@ -174,14 +174,20 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     static_assert(BN % NB == 0, "B tile must be whole 128-byte boxes");
     // a split over K: this CTA is rank r of a cluster of `split` sharing one
     // tile, and takes k-blocks kb_lo .. kb_lo + num_kb - 1 of it
-    const int rank = split > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-    const int nkb_all = (K + BK - 1) / BK;
-    const int kb_lo = static_cast<int>(static_cast<long long>(rank) * nkb_all / split);
-    const int num_kb = static_cast<int>(static_cast<long long>(rank + 1) * nkb_all / split) - kb_lo;
+    // (the divisions are kept off the unsplit kernel's path to its first
+    // load: a 64-bit division alone costs ~100 instructions)
     const int total = tiles_m * tiles_n * bt.count;
+    int rank = 0, kb_lo = 0, num_kb = (K + BK - 1) / BK;
     // the tiles this CTA walks: t_first, t_first + t_step, ... (one tile when split)
-    const int t_first = static_cast<int>(blockIdx.x) / split;
-    const int t_step = split > 1 ? total : static_cast<int>(gridDim.x);
+    int t_first = static_cast<int>(blockIdx.x), t_step = static_cast<int>(gridDim.x);
+    if (split > 1) {
+        const int nkb_all = num_kb;  // < 2^25, so rank * nkb_all fits in an int
+        rank = static_cast<int>(cluster_ctarank());
+        kb_lo = rank * nkb_all / split;
+        num_kb = (rank + 1) * nkb_all / split - kb_lo;
+        t_first = static_cast<int>(blockIdx.x) / split;
+        t_step = total;
+    }
     // the producer's first tile, found before the wait for the previous
     // kernel (the integer divisions of the tile order are on the critical
     // path of a one-tile CTA otherwise)
@@ -438,73 +444,56 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             batch_tile_coords(t_first, tiles_m, tiles_n, group_m, b, tm, tn);
             void* Cb = batch_ptr(C, b, bt.sC, OUT_F32 ? 4 : 2);
             // rows rank*rows .. of the tile, four columns per item, every
-            // thread of the CTA; the partials are added in rank order.  A
-            // thread issues the remote loads of kUnroll items before it adds
-            // any, so that several round trips overlap.
+            // thread of the CTA; the partials are added in rank order
             const int rows = BM / split;
             constexpr int quads = BN / 4;
-            constexpr int kUnroll = 4;
-            const int items = rows * quads;
-            for (int i0 = threadIdx.x; i0 < items; i0 += kThreads * kUnroll) {
-                float4 part[kUnroll][kMaxSplitK];
+            for (int idx = threadIdx.x; idx < rows * quads; idx += kThreads) {
+                const int ml = rank * rows + idx / quads;
+                const int nl = 4 * (idx % quads);
+                const int m = tm * BM + ml, n = tn * BN + nl;
+                if (m >= M || n >= N) continue;
+                const uint32_t off = static_cast<uint32_t>((ml * RedCfg<BN>::LD + nl) * 4);
+                float4 part[kMaxSplitK];
 #pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    const int idx = i0 + u * kThreads;
-                    if (idx >= items) break;
-                    const int ml = rank * rows + idx / quads;
-                    const int nl = 4 * (idx % quads);
-                    const uint32_t off = static_cast<uint32_t>((ml * RedCfg<BN>::LD + nl) * 4);
+                for (int r = 0; r < kMaxSplitK; ++r)
+                    if (r < split) part[r] = ld_cluster_f32x4(mapa_shared(base + off, static_cast<uint32_t>(r)));
+                float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-                    for (int r = 0; r < kMaxSplitK; ++r)
-                        if (r < split)
-                            part[u][r] = ld_cluster_f32x4(mapa_shared(base + off, static_cast<uint32_t>(r)));
-                }
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    const int idx = i0 + u * kThreads;
-                    if (idx >= items) break;
-                    const int ml = rank * rows + idx / quads;
-                    const int nl = 4 * (idx % quads);
-                    const int m = tm * BM + ml, n = tn * BN + nl;
-                    if (m >= M || n >= N) continue;
-                    float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-                    for (int r = 0; r < kMaxSplitK; ++r) {
-                        if (r < split) {
-                            v[0] += part[u][r].x;
-                            v[1] += part[u][r].y;
-                            v[2] += part[u][r].z;
-                            v[3] += part[u][r].w;
-                        }
+                for (int r = 0; r < kMaxSplitK; ++r) {
+                    if (r < split) {
+                        v[0] += part[r].x;
+                        v[1] += part[r].y;
+                        v[2] += part[r].z;
+                        v[3] += part[r].w;
                     }
-                    const bool full = n + 4 <= N;
-                    if (epi.on) {
+                }
+                const bool full = n + 4 <= N;
+                if (epi.on) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (n + j < N) v[j] = epilogue_elem<OUT_F32>(v[j], m, n + j, epi);
+                }
+                if constexpr (OUT_F32) {
+                    float* row = static_cast<float*>(Cb) + static_cast<long long>(m) * ldc + n;
+                    if (c_vec && full) {
+                        *reinterpret_cast<float4*>(row) = make_float4(v[0], v[1], v[2], v[3]);
+                    } else {
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            if (n + j < N) v[j] = epilogue_elem<OUT_F32>(v[j], m, n + j, epi);
+                            if (n + j < N) row[j] = v[j];
                     }
-                    if constexpr (OUT_F32) {
-                        float* row = static_cast<float*>(Cb) + static_cast<long long>(m) * ldc + n;
-                        if (c_vec && full) {
-                            *reinterpret_cast<float4*>(row) = make_float4(v[0], v[1], v[2], v[3]);
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                if (n + j < N) row[j] = v[j];
-                        }
+                } else {
+                    __half* row = static_cast<__half*>(Cb) + static_cast<long long>(m) * ldc + n;
+                    if (c_vec && full) {
+                        const __half2 lo = __floats2half2_rn(v[0], v[1]);
+                        const __half2 hi = __floats2half2_rn(v[2], v[3]);
+                        *reinterpret_cast<uint2*>(row) =
+                            make_uint2(*reinterpret_cast<const uint32_t*>(&lo),
+                                       *reinterpret_cast<const uint32_t*>(&hi));
                     } else {
-                        __half* row = static_cast<__half*>(Cb) + static_cast<long long>(m) * ldc + n;
-                        if (c_vec && full) {
-                            const __half2 lo = __floats2half2_rn(v[0], v[1]);
-                            const __half2 hi = __floats2half2_rn(v[2], v[3]);
-                            *reinterpret_cast<uint2*>(row) =
-                                make_uint2(*reinterpret_cast<const uint32_t*>(&lo),
-                                           *reinterpret_cast<const uint32_t*>(&hi));
-                        } else {
 #pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                if (n + j < N) row[j] = __float2half_rn(v[j]);
-                        }
+                        for (int j = 0; j < 4; ++j)
+                            if (n + j < N) row[j] = __float2half_rn(v[j]);
                     }
                 }
             }
