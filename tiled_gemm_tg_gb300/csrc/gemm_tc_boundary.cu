@@ -177,7 +177,7 @@ gemm_tc_boundary_kernel(const __half* __restrict__ A0, long long lda, const __ha
     const int m0 = blockIdx.y * BM;
     // a cluster of `split` CTAs along x shares one output tile
     const int rank = split > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-    const int n0 = static_cast<int>(split > 1 ? blockIdx.x / split : blockIdx.x) * BN;
+    const int n0 = static_cast<int>(blockIdx.x / split) * BN;
 
     if (tid == 0) {
         mbar_init(smem_u32(&mma_bar[0]), 1);
@@ -196,14 +196,9 @@ gemm_tc_boundary_kernel(const __half* __restrict__ A0, long long lda, const __ha
     pdl_wait();  // the previous kernel on the stream is complete from here on
 
     constexpr uint32_t idesc = idesc_f16_f32(BM, BN, false, true);
-    // this CTA's k-blocks kb0 .. kb0 + num_kb - 1 (the divisions only in
-    // split calls; nkb < 2^26, so rank * nkb fits in an int)
-    int kb0 = 0, num_kb = (K + BK - 1) / BK;
-    if (split > 1) {
-        const int nkb_all = num_kb;
-        kb0 = rank * nkb_all / split;
-        num_kb = (rank + 1) * nkb_all / split - kb0;
-    }
+    const int nkb_all = (K + BK - 1) / BK;
+    const int kb0 = static_cast<int>(static_cast<long long>(rank) * nkb_all / split);
+    const int num_kb = static_cast<int>(static_cast<long long>(rank + 1) * nkb_all / split) - kb0;
     bool aborted = false;
 
     // Registers carry k-block i+1 while the tensor core works on k-block i
