@@ -438,9 +438,10 @@ tg_status tg_gemm_force_split_k(int split);
  * M x N x K call (batch products) of in_dtype (TG_F16 or TG_E4M3) on
  * num_sms SMs: returns the split S (1: none) and writes the tile width
  * (64, 128 or 256) to *bn.  The default width, unsplit, competes with every
- * width whose tiles fill at most half of the SMs, at its largest split (2, 4
- * or 8 with tiles * S <= num_sms and S <= k-blocks), by a time estimate
- * measured on GB300: ~86 KB/us of A and B per CTA unsplit, ~95 KB/us split,
+ * other width unsplit and with every width whose tiles fill at most half of
+ * the SMs at its largest split (2, 4 or 8 with tiles * S <= num_sms and
+ * S <= k-blocks), by a time estimate (waves of CTAs included; a challenger
+ * must be 5 % faster) measured on GB300: ~86 KB/us of A and B per CTA unsplit, ~95 KB/us split,
  * plus 1.5, 2.5 or 4.0 us for a split of 64-, 128- or 256-column tiles.  On
  * a device the library also requires every cluster to be resident at once
  * (GB300 holds 15 clusters of 8 of these CTAs), which can change the choice.

@@ -515,6 +515,10 @@ def test_boundary_split_rule(tiles, kblocks, sms, want):
     ((304, 520, 1024, 1, (64, 4))),
     ((512, 1024, 2048, 1, (128, 4))),
     ((256, 4096, 4096, 1, (256, 4))),
+    # unsplit, but wider tiles in fewer waves than the default width
+    ((2048, 2048, 1024, 1, (256, 1))),
+    ((4096, 1024, 2048, 1, (256, 1))),
+    ((1536, 1536, 1024, 1, (128, 1))),
     # no split: the tiles fill the GPU, or K is too short to pay for it
     ((1024, 2048, 512, 1, (128, 1))),
     ((1024, 1024, 1024, 1, (64, 1))),

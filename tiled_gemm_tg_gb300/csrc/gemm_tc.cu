@@ -624,8 +624,8 @@ double main_cost_us(long long M, long long N, long long K, long long batch, int 
 // The tile width and split for a call (max_clusters(bn) gives the residency
 // of each instance, or null for the rule alone).  A forced split is used as
 // given (halved while it exceeds the k-blocks); otherwise the default tile
-// width, unsplit, competes with every tile width at its largest split by
-// estimated time.
+// width, unsplit, competes with every other width unsplit and every width
+// at its largest split, by estimated time.
 template <typename MC>
 void plan(long long M, long long N, long long K, long long batch, int es, int num_sms,
           int forced_bn, int forced_split, MC max_clusters, int* bn_out, int* split_out)
@@ -641,18 +641,23 @@ void plan(long long M, long long N, long long K, long long batch, int es, int nu
         split = forced_split;
         while (split > 1 && split > nkb) split >>= 1;
     } else {
-        double best = main_cost_us(M, N, K, batch, es, num_sms, bn, 1);
+        // another width or a split must be estimated 5 % faster than the
+        // default width, unsplit, to replace it
+        double best = 0.95 * main_cost_us(M, N, K, batch, es, num_sms, bn, 1);
         const int widths[3] = {64, 128, 256};
         for (int w : widths) {
             if ((forced_bn != 0 && w != forced_bn) || (es == 1 && w == 64)) continue;
             const long long tiles = ((M + BM - 1) / BM) * ((N + w - 1) / w) * batch;
             const int sw = main_split_k(tiles, nkb, num_sms, max_clusters(w));
-            if (sw <= 1) continue;
-            const double c = main_cost_us(M, N, K, batch, es, num_sms, w, sw);
-            if (c < best) {
-                best = c;
-                bn = w;
-                split = sw;
+            const int tries[2] = {1, sw};
+            for (int sp : tries) {
+                if (sp == 1 && w == bn) continue;
+                const double c = main_cost_us(M, N, K, batch, es, num_sms, w, sp);
+                if (c < best) {
+                    best = c;
+                    bn = w;
+                    split = sp;
+                }
             }
         }
     }
