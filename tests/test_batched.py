@@ -168,6 +168,28 @@ def test_batched_integer_bitwise(path):
     _check(a_list, b_list, outs, out, exact=True)
 
 
+@pytest.mark.parametrize("kind", ["packed", "bcast_b"])
+@pytest.mark.parametrize("split", [0, 2, 8])
+def test_batched_split_k_integer_bitwise(kind, split):
+    """A strided batch through the one-CTA kernel split over K (0: the
+    automatic choice, which splits these few deep-K tiles): each cluster
+    reduces one tile of one product, exactly."""
+    M, N, K, batch = 200, 136, 3000, 3
+    a_list = _mats(batch, (M, K), "int2", 11600, "f16", K)
+    b_list = _mats(1 if kind == "bcast_b" else batch, (K, N), "int2", 11700, "f16", K)
+    lda, sA, ldb, sB, ldc, sC = _layout(MAIN, M, N, K, kind)
+    tg.tg_gemm_force_path(MAIN)
+    assert tg.tg_gemm_force_split_k(split) == tg.TG_OK
+    try:
+        outs, intact, p = run_batched(a_list, b_list, torch.float16, lda, sA, ldb, sB, ldc, sC,
+                                      batch)
+    finally:
+        tg.tg_gemm_force_split_k(0)
+        tg.tg_gemm_force_path(0)
+    assert p == MAIN and intact
+    _check(a_list, b_list, outs, torch.float16, exact=True)
+
+
 @pytest.mark.parametrize("batch,M,N,K,want", [
     (16, 512, 512, 4096, PAIR),     # 64 pair tiles over the batch, K = 4096
     (16, 512, 512, 1024, MAIN),     # 64 pair tiles with K < 4096

@@ -212,3 +212,45 @@ def test_epilogue_square_8192_sampled():
     dsub = d[torch.from_numpy(rows)]
     ref = oracle.epilogue(C, epi["alpha"], epi["beta"], dsub.numpy(), bias, epi["act"])
     compare_ex(got[rows], ref, S, epi["alpha"], epi["beta"], dsub, bias, True, "8192^3 sampled")
+
+
+@pytest.mark.parametrize("split", [2, 4])
+@pytest.mark.parametrize("name", sorted(EPILOGUES))
+@pytest.mark.parametrize("out", [torch.float16, torch.float32])
+def test_epilogue_split_k(split, name, out):
+    """The one-CTA kernel split over K (forced) applies the fused epilogue in
+    its cluster reduction, once per element after the partials are added."""
+    M, N, K, dt = 300, 520, 1000, "f16"
+    epi = EPILOGUES[name]
+    a, b = _operands(M, N, K, dt, "normal_rsqrtk", 9800 + split)
+    d, bias = _extras(M, N, out, epi, 9810 + split)
+    assert tg.tg_gemm_force_split_k(split) == tg.TG_OK
+    try:
+        with forced(MAIN):
+            got, intact, p = run_ex(a, b, out, epi["alpha"], epi["beta"], d, bias, epi["act"],
+                                    lda=_ld(MAIN, K), ldb=_ld(MAIN, N), ldc=N + 3,
+                                    ldd=N + 5 if d is not None else None)
+    finally:
+        tg.tg_gemm_force_split_k(0)
+    assert p == MAIN and intact
+    ref, S = _reference(a, b, epi, d, bias)
+    compare_ex(got, ref, S, epi["alpha"], epi["beta"], d, bias, out == torch.float16,
+               f"{name} split {split}")
+
+
+def test_epilogue_split_k_in_place_integer():
+    """Split over K with D == C (C = AB + C), integer values: exact."""
+    M, N, K = 256, 264, 2048
+    a, b = _operands(M, N, K, "f16", "int2", 9820)
+    rng = np.random.default_rng(9821)
+    c0 = torch.from_numpy(rng.integers(-100, 101, (M, N)).astype(np.float32))
+    assert tg.tg_gemm_force_split_k(8) == tg.TG_OK
+    try:
+        with forced(MAIN):
+            got, intact, p = run_ex(a, b, torch.float32, 1.0, 1.0, c0, None, tg.ACT_NONE,
+                                    lda=_ld(MAIN, K), ldb=_ld(MAIN, N), in_place=True)
+    finally:
+        tg.tg_gemm_force_split_k(0)
+    assert p == MAIN and intact
+    C, _ = oracle.gemm(a.numpy(), b.numpy())
+    assert np.array_equal(got, C + c0.double().numpy())
