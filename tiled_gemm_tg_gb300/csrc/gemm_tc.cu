@@ -671,11 +671,9 @@ cudaError_t launch_cfg(const GemmArgs& a)
     using Cfg = MainCfg<BN>;
     using KB = KBlock<ES>;
     auto kernel = gemm_tc_main_kernel<BN, OUT_F32, ES>;
+    const int* mc = nullptr;
     {
-        // the instance's launch attributes (its cluster residency is the
-        // plan's concern)
-        const int* residency = nullptr;
-        const cudaError_t e = init_instance<BN, OUT_F32, ES>(&residency);
+        const cudaError_t e = init_instance<BN, OUT_F32, ES>(&mc);
         if (e != cudaSuccess) return e;
     }
     const int split = a.split_k > 1 ? a.split_k : 1;
