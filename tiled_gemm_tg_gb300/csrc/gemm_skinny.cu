@@ -19,8 +19,10 @@
 //     [r*128/S, (r+1)*128/S) of all S partials, rounds to the output type and
 //     stores them.  No global workspace, one launch.
 // Roles (192 threads per CTA): warp 0 TMA producer (k-block 128, four
-// stages), warp 1 TMEM allocation + single-thread tcgen05.mma issue, warps
-// 2-5 read the accumulator, one per TMEM lane quadrant.  Waits are bounded; on expiry the kernel records
+// stages; a stage's two B^T column blocks, and its two A k-blocks of 64, in
+// one 4-D copy each when N, and K, are whole numbers of blocks), warp 1
+// TMEM allocation + single-thread tcgen05.mma issue, warps 2-5 read the
+// accumulator, one per TMEM lane quadrant.  Waits are bounded; on expiry the kernel records
 // a bit in the device error word, stops issuing, waits for its own copies and
 // MMAs, and still reaches the cluster barriers so no CTA waits on a missing
 // peer.
@@ -74,7 +76,7 @@ __device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t cluster_addr)
 template <int MP, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmBT,
-                   void* C, long long ldc, int M, int N, int K, int split,
+                   void* C, long long ldc, int M, int N, int K, int split, int chunked,
                    int hook, unsigned int* err, Epilogue epi, BatchArgs bt)
 {
     using Cfg = SkinnyCfg<MP>;
@@ -113,10 +115,18 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         tma_prefetch_desc(&tmBT);
         // this CTA's first stages into L2 while the previous kernel finishes
         for (int kb = kb0; kb < kb1 && kb < kb0 + min(STAGES, kPrefetchStagesSingle); ++kb) {
-            for (int j = 0; j < BNT / 64; ++j)
-                tma_prefetch_l2_3d(&tmBT, n0 + j * 64, kb * BK, bz * bt.zb);
-            for (int j = 0; j < BK / 64; ++j)
-                tma_prefetch_l2_3d(&tmA, kb * BK + j * 64, 0, bz * bt.za);
+            if (chunked & 1) {
+                tma_prefetch_l2_4d(&tmBT, 0, kb * BK, n0 / 64, bz * bt.zb);
+            } else {
+                for (int j = 0; j < BNT / 64; ++j)
+                    tma_prefetch_l2_3d(&tmBT, n0 + j * 64, kb * BK, bz * bt.zb);
+            }
+            if (chunked & 2) {
+                tma_prefetch_l2_4d(&tmA, 0, 0, kb * (BK / 64), bz * bt.za);
+            } else {
+                for (int j = 0; j < BK / 64; ++j)
+                    tma_prefetch_l2_3d(&tmA, kb * BK + j * 64, 0, bz * bt.za);
+            }
         }
     }
     if (warp == 1) {
@@ -153,13 +163,23 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 const uint32_t fb = smem_u32(&full_bar[s]);
                 const uint32_t sa = base + s * Cfg::STAGE;
                 mbar_arrive_expect_tx(fb, Cfg::STAGE);
+// the stage's column blocks of B^T (and k-blocks of A) in one copy
+                // each when the sizes are whole blocks (chunked bit 0 / 1)
+                if (chunked & 1) {
+                    tma_load_4d(sa, &tmBT, fb, 0, kb * BK, n0 / 64, bz * bt.zb);
+                } else {
 #pragma unroll
-                for (int j = 0; j < BNT / 64; ++j)
-                    tma_load_3d(sa + j * BT_BOX, &tmBT, fb, n0 + j * 64, kb * BK, bz * bt.zb);
+                    for (int j = 0; j < BNT / 64; ++j)
+                        tma_load_3d(sa + j * BT_BOX, &tmBT, fb, n0 + j * 64, kb * BK, bz * bt.zb);
+                }
+                if (chunked & 2) {
+                    tma_load_4d(sa + BT_STAGE, &tmA, fb, 0, 0, kb * (BK / 64), bz * bt.za);
+                } else {
 #pragma unroll
-                for (int j = 0; j < BK / 64; ++j)
-                    tma_load_3d(sa + BT_STAGE + j * Cfg::A_ATOM, &tmA, fb, kb * BK + j * 64, 0,
-                                bz * bt.za);
+                    for (int j = 0; j < BK / 64; ++j)
+                        tma_load_3d(sa + BT_STAGE + j * Cfg::A_ATOM, &tmA, fb, kb * BK + j * 64, 0,
+                                    bz * bt.za);
+                }
                 ++issued;
                 if (++s == STAGES) {
                     s = 0;
@@ -355,11 +375,21 @@ cudaError_t launch_cfg(const GemmArgs& a)
                              (a.K + BK - 1) / BK, a.num_sms, g_max_clusters[dev][slot]);
     }
     CUtensorMap ta, tbt;
-    if (!encode_tmap(&ta, a.A, 2, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M),
-                         static_cast<uint64_t>(a.lda), a.batch, a.sA, 64, MP))
+    // A's two k-blocks of 64 and B^T's two column blocks of 64 in one copy
+    // each when K (for A) or N (for B^T) is a whole number of blocks
+    const int chunked = (a.N % 64 == 0 ? 1 : 0) |
+                        (a.K % 64 == 0 ? 2 : 0);
+    if ((chunked & 2)
+            ? !encode_tmap_chunks(&ta, a.A, 2, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M),
+                                  static_cast<uint64_t>(a.lda), a.batch, a.sA, 64, MP, BK / 64)
+            : !encode_tmap(&ta, a.A, 2, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M),
+                           static_cast<uint64_t>(a.lda), a.batch, a.sA, 64, MP))
         return cudaErrorInvalidValue;
-    if (!encode_tmap(&tbt, a.B, 2, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
-                         static_cast<uint64_t>(a.ldb), a.batch, a.sB, 64, BK))
+    if ((chunked & 1)
+            ? !encode_tmap_chunks(&tbt, a.B, 2, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
+                                  static_cast<uint64_t>(a.ldb), a.batch, a.sB, 64, BK, BNT / 64)
+            : !encode_tmap(&tbt, a.B, 2, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
+                           static_cast<uint64_t>(a.ldb), a.batch, a.sB, 64, BK))
         return cudaErrorInvalidValue;
     const int n_tiles = (a.N + BNT - 1) / BNT;
     if (n_tiles > 65535 || a.batch > 65535) return cudaErrorInvalidConfiguration;
@@ -376,8 +406,8 @@ cudaError_t launch_cfg(const GemmArgs& a)
     set_pdl_attr(at[1]);
     cfg.attrs = at;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kernel, ta, tbt, a.C, a.ldc, a.M, a.N, a.K, split, a.hook, a.err,
-                              a.epi, a.batch_args());
+    return cudaLaunchKernelEx(&cfg, kernel, ta, tbt, a.C, a.ldc, a.M, a.N, a.K, split, chunked,
+                              a.hook, a.err, a.epi, a.batch_args());
 }
 
 }  // namespace

@@ -18,9 +18,11 @@
 //     128-byte swizzle atom; a strided batch walks every tile of every
 //     matrix through 3-D tensor maps;
 //   * warp 0: TMA producer.  A is loaded K-major ([128 rows][128 B]), B is
-//     loaded MN-major in 128-byte-wide boxes of [k rows][128 B of n], all
+//     loaded MN-major in 128-byte-wide blocks of [k rows][128 B of n], all
 //     with the 128-byte swizzle, into a ring of STAGES full/empty mbarrier
-//     pairs;
+//     pairs; when N is a whole number of blocks one 4-D copy brings all
+//     BN / 64 blocks of a stage (a copy costs about the same whatever its
+//     size, so fewer, larger copies fill a stage sooner);
 //   * warp 1: allocates tensor memory and issues tcgen05.mma (M=128, N=BN,
 //     32 bytes of k each, four per k-block) from one thread, accumulating in
 //     a double-buffered TMEM accumulator (2 x BN fp32 columns);
@@ -137,7 +139,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, void* C, long long ldc, int M,
                     int N, int K, int tiles_m, int tiles_n, int group_m, int stages, int c_vec,
-                    int c_tma, int split, int hook, unsigned int* err, Epilogue epi, BatchArgs bt)
+                    int c_tma, int split, int b_chunks, int hook, unsigned int* err, Epilogue epi,
+                    BatchArgs bt)
 {
     using Cfg = MainCfg<BN>;
     constexpr int STAGES = Cfg::STAGES;  // the most stages; `stages` are in use
@@ -202,8 +205,12 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const int pf = total > t_step ? stages : min(stages, kPrefetchStagesSingle);
             for (int kb = 0; kb < num_kb && kb < pf; ++kb) {
                 tma_prefetch_l2_3d(&tmA, (kb_lo + kb) * BK, tm * BM, b * bt.za);
-                for (int j = 0; j < BN / NB; ++j)
-                    tma_prefetch_l2_3d(&tmB, tn * BN + j * NB, (kb_lo + kb) * BK, b * bt.zb);
+                if (b_chunks) {
+                    tma_prefetch_l2_4d(&tmB, 0, (kb_lo + kb) * BK, tn * (BN / NB), b * bt.zb);
+                } else {
+                    for (int j = 0; j < BN / NB; ++j)
+                        tma_prefetch_l2_3d(&tmB, tn * BN + j * NB, (kb_lo + kb) * BK, b * bt.zb);
+                }
             }
         }
     }
@@ -253,10 +260,16 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const uint32_t sa = base + s * Cfg::STAGE;
                     mbar_arrive_expect_tx(fb, Cfg::STAGE);
                     tma_load_3d(sa, &tmA, fb, (kb_lo + kb) * BK, tm * BM, za);
+                    if (b_chunks) {
+                        // all BN / NB column blocks of B in one copy
+                        tma_load_4d(sa + A_STAGE, &tmB, fb, 0, (kb_lo + kb) * BK, tn * (BN / NB),
+                                    zb);
+                    } else {
 #pragma unroll
-                    for (int j = 0; j < BN / NB; ++j)
-                        tma_load_3d(sa + A_STAGE + j * B_BOX, &tmB, fb, tn * BN + j * NB,
-                                    (kb_lo + kb) * BK, zb);
+                        for (int j = 0; j < BN / NB; ++j)
+                            tma_load_3d(sa + A_STAGE + j * B_BOX, &tmB, fb, tn * BN + j * NB,
+                                        (kb_lo + kb) * BK, zb);
+                    }
                     ++issued;
                     if (++s == stages) {
                         s = 0;
@@ -681,9 +694,18 @@ cudaError_t launch_cfg(const GemmArgs& a)
     if (!encode_tmap(&ta, a.A, ES, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M),
                      static_cast<uint64_t>(a.lda), a.batch, a.sA, KB::BK, BM))
         return cudaErrorInvalidValue;
-    if (!encode_tmap(&tb, a.B, ES, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
-                     static_cast<uint64_t>(a.ldb), a.batch, a.sB, KB::NB, KB::BK))
+    // B's BN / NB column blocks of a k-block in one copy when N is a whole
+    // number of blocks (a block past N would read beyond the matrix)
+    const int b_chunks = BN > KB::NB && a.N % KB::NB == 0 ? 1 : 0;
+    if (b_chunks) {
+        if (!encode_tmap_chunks(&tb, a.B, ES, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
+                                static_cast<uint64_t>(a.ldb), a.batch, a.sB, KB::NB, KB::BK,
+                                BN / KB::NB))
+            return cudaErrorInvalidValue;
+    } else if (!encode_tmap(&tb, a.B, ES, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
+                            static_cast<uint64_t>(a.ldb), a.batch, a.sB, KB::NB, KB::BK)) {
         return cudaErrorInvalidValue;
+    }
     const int tiles_m = (a.M + BM - 1) / BM;
     const int tiles_n = (a.N + BN - 1) / BN;
     const int total = tiles_m * tiles_n * a.batch;
@@ -723,8 +745,8 @@ cudaError_t launch_cfg(const GemmArgs& a)
     cfg.attrs = at;
     cfg.numAttrs = split > 1 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kernel, ta, tb, tc, a.C, a.ldc, a.M, a.N, a.K, tiles_m,
-                              tiles_n, group_m, stages, c_vec, c_tma, split, a.hook, a.err, a.epi,
-                              a.batch_args());
+                              tiles_n, group_m, stages, c_vec, c_tma, split, b_chunks, a.hook,
+                              a.err, a.epi, a.batch_args());
 }
 
 }  // namespace

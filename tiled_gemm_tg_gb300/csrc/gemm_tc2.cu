@@ -21,8 +21,10 @@
 //
 // Roles (320 threads per CTA, the same in both CTAs of the pair):
 //   warp 0   TMA producer.  Each CTA loads its own halves into its own shared
-//            memory; every copy signals the EVEN (leader) CTA's full barrier,
-//            which the leader's producer arms with both CTAs' bytes.
+//            memory (a k-block's two A atoms, and its two B column blocks,
+//            in one 4-D copy each when K, and N, are whole numbers of
+//            blocks); every copy signals the EVEN (leader) CTA's full
+//            barrier, which the leader's producer arms with both CTAs' bytes.
 //   warp 1   both CTAs allocate 512 TMEM columns together (two 256-column
 //            accumulators); only the leader's lane 0 issues the MMAs.  Each
 //            k-block's commit is multicast to both CTAs' empty barriers,
@@ -136,10 +138,11 @@ __device__ __forceinline__ void work_item(int t, int tiles_m, int tiles_n, int g
 template <bool OUT_F32, int ES>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmB4,
                     const __grid_constant__ CUtensorMap tmC, void* C, long long ldc, int M,
                     int N, int K, int tiles_m, int tiles_n, int group_m, int split_tail,
-                    int stages, int c_vec, int c_tma, int hook, unsigned int* err, Epilogue epi,
-                    BatchArgs bt)
+                    int stages, int c_vec, int c_tma, int chunked, int hook, unsigned int* err,
+                    Epilogue epi, BatchArgs bt)
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[STAGES];   // used in the leader only
@@ -174,6 +177,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (chunked & 1) tma_prefetch_desc(&tmB4);
     }
     if (warp == 1) {
         tmem_alloc_pair(smem_u32(&tmem_slot), TMEM_COLS);
@@ -241,13 +245,24 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[s]), 2 * stage_bytes);
                     const uint32_t fb = full0 + 8u * static_cast<uint32_t>(s);
                     const uint32_t sa = base + s * STAGE;
+                    // the k-block's A atoms, and the CTA's B column blocks, in
+                    // one copy each when the sizes are whole blocks
+                    if (chunked & 2) {
+                        tma_load_4d_pair_hint(sa, &tmA, fb, 0, row, kk * KA, za, pol_a);
+                    } else {
 #pragma unroll
-                    for (int j = 0; j < KA; ++j)
-                        tma_load_3d_pair_hint(sa + j * A_ATOM, &tmA, fb, kk * BK + j * KG::AE,
-                                              row, za, pol_a);
-                    for (int j = 0; j < nbox; ++j)
-                        tma_load_3d_pair_hint(sa + A_STAGE + j * KG::B_BOX, &tmB, fb,
-                                              col + j * KG::NB, kk * BK, zb, pol_b);
+                        for (int j = 0; j < KA; ++j)
+                            tma_load_3d_pair_hint(sa + j * A_ATOM, &tmA, fb, kk * BK + j * KG::AE,
+                                                  row, za, pol_a);
+                    }
+                    if ((chunked & 1) && nbox > 1) {
+                        tma_load_4d_pair_hint(sa + A_STAGE, &tmB4, fb, 0, kk * BK, col / KG::NB, zb,
+                                              pol_b);
+                    } else {
+                        for (int j = 0; j < nbox; ++j)
+                            tma_load_3d_pair_hint(sa + A_STAGE + j * KG::B_BOX, &tmB, fb,
+                                                  col + j * KG::NB, kk * BK, zb, pol_b);
+                    }
                     ++issued;
                     if (++s == stages) {
                         s = 0;
@@ -461,13 +476,29 @@ cudaError_t launch_cfg(const GemmArgs& a)
         }
         max_clusters = g_max_clusters[dev][slot];
     }
-    CUtensorMap ta, tb;
-    if (!encode_tmap(&ta, a.A, ES, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M),
-                     static_cast<uint64_t>(a.lda), a.batch, a.sA, KG::AE, HM))
+    // A's KA atoms of a k-block in one copy when K is a whole number of
+    // atoms (bit 1), and a CTA's HN / NB column blocks of B in one copy when
+    // N is a whole number of blocks (bit 0, through a second map: the halves
+    // of a cut last wave load one block through the first)
+    CUtensorMap ta, tb, tb4;
+    std::memset(&tb4, 0, sizeof(tb4));
+    const int chunk_a = a.K % KG::AE == 0 ? 2 : 0;
+    const int chunk_b = HN > KG::NB && a.N % KG::NB == 0 ? 1 : 0;
+    if (chunk_a ? !encode_tmap_chunks(&ta, a.A, ES, static_cast<uint64_t>(a.K),
+                                      static_cast<uint64_t>(a.M), static_cast<uint64_t>(a.lda),
+                                      a.batch, a.sA, KG::AE, HM, KA)
+                : !encode_tmap(&ta, a.A, ES, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M),
+                               static_cast<uint64_t>(a.lda), a.batch, a.sA, KG::AE, HM))
         return cudaErrorInvalidValue;
     if (!encode_tmap(&tb, a.B, ES, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
                      static_cast<uint64_t>(a.ldb), a.batch, a.sB, KG::NB, KG::BK))
         return cudaErrorInvalidValue;
+    if (chunk_b &&
+        !encode_tmap_chunks(&tb4, a.B, ES, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.K),
+                            static_cast<uint64_t>(a.ldb), a.batch, a.sB, KG::NB, KG::BK,
+                            HN / KG::NB))
+        return cudaErrorInvalidValue;
+    const int chunked = chunk_a | chunk_b;
     const int tiles_m = (a.M + PM - 1) / PM;
     const int tiles_n = (a.N + PN - 1) / PN;
     const int total = tiles_m * tiles_n * a.batch;
@@ -505,9 +536,9 @@ cudaError_t launch_cfg(const GemmArgs& a)
     set_pdl_attr(at[1]);
     cfg.attrs = at;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kernel, ta, tb, tc, a.C, a.ldc, a.M, a.N, a.K, tiles_m,
-                              tiles_n, group_m, split_tail, stages, c_vec, c_tma, a.hook, a.err,
-                              a.epi, a.batch_args());
+    return cudaLaunchKernelEx(&cfg, kernel, ta, tb, tb4, tc, a.C, a.ldc, a.M, a.N, a.K, tiles_m,
+                              tiles_n, group_m, split_tail, stages, c_vec, c_tma, chunked, a.hook,
+                              a.err, a.epi, a.batch_args());
 }
 
 }  // namespace

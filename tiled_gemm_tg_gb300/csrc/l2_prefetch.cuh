@@ -37,5 +37,14 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int32
                  : "memory");
 }
 
+// The same for a 4-D map.
+__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap* map, int32_t x, int32_t y,
+                                                   int32_t z, int32_t w)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w)
+                 : "memory");
+}
+
 }  // namespace dev
 }  // namespace tg

@@ -96,6 +96,18 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// The same for a 4-D map (a box of several column blocks: x, y = row, z =
+// column block, w = matrix of a batch).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t x, int32_t y, int32_t z, int32_t w)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
+        : "memory");
+}
+
 // 3-D tiled bulk-tensor store shared -> global of the box of `map` at
 // (x, y, z), read from `src`; parts of the box outside the tensor are not
 // written.  Tracked as a bulk async group of the issuing thread
@@ -410,6 +422,19 @@ __device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const CUtens
         ".mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;"
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z),
         "l"(policy)
+        : "memory");
+}
+
+// The same for a 4-D map (a box of several column or k blocks).
+__device__ __forceinline__ void tma_load_4d_pair_hint(uint32_t dst, const CUtensorMap* map,
+                                                      uint32_t bar, int32_t x, int32_t y,
+                                                      int32_t z, int32_t w, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile"
+        ".mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7;"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z),
+        "r"(w), "l"(policy)
         : "memory");
 }
 

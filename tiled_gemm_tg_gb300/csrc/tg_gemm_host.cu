@@ -349,11 +349,13 @@ struct TmapKey {
     uint32_t box_cols, box_rows;
     int es;
     int kind;  // 0: operand load map (128-byte swizzle), 1: output store map (no swizzle)
+    uint32_t box_chunks;  // > 0: a 4-D operand map of column blocks (kind 0)
     bool operator==(const TmapKey& o) const
     {
         return ptr == o.ptr && cols == o.cols && rows == o.rows && ld == o.ld &&
                batch == o.batch && stride == o.stride && box_cols == o.box_cols &&
-               box_rows == o.box_rows && es == o.es && kind == o.kind;
+               box_rows == o.box_rows && es == o.es && kind == o.kind &&
+               box_chunks == o.box_chunks;
     }
 };
 
@@ -388,7 +390,8 @@ int tmap_slot(const TmapKey& k)
     h = mix(h, k.batch);
     h = mix(h, k.stride);
     h = mix(h, (static_cast<uint64_t>(k.box_cols) << 32) | k.box_rows);
-    h = mix(h, static_cast<uint64_t>(k.es) | (static_cast<uint64_t>(k.kind) << 8));
+    h = mix(h, static_cast<uint64_t>(k.es) | (static_cast<uint64_t>(k.kind) << 8) |
+                   (static_cast<uint64_t>(k.box_chunks) << 16));
     return static_cast<int>(h % kTmapCacheSize);
 }
 
@@ -396,7 +399,8 @@ int tmap_slot(const TmapKey& k)
 // (fp16 or byte elements, 128-byte swizzle, 256-byte L2 promotion), kind 1:
 // an output store map (fp16 or fp32 elements, no swizzle).
 bool encode_map(CUtensorMap* map, int kind, const void* ptr, int es, uint64_t cols, uint64_t rows,
-                uint64_t ld, uint64_t batch, uint64_t stride, uint32_t box_cols, uint32_t box_rows)
+                uint64_t ld, uint64_t batch, uint64_t stride, uint32_t box_cols, uint32_t box_rows,
+                uint32_t box_chunks = 0)
 {
     if (!g_encode) return false;
     if (kind == 0 ? (es != 1 && es != 2) : (es != 2 && es != 4)) return false;
@@ -406,7 +410,7 @@ bool encode_map(CUtensorMap* map, int kind, const void* ptr, int es, uint64_t co
         batch = 1;
         stride = (rows * ld * es + 15) / 16 * 16 / es;
     }
-    const TmapKey key{ptr, cols, rows, ld, batch, stride, box_cols, box_rows, es, kind};
+    const TmapKey key{ptr, cols, rows, ld, batch, stride, box_cols, box_rows, es, kind, box_chunks};
     const int slot = tmap_slot(key);
     {
         std::lock_guard<std::mutex> lock(g_tmap_mu);
@@ -416,14 +420,28 @@ bool encode_map(CUtensorMap* map, int kind, const void* ptr, int es, uint64_t co
             return true;
         }
     }
-    cuuint64_t dims[3] = {cols, rows, batch};
-    cuuint64_t strides[2] = {ld * es, stride * es};
-    cuuint32_t box[3] = {box_cols, box_rows, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
+    // 3-D: {cols, rows, batch}.  4-D (box_chunks > 0): the same bytes seen
+    // as {box_cols, rows, cols / box_cols column blocks, batch}, the block
+    // stride box_cols elements, so that one box brings box_chunks adjacent
+    // column blocks, each landing as its own [box_rows][box_cols] block
+    const uint32_t rank = box_chunks > 0 ? 4 : 3;
+    cuuint64_t dims[4] = {cols, rows, batch, 1};
+    cuuint64_t strides[3] = {ld * es, stride * es, 0};
+    cuuint32_t box[4] = {box_cols, box_rows, 1, 1};
+    if (box_chunks > 0) {
+        if (cols % box_cols != 0) return false;
+        dims[0] = box_cols;
+        dims[2] = cols / box_cols;
+        dims[3] = batch;
+        strides[1] = static_cast<cuuint64_t>(box_cols) * es;
+        strides[2] = stride * es;
+        box[2] = box_chunks;
+    }
+    cuuint32_t estr[4] = {1, 1, 1, 1};
     const CUtensorMapDataType dt = es == 4   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                    : es == 2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                              : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-    CUresult r = g_encode(map, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+    CUresult r = g_encode(map, dt, rank, const_cast<void*>(ptr), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE,
                           kind == 0 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                           kind == 0 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
@@ -445,6 +463,14 @@ bool encode_tmap(CUtensorMap* map, const void* ptr, int es, uint64_t cols, uint6
                  uint32_t box_rows)
 {
     return encode_map(map, 0, ptr, es, cols, rows, ld, batch, stride, box_cols, box_rows);
+}
+
+bool encode_tmap_chunks(CUtensorMap* map, const void* ptr, int es, uint64_t cols, uint64_t rows,
+                        uint64_t ld, uint64_t batch, uint64_t stride, uint32_t box_cols,
+                        uint32_t box_rows, uint32_t box_chunks)
+{
+    return encode_map(map, 0, ptr, es, cols, rows, ld, batch, stride, box_cols, box_rows,
+                      box_chunks);
 }
 
 bool encode_tmap_store(CUtensorMap* map, const void* ptr, int es, uint64_t cols, uint64_t rows,

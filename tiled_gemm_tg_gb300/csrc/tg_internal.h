@@ -119,6 +119,15 @@ bool encode_tmap(CUtensorMap* map, const void* ptr, int es, uint64_t cols, uint6
                  uint64_t ld, uint64_t batch, uint64_t stride, uint32_t box_cols,
                  uint32_t box_rows);
 
+// The same bytes as a 4-D map {box_cols, rows, cols / box_cols, batch} whose
+// box {box_cols, box_rows, box_chunks, 1} brings box_chunks adjacent
+// column blocks in one copy, block j landing box_rows * box_cols elements
+// after block j - 1.  cols must be a multiple of box_cols (no block may end
+// past the last column: such a box would read beyond the matrix).
+bool encode_tmap_chunks(CUtensorMap* map, const void* ptr, int es, uint64_t cols, uint64_t rows,
+                        uint64_t ld, uint64_t batch, uint64_t stride, uint32_t box_cols,
+                        uint32_t box_rows, uint32_t box_chunks);
+
 // The same for an output written by TMA stores: es = 2 (fp16) or 4 (fp32),
 // no swizzle, box_cols x box_rows x 1.
 bool encode_tmap_store(CUtensorMap* map, const void* ptr, int es, uint64_t cols, uint64_t rows,
