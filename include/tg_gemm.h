@@ -393,7 +393,8 @@ void tg_gemm_test_hook(int hook);
  * Tiling override, for configuration sweeps, tests and benchmarks (the
  * pages' tuning harness: block sizes and rasterisation, screened per shape).
  *   bn       tile width of the one-CTA kernel (path 3): 64, 128 or 256
- *            (with 8, 6 or 4 pipeline stages); 0 = chosen per problem.
+ *            (with 4, 3 or 4 pipeline stages of k-blocks of 128, 128 or 64
+ *            fp16 elements); 0 = chosen per problem.
  *   group_m  height, in tile rows, of the grouped tile order of the one-CTA
  *            and pair kernels (1..64); 0 = each kernel's default (16 for
  *            128-row tiles, 8 for 256-row pair tiles).
@@ -441,8 +442,10 @@ tg_status tg_gemm_force_split_k(int split);
  * other width unsplit and with every width whose tiles fill at most half of
  * the SMs at its largest split (2, 4 or 8 with tiles * S <= num_sms and
  * S <= k-blocks), by a time estimate (waves of CTAs included; a challenger
- * must be 5 % faster) measured on GB300: ~86 KB/us of A and B per CTA unsplit, ~95 KB/us split,
- * plus 1.5, 2.5 or 4.0 us for a split of 64-, 128- or 256-column tiles.  On
+ * must be 5 % faster) measured on GB300: A and B taken in at ~100 KB/us per
+ * CTA unsplit and ~110 KB/us split for 64- and 128-column tiles (~86 and
+ * ~95 for 256 columns), plus 1.5, 2.5 or 4.0 us for a split of 64-, 128- or
+ * 256-column tiles.  On
  * a device the library also requires every cluster to be resident at once
  * (GB300 holds 15 clusters of 8 of these CTAs), which can change the choice.
  * Returns 0 (and *bn = 0) for non-positive sizes or another dtype.

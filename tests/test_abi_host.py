@@ -506,20 +506,20 @@ def test_boundary_split_rule(tiles, kblocks, sms, want):
 
 @pytest.mark.parametrize("M,N,K,batch,want", [
     # measured best on GB300 (tile width / split): the estimate picks them
-    ((128, 256, 512, 1, (64, 8))),
     ((256, 256, 8192, 1, (64, 8))),
     # 16 clusters of 8: more than GB300 holds at once, so on the device
     # the library falls back to 64 / 4, the measured best
     ((512, 512, 8192, 1, (128, 8))),
-    ((1024, 1024, 4096, 1, (256, 4))),
+    ((1024, 1024, 4096, 1, (128, 2))),
     ((304, 520, 1024, 1, (64, 4))),
     ((512, 1024, 2048, 1, (128, 4))),
-    ((256, 4096, 4096, 1, (256, 4))),
+    ((256, 4096, 4096, 1, (128, 2))),
     # unsplit, but wider tiles in fewer waves than the default width
     ((2048, 2048, 1024, 1, (256, 1))),
     ((4096, 1024, 2048, 1, (256, 1))),
     ((1536, 1536, 1024, 1, (128, 1))),
     # no split: the tiles fill the GPU, or K is too short to pay for it
+    ((128, 256, 512, 1, (64, 1))),
     ((1024, 2048, 512, 1, (128, 1))),
     ((1024, 1024, 1024, 1, (64, 1))),
     ((2048, 1024, 512, 1, (128, 1))),

@@ -684,10 +684,10 @@ def test_forced_tilings(path, bn, group):
     assert np.array_equal(have, f16_bits_of(C_ref))
 
 
-@pytest.mark.parametrize("path,bn,stages", [(MAIN, 64, 2), (MAIN, 64, 5), (MAIN, 64, 8),
-                                            (MAIN, 128, 2), (MAIN, 128, 3), (MAIN, 128, 6),
-                                            (MAIN, 256, 2), (MAIN, 256, 3), (PAIR, 0, 2),
-                                            (PAIR, 0, 3)])
+@pytest.mark.parametrize("path,bn,stages", [(MAIN, 64, 2), (MAIN, 64, 3), (MAIN, 64, 4),
+                                            (MAIN, 128, 2), (MAIN, 128, 3),
+                                            (MAIN, 256, 2), (MAIN, 256, 3), (MAIN, 256, 4),
+                                            (PAIR, 0, 2), (PAIR, 0, 3)])
 def test_forced_stages(path, bn, stages):
     """Every pipeline depth the sweep can choose computes the same exact
     product (more k-blocks than stages, so the ring wraps many times)."""
@@ -708,19 +708,23 @@ def test_forced_stages(path, bn, stages):
     assert np.array_equal(have, f16_bits_of(C_ref))
 
 
-def test_forced_stages_beyond_the_kernel_are_refused():
+@pytest.mark.parametrize("path,bn,stages", [(PAIR, 0, 4), (MAIN, 128, 4), (MAIN, 64, 5),
+                                            (MAIN, 256, 5)])
+def test_forced_stages_beyond_the_kernel_are_refused(path, bn, stages):
     dev = torch.device("cuda")
     a = torch.ones((512, 1024), dtype=torch.float16, device=dev)
     b = torch.ones((1024, 512), dtype=torch.float16, device=dev)
     c = torch.full((512, 512), 7.0, dtype=torch.float16, device=dev)
     s = torch.cuda.current_stream().cuda_stream
-    tg.tg_gemm_force_path(PAIR)
-    assert tg.tg_gemm_force_stages(4) == tg.TG_OK
+    tg.tg_gemm_force_path(path)
+    assert tg.tg_gemm_force_tiling(bn, 0) == tg.TG_OK
+    assert tg.tg_gemm_force_stages(stages) == tg.TG_OK
     try:
         st = tg.tg_gemm(512, 512, 1024, a.data_ptr(), 1024, b.data_ptr(), 512, c.data_ptr(), 512,
                         tg.F16, tg.F16, s)
     finally:
         tg.tg_gemm_force_stages(0)
+        tg.tg_gemm_force_tiling(0, 0)
         tg.tg_gemm_force_path(0)
     assert st == tg.TG_ERR_UNSUPPORTED
     assert tg.tg_gemm_check(s) == tg.TG_OK

@@ -13,10 +13,10 @@
 //   * persistent grid of one CTA per SM walking a grouped tile order, so a
 //     wave of tiles shares A rows and B columns in L2 (the "block_wise"
 //     mapping of "TileLang：GPU异构计算的声明式分块编程范式" (kwkr.cn), §3.3);
-//   * tiles of 128 x BN (BN = 256, 128 or 64), k-blocks of 128 bytes per
-//     row (64 fp16 or 128 E4M3), so one A row of a k-block is exactly one
-//     128-byte swizzle atom; a strided batch walks every tile of every
-//     matrix through 3-D tensor maps;
+//   * tiles of 128 x BN (BN = 256, 128 or 64), k-blocks of one 128-byte
+//     swizzle atom per row (64 fp16 or 128 E4M3) for BN = 256 and of two
+//     for BN = 128 or 64; a strided batch walks every tile of every matrix
+//     through 3-D (or 4-D) tensor maps;
 //   * warp 0: TMA producer.  A is loaded K-major ([128 rows][128 B]), B is
 //     loaded MN-major in 128-byte-wide blocks of [k rows][128 B of n], all
 //     with the 128-byte swizzle, into a ring of STAGES full/empty mbarrier
@@ -74,16 +74,25 @@ namespace {
 using namespace tg::dev;
 
 constexpr int BM = 128;
-// A k-block is 128 bytes of every row: one 128-byte swizzle atom, 64 fp16 or
-// 128 E4M3 elements (ES = element size in bytes), four MMAs of 32 bytes.
-template <int ES>
+// 128-byte swizzle atoms of A per k-block: two for tiles of 64 or 128
+// columns (stages of 48 or 64 KB, four or three deep), one for 256 columns
+// (48 KB, four deep).  Measured in CUDA-graph replay against one atom
+// everywhere: 1024 x 2048 x 512 5.51 against 6.35 us, 1024^3 6.42 against
+// 8.45; with 256 columns two atoms (two stages of 96 KB) were slower
+// (2048 x 2048 x 1024 11.6 against 10.3 us).
+constexpr int katoms(int bn) { return bn == 256 ? 1 : 2; }
+// A k-block is KATOMS x 128 bytes of every row: KATOMS atoms of 64 fp16 or
+// 128 E4M3 elements (ES = element size in bytes), four MMAs of 32 bytes per
+// atom.
+template <int ES, int KATOMS>
 struct KBlock {
-    static constexpr int BK = 128 / ES;             // k elements per k-block
+    static constexpr int AE = 128 / ES;             // k elements per A atom
+    static constexpr int BK = KATOMS * AE;          // k elements per k-block
     static constexpr int NB = 128 / ES;             // n elements per B box (128 bytes)
     static constexpr uint32_t B_BOX = BK * 128;     // one [BK k][NB n] box
     static constexpr uint32_t B_KSTEP = 32 / ES * 128 / 16;  // 16-byte units per MMA k step
 };
-constexpr uint32_t A_STAGE = BM * 128;
+constexpr uint32_t A_ATOM = BM * 128;
 // Two epilogue warps per TMEM lane quadrant, each draining half of the
 // accumulator's columns: a long fused epilogue (GELU) then keeps up with the
 // MMAs instead of holding the accumulator buffer.
@@ -118,11 +127,13 @@ __device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t cluster_addr)
 
 template <int BN>
 struct MainCfg {
-    static constexpr uint32_t B_STAGE = BN * 128;
+    static constexpr int KATOMS = katoms(BN);
+    static constexpr uint32_t A_STAGE = KATOMS * A_ATOM;
+    static constexpr uint32_t B_STAGE = BN * 128 * KATOMS;
     static constexpr uint32_t STAGE = A_STAGE + B_STAGE;
     // the most stages that fit (the default); a ring of 2..STAGES can be
     // requested (tg_gemm_force_stages), shared memory is sized to it
-    static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+    static constexpr int STAGES = (BN == 256 ? 4 : (BN == 128 ? 6 : 8)) / KATOMS;
     static constexpr uint32_t TMEM_COLS = 2 * BN;
     static constexpr uint32_t SMEM = STAGES * STAGE + 1024;  // + alignment slack
     static constexpr uint32_t smem(int stages, bool c_tma)
@@ -139,7 +150,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, void* C, long long ldc, int M,
                     int N, int K, int tiles_m, int tiles_n, int group_m, int stages, int c_vec,
-                    int c_tma, int split, int b_chunks, int hook, unsigned int* err, Epilogue epi,
+                    int c_tma, int split, int b_chunks, int a_chunks, int hook, unsigned int* err,
+                    Epilogue epi,
                     BatchArgs bt)
 {
     using Cfg = MainCfg<BN>;
@@ -171,9 +183,12 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         abort_flag = 0;
         fence_mbar_init();
     }
-    constexpr int BK = KBlock<ES>::BK;
-    constexpr int NB = KBlock<ES>::NB;
-    constexpr uint32_t B_BOX = KBlock<ES>::B_BOX;
+    constexpr int KATOMS = Cfg::KATOMS;
+    using KB = KBlock<ES, KATOMS>;
+    constexpr int BK = KB::BK;
+    constexpr int NB = KB::NB;
+    constexpr uint32_t B_BOX = KB::B_BOX;
+    constexpr uint32_t A_STAGE = Cfg::A_STAGE;
     static_assert(BN % NB == 0, "B tile must be whole 128-byte boxes");
     // a split over K: this CTA is rank r of a cluster of `split` sharing one
     // tile, and takes k-blocks kb_lo .. kb_lo + num_kb - 1 of it
@@ -204,7 +219,13 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const int b = b0, tm = tm0, tn = tn0;
             const int pf = total > t_step ? stages : min(stages, kPrefetchStagesSingle);
             for (int kb = 0; kb < num_kb && kb < pf; ++kb) {
-                tma_prefetch_l2_3d(&tmA, (kb_lo + kb) * BK, tm * BM, b * bt.za);
+                if (a_chunks) {
+                    tma_prefetch_l2_4d(&tmA, 0, tm * BM, (kb_lo + kb) * KATOMS, b * bt.za);
+                } else {
+                    for (int j = 0; j < KATOMS; ++j)
+                        tma_prefetch_l2_3d(&tmA, (kb_lo + kb) * BK + j * KB::AE, tm * BM,
+                                           b * bt.za);
+                }
                 if (b_chunks) {
                     tma_prefetch_l2_4d(&tmB, 0, (kb_lo + kb) * BK, tn * (BN / NB), b * bt.zb);
                 } else {
@@ -259,7 +280,14 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const uint32_t fb = smem_u32(&full_bar[s]);
                     const uint32_t sa = base + s * Cfg::STAGE;
                     mbar_arrive_expect_tx(fb, Cfg::STAGE);
-                    tma_load_3d(sa, &tmA, fb, (kb_lo + kb) * BK, tm * BM, za);
+                    if (a_chunks) {
+                        tma_load_4d(sa, &tmA, fb, 0, tm * BM, (kb_lo + kb) * KATOMS, za);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < KATOMS; ++j)
+                            tma_load_3d(sa + j * A_ATOM, &tmA, fb,
+                                        (kb_lo + kb) * BK + j * KB::AE, tm * BM, za);
+                    }
                     if (b_chunks) {
                         // all BN / NB column blocks of B in one copy
                         tma_load_4d(sa + A_STAGE, &tmB, fb, 0, (kb_lo + kb) * BK, tn * (BN / NB),
@@ -321,9 +349,9 @@ gemm_tc_main_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const uint64_t ad = sdesc_sw128(sa, 16, 1024);
                     const uint64_t bd = sdesc_sw128(sa + A_STAGE, B_BOX, 1024);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        umma<ES>(d, ad + 2ull * k, bd + KBlock<ES>::B_KSTEP * k, idesc,
-                                 (kb | k) != 0 ? 1u : 0u);
+                    for (int k = 0; k < 4 * KATOMS; ++k)
+                        umma<ES>(d, ad + ((k / 4) * (A_ATOM >> 4) + (k % 4) * 2ull),
+                                 bd + KB::B_KSTEP * k, idesc, (kb | k) != 0 ? 1u : 0u);
                     umma_commit(smem_u32(&empty_bar[s]));
                     if (++s == stages) {
                         s = 0;
@@ -612,15 +640,17 @@ cudaError_t clusters_of(const GemmArgs& a, int bn, const int** mc)
 }
 
 // Estimated microseconds of a call with tile width bn split s ways over K,
-// from a sweep of every tile width and split on GB300 (CUDA-graph replay,
-// operands past L2): each CTA takes in A and B at ~86 KB/us on its own and
-// ~95 KB/us in a split, times the waves when the CTAs outnumber the SMs; a
-// split adds ~1.5, 2.5 or 4.0 us for 64, 128 or 256 columns (the partial
-// tile through distributed shared memory and the two cluster barriers).
+// from sweeps of every tile width and split on GB300 (CUDA-graph replay,
+// operands past L2): each CTA takes in A and B at ~100 KB/us on its own and
+// ~110 KB/us in a split with k-blocks of two atoms (64- and 128-column
+// tiles), ~86 and ~95 KB/us with one (256 columns), times the waves when the
+// CTAs outnumber the SMs; a split adds ~1.5, 2.5 or 4.0 us for 64, 128 or
+// 256 columns (the partial tile through distributed shared memory and the
+// two cluster barriers).
 double main_cost_us(long long M, long long N, long long K, long long batch, int es, int num_sms,
                     int bn, int s)
 {
-    const int bk = 128 / es;
+    const int bk = katoms(bn) * 128 / es;
     const long long tiles = ((M + BM - 1) / BM) * ((N + bn - 1) / bn) * batch;
     const long long waves = (tiles * s + num_sms - 1) / num_sms;
     const long long nkb = (K + bk - 1) / bk;
@@ -629,9 +659,10 @@ double main_cost_us(long long M, long long N, long long K, long long batch, int 
     const long long n64 = (N + 63) / 64 * 64;
     const long long cols = n64 < bn ? n64 : bn;
     const double kbytes = static_cast<double>((rows + cols) * kper * es) / 1024.0;
-    if (s == 1) return static_cast<double>(waves) * kbytes / 86.0;
+    const bool two = katoms(bn) == 2;
+    if (s == 1) return static_cast<double>(waves) * kbytes / (two ? 100.0 : 86.0);
     const double extra = bn == 64 ? 1.5 : bn == 128 ? 2.5 : 4.0;
-    return static_cast<double>(waves) * kbytes / 95.0 + extra;
+    return static_cast<double>(waves) * kbytes / (two ? 110.0 : 95.0) + extra;
 }
 
 // The tile width and split for a call (max_clusters(bn) gives the residency
@@ -643,16 +674,16 @@ template <typename MC>
 void plan(long long M, long long N, long long K, long long batch, int es, int num_sms,
           int forced_bn, int forced_split, MC max_clusters, int* bn_out, int* split_out)
 {
-    const int bk = 128 / es;
-    const long long nkb = (K + bk - 1) / bk;
     int bn = forced_bn != 0 ? forced_bn
                             : main_tile_n(static_cast<int>(M), static_cast<int>(N),
                                           static_cast<int>(batch), num_sms);
     if (es == 1 && bn == 64) bn = 128;  // E4M3 B boxes are 128 elements wide
+    // k-blocks of a tile width
+    auto nkb_of = [&](int w) { return (K + katoms(w) * 128 / es - 1) / (katoms(w) * 128 / es); };
     int split = 1;
     if (forced_split > 0) {
         split = forced_split;
-        while (split > 1 && split > nkb) split >>= 1;
+        while (split > 1 && split > nkb_of(bn)) split >>= 1;
     } else {
         // another width or a split must be estimated 5 % faster than the
         // default width, unsplit, to replace it
@@ -661,7 +692,7 @@ void plan(long long M, long long N, long long K, long long batch, int es, int nu
         for (int w : widths) {
             if ((forced_bn != 0 && w != forced_bn) || (es == 1 && w == 64)) continue;
             const long long tiles = ((M + BM - 1) / BM) * ((N + w - 1) / w) * batch;
-            const int sw = main_split_k(tiles, nkb, num_sms, max_clusters(w));
+            const int sw = main_split_k(tiles, nkb_of(w), num_sms, max_clusters(w));
             const int tries[2] = {1, sw};
             for (int sp : tries) {
                 if (sp == 1 && w == bn) continue;
@@ -682,7 +713,8 @@ template <int BN, bool OUT_F32, int ES>
 cudaError_t launch_cfg(const GemmArgs& a)
 {
     using Cfg = MainCfg<BN>;
-    using KB = KBlock<ES>;
+    using KB = KBlock<ES, Cfg::KATOMS>;
+    constexpr int KATOMS = Cfg::KATOMS;
     auto kernel = gemm_tc_main_kernel<BN, OUT_F32, ES>;
     const int* mc = nullptr;
     {
@@ -691,8 +723,14 @@ cudaError_t launch_cfg(const GemmArgs& a)
     }
     const int split = a.split_k > 1 ? a.split_k : 1;
     CUtensorMap ta, tb;
-    if (!encode_tmap(&ta, a.A, ES, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M),
-                     static_cast<uint64_t>(a.lda), a.batch, a.sA, KB::BK, BM))
+    // A's KATOMS atoms of a k-block in one copy when K is a whole number of
+    // atoms
+    const int a_chunks = KATOMS > 1 && a.K % KB::AE == 0 ? 1 : 0;
+    if (a_chunks ? !encode_tmap_chunks(&ta, a.A, ES, static_cast<uint64_t>(a.K),
+                                       static_cast<uint64_t>(a.M), static_cast<uint64_t>(a.lda),
+                                       a.batch, a.sA, KB::AE, BM, KATOMS)
+                 : !encode_tmap(&ta, a.A, ES, static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M),
+                                static_cast<uint64_t>(a.lda), a.batch, a.sA, KB::AE, BM))
         return cudaErrorInvalidValue;
     // B's BN / NB column blocks of a k-block in one copy when N is a whole
     // number of blocks (a block past N would read beyond the matrix)
@@ -745,8 +783,8 @@ cudaError_t launch_cfg(const GemmArgs& a)
     cfg.attrs = at;
     cfg.numAttrs = split > 1 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kernel, ta, tb, tc, a.C, a.ldc, a.M, a.N, a.K, tiles_m,
-                              tiles_n, group_m, stages, c_vec, c_tma, split, b_chunks, a.hook,
-                              a.err, a.epi, a.batch_args());
+                              tiles_n, group_m, stages, c_vec, c_tma, split, b_chunks, a_chunks,
+                              a.hook, a.err, a.epi, a.batch_args());
 }
 
 }  // namespace

@@ -6,7 +6,8 @@ Configurations, two axes at a time as the pages tune them: the CTA-pair
 kernel (256 x 256 tiles, k-block 128) with grouped tile orders of 2..32
 tile rows at its default three stages, and with 2 or 3 stages at its
 default group; the one-CTA kernel with 128 x 64 / 128 x 128 / 128 x 256
-tiles (at most 8 / 6 / 4 stages of k-block 64) with group heights 4..32 at
+tiles (at most 4 / 3 / 4 stages, k-blocks of 128 / 128 / 64 fp16
+elements) with group heights 4..32 at
 the most stages, with every depth from 2 stages up at the default group,
 and unsplit or split over K by clusters of 2, 4 or 8 CTAs; the skinny
 kernel when M <= 64.  Each configuration is forced through
@@ -30,7 +31,7 @@ PAIR, MAIN, SKINNY = 6, 3, 5
 L2_BYTES = 129 * 2**20
 
 
-MAX_STAGES = {(PAIR, 0): 3, (MAIN, 64): 8, (MAIN, 128): 6, (MAIN, 256): 4}
+MAX_STAGES = {(PAIR, 0): 3, (MAIN, 64): 4, (MAIN, 128): 3, (MAIN, 256): 4}
 
 
 def candidates(M: int, N: int, K: int):
