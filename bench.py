@@ -4,7 +4,7 @@
 A step is one pass of the whole path: one tg_gemm call (one kernel launch)
 on one batch of synthetic fp16 operands already resident in HBM.  The
 default workload is the 8192^3 fp16 GEMM (U(-1,1) inputs, fp32 accumulation,
-fp16 output), the shape the tensor-core roofline is judged on.  Two operand
+fp16 output), the compute-bound shape of the tensor-core roofline.  Two operand
 sets rotate between steps so every step streams 384 MB of fresh A/B/C, more
 than the 129 MB L2.
 
@@ -658,15 +658,15 @@ def main_attention(args, w):
     return 0
 
 
-# The judged configurations besides the headline 8192^3 square, measured in
-# the same run as the headline: (config label, workload name).
-JUDGED_CONFIGS = [
-    ("1", "f32_128x128x128"),
-    ("2", "edge_4x4x4"), ("2", "edge_128x256x512"), ("2", "edge_127x255x512"),
-    ("2", "edge_1x255x17"),
-    ("3", "tile_1024x2048x512"),
-    ("5a", "skinny_16x4096x4096"),
-    ("5b", "wide_4096x16384x4096"),
+# The specified workloads besides the headline 8192^3 square, measured in
+# the same run as the headline: (group, workload name).
+SPEC_WORKLOADS = [
+    ("fp32 example", "f32_128x128x128"),
+    ("edge set", "edge_4x4x4"), ("edge set", "edge_128x256x512"),
+    ("edge set", "edge_127x255x512"), ("edge set", "edge_1x255x17"),
+    ("tiling example", "tile_1024x2048x512"),
+    ("skinny", "skinny_16x4096x4096"),
+    ("wide", "wide_4096x16384x4096"),
 ]
 
 KERNEL_OF_PATH = {1: "epilogue_only_kernel", 2: "gemm_simt_f32_kernel", 3: "gemm_tc_main_kernel",
@@ -685,7 +685,7 @@ def roofline_of(flops: float, alg_bytes: float, seconds: float, peak_tflops: flo
 
 
 def measure_config(label, w, dev, launches, sampler, peaks, cpu_s, num_sms):
-    """One judged configuration: per-launch time stream-launched (launches
+    """One specified workload: per-launch time stream-launched (launches
     back to back from the host, CUDA events around the whole loop) and
     replayed from one CUDA graph (no host gaps),
     operand sets rotated so one pass over them is at least 3x the L2; the
@@ -763,7 +763,7 @@ def measure_config(label, w, dev, launches, sampler, peaks, cpu_s, num_sms):
     bound, frac_graph = roofline_of(flops, set_bytes, us_graph * 1e-6, peak, hbm, alu)
     _, frac_stream = roofline_of(flops, set_bytes, us_stream * 1e-6, peak, hbm, alu)
     rec = {
-        "config": label, "workload": w.name, "M": M, "N": N, "K": K,
+        "group": label, "workload": w.name, "M": M, "N": N, "K": K,
         "in_dtype": w.in_dtype, "out_dtype": w.out_dtype, "dist": w.dist,
         "path": tg.PATHS.get(path, str(path)), "kernel": KERNEL_OF_PATH.get(path, str(path)),
         "launches": launches,
@@ -818,9 +818,10 @@ def main():
                     help="attention workloads: the library's choice of forward kernel, or one "
                          "forced (tmem_p serves d <= 128, dv <= 128)")
     ap.add_argument("--no-configs", action="store_true",
-                    help="skip the per-configuration records (configs 1, 2, 3, 5a, 5b)")
+                    help="skip the per-workload records (fp32 example, edge set, tiling "
+                         "example, skinny, wide)")
     ap.add_argument("--config-launches", type=int, default=200,
-                    help="launches per judged configuration, stream-launched and in a graph")
+                    help="launches per specified workload, stream-launched and in a graph")
     ap.add_argument("--group-m", type=int, default=0,
                     help="grouped tile-order height of the GEMM kernels (tg_gemm_force_tiling); "
                          "0 = each kernel's default")
@@ -1104,7 +1105,7 @@ def main():
         time.sleep(0.3)
         configs = [measure_config(label, inputs.WORKLOADS[name], dev, args.config_launches,
                                   sampler, peaks, 0.0 if args.no_cpu_baseline else 2.0, num_sms)
-                   for label, name in JUDGED_CONFIGS]
+                   for label, name in SPEC_WORKLOADS]
         sampler.stop()
 
     if rank == 0:

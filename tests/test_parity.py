@@ -8,7 +8,7 @@ inputs are small integers every partial sum is exact in fp32, the result is
 unique, and the GPU must match the oracle's round-to-nearest-even result
 bit for bit.
 
-The workloads are the five judged configurations (fp32 128^3, the fp16 edge
+The workloads are the five specified ones (fp32 128^3, the fp16 edge
 set, the 1024x2048x512 tiling example, 8192^3, and the skinny/wide pair),
 followed by the verification flow of that article's §3.3: small cross-
 checks, unaligned sizes, seeded random stress with a 100% pass rate.

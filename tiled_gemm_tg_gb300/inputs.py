@@ -6,7 +6,7 @@ fp32 on the CPU from ``torch.Generator().manual_seed(seed)`` and then cast to
 the input dtype (fp32 -> fp16 rounds to nearest even).  The A seed of a
 workload is ``seed_base + 1`` and the B seed ``seed_base + 2``.
 
-The shapes and distributions are the five workloads the GEMM is judged on:
+The shapes and distributions are the five specified GEMM workloads:
 the fp32 128^3 triple-loop example, the fp16 edge set, the A[1024,512] x
 B[512,2048] tiling example, the 8192^3 compute-bound square and the two
 skinny/wide shapes; two strided batches (256 products of 256^3, 16 of
