@@ -421,7 +421,8 @@ tg_status tg_gemm_force_stages(int stages);
  * call whose 128 x BN output tiles (all products of a call together) leave
  * at least half of the SMs idle can share each tile over K among a cluster
  * of S CTAs: each CTA computes an fp32 partial over its range of k-blocks
- * (64 fp16 or 128 E4M3 elements each) and the cluster adds the S partials
+ * (128 fp16 or 256 E4M3 elements each for tiles 64 or 128 wide, 64 or 128
+ * for tiles 256 wide) and the cluster adds the S partials
  * in distributed shared memory, in rank order, before the epilogue.
  *   split  0: automatic (tg_gemm_main_plan's choice, with every cluster
  *          resident at once); 1: never; 2, 4 or 8: always that many CTAs
