@@ -23,7 +23,7 @@ import oracle
 import tiled_gemm_tg_gb300 as tg
 from tiled_gemm_tg_gb300 import inputs
 
-from gpu_util import check_full, compare, f16_bits_of, run
+from gpu_util import DevMatrix, check_full, compare, f16_bits_of, run
 
 pytestmark = pytest.mark.gpu
 
@@ -170,8 +170,9 @@ def test_skinny_integer_bitwise():
 @pytest.mark.parametrize("M", [16, 3])
 def test_skinny_splits_integer_bitwise(M, N):
     """M <= 16 on every split of the cluster (1, 2, 4 and 8 CTAs per 128
-    columns for 128, 64, 32 and 16 column tiles): the partials pushed to the
-    reducing CTA and added in rank order give the exact result."""
+    columns for 128, 64, 32 and 16 column tiles): the partials, read by each
+    reducing CTA through distributed shared memory and added in rank order,
+    give the exact result."""
     a = inputs.draw((M, 2048), "int2", 8311 + M, "f16")
     b = inputs.draw((2048, N), "int2", 8312 + N, "f16")
     got, intact, p = run(a, b, torch.float16, ldc=N + 8)
@@ -263,6 +264,60 @@ def test_chain_reads_the_previous_output(M, widths, path):
     assert tg.tg_gemm_check(s.cuda_stream) == tg.TG_OK
     check()
     for a in acts[1:]:
+        a.fill_(float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        chain(torch.cuda.current_stream().cuda_stream)
+    g.replay()
+    g.replay()
+    assert tg.tg_gemm_check(s.cuda_stream) == tg.TG_OK
+    check()
+
+
+def test_chain_across_kernels():
+    """A chain whose steps take different kernels, each step's A the previous
+    step's C, launched back to back (each prologue overlaps the previous
+    kernel through programmatic dependent launch) and again from a CUDA
+    graph: the CTA-pair kernel, the one-CTA kernel split over K by clusters,
+    the boundary kernel (B rows of 510 bytes) writing a 255-column C into
+    rows of 256, and the one-CTA kernel reading that C with K = 255.  Each
+    step against the oracle on the step's own input."""
+    dev = torch.device("cuda")
+    M = 512
+    # (N, K, ldb, ldc, path): A of step i is C of step i - 1 (lda = its ldc)
+    steps = [(18432, 1024, 18432, 18432, PAIR), (256, 18432, 256, 256, MAIN),
+             (255, 256, 255, 256, BOUNDARY), (768, 255, 768, 768, MAIN)]
+    ws = [inputs.draw((K, N), "normal_rsqrtk", 8470 + i, "f16", k=K)
+          for i, (N, K, _, _, _) in enumerate(steps)]
+    wd = [DevMatrix(w, ldb, 0, dev) for w, (_, _, ldb, _, _) in zip(ws, steps)]
+    x0 = inputs.draw((M, steps[0][1]), "normal", 8469, "f16")
+    acts = [(x0.to(dev), steps[0][1])]
+    for N, _, _, ldc, _ in steps:
+        acts.append((torch.empty((M, ldc), dtype=torch.float16, device=dev), ldc))
+    s = torch.cuda.current_stream()
+
+    def chain(h):
+        for i, (N, K, ldb, ldc, _) in enumerate(steps):
+            a, lda = acts[i]
+            st = tg.tg_gemm(M, N, K, a.data_ptr(), lda, wd[i].ptr, ldb, acts[i + 1][0].data_ptr(),
+                            ldc, tg.F16, tg.F16, h)
+            assert st == tg.TG_OK
+
+    def check():
+        for i, (N, K, _, _, _) in enumerate(steps):
+            x = acts[i][0][:, :K].contiguous().cpu()
+            C_ref, S = oracle.gemm(x.numpy(), ws[i].numpy(), nthreads=_oracle_threads())
+            got = acts[i + 1][0][:, :N].double().cpu().numpy()
+            compare(got, C_ref, S, True, f"chain step {i}")
+
+    for i, (N, K, ldb, ldc, path) in enumerate(steps):
+        a, lda = acts[i]
+        assert tg.tg_gemm_path(M, N, K, a.data_ptr(), lda, wd[i].ptr, ldb,
+                               acts[i + 1][0].data_ptr(), ldc, tg.F16, tg.F16) == path, i
+    chain(s.cuda_stream)
+    assert tg.tg_gemm_check(s.cuda_stream) == tg.TG_OK
+    check()
+    for a, _ in acts[1:]:
         a.fill_(float("nan"))
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
