@@ -406,9 +406,9 @@ tg_status tg_gemm_force_tiling(int bn, int group_m);
 /*
  * Pipeline-depth override, for configuration sweeps (the pages' num_stages,
  * tuned separately from the tile size): the number of shared-memory stages
- * in the TMA load ring of the one-CTA kernel (path 3; at most 4, 6 or 8 for
- * tiles 256, 128 or 64 wide, the default) and of the CTA-pair kernel (path
- * 6; at most 3, the default).
+ * in the TMA load ring of the one-CTA kernel (path 3; at most 4, 3 or 4 for
+ * tiles 256, 128 or 64 wide, the default: stages of 48, 64 or 48 KB) and of
+ * the CTA-pair kernel (path 6; at most 3, the default).
  *   stages  0: each kernel's default; 2..8: that many stages.
  * Process-wide; stays in force until changed.  Returns TG_ERR_INVALID_ARG
  * (and changes nothing) for other values.  A later call whose kernel holds
