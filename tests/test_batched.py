@@ -205,6 +205,49 @@ def test_batched_natural_paths(batch, M, N, K, want):
     _check(a_list, b_list, outs, torch.float16, exact=True)
 
 
+@pytest.mark.parametrize("M,N,K,dt,want", [
+    (4, 4, 4, "f32", SIMT),
+    (4, 4, 4, "f16", BOUNDARY),    # 8-byte rows: not TMA-addressable
+    (16, 128, 64, "f16", SKINNY),
+    (72, 64, 64, "f16", MAIN),
+])
+def test_batched_largest_batch(M, N, K, dt, want):
+    """The largest batch the ABI accepts, 65535 packed products, on every
+    kernel that indexes the batch (the grid's z extent, or the tile order and
+    the tensor maps' third dimension): integer inputs, so each product is
+    unique and compared bit for bit with the oracle's, on every product for
+    the tiny shapes and on 300 of them (the first, the last and random ones)
+    for the others; the guard bands around C keep their canary."""
+    batch = 65535
+    a_list = _mats(batch, (M, K), "int2", 11900, dt, K)
+    b_list = _mats(batch, (K, N), "int2", 11950, dt, K)
+    out_dtype = torch.float32 if dt == "f32" else torch.float16
+    A = torch.stack(a_list).cuda()
+    B = torch.stack(b_list).cuda()
+    Cbuf = torch.empty(GUARD + batch * M * N + GUARD, dtype=out_dtype, device="cuda")
+    bits(Cbuf).fill_(0x7E5A if out_dtype == torch.float16 else 0x7FC0A5A5)
+    canary = bits(Cbuf[:1].clone()).item()
+    C = Cbuf.data_ptr() + GUARD * esize(out_dtype)
+    s = torch.cuda.current_stream().cuda_stream
+    args = (batch, M, N, K, A.data_ptr(), K, M * K, B.data_ptr(), N, K * N, C, N, M * N,
+            code(A.dtype), code(out_dtype))
+    assert tg.tg_gemm_batched_path(*args) == want
+    st = tg.tg_gemm_batched(*args, s)
+    assert st == tg.TG_OK, tg.tg_status_string(st)
+    assert tg.tg_gemm_check(s) == tg.TG_OK
+    h = Cbuf.cpu()
+    hb = bits(h)
+    assert bool((hb[:GUARD] == canary).all()) and bool((hb[-GUARD:] == canary).all())
+    body = h[GUARD:GUARD + batch * M * N].view(batch, M, N)
+    if M * N * K <= 64:
+        pick = list(range(batch))
+    else:
+        rng = np.random.default_rng(11999)
+        pick = sorted({0, 1, batch - 2, batch - 1, *rng.integers(0, batch, 296).tolist()})
+    _check([a_list[i] for i in pick], [b_list[i] for i in pick],
+           [body[i].double().numpy() for i in pick], out_dtype, exact=True)
+
+
 @pytest.mark.parametrize("out", [torch.float16, torch.float32])
 def test_batched_k_zero(out):
     M, N, batch = 40, 70, 4
