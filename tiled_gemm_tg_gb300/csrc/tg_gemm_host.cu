@@ -395,7 +395,8 @@ int tmap_slot(const TmapKey& k)
     return static_cast<int>(h % kTmapCacheSize);
 }
 
-// Encodes (or finds in the cache) a 3-D map; kind 0: an operand load map
+// Encodes (or finds in the cache) a 3-D map, or with box_chunks > 0 the
+// 4-D view described below; kind 0: an operand load map
 // (fp16 or byte elements, 128-byte swizzle, 256-byte L2 promotion), kind 1:
 // an output store map (fp16 or fp32 elements, no swizzle).
 bool encode_map(CUtensorMap* map, int kind, const void* ptr, int es, uint64_t cols, uint64_t rows,
