@@ -525,6 +525,9 @@ def test_boundary_split_rule(tiles, kblocks, sms, want):
     ((2048, 1024, 512, 1, (128, 1))),
     ((8192, 8192, 8192, 1, (256, 1))),
     ((256, 256, 256, 256, (256, 1))),
+    # many tiles, but no wider than N needs
+    ((72, 64, 64, 65535, (64, 1))),
+    ((4096, 100, 1024, 8, (128, 1))),
 ])
 def test_main_plan(M, N, K, batch, want):
     """The one-CTA kernel's tile width and split over K, on the host."""
