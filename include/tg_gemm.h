@@ -439,16 +439,18 @@ tg_status tg_gemm_force_split_k(int split);
  * The one-CTA kernel's automatic choice, computed on the host alone for an
  * M x N x K call (batch products) of in_dtype (TG_F16 or TG_E4M3) on
  * num_sms SMs: returns the split S (1: none) and writes the tile width
- * (64, 128 or 256) to *bn.  The default width, unsplit, competes with every
+ * (64, 128 or 256) to *bn.  The default width (256 when 256-column tiles
+ * fill the SMs, else 128 when 128-column tiles fill half of them, else 64;
+ * never wider than N rounded up to 64 or 128), unsplit, competes with every
  * other width unsplit and with every width whose tiles fill at most half of
  * the SMs at its largest split (2, 4 or 8 with tiles * S <= num_sms and
  * S <= k-blocks), by a time estimate (waves of CTAs included; a challenger
- * must be 5 % faster) measured on GB300: A and B taken in at ~100 KB/us per
- * CTA unsplit and ~110 KB/us split for 64- and 128-column tiles (~86 and
- * ~95 for 256 columns), plus 1.5, 2.5 or 4.0 us for a split of 64-, 128- or
- * 256-column tiles.  On
- * a device the library also requires every cluster to be resident at once
- * (GB300 holds 15 clusters of 8 of these CTAs), which can change the choice.
+ * must be 5 % faster) measured on GB300: a CTA's A and B bytes (its k-range
+ * counted up to K) taken in at ~100 KB/us unsplit and ~110 KB/us split for
+ * 64- and 128-column tiles (~86 and ~95 for 256 columns), plus 1.5, 2.5 or
+ * 4.0 us for a split of 64-, 128- or 256-column tiles.  On a device the
+ * library also requires every cluster to be resident at once (GB300 holds
+ * 15 clusters of 8 of these CTAs), which can change the choice.
  * Returns 0 (and *bn = 0) for non-positive sizes or another dtype.
  */
 int tg_gemm_main_plan(int64_t M, int64_t N, int64_t K, int64_t batch, tg_dtype in_dtype,
