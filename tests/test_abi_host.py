@@ -554,6 +554,23 @@ def test_main_plan_rules():
     assert tg.tg_gemm_main_plan(8, 8, 8, 1, tg.F32, 152) == (0, 0)
 
 
+def test_main_plan_width_never_wider_than_n():
+    """Narrow products, alone or in batches up to 65535: the tile width is
+    at most N rounded up to 64 or 128 columns (128 at least for E4M3, whose
+    B copies are 128 elements wide), since wider tiles only multiply zeros."""
+    rng = np.random.default_rng(6)
+    for _ in range(300):
+        M = int(rng.integers(65, 5000))
+        N = int(rng.integers(1, 129))
+        K = int(rng.integers(1, 5000))
+        batch = int(rng.integers(1, 65536))
+        cap = 64 if N <= 64 else 128
+        bn, split = tg.tg_gemm_main_plan(M, N, K, batch, tg.F16, 152)
+        assert bn <= cap, (M, N, K, batch, bn)
+        bn8, _ = tg.tg_gemm_main_plan(M, N, K, batch, tg.E4M3, 152)
+        assert bn8 == 128, (M, N, K, batch, bn8)
+
+
 def test_force_split_k_arguments():
     for bad in (-1, 3, 5, 6, 16):
         assert tg.tg_gemm_force_split_k(bad) == tg.TG_ERR_INVALID_ARG
