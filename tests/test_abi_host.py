@@ -230,6 +230,31 @@ def test_force_tiling_validates():
         assert tg.tg_gemm_force_tiling(0, 0) == tg.TG_OK
 
 
+def test_missing_library_fails_loudly():
+    """Without the built library every entry point raises: there is no CPU
+    or library fallback to run instead (checked in a child process whose
+    binding points at a path that does not exist)."""
+    import subprocess
+    import sys
+    code = (
+        "import tiled_gemm_tg_gb300 as tg\n"
+        "tg._LIB_PATH = '/nonexistent/libtg_gemm.so'\n"
+        "tg._lib = None\n"
+        "for f in (tg.tg_gemm_version, lambda: tg.tg_gemm(8, 8, 8, 0, 8, 0, 8, 0, 8, tg.F16, tg.F16),\n"
+        "          lambda: tg.tg_gemm_path(8, 8, 8, 0, 8, 0, 8, 0, 8, tg.F16, tg.F16)):\n"
+        "    try:\n"
+        "        f()\n"
+        "    except RuntimeError as e:\n"
+        "        assert 'is missing' in str(e), e\n"
+        "    else:\n"
+        "        raise SystemExit('an entry point ran without the library')\n"
+        "print('ok')\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True,
+                       timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
+
+
 def test_product_path_never_imports_oracle():
     """The CUDA package must not import, load or call the CPU oracle."""
     pkg = os.path.dirname(tg.__file__)
