@@ -230,6 +230,50 @@ def test_force_tiling_validates():
         assert tg.tg_gemm_force_tiling(0, 0) == tg.TG_OK
 
 
+C_CLIENT = r"""
+#include <stdio.h>
+#include "tg_gemm.h"
+int main(void) {
+    int bn = 0;
+    int split = tg_gemm_main_plan(256, 256, 8192, 1, TG_F16, 152, &bn);
+    int path = tg_gemm_path(8192, 8192, 8192, (const void*)0x7F0000000000, 8192,
+                            (const void*)0x7F1000000000, 8192, (void*)0x7F2000000000, 8192,
+                            TG_F16, TG_F16);
+    tg_status bad = tg_gemm(-1, 8, 8, 0, 8, 0, 8, 0, 8, TG_F16, TG_F16, 0);
+    printf("%d %s %d %d %d %d\n", tg_gemm_version(), tg_status_string(bad), path, bn, split,
+           (int)bad);
+    return 0;
+}
+"""
+
+
+def test_plain_c_client(tmp_path):
+    """The header is plain C: a C99 program (-pedantic, warnings as errors)
+    includes it, links libtg_gemm.so and calls host-only entry points."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(tg.library_path())
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                        f"-I{os.path.dirname(HEADER)}", str(src), f"-L{libdir}", "-ltg_gemm",
+                        f"-Wl,-rpath,{libdir}", "-o", str(exe)],
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stderr
+    version, status, path, bn, split, code = r.stdout.split()
+    assert int(version) == tg.tg_gemm_version()
+    assert status == tg.tg_status_string(tg.TG_ERR_INVALID_ARG)
+    assert int(code) == tg.TG_ERR_INVALID_ARG
+    assert int(path) == 6  # the CTA-pair kernel for 8192^3
+    assert (int(bn), int(split)) == (64, 8)
+
+
 def test_missing_library_fails_loudly():
     """Without the built library every entry point raises: there is no CPU
     or library fallback to run instead (checked in a child process whose
